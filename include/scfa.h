@@ -1,0 +1,227 @@
+/*
+ * scfa.h — C ABI of libscfa.so: sparse causal flash attention (SCFA) on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation: exact causal softmax attention, forward and backward, over
+ * irregular dynamic-sparse layouts ("Faster Causal Attention Over Large
+ * Sequences Through Sparse Flash Attention", summary page on deep-paper.org
+ * of arXiv 2306.01160, section "SCFA 解决方案"):
+ *   - QK-sparse: queries and keys were dropped and the kept rows compacted;
+ *     q_idx / k_idx hold their original positions; a 128 x 128 tile is skipped
+ *     when max(q_idx) < min(k_idx), and inside live tiles an element is kept
+ *     iff q_idx >= k_idx  (part 1 "QK-Sparse").
+ *   - Hash-sparse: tokens are bucket-sorted by an LSH id (q_hash / k_hash);
+ *     tiles whose bucket ranges do not overlap, or that are wholly acausal,
+ *     are skipped, and inside live tiles an element is kept iff it is causal
+ *     in original positions AND in the same bucket (part 2 "Hash-Sparse").
+ *   - Dense causal (the comparator of section "FlashAttention 的兴起"): the
+ *     same kernels with q_idx = k_idx = position.
+ *
+ * Conventions for every entry point below:
+ *   - Tensor pointers are DEVICE pointers to contiguous row-major arrays.
+ *     bf16 tensors are passed as uint16_t (IEEE bfloat16 bit patterns).
+ *     Q/K/V/O/dO/dQ/dK/dV have layout [B][H][T][D]; LSE, idx and hash arrays
+ *     [B][H][T]. bf16 tensor pointers must be 16-byte aligned.
+ *   - D is the head dimension (64 or 128 where stated); scale multiplies QK^T
+ *     (normally 1/sqrt(D)). LSE is the natural-log softmax denominator, fp32.
+ *   - A query row with no admissible key gets O = 0, LSE = -inf and passes no
+ *     gradient; a key no query may see gets dK = dV = 0. Outputs are fully
+ *     overwritten. Inputs are read only. Inputs and outputs must not alias.
+ *   - The caller owns all memory. The library never allocates, frees or
+ *     synchronises, except scfa_get_device_status (which synchronises the
+ *     stream) and SCFA_FLAG_DEBUG_SYNC. Scratch space is the caller's
+ *     workspace `ws` of `ws_bytes` bytes (256-byte aligned), sized by the
+ *     *_workspace_size functions. One workspace must not be used by two calls
+ *     that may run at the same time.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     call is asynchronous on that stream.
+ *   - Errors: arguments are validated on the host before any launch and a bad
+ *     argument returns SCFA_ERR_INVALID / SCFA_ERR_UNSUPPORTED /
+ *     SCFA_ERR_WORKSPACE with nothing launched. A failed launch returns
+ *     SCFA_ERR_CUDA. Device-side failures (a pipeline wait that ran past its
+ *     time limit) are written to a status word in the workspace and read with
+ *     scfa_get_device_status; kernels never trap.
+ */
+#ifndef SCFA_H
+#define SCFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int scfa_status;
+enum {
+  SCFA_OK = 0,
+  SCFA_ERR_INVALID = 1,      /* null pointer, bad size, misaligned pointer */
+  SCFA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head dim) */
+  SCFA_ERR_WORKSPACE = 3,    /* workspace too small or misaligned */
+  SCFA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  SCFA_ERR_TIMEOUT = 5       /* device: a pipeline wait passed its limit */
+};
+
+/* attention modes */
+enum { SCFA_MODE_DENSE = 0, SCFA_MODE_QK = 1, SCFA_MODE_HASH = 2 };
+
+/* flags */
+enum {
+  SCFA_FLAG_NO_PRUNE = 1,   /* treat every tile as live (results unchanged) */
+  SCFA_FLAG_DEBUG_SYNC = 4  /* synchronise the stream after every launch */
+};
+
+/* Tiles are SCFA_TILE rows of queries by SCFA_TILE rows of keys. */
+#define SCFA_TILE 128
+
+/* Human-readable name of a status code (static string). */
+const char* scfa_status_string(scfa_status s);
+
+/* ----------------------------------------------------------------------------
+ * Workspace sizing.
+ * scfa_attn_workspace_size: bytes needed by scfa_{dense,qk,hash}_{fwd,bwd} and
+ * scfa_tiles for the given mode (SCFA_MODE_*), direction (backward = 0 / 1)
+ * and shape. Tq = Tk = T for dense and hash modes. Returns 0 on bad sizes.
+ * ------------------------------------------------------------------------- */
+size_t scfa_attn_workspace_size(int mode, int backward, int B, int H, int Tq, int Tk, int D);
+
+/* ----------------------------------------------------------------------------
+ * Dense causal attention (comparator; page section "FlashAttention 的兴起":
+ * a token sees only earlier tokens). q, k, v, o, do_, dq, dk, dv: [B,H,T,D]
+ * bf16; lse: [B,H,T] fp32. D = 64.
+ * ------------------------------------------------------------------------- */
+scfa_status scfa_dense_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           int B, int H, int T, int D, float scale,
+                           uint16_t* o, float* lse,
+                           void* ws, size_t ws_bytes, unsigned flags, void* stream);
+scfa_status scfa_dense_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const uint16_t* o, const float* lse, const uint16_t* do_,
+                           int B, int H, int T, int D, float scale,
+                           uint16_t* dq, uint16_t* dk, uint16_t* dv,
+                           void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * QK-sparse attention (page section "SCFA 解决方案", part 1 "QK-Sparse").
+ * q, o, do_, dq: [B,H,Tq,D]; k, v, dk, dv: [B,H,Tk,D]; q_idx [B,H,Tq] and
+ * k_idx [B,H,Tk] int32 original positions, ascending within each (b,h) over
+ * the kept rows. Heads keep different counts, so rows past a head's count are
+ * padding with sentinels: q_idx = -1 for padded queries, k_idx = INT32_MAX
+ * for padded keys (never admissible). Outputs are in compacted order. D = 64.
+ * ------------------------------------------------------------------------- */
+scfa_status scfa_qk_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const int32_t* q_idx, const int32_t* k_idx,
+                        int B, int H, int Tq, int Tk, int D, float scale,
+                        uint16_t* o, float* lse,
+                        void* ws, size_t ws_bytes, unsigned flags, void* stream);
+scfa_status scfa_qk_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const uint16_t* o, const float* lse, const uint16_t* do_,
+                        const int32_t* q_idx, const int32_t* k_idx,
+                        int B, int H, int Tq, int Tk, int D, float scale,
+                        uint16_t* dq, uint16_t* dk, uint16_t* dv,
+                        void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * Hash-sparse attention on bucket-sorted rows (page section "SCFA 解决方案",
+ * part 2 "Hash-Sparse"). All row tensors are in SORTED order, as produced by
+ * lsh_bucket_sort / lsh_gather: q_s, o_s, do_s, dq_s use the query order,
+ * k_s, v_s, dk_s, dv_s the key order. q_idx / k_idx [B,H,T] are the original
+ * positions of the sorted rows (the perm of lsh_bucket_sort) and q_hash /
+ * k_hash [B,H,T] their bucket ids, non-decreasing within each (b,h).
+ * Put results back in original order with lsh_unsort. D = 64.
+ * ------------------------------------------------------------------------- */
+scfa_status scfa_hash_fwd(const uint16_t* q_s, const uint16_t* k_s, const uint16_t* v_s,
+                          const int32_t* q_idx, const int32_t* k_idx,
+                          const int32_t* q_hash, const int32_t* k_hash,
+                          int B, int H, int T, int D, float scale,
+                          uint16_t* o_s, float* lse_s,
+                          void* ws, size_t ws_bytes, unsigned flags, void* stream);
+scfa_status scfa_hash_bwd(const uint16_t* q_s, const uint16_t* k_s, const uint16_t* v_s,
+                          const uint16_t* o_s, const float* lse_s, const uint16_t* do_s,
+                          const int32_t* q_idx, const int32_t* k_idx,
+                          const int32_t* q_hash, const int32_t* k_hash,
+                          int B, int H, int T, int D, float scale,
+                          uint16_t* dq_s, uint16_t* dk_s, uint16_t* dv_s,
+                          void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * LSH bucketing (page section "动态稀疏性为何会破坏它", item 2: similar tokens
+ * are grouped into buckets with LSH as in Reformer, and reordered by bucket).
+ * Construction: h(x) = argmax_j v_j with v = [x R, -x R], R a [D, m] bf16
+ * random rotation shared by queries and keys, n_buckets = 2 m. The argmax is
+ * of the EXACT real values (ties -> smallest j); L2 normalisation of x does
+ * not change it and is not applied. Inputs must be finite.
+ * x: [B,H,T,D] bf16, D a multiple of 8 and <= 256; 2 <= n_buckets <= 32768,
+ * even.
+ *
+ * lsh_hash: hash [B,H,T] int32 in original order.
+ * lsh_bucket_sort: per (b,h) stable sort by (bucket, position). perm [B,H,T]:
+ *   sorted slot -> original position; hash_sorted [B,H,T]; bucket_off
+ *   [B,H,n_buckets+1]: number of tokens with a smaller bucket id; x_sorted
+ *   (nullable) [B,H,T,D] = x gathered by perm. Workspace:
+ *   lsh_workspace_size.
+ * lsh_gather: x_sorted[b,h,s,:] = x[b,h,perm[b,h,s],:].
+ * lsh_unsort: y[b,h,perm[b,h,s],:] = y_sorted[b,h,s,:]. Rows whose perm entry
+ *   is out of [0, T) are skipped.
+ * ------------------------------------------------------------------------- */
+size_t lsh_workspace_size(int B, int H, int T, int n_buckets);
+scfa_status lsh_hash(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D,
+                     int n_buckets, int32_t* hash, void* stream);
+scfa_status lsh_bucket_sort(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D,
+                            int n_buckets, int32_t* hash_sorted, int32_t* perm,
+                            int32_t* bucket_off, uint16_t* x_sorted,
+                            void* ws, size_t ws_bytes, unsigned flags, void* stream);
+scfa_status lsh_gather(const uint16_t* x, const int32_t* perm, int B, int H, int T, int D,
+                       uint16_t* x_sorted, void* stream);
+scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int H, int T, int D,
+                       uint16_t* y, void* stream);
+
+/* ----------------------------------------------------------------------------
+ * Tile metadata and the live-tile work list (page section "SCFA 解决方案":
+ * tile pruning of part 1, bucket and causal pruning of part 2). Normally run
+ * inside the attention calls; exposed for inspection and tests. Writes into
+ * the workspace (sized for `mode`, backward = 1). Index arguments as for the
+ * attention call of that mode (NULL where the mode has none).
+ * Definitions, over the valid rows of each 128-row tile:
+ *   QK / dense: live(i,j) = max q_idx(i) >= min k_idx(j).
+ *   hash: live(i,j) = bucket ranges overlap AND max q_idx(i) >= min k_idx(j).
+ *   FULL(i,j) (no element mask needed): both tiles have 128 valid rows, min
+ *   q_idx(i) >= max k_idx(j) and, in hash mode, all four bucket bounds equal.
+ * scfa_tile_view_get fills device pointers into the workspace:
+ *   row_ptr [B*H*nQt+1], cols, fflags (CSR over q tiles, columns ascending);
+ *   csc_ptr [B*H*nKt+1], csc_rows, cflags (CSC over k tiles, rows ascending);
+ *   flag bit 0 = FULL; work_fwd [B*H*nQt] and work_bwd [B*H*nKt]: every tile
+ *   id sorted by live count descending, then id ascending.
+ * ------------------------------------------------------------------------- */
+scfa_status scfa_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
+                       const int32_t* q_hash, const int32_t* k_hash,
+                       int B, int H, int Tq, int Tk, int D,
+                       void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+typedef struct {
+  const int32_t* row_ptr;
+  const int32_t* cols;
+  const uint8_t* fflags;
+  const int32_t* csc_ptr;
+  const int32_t* csc_rows;
+  const uint8_t* cflags;
+  const int32_t* work_fwd;
+  const int32_t* work_bwd;
+  int n_q_tiles;   /* per head */
+  int n_k_tiles;   /* per head */
+} scfa_tile_view;
+
+scfa_status scfa_tile_view_get(const void* ws, int mode, int B, int H, int Tq, int Tk, int D,
+                               scfa_tile_view* out);
+
+/* ----------------------------------------------------------------------------
+ * Device status word of a workspace: SCFA_OK, or the first device-side error
+ * (SCFA_ERR_TIMEOUT) raised by the last attention call that used `ws`.
+ * Synchronises `stream`. Returns SCFA_ERR_CUDA if the copy fails.
+ * ------------------------------------------------------------------------- */
+scfa_status scfa_get_device_status(const void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SCFA_H */

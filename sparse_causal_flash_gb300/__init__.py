@@ -1,0 +1,196 @@
+"""Python binding of libscfa.so (sparse causal flash attention on GB300).
+
+Argument marshalling only: every function hands device pointers of torch
+tensors to the C ABI declared in include/scfa.h, which launches the CUDA
+kernels. Nothing here computes any part of the attention, hashing, sorting
+or tiling. PyTorch provides device memory and streams.
+
+If the shared library is missing, importing this package raises: there is
+no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libscfa.so")
+
+MODE_DENSE, MODE_QK, MODE_HASH = 0, 1, 2
+FLAG_NO_PRUNE, FLAG_DEBUG_SYNC = 1, 4
+TILE = 128
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "CUDA error", 5: "device timeout"}
+
+
+class ScfaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_causal_flash_gb300.build`")
+    return ctypes.CDLL(LIB_PATH)
+
+
+_lib = _load()
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_S = ctypes.c_size_t
+_U = ctypes.c_uint
+
+_SIGS = {
+    "scfa_status_string": ([_I], ctypes.c_char_p),
+    "scfa_attn_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _S),
+    "scfa_dense_fwd": ([_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _S, _U, _P], _I),
+    "scfa_dense_bwd": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _S, _U, _P], _I),
+    "scfa_qk_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _U, _P], _I),
+    "scfa_qk_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _S, _U, _P], _I),
+    "scfa_hash_fwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _S, _U, _P], _I),
+    "scfa_hash_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _S, _U, _P], _I),
+    "lsh_workspace_size": ([_I, _I, _I, _I], _S),
+    "lsh_hash": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "lsh_bucket_sort": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _U, _P], _I),
+    "lsh_gather": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "lsh_unsort": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "scfa_tiles": ([_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _U, _P], _I),
+    "scfa_tile_view_get": ([_P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "scfa_get_device_status": ([_P, _P], _I),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+EXPORTED = tuple(_SIGS)
+
+
+class TileView(ctypes.Structure):
+    _fields_ = [("row_ptr", _P), ("cols", _P), ("fflags", _P), ("csc_ptr", _P), ("csc_rows", _P),
+                ("cflags", _P), ("work_fwd", _P), ("work_bwd", _P), ("n_q_tiles", _I), ("n_k_tiles", _I)]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise ScfaError(fn, code)
+
+
+def _need(t, dtype, name):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA tensor of {dtype}, got {t.dtype} on {t.device}")
+
+
+def attn_workspace_size(mode, backward, B, H, Tq, Tk, D) -> int:
+    return int(_lib.scfa_attn_workspace_size(mode, int(backward), B, H, Tq, Tk, D))
+
+
+def lsh_workspace_size(B, H, T, n_buckets) -> int:
+    return int(_lib.lsh_workspace_size(B, H, T, n_buckets))
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Caller-owned workspace (torch allocations are 256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------- attention
+def scfa_dense_fwd(q, k, v, scale, o, lse, ws, flags=0, stream=None):
+    B, H, T, D = q.shape
+    _check("scfa_dense_fwd", _lib.scfa_dense_fwd(_ptr(q), _ptr(k), _ptr(v), B, H, T, D, scale, _ptr(o), _ptr(lse),
+                                                 _ptr(ws), ws.numel(), flags, _stream(stream)))
+
+
+def scfa_dense_bwd(q, k, v, o, lse, do, scale, dq, dk, dv, ws, flags=0, stream=None):
+    B, H, T, D = q.shape
+    _check("scfa_dense_bwd", _lib.scfa_dense_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), B, H, T, D,
+                                                 scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), flags,
+                                                 _stream(stream)))
+
+
+def scfa_qk_fwd(q, k, v, q_idx, k_idx, scale, o, lse, ws, flags=0, stream=None):
+    B, H, Tq, D = q.shape
+    Tk = k.shape[2]
+    _check("scfa_qk_fwd", _lib.scfa_qk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), B, H, Tq, Tk, D,
+                                           scale, _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), flags, _stream(stream)))
+
+
+def scfa_qk_bwd(q, k, v, o, lse, do, q_idx, k_idx, scale, dq, dk, dv, ws, flags=0, stream=None):
+    B, H, Tq, D = q.shape
+    Tk = k.shape[2]
+    _check("scfa_qk_bwd", _lib.scfa_qk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(q_idx),
+                                           _ptr(k_idx), B, H, Tq, Tk, D, scale, _ptr(dq), _ptr(dk), _ptr(dv),
+                                           _ptr(ws), ws.numel(), flags, _stream(stream)))
+
+
+def scfa_hash_fwd(q_s, k_s, v_s, q_idx, k_idx, q_hash, k_hash, scale, o_s, lse_s, ws, flags=0, stream=None):
+    B, H, T, D = q_s.shape
+    _check("scfa_hash_fwd", _lib.scfa_hash_fwd(_ptr(q_s), _ptr(k_s), _ptr(v_s), _ptr(q_idx), _ptr(k_idx),
+                                               _ptr(q_hash), _ptr(k_hash), B, H, T, D, scale, _ptr(o_s), _ptr(lse_s),
+                                               _ptr(ws), ws.numel(), flags, _stream(stream)))
+
+
+def scfa_hash_bwd(q_s, k_s, v_s, o_s, lse_s, do_s, q_idx, k_idx, q_hash, k_hash, scale, dq_s, dk_s, dv_s, ws,
+                  flags=0, stream=None):
+    B, H, T, D = q_s.shape
+    _check("scfa_hash_bwd", _lib.scfa_hash_bwd(_ptr(q_s), _ptr(k_s), _ptr(v_s), _ptr(o_s), _ptr(lse_s), _ptr(do_s),
+                                               _ptr(q_idx), _ptr(k_idx), _ptr(q_hash), _ptr(k_hash), B, H, T, D,
+                                               scale, _ptr(dq_s), _ptr(dk_s), _ptr(dv_s), _ptr(ws), ws.numel(),
+                                               flags, _stream(stream)))
+
+
+# ---------------------------------------------------------------- LSH / sort / gather
+def lsh_hash(x, R, n_buckets, hash_out, stream=None):
+    B, H, T, D = x.shape
+    _check("lsh_hash", _lib.lsh_hash(_ptr(x), _ptr(R), B, H, T, D, n_buckets, _ptr(hash_out), _stream(stream)))
+
+
+def lsh_bucket_sort(x, R, n_buckets, hash_sorted, perm, bucket_off, x_sorted, ws, flags=0, stream=None):
+    B, H, T, D = x.shape
+    _check("lsh_bucket_sort", _lib.lsh_bucket_sort(_ptr(x), _ptr(R), B, H, T, D, n_buckets, _ptr(hash_sorted),
+                                                   _ptr(perm), _ptr(bucket_off), _ptr(x_sorted), _ptr(ws),
+                                                   ws.numel(), flags, _stream(stream)))
+
+
+def lsh_gather(x, perm, x_sorted, stream=None):
+    B, H, T, D = x.shape
+    _check("lsh_gather", _lib.lsh_gather(_ptr(x), _ptr(perm), B, H, T, D, _ptr(x_sorted), _stream(stream)))
+
+
+def lsh_unsort(y_sorted, perm, y, stream=None):
+    B, H, T, D = y_sorted.shape
+    _check("lsh_unsort", _lib.lsh_unsort(_ptr(y_sorted), _ptr(perm), B, H, T, D, _ptr(y), _stream(stream)))
+
+
+# ---------------------------------------------------------------- tiles
+def scfa_tiles(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, D, ws, flags=0, stream=None):
+    _check("scfa_tiles", _lib.scfa_tiles(mode, _ptr(q_idx), _ptr(k_idx), _ptr(q_hash), _ptr(k_hash), B, H, Tq, Tk,
+                                         D, _ptr(ws), ws.numel(), flags, _stream(stream)))
+
+
+def scfa_tile_view_get(ws, mode, B, H, Tq, Tk, D) -> TileView:
+    tv = TileView()
+    _check("scfa_tile_view_get", _lib.scfa_tile_view_get(_ptr(ws), mode, B, H, Tq, Tk, D, ctypes.byref(tv)))
+    return tv
+
+
+def scfa_get_device_status(ws, stream=None) -> int:
+    return int(_lib.scfa_get_device_status(_ptr(ws), _stream(stream)))
+
+
+def status_string(code: int) -> str:
+    return _lib.scfa_status_string(code).decode()

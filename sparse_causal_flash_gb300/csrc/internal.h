@@ -1,0 +1,77 @@
+// Host-side internals shared by the translation units of libscfa.so:
+// workspace layouts and the launchers of each kernel family.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/scfa.h"
+
+namespace scfa {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Byte offsets of the arrays an attention call keeps in its workspace.
+struct AttnWs {
+  int nQt = 0, nKt = 0;
+  long long n_qtiles = 0, n_ktiles = 0;  // over all heads
+  long long max_live = 0;                // capacity of the live lists
+  size_t header = 0;
+  size_t qstat = 0, kstat = 0;           // int4 per tile: min idx, max idx, min hash, max hash
+  size_t qcount = 0, kcount = 0;         // live count per q tile / k tile
+  size_t row_ptr = 0, csc_ptr = 0;
+  size_t cols = 0, csc_rows = 0;
+  size_t fflags = 0, cflags = 0;
+  size_t work_fwd = 0, work_bwd = 0;
+  size_t cursor = 0;                     // scratch of the work-order sort
+  size_t dq_acc = 0;                     // backward: fp32 dQ accumulator [B,H,Tq,D]
+  size_t drow = 0;                       // backward: fp32 rowsum(dO * O) [B,H,Tq]
+  size_t total = 0;
+};
+
+// Returns false if the sizes are out of range.
+bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D, AttnWs* L);
+
+struct LshWs {
+  size_t header = 0;
+  size_t hash = 0;    // int32 [B,H,T], original order
+  size_t total = 0;
+};
+bool lsh_ws_layout(int B, int H, int T, int n_buckets, LshWs* L);
+
+int num_sms();
+
+// tiles.cu
+cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
+                         const int32_t* q_hash, const int32_t* k_hash,
+                         int B, int H, int Tq, int Tk, unsigned flags,
+                         char* ws, const AttnWs& L, cudaStream_t st);
+
+// lsh.cu
+cudaError_t launch_lsh_hash(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
+                            int32_t* hash, cudaStream_t st);
+cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int n_buckets,
+                               int32_t* perm, int32_t* hash_sorted, int32_t* bucket_off,
+                               cudaStream_t st);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int BH, int T, int D,
+                          uint16_t* out, bool unsort, cudaStream_t st);
+
+// attn_fwd.cu / attn_bwd.cu
+struct AttnArgs {
+  int mode;
+  int B, H, Tq, Tk, D;
+  float scale;
+  const uint16_t *q, *k, *v, *o, *do_;
+  const float* lse_in;
+  const int32_t *q_idx, *k_idx, *q_hash, *k_hash;
+  uint16_t* o_out;
+  float* lse_out;
+  uint16_t *dq, *dk, *dv;
+  char* ws;
+  const AttnWs* L;
+};
+cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st);
+
+}  // namespace scfa

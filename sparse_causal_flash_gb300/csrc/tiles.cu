@@ -1,0 +1,308 @@
+// Tile metadata and the live-tile work list.
+//
+// Page: "Faster Causal Attention Over Large Sequences Through Sparse Flash
+// Attention" (deep-paper.org), section "SCFA 解决方案": tile pruning by
+// max(q_idx_i) < min(k_idx_j) (part 1), bucket and causal pruning (part 2).
+// Tiles are 128 x 128. Per tile the pass records min / max of the original
+// positions and of the bucket ids over its valid rows, tests every candidate
+// (query tile, key tile) pair, and emits CSR (by query tile), CSC (by key
+// tile), a FULL flag per entry (all 128 x 128 pairs admissible: no element
+// mask needed), and the work order (tile ids by live count descending, then
+// id ascending) that the persistent attention kernels walk.
+//
+// All passes are integer and tiny next to the attention itself. In hash mode
+// the bucket ids are non-decreasing along the sorted rows, so the key tiles
+// whose bucket range can overlap a query tile's form one contiguous run found
+// by binary search; QK and dense modes test every pair of tiles of a head.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace scfa {
+namespace {
+
+__device__ __forceinline__ int warp_min(int v) {
+  for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ int warp_max(int v) {
+  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// One warp per tile: {min idx, max idx, min hash, max hash} over valid rows.
+__global__ void tile_stats_kernel(int mode, const int32_t* __restrict__ idx,
+                                  const int32_t* __restrict__ hash,
+                                  long long n_tiles, int T, int nT, int4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < n_tiles; t += warps) {
+    const long long bh = t / nT;
+    const int r0 = static_cast<int>(t % nT) * kTile;
+    const int rows = min(kTile, T - r0);
+    int mn = INT_MAX, mx = INT_MIN, hmn = INT_MAX, hmx = INT_MIN;
+    for (int r = lane; r < rows; r += 32) {
+      const long long g = bh * T + r0 + r;
+      const int id = (mode == SCFA_MODE_DENSE) ? (r0 + r) : idx[g];
+      mn = min(mn, id);
+      mx = max(mx, id);
+      if (mode == SCFA_MODE_HASH) {
+        const int h = hash[g];
+        hmn = min(hmn, h);
+        hmx = max(hmx, h);
+      }
+    }
+    mn = warp_min(mn);
+    mx = warp_max(mx);
+    hmn = warp_min(hmn);
+    hmx = warp_max(hmx);
+    if (lane == 0) out[t] = make_int4(mn, mx, hmn, hmx);
+  }
+}
+
+struct TileCtx {
+  int mode;
+  unsigned flags;
+  int Tq, Tk, nQt, nKt;
+  const int4* qstat;
+  const int4* kstat;
+};
+
+__device__ __forceinline__ bool tile_live(const TileCtx& c, const int4& qs, const int4& ks) {
+  if (c.flags & SCFA_FLAG_NO_PRUNE) return true;
+  bool live = qs.y >= ks.x;
+  if (c.mode == SCFA_MODE_HASH) live = live && (qs.z <= ks.w) && (ks.z <= qs.w);
+  return live;
+}
+__device__ __forceinline__ bool tile_full(const TileCtx& c, int i, int j, const int4& qs, const int4& ks) {
+  const bool complete = (min(kTile, c.Tq - i * kTile) == kTile) && (min(kTile, c.Tk - j * kTile) == kTile);
+  bool full = complete && (qs.x >= ks.y);
+  if (c.mode == SCFA_MODE_HASH) full = full && (qs.z == qs.w) && (ks.z == ks.w) && (qs.z == ks.z);
+  return full;
+}
+
+// first index in [0, n) with key(i) >= v, for a non-decreasing key
+template <typename F>
+__device__ __forceinline__ int lower_bound_by(int n, int v, F key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (key(mid) < v) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// Candidate range [lo, hi) of partner tiles of one tile.
+__device__ __forceinline__ void partner_range(const TileCtx& c, bool by_q, const int4& self, long long bh,
+                                              int* lo, int* hi) {
+  const int n = by_q ? c.nKt : c.nQt;
+  if (c.mode != SCFA_MODE_HASH || (c.flags & SCFA_FLAG_NO_PRUNE)) {
+    *lo = 0;
+    *hi = n;
+    return;
+  }
+  const int4* other = (by_q ? c.kstat : c.qstat) + bh * n;
+  // partners with max hash >= my min hash, and min hash <= my max hash
+  *lo = lower_bound_by(n, self.z, [&](int t) { return other[t].w; });
+  *hi = lower_bound_by(n, self.w + 1, [&](int t) { return other[t].z; });
+  if (self.w == INT_MAX) *hi = n;
+}
+
+// One thread per query tile (first B*H*nQt ids) or key tile (next B*H*nKt).
+__global__ void tile_count_kernel(TileCtx c, long long n_q, long long n_k,
+                                  int32_t* __restrict__ qcount, int32_t* __restrict__ kcount) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n_q + n_k; t += stride) {
+    const bool by_q = t < n_q;
+    const long long id = by_q ? t : t - n_q;
+    const int nself = by_q ? c.nQt : c.nKt;
+    const long long bh = id / nself;
+    const int4 self = (by_q ? c.qstat : c.kstat)[id];
+    int lo, hi;
+    partner_range(c, by_q, self, bh, &lo, &hi);
+    int cnt = 0;
+    for (int p = lo; p < hi; ++p) {
+      const int4 other = (by_q ? c.kstat : c.qstat)[bh * (by_q ? c.nKt : c.nQt) + p];
+      cnt += by_q ? tile_live(c, self, other) : tile_live(c, other, self);
+    }
+    (by_q ? qcount : kcount)[id] = cnt;
+  }
+}
+
+// Exclusive scans: block 0 -> row_ptr from qcount, block 1 -> csc_ptr from kcount.
+__global__ void tile_scan_kernel(const int32_t* __restrict__ qcount, long long n_q, int32_t* __restrict__ row_ptr,
+                                 const int32_t* __restrict__ kcount, long long n_k, int32_t* __restrict__ csc_ptr,
+                                 WsHeader* hdr) {
+  const int32_t* in = blockIdx.x == 0 ? qcount : kcount;
+  int32_t* out = blockIdx.x == 0 ? row_ptr : csc_ptr;
+  const long long n = blockIdx.x == 0 ? n_q : n_k;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const long long per = (n + nt - 1) / nt;
+  const long long b = min(n, per * tid), e = min(n, b + per);
+  long long sum = 0;
+  for (long long i = b; i < e; ++i) sum += in[i];
+  __shared__ long long wsum[32];
+  // block exclusive scan of the per-thread sums
+  long long x = sum;
+  const int lane = tid & 31, w = tid >> 5;
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    long long s = (lane < (nt >> 5)) ? wsum[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    wsum[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  long long run = x - sum + (w > 0 ? wsum[w - 1] : 0);
+  for (long long i = b; i < e; ++i) {
+    out[i] = static_cast<int32_t>(run);
+    run += in[i];
+  }
+  if (tid == nt - 1) {
+    out[n] = static_cast<int32_t>(run);
+    if (blockIdx.x == 0) hdr->n_live = static_cast<int>(run);
+  }
+}
+
+__global__ void tile_fill_kernel(TileCtx c, long long n_q, long long n_k,
+                                 const int32_t* __restrict__ row_ptr, int32_t* __restrict__ cols,
+                                 uint8_t* __restrict__ fflags,
+                                 const int32_t* __restrict__ csc_ptr, int32_t* __restrict__ csc_rows,
+                                 uint8_t* __restrict__ cflags) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n_q + n_k; t += stride) {
+    const bool by_q = t < n_q;
+    const long long id = by_q ? t : t - n_q;
+    const int nself = by_q ? c.nQt : c.nKt;
+    const long long bh = id / nself;
+    const int me = static_cast<int>(id % nself);
+    const int4 self = (by_q ? c.qstat : c.kstat)[id];
+    int lo, hi;
+    partner_range(c, by_q, self, bh, &lo, &hi);
+    long long pos = by_q ? row_ptr[id] : csc_ptr[id];
+    for (int p = lo; p < hi; ++p) {
+      const int4 other = (by_q ? c.kstat : c.qstat)[bh * (by_q ? c.nKt : c.nQt) + p];
+      const int4 qs = by_q ? self : other;
+      const int4 ks = by_q ? other : self;
+      if (!tile_live(c, qs, ks)) continue;
+      const uint8_t f = tile_full(c, by_q ? me : p, by_q ? p : me, qs, ks) ? kFlagFull : 0;
+      if (by_q) {
+        cols[pos] = p;
+        fflags[pos] = f;
+      } else {
+        csc_rows[pos] = p;
+        cflags[pos] = f;
+      }
+      ++pos;
+    }
+  }
+}
+
+// Stable counting sort of tile ids by live count, descending. Block 0 builds
+// the forward order, block 1 the backward order. The whole block histograms;
+// warp 0 scans and scatters in id order (stable by construction).
+__global__ void work_order_kernel(const int32_t* __restrict__ qcount, long long n_q, int max_q,
+                                  int32_t* __restrict__ work_fwd,
+                                  const int32_t* __restrict__ kcount, long long n_k, int max_k,
+                                  int32_t* __restrict__ work_bwd,
+                                  int32_t* __restrict__ gcursor, int smem_bins) {
+  extern __shared__ int32_t scur[];
+  const bool fwd = blockIdx.x == 0;
+  const int32_t* cnt = fwd ? qcount : kcount;
+  const long long n = fwd ? n_q : n_k;
+  const int maxc = fwd ? max_q : max_k;
+  int32_t* out = fwd ? work_fwd : work_bwd;
+  int32_t* cur = (maxc + 1 <= smem_bins) ? scur : gcursor + (fwd ? 0 : (max_q + 1));
+  for (int cc = threadIdx.x; cc <= maxc; cc += blockDim.x) cur[cc] = 0;
+  __syncthreads();
+  for (long long i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&cur[min(max(cnt[i], 0), maxc)], 1);
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  // start[c] = number of ids with a larger count
+  int running = 0;
+  for (int base = maxc; base >= 0; base -= 32) {
+    const int cc = base - lane;
+    const int v = cc >= 0 ? cur[cc] : 0;
+    int x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (cc >= 0) cur[cc] = running + x - v;
+    running += __shfl_sync(0xffffffffu, x, 31);
+  }
+  __syncwarp();
+  for (long long base = 0; base < n; base += 32) {
+    const long long i = base + lane;
+    const bool active = i < n;
+    const int cc = active ? min(max(cnt[i], 0), maxc) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, cc);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int start = active ? cur[cc] : 0;
+    __syncwarp();
+    if (active) {
+      out[start + rank] = static_cast<int32_t>(i);
+      if (rank == 0) cur[cc] = start + __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+inline int grid_for(long long work, int block, int max_blocks) {
+  long long g = (work + block - 1) / block;
+  if (g < 1) g = 1;
+  if (g > max_blocks) g = max_blocks;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
+                         const int32_t* q_hash, const int32_t* k_hash,
+                         int B, int H, int Tq, int Tk, unsigned flags,
+                         char* ws, const AttnWs& L, cudaStream_t st) {
+  const int sms = num_sms();
+  const long long BH = static_cast<long long>(B) * H;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
+  int4* qstat = reinterpret_cast<int4*>(ws + L.qstat);
+  int4* kstat = reinterpret_cast<int4*>(ws + L.kstat);
+  int32_t* qcount = reinterpret_cast<int32_t*>(ws + L.qcount);
+  int32_t* kcount = reinterpret_cast<int32_t*>(ws + L.kcount);
+  int32_t* row_ptr = reinterpret_cast<int32_t*>(ws + L.row_ptr);
+  int32_t* csc_ptr = reinterpret_cast<int32_t*>(ws + L.csc_ptr);
+
+  cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st);
+  if (e != cudaSuccess) return e;
+  tile_stats_kernel<<<grid_for(L.n_qtiles * 32, 256, sms * 8), 256, 0, st>>>(
+      mode, q_idx, q_hash, L.n_qtiles, Tq, L.nQt, qstat);
+  tile_stats_kernel<<<grid_for(L.n_ktiles * 32, 256, sms * 8), 256, 0, st>>>(
+      mode, k_idx, k_hash, L.n_ktiles, Tk, L.nKt, kstat);
+  TileCtx c{mode, flags, Tq, Tk, L.nQt, L.nKt, qstat, kstat};
+  const long long nt = L.n_qtiles + L.n_ktiles;
+  tile_count_kernel<<<grid_for(nt, 128, sms * 16), 128, 0, st>>>(c, L.n_qtiles, L.n_ktiles, qcount, kcount);
+  tile_scan_kernel<<<2, 1024, 0, st>>>(qcount, L.n_qtiles, row_ptr, kcount, L.n_ktiles, csc_ptr, hdr);
+  tile_fill_kernel<<<grid_for(nt, 128, sms * 16), 128, 0, st>>>(
+      c, L.n_qtiles, L.n_ktiles, row_ptr, reinterpret_cast<int32_t*>(ws + L.cols),
+      reinterpret_cast<uint8_t*>(ws + L.fflags), csc_ptr, reinterpret_cast<int32_t*>(ws + L.csc_rows),
+      reinterpret_cast<uint8_t*>(ws + L.cflags));
+  const int smem_bins = 12 * 1024;  // 48 KB of shared memory; larger histograms use the workspace
+  const int maxc = (L.nKt > L.nQt ? L.nKt : L.nQt) + 1;
+  const size_t smem = static_cast<size_t>(maxc <= smem_bins ? maxc : 0) * sizeof(int32_t);
+  work_order_kernel<<<2, 1024, smem, st>>>(qcount, L.n_qtiles, L.nKt,
+                                           reinterpret_cast<int32_t*>(ws + L.work_fwd),
+                                           kcount, L.n_ktiles, L.nQt,
+                                           reinterpret_cast<int32_t*>(ws + L.work_bwd),
+                                           reinterpret_cast<int32_t*>(ws + L.cursor), smem_bins);
+  return cudaGetLastError();
+}
+
+}  // namespace scfa

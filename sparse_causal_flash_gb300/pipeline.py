@@ -1,0 +1,80 @@
+"""One fwd+bwd step of each SCFA mode, composed from C-ABI calls.
+
+Call order only (no arithmetic): the hash-sparse step hashes and
+bucket-sorts queries and keys, gathers V and dO into sorted order, runs the
+sparse attention forward and backward on the sorted rows, and puts O, dQ, dK
+and dV back in original order ("Faster Causal Attention Over Large Sequences
+Through Sparse Flash Attention", deep-paper.org, sections "动态稀疏性为何会破坏它"
+and "SCFA 解决方案" part 2). LSE stays in sorted query order (the backward
+consumes it there). Buffers are allocated once per shape and reused.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size, lsh_bucket_sort, lsh_gather,
+               lsh_unsort, lsh_workspace_size, scfa_dense_bwd, scfa_dense_fwd, scfa_hash_bwd, scfa_hash_fwd,
+               scfa_qk_bwd, scfa_qk_fwd, workspace)
+
+
+class Step:
+    """Buffers and the launch sequence of one fwd+bwd step for a fixed shape."""
+
+    def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
+                 device="cuda", flags: int = 0):
+        self.mode, self.B, self.H, self.Tq, self.Tk, self.D = mode, B, H, Tq, Tk, D
+        self.nb = n_buckets
+        self.flags = flags
+        dev = torch.device(device)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.o = torch.empty((B, H, Tq, D), **bf)
+        self.lse = torch.empty((B, H, Tq), dtype=torch.float32, device=dev)
+        self.dq = torch.empty((B, H, Tq, D), **bf)
+        self.dk = torch.empty((B, H, Tk, D), **bf)
+        self.dv = torch.empty((B, H, Tk, D), **bf)
+        self.ws_f = workspace(attn_workspace_size(mode, 0, B, H, Tq, Tk, D), dev)
+        self.ws_b = workspace(attn_workspace_size(mode, 1, B, H, Tq, Tk, D), dev)
+        if mode == MODE_HASH:
+            T = Tq
+            self.ws_l = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
+            self.qh = torch.empty((B, H, T), **i32)
+            self.kh = torch.empty((B, H, T), **i32)
+            self.pq = torch.empty((B, H, T), **i32)
+            self.pk = torch.empty((B, H, T), **i32)
+            self.offq = torch.empty((B, H, n_buckets + 1), **i32)
+            self.offk = torch.empty((B, H, n_buckets + 1), **i32)
+            self.q_s = torch.empty((B, H, T, D), **bf)
+            self.k_s = torch.empty((B, H, T, D), **bf)
+            self.v_s = torch.empty((B, H, T, D), **bf)
+            self.do_s = torch.empty((B, H, T, D), **bf)
+            self.o_s = torch.empty((B, H, T, D), **bf)
+            self.dq_s = torch.empty((B, H, T, D), **bf)
+            self.dk_s = torch.empty((B, H, T, D), **bf)
+            self.dv_s = torch.empty((B, H, T, D), **bf)
+
+    def run(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None, stream=None):
+        """Forward + backward. Results land in self.o/lse/dq/dk/dv."""
+        f = self.flags
+        if self.mode == MODE_DENSE:
+            scfa_dense_fwd(q, k, v, scale, self.o, self.lse, self.ws_f, f, stream)
+            scfa_dense_bwd(q, k, v, self.o, self.lse, do, scale, self.dq, self.dk, self.dv, self.ws_b, f, stream)
+        elif self.mode == MODE_QK:
+            scfa_qk_fwd(q, k, v, q_idx, k_idx, scale, self.o, self.lse, self.ws_f, f, stream)
+            scfa_qk_bwd(q, k, v, self.o, self.lse, do, q_idx, k_idx, scale, self.dq, self.dk, self.dv, self.ws_b,
+                        f, stream)
+        else:
+            nb = self.nb
+            lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, stream)
+            lsh_bucket_sort(k, R, nb, self.kh, self.pk, self.offk, self.k_s, self.ws_l, 0, stream)
+            lsh_gather(v, self.pk, self.v_s, stream)
+            scfa_hash_fwd(self.q_s, self.k_s, self.v_s, self.pq, self.pk, self.qh, self.kh, scale, self.o_s,
+                          self.lse, self.ws_f, f, stream)
+            lsh_gather(do, self.pq, self.do_s, stream)
+            scfa_hash_bwd(self.q_s, self.k_s, self.v_s, self.o_s, self.lse, self.do_s, self.pq, self.pk, self.qh,
+                          self.kh, scale, self.dq_s, self.dk_s, self.dv_s, self.ws_b, f, stream)
+            lsh_unsort(self.o_s, self.pq, self.o, stream)
+            lsh_unsort(self.dq_s, self.pq, self.dq, stream)
+            lsh_unsort(self.dk_s, self.pk, self.dk, stream)
+            lsh_unsort(self.dv_s, self.pk, self.dv, stream)
+        return self

@@ -1,0 +1,273 @@
+"""GPU parity of every step of the hot path against the float64 oracle.
+
+Index work (LSH bucket ids, sort permutation, sorted ids, bucket offsets,
+gathered / unsorted rows, live-tile lists) must be bit-exact; O, dQ, dK, dV
+within max abs 2e-2 and relative L2 5e-3; LSE within 2e-3 (and -inf exactly).
+Sizes span several 128-row tiles with ragged tails; the full-size workloads
+are checked on sampled heads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from harness import check_close, check_lse, to_np
+from oracle import attention, lsh, pipelines, tiles
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def scfa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_causal_flash_gb300 import build
+    build.build()
+    import sparse_causal_flash_gb300 as s
+    return s
+
+
+def cuda(t):
+    return t.contiguous().cuda()
+
+
+# ------------------------------------------------------------------ LSH + sort
+@pytest.mark.parametrize("B,H,T,D,nb", [(1, 2, 512, 64, 4), (2, 3, 1000, 64, 16), (1, 2, 700, 128, 64)])
+def test_lsh_hash_bitexact(scfa, B, H, T, D, nb):
+    x = synth.normal_bf16(77, 1, (B, H, T, D))
+    R = synth.rotation_bf16(77, D, nb // 2)
+    h = torch.empty((B, H, T), dtype=torch.int32, device="cuda")
+    scfa.lsh_hash(cuda(x), cuda(R), nb, h)
+    ref = lsh.lsh_hash(x.double().numpy(), R.double().numpy())
+    np.testing.assert_array_equal(h.cpu().numpy(), ref)
+
+
+def test_lsh_hash_exact_ties_and_cancellation(scfa):
+    D, m = 64, 4
+    rng = np.random.default_rng(5)
+    c0 = torch.from_numpy(rng.standard_normal(D)).to(torch.bfloat16)
+    R = torch.stack([c0, c0, -c0, torch.zeros(D, dtype=torch.bfloat16)], dim=1)  # ties between columns
+    rows = [torch.zeros(D, dtype=torch.bfloat16)]                                   # all candidates 0
+    rows += [synth.normal_bf16(9, 1, (D,)) for _ in range(60)]
+    big = torch.zeros(D, dtype=torch.bfloat16)                                      # 2^60 + 1 - 2^60
+    big[0], big[1], big[2] = 2.0**60, 1.0, -(2.0**60)
+    rows.append(big)
+    x = torch.stack(rows)[None, None]
+    R2 = R.clone()
+    R2[:, 3] = torch.ones(D, dtype=torch.bfloat16)
+    for RR in (R, R2):
+        h = torch.empty((1, 1, x.shape[2]), dtype=torch.int32, device="cuda")
+        scfa.lsh_hash(cuda(x), cuda(RR), 2 * m, h)
+        ref = lsh.lsh_hash(x.double().numpy(), RR.double().numpy())
+        np.testing.assert_array_equal(h.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("B,H,T,D,nb", [(1, 2, 512, 64, 4), (2, 3, 1000, 64, 16), (1, 1, 5000, 64, 512)])
+def test_bucket_sort_and_gather_bitexact(scfa, B, H, T, D, nb):
+    x = synth.normal_bf16(78, 2, (B, H, T, D))
+    R = synth.rotation_bf16(78, D, nb // 2)
+    dev = dict(dtype=torch.int32, device="cuda")
+    hs = torch.empty((B, H, T), **dev)
+    perm = torch.empty((B, H, T), **dev)
+    off = torch.empty((B, H, nb + 1), **dev)
+    xs = torch.empty((B, H, T, D), dtype=torch.bfloat16, device="cuda")
+    ws = scfa.workspace(scfa.lsh_workspace_size(B, H, T, nb))
+    scfa.lsh_bucket_sort(cuda(x), cuda(R), nb, hs, perm, off, xs, ws)
+    href = lsh.lsh_hash(x.double().numpy(), R.double().numpy())
+    pr, hr, orf = pipelines.hash_sort_view(href, nb)
+    np.testing.assert_array_equal(perm.cpu().numpy(), pr)
+    np.testing.assert_array_equal(hs.cpu().numpy(), hr)
+    np.testing.assert_array_equal(off.cpu().numpy(), orf)
+    xs_ref = torch.stack([torch.stack([x[b, h][torch.from_numpy(pr[b, h]).long()] for h in range(H)]) for b in range(B)])
+    assert torch.equal(xs.cpu().view(torch.int16), xs_ref.view(torch.int16))
+    # unsort puts every row back, bit for bit
+    back = torch.empty_like(xs)
+    scfa.lsh_unsort(xs, perm, back)
+    assert torch.equal(back.cpu().view(torch.int16), x.view(torch.int16))
+    g = torch.empty_like(xs)
+    scfa.lsh_gather(cuda(x), perm, g)
+    assert torch.equal(g.cpu().view(torch.int16), xs_ref.view(torch.int16))
+
+
+# ------------------------------------------------------------------ tiles
+def read_tiles(scfa, ws, mode, B, H, Tq, Tk, D):
+    tv = scfa.scfa_tile_view_get(ws, mode, B, H, Tq, Tk, D)
+    base = ws.data_ptr()
+    nq, nk = B * H * tv.n_q_tiles, B * H * tv.n_k_tiles
+
+    def arr(ptr, n, dt):
+        off = ptr - base
+        size = np.dtype(dt).itemsize
+        return ws[off:off + n * size].cpu().numpy().view(dt).copy()
+
+    torch.cuda.synchronize()
+    row_ptr = arr(tv.row_ptr, nq + 1, np.int32)
+    csc_ptr = arr(tv.csc_ptr, nk + 1, np.int32)
+    nl = int(row_ptr[-1])
+    return {
+        "row_ptr": row_ptr, "cols": arr(tv.cols, nl, np.int32), "fflags": arr(tv.fflags, nl, np.uint8),
+        "csc_ptr": csc_ptr, "csc_rows": arr(tv.csc_rows, int(csc_ptr[-1]), np.int32),
+        "cflags": arr(tv.cflags, int(csc_ptr[-1]), np.uint8),
+        "work_fwd": arr(tv.work_fwd, nq, np.int32), "work_bwd": arr(tv.work_bwd, nk, np.int32),
+    }
+
+
+def compare_tiles(got, ref):
+    for key in ("row_ptr", "cols", "fflags", "csc_ptr", "csc_rows", "cflags", "work_fwd", "work_bwd"):
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+
+
+@pytest.mark.parametrize("T,keep", [(1000, 0.7), (3000, 0.3), (8192, 0.7)])
+def test_tiles_qk_bitexact(scfa, T, keep):
+    wl = synth.Workload("t", "qk", 2, 3, T, 64, 91, p_keep=keep)
+    p = synth.make_problem(wl)
+    B, H, Tq, _ = p.q.shape
+    Tk = p.k.shape[2]
+    ws = scfa.workspace(scfa.attn_workspace_size(scfa.MODE_QK, 1, B, H, Tq, Tk, 64))
+    scfa.scfa_tiles(scfa.MODE_QK, cuda(p.q_idx), cuda(p.k_idx), None, None, B, H, Tq, Tk, 64, ws)
+    got = read_tiles(scfa, ws, scfa.MODE_QK, B, H, Tq, Tk, 64)
+    compare_tiles(got, tiles.live_list("qk", B, H, Tq, Tk, p.q_idx.numpy(), p.k_idx.numpy()))
+
+
+@pytest.mark.parametrize("T,nb", [(512, 4), (1000, 8), (8192, 16)])
+def test_tiles_hash_bitexact(scfa, T, nb):
+    rng = np.random.default_rng(T + nb)
+    B, H = 2, 2
+    qh = rng.integers(0, nb, (B, H, T))
+    kh = rng.integers(0, nb, (B, H, T))
+    pq, qs, _ = pipelines.hash_sort_view(qh, nb)
+    pk, ks, _ = pipelines.hash_sort_view(kh, nb)
+    ws = scfa.workspace(scfa.attn_workspace_size(scfa.MODE_HASH, 1, B, H, T, T, 64))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    scfa.scfa_tiles(scfa.MODE_HASH, t(pq), t(pk), t(qs), t(ks), B, H, T, T, 64, ws)
+    got = read_tiles(scfa, ws, scfa.MODE_HASH, B, H, T, T, 64)
+    compare_tiles(got, tiles.live_list("hash", B, H, T, T, pq, pk, qs, ks))
+
+
+@pytest.mark.parametrize("T", [1, 130, 1000])
+def test_tiles_dense_bitexact(scfa, T):
+    ws = scfa.workspace(scfa.attn_workspace_size(scfa.MODE_DENSE, 1, 1, 2, T, T, 64))
+    scfa.scfa_tiles(scfa.MODE_DENSE, None, None, None, None, 1, 2, T, T, 64, ws)
+    got = read_tiles(scfa, ws, scfa.MODE_DENSE, 1, 2, T, T, 64)
+    compare_tiles(got, tiles.live_list("dense", 1, 2, T, T))
+
+
+# ------------------------------------------------------------------ attention
+def run_step(scfa, p, mode, flags=0):
+    from sparse_causal_flash_gb300.pipeline import Step
+    B, H, Tq, D = p.q.shape
+    Tk = p.k.shape[2]
+    st = Step(mode, B, H, Tq, Tk, D, n_buckets=p.wl.n_buckets, flags=flags)
+    st.run(cuda(p.q), cuda(p.k), cuda(p.v), cuda(p.do), p.wl.scale,
+           q_idx=None if p.q_idx is None else cuda(p.q_idx), k_idx=None if p.k_idx is None else cuda(p.k_idx),
+           R=None if p.R is None else cuda(p.R))
+    torch.cuda.synchronize()
+    return st
+
+
+def compare_heads(st, ref, heads, lse_perm=None):
+    for (b, h) in heads:
+        r = ref[(b, h)]
+        check_close(f"O[{b},{h}]", st.o[b, h], r["o"])
+        lse_ref = r["lse"] if lse_perm is None else r["lse"][lse_perm[b, h]]
+        check_lse(f"LSE[{b},{h}]", st.lse[b, h], lse_ref)
+        check_close(f"dQ[{b},{h}]", st.dq[b, h], r["dq"])
+        check_close(f"dK[{b},{h}]", st.dk[b, h], r["dk"])
+        check_close(f"dV[{b},{h}]", st.dv[b, h], r["dv"])
+
+
+@pytest.mark.parametrize("B,H,T,keep,seed", [(2, 3, 1000, 0.7, 11), (1, 2, 2000, 0.3, 12), (1, 2, 300, 0.9, 13)])
+def test_qk_parity(scfa, B, H, T, keep, seed):
+    p = synth.make_problem(synth.Workload("qk", "qk", B, H, T, 64, seed, p_keep=keep))
+    st = run_step(scfa, p, scfa.MODE_QK)
+    ref = pipelines.run_qk(p.q, p.k, p.v, p.do, p.q_idx.numpy(), p.k_idx.numpy(), p.wl.scale)
+    compare_heads(st, ref, ref.keys())
+
+
+@pytest.mark.parametrize("B,H,T,nb,seed", [(1, 2, 512, 4, 1001), (1, 2, 1000, 8, 21), (2, 1, 1500, 2, 22)])
+def test_hash_parity(scfa, B, H, T, nb, seed):
+    p = synth.make_problem(synth.Workload("h", "hash", B, H, T, 64, seed, n_buckets=nb))
+    st = run_step(scfa, p, scfa.MODE_HASH)
+    ref, qh, kh = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, p.wl.scale)
+    pq, _, _ = pipelines.hash_sort_view(qh, nb)
+    compare_heads(st, ref, ref.keys(), lse_perm=pq)
+
+
+@pytest.mark.parametrize("B,H,T", [(1, 2, 700), (2, 1, 128), (1, 1, 1)])
+def test_dense_parity(scfa, B, H, T):
+    p = synth.make_problem(synth.Workload("d", "dense", B, H, T, 64, 31))
+    st = run_step(scfa, p, scfa.MODE_DENSE)
+    ref = pipelines.run_dense(p.q, p.k, p.v, p.do, p.wl.scale)
+    compare_heads(st, ref, ref.keys())
+
+
+def test_no_prune_gives_identical_results(scfa):
+    p = synth.make_problem(synth.Workload("qk", "qk", 1, 2, 1500, 64, 41, p_keep=0.6))
+    a = run_step(scfa, p, scfa.MODE_QK)
+    b = run_step(scfa, p, scfa.MODE_QK, flags=scfa.FLAG_NO_PRUNE)
+    for name in ("o", "lse", "dk", "dv"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    check_close("dQ no-prune", b.dq, to_np(a.dq), atol=1e-2, rel_l2=2e-3)
+
+
+def test_repeat_run_is_bit_identical_forward(scfa):
+    p = synth.make_problem(synth.Workload("h", "hash", 1, 2, 1000, 64, 42, n_buckets=8))
+    a = run_step(scfa, p, scfa.MODE_HASH)
+    o1, l1, dk1, dv1 = a.o.clone(), a.lse.clone(), a.dk.clone(), a.dv.clone()
+    b = run_step(scfa, p, scfa.MODE_HASH)
+    assert torch.equal(o1, b.o) and torch.equal(l1, b.lse)
+    assert torch.equal(dk1, b.dk) and torch.equal(dv1, b.dv)
+
+
+def test_empty_rows_output_zero(scfa):
+    # queries placed before every key: no admissible key -> O = 0, LSE = -inf, dQ = 0
+    B, H, Tq, Tk, D = 1, 1, 200, 300, 64
+    q_idx = torch.arange(Tq, dtype=torch.int32)[None, None]
+    k_idx = (torch.arange(Tk, dtype=torch.int32) + 150)[None, None]
+    q = synth.normal_bf16(3, 1, (B, H, Tq, D))
+    k = synth.normal_bf16(3, 2, (B, H, Tk, D))
+    v = synth.normal_bf16(3, 3, (B, H, Tk, D))
+    do = synth.normal_bf16(3, 4, (B, H, Tq, D))
+    p = synth.Problem(synth.Workload("e", "qk", B, H, Tq, D, 3), q, k, v, do, q_idx, k_idx)
+    st = run_step(scfa, p, scfa.MODE_QK)
+    assert torch.all(st.o[0, 0, :150] == 0) and torch.all(torch.isneginf(st.lse[0, 0, :150]))
+    assert torch.all(st.dq[0, 0, :150] == 0)
+    ref = pipelines.run_qk(q, k, v, do, q_idx.numpy(), k_idx.numpy(), p.wl.scale)
+    compare_heads(st, ref, ref.keys())
+
+
+def test_sentinel_padded_heads(scfa):
+    # heads with very different kept counts; padding rows must stay inert
+    p = synth.make_problem(synth.Workload("qk", "qk", 1, 4, 700, 64, 44, p_keep=0.5))
+    p.q_idx[0, 1, 100:] = synth.Q_SENTINEL
+    p.q[0, 1, 100:] = 0
+    p.k_idx[0, 2, 50:] = synth.K_SENTINEL
+    p.k[0, 2, 50:] = 0
+    st = run_step(scfa, p, scfa.MODE_QK)
+    ref = pipelines.run_qk(p.q, p.k, p.v, p.do, p.q_idx.numpy(), p.k_idx.numpy(), p.wl.scale)
+    compare_heads(st, ref, ref.keys())
+    assert torch.all(st.o[0, 1, 100:] == 0)
+    assert torch.all(st.dk[0, 2, 50:] == 0) and torch.all(st.dv[0, 2, 50:] == 0)
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled heads
+def test_full_qk_8k_sampled_heads(scfa):
+    wl = synth.WORKLOADS["qk_b4h12_t8192_d64_keep0.7"]
+    p = synth.make_problem(wl)
+    st = run_step(scfa, p, scfa.MODE_QK)
+    heads = [(0, 0), (3, 11)]
+    ref = pipelines.run_qk(p.q, p.k, p.v, p.do, p.q_idx.numpy(), p.k_idx.numpy(), wl.scale, heads=heads)
+    compare_heads(st, ref, heads)
+
+
+def test_full_hash_8k_sampled_heads(scfa):
+    wl = synth.WORKLOADS["hash_b4h12_t8192_d64_nb16"]
+    p = synth.make_problem(wl)
+    st = run_step(scfa, p, scfa.MODE_HASH)
+    heads = [(1, 5)]
+    qh = lsh.lsh_hash(p.q.double().numpy(), p.R.double().numpy())
+    kh = lsh.lsh_hash(p.k.double().numpy(), p.R.double().numpy())
+    np.testing.assert_array_equal(st.qh.cpu().numpy(), pipelines.hash_sort_view(qh, wl.n_buckets)[1])
+    ref, _, _ = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, wl.scale, heads=heads, q_hash=qh, k_hash=kh)
+    pq, _, _ = pipelines.hash_sort_view(qh, wl.n_buckets)
+    compare_heads(st, ref, heads, lse_perm=pq)
