@@ -67,8 +67,14 @@ enum { SCFA_MODE_DENSE = 0, SCFA_MODE_QK = 1, SCFA_MODE_HASH = 2 };
 
 /* flags */
 enum {
-  SCFA_FLAG_NO_PRUNE = 1,   /* treat every tile as live (results unchanged) */
-  SCFA_FLAG_DEBUG_SYNC = 4  /* synchronise the stream after every launch */
+  SCFA_FLAG_NO_PRUNE = 1,    /* treat every tile as live (results unchanged) */
+  SCFA_FLAG_DEBUG_SYNC = 4,  /* synchronise the stream after every launch */
+  SCFA_FLAG_REUSE_TILES = 8  /* the workspace already holds the live-tile list
+                                of these exact indices and shape (built by
+                                scfa_tiles or an earlier call on the same
+                                workspace): skip the metadata pass. One
+                                backward-sized workspace may then serve the
+                                forward and the backward call of a step. */
 };
 
 /* Tiles are SCFA_TILE rows of queries by SCFA_TILE rows of keys. */
@@ -212,6 +218,17 @@ typedef struct {
 
 scfa_status scfa_tile_view_get(const void* ws, int mode, int B, int H, int Tq, int Tk, int D,
                                scfa_tile_view* out);
+
+/* ----------------------------------------------------------------------------
+ * Profiling hook: when set, every later attention call records
+ * `start_event` (cudaEvent_t) on its stream right before launching the main
+ * attention kernel (forward: the fused forward kernel; backward: the fused
+ * backward kernel) and `stop_event` right after it, so the caller can time
+ * that kernel alone with cudaEventElapsedTime. `which` = 0 sets the events of
+ * forward kernels, 1 of backward kernels; NULL events switch the hook off.
+ * Process-wide setting; not synchronised between host threads.
+ * ------------------------------------------------------------------------- */
+scfa_status scfa_set_kernel_events(int which, void* start_event, void* stop_event);
 
 /* ----------------------------------------------------------------------------
  * Device status word of a workspace: SCFA_OK, or the first device-side error

@@ -5,8 +5,9 @@ tensors to the C ABI declared in include/scfa.h, which launches the CUDA
 kernels. Nothing here computes any part of the attention, hashing, sorting
 or tiling. PyTorch provides device memory and streams.
 
-If the shared library is missing, importing this package raises: there is
-no fallback path.
+The shared library is loaded on first use; if it is missing or lacks a
+declared entry point, that first call raises ImportError: there is no
+fallback path.
 """
 from __future__ import annotations
 
@@ -19,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libscfa.so")
 
 MODE_DENSE, MODE_QK, MODE_HASH = 0, 1, 2
-FLAG_NO_PRUNE, FLAG_DEBUG_SYNC = 1, 4
+FLAG_NO_PRUNE, FLAG_DEBUG_SYNC, FLAG_REUSE_TILES = 1, 4, 8
 TILE = 128
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "CUDA error", 5: "device timeout"}
 
@@ -29,14 +30,6 @@ class ScfaError(RuntimeError):
         super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({code})")
         self.code = code
 
-
-def _load() -> ctypes.CDLL:
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_causal_flash_gb300.build`")
-    return ctypes.CDLL(LIB_PATH)
-
-
-_lib = _load()
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -61,13 +54,42 @@ _SIGS = {
     "scfa_tiles": ([_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _U, _P], _I),
     "scfa_tile_view_get": ([_P, _I, _I, _I, _I, _I, _I, _P], _I),
     "scfa_get_device_status": ([_P, _P], _I),
+    "scfa_set_kernel_events": ([_I, _P, _P], _I),
 }
-for _name, (_args, _res) in _SIGS.items():
-    _fn = getattr(_lib, _name)
-    _fn.argtypes = _args
-    _fn.restype = _res
-
 EXPORTED = tuple(_SIGS)
+
+
+class _Lib:
+    """libscfa.so with typed entry points, opened on first attribute access."""
+
+    def __init__(self):
+        self._dll = None
+
+    def _open(self):
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_causal_flash_gb300.build`")
+        dll = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            try:
+                fn = getattr(dll, name)
+            except AttributeError as e:
+                raise ImportError(f"{LIB_PATH} lacks {name}: rebuild it") from e
+            fn.argtypes = args
+            fn.restype = res
+        self._dll = dll
+
+    def __getattr__(self, name):
+        if self._dll is None:
+            self._open()
+        return getattr(self._dll, name)
+
+
+_lib = _Lib()
+
+
+def load() -> None:
+    """Open libscfa.so now (raises ImportError if it is missing)."""
+    _lib.scfa_status_string
 
 
 class TileView(ctypes.Structure):
@@ -190,6 +212,13 @@ def scfa_tile_view_get(ws, mode, B, H, Tq, Tk, D) -> TileView:
 
 def scfa_get_device_status(ws, stream=None) -> int:
     return int(_lib.scfa_get_device_status(_ptr(ws), _stream(stream)))
+
+
+def scfa_set_kernel_events(which: int, start=None, stop=None):
+    """Record torch.cuda.Event `start` / `stop` around the fwd (0) / bwd (1) attention kernel."""
+    sp = None if start is None else ctypes.c_void_p(start.cuda_event)
+    ep = None if stop is None else ctypes.c_void_p(stop.cuda_event)
+    _check("scfa_set_kernel_events", _lib.scfa_set_kernel_events(which, sp, ep))
 
 
 def status_string(code: int) -> str:

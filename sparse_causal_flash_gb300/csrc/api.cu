@@ -91,6 +91,13 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
   return true;
 }
 
+static cudaEvent_t g_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
+
+void record_kernel_event(int which, bool start, cudaStream_t st) {
+  cudaEvent_t e = g_events[which][start ? 0 : 1];
+  if (e) cudaEventRecord(e, st);
+}
+
 bool lsh_ws_layout(int B, int H, int T, int n_buckets, LshWs* L) {
   if (B < 1 || H < 1 || T < 1 || n_buckets < 2) return false;
   LshWs w;
@@ -149,8 +156,11 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   if (!aligned256(ws) || ws_bytes < L.total) return SCFA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  cudaError_t e = launch_tiles(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, flags, w, L, st);
-  if (e != cudaSuccess) return SCFA_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (!(flags & SCFA_FLAG_REUSE_TILES)) {
+    e = launch_tiles(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, flags, w, L, st);
+    if (e != cudaSuccess) return SCFA_ERR_CUDA;
+  }
   AttnArgs a;
   a.mode = mode;
   a.B = B;
@@ -341,6 +351,13 @@ scfa_status scfa_tile_view_get(const void* ws, int mode, int B, int H, int Tq, i
   out->work_bwd = reinterpret_cast<const int32_t*>(w + L.work_bwd);
   out->n_q_tiles = L.nQt;
   out->n_k_tiles = L.nKt;
+  return SCFA_OK;
+}
+
+scfa_status scfa_set_kernel_events(int which, void* start_event, void* stop_event) {
+  if (which < 0 || which > 1) return SCFA_ERR_INVALID;
+  g_events[which][0] = static_cast<cudaEvent_t>(start_event);
+  g_events[which][1] = static_cast<cudaEvent_t>(stop_event);
   return SCFA_OK;
 }
 

@@ -501,7 +501,9 @@ cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
   int grid = sms;
   if (grid > p.n_work) grid = p.n_work;
   if (grid < 1) grid = 1;
+  record_kernel_event(1, true, st);
   attn_bwd_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, p);
+  record_kernel_event(1, false, st);
   {
     const long long n8 = qrows * D / 8;
     long long g = (n8 + 255) / 256;

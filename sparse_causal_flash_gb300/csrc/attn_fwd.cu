@@ -402,7 +402,9 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st) {
   int grid = num_sms();
   if (grid > p.n_work) grid = p.n_work;
   if (grid < 1) grid = 1;
+  record_kernel_event(0, true, st);
   attn_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, p);
+  record_kernel_event(0, false, st);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,9 @@ struct AttnArgs {
   const AttnWs* L;
 };
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st);
+
+// profiling hook: events recorded around the main fwd (0) / bwd (1) kernel
+void record_kernel_event(int which, bool start, cudaStream_t st);
 cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st);
 
 }  // namespace scfa

@@ -12,7 +12,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size, lsh_bucket_sort, lsh_gather,
+from . import (FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size, lsh_bucket_sort, lsh_gather,
                lsh_unsort, lsh_workspace_size, scfa_dense_bwd, scfa_dense_fwd, scfa_hash_bwd, scfa_hash_fwd,
                scfa_qk_bwd, scfa_qk_fwd, workspace)
 
@@ -33,8 +33,10 @@ class Step:
         self.dq = torch.empty((B, H, Tq, D), **bf)
         self.dk = torch.empty((B, H, Tk, D), **bf)
         self.dv = torch.empty((B, H, Tk, D), **bf)
-        self.ws_f = workspace(attn_workspace_size(mode, 0, B, H, Tq, Tk, D), dev)
+        # one backward-sized workspace: the forward call builds the live-tile
+        # list in it and the backward call reuses that list
         self.ws_b = workspace(attn_workspace_size(mode, 1, B, H, Tq, Tk, D), dev)
+        self.ws_f = self.ws_b
         if mode == MODE_HASH:
             T = Tq
             self.ws_l = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
@@ -56,13 +58,14 @@ class Step:
     def run(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None, stream=None):
         """Forward + backward. Results land in self.o/lse/dq/dk/dv."""
         f = self.flags
+        fr = f | FLAG_REUSE_TILES
         if self.mode == MODE_DENSE:
             scfa_dense_fwd(q, k, v, scale, self.o, self.lse, self.ws_f, f, stream)
-            scfa_dense_bwd(q, k, v, self.o, self.lse, do, scale, self.dq, self.dk, self.dv, self.ws_b, f, stream)
+            scfa_dense_bwd(q, k, v, self.o, self.lse, do, scale, self.dq, self.dk, self.dv, self.ws_b, fr, stream)
         elif self.mode == MODE_QK:
             scfa_qk_fwd(q, k, v, q_idx, k_idx, scale, self.o, self.lse, self.ws_f, f, stream)
             scfa_qk_bwd(q, k, v, self.o, self.lse, do, q_idx, k_idx, scale, self.dq, self.dk, self.dv, self.ws_b,
-                        f, stream)
+                        fr, stream)
         else:
             nb = self.nb
             lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, stream)
@@ -72,7 +75,7 @@ class Step:
                           self.lse, self.ws_f, f, stream)
             lsh_gather(do, self.pq, self.do_s, stream)
             scfa_hash_bwd(self.q_s, self.k_s, self.v_s, self.o_s, self.lse, self.do_s, self.pq, self.pk, self.qh,
-                          self.kh, scale, self.dq_s, self.dk_s, self.dv_s, self.ws_b, f, stream)
+                          self.kh, scale, self.dq_s, self.dk_s, self.dv_s, self.ws_b, fr, stream)
             lsh_unsort(self.o_s, self.pq, self.o, stream)
             lsh_unsort(self.dq_s, self.pq, self.dq, stream)
             lsh_unsort(self.dk_s, self.pk, self.dk, stream)
