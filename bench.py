@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark of sparse causal flash attention (SCFA) forward + backward on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input: the
+live-tile metadata, the attention forward, the backward pre-pass, the
+attention backward and the dQ finalisation (hash mode adds the LSH hash,
+bucket sort, row gathers and unsorts). Default workload: QK-sparse,
+B=4, H=12, T=8192, D=64, each head keeping each query and key with
+probability 0.7 (30% drop), bf16 N(0,1) inputs.
+
+Reported (one JSON line on rank 0):
+  value        useful TFLOP/s of the whole job: 14 * D * (admissible pairs)
+               per step (4 D forward + 10 D backward per pair), divided by the
+               device time of the step; inputs resident in HBM; L2 flushed
+               (256 MiB write) before every timed step, outside its events.
+  e2e          the same metric with, every step, the host->device copy of the
+               step's inputs from pinned memory and the device->host copy of
+               O, LSE, dQ, dK, dV inside the timed region.
+  dense        the library's own dense causal kernels at the same (B,H,T,D).
+  roofline     the dominant attention kernel (timed alone with CUDA events
+               recorded by the library around its launch) against the
+               measured bf16 tensor peak.
+  cpu_baseline the float64 CPU oracle on a bounded sample of the workload.
+
+--impl reference times that oracle on the host cores as the reference arm.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+heads are independent problems; no collective on the data path); timing is
+the max over ranks and value sums the units of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SCFA fwd+bwd ms and useful TFLOP/s vs own dense causal, % of BF16 TC peak"
+DEFAULT_WORKLOAD = "qk_b4h12_t8192_d64_keep0.7"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------- units
+def admissible_pairs(wl, prob, step=None) -> int:
+    """Exact count of unmasked (query, key) pairs of the whole workload."""
+    if wl.mode == "dense":
+        return wl.B * wl.H * wl.T * (wl.T + 1) // 2
+    if wl.mode == "qk":
+        qi = prob.q_idx.numpy().astype(np.int64)
+        ki = prob.k_idx.numpy().astype(np.int64)
+        total = 0
+        for b in range(qi.shape[0]):
+            for h in range(qi.shape[1]):
+                q = qi[b, h][qi[b, h] >= 0]
+                k = np.sort(ki[b, h][ki[b, h] != 2**31 - 1])
+                total += int(np.searchsorted(k, q, side="right").sum())
+        return total
+    # hash: bucket ids from the library's own (bit-exact) hash, original order
+    pq = step.pq.cpu().numpy().astype(np.int64)
+    pk = step.pk.cpu().numpy().astype(np.int64)
+    hq = step.qh.cpu().numpy().astype(np.int64)
+    hk = step.kh.cpu().numpy().astype(np.int64)
+    total = 0
+    for b in range(pq.shape[0]):
+        for h in range(pq.shape[1]):
+            # within a bucket, both lists are in position order (stable sort)
+            for c in np.unique(hq[b, h]):
+                qpos = pq[b, h][hq[b, h] == c]
+                kpos = pk[b, h][hk[b, h] == c]
+                total += int(np.searchsorted(kpos, qpos, side="right").sum())
+    return total
+
+
+def kernels_per_step(mode: str) -> int:
+    tiles = 6            # tile stats (q, k), count, scan, fill, work order
+    attn = 1 + 3         # forward; backward pre-pass, backward, dQ finalise
+    if mode == "hash":
+        return tiles + attn + 2 * 3 + 2 + 4   # 2 x (hash, sort, gather), gather V / dO, 4 unsorts
+    return tiles + attn
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                self.rows.append((time.time(), parts))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [p for (t, p) in self.rows if t0 - 0.2 <= t <= t1 + 0.2]
+        use = inside if len(inside) >= 3 else [p for (_, p) in self.rows]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[2]) for p in use if num(p[2]) is not None]
+        smax = [num(p[3]) for p in use if num(p[3]) is not None]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for p in use:
+            for name, val in zip(names, p[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------- CPU oracle sample
+def oracle_sample(wl, prob, budget_s: float, max_heads: int | None = None):
+    """Run the float64 oracle head by head until the budget is spent."""
+    from oracle import pipelines
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    flops = 0.0
+    done = []
+    t0 = time.perf_counter()
+    for bh in heads:
+        if wl.mode == "qk":
+            r = pipelines.run_qk(prob.q, prob.k, prob.v, prob.do, prob.q_idx.numpy(), prob.k_idx.numpy(), wl.scale,
+                                 heads=[bh])
+        elif wl.mode == "hash":
+            r, _, _ = pipelines.run_hash(prob.q[bh[0]:bh[0] + 1, bh[1]:bh[1] + 1], prob.k[bh[0]:bh[0] + 1, bh[1]:bh[1] + 1],
+                                         prob.v[bh[0]:bh[0] + 1, bh[1]:bh[1] + 1],
+                                         prob.do[bh[0]:bh[0] + 1, bh[1]:bh[1] + 1], prob.R, wl.scale)
+        else:
+            r = pipelines.run_dense(prob.q, prob.k, prob.v, prob.do, wl.scale, heads=[bh])
+        pairs = sum(x["pairs"] for x in r.values())
+        flops += pipelines.useful_flops(pairs, wl.D)
+        done.append(bh)
+        if time.perf_counter() - t0 >= budget_s or (max_heads and len(done) >= max_heads):
+            break
+    el = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(done)} of {wl.B * wl.H} heads, full fwd+bwd each, float64 numpy/OpenBLAS, {el:.1f} s",
+            "seconds": el, "heads": len(done)}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = rec.get(kernel)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "sparse_causal_flash_gb300", "csrc", e["source"])
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    if digest != e.get("sha256") or e.get("workload") is None:
+        return None
+    return e
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return
+    import synth
+    prob = synth.make_problem(wl)
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    from oracle import pipelines
+
+    def one(bh):
+        if wl.mode == "qk":
+            r = pipelines.run_qk(prob.q, prob.k, prob.v, prob.do, prob.q_idx.numpy(), prob.k_idx.numpy(), wl.scale,
+                                 heads=[bh])
+        elif wl.mode == "hash":
+            sl = lambda t: t[bh[0]:bh[0] + 1, bh[1]:bh[1] + 1]
+            r, _, _ = pipelines.run_hash(sl(prob.q), sl(prob.k), sl(prob.v), sl(prob.do), prob.R, wl.scale)
+        else:
+            r = pipelines.run_dense(prob.q, prob.k, prob.v, prob.do, wl.scale, heads=[bh])
+        return pipelines.useful_flops(sum(x["pairs"] for x in r.values()), wl.D)
+
+    for i in range(args.warmup):
+        one(heads[i % len(heads)])
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops += one(heads[i % len(heads)])
+    el = time.perf_counter() - t0
+    value = flops / el / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "T": wl.T, "D": wl.D,
+                   "step": "one (batch, head) problem of the workload, fwd+bwd, cycling over heads"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} heads of {wl.B * wl.H}, one per step, float64 fwd+bwd"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- our arm
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl, rank, world)
+
+    prob = synth.make_problem(wl)  # host tensors (also used by the CPU oracle sample)
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base = oracle_sample(wl, prob, args.cpu_seconds)  # before the first GPU call
+
+    import torch
+    import sparse_causal_flash_gb300 as scfa
+    from sparse_causal_flash_gb300 import build as scfa_build
+    from sparse_causal_flash_gb300.pipeline import Step
+    scfa_build.build()
+    scfa.load()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    mode = {"dense": scfa.MODE_DENSE, "qk": scfa.MODE_QK, "hash": scfa.MODE_HASH}[wl.mode]
+    B, H, Tq, D = prob.q.shape
+    Tk = prob.k.shape[2]
+    step = Step(mode, B, H, Tq, Tk, D, n_buckets=wl.n_buckets, device=dev)
+    q, k, v, do = (t.to(dev) for t in (prob.q, prob.k, prob.v, prob.do))
+    q_idx = prob.q_idx.to(dev) if prob.q_idx is not None else None
+    k_idx = prob.k_idx.to(dev) if prob.k_idx is not None else None
+    R = prob.R.to(dev) if prob.R is not None else None
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def run_once():
+        step.run(q, k, v, do, wl.scale, q_idx=q_idx, k_idx=k_idx, R=R)
+
+    for _ in range(max(args.warmup, 3)):
+        run_once()
+    torch.cuda.synchronize()
+    assert scfa.scfa_get_device_status(step.ws_b) == 0, "device status not ok after warm-up"
+    pairs = admissible_pairs(wl, prob, step)
+    useful = 14.0 * D * pairs
+
+    def timed(run, K, kernel_events=False):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+               for _ in range(K)] if kernel_events else None
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(K):
+            flush.zero_()
+            if kev is not None:
+                scfa.scfa_set_kernel_events(0, *kev[i][0])
+                scfa.scfa_set_kernel_events(1, *kev[i][1])
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        t1 = time.time()
+        scfa.scfa_set_kernel_events(0)
+        scfa.scfa_set_kernel_events(1)
+        ms = [a.elapsed_time(b) for a, b in ev]
+        kms = None
+        if kev is not None:
+            kms = ([a.elapsed_time(b) for (a, b) in (x[0] for x in kev)],
+                   [a.elapsed_time(b) for (a, b) in (x[1] for x in kev)])
+        return ms, kms, t0, t1
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    ms, kms, t0, t1 = timed(run_once, args.steps, kernel_events=True)
+    clocks = sampler.stop(t0, t1) if sampler else None
+    assert scfa.scfa_get_device_status(step.ws_b) == 0, "device status not ok after the timed steps"
+    total_ms = sum(ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * useful * args.steps / (total_ms / 1e3) / 1e12
+
+    # the attention kernels timed alone (events recorded by the library around each launch)
+    fwd_ms = statistics.mean(kms[0])
+    bwd_ms = statistics.mean(kms[1])
+    peak_burst, peak_sus, peak_kind = load_peaks()
+    long_region = (t1 - t0) > 1.0
+    peak = peak_sus if long_region else peak_burst
+    if bwd_ms >= fwd_ms:
+        dom, dom_ms, dom_flops, src = "attn_bwd_kernel", bwd_ms, 10.0 * D * pairs, "attn_bwd.cu"
+    else:
+        dom, dom_ms, dom_flops, src = "attn_fwd_kernel", fwd_ms, 4.0 * D * pairs, "attn_fwd.cu"
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    tr = load_traffic(dom)
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None if tr is None else tr["bytes_per_launch"],
+                "peak_source": f"{peak_kind} bf16 {'sustained' if long_region else 'burst'}",
+                "kernel_ms": dom_ms, "fwd_kernel_ms": fwd_ms, "bwd_kernel_ms": bwd_ms,
+                "fwd_kernel_tflops": 4.0 * D * pairs / (fwd_ms / 1e3) / 1e12,
+                "bwd_kernel_tflops": 10.0 * D * pairs / (bwd_ms / 1e3) / 1e12}
+
+    dense = None
+    if not args.no_dense and wl.mode != "dense":
+        dstep = Step(scfa.MODE_DENSE, wl.B, wl.H, wl.T, wl.T, D, device=dev)
+        dq_ = synth.normal_bf16(wl.seed, synth.TID_Q, (wl.B, wl.H, wl.T, D)).to(dev)
+        dk_ = synth.normal_bf16(wl.seed, synth.TID_K, (wl.B, wl.H, wl.T, D)).to(dev)
+        dv_ = synth.normal_bf16(wl.seed, synth.TID_V, (wl.B, wl.H, wl.T, D)).to(dev)
+        ddo = synth.normal_bf16(wl.seed, synth.TID_DO, (wl.B, wl.H, wl.T, D)).to(dev)
+        run_dense = lambda: dstep.run(dq_, dk_, dv_, ddo, wl.scale)
+        for _ in range(3):
+            run_dense()
+        dK = max(5, args.steps // 4)
+        dms, _, _, _ = timed(run_dense, dK)
+        d_ms = sum(dms) / dK
+        d_useful = 14.0 * D * wl.B * wl.H * wl.T * (wl.T + 1) / 2
+        dense = {"ms_per_step": d_ms, "useful_tflops": d_useful / (d_ms / 1e3) / 1e12, "steps": dK,
+                 "speedup_sparse_vs_dense": d_ms / ms_per_step}
+        del dstep, dq_, dk_, dv_, ddo
+
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.pin_memory() if t is not None else None
+        hq, hk, hv, hdo = pin(prob.q), pin(prob.k), pin(prob.v), pin(prob.do)
+        hqi, hki, hR = pin(prob.q_idx), pin(prob.k_idx), pin(prob.R)
+        outs = [step.o, step.lse, step.dq, step.dk, step.dv]
+        houts = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hqi, hki, hR) if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in houts)
+
+        def run_e2e():
+            for dst, src in ((q, hq), (k, hk), (v, hv), (do, hdo), (q_idx, hqi), (k_idx, hki), (R, hR)):
+                if src is not None:
+                    dst.copy_(src, non_blocking=True)
+            run_once()
+            for h, o in zip(houts, outs):
+                h.copy_(o, non_blocking=True)
+
+        for _ in range(2):
+            run_e2e()
+        K = max(5, args.steps // 2)
+        ems, _, _, _ = timed(run_e2e, K)
+        tot = sum(ems)
+        if dist is not None:
+            t = torch.tensor([tot], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            tot = float(t.item())
+        e2e = {"value": world * useful * K / (tot / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": tot / K, "steps": K}
+
+    if rank == 0:
+        cfg = {"workload": wl.name, "mode": wl.mode, "B": wl.B, "H": wl.H, "T": wl.T, "D": wl.D,
+               "Tq": Tq, "Tk": Tk, "admissible_pairs": pairs, "useful_flop_per_step": useful,
+               "l2": "flushed before every timed step (256 MiB write), outside the step's events",
+               "parallelism": f"replicas x{world}"}
+        if wl.mode == "qk":
+            cfg["p_keep"] = wl.p_keep
+        if wl.mode == "hash":
+            cfg["n_buckets"] = wl.n_buckets
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "pct_of_bf16_peak": 100.0 * (value / world) / peak,
+            "dense": dense, "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
+            "gpu_launches": kernels_per_step(wl.mode) * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
