@@ -316,6 +316,11 @@ def main():
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
                for _ in range(K)] if kernel_events else None
+        if kev is not None:  # torch creates the CUDA event on first record; the library re-records it
+            for pair in kev:
+                for a, b in pair:
+                    a.record(stream)
+                    b.record(stream)
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
