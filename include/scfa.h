@@ -237,6 +237,36 @@ scfa_status scfa_set_kernel_events(int which, void* start_event, void* stop_even
  * ------------------------------------------------------------------------- */
 scfa_status scfa_get_device_status(const void* ws, void* stream);
 
+/* ----------------------------------------------------------------------------
+ * Allocation-free QK-sparse forward (the paper has no counterpart: this is a
+ * packaging variant for callers that cannot allocate device memory).
+ *
+ * Same operation, arguments, layouts and results as scfa_qk_fwd, without the
+ * workspace: the forward's scratch (the live-tile metadata) is a
+ * SCFA_NOALLOC_SCRATCH_BYTES array compiled into the library, which every GPU
+ * that loads the library keeps until the process exits. For callers that may
+ * not call cudaMalloc where they run attention: inside CUDA graph capture,
+ * under a fixed-pool allocator, or in a host framework's callbacks. The call
+ * allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
+ *
+ * - Shapes whose forward scratch exceeds SCFA_NOALLOC_SCRATCH_BYTES (see
+ *   scfa_attn_workspace_size(SCFA_MODE_QK, 0, ...)) are rejected on the host
+ *   with SCFA_ERR_WORKSPACE before anything is launched.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture begins.
+ * - Every call shares the one array: calls that overlap on the GPU (e.g. on
+ *   two unordered streams) race. Each call clears and rewrites all the
+ *   scratch it reads.
+ * - The device status word lives in the array and is not exposed.
+ * ------------------------------------------------------------------------- */
+#define SCFA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+scfa_status scfa_qk_fwd_noalloc(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                const int32_t* q_idx, const int32_t* k_idx,
+                                int B, int H, int Tq, int Tk, int D, float scale,
+                                uint16_t* o, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
