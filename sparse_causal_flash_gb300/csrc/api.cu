@@ -51,6 +51,21 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, long long T, l
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a [BH][T][64] fp32 tensor; box = 32 columns x 128 rows x 1
+// head, 128-byte swizzle (used by TMA reduce-add; rows past T are skipped).
+bool make_tmap_f32_3d_w64(CUtensorMap* map, void* base, long long T, long long BH) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {64 * 4, static_cast<cuuint64_t>(T) * 64 * 4};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D, AttnWs* L) {
   if (mode < SCFA_MODE_DENSE || mode > SCFA_MODE_HASH) return false;
   if (B < 1 || H < 1 || Tq < 1 || Tk < 1 || D < 1) return false;

@@ -11,19 +11,27 @@
 //
 // GB300 design: persistent CTAs walk the backward work order (key tiles by
 // live count, longest first); each work item keeps K_j, V_j resident and
-// streams the live query tiles of its CSC column:
-//   warp 0      TMA producer: K_j, V_j once; Q_i, dO_i into a 2-stage ring.
-//   warp 1      TMEM owner; lane 0 issues tcgen05.mma:
-//               S^T = K Q^T and dP^T = V dO^T (TMEM, keys on lanes), then
-//               dV += P^T dO, dK += dS^T Q (TMEM accumulators for the whole
-//               item) and dQ_i = dS K (TMEM, queries on lanes).
-//   warps 2-5   thread = key row: P^T = exp2(S^T - LSE) under the mask,
-//               dS^T = P^T (dP^T - Drow) * scale, both written as bf16 to
-//               shared memory; one buffer serves as K-major A operand of
-//               dV / dK and as MN-major A operand (dS) of dQ.
-//   warps 6-9   thread = query row: dQ_i from TMEM, added into an fp32
-//               accumulator in the workspace with 16-byte vector atomics.
-// The epilogue of each item writes dK, dV (bf16) straight from TMEM.
+// streams the live query tiles i of its CSC column. Per query tile:
+//   A(i): S^T = K Q_i^T and dP^T = V dO_i^T      (tcgen05, TMEM, keys on lanes)
+//   compute(i): P^T = exp2(S^T - LSE) under the mask -> TMEM (bf16, the A
+//         operand of the dV MMA); dS^T = P^T (dP^T - Drow) scale -> shared
+//         memory (bf16, double-buffered)
+//   B(i): dV += P^T dO_i (A from TMEM), dK += dS^T Q_i, dQ_i = dS K
+// The MMA warp issues A(i+1) as soon as compute(i) has read S^T / dP^T out of
+// TMEM, so the tensor core runs A(i+1) and B(i-1) while compute(i) works.
+// Roles (448 threads):
+//   warp 0       producer: lane 0 issues the TMA loads of K_j, V_j (once per
+//                item) and Q_i, dO_i (2-stage ring); all 32 lanes stage the
+//                query metadata (position, bucket, LSE in log2 units,
+//                rowsum * scale) of tile i next to it.
+//   warp 1       TMEM owner (512 columns); lane 0 issues every tcgen05.mma.
+//   warps 2-9    two compute warpgroups; thread = key row = TMEM lane; the
+//                first group owns query columns 0-63, the second 64-127.
+//   warps 10-13  dQ warpgroup; thread = query row: dQ_i from TMEM into a
+//                swizzled fp32 shared tile, then one TMA reduce-add per
+//                64-column half into the fp32 accumulator in the workspace.
+// TMEM columns: S^T [0,128) dP^T [128,256) dV [256,320) dK [320,384)
+// dQ [384,448) P^T (bf16 pairs) [448,512). Every wait is bounded.
 #include <climits>
 
 #include "common.cuh"
@@ -33,7 +41,7 @@ namespace scfa {
 namespace {
 
 constexpr int kSubBytes = kTile * 128;
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 448;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -43,15 +51,15 @@ struct __align__(1024) BwdSmem {
   uint8_t v[D / 64][kSubBytes];
   uint8_t q[2][D / 64][kSubBytes];
   uint8_t dO[2][D / 64][kSubBytes];
-  uint8_t pt[2][kSubBytes];   // P^T  [128 keys][128 queries] as two 64-query halves
-  uint8_t dst[2][kSubBytes];  // dS^T [128 keys][128 queries]
+  uint8_t dst[2][2][kSubBytes];   // dS^T [buffer][query half][128 keys x 64 queries]
+  uint8_t dqs[2][kSubBytes];      // dQ fp32 staging: [column half][128 rows x 32 floats], swizzled
   int32_t qidx[2][kTile];
   int32_t qhash[2][kTile];
-  float lse2[2][kTile];
-  float drow[2][kTile];
+  float lse2[2][kTile];           // LSE * log2(e)
+  float drs[2][kTile];            // rowsum(dO * O) * scale
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2];
-  uint64_t s_full, dp_full, st_empty, ds_full, ds_empty, dq_full, dq_empty, dkv_full, dkv_empty, drain;
+  uint64_t s_full, st_empty, ds_full, pt_free, ds_free[2], dq_full, dq_empty, dkv_full, dkv_empty, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -71,7 +79,6 @@ struct BwdParams {
   const uint8_t* cflags;
   const int32_t* work;
   int n_work;
-  float* dq_acc;
   uint16_t* dk;
   uint16_t* dv;
   int* status;
@@ -93,29 +100,30 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  static_assert(D == 64, "the backward TMEM plan holds D = 64");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw + pad);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr uint32_t kColS = 0, kColDP = kTile, kColDV = 2 * kTile, kColDK = 2 * kTile + D, kColDQ = 2 * kTile + 2 * D;
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384, kColPT = 448;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_full[s], 2);
       mbar_init(&sm.q_empty[s], 1);
+      mbar_init(&sm.ds_free[s], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.st_empty, 128);
-    mbar_init(&sm.ds_full, 128);
-    mbar_init(&sm.ds_empty, 1);
+    mbar_init(&sm.st_empty, 256);
+    mbar_init(&sm.ds_full, 256);
+    mbar_init(&sm.pt_free, 1);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_empty, 128);
     mbar_init(&sm.dkv_full, 1);
-    mbar_init(&sm.dkv_empty, 128);
+    mbar_init(&sm.dkv_empty, 256);
     mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
@@ -123,6 +131,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
   tc_fence_before();
@@ -132,36 +141,62 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   volatile int* abort_flag = &sm.abort_flag;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int q_it = 0, item = 0, last_kv = -1;
-      for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
-        const int g = p.work[w];
-        const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
-        if (n == 0) continue;
-        const int bh = g / p.nKt, j = g % p.nKt;
-        if (!mbar_wait(&sm.kv_empty, (item & 1) ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&sm.kv_full, 2 * D * kTile * 2);
-        for (int sub = 0; sub < D / 64; ++sub) {
-          tma_load_3d(sm.k[sub], &tm_k, &sm.kv_full, sub * 64, j * kTile, bh);
-          tma_load_3d(sm.v[sub], &tm_v, &sm.kv_full, sub * 64, j * kTile, bh);
-        }
-        last_kv = item;
-        bool ok = true;
-        for (int t = 0; t < n; ++t) {
-          const int i = p.csc_rows[start + t];
-          const int s = q_it & 1;
-          if (!mbar_wait(&sm.q_empty[s], ((q_it >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&sm.q_full[s], 2 * D * kTile * 2);
+    // ------------------------------------------------------------ producer warp
+    int q_it = 0, item = 0, last_kv = -1;
+    for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+      const int g = p.work[w];
+      const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
+      if (n == 0) continue;
+      const int bh = g / p.nKt, j = g % p.nKt;
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&sm.kv_empty, (item & 1) ^ 1, abort_flag, p.status);
+        if (ok) {
+          mbar_arrive_expect_tx(&sm.kv_full, 2 * D * kTile * 2);
           for (int sub = 0; sub < D / 64; ++sub) {
-            tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
-            tma_load_3d(sm.dO[s][sub], &tm_do, &sm.q_full[s], sub * 64, i * kTile, bh);
+            tma_load_3d(sm.k[sub], &tm_k, &sm.kv_full, sub * 64, j * kTile, bh);
+            tma_load_3d(sm.v[sub], &tm_v, &sm.kv_full, sub * 64, j * kTile, bh);
           }
-          ++q_it;
+          last_kv = item;
         }
-        if (!ok) break;
-        ++item;
       }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      for (int t = 0; t < n; ++t) {
+        const int i = p.csc_rows[start + t];
+        const int s = q_it & 1;
+        if (lane == 0) {
+          ok = mbar_wait(&sm.q_empty[s], ((q_it >> 1) & 1) ^ 1, abort_flag, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.q_full[s], 2 * D * kTile * 2);
+            for (int sub = 0; sub < D / 64; ++sub) {
+              tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
+              tma_load_3d(sm.dO[s][sub], &tm_do, &sm.q_full[s], sub * 64, i * kTile, bh);
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+        // query metadata of tile i, next to its Q / dO stage
+        for (int c = lane; c < kTile; c += 32) {
+          const int qrow = i * kTile + c;
+          const bool qv = qrow < p.Tq;
+          const long long gq = static_cast<long long>(bh) * p.Tq + qrow;
+          int qid;
+          if (p.mode == SCFA_MODE_DENSE) qid = qv ? qrow : INT_MIN;
+          else qid = qv ? p.q_idx[gq] : INT_MIN;
+          sm.qidx[s][c] = qid;
+          sm.qhash[s][c] = (p.mode == SCFA_MODE_HASH && qv) ? p.q_hash[gq] : 0;
+          sm.lse2[s][c] = qv ? p.lse[gq] * kLog2e : 0.f;
+          sm.drs[s][c] = qv ? p.drow[gq] * p.scale : 0.f;
+        }
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.q_full[s]);
+        ++q_it;
+      }
+      if (!ok) break;
+      ++item;
+    }
+    if (lane == 0) {
       for (int d = 1; d <= 2 && d <= q_it; ++d) {
         const int it = q_it - d;
         mbar_wait(&sm.q_full[it & 1], (it >> 1) & 1, abort_flag, p.status);
@@ -176,57 +211,67 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       constexpr uint32_t idesc_q = idesc_bf16_f32(kTile, D, 1, 1);
       const uint32_t k_base = smem_u32(sm.k[0]);
       const uint32_t v_base = smem_u32(sm.v[0]);
-      const uint32_t pt_base = smem_u32(sm.pt[0]);
-      const uint32_t dst_base = smem_u32(sm.dst[0]);
       int q_it = 0, it = 0, item = 0;
       bool ok = true;
+      // A(i): S^T and dP^T of query tile stage s into TMEM
+      auto issue_a = [&](int qi, int ii) -> bool {
+        const int s = qi & 1;
+        if (!mbar_wait(&sm.q_full[s], (qi >> 1) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&sm.st_empty, (ii & 1) ^ 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t q_base = smem_u32(sm.q[s][0]);
+        const uint32_t do_base = smem_u32(sm.dO[s][0]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + kColS, smem_desc_sw128(k_base + off, 16, 1024),
+                      smem_desc_sw128(q_base + off, 16, 1024), idesc_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + kColDP, smem_desc_sw128(v_base + off, 16, 1024),
+                      smem_desc_sw128(do_base + off, 16, 1024), idesc_s, kk > 0);
+        }
+        tc_commit(&sm.s_full);
+        return true;
+      };
       for (int w = blockIdx.x; w < p.n_work && ok; w += gridDim.x) {
         const int g = p.work[w];
         const int n = p.csc_ptr[g + 1] - p.csc_ptr[g];
         if (n == 0) continue;
         if (!mbar_wait(&sm.kv_full, item & 1, abort_flag, p.status)) break;
+        if (!issue_a(q_it, it)) break;
         for (int t = 0; t < n; ++t) {
           const int s = q_it & 1;
-          if (!mbar_wait(&sm.q_full[s], (q_it >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-          if (!mbar_wait(&sm.st_empty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t q_base = smem_u32(sm.q[s][0]);
-          const uint32_t do_base = smem_u32(sm.dO[s][0]);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-            mma_bf16_ss(tmem + kColS, smem_desc_sw128(k_base + off, 16, 1024),
-                        smem_desc_sw128(q_base + off, 16, 1024), idesc_s, kk > 0);
-          }
-          tc_commit(&sm.s_full);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-            mma_bf16_ss(tmem + kColDP, smem_desc_sw128(v_base + off, 16, 1024),
-                        smem_desc_sw128(do_base + off, 16, 1024), idesc_s, kk > 0);
-          }
-          tc_commit(&sm.dp_full);
+          const int db = it & 1;
+          if (t + 1 < n && !issue_a(q_it + 1, it + 1)) { ok = false; break; }
           if (!mbar_wait(&sm.ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
           if (t == 0 && !mbar_wait(&sm.dkv_empty, (item & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
           if (!mbar_wait(&sm.dq_empty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
+          const uint32_t q_base = smem_u32(sm.q[s][0]);
+          const uint32_t do_base = smem_u32(sm.dO[s][0]);
+          const uint32_t ds_base = smem_u32(sm.dst[db][0]);
+          // dV += P^T dO (A = P^T in TMEM, two bf16 per column along the queries)
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t a_off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-            const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-            mma_bf16_ss(tmem + kColDV, smem_desc_sw128(pt_base + a_off, 16, 1024),
-                        smem_desc_sw128(do_base + kk * 2048, kSubBytes, 1024), idesc_kv, acc);
-            mma_bf16_ss(tmem + kColDK, smem_desc_sw128(dst_base + a_off, 16, 1024),
-                        smem_desc_sw128(q_base + kk * 2048, kSubBytes, 1024), idesc_kv, acc);
-          }
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
+                        smem_desc_sw128(do_base + kk * 2048, kSubBytes, 1024), idesc_kv, (t > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&sm.pt_free);
+          // dK += dS^T Q
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            mma_bf16_ss(tmem + kColDQ, smem_desc_sw128(dst_base + kk * 2048, kSubBytes, 1024),
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss(tmem + kColDK, smem_desc_sw128(ds_base + (kk >> 2) * kSubBytes + (kk & 3) * 32, 16, 1024),
+                        smem_desc_sw128(q_base + kk * 2048, kSubBytes, 1024), idesc_kv, (t > 0 || kk > 0) ? 1u : 0u);
+          // dQ_i = dS K (A = dS^T viewed MN-major: queries contiguous, keys along rows)
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss(tmem + kColDQ, smem_desc_sw128(ds_base + kk * 2048, kSubBytes, 1024),
                         smem_desc_sw128(k_base + kk * 2048, kSubBytes, 1024), idesc_q, kk > 0 ? 1u : 0u);
-          }
           tc_commit(&sm.dq_full);
           tc_commit(&sm.q_empty[s]);
-          tc_commit(&sm.ds_empty);
+          tc_commit(&sm.ds_free[db]);
           ++q_it;
           ++it;
         }
@@ -238,13 +283,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc_commit(&sm.drain);
       mbar_wait(&sm.drain, 0, abort_flag, p.status);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ P^T / dS^T warpgroup
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ P^T / dS^T warpgroups
+    const int grp = (warp - 2) >> 2;       // 0: query columns 0-63, 1: 64-127
     const int quarter = warp & 3;
-    const int kr = quarter * 32 + lane;  // key row = TMEM lane
-    const int tid = threadIdx.x - 64;    // 0..127
+    const int kr = quarter * 32 + lane;    // key row = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    int it = 0, item = 0;
+    int it = 0, q_it = 0, item = 0;
     for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
       const int g = p.work[w];
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
@@ -254,13 +299,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const long long gk = static_cast<long long>(bh) * p.Tk + key;
       if (n == 0) {
         if (kvalid) {
-          uint4* a = reinterpret_cast<uint4*>(p.dk + gk * D);
-          uint4* b = reinterpret_cast<uint4*>(p.dv + gk * D);
+          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + gk * D);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
-            a[c] = make_uint4(0, 0, 0, 0);
-            b[c] = make_uint4(0, 0, 0, 0);
-          }
+          for (int c = 0; c < D / 8; ++c) a[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -270,92 +311,116 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (p.mode == SCFA_MODE_HASH && kvalid) kh = p.k_hash[gk];
       bool ok = true;
       for (int t = 0; t < n; ++t) {
-        const int i = p.csc_rows[start + t];
         const bool full = (p.cflags[start + t] & kFlagFull) != 0;
-        const int b = it & 1;
-        {
-          const int qrow = i * kTile + tid;
-          const bool qv = qrow < p.Tq;
-          const long long gq = static_cast<long long>(bh) * p.Tq + qrow;
-          int qid;
-          if (p.mode == SCFA_MODE_DENSE) qid = qv ? qrow : INT_MIN;
-          else qid = qv ? p.q_idx[gq] : INT_MIN;
-          sm.qidx[b][tid] = qid;
-          sm.qhash[b][tid] = (p.mode == SCFA_MODE_HASH && qv) ? p.q_hash[gq] : 0;
-          sm.lse2[b][tid] = qv ? p.lse[gq] * kLog2e : 0.f;
-          sm.drow[b][tid] = qv ? p.drow[gq] : 0.f;
-        }
-        named_bar_sync(1, 128);
-        ok = mbar_wait(&sm.s_full, it & 1, abort_flag, p.status) &&
-             mbar_wait(&sm.dp_full, it & 1, abort_flag, p.status) &&
-             mbar_wait(&sm.ds_empty, (it & 1) ^ 1, abort_flag, p.status);
+        const int s = q_it & 1;
+        const int db = it & 1;
+        ok = mbar_wait(&sm.q_full[s], (q_it >> 1) & 1, abort_flag, p.status) &&
+             mbar_wait(&sm.s_full, it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-#pragma unroll 1
-        for (int cc = 0; cc < kTile / 32; ++cc) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(lane_base + kColS + cc * 32, sr);
-          tmem_ld32(lane_base + kColDP + cc * 32, dr);
-          tmem_wait_ld();
-          float pv[32], dsv[32];
+        const float* lse2 = sm.lse2[s] + grp * 64;
+        const float* drs = sm.drs[s] + grp * 64;
+        const int* qid = sm.qidx[s] + grp * 64;
+        const int* qhs = sm.qhash[s] + grp * 64;
+        // one 32-query chunk: P^T and dS^T as packed bf16 pairs
+        auto chunk = [&](int c, const uint32_t (&sr)[32], const uint32_t (&dr)[32], uint32_t (&pk)[16],
+                         uint32_t (&dk16)[16]) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int c = cc * 32 + e;
-            bool adm = true;
-            if (!full) {
-              adm = sm.qidx[b][c] >= ki;
-              if (p.mode == SCFA_MODE_HASH) adm = adm && (sm.qhash[b][c] == kh);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const int e = e4 * 4;
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 32 + e);
+            const float4 d4 = *reinterpret_cast<const float4*>(drs + c * 32 + e);
+            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), p.scale_log2, -la[u]));
+              pv[u] = pe;
+              dv[u] = pe * fmaf(__uint_as_float(dr[e + u]), p.scale, -da[u]);
             }
-            const float pe = ex2_approx(__uint_as_float(sr[e]) * p.scale_log2 - sm.lse2[b][c]);
-            pv[e] = adm ? pe : 0.f;
-            dsv[e] = pv[e] * (__uint_as_float(dr[e]) - sm.drow[b][c]) * p.scale;
-          }
-          const int h = cc >> 1;
+            if (!full) {
+              const int4 q4 = *reinterpret_cast<const int4*>(qid + c * 32 + e);
+              const int qa[4] = {q4.x, q4.y, q4.z, q4.w};
+              int ha[4] = {0, 0, 0, 0};
+              if (p.mode == SCFA_MODE_HASH) {
+                const int4 h4 = *reinterpret_cast<const int4*>(qhs + c * 32 + e);
+                ha[0] = h4.x; ha[1] = h4.y; ha[2] = h4.z; ha[3] = h4.w;
+              }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int ch = (cc & 1) * 4 + u;
-            uint4 a, d;
-            a.x = pack_bf16x2(pv[u * 8 + 0], pv[u * 8 + 1]);
-            a.y = pack_bf16x2(pv[u * 8 + 2], pv[u * 8 + 3]);
-            a.z = pack_bf16x2(pv[u * 8 + 4], pv[u * 8 + 5]);
-            a.w = pack_bf16x2(pv[u * 8 + 6], pv[u * 8 + 7]);
-            d.x = pack_bf16x2(dsv[u * 8 + 0], dsv[u * 8 + 1]);
-            d.y = pack_bf16x2(dsv[u * 8 + 2], dsv[u * 8 + 3]);
-            d.z = pack_bf16x2(dsv[u * 8 + 4], dsv[u * 8 + 5]);
-            d.w = pack_bf16x2(dsv[u * 8 + 6], dsv[u * 8 + 7]);
-            *reinterpret_cast<uint4*>(sm.pt[h] + sw128_offset(kr, ch)) = a;
-            *reinterpret_cast<uint4*>(sm.dst[h] + sw128_offset(kr, ch)) = d;
+              for (int u = 0; u < 4; ++u) {
+                const bool adm = qa[u] >= ki && (p.mode != SCFA_MODE_HASH || ha[u] == kh);
+                if (!adm) {
+                  pv[u] = 0.f;
+                  dv[u] = 0.f;
+                }
+              }
+            }
+            pk[e4 * 2] = pack_bf16x2(pv[0], pv[1]);
+            pk[e4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+            dk16[e4 * 2] = pack_bf16x2(dv[0], dv[1]);
+            dk16[e4 * 2 + 1] = pack_bf16x2(dv[2], dv[3]);
           }
+        };
+        uint32_t pk[2][16], dsk[2][16];
+        {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(lane_base + kColS + grp * 64, sr);
+          tmem_ld32(lane_base + kColDP + grp * 64, dr);
+          tmem_wait_ld();
+          chunk(0, sr, dr, pk[0], dsk[0]);
         }
-        tc_fence_before();
-        mbar_arrive(&sm.st_empty);
+        {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(lane_base + kColS + grp * 64 + 32, sr);
+          tmem_ld32(lane_base + kColDP + grp * 64 + 32, dr);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&sm.st_empty);  // S^T / dP^T may now be overwritten by the next A
+          chunk(1, sr, dr, pk[1], dsk[1]);
+        }
+        // the previous dV MMA must have read P^T, the MMAs two tiles back dS^T[db]
+        ok = mbar_wait(&sm.pt_free, (it & 1) ^ 1, abort_flag, p.status) &&
+             mbar_wait(&sm.ds_free[db], ((it >> 1) & 1) ^ 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* dsh = sm.dst[db][grp];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          // P^T (bf16 pairs) -> TMEM columns of this group's queries
+          tmem_st16(lane_base + kColPT + grp * 32 + c * 16, pk[c]);
+          // dS^T -> shared memory, 128-byte swizzle, K-major over queries
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(dsh + sw128_offset(kr, c * 4 + u)) =
+                make_uint4(dsk[c][u * 4], dsk[c][u * 4 + 1], dsk[c][u * 4 + 2], dsk[c][u * 4 + 3]);
+        }
+        tmem_wait_st();
         fence_proxy_async_smem();
+        tc_fence_before();
         mbar_arrive(&sm.ds_full);
         ++it;
+        ++q_it;
       }
       if (!ok) break;
+      // item epilogue: group 0 writes dV, group 1 writes dK
       ok = mbar_wait(&sm.dkv_full, item & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      uint32_t dvr[D / 32][32], dkr[D / 32][32];
+      uint32_t acc[D / 32][32];
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        tmem_ld32(lane_base + kColDV + cc * 32, dvr[cc]);
-        tmem_ld32(lane_base + kColDK + cc * 32, dkr[cc]);
-      }
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_base + (grp == 0 ? kColDV : kColDK) + cc * 32, acc[cc]);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&sm.dkv_empty);
-      if (kvalid) {
-        store_row_bf16(p.dv + gk * D, &dvr[0][0], D);
-        store_row_bf16(p.dk + gk * D, &dkr[0][0], D);
-      }
+      if (kvalid) store_row_bf16((grp == 0 ? p.dv : p.dk) + gk * D, &acc[0][0], D);
       ++item;
     }
   } else {
     // ------------------------------------------------------------ dQ warpgroup
     const int quarter = warp & 3;
     const int qr = quarter * 32 + lane;  // query row = TMEM lane
+    const int tid = threadIdx.x - 320;   // 0..127
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0;
     for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
@@ -375,20 +440,27 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&sm.dq_empty);
-        const int qrow = i * kTile + qr;
-        if (qrow < p.Tq) {
-          float4* dst = reinterpret_cast<float4*>(p.dq_acc + (static_cast<long long>(bh) * p.Tq + qrow) * D);
+        // the previous reduce must have read the staging tile before it is rewritten
+        if (tid == 0) bulk_wait_group_read0();
+        named_bar_sync(2, 128);
 #pragma unroll
-          for (int c = 0; c < D / 4; ++c) {
-            const int e = c * 4;
-            atomicAdd(dst + c, make_float4(__uint_as_float(qv[e >> 5][e & 31]), __uint_as_float(qv[e >> 5][(e + 1) & 31]),
-                                           __uint_as_float(qv[e >> 5][(e + 2) & 31]), __uint_as_float(qv[e >> 5][(e + 3) & 31])));
-          }
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(sm.dqs[h] + sw128_offset(qr, c)) =
+                make_uint4(qv[h][c * 4], qv[h][c * 4 + 1], qv[h][c * 4 + 2], qv[h][c * 4 + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (tid == 0) {
+          tma_reduce_add_3d(&tm_dq, sm.dqs[0], 0, i * kTile, bh);
+          tma_reduce_add_3d(&tm_dq, sm.dqs[1], 32, i * kTile, bh);
+          bulk_commit_group();
         }
         ++it;
       }
       if (!ok) break;
     }
+    if (tid == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
@@ -451,6 +523,7 @@ __global__ void dq_finalize_kernel(const float* __restrict__ dq_acc, long long n
 }  // namespace
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, long long T, long long BH);
+bool make_tmap_f32_3d_w64(CUtensorMap* map, void* base, long long T, long long BH);
 
 cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
   if (a.D != 64) return cudaErrorInvalidValue;
@@ -468,9 +541,10 @@ cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
     if (g < 1) g = 1;
     bwd_pre_kernel<D><<<static_cast<int>(g), 256, 0, st>>>(a.o, a.do_, qrows, drow, dq_acc);
   }
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, BH) || !make_tmap_bf16_3d(&tk, a.k, D, a.Tk, BH) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, BH) || !make_tmap_bf16_3d(&tdo, a.do_, D, a.Tq, BH))
+      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, BH) || !make_tmap_bf16_3d(&tdo, a.do_, D, a.Tq, BH) ||
+      !make_tmap_f32_3d_w64(&tdq, dq_acc, a.Tq, BH))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.mode = a.mode;
@@ -490,7 +564,6 @@ cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
   p.cflags = reinterpret_cast<const uint8_t*>(a.ws + L.cflags);
   p.work = reinterpret_cast<const int32_t*>(a.ws + L.work_bwd);
   p.n_work = static_cast<int>(L.n_ktiles);
-  p.dq_acc = dq_acc;
   p.dk = a.dk;
   p.dv = a.dv;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
@@ -502,7 +575,7 @@ cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
   if (grid > p.n_work) grid = p.n_work;
   if (grid < 1) grid = 1;
   record_kernel_event(1, true, st);
-  attn_bwd_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, p);
+  attn_bwd_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
   record_kernel_event(1, false, st);
   {
     const long long n8 = qrows * D / 8;
