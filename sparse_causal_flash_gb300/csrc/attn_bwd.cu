@@ -41,6 +41,7 @@ namespace scfa {
 namespace {
 
 constexpr int kSubBytes = kTile * 128;
+constexpr int kQStages = 3;  // Q / dO / query-metadata ring depth
 constexpr int kBwdThreads = 448;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -49,16 +50,16 @@ template <int D>
 struct __align__(1024) BwdSmem {
   uint8_t k[D / 64][kSubBytes];
   uint8_t v[D / 64][kSubBytes];
-  uint8_t q[2][D / 64][kSubBytes];
-  uint8_t dO[2][D / 64][kSubBytes];
+  uint8_t q[kQStages][D / 64][kSubBytes];
+  uint8_t dO[kQStages][D / 64][kSubBytes];
   uint8_t dst[2][2][kSubBytes];   // dS^T [buffer][query half][128 keys x 64 queries]
-  uint8_t dqs[2][kSubBytes];      // dQ fp32 staging: [column half][128 rows x 32 floats], swizzled
-  int32_t qidx[2][kTile];
-  int32_t qhash[2][kTile];
-  float lse2[2][kTile];           // LSE * log2(e)
-  float drs[2][kTile];            // rowsum(dO * O) * scale
+  uint8_t dqs[kSubBytes];         // dQ fp32 staging: one [128 rows x 32 floats] swizzled half at a time
+  int32_t qidx[kQStages][kTile];
+  int32_t qhash[kQStages][kTile];
+  float lse2[kQStages][kTile];    // LSE * log2(e)
+  float drs[kQStages][kTile];     // rowsum(dO * O) * scale
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t s_full, st_empty, ds_full, pt_free, ds_free[2], dq_full, dq_empty, dkv_full, dkv_empty, drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -111,11 +112,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (threadIdx.x == 0) {
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kQStages; ++s) {
       mbar_init(&sm.q_full[s], 2);
       mbar_init(&sm.q_empty[s], 1);
-      mbar_init(&sm.ds_free[s], 1);
     }
+    for (int s = 0; s < 2; ++s) mbar_init(&sm.ds_free[s], 1);
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.st_empty, 256);
     mbar_init(&sm.ds_full, 256);
@@ -163,9 +164,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       for (int t = 0; t < n; ++t) {
         const int i = p.csc_rows[start + t];
-        const int s = q_it & 1;
+        const int s = q_it % kQStages;
         if (lane == 0) {
-          ok = mbar_wait(&sm.q_empty[s], ((q_it >> 1) & 1) ^ 1, abort_flag, p.status);
+          ok = mbar_wait(&sm.q_empty[s], ((q_it / kQStages) & 1) ^ 1, abort_flag, p.status);
           if (ok) {
             mbar_arrive_expect_tx(&sm.q_full[s], 2 * D * kTile * 2);
             for (int sub = 0; sub < D / 64; ++sub) {
@@ -175,18 +176,30 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
-        // query metadata of tile i, next to its Q / dO stage
-        for (int c = lane; c < kTile; c += 32) {
-          const int qrow = i * kTile + c;
-          const bool qv = qrow < p.Tq;
-          const long long gq = static_cast<long long>(bh) * p.Tq + qrow;
-          int qid;
-          if (p.mode == SCFA_MODE_DENSE) qid = qv ? qrow : INT_MIN;
-          else qid = qv ? p.q_idx[gq] : INT_MIN;
-          sm.qidx[s][c] = qid;
-          sm.qhash[s][c] = (p.mode == SCFA_MODE_HASH && qv) ? p.q_hash[gq] : 0;
-          sm.lse2[s][c] = qv ? p.lse[gq] * kLog2e : 0.f;
-          sm.drs[s][c] = qv ? p.drow[gq] * p.scale : 0.f;
+        // query metadata of tile i, next to its Q / dO stage: every lane issues
+        // its 16 loads before any store, so the warp pays one memory latency
+        {
+          int qid[4], qhv[4];
+          float lsev[4], drv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = lane + 32 * u;
+            const int qrow = i * kTile + c;
+            const bool qv = qrow < p.Tq;
+            const long long gq = static_cast<long long>(bh) * p.Tq + (qv ? qrow : 0);
+            qid[u] = (p.mode == SCFA_MODE_DENSE) ? (qv ? qrow : INT_MIN) : (qv ? p.q_idx[gq] : INT_MIN);
+            qhv[u] = (p.mode == SCFA_MODE_HASH && qv) ? p.q_hash[gq] : 0;
+            lsev[u] = qv ? p.lse[gq] : 0.f;
+            drv[u] = qv ? p.drow[gq] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = lane + 32 * u;
+            sm.qidx[s][c] = qid[u];
+            sm.qhash[s][c] = qhv[u];
+            sm.lse2[s][c] = lsev[u] * kLog2e;
+            sm.drs[s][c] = drv[u] * p.scale;
+          }
         }
         __threadfence_block();
         __syncwarp();
@@ -197,9 +210,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ++item;
     }
     if (lane == 0) {
-      for (int d = 1; d <= 2 && d <= q_it; ++d) {
+      for (int d = 1; d <= kQStages && d <= q_it; ++d) {
         const int it = q_it - d;
-        mbar_wait(&sm.q_full[it & 1], (it >> 1) & 1, abort_flag, p.status);
+        mbar_wait(&sm.q_full[it % kQStages], (it / kQStages) & 1, abort_flag, p.status);
       }
       if (last_kv >= 0) mbar_wait(&sm.kv_full, last_kv & 1, abort_flag, p.status);
     }
@@ -215,8 +228,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       bool ok = true;
       // A(i): S^T and dP^T of query tile stage s into TMEM
       auto issue_a = [&](int qi, int ii) -> bool {
-        const int s = qi & 1;
-        if (!mbar_wait(&sm.q_full[s], (qi >> 1) & 1, abort_flag, p.status)) return false;
+        const int s = qi % kQStages;
+        if (!mbar_wait(&sm.q_full[s], (qi / kQStages) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(&sm.st_empty, (ii & 1) ^ 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint32_t q_base = smem_u32(sm.q[s][0]);
@@ -243,12 +256,28 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!mbar_wait(&sm.kv_full, item & 1, abort_flag, p.status)) break;
         if (!issue_a(q_it, it)) break;
         for (int t = 0; t < n; ++t) {
-          const int s = q_it & 1;
+          const int s = q_it % kQStages;
           const int db = it & 1;
-          if (t + 1 < n && !issue_a(q_it + 1, it + 1)) { ok = false; break; }
-          if (!mbar_wait(&sm.ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
-          if (t == 0 && !mbar_wait(&sm.dkv_empty, (item & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-          if (!mbar_wait(&sm.dq_empty, (it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          // Issue A(t+1) as soon as its inputs are ready, but never let B(t)
+          // wait behind it: poll both until B(t) can go.
+          bool a_next = (t + 1 >= n);
+          {
+            WaitClock wc;
+            const int s1 = (q_it + 1) % kQStages;
+            for (;;) {
+              if (!a_next && mbar_test(&sm.q_full[s1], ((q_it + 1) / kQStages) & 1) &&
+                  mbar_test(&sm.st_empty, ((it + 1) & 1) ^ 1)) {
+                if (!issue_a(q_it + 1, it + 1)) { ok = false; break; }
+                a_next = true;
+              }
+              if (mbar_test(&sm.ds_full, it & 1) &&
+                  (t > 0 || mbar_test(&sm.dkv_empty, (item & 1) ^ 1)) &&
+                  mbar_test(&sm.dq_empty, (it & 1) ^ 1))
+                break;
+              if (!wc.tick(abort_flag, p.status)) { ok = false; break; }
+            }
+            if (!ok) break;
+          }
           tc_fence_after();
           const uint32_t q_base = smem_u32(sm.q[s][0]);
           const uint32_t do_base = smem_u32(sm.dO[s][0]);
@@ -272,6 +301,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tc_commit(&sm.dq_full);
           tc_commit(&sm.q_empty[s]);
           tc_commit(&sm.ds_free[db]);
+          if (!a_next && !issue_a(q_it + 1, it + 1)) { ok = false; break; }
           ++q_it;
           ++it;
         }
@@ -312,9 +342,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       bool ok = true;
       for (int t = 0; t < n; ++t) {
         const bool full = (p.cflags[start + t] & kFlagFull) != 0;
-        const int s = q_it & 1;
+        const int s = q_it % kQStages;
         const int db = it & 1;
-        ok = mbar_wait(&sm.q_full[s], (q_it >> 1) & 1, abort_flag, p.status) &&
+        ok = mbar_wait(&sm.q_full[s], (q_it / kQStages) & 1, abort_flag, p.status) &&
              mbar_wait(&sm.s_full, it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -440,21 +470,22 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&sm.dq_empty);
-        // the previous reduce must have read the staging tile before it is rewritten
-        if (tid == 0) bulk_wait_group_read0();
-        named_bar_sync(2, 128);
+        // the two 32-column halves go through one 16 KB staging tile; the
+        // previous reduce must have read it before it is rewritten
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h) {
+          if (tid == 0) bulk_wait_group_read0();
+          named_bar_sync(2, 128);
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(sm.dqs[h] + sw128_offset(qr, c)) =
+            *reinterpret_cast<uint4*>(sm.dqs + sw128_offset(qr, c)) =
                 make_uint4(qv[h][c * 4], qv[h][c * 4 + 1], qv[h][c * 4 + 2], qv[h][c * 4 + 3]);
-        fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (tid == 0) {
-          tma_reduce_add_3d(&tm_dq, sm.dqs[0], 0, i * kTile, bh);
-          tma_reduce_add_3d(&tm_dq, sm.dqs[1], 32, i * kTile, bh);
-          bulk_commit_group();
+          fence_proxy_async_smem();
+          named_bar_sync(2, 128);
+          if (tid == 0) {
+            tma_reduce_add_3d(&tm_dq, sm.dqs, h * 32, i * kTile, bh);
+            bulk_commit_group();
+          }
         }
         ++it;
       }

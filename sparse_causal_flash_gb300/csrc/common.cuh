@@ -81,6 +81,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// non-blocking test of phase `parity`
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
 // Wall-clock limit of one pipeline wait. Every stage of every kernel finishes
 // in microseconds, so a wait this long means the pipeline is broken.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
@@ -104,6 +115,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
   }
 }
+
+// Deadline helper for polling loops that test several barriers: returns false
+// (after raising the status word and the abort flag) once the limit passes.
+struct WaitClock {
+  uint64_t t0 = 0;
+  uint32_t it = 0;
+  __device__ __forceinline__ bool tick(volatile int* abort_flag, int* status) {
+    if (((++it) & 63u) != 0) return true;
+    if (*abort_flag) return false;
+    const uint64_t now = global_timer_ns();
+    if (t0 == 0) t0 = now;
+    if (now - t0 > kWaitLimitNs) {
+      raise_status(status, SCFA_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+    return true;
+  }
+};
 
 // ---------------------------------------------------------------------------
 // TMA (tensor copies, global -> shared), completion counted on an mbarrier
