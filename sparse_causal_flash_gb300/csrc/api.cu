@@ -75,6 +75,8 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
   const long long BH = static_cast<long long>(B) * H;
   w.n_qtiles = BH * w.nQt;
   w.n_ktiles = BH * w.nKt;
+  w.nPairs = (w.nQt + 1) / 2;
+  w.n_pairs = BH * w.nPairs;
   w.max_live = w.n_qtiles * w.nKt;
   if (w.max_live >= INT_MAX || w.n_qtiles >= INT_MAX / 2 || w.n_ktiles >= INT_MAX / 2) return false;
   size_t off = 0;
@@ -96,7 +98,9 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
   w.cflags = take(w.max_live);
   w.work_fwd = take(sizeof(int32_t) * w.n_qtiles);
   w.work_bwd = take(sizeof(int32_t) * w.n_ktiles);
-  w.cursor = take(sizeof(int32_t) * (w.nQt + w.nKt + 2));
+  w.cursor = take(sizeof(int32_t) * (w.nQt + 2 * w.nKt + 3));
+  w.pcount = take(sizeof(int32_t) * w.n_pairs);
+  w.work_pairs = take(sizeof(int32_t) * w.n_pairs);
   if (backward) {
     w.dq_acc = take(sizeof(float) * static_cast<size_t>(BH) * Tq * D);
     w.drow = take(sizeof(float) * static_cast<size_t>(BH) * Tq);

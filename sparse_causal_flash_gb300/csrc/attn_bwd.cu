@@ -222,8 +222,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       constexpr uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
       constexpr uint32_t idesc_kv = idesc_bf16_f32(kTile, D, 0, 1);
       constexpr uint32_t idesc_q = idesc_bf16_f32(kTile, D, 1, 1);
-      const uint32_t k_base = smem_u32(sm.k[0]);
-      const uint32_t v_base = smem_u32(sm.v[0]);
+      // descriptors built once; steps, stages and buffers are constant adds
+      constexpr uint32_t kStage16 = (D / 64) * kSubBytes >> 4;
+      const uint64_t kdesc_k = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);           // K, K-major
+      const uint64_t vdesc_k = smem_desc_sw128(smem_u32(sm.v[0]), 16, 1024);           // V, K-major
+      const uint64_t kdesc_mn = smem_desc_sw128(smem_u32(sm.k[0]), kSubBytes, 1024);   // K, MN-major
+      const uint64_t qdesc_k = smem_desc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
+      const uint64_t qdesc_mn = smem_desc_sw128(smem_u32(sm.q[0][0]), kSubBytes, 1024);
+      const uint64_t odesc_k = smem_desc_sw128(smem_u32(sm.dO[0][0]), 16, 1024);
+      const uint64_t odesc_mn = smem_desc_sw128(smem_u32(sm.dO[0][0]), kSubBytes, 1024);
+      const uint64_t sdesc_k = smem_desc_sw128(smem_u32(sm.dst[0][0]), 16, 1024);      // dS^T, K-major
+      const uint64_t sdesc_mn = smem_desc_sw128(smem_u32(sm.dst[0][0]), kSubBytes, 1024);  // dS, MN-major
+      constexpr uint32_t kDsBuf16 = 2 * kSubBytes >> 4;
       int q_it = 0, it = 0, item = 0;
       bool ok = true;
       // A(i): S^T and dP^T of query tile stage s into TMEM
@@ -232,20 +242,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!mbar_wait(&sm.q_full[s], (qi / kQStages) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(&sm.st_empty, (ii & 1) ^ 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t q_base = smem_u32(sm.q[s][0]);
-        const uint32_t do_base = smem_u32(sm.dO[s][0]);
+        const uint64_t qb = qdesc_k + static_cast<uint64_t>(s * kStage16);
+        const uint64_t ob = odesc_k + static_cast<uint64_t>(s * kStage16);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColS, smem_desc_sw128(k_base + off, 16, 1024),
-                      smem_desc_sw128(q_base + off, 16, 1024), idesc_s, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + kColS, kdesc_k + kstep_off16(kk, kSubBytes), qb + kstep_off16(kk, kSubBytes), idesc_s, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + kColDP, smem_desc_sw128(v_base + off, 16, 1024),
-                      smem_desc_sw128(do_base + off, 16, 1024), idesc_s, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + kColDP, vdesc_k + kstep_off16(kk, kSubBytes), ob + kstep_off16(kk, kSubBytes), idesc_s, kk > 0);
         tc_commit(&sm.s_full);
         return true;
       };
@@ -279,25 +283,27 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!ok) break;
           }
           tc_fence_after();
-          const uint32_t q_base = smem_u32(sm.q[s][0]);
-          const uint32_t do_base = smem_u32(sm.dO[s][0]);
-          const uint32_t ds_base = smem_u32(sm.dst[db][0]);
+          const uint64_t qmn = qdesc_mn + static_cast<uint64_t>(s * kStage16);
+          const uint64_t omn = odesc_mn + static_cast<uint64_t>(s * kStage16);
+          const uint64_t dsk = sdesc_k + static_cast<uint64_t>(db * kDsBuf16);
+          const uint64_t dsm = sdesc_mn + static_cast<uint64_t>(db * kDsBuf16);
+          const uint32_t acc0 = t > 0 ? 1u : 0u;
           // dV += P^T dO (A = P^T in TMEM, two bf16 per column along the queries)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8,
-                        smem_desc_sw128(do_base + kk * 2048, kSubBytes, 1024), idesc_kv, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8, omn + static_cast<uint64_t>(kk * 128), idesc_kv,
+                        kk > 0 ? 1u : acc0);
           tc_commit(&sm.pt_free);
           // dK += dS^T Q
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(tmem + kColDK, smem_desc_sw128(ds_base + (kk >> 2) * kSubBytes + (kk & 3) * 32, 16, 1024),
-                        smem_desc_sw128(q_base + kk * 2048, kSubBytes, 1024), idesc_kv, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ss(tmem + kColDK, dsk + kstep_off16(kk, kSubBytes), qmn + static_cast<uint64_t>(kk * 128),
+                        idesc_kv, kk > 0 ? 1u : acc0);
           // dQ_i = dS K (A = dS^T viewed MN-major: queries contiguous, keys along rows)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(tmem + kColDQ, smem_desc_sw128(ds_base + kk * 2048, kSubBytes, 1024),
-                        smem_desc_sw128(k_base + kk * 2048, kSubBytes, 1024), idesc_q, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(tmem + kColDQ, dsm + static_cast<uint64_t>(kk * 128), kdesc_mn + static_cast<uint64_t>(kk * 128),
+                        idesc_q, kk > 0 ? 1u : 0u);
           tc_commit(&sm.dq_full);
           tc_commit(&sm.q_empty[s]);
           tc_commit(&sm.ds_free[db]);

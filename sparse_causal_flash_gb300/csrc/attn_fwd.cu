@@ -8,26 +8,29 @@
 // rescaled accumulator, stored log-sum-exp) is the standard way to keep that
 // maths exact across tiles; the page does not print it.
 //
-// GB300 design: one persistent CTA per SM runs TWO independent pipelines, each
-// walking its own share of the forward work order (query tiles by live count,
-// longest first), so that one pipeline's MMAs keep the tensor core busy while
-// the other pipeline's softmax runs. Per pipeline (6 warps):
-//   producer warp  TMA: the Q tile once per work item, then K_j / V_j of each
-//                  live key tile into a 2-stage ring (128-byte swizzle).
-//   MMA warp       lane 0 issues tcgen05.mma: S = Q K_j^T into TMEM, then
-//                  O += P V_j with P read from TMEM (it overwrites S in place
-//                  as bf16 pairs), then S of the next tile into the same
-//                  columns: the tensor core runs one thread's MMAs in order,
-//                  so the next S cannot overtake the PV that reads P.
-//   softmax WG     thread = query row = TMEM lane: reads S, applies the
-//                  element mask only on tiles not flagged FULL, online softmax
-//                  in the log2 domain with a lazy rescale (O is rescaled only
-//                  when the row max grows by more than 2^8; S_j complete
-//                  implies PV_{j-1} complete, so O is stable then), writes P,
-//                  and at the end normalises O and writes O (bf16) and LSE.
-// TMEM (512 columns): pipeline p uses S at [256 p, 256 p + 128) and O at
-// [256 p + 128, 256 p + 128 + D). Every wait is bounded (1 s); on expiry the
-// CTA raises the workspace status word, leaves its loops and frees TMEM.
+// GB300 design: one persistent CTA per SM walks the pair work order: a work
+// item is a pair of adjacent query tiles (2m, 2m + 1) of one head, and the CTA
+// streams the UNION of their live key-tile lists once, so each K / V tile load
+// serves both query tiles. Roles (320 threads):
+//   warp 0      producer: TMA of Q_2m and Q_2m+1 per item, then K_j / V_j of
+//               each union tile into a 4-stage ring (128-byte swizzle).
+//   warp 1      TMEM owner; lane 0 issues tcgen05.mma in the order
+//               S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ..., where
+//               S_g = Q_g K_j^T lands in TMEM and PV_g reads P_g from TMEM (P
+//               overwrites S_g in place as bf16 pairs). One thread's MMAs run
+//               in order, so S_g(j+1) cannot overtake the PV_g(j) reading P_g.
+//               A tile that is live for only one query tile skips the other's
+//               S and PV.
+//   warps 2-5, 6-9  softmax warpgroup g = 0, 1 (query tile 2m + g); thread =
+//               query row = TMEM lane: element mask only on tiles not flagged
+//               FULL, online softmax in the log2 domain with a lazy rescale
+//               (O_g is rescaled only when the row max grows by more than
+//               2^8; S_g(j) complete implies PV_g(j-1) complete, so O_g is
+//               stable then), P_g written back to TMEM, and the epilogue
+//               (O / l in bf16, LSE in fp32, natural log).
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+// Every wait is bounded (1 s); on expiry the CTA raises the workspace status
+// word, leaves its loops and frees TMEM.
 #include <climits>
 
 #include "common.cuh"
@@ -36,38 +39,31 @@
 namespace scfa {
 namespace {
 
-constexpr int kStages = 2;
-constexpr int kPipes = 2;
+constexpr int kStages = 4;
 constexpr int kSubBytes = kTile * 128;  // one [128 rows][64 bf16] swizzled sub-tile
-constexpr int kWarpsPerPipe = 6;
-constexpr int kFwdThreads = kPipes * kWarpsPerPipe * 32;
+constexpr int kFwdThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
-struct __align__(1024) FwdPipe {
-  uint8_t q[D / 64][kSubBytes];
+struct __align__(1024) FwdSmem {
+  uint8_t q[2][D / 64][kSubBytes];
   uint8_t k[kStages][D / 64][kSubBytes];
   uint8_t v[kStages][D / 64][kSubBytes];
-  int32_t kidx[2][kTile];
-  int32_t khash[2][kTile];
+  int32_t kidx[2][2][kTile];   // [softmax group][buffer][key]
+  int32_t khash[2][2][kTile];
   uint64_t q_full, q_empty;
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t s_full, p_full, o_full, o_empty, drain;
-};
-
-template <int D>
-struct __align__(1024) FwdSmem {
-  FwdPipe<D> pipe[kPipes];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2], drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 struct FwdParams {
   int mode;
-  int Tq, Tk, nQt;
+  int Tq, Tk, nQt, nPairs;
   float scale_log2;
   const int32_t* q_idx;
   const int32_t* k_idx;
@@ -76,11 +72,42 @@ struct FwdParams {
   const int32_t* row_ptr;
   const int32_t* cols;
   const uint8_t* fflags;
-  const int32_t* work;
-  int n_work;
+  const int32_t* work_pairs;
+  const int32_t* pcount;
+  int n_pairs;
   uint16_t* o;
   float* lse;
   int* status;
+};
+
+// Merge walk over the live lists of query tiles 2m and 2m + 1 (ascending).
+struct PairWalk {
+  const int32_t* cols;
+  const uint8_t* ff;
+  int a, ae, b, be;
+  __device__ __forceinline__ void init(const FwdParams& p, long long g0, bool has1) {
+    cols = p.cols;
+    ff = p.fflags;
+    a = p.row_ptr[g0];
+    ae = p.row_ptr[g0 + 1];
+    b = has1 ? p.row_ptr[g0 + 1] : 0;
+    be = has1 ? p.row_ptr[g0 + 2] : 0;
+  }
+  // next union tile: key tile j; bits: 1 live for g=0, 2 FULL for g=0, 4 live for g=1, 8 FULL for g=1
+  __device__ __forceinline__ void next(int& j, int& bits) {
+    const int ja = a < ae ? cols[a] : INT_MAX;
+    const int jb = b < be ? cols[b] : INT_MAX;
+    j = min(ja, jb);
+    bits = 0;
+    if (ja == j) {
+      bits |= 1 | ((ff[a] & kFlagFull) ? 2 : 0);
+      ++a;
+    }
+    if (jb == j) {
+      bits |= 4 | ((ff[b] & kFlagFull) ? 8 : 0);
+      ++b;
+    }
+  }
 };
 
 template <int D>
@@ -91,26 +118,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(smem_raw + pad);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pi = warp / kWarpsPerPipe;      // pipeline of this warp
-  const int role = warp % kWarpsPerPipe;    // 0 producer, 1 MMA, 2-5 softmax
-  FwdPipe<D>& pp = sm.pipe[pi];
 
   if (threadIdx.x == 0) {
-    for (int q = 0; q < kPipes; ++q) {
-      FwdPipe<D>& P = sm.pipe[q];
-      mbar_init(&P.q_full, 1);
-      mbar_init(&P.q_empty, 1);
-      for (int s = 0; s < kStages; ++s) {
-        mbar_init(&P.k_full[s], 1);
-        mbar_init(&P.v_full[s], 1);
-        mbar_init(&P.kv_empty[s], 1);
-      }
-      mbar_init(&P.s_full, 1);
-      mbar_init(&P.p_full, 128);
-      mbar_init(&P.o_full, 1);
-      mbar_init(&P.o_empty, 128);
-      mbar_init(&P.drain, 1);
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
     }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&sm.s_full[g], 1);
+      mbar_init(&sm.p_full[g], 128);
+      mbar_init(&sm.o_full[g], 1);
+      mbar_init(&sm.o_empty[g], 128);
+    }
+    mbar_init(&sm.drain, 1);
     sm.abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -122,35 +145,39 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t colS = 256u * pi, colO = 256u * pi + 128u;
   volatile int* abort_flag = &sm.abort_flag;
-  // this pipeline's share of the work order
-  const int first = blockIdx.x * kPipes + pi;
-  const int stride = gridDim.x * kPipes;
 
-  if (role == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int kv_it = 0, item = 0, last_q = -1;
-      for (int w = first; w < p.n_work; w += stride) {
-        const int g = p.work[w];
-        const int start = p.row_ptr[g], n = p.row_ptr[g + 1] - start;
-        if (n == 0) continue;
-        const int bh = g / p.nQt, i = g % p.nQt;
-        if (!mbar_wait(&pp.q_empty, (item & 1) ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&pp.q_full, D * kTile * 2);
-        for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(pp.q[sub], &tm_q, &pp.q_full, sub * 64, i * kTile, bh);
+      for (int w = blockIdx.x; w < p.n_pairs; w += gridDim.x) {
+        const int pid = p.work_pairs[w];
+        const int cnt = p.pcount[pid];
+        if (cnt == 0) continue;
+        const int bh = pid / p.nPairs, m = pid % p.nPairs;
+        const bool has1 = 2 * m + 1 < p.nQt;
+        const long long g0 = static_cast<long long>(bh) * p.nQt + 2 * m;
+        if (!mbar_wait(&sm.q_empty, (item & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&sm.q_full, (has1 ? 2 : 1) * D * kTile * 2);
+        for (int sub = 0; sub < D / 64; ++sub) {
+          tma_load_3d(sm.q[0][sub], &tm_q, &sm.q_full, sub * 64, 2 * m * kTile, bh);
+          if (has1) tma_load_3d(sm.q[1][sub], &tm_q, &sm.q_full, sub * 64, (2 * m + 1) * kTile, bh);
+        }
         last_q = item;
+        PairWalk wk;
+        wk.init(p, g0, has1);
         bool ok = true;
-        for (int t = 0; t < n; ++t) {
-          const int j = p.cols[start + t];
+        for (int t = 0; t < cnt; ++t) {
+          int j, bits;
+          wk.next(j, bits);
           const int s = kv_it % kStages;
           const uint32_t ph = (kv_it / kStages) & 1;
-          if (!mbar_wait(&pp.kv_empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&pp.k_full[s], D * kTile * 2);
-          for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(pp.k[s][sub], &tm_k, &pp.k_full[s], sub * 64, j * kTile, bh);
-          mbar_arrive_expect_tx(&pp.v_full[s], D * kTile * 2);
-          for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(pp.v[s][sub], &tm_v, &pp.v_full[s], sub * 64, j * kTile, bh);
+          if (!mbar_wait(&sm.kv_empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.k_full[s], D * kTile * 2);
+          for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(sm.k[s][sub], &tm_k, &sm.k_full[s], sub * 64, j * kTile, bh);
+          mbar_arrive_expect_tx(&sm.v_full[s], D * kTile * 2);
+          for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(sm.v[s][sub], &tm_v, &sm.v_full[s], sub * 64, j * kTile, bh);
           ++kv_it;
         }
         if (!ok) break;
@@ -161,97 +188,132 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int it = kv_it - d;
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        mbar_wait(&pp.k_full[s], ph, abort_flag, p.status);
-        mbar_wait(&pp.v_full[s], ph, abort_flag, p.status);
+        mbar_wait(&sm.k_full[s], ph, abort_flag, p.status);
+        mbar_wait(&sm.v_full[s], ph, abort_flag, p.status);
       }
-      if (last_q >= 0) mbar_wait(&pp.q_full, last_q & 1, abort_flag, p.status);
+      if (last_q >= 0) mbar_wait(&sm.q_full, last_q & 1, abort_flag, p.status);
     }
-  } else if (role == 1) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kTile, D, 0, 1);
-      const uint32_t q_base = smem_u32(pp.q[0]);
-      int kv_it = 0, p_it = 0, item = 0;
+      int kv_it = 0, item = 0;
+      int p_it[2] = {0, 0}, o_it[2] = {0, 0};
       bool ok = true;
-      auto issue_s = [&](int kvi) -> bool {
+      // descriptors built once; steps and stages are constant adds
+      constexpr uint32_t kStage16 = (D / 64) * kSubBytes >> 4;
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
+      const uint64_t kdesc = smem_desc_sw128(smem_u32(sm.k[0][0]), 16, 1024);
+      const uint64_t vdesc = smem_desc_sw128(smem_u32(sm.v[0][0]), kSubBytes, 1024);
+      auto issue_s = [&](int g, int kvi) -> bool {
         const int s = kvi % kStages;
-        if (!mbar_wait(&pp.k_full[s], (kvi / kStages) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&sm.k_full[s], (kvi / kStages) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t k_base = smem_u32(pp.k[s][0]);
+        const uint64_t a = qdesc + static_cast<uint64_t>(g * kStage16);
+        const uint64_t b = kdesc + static_cast<uint64_t>(s * kStage16);
+        const uint32_t d = tmem + 128u * g;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + colS, smem_desc_sw128(q_base + off, 16, 1024),
-                      smem_desc_sw128(k_base + off, 16, 1024), idesc_s, kk > 0);
-        }
-        tc_commit(&pp.s_full);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(d, a + kstep_off16(kk, kSubBytes), b + kstep_off16(kk, kSubBytes), idesc_s, kk > 0);
+        tc_commit(&sm.s_full[g]);
         return true;
       };
-      for (int w = first; w < p.n_work && ok; w += stride) {
-        const int g = p.work[w];
-        const int n = p.row_ptr[g + 1] - p.row_ptr[g];
-        if (n == 0) continue;
-        if (!mbar_wait(&pp.q_full, item & 1, abort_flag, p.status)) break;
-        if (!issue_s(kv_it)) break;
-        for (int t = 0; t < n; ++t) {
+      for (int w = blockIdx.x; w < p.n_pairs && ok; w += gridDim.x) {
+        const int pid = p.work_pairs[w];
+        const int cnt = p.pcount[pid];
+        if (cnt == 0) continue;
+        const int bh = pid / p.nPairs, m = pid % p.nPairs;
+        const bool has1 = 2 * m + 1 < p.nQt;
+        const long long g0 = static_cast<long long>(bh) * p.nQt + 2 * m;
+        PairWalk wk;
+        wk.init(p, g0, has1);
+        int j_cur, bits_cur, j_nxt = 0, bits_nxt = 0;
+        wk.next(j_cur, bits_cur);
+        if (!mbar_wait(&sm.q_full, item & 1, abort_flag, p.status)) break;
+        if ((bits_cur & 1) && !issue_s(0, kv_it)) break;
+        if ((bits_cur & 4) && !issue_s(1, kv_it)) break;
+        bool pv_first[2] = {true, true};
+        for (int t = 0; t < cnt && ok; ++t) {
+          const bool more = t + 1 < cnt;
+          if (more) wk.next(j_nxt, bits_nxt);
           const int s = kv_it % kStages;
-          if (!mbar_wait(&pp.p_full, p_it & 1, abort_flag, p.status)) { ok = false; break; }
-          if (t == 0 && !mbar_wait(&pp.o_empty, (item & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-          if (!mbar_wait(&pp.v_full[s], (kv_it / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t v_base = smem_u32(pp.v[s][0]);
+          for (int g = 0; g < 2; ++g) {
+            const int live = g == 0 ? (bits_cur & 1) : (bits_cur & 4);
+            if (live) {
+              if (!mbar_wait(&sm.p_full[g], p_it[g] & 1, abort_flag, p.status)) { ok = false; break; }
+              if (pv_first[g] && !mbar_wait(&sm.o_empty[g], (o_it[g] & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+              if (!mbar_wait(&sm.v_full[s], (kv_it / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t vb = vdesc + static_cast<uint64_t>(s * kStage16);
+              const uint32_t dO_ = tmem + 256u + D * g, aP = tmem + 128u * g;
+              const uint32_t acc0 = pv_first[g] ? 0u : 1u;
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ts(tmem + colO, tmem + colS + kk * 8, smem_desc_sw128(v_base + kk * 2048, kSubBytes, 1024),
-                        idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&pp.kv_empty[s]);
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_bf16_ts(dO_, aP + kk * 8, vb + static_cast<uint64_t>(kk * 128), idesc_o, kk > 0 ? 1u : acc0);
+              pv_first[g] = false;
+              ++p_it[g];
+            }
+            if (g == 1) tc_commit(&sm.kv_empty[s]);
+            const int live_n = g == 0 ? (bits_nxt & 1) : (bits_nxt & 4);
+            if (more && live_n && !issue_s(g, kv_it + 1)) { ok = false; break; }
+          }
+          if (!ok) break;
           ++kv_it;
-          ++p_it;
-          if (t + 1 < n && !issue_s(kv_it)) { ok = false; break; }
+          j_cur = j_nxt;
+          bits_cur = bits_nxt;
         }
         if (!ok) break;
-        tc_commit(&pp.o_full);
-        tc_commit(&pp.q_empty);
+        for (int g = 0; g < 2; ++g) {
+          if (!pv_first[g]) {
+            tc_commit(&sm.o_full[g]);
+            ++o_it[g];
+          }
+        }
+        tc_commit(&sm.q_empty);
         ++item;
       }
       // drain: all MMAs issued by this thread are complete before TMEM is freed
-      tc_commit(&pp.drain);
-      mbar_wait(&pp.drain, 0, abort_flag, p.status);
+      tc_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0, abort_flag, p.status);
     }
   } else {
-    // ------------------------------------------------------------ softmax warpgroup
+    // ------------------------------------------------------------ softmax warpgroups
+    const int grp = (warp - 2) >> 2;            // query tile 2m + grp
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;          // row of the tile = TMEM lane
-    const int tid = (role - 2) * 32 + lane;     // 0..127 for cooperative staging
-    const int bar_id = 1 + pi;
+    const int tid = (warp - 2 - 4 * grp) * 32 + lane;  // 0..127 for cooperative staging
+    const int bar_id = 1 + grp;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    int s_it = 0, item = 0;
-    for (int w = first; w < p.n_work; w += stride) {
-      const int g = p.work[w];
-      const int start = p.row_ptr[g], n = p.row_ptr[g + 1] - start;
-      const int bh = g / p.nQt, i = g % p.nQt;
+    const uint32_t colS = 128u * grp, colO = 256u + D * grp;
+    const int live_bit = grp == 0 ? 1 : 4, full_bit = grp == 0 ? 2 : 8;
+    int s_it = 0, o_it = 0;
+    for (int w = blockIdx.x; w < p.n_pairs; w += gridDim.x) {
+      const int pid = p.work_pairs[w];
+      const int cnt = p.pcount[pid];
+      const int bh = pid / p.nPairs, m = pid % p.nPairs;
+      const int i = 2 * m + grp;
+      const bool has1 = 2 * m + 1 < p.nQt;
+      const long long g0 = static_cast<long long>(bh) * p.nQt + 2 * m;
       const int row = i * kTile + r;
-      const bool valid = row < p.Tq;
+      const bool valid = i < p.nQt && row < p.Tq;
       const long long grow = static_cast<long long>(bh) * p.Tq + row;
-      int qi, qh = 0;
-      if (p.mode == SCFA_MODE_DENSE) qi = valid ? row : INT_MIN;
-      else qi = valid ? p.q_idx[grow] : INT_MIN;
-      if (p.mode == SCFA_MODE_HASH && valid) qh = p.q_hash[grow];
-      if (n == 0) {
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
-#pragma unroll
-          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-          p.lse[grow] = -INFINITY;
-        }
-        continue;
+      int qi = INT_MIN, qh = 0;
+      if (valid) {
+        qi = (p.mode == SCFA_MODE_DENSE) ? row : p.q_idx[grow];
+        if (p.mode == SCFA_MODE_HASH) qh = p.q_hash[grow];
       }
+      PairWalk wk;
+      wk.init(p, g0, has1);
       float m_used = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int t = 0; t < n; ++t) {
-        const int j = p.cols[start + t];
-        const bool full = (p.fflags[start + t] & kFlagFull) != 0;
+      bool ok = true, any = false;
+      for (int t = 0; t < cnt; ++t) {
+        int j, bits;
+        wk.next(j, bits);
+        if (!(bits & live_bit)) continue;
+        const bool first_tile = !any;
+        any = true;
+        const bool full = (bits & full_bit) != 0;
         const int b = s_it & 1;
         if (!full) {
           const int col = j * kTile + tid;
@@ -260,42 +322,44 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           int kid;
           if (p.mode == SCFA_MODE_DENSE) kid = kv ? col : INT_MAX;
           else kid = kv ? p.k_idx[gk] : INT_MAX;
-          pp.kidx[b][tid] = kid;
-          if (p.mode == SCFA_MODE_HASH) pp.khash[b][tid] = kv ? p.k_hash[gk] : INT_MIN;
+          sm.kidx[grp][b][tid] = kid;
+          if (p.mode == SCFA_MODE_HASH) sm.khash[grp][b][tid] = kv ? p.k_hash[gk] : INT_MIN;
           named_bar_sync(bar_id, 128);
         }
-        ok = mbar_wait(&pp.s_full, s_it & 1, abort_flag, p.status);
+        ok = mbar_wait(&sm.s_full[grp], s_it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        float sv[kTile];
+        // raw scores of this row: four 32-column loads, one wait
+        uint32_t sr[kTile];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t sr[32];
-          tmem_ld32(lane_base + colS + cc * 32, sr);
-          tmem_wait_ld();
+        for (int cc = 0; cc < 4; ++cc)
+          tmem_ld32(lane_base + colS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+        tmem_wait_ld();
+        if (!full) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) sv[cc * 32 + c] = __uint_as_float(sr[c]) * p.scale_log2;
-          if (!full) {
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              const int4 k4 = *reinterpret_cast<const int4*>(&pp.kidx[b][cc * 32 + c4 * 4]);
-              bool adm[4] = {qi >= k4.x, qi >= k4.y, qi >= k4.z, qi >= k4.w};
-              if (p.mode == SCFA_MODE_HASH) {
-                const int4 h4 = *reinterpret_cast<const int4*>(&pp.khash[b][cc * 32 + c4 * 4]);
-                adm[0] = adm[0] && qh == h4.x;
-                adm[1] = adm[1] && qh == h4.y;
-                adm[2] = adm[2] && qh == h4.z;
-                adm[3] = adm[3] && qh == h4.w;
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                if (!adm[u]) sv[cc * 32 + c4 * 4 + u] = -INFINITY;
+          for (int c4 = 0; c4 < kTile / 4; ++c4) {
+            const int4 k4 = *reinterpret_cast<const int4*>(&sm.kidx[grp][b][c4 * 4]);
+            bool adm[4] = {qi >= k4.x, qi >= k4.y, qi >= k4.z, qi >= k4.w};
+            if (p.mode == SCFA_MODE_HASH) {
+              const int4 h4 = *reinterpret_cast<const int4*>(&sm.khash[grp][b][c4 * 4]);
+              adm[0] = adm[0] && qh == h4.x;
+              adm[1] = adm[1] && qh == h4.y;
+              adm[2] = adm[2] && qh == h4.z;
+              adm[3] = adm[3] && qh == h4.w;
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (!adm[u]) sr[c4 * 4 + u] = 0xff800000u;  // -inf
           }
         }
-        float mt = sv[0];
+        // row max: eight independent chains, then a tree
+        float mx[8];
 #pragma unroll
-        for (int c = 1; c < kTile; ++c) mt = fmaxf(mt, sv[c]);
+        for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(sr[u]);
+#pragma unroll
+        for (int c = 8; c < kTile; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
         const float m_new = fmaxf(m_used, mt);
         const bool resc = m_new > m_used + kRescaleThreshold;
         float alpha = 1.f;
@@ -304,23 +368,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           m_used = m_new;
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        float rs = 0.f;
-        // P (bf16 pairs) over the first 64 columns of S, one 64-key half at a time
+        float rsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // P = 2^(s * scale * log2(e) - m) as bf16 pairs over the first 64 columns of S_g
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float e0 = ex2_approx(sv[h * 64 + c] - msub);
-            const float e1 = ex2_approx(sv[h * 64 + c + 1] - msub);
-            rs += e0 + e1;
+          for (int c = 0; c < 32; c += 2) {
+            const float e0 = ex2_approx(fmaf(__uint_as_float(sr[h * 32 + c]), p.scale_log2, -msub));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(sr[h * 32 + c + 1]), p.scale_log2, -msub));
+            rsum[(c >> 1) & 7] += e0 + e1;
             pk[c >> 1] = pack_bf16x2(e0, e1);
           }
-          tmem_st32(lane_base + colS + h * 32, pk);
+          tmem_st16(lane_base + colS + h * 16, pk);
         }
+        const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
         l = l * alpha + rs;
-        // rescale O (rare). S_t complete => PV_{t-1} complete (in-order tensor pipe): O is stable
-        if (t > 0 && __any_sync(0xffffffffu, resc)) {
+        // rescale O (rare). S_g(t) complete => PV_g(t-1) complete: O_g is stable
+        if (!first_tile && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t orr[32];
@@ -333,12 +398,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&pp.p_full);
+        mbar_arrive(&sm.p_full[grp]);
         ++s_it;
       }
       if (!ok) break;
+      if (!any) {
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          p.lse[grow] = -INFINITY;
+        }
+        continue;
+      }
       // epilogue: O / l, LSE
-      ok = mbar_wait(&pp.o_full, item & 1, abort_flag, p.status);
+      ok = mbar_wait(&sm.o_full[grp], o_it & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       uint32_t orr[D / 32][32];
@@ -346,7 +420,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_base + colO + cc * 32, orr[cc]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&pp.o_empty);
+      mbar_arrive(&sm.o_empty[grp]);
+      ++o_it;
       if (valid) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
@@ -362,7 +437,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         p.lse[grow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       }
-      ++item;
     }
   }
 
@@ -398,8 +472,10 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st) {
   p.row_ptr = reinterpret_cast<const int32_t*>(a.ws + L.row_ptr);
   p.cols = reinterpret_cast<const int32_t*>(a.ws + L.cols);
   p.fflags = reinterpret_cast<const uint8_t*>(a.ws + L.fflags);
-  p.work = reinterpret_cast<const int32_t*>(a.ws + L.work_fwd);
-  p.n_work = static_cast<int>(L.n_qtiles);
+  p.nPairs = L.nPairs;
+  p.work_pairs = reinterpret_cast<const int32_t*>(a.ws + L.work_pairs);
+  p.pcount = reinterpret_cast<const int32_t*>(a.ws + L.pcount);
+  p.n_pairs = static_cast<int>(L.n_pairs);
   p.o = a.o_out;
   p.lse = a.lse_out;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
@@ -408,7 +484,7 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st) {
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int grid = num_sms();
-  if (grid > (p.n_work + kPipes - 1) / kPipes) grid = (p.n_work + kPipes - 1) / kPipes;
+  if (grid > p.n_pairs) grid = p.n_pairs;
   if (grid < 1) grid = 1;
   record_kernel_event(0, true, st);
   attn_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, p);

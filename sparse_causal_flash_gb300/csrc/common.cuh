@@ -226,6 +226,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Byte offset of 16-element K step kk inside a K-major tile made of
+// [128 rows][64 bf16] swizzled sub-tiles, in descriptor units (16 bytes):
+// added to a descriptor it moves the start address (bits 0-13) only, since
+// every shared-memory address is below 256 KB.
+__host__ __device__ constexpr uint64_t kstep_off16(int kk, int sub_bytes) {
+  return static_cast<uint64_t>(((kk >> 2) * sub_bytes + (kk & 3) * 32) >> 4);
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: operand is MN-major (1) instead of K-major (0).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {

@@ -25,6 +25,12 @@ struct AttnWs {
   size_t fflags = 0, cflags = 0;
   size_t work_fwd = 0, work_bwd = 0;
   size_t cursor = 0;                     // scratch of the work-order sort
+  // forward scheduling unit: a pair of adjacent query tiles (2m, 2m + 1) of
+  // one head that share K / V loads over the union of their live lists
+  int nPairs = 0;                        // per head
+  long long n_pairs = 0;                 // over all heads
+  size_t pcount = 0;                     // union size per pair
+  size_t work_pairs = 0;                 // pair ids by union size descending
   size_t dq_acc = 0;                     // backward: fp32 dQ accumulator [B,H,Tq,D]
   size_t drow = 0;                       // backward: fp32 rowsum(dO * O) [B,H,Tq]
   size_t total = 0;

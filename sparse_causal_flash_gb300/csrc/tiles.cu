@@ -206,21 +206,53 @@ __global__ void tile_fill_kernel(TileCtx c, long long n_q, long long n_k,
   }
 }
 
-// Stable counting sort of tile ids by live count, descending. Block 0 builds
-// the forward order, block 1 the backward order. The whole block histograms;
-// warp 0 scans and scatters in id order (stable by construction).
-__global__ void work_order_kernel(const int32_t* __restrict__ qcount, long long n_q, int max_q,
-                                  int32_t* __restrict__ work_fwd,
-                                  const int32_t* __restrict__ kcount, long long n_k, int max_k,
-                                  int32_t* __restrict__ work_bwd,
-                                  int32_t* __restrict__ gcursor, int smem_bins) {
+// Live-list union size of each query-tile pair (2m, 2m + 1): a merge count of
+// the two ascending CSR rows.
+__global__ void pair_count_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cols,
+                                  int nQt, int nPairs, long long n_pairs, int32_t* __restrict__ pcount) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long pid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; pid < n_pairs; pid += stride) {
+    const long long bh = pid / nPairs;
+    const int m = static_cast<int>(pid % nPairs);
+    const long long g0 = bh * nQt + 2 * m;
+    int a = row_ptr[g0], ae = row_ptr[g0 + 1];
+    int b = 0, be = 0;
+    if (2 * m + 1 < nQt) {
+      b = row_ptr[g0 + 1];
+      be = row_ptr[g0 + 2];
+    }
+    int cnt = 0;
+    while (a < ae || b < be) {
+      const int ja = a < ae ? cols[a] : INT_MAX;
+      const int jb = b < be ? cols[b] : INT_MAX;
+      if (ja <= jb) ++a;
+      if (jb <= ja) ++b;
+      ++cnt;
+    }
+    pcount[pid] = cnt;
+  }
+}
+
+struct OrderList {
+  const int32_t* count;
+  long long n;
+  int maxc;
+  int32_t* out;
+  int32_t* gcur;
+};
+
+// Stable counting sort of ids by count, descending: block 0 builds the
+// forward order (query tiles), block 1 the backward order (key tiles), block
+// 2 the order of query-tile pairs. The whole block histograms; warp 0 scans
+// and scatters in id order (stable by construction).
+__global__ void work_order_kernel(OrderList l0, OrderList l1, OrderList l2, int smem_bins) {
   extern __shared__ int32_t scur[];
-  const bool fwd = blockIdx.x == 0;
-  const int32_t* cnt = fwd ? qcount : kcount;
-  const long long n = fwd ? n_q : n_k;
-  const int maxc = fwd ? max_q : max_k;
-  int32_t* out = fwd ? work_fwd : work_bwd;
-  int32_t* cur = (maxc + 1 <= smem_bins) ? scur : gcursor + (fwd ? 0 : (max_q + 1));
+  const OrderList L = blockIdx.x == 0 ? l0 : (blockIdx.x == 1 ? l1 : l2);
+  const int32_t* cnt = L.count;
+  const long long n = L.n;
+  const int maxc = L.maxc;
+  int32_t* out = L.out;
+  int32_t* cur = (maxc + 1 <= smem_bins) ? scur : L.gcur;
   for (int cc = threadIdx.x; cc <= maxc; cc += blockDim.x) cur[cc] = 0;
   __syncthreads();
   for (long long i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&cur[min(max(cnt[i], 0), maxc)], 1);
@@ -271,7 +303,6 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
                          int B, int H, int Tq, int Tk, unsigned flags,
                          char* ws, const AttnWs& L, cudaStream_t st) {
   const int sms = num_sms();
-  const long long BH = static_cast<long long>(B) * H;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
   int4* qstat = reinterpret_cast<int4*>(ws + L.qstat);
   int4* kstat = reinterpret_cast<int4*>(ws + L.kstat);
@@ -294,14 +325,18 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
       c, L.n_qtiles, L.n_ktiles, row_ptr, reinterpret_cast<int32_t*>(ws + L.cols),
       reinterpret_cast<uint8_t*>(ws + L.fflags), csc_ptr, reinterpret_cast<int32_t*>(ws + L.csc_rows),
       reinterpret_cast<uint8_t*>(ws + L.cflags));
+  pair_count_kernel<<<grid_for(L.n_pairs, 128, sms * 16), 128, 0, st>>>(
+      row_ptr, reinterpret_cast<const int32_t*>(ws + L.cols), L.nQt, L.nPairs, L.n_pairs,
+      reinterpret_cast<int32_t*>(ws + L.pcount));
   const int smem_bins = 12 * 1024;  // 48 KB of shared memory; larger histograms use the workspace
   const int maxc = (L.nKt > L.nQt ? L.nKt : L.nQt) + 1;
   const size_t smem = static_cast<size_t>(maxc <= smem_bins ? maxc : 0) * sizeof(int32_t);
-  work_order_kernel<<<2, 1024, smem, st>>>(qcount, L.n_qtiles, L.nKt,
-                                           reinterpret_cast<int32_t*>(ws + L.work_fwd),
-                                           kcount, L.n_ktiles, L.nQt,
-                                           reinterpret_cast<int32_t*>(ws + L.work_bwd),
-                                           reinterpret_cast<int32_t*>(ws + L.cursor), smem_bins);
+  int32_t* gcur = reinterpret_cast<int32_t*>(ws + L.cursor);
+  OrderList lf{qcount, L.n_qtiles, L.nKt, reinterpret_cast<int32_t*>(ws + L.work_fwd), gcur};
+  OrderList lb{kcount, L.n_ktiles, L.nQt, reinterpret_cast<int32_t*>(ws + L.work_bwd), gcur + L.nKt + 1};
+  OrderList lp{reinterpret_cast<const int32_t*>(ws + L.pcount), L.n_pairs, L.nKt,
+               reinterpret_cast<int32_t*>(ws + L.work_pairs), gcur + L.nKt + L.nQt + 2};
+  work_order_kernel<<<3, 1024, smem, st>>>(lf, lb, lp, smem_bins);
   return cudaGetLastError();
 }
 
