@@ -94,7 +94,7 @@ size_t scfa_attn_workspace_size(int mode, int backward, int B, int H, int Tq, in
 /* ----------------------------------------------------------------------------
  * Dense causal attention (comparator; page section "FlashAttention 的兴起":
  * a token sees only earlier tokens). q, k, v, o, do_, dq, dk, dv: [B,H,T,D]
- * bf16; lse: [B,H,T] fp32. D = 64.
+ * bf16; lse: [B,H,T] fp32. D = 64 or 128.
  * ------------------------------------------------------------------------- */
 scfa_status scfa_dense_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                            int B, int H, int T, int D, float scale,
@@ -112,7 +112,7 @@ scfa_status scfa_dense_bwd(const uint16_t* q, const uint16_t* k, const uint16_t*
  * k_idx [B,H,Tk] int32 original positions, ascending within each (b,h) over
  * the kept rows. Heads keep different counts, so rows past a head's count are
  * padding with sentinels: q_idx = -1 for padded queries, k_idx = INT32_MAX
- * for padded keys (never admissible). Outputs are in compacted order. D = 64.
+ * for padded keys (never admissible). Outputs are in compacted order. D = 64 or 128.
  * ------------------------------------------------------------------------- */
 scfa_status scfa_qk_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         const int32_t* q_idx, const int32_t* k_idx,
@@ -133,7 +133,7 @@ scfa_status scfa_qk_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * k_s, v_s, dk_s, dv_s the key order. q_idx / k_idx [B,H,T] are the original
  * positions of the sorted rows (the perm of lsh_bucket_sort) and q_hash /
  * k_hash [B,H,T] their bucket ids, non-decreasing within each (b,h).
- * Put results back in original order with lsh_unsort. D = 64.
+ * Put results back in original order with lsh_unsort. D = 64 or 128.
  * ------------------------------------------------------------------------- */
 scfa_status scfa_hash_fwd(const uint16_t* q_s, const uint16_t* k_s, const uint16_t* v_s,
                           const int32_t* q_idx, const int32_t* k_idx,

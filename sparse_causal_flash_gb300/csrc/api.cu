@@ -51,13 +51,13 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, long long T, l
   return r == CUDA_SUCCESS;
 }
 
-// 3-D map over a [BH][T][64] fp32 tensor; box = 32 columns x 128 rows x 1
+// 3-D map over a [BH][T][D] fp32 tensor; box = 32 columns x 128 rows x 1
 // head, 128-byte swizzle (used by TMA reduce-add; rows past T are skipped).
-bool make_tmap_f32_3d_w64(CUtensorMap* map, void* base, long long T, long long BH) {
+bool make_tmap_f32_3d(CUtensorMap* map, void* base, int D, long long T, long long BH) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {64 * 4, static_cast<cuuint64_t>(T) * 64 * 4};
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(T) * D * 4};
   cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kTile), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
@@ -159,7 +159,7 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   if (!q || !k || !v || !ws) return SCFA_ERR_INVALID;
   if (B < 1 || H < 1 || Tq < 1 || Tk < 1) return SCFA_ERR_INVALID;
   if (!(scale == scale) || scale <= 0.f) return SCFA_ERR_INVALID;
-  if (D != 64) return SCFA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return SCFA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return SCFA_ERR_INVALID;
   if (mode != SCFA_MODE_DENSE && (!q_idx || !k_idx)) return SCFA_ERR_INVALID;
   if (mode == SCFA_MODE_HASH && (!q_hash || !k_hash)) return SCFA_ERR_INVALID;

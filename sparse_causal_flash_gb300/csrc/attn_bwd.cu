@@ -41,13 +41,17 @@ namespace scfa {
 namespace {
 
 constexpr int kSubBytes = kTile * 128;
-constexpr int kQStages = 3;  // Q / dO / query-metadata ring depth
+// Q / dO / query-metadata ring depth: 3 at D = 64; 1 at D = 128, where the
+// 64 KB Q + dO stage leaves no room for a second one
+template <int D>
+constexpr int bwd_qstages() { return D == 64 ? 3 : 1; }
 constexpr int kBwdThreads = 448;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct __align__(1024) BwdSmem {
+  static constexpr int kQStages = bwd_qstages<D>();
   uint8_t k[D / 64][kSubBytes];
   uint8_t v[D / 64][kSubBytes];
   uint8_t q[kQStages][D / 64][kSubBytes];
@@ -102,10 +106,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
-  static_assert(D == 64, "the backward TMEM plan holds D = 64");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw + pad);
+  constexpr int kQStages = BwdSmem<D>::kQStages;
+  constexpr int kHalves = D / 64;  // a work item = (key tile, 64-column half of D)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384, kColPT = 448;
 
@@ -145,7 +150,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ------------------------------------------------------------ producer warp
     int q_it = 0, item = 0, last_kv = -1;
     for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
-      const int g = p.work[w];
+      const int g = p.work[w / kHalves];  // both halves load all of K, V, Q, dO
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
       if (n == 0) continue;
       const int bh = g / p.nKt, j = g % p.nKt;
@@ -220,8 +225,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
-      constexpr uint32_t idesc_kv = idesc_bf16_f32(kTile, D, 0, 1);
-      constexpr uint32_t idesc_q = idesc_bf16_f32(kTile, D, 1, 1);
+      constexpr uint32_t idesc_kv = idesc_bf16_f32(kTile, 64, 0, 1);  // dV, dK: one 64-column half of D
+      constexpr uint32_t idesc_q = idesc_bf16_f32(kTile, 64, 1, 1);   // dQ: one 64-column half of D
       // descriptors built once; steps, stages and buffers are constant adds
       constexpr uint32_t kStage16 = (D / 64) * kSubBytes >> 4;
       const uint64_t kdesc_k = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);           // K, K-major
@@ -254,7 +259,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         return true;
       };
       for (int w = blockIdx.x; w < p.n_work && ok; w += gridDim.x) {
-        const int g = p.work[w];
+        const int g = p.work[w / kHalves];
+        const int hh = w % kHalves;
         const int n = p.csc_ptr[g + 1] - p.csc_ptr[g];
         if (n == 0) continue;
         if (!mbar_wait(&sm.kv_full, item & 1, abort_flag, p.status)) break;
@@ -283,8 +289,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!ok) break;
           }
           tc_fence_after();
-          const uint64_t qmn = qdesc_mn + static_cast<uint64_t>(s * kStage16);
-          const uint64_t omn = odesc_mn + static_cast<uint64_t>(s * kStage16);
+          const uint64_t half16 = static_cast<uint64_t>(hh * (kSubBytes >> 4));
+          const uint64_t qmn = qdesc_mn + static_cast<uint64_t>(s * kStage16) + half16;
+          const uint64_t omn = odesc_mn + static_cast<uint64_t>(s * kStage16) + half16;
+          const uint64_t kmn = kdesc_mn + half16;
           const uint64_t dsk = sdesc_k + static_cast<uint64_t>(db * kDsBuf16);
           const uint64_t dsm = sdesc_mn + static_cast<uint64_t>(db * kDsBuf16);
           const uint32_t acc0 = t > 0 ? 1u : 0u;
@@ -302,7 +310,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           // dQ_i = dS K (A = dS^T viewed MN-major: queries contiguous, keys along rows)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(tmem + kColDQ, dsm + static_cast<uint64_t>(kk * 128), kdesc_mn + static_cast<uint64_t>(kk * 128),
+            mma_bf16_ss(tmem + kColDQ, dsm + static_cast<uint64_t>(kk * 128), kmn + static_cast<uint64_t>(kk * 128),
                         idesc_q, kk > 0 ? 1u : 0u);
           tc_commit(&sm.dq_full);
           tc_commit(&sm.q_empty[s]);
@@ -327,7 +335,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0, q_it = 0, item = 0;
     for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
-      const int g = p.work[w];
+      const int g = p.work[w / kHalves];
+      const int hh = w % kHalves;  // which 64-column half of D
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
       const int bh = g / p.nKt, j = g % p.nKt;
       const int key = j * kTile + kr;
@@ -335,9 +344,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const long long gk = static_cast<long long>(bh) * p.Tk + key;
       if (n == 0) {
         if (kvalid) {
-          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + gk * D);
+          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + gk * D + 64 * hh);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) a[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 8; ++c) a[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -443,13 +452,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ok = mbar_wait(&sm.dkv_full, item & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      uint32_t acc[D / 32][32];
+      uint32_t acc[2][32];
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_base + (grp == 0 ? kColDV : kColDK) + cc * 32, acc[cc]);
+      for (int cc = 0; cc < 2; ++cc) tmem_ld32(lane_base + (grp == 0 ? kColDV : kColDK) + cc * 32, acc[cc]);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&sm.dkv_empty);
-      if (kvalid) store_row_bf16((grp == 0 ? p.dv : p.dk) + gk * D, &acc[0][0], D);
+      if (kvalid) store_row_bf16((grp == 0 ? p.dv : p.dk) + gk * D + 64 * hh, &acc[0][0], 64);
       ++item;
     }
   } else {
@@ -460,7 +469,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0;
     for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
-      const int g = p.work[w];
+      const int g = p.work[w / kHalves];
+      const int hh = w % kHalves;  // which 64-column half of D
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
       if (n == 0) continue;
       const int bh = g / p.nKt;
@@ -470,9 +480,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ok = mbar_wait(&sm.dq_full, it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        uint32_t qv[D / 32][32];
+        uint32_t qv[2][32];
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_base + kColDQ + cc * 32, qv[cc]);
+        for (int cc = 0; cc < 2; ++cc) tmem_ld32(lane_base + kColDQ + cc * 32, qv[cc]);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&sm.dq_empty);
@@ -489,7 +499,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           fence_proxy_async_smem();
           named_bar_sync(2, 128);
           if (tid == 0) {
-            tma_reduce_add_3d(&tm_dq, sm.dqs, h * 32, i * kTile, bh);
+            tma_reduce_add_3d(&tm_dq, sm.dqs, 64 * hh + h * 32, i * kTile, bh);
             bulk_commit_group();
           }
         }
@@ -560,11 +570,10 @@ __global__ void dq_finalize_kernel(const float* __restrict__ dq_acc, long long n
 }  // namespace
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, long long T, long long BH);
-bool make_tmap_f32_3d_w64(CUtensorMap* map, void* base, long long T, long long BH);
+bool make_tmap_f32_3d(CUtensorMap* map, void* base, int D, long long T, long long BH);
 
-cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
-  if (a.D != 64) return cudaErrorInvalidValue;
-  constexpr int D = 64;
+template <int D>
+static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   const AttnWs& L = *a.L;
   const long long BH = static_cast<long long>(a.B) * a.H;
   const int sms = num_sms();
@@ -581,7 +590,7 @@ cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, BH) || !make_tmap_bf16_3d(&tk, a.k, D, a.Tk, BH) ||
       !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, BH) || !make_tmap_bf16_3d(&tdo, a.do_, D, a.Tq, BH) ||
-      !make_tmap_f32_3d_w64(&tdq, dq_acc, a.Tq, BH))
+      !make_tmap_f32_3d(&tdq, dq_acc, D, a.Tq, BH))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.mode = a.mode;
@@ -600,7 +609,7 @@ cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
   p.csc_rows = reinterpret_cast<const int32_t*>(a.ws + L.csc_rows);
   p.cflags = reinterpret_cast<const uint8_t*>(a.ws + L.cflags);
   p.work = reinterpret_cast<const int32_t*>(a.ws + L.work_bwd);
-  p.n_work = static_cast<int>(L.n_ktiles);
+  p.n_work = static_cast<int>(L.n_ktiles) * (D / 64);
   p.dk = a.dk;
   p.dv = a.dv;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
@@ -622,6 +631,12 @@ cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
     dq_finalize_kernel<<<static_cast<int>(g), 256, 0, st>>>(dq_acc, n8, a.dq);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(const AttnArgs& a, cudaStream_t st) {
+  if (a.D == 64) return launch_bwd_d<64>(a, st);
+  if (a.D == 128) return launch_bwd_d<128>(a, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace scfa

@@ -39,7 +39,9 @@
 namespace scfa {
 namespace {
 
-constexpr int kStages = 4;
+// K / V ring depth: 4 stages of 32 KB at D = 64, 2 stages of 64 KB at D = 128
+template <int D>
+constexpr int fwd_stages() { return D == 64 ? 4 : 2; }
 constexpr int kSubBytes = kTile * 128;  // one [128 rows][64 bf16] swizzled sub-tile
 constexpr int kFwdThreads = 320;
 constexpr uint32_t kTmemCols = 512;
@@ -49,6 +51,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct __align__(1024) FwdSmem {
+  static constexpr int kStages = fwd_stages<D>();
   uint8_t q[2][D / 64][kSubBytes];
   uint8_t k[kStages][D / 64][kSubBytes];
   uint8_t v[kStages][D / 64][kSubBytes];
@@ -117,6 +120,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(smem_raw + pad);
+  constexpr int kStages = FwdSmem<D>::kStages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -450,9 +454,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, long long T, long long BH);
 
-cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st) {
-  if (a.D != 64) return cudaErrorInvalidValue;
-  constexpr int D = 64;
+template <int D>
+static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   const AttnWs& L = *a.L;
   const long long BH = static_cast<long long>(a.B) * a.H;
   CUtensorMap tq, tk, tv;
@@ -490,6 +493,12 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st) {
   attn_fwd_kernel<D><<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, p);
   record_kernel_event(0, false, st);
   return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st) {
+  if (a.D == 64) return launch_fwd_d<64>(a, st);
+  if (a.D == 128) return launch_fwd_d<128>(a, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace scfa

@@ -176,26 +176,28 @@ def compare_heads(st, ref, heads, lse_perm=None):
         check_close(f"dV[{b},{h}]", st.dv[b, h], r["dv"])
 
 
-@pytest.mark.parametrize("B,H,T,keep,seed", [(2, 3, 1000, 0.7, 11), (1, 2, 2000, 0.3, 12), (1, 2, 300, 0.9, 13)])
-def test_qk_parity(scfa, B, H, T, keep, seed):
-    p = synth.make_problem(synth.Workload("qk", "qk", B, H, T, 64, seed, p_keep=keep))
+@pytest.mark.parametrize("B,H,T,D,keep,seed", [(2, 3, 1000, 64, 0.7, 11), (1, 2, 2000, 64, 0.3, 12),
+                                               (1, 2, 300, 64, 0.9, 13), (1, 3, 1100, 128, 0.6, 14)])
+def test_qk_parity(scfa, B, H, T, D, keep, seed):
+    p = synth.make_problem(synth.Workload("qk", "qk", B, H, T, D, seed, p_keep=keep))
     st = run_step(scfa, p, scfa.MODE_QK)
     ref = pipelines.run_qk(p.q, p.k, p.v, p.do, p.q_idx.numpy(), p.k_idx.numpy(), p.wl.scale)
     compare_heads(st, ref, ref.keys())
 
 
-@pytest.mark.parametrize("B,H,T,nb,seed", [(1, 2, 512, 4, 1001), (1, 2, 1000, 8, 21), (2, 1, 1500, 2, 22)])
-def test_hash_parity(scfa, B, H, T, nb, seed):
-    p = synth.make_problem(synth.Workload("h", "hash", B, H, T, 64, seed, n_buckets=nb))
+@pytest.mark.parametrize("B,H,T,D,nb,seed", [(1, 2, 512, 64, 4, 1001), (1, 2, 1000, 64, 8, 21),
+                                             (2, 1, 1500, 64, 2, 22), (1, 2, 1300, 128, 8, 23)])
+def test_hash_parity(scfa, B, H, T, D, nb, seed):
+    p = synth.make_problem(synth.Workload("h", "hash", B, H, T, D, seed, n_buckets=nb))
     st = run_step(scfa, p, scfa.MODE_HASH)
     ref, qh, kh = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, p.wl.scale)
     pq, _, _ = pipelines.hash_sort_view(qh, nb)
     compare_heads(st, ref, ref.keys(), lse_perm=pq)
 
 
-@pytest.mark.parametrize("B,H,T", [(1, 2, 700), (2, 1, 128), (1, 1, 1)])
-def test_dense_parity(scfa, B, H, T):
-    p = synth.make_problem(synth.Workload("d", "dense", B, H, T, 64, 31))
+@pytest.mark.parametrize("B,H,T,D", [(1, 2, 700, 64), (2, 1, 128, 64), (1, 1, 1, 64), (1, 2, 900, 128)])
+def test_dense_parity(scfa, B, H, T, D):
+    p = synth.make_problem(synth.Workload("d", "dense", B, H, T, D, 31))
     st = run_step(scfa, p, scfa.MODE_DENSE)
     ref = pipelines.run_dense(p.q, p.k, p.v, p.do, p.wl.scale)
     compare_heads(st, ref, ref.keys())
