@@ -67,22 +67,25 @@ def lsh_hash(x, R, exact_all: bool = False) -> np.ndarray:
         for n in range(X.shape[0]):
             out[n] = _exact_bucket(X[n], R)
         return out.reshape(shape)
-    s = X @ R
-    A = np.abs(X) @ np.abs(R)
     gamma = D * _U64 / (1.0 - D * _U64)
-    err = gamma * A * (1.0 + 1e-10)
-    v = np.concatenate([s, -s], axis=1)
-    e = np.concatenate([err, err], axis=1)
-    top = np.argmax(v, axis=1)
-    rows = np.arange(X.shape[0])
-    margin = v[rows, top][:, None] - v
-    need = 2.0 * (e[rows, top][:, None] + e)
-    ok = (margin > need)
-    ok[rows, top] = True
-    certified = ok.all(axis=1)
-    out[:] = top
-    for n in np.nonzero(~certified)[0]:
-        out[n] = _exact_bucket(X[n], R)
+    absR = np.abs(R)
+    for r0 in range(0, X.shape[0], 65536):  # row blocks only bound memory
+        Xb = X[r0:r0 + 65536]
+        s = Xb @ R
+        A = np.abs(Xb) @ absR
+        err = gamma * A * (1.0 + 1e-10)
+        v = np.concatenate([s, -s], axis=1)
+        e = np.concatenate([err, err], axis=1)
+        top = np.argmax(v, axis=1)
+        rows = np.arange(Xb.shape[0])
+        margin = v[rows, top][:, None] - v
+        need = 2.0 * (e[rows, top][:, None] + e)
+        ok = (margin > need)
+        ok[rows, top] = True
+        certified = ok.all(axis=1)
+        out[r0:r0 + Xb.shape[0]] = top
+        for n in np.nonzero(~certified)[0]:
+            out[r0 + n] = _exact_bucket(Xb[n], R)
     return out.reshape(shape)
 
 

@@ -104,3 +104,26 @@ def run_hash(q, k, v, do, R, scale, heads=None, backward=True, q_hash=None, k_ha
 def useful_flops(pairs: int, D: int, backward: bool = True) -> float:
     """4 D flops per admissible pair forward, 10 D backward (S recomputed)."""
     return float(pairs) * D * (14.0 if backward else 4.0)
+
+
+def run_hash_buckets(q, k, v, do, scale, q_hash, k_hash, buckets):
+    """Hash-sparse attention of ONE head, evaluated bucket by bucket.
+
+    q, k, v, do: [T, D]; q_hash, k_hash: [T] bucket ids in original order.
+    The hash mask (same bucket AND causal) never pairs tokens of different
+    buckets, so restricting the explicit-mask problem to the queries and keys
+    of one bucket c gives exactly the rows of those queries (O, LSE, dQ) and
+    keys (dK, dV) in the whole problem. This is how sequences too long for a
+    T x T mask are checked. Returns {c: dict(q_pos, k_pos, o, lse, dq, dk, dv)}.
+    """
+    q_hash = np.asarray(q_hash)
+    k_hash = np.asarray(k_hash)
+    out = {}
+    for c in buckets:
+        qp = np.nonzero(q_hash == c)[0]
+        kp = np.nonzero(k_hash == c)[0]
+        mask = attention.mask_hash(q_hash[qp], k_hash[kp], q_pos=qp, k_pos=kp)
+        O, lse, dq, dk, dv = attention.backward(_f64(q)[qp], _f64(k)[kp], _f64(v)[kp], _f64(do)[qp], mask, scale)
+        out[int(c)] = dict(q_pos=qp, k_pos=kp, o=O, lse=lse, dq=dq, dk=dk, dv=dv,
+                           pairs=attention.admissible_pairs(mask))
+    return out

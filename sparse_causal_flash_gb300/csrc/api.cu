@@ -299,7 +299,8 @@ scfa_status lsh_hash(const uint16_t* x, const uint16_t* R, int B, int H, int T, 
   scfa_status s = check_lsh_args(x, R, B, H, T, D, n_buckets);
   if (s != SCFA_OK) return s;
   if (!hash) return SCFA_ERR_INVALID;
-  if (static_cast<size_t>(D) * (n_buckets / 2) * sizeof(float) > 200 * 1024) return SCFA_ERR_UNSUPPORTED;
+  if ((static_cast<size_t>(D) * ((n_buckets / 2 + 3) & ~3) + 256u * (D / 2 + 1)) * sizeof(float) > 200 * 1024)
+    return SCFA_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(B) * H * T;
   return finish(launch_lsh_hash(x, R, rows, D, n_buckets / 2, hash, static_cast<cudaStream_t>(stream)), 0, nullptr);
 }
@@ -311,7 +312,8 @@ scfa_status lsh_bucket_sort(const uint16_t* x, const uint16_t* R, int B, int H, 
   if (s != SCFA_OK) return s;
   if (!hash_sorted || !perm || !bucket_off || !ws) return SCFA_ERR_INVALID;
   if (x_sorted && !aligned16(x_sorted)) return SCFA_ERR_INVALID;
-  if (static_cast<size_t>(D) * (n_buckets / 2) * sizeof(float) > 200 * 1024) return SCFA_ERR_UNSUPPORTED;
+  if ((static_cast<size_t>(D) * ((n_buckets / 2 + 3) & ~3) + 256u * (D / 2 + 1)) * sizeof(float) > 200 * 1024)
+    return SCFA_ERR_UNSUPPORTED;
   LshWs L;
   if (!lsh_ws_layout(B, H, T, n_buckets, &L)) return SCFA_ERR_INVALID;
   if (!aligned256(ws) || ws_bytes < L.total) return SCFA_ERR_WORKSPACE;

@@ -109,75 +109,197 @@ __device__ void fix_dot(const uint16_t* __restrict__ x, const uint16_t* __restri
   }
 }
 
-// Exact argmax over [x R, -x R] with the smallest index on ties.
-__device__ int exact_bucket(const uint16_t* __restrict__ x, const uint16_t* __restrict__ R, int D, int m) {
-  Fix576 best, cur;
-  int best_j = 0;
-  fix_dot(x, R, D, m, 0, best);
-  for (int j = 1; j < 2 * m; ++j) {
-    fix_dot(x, R, D, m, j % m, cur);
-    if (j >= m) fix_negate(cur);
-    if (fix_greater(cur, best)) {
-      best = cur;
-      best_j = j;
-    }
-  }
-  return best_j;
-}
-
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// One thread per row; R staged in shared memory as fp32 [D][m].
-__global__ void lsh_hash_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ R,
-                                long long rows, int D, int m, int32_t* __restrict__ hash) {
-  extern __shared__ float sR[];
-  for (int i = threadIdx.x; i < D * m; i += blockDim.x) sR[i] = bf16_to_f32(R[i]);
+// One thread per row. A block stages its rows in shared memory as bf16 pairs
+// with a padded stride (thread t reads row t without bank conflicts) and R as
+// fp32 [D][m4] (m4 = m rounded up to 4, zero columns appended), so one 16-byte
+// load of R feeds four columns. A compiler memory barrier at each column group
+// keeps the row loads inside the loop instead of hoisting the whole row into
+// registers.
+//
+// Certification, three levels, all exact in outcome:
+//  1. fp32: every candidate's fp32 value is within
+//     gamma_D * sum_d |x_d R_dc| <= gamma_D * ||x||_2 * max_c ||R_c||_2
+//     (Cauchy-Schwarz; both norms rounded up, plus subnormal slack) of its
+//     exact value; emax doubles that. If the top beats the runner-up by more
+//     than thr = 2 emax, the top is the exact argmax.
+//  2. Otherwise only candidates within thr of the top can win; the pass keeps
+//     the four best candidates, and if the fourth is also within thr (so more
+//     might be) it falls through to a full scan. The few candidates are
+//     re-evaluated in fp64 (bf16 x bf16 products are exact in fp64, the sum
+//     is off by at most D 2^-53 sum |x_d R_dc|, doubled here): a strict winner
+//     beyond both bounds is the exact argmax.
+//  3. Otherwise those candidates (or, after a full scan, every candidate
+//     within thr) get exact 576-bit fixed-point sums, compared in index order
+//     with a strict comparison, which keeps the smallest index among ties.
+constexpr int kHashRows = 256;
+
+__global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __restrict__ x,
+                                                             const uint16_t* __restrict__ R, long long rows,
+                                                             int D, int m, int32_t* __restrict__ hash) {
+  const int m4 = (m + 3) & ~3;
+  const int xs = D / 2 + 1;  // padded row stride of the staged rows, in 32-bit words
+  extern __shared__ float smem[];
+  float* sR = smem;                                                  // [D][m4]
+  uint32_t* sX = reinterpret_cast<uint32_t*>(smem + D * m4);         // [kHashRows][xs]
+  for (int i = threadIdx.x; i < D * m4; i += blockDim.x) {
+    const int d = i / m4, c = i % m4;
+    sR[i] = c < m ? bf16_to_f32(R[d * m + c]) : 0.f;
+  }
+  // largest column norm ||R_c||_2, evaluated in fp64 and rounded up
+  __shared__ float s_rn;
+  if (threadIdx.x == 0) s_rn = 0.f;
   __syncthreads();
+  {
+    float mx = 0.f;
+    for (int c = threadIdx.x; c < m; c += blockDim.x) {
+      double ss = 0.0;
+      for (int d = 0; d < D; ++d) ss = fma(static_cast<double>(sR[d * m4 + c]), static_cast<double>(sR[d * m4 + c]), ss);
+      mx = fmaxf(mx, static_cast<float>(sqrt(ss * (1.0 + 1e-12))) * 1.000001f);
+    }
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int*>(&s_rn), __float_as_int(mx));
+  }
+  __syncthreads();
+  const float rnmax = s_rn;
+  const float4* sR4 = reinterpret_cast<const float4*>(sR);
   // fp32 rounding bound of one dot product, doubled: 2 * gamma_D with gamma_D < (D+1) 2^-24
   const float rel = static_cast<float>(D + 1) * 0x1p-23f;
   const float absb = static_cast<float>(D) * 0x1p-148f;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; r < rows; r += stride) {
-    const uint16_t* xr = x + r * D;
-    float xv[256];
-    for (int d8 = 0; d8 < D; d8 += 8) {
-      const uint4 u = *reinterpret_cast<const uint4*>(xr + d8);
-      const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        xv[d8 + 2 * t] = __uint_as_float(ws[t] << 16);
-        xv[d8 + 2 * t + 1] = __uint_as_float(ws[t] & 0xFFFF0000u);
+  const int wpr = D / 2;  // 32-bit words per row
+  for (long long r0 = static_cast<long long>(blockIdx.x) * kHashRows; r0 < rows;
+       r0 += static_cast<long long>(gridDim.x) * kHashRows) {
+    const int nr = static_cast<int>(rows - r0 < kHashRows ? rows - r0 : kHashRows);
+    __syncthreads();
+    const uint32_t* gx = reinterpret_cast<const uint32_t*>(x + r0 * D);
+    for (int i = threadIdx.x; i < nr * wpr; i += blockDim.x) sX[(i / wpr) * xs + (i % wpr)] = gx[i];
+    __syncthreads();
+    if (threadIdx.x >= nr) continue;
+    const long long r = r0 + threadIdx.x;
+    const uint32_t* xrow = sX + threadIdx.x * xs;
+    auto xval = [&](int d) -> float {
+      const uint32_t w = xrow[d >> 1];
+      return __uint_as_float((d & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    };
+    // ||x||_2 rounded up: squares of bf16 are exact unless subnormal
+    // (covered by D 2^-148), the fp32 sum by the (D+2) 2^-22 factor
+    float l2sq = 0.f;
+    for (int d = 0; d < D; ++d) l2sq = fmaf(xval(d), xval(d), l2sq);
+    const float l2 = sqrtf(l2sq * (1.f + static_cast<float>(D + 2) * 0x1p-22f) + static_cast<float>(D) * 0x1p-148f) *
+                     1.000001f;
+    const float emax = l2 * rnmax * rel * 1.000001f + absb;
+    // the four best candidates (values t, candidate indices j)
+    float t0 = -INFINITY, t1 = -INFINITY, t2 = -INFINITY, t3 = -INFINITY;
+    int j0 = 0, j1 = 0, j2 = 0, j3 = 0;  // j3 is only needed to keep the list ordered
+    for (int c0 = 0; c0 < m4; c0 += 4) {
+      asm volatile("" ::: "memory");
+      float sv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+      for (int d2 = 0; d2 < D; d2 += 2) {
+        const uint32_t w = xrow[d2 >> 1];
+        const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+        const float4 ra = sR4[(d2 * m4 + c0) >> 2];
+        const float4 rb = sR4[((d2 + 1) * m4 + c0) >> 2];
+        sv[0] = fmaf(x1, rb.x, fmaf(x0, ra.x, sv[0]));
+        sv[1] = fmaf(x1, rb.y, fmaf(x0, ra.y, sv[1]));
+        sv[2] = fmaf(x1, rb.z, fmaf(x0, ra.z, sv[2]));
+        sv[3] = fmaf(x1, rb.w, fmaf(x0, ra.w, sv[3]));
       }
-    }
-    float top = -INFINITY, second = -INFINITY, emax = 0.f;
-    int top_j = 0;
-    for (int c = 0; c < m; ++c) {
-      float s = 0.f, a = 0.f;
-      for (int d = 0; d < D; ++d) {
-        const float rv = sR[d * m + c];
-        s = fmaf(xv[d], rv, s);
-        a = fmaf(fabsf(xv[d]), fabsf(rv), a);
-      }
-      emax = fmaxf(emax, a * rel + absb);
-      // candidate c (+s) and candidate m + c (-s)
-      const float cand[2] = {s, -s};
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const float v = cand[t];
-        if (v > top) {
-          second = top;
-          top = v;
-          top_j = c + t * m;
-        } else if (v > second) {
-          second = v;
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u;
+        if (c >= m) break;
+        // candidate c (+s) and candidate m + c (-s)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const float v = t ? -sv[u] : sv[u];
+          const int j = c + t * m;
+          if (v > t3) {
+            if (v > t2) {
+              t3 = t2; j3 = j2;
+              if (v > t1) {
+                t2 = t1; j2 = j1;
+                if (v > t0) { t1 = t0; j1 = j0; t0 = v; j0 = j; } else { t1 = v; j1 = j; }
+              } else { t2 = v; j2 = j; }
+            } else { t3 = v; j3 = j; }
+          }
         }
       }
     }
-    // certified when the lead beats twice the largest per-candidate bound
-    int h = top_j;
-    if (!(top - second > 2.f * emax * 1.0001f)) h = exact_bucket(xr, R, D, m);
+    (void)j3;
+    int h = j0;
+    const float thr = 2.f * emax * 1.0001f;
+    if (!(t0 - t1 > thr)) {
+      const uint16_t* xr = x + r * D;
+      const bool few = (t0 - t3 > thr);  // every candidate within thr of the top is among the four
+      bool done = false;
+      int cj[3];
+      int nc = 0;
+      if (few) {
+        // candidates within thr, in index order
+        cj[nc++] = j0;
+        if (t0 - t1 <= thr) cj[nc++] = j1;
+        if (t0 - t2 <= thr) cj[nc++] = j2;
+        for (int a = 1; a < nc; ++a)
+          for (int b2 = a; b2 > 0 && cj[b2 - 1] > cj[b2]; --b2) {
+            const int tmp = cj[b2]; cj[b2] = cj[b2 - 1]; cj[b2 - 1] = tmp;
+          }
+        // level 2: fp64 values and bounds
+        double val[3], err[3];
+        for (int k = 0; k < nc; ++k) {
+          const int c = cj[k] % m;
+          double sacc = 0.0, aacc = 0.0;
+          for (int d = 0; d < D; ++d) {
+            const double xd = static_cast<double>(xval(d)), rd = static_cast<double>(sR[d * m4 + c]);
+            sacc = fma(xd, rd, sacc);
+            aacc = fma(fabs(xd), fabs(rd), aacc);
+          }
+          val[k] = cj[k] < m ? sacc : -sacc;
+          err[k] = aacc * static_cast<double>(D) * 0x1p-52 + 0x1p-1000;
+        }
+        int bi = 0;
+        for (int k = 1; k < nc; ++k)
+          if (val[k] > val[bi]) bi = k;
+        bool cert = true;
+        for (int k = 0; k < nc; ++k)
+          if (k != bi && !(val[bi] - val[k] > err[bi] + err[k])) cert = false;
+        if (cert) {
+          h = cj[bi];
+          done = true;
+        }
+      }
+      if (!done) {
+        // level 3: exact sums of the candidates that may beat the top, in index order
+        Fix576 best, cur;
+        int best_j = -1;
+        for (int pass = 0; pass < 2; ++pass) {
+          for (int c = 0; c < m; ++c) {
+            const int j = c + pass * m;
+            bool cand;
+            if (few) {
+              cand = false;
+              for (int k = 0; k < nc; ++k) cand = cand || (cj[k] == j);
+            } else {
+              float sc = 0.f;
+              for (int d = 0; d < D; ++d) sc = fmaf(xval(d), sR[d * m4 + c], sc);
+              const float vj = pass == 0 ? sc : -sc;
+              cand = (t0 - vj <= thr) || (vj != vj);
+            }
+            if (!cand) continue;
+            fix_dot(xr, R, D, m, c, cur);
+            if (pass == 1) fix_negate(cur);
+            if (best_j < 0 || fix_greater(cur, best)) {
+              best = cur;
+              best_j = j;
+            }
+          }
+        }
+        h = best_j >= 0 ? best_j : j0;
+      }
+    }
     hash[r] = h;
   }
 }
@@ -282,16 +404,16 @@ __global__ void row_move_kernel(const uint4* __restrict__ x, const int32_t* __re
 
 cudaError_t launch_lsh_hash(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
                             int32_t* hash, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(D) * m * sizeof(float);
+  const size_t smem = (static_cast<size_t>(D) * ((m + 3) & ~3) + static_cast<size_t>(kHashRows) * (D / 2 + 1)) *
+                      sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(lsh_hash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int block = 128;
-  long long g = (rows + block - 1) / block;
-  const long long cap = static_cast<long long>(num_sms()) * 16;
+  long long g = (rows + kHashRows - 1) / kHashRows;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
   if (g > cap) g = cap;
   if (g < 1) g = 1;
-  lsh_hash_kernel<<<static_cast<int>(g), block, smem, st>>>(x, R, rows, D, m, hash);
+  lsh_hash_kernel<<<static_cast<int>(g), kHashRows, smem, st>>>(x, R, rows, D, m, hash);
   return cudaGetLastError();
 }
 

@@ -210,3 +210,24 @@ def test_hash_mask_sorted_view_is_a_permutation():
     np.testing.assert_allclose(dk[pk], dks, atol=1e-12)
     np.testing.assert_allclose(dv[pk], dvs, atol=1e-12)
     np.testing.assert_array_equal(np.isneginf(lse[pq]), np.isneginf(lses))
+
+
+def test_bucketwise_hash_equals_whole_problem():
+    # the block-diagonal structure of the hash mask: per-bucket subproblems
+    # reproduce every row of the full explicit-mask problem
+    rng = np.random.default_rng(13)
+    T, D, nb = 90, 8, 5
+    q, k, v, do = (rng.standard_normal((T, D)) for _ in range(4))
+    qh, kh = rng.integers(0, nb, T), rng.integers(0, nb, T)
+    O, lse, dq, dk, dv = attention.backward(q, k, v, do, attention.mask_hash(qh, kh), 0.4)
+    per = pipelines.run_hash_buckets(q, k, v, do, 0.4, qh, kh, range(nb))
+    seen_q, seen_k = [], []
+    for c, r in per.items():
+        np.testing.assert_allclose(r["o"], O[r["q_pos"]], atol=1e-12)
+        np.testing.assert_allclose(r["dq"], dq[r["q_pos"]], atol=1e-12)
+        np.testing.assert_allclose(r["dk"], dk[r["k_pos"]], atol=1e-12)
+        np.testing.assert_allclose(r["dv"], dv[r["k_pos"]], atol=1e-12)
+        np.testing.assert_array_equal(np.isneginf(r["lse"]), np.isneginf(lse[r["q_pos"]]))
+        seen_q += list(r["q_pos"])
+        seen_k += list(r["k_pos"])
+    assert sorted(seen_q) == list(range(T)) and sorted(seen_k) == list(range(T))
