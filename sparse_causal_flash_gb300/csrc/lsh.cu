@@ -128,13 +128,12 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
 //     than thr = 2 emax, the top is the exact argmax.
 //  2. Otherwise only candidates within thr of the top can win; the pass keeps
 //     the four best candidates, and if the fourth is also within thr (so more
-//     might be) it falls through to a full scan. The few candidates are
-//     re-evaluated in fp64 (bf16 x bf16 products are exact in fp64, the sum
-//     is off by at most D 2^-53 sum |x_d R_dc|, doubled here): a strict winner
-//     beyond both bounds is the exact argmax.
-//  3. Otherwise those candidates (or, after a full scan, every candidate
-//     within thr) get exact 576-bit fixed-point sums, compared in index order
-//     with a strict comparison, which keeps the smallest index among ties.
+//     might be) every column is screened again. Each remaining candidate gets
+//     its EXACT value: with every product written as an integer times 2^e,
+//     the sum is an exact 128-bit integer once the row's exponent span (of x
+//     times that of R) is at most 100 bits, else an exact 576-bit one.
+//     Candidates are compared in index order with a strict comparison, which
+//     keeps the smallest index among exact ties.
 constexpr int kHashRows = 256;
 
 __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __restrict__ x,
@@ -149,22 +148,51 @@ __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __r
     const int d = i / m4, c = i % m4;
     sR[i] = c < m ? bf16_to_f32(R[d * m + c]) : 0.f;
   }
-  // largest column norm ||R_c||_2, evaluated in fp64 and rounded up
+  // largest column norm ||R_c||_2 rounded up (squares of bf16 are exact in
+  // fp32 unless subnormal: D 2^-148 slack; the sum: (D+2) 2^-22 relative),
+  // and the range of the exponents E of the nonzero entries of R (value =
+  // M 2^E with an integer M < 256)
   __shared__ float s_rn;
-  if (threadIdx.x == 0) s_rn = 0.f;
+  __shared__ int s_remin, s_remax;
+  if (threadIdx.x == 0) {
+    s_rn = 0.f;
+    s_remin = INT_MAX;
+    s_remax = INT_MIN;
+  }
   __syncthreads();
   {
     float mx = 0.f;
     for (int c = threadIdx.x; c < m; c += blockDim.x) {
-      double ss = 0.0;
-      for (int d = 0; d < D; ++d) ss = fma(static_cast<double>(sR[d * m4 + c]), static_cast<double>(sR[d * m4 + c]), ss);
-      mx = fmaxf(mx, static_cast<float>(sqrt(ss * (1.0 + 1e-12))) * 1.000001f);
+      float ss = 0.f;
+      for (int d = 0; d < D; ++d) ss = fmaf(sR[d * m4 + c], sR[d * m4 + c], ss);
+      mx = fmaxf(mx, sqrtf(ss * (1.f + static_cast<float>(D + 2) * 0x1p-22f) + static_cast<float>(D) * 0x1p-148f) *
+                         1.000001f);
     }
-    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<int*>(&s_rn), __float_as_int(mx));
+    int emn = INT_MAX, emx = INT_MIN;
+    for (int i = threadIdx.x; i < D * m4; i += blockDim.x) {
+      bool ng;
+      uint32_t M;
+      int E;
+      bf16_parts(static_cast<uint16_t>(__float_as_uint(sR[i]) >> 16), &ng, &M, &E);
+      if (M != 0) {
+        emn = min(emn, E);
+        emx = max(emx, E);
+      }
+    }
+    for (int o = 16; o; o >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      emn = min(emn, __shfl_xor_sync(0xffffffffu, emn, o));
+      emx = max(emx, __shfl_xor_sync(0xffffffffu, emx, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+      atomicMax(reinterpret_cast<int*>(&s_rn), __float_as_int(mx));
+      atomicMin(&s_remin, emn);
+      atomicMax(&s_remax, emx);
+    }
   }
   __syncthreads();
   const float rnmax = s_rn;
+  const int r_emin = s_remin, r_emax = s_remax;
   const float4* sR4 = reinterpret_cast<const float4*>(sR);
   // fp32 rounding bound of one dot product, doubled: 2 * gamma_D with gamma_D < (D+1) 2^-24
   const float rel = static_cast<float>(D + 1) * 0x1p-23f;
@@ -193,7 +221,7 @@ __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __r
     const float emax = l2 * rnmax * rel * 1.000001f + absb;
     // the four best candidates (values t, candidate indices j)
     float t0 = -INFINITY, t1 = -INFINITY, t2 = -INFINITY, t3 = -INFINITY;
-    int j0 = 0, j1 = 0, j2 = 0, j3 = 0;  // j3 is only needed to keep the list ordered
+    int j0 = 0, j1 = 0, j2 = 0;
     for (int c0 = 0; c0 < m4; c0 += 4) {
       asm volatile("" ::: "memory");
       float sv[4] = {0.f, 0.f, 0.f, 0.f};
@@ -219,86 +247,95 @@ __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __r
           const int j = c + t * m;
           if (v > t3) {
             if (v > t2) {
-              t3 = t2; j3 = j2;
+              t3 = t2;
               if (v > t1) {
                 t2 = t1; j2 = j1;
                 if (v > t0) { t1 = t0; j1 = j0; t0 = v; j0 = j; } else { t1 = v; j1 = j; }
               } else { t2 = v; j2 = j; }
-            } else { t3 = v; j3 = j; }
+            } else { t3 = v; }
           }
         }
       }
     }
-    (void)j3;
     int h = j0;
     const float thr = 2.f * emax * 1.0001f;
     if (!(t0 - t1 > thr)) {
       const uint16_t* xr = x + r * D;
       const bool few = (t0 - t3 > thr);  // every candidate within thr of the top is among the four
-      bool done = false;
       int cj[3];
       int nc = 0;
       if (few) {
-        // candidates within thr, in index order
         cj[nc++] = j0;
         if (t0 - t1 <= thr) cj[nc++] = j1;
         if (t0 - t2 <= thr) cj[nc++] = j2;
-        for (int a = 1; a < nc; ++a)
-          for (int b2 = a; b2 > 0 && cj[b2 - 1] > cj[b2]; --b2) {
-            const int tmp = cj[b2]; cj[b2] = cj[b2 - 1]; cj[b2 - 1] = tmp;
-          }
-        // level 2: fp64 values and bounds
-        double val[3], err[3];
-        for (int k = 0; k < nc; ++k) {
-          const int c = cj[k] % m;
-          double sacc = 0.0, aacc = 0.0;
-          for (int d = 0; d < D; ++d) {
-            const double xd = static_cast<double>(xval(d)), rd = static_cast<double>(sR[d * m4 + c]);
-            sacc = fma(xd, rd, sacc);
-            aacc = fma(fabs(xd), fabs(rd), aacc);
-          }
-          val[k] = cj[k] < m ? sacc : -sacc;
-          err[k] = aacc * static_cast<double>(D) * 0x1p-52 + 0x1p-1000;
-        }
-        int bi = 0;
-        for (int k = 1; k < nc; ++k)
-          if (val[k] > val[bi]) bi = k;
-        bool cert = true;
-        for (int k = 0; k < nc; ++k)
-          if (k != bi && !(val[bi] - val[k] > err[bi] + err[k])) cert = false;
-        if (cert) {
-          h = cj[bi];
-          done = true;
+      }
+      // exponent span of the row's products
+      int xemin = INT_MAX, xemax = INT_MIN;
+      for (int d = 0; d < D; ++d) {
+        bool ng;
+        uint32_t M;
+        int E;
+        bf16_parts(static_cast<uint16_t>(__float_as_uint(xval(d)) >> 16), &ng, &M, &E);
+        if (M != 0) {
+          xemin = min(xemin, E);
+          xemax = max(xemax, E);
         }
       }
-      if (!done) {
-        // level 3: exact sums of the candidates that may beat the top, in index order
+      const bool any_term = xemin != INT_MAX && r_emin != INT_MAX;
+      const int ebase = any_term ? xemin + r_emin : 0;
+      const bool fits128 = !any_term || (xemax + r_emax) - ebase <= 100;
+      // exact sum of column c as an integer times 2^ebase (fits128 only)
+      auto exact128 = [&](int c) -> __int128 {
+        __int128 acc = 0;
+        if (!any_term) return acc;
+        for (int d = 0; d < D; ++d) {
+          bool nx, nr2;
+          uint32_t Mx, Mr;
+          int Ex, Er;
+          bf16_parts(static_cast<uint16_t>(__float_as_uint(xval(d)) >> 16), &nx, &Mx, &Ex);
+          bf16_parts(static_cast<uint16_t>(__float_as_uint(sR[d * m4 + c]) >> 16), &nr2, &Mr, &Er);
+          if (Mx == 0 || Mr == 0) continue;
+          const __int128 term = static_cast<__int128>(Mx * Mr) << (Ex + Er - ebase);
+          acc = (nx != nr2) ? acc - term : acc + term;
+        }
+        return acc;
+      };
+      auto is_cand = [&](int j) -> bool {
+        if (few) {
+          bool in = false;
+          for (int k = 0; k < nc; ++k) in = in || (cj[k] == j);
+          return in;
+        }
+        const int c = j < m ? j : j - m;
+        float sc = 0.f;
+        for (int d = 0; d < D; ++d) sc = fmaf(xval(d), sR[d * m4 + c], sc);
+        const float vj = j < m ? sc : -sc;
+        return (t0 - vj <= thr) || (vj != vj);
+      };
+      int best_j = -1;
+      if (fits128) {
+        __int128 best = 0;
+        for (int j = 0; j < 2 * m; ++j) {
+          if (!is_cand(j)) continue;
+          const __int128 v = (j < m) ? exact128(j) : -exact128(j - m);
+          if (best_j < 0 || v > best) {
+            best = v;
+            best_j = j;
+          }
+        }
+      } else {
         Fix576 best, cur;
-        int best_j = -1;
-        for (int pass = 0; pass < 2; ++pass) {
-          for (int c = 0; c < m; ++c) {
-            const int j = c + pass * m;
-            bool cand;
-            if (few) {
-              cand = false;
-              for (int k = 0; k < nc; ++k) cand = cand || (cj[k] == j);
-            } else {
-              float sc = 0.f;
-              for (int d = 0; d < D; ++d) sc = fmaf(xval(d), sR[d * m4 + c], sc);
-              const float vj = pass == 0 ? sc : -sc;
-              cand = (t0 - vj <= thr) || (vj != vj);
-            }
-            if (!cand) continue;
-            fix_dot(xr, R, D, m, c, cur);
-            if (pass == 1) fix_negate(cur);
-            if (best_j < 0 || fix_greater(cur, best)) {
-              best = cur;
-              best_j = j;
-            }
+        for (int j = 0; j < 2 * m; ++j) {
+          if (!is_cand(j)) continue;
+          fix_dot(xr, R, D, m, j < m ? j : j - m, cur);
+          if (j >= m) fix_negate(cur);
+          if (best_j < 0 || fix_greater(cur, best)) {
+            best = cur;
+            best_j = j;
           }
         }
-        h = best_j >= 0 ? best_j : j0;
       }
+      h = best_j >= 0 ? best_j : j0;
     }
     hash[r] = h;
   }
