@@ -325,6 +325,7 @@ def main():
     import sparse_causal_flash_gb300 as scfa
     from sparse_causal_flash_gb300 import build as scfa_build
     from sparse_causal_flash_gb300.pipeline import Step
+    from sparse_causal_flash_gb300.replicas import job_throughput, max_over_ranks
     scfa_build.build()
     scfa.load()
     torch.cuda.set_device(local)
@@ -393,13 +394,9 @@ def main():
     ms, kms, t0, t1 = timed(run_once, args.steps, kernel_events=True)
     clocks = sampler.stop(t0, t1) if sampler else None
     assert scfa.scfa_get_device_status(step.ws_b) == 0, "device status not ok after the timed steps"
-    total_ms = sum(ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(ms), dev)
     ms_per_step = total_ms / args.steps
-    value = world * useful * args.steps / (total_ms / 1e3) / 1e12
+    value = job_throughput(useful, args.steps, total_ms, world) / 1e12
 
     # the attention kernels timed alone (events recorded by the library around each launch)
     fwd_ms = statistics.mean(kms[0])
@@ -461,12 +458,8 @@ def main():
             run_e2e()
         K = max(5, args.steps // 2)
         ems, _, _, _ = timed(run_e2e, K)
-        tot = sum(ems)
-        if dist is not None:
-            t = torch.tensor([tot], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            tot = float(t.item())
-        e2e = {"value": world * useful * K / (tot / 1e3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        tot = max_over_ranks(sum(ems), dev)
+        e2e = {"value": job_throughput(useful, K, tot, world) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": tot / K, "steps": K}
 
     if rank == 0:

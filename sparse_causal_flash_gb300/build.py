@@ -7,6 +7,7 @@ Run as `python -m sparse_causal_flash_gb300.build` or call build().
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -41,8 +42,21 @@ def _compile(src: str, extra: list[str]) -> str:
 
 
 def build(verbose_ptxas: bool = False, force: bool = False) -> str:
-    """Compile every CUDA source and link libscfa.so; returns its path."""
+    """Compile every CUDA source and link libscfa.so; returns its path.
+
+    Serialised by a file lock, so several processes (one per GPU) may call it
+    at once: the first compiles, the others find the library up to date.
+    """
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(verbose_ptxas, force)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose_ptxas: bool, force: bool) -> str:
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     deps = srcs + [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".cuh", ".h"))]
     deps.append(os.path.join(os.path.dirname(HERE), "include", "scfa.h"))
