@@ -285,6 +285,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                   mbar_test(&sm.dq_empty, (it & 1) ^ 1))
                 break;
               if (!wc.tick(abort_flag, p.status)) { ok = false; break; }
+              __nanosleep(32);  // leave issue slots to the compute warps sharing this SMSP
             }
             if (!ok) break;
           }

@@ -11,24 +11,27 @@
 // GB300 design: one persistent CTA per SM walks the pair work order: a work
 // item is a pair of adjacent query tiles (2m, 2m + 1) of one head, and the CTA
 // streams the UNION of their live key-tile lists once, so each K / V tile load
-// serves both query tiles. Roles (320 threads):
+// serves both query tiles. Roles (352 threads):
 //   warp 0      producer: TMA of Q_2m and Q_2m+1 per item, then K_j / V_j of
-//               each union tile into a 4-stage ring (128-byte swizzle).
-//   warp 1      TMEM owner; lane 0 issues tcgen05.mma in the order
-//               S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ..., where
-//               S_g = Q_g K_j^T lands in TMEM and PV_g reads P_g from TMEM (P
-//               overwrites S_g in place as bf16 pairs). One thread's MMAs run
-//               in order, so S_g(j+1) cannot overtake the PV_g(j) reading P_g.
-//               A tile that is live for only one query tile skips the other's
-//               S and PV.
-//   warps 2-5, 6-9  softmax warpgroup g = 0, 1 (query tile 2m + g); thread =
-//               query row = TMEM lane: element mask only on tiles not flagged
-//               FULL, online softmax in the log2 domain with a lazy rescale
-//               (O_g is rescaled only when the row max grows by more than
-//               2^8; S_g(j) complete implies PV_g(j-1) complete, so O_g is
-//               stable then), P_g written back to TMEM, and the epilogue
-//               (O / l in bf16, LSE in fp32, natural log).
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+//               each union tile into a ring (128-byte swizzle).
+//   warps 1, 10 MMA issuers for query tile g = 0, 1 (lane 0; warp 1 also owns
+//               TMEM): S_g = Q_g K_j^T into TMEM, then PV_g with P_g read from
+//               TMEM. Two issuers keep one tile's S -> softmax -> PV chain from
+//               waiting on the other's softmax. A tile live for only one query
+//               tile skips the other's S and PV, but both issuers release every
+//               ring stage (two arrivals).
+//   warps 2-5, 6-9  softmax warpgroup g (query tile 2m + g); thread = query
+//               row = TMEM lane: element mask only on tiles not flagged FULL,
+//               online softmax in the log2 domain with a lazy rescale (O_g is
+//               rescaled only when the row max grows by more than 2^8), P_g
+//               written to TMEM as bf16 pairs, and the epilogue (O / l in bf16,
+//               LSE in fp32, natural log). Max, argument and row sum use the
+//               three-input max and packed f32x2 FMA / add.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D);
+// at D = 64, P_0 [384,448) and P_1 [448,512), so S_g(j+1) is computed while the
+// softmax of S_g(j) runs (the softmax frees S_g once it is in registers, and
+// waits for PV_g(j-1) before overwriting P_g); at D = 128, P_g overwrites S_g
+// and one issuer's in-order MMAs keep S_g(j+1) behind PV_g(j).
 // Every wait is bounded (1 s); on expiry the CTA raises the workspace status
 // word, leaves its loops and frees TMEM.
 #include <climits>
@@ -43,11 +46,17 @@ namespace {
 template <int D>
 constexpr int fwd_stages() { return D == 64 ? 4 : 2; }
 constexpr int kSubBytes = kTile * 128;  // one [128 rows][64 bf16] swizzled sub-tile
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 352;  // producer, MMA for tile 0, 2 x 4 softmax warps, MMA for tile 1
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// At D = 64, S_0, S_1, O_0, O_1 take 384 of the 512 TMEM columns and P_g gets
+// its own 64 columns; then S_g(j+1) can be computed while the softmax of
+// S_g(j) runs. At D = 128 the columns are all taken and P_g overwrites S_g.
+template <int D>
+constexpr bool fwd_separate_p() { return D == 64; }
 
 template <int D>
 struct __align__(1024) FwdSmem {
@@ -59,7 +68,8 @@ struct __align__(1024) FwdSmem {
   int32_t khash[2][2][kTile];
   uint64_t q_full, q_empty;
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2], drain;
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2], drain[2];
+  uint64_t s_free[2], pv_done[2];  // used when P has its own TMEM columns
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -125,19 +135,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.q_empty, 2);  // one commit from each MMA warp
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.kv_empty[s], 2);  // one commit from each MMA warp
     }
     for (int g = 0; g < 2; ++g) {
       mbar_init(&sm.s_full[g], 1);
       mbar_init(&sm.p_full[g], 128);
       mbar_init(&sm.o_full[g], 1);
       mbar_init(&sm.o_empty[g], 128);
+      mbar_init(&sm.s_free[g], 128);
+      mbar_init(&sm.pv_done[g], 1);
     }
-    mbar_init(&sm.drain, 1);
+    mbar_init(&sm.drain[0], 1);
+    mbar_init(&sm.drain[1], 1);
     sm.abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -197,30 +210,40 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (last_q >= 0) mbar_wait(&sm.q_full, last_q & 1, abort_flag, p.status);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues the MMAs of query tile 0 and warp 10 those of query tile
+    // 1, so neither tile's S -> softmax -> PV chain waits on the other's
+    // softmax; the tensor core interleaves the two instruction streams. Both
+    // walk the same union list and release each K / V stage (2 arrivals).
+    constexpr bool kSepP = fwd_separate_p<D>();
+    const int g = warp == 1 ? 0 : 1;
+    const int live_bit = g == 0 ? 1 : 4;
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kTile, D, 0, 1);
-      int kv_it = 0, item = 0;
-      int p_it[2] = {0, 0}, o_it[2] = {0, 0};
+      int kv_it = 0, item = 0, p_it = 0, o_it = 0, n_s = 0;
       bool ok = true;
       // descriptors built once; steps and stages are constant adds
       constexpr uint32_t kStage16 = (D / 64) * kSubBytes >> 4;
-      const uint64_t qdesc = smem_desc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(sm.q[g][0]), 16, 1024);
       const uint64_t kdesc = smem_desc_sw128(smem_u32(sm.k[0][0]), 16, 1024);
       const uint64_t vdesc = smem_desc_sw128(smem_u32(sm.v[0][0]), kSubBytes, 1024);
-      auto issue_s = [&](int g, int kvi) -> bool {
+      const uint32_t dS = tmem + 128u * g, dO_ = tmem + 256u + D * g;
+      const uint32_t aP = kSepP ? tmem + 384u + 64u * g : dS;
+      auto issue_s = [&](int kvi) -> bool {
         const int s = kvi % kStages;
+        // with its own P columns, S_g is overwritten once the softmax has read
+        // the previous S_g; otherwise issue order behind PV_g protects it
+        if (kSepP && n_s > 0 && !mbar_wait(&sm.s_free[g], (n_s - 1) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(&sm.k_full[s], (kvi / kStages) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint64_t a = qdesc + static_cast<uint64_t>(g * kStage16);
         const uint64_t b = kdesc + static_cast<uint64_t>(s * kStage16);
-        const uint32_t d = tmem + 128u * g;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(d, a + kstep_off16(kk, kSubBytes), b + kstep_off16(kk, kSubBytes), idesc_s, kk > 0);
+          mma_bf16_ss(dS, qdesc + kstep_off16(kk, kSubBytes), b + kstep_off16(kk, kSubBytes), idesc_s, kk > 0);
         tc_commit(&sm.s_full[g]);
+        ++n_s;
         return true;
       };
       for (int w = blockIdx.x; w < p.n_pairs && ok; w += gridDim.x) {
@@ -235,51 +258,57 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int j_cur, bits_cur, j_nxt = 0, bits_nxt = 0;
         wk.next(j_cur, bits_cur);
         if (!mbar_wait(&sm.q_full, item & 1, abort_flag, p.status)) break;
-        if ((bits_cur & 1) && !issue_s(0, kv_it)) break;
-        if ((bits_cur & 4) && !issue_s(1, kv_it)) break;
-        bool pv_first[2] = {true, true};
-        for (int t = 0; t < cnt && ok; ++t) {
+        if ((bits_cur & live_bit) && !issue_s(kv_it)) break;
+        bool pv_first = true;
+        for (int t = 0; t < cnt; ++t) {
           const bool more = t + 1 < cnt;
           if (more) wk.next(j_nxt, bits_nxt);
+          const bool s_next = more && (bits_nxt & live_bit);
+          bool s_next_issued = false;
           const int s = kv_it % kStages;
-          for (int g = 0; g < 2; ++g) {
-            const int live = g == 0 ? (bits_cur & 1) : (bits_cur & 4);
-            if (live) {
-              if (!mbar_wait(&sm.p_full[g], p_it[g] & 1, abort_flag, p.status)) { ok = false; break; }
-              if (pv_first[g] && !mbar_wait(&sm.o_empty[g], (o_it[g] & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-              if (!mbar_wait(&sm.v_full[s], (kv_it / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
-              tc_fence_after();
-              const uint64_t vb = vdesc + static_cast<uint64_t>(s * kStage16);
-              const uint32_t dO_ = tmem + 256u + D * g, aP = tmem + 128u * g;
-              const uint32_t acc0 = pv_first[g] ? 0u : 1u;
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_bf16_ts(dO_, aP + kk * 8, vb + static_cast<uint64_t>(kk * 128), idesc_o, kk > 0 ? 1u : acc0);
-              pv_first[g] = false;
-              ++p_it[g];
+          if (bits_cur & live_bit) {
+            // S_g(j+1) ahead of PV_g(j) when the next union tile is live here
+            // (its stage was filled before this one's release is needed)
+            if (kSepP && s_next) {
+              if (!issue_s(kv_it + 1)) { ok = false; break; }
+              s_next_issued = true;
             }
-            if (g == 1) tc_commit(&sm.kv_empty[s]);
-            const int live_n = g == 0 ? (bits_nxt & 1) : (bits_nxt & 4);
-            if (more && live_n && !issue_s(g, kv_it + 1)) { ok = false; break; }
+            if (!mbar_wait(&sm.p_full[g], p_it & 1, abort_flag, p.status)) { ok = false; break; }
+            if (pv_first && !mbar_wait(&sm.o_empty[g], (o_it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+            if (!mbar_wait(&sm.v_full[s], (kv_it / kStages) & 1, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t vb = vdesc + static_cast<uint64_t>(s * kStage16);
+            const uint32_t acc0 = pv_first ? 0u : 1u;
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_bf16_ts(dO_, aP + kk * 8, vb + static_cast<uint64_t>(kk * 128), idesc_o, kk > 0 ? 1u : acc0);
+            if (kSepP) tc_commit(&sm.pv_done[g]);
+            pv_first = false;
+            ++p_it;
+          } else if (!mbar_wait(&sm.k_full[s], (kv_it / kStages) & 1, abort_flag, p.status)) {
+            // a tile this query tile skips is still released only once it has
+            // landed: without the wait this warp could run ahead through skipped
+            // tiles and give both arrivals of a stage's release on its own
+            ok = false;
+            break;
           }
-          if (!ok) break;
+          tc_commit(&sm.kv_empty[s]);
+          if (s_next && !s_next_issued && !issue_s(kv_it + 1)) { ok = false; break; }
           ++kv_it;
           j_cur = j_nxt;
           bits_cur = bits_nxt;
         }
         if (!ok) break;
-        for (int g = 0; g < 2; ++g) {
-          if (!pv_first[g]) {
-            tc_commit(&sm.o_full[g]);
-            ++o_it[g];
-          }
+        if (!pv_first) {
+          tc_commit(&sm.o_full[g]);
+          ++o_it;
         }
         tc_commit(&sm.q_empty);
         ++item;
       }
       // drain: all MMAs issued by this thread are complete before TMEM is freed
-      tc_commit(&sm.drain);
-      mbar_wait(&sm.drain, 0, abort_flag, p.status);
+      tc_commit(&sm.drain[g]);
+      mbar_wait(&sm.drain[g], 0, abort_flag, p.status);
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -289,7 +318,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int tid = (warp - 2 - 4 * grp) * 32 + lane;  // 0..127 for cooperative staging
     const int bar_id = 1 + grp;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    constexpr bool kSepP = fwd_separate_p<D>();
     const uint32_t colS = 128u * grp, colO = 256u + D * grp;
+    const uint32_t colP = kSepP ? 384u + 64u * grp : colS;
+    int n_p = 0;  // P_g tiles written so far
     const int live_bit = grp == 0 ? 1 : 4, full_bit = grp == 0 ? 2 : 8;
     int s_it = 0, o_it = 0;
     for (int w = blockIdx.x; w < p.n_pairs; w += gridDim.x) {
@@ -339,6 +371,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int cc = 0; cc < 4; ++cc)
           tmem_ld32(lane_base + colS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
         tmem_wait_ld();
+        if (kSepP) {
+          // S_g is in registers: the MMA warp may compute the next S_g
+          tc_fence_before();
+          mbar_arrive(&sm.s_free[grp]);
+        }
         if (!full) {
 #pragma unroll
           for (int c4 = 0; c4 < kTile / 4; ++c4) {
@@ -356,14 +393,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               if (!adm[u]) sr[c4 * 4 + u] = 0xff800000u;  // -inf
           }
         }
-        // row max: eight independent chains, then a tree
-        float mx[8];
+        // row max: four independent chains of three-input maxima
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(sr[u]);
-#pragma unroll
-        for (int c = 8; c < kTile; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c]));
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+        for (int c = 4; c < kTile; c += 8) {
+          mx0 = max3f(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+          mx1 = max3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+          mx2 = max3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+          mx3 = max3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+        }
+        const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
         const float m_new = fmaxf(m_used, mt);
         const bool resc = m_new > m_used + kRescaleThreshold;
         float alpha = 1.f;
@@ -372,23 +412,38 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           m_used = m_new;
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        float rsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        // P = 2^(s * scale * log2(e) - m) as bf16 pairs over the first 64 columns of S_g
+        // P = 2^(s * scale * log2(e) - m) as bf16 pairs over the first 64 columns
+        // of S_g; the argument and the row sum run on packed f32 pairs
+        const uint64_t sl2 = f2(p.scale_log2, p.scale_log2), nm2 = f2(-msub, -msub);
+        if (kSepP && n_p > 0) {
+          // the previous PV_g has read P_g (and finished adding into O_g)
+          ok = mbar_wait(&sm.pv_done[grp], (n_p - 1) & 1, abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+        }
+        ++n_p;
+        uint64_t rsum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float e0 = ex2_approx(fmaf(__uint_as_float(sr[h * 32 + c]), p.scale_log2, -msub));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(sr[h * 32 + c + 1]), p.scale_log2, -msub));
-            rsum[(c >> 1) & 7] += e0 + e1;
+            const uint64_t arg = fma2(f2(__uint_as_float(sr[h * 32 + c]), __uint_as_float(sr[h * 32 + c + 1])), sl2, nm2);
+            float a0, a1;
+            f2_split(arg, a0, a1);
+            const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+            rsum2[(c >> 1) & 3] = add2(rsum2[(c >> 1) & 3], f2(e0, e1));
             pk[c >> 1] = pack_bf16x2(e0, e1);
           }
-          tmem_st16(lane_base + colS + h * 16, pk);
+          tmem_st16(lane_base + colP + h * 16, pk);
         }
-        const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
+        const uint64_t rs2 = add2(add2(rsum2[0], rsum2[1]), add2(rsum2[2], rsum2[3]));
+        float rs_lo, rs_hi;
+        f2_split(rs2, rs_lo, rs_hi);
+        const float rs = rs_lo + rs_hi;
         l = l * alpha + rs;
-        // rescale O (rare). S_g(t) complete => PV_g(t-1) complete: O_g is stable
+        // rescale O (rare). PV_g(t-1) is complete here: with separate P columns
+        // the wait above says so; otherwise S_g(t) complete implies it
         if (!first_tile && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
