@@ -197,6 +197,13 @@ scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int
  *   csc_ptr [B*H*nKt+1], csc_rows, cflags (CSC over k tiles, rows ascending);
  *   flag bit 0 = FULL; work_fwd [B*H*nQt] and work_bwd [B*H*nKt]: every tile
  *   id sorted by live count descending, then id ascending.
+ *   Forward schedule over pairs of query tiles (2m, 2m + 1) of one head, pair
+ *   id = (b*H + h) * ceil(nQt / 2) + m: pair_count [pairs] = size of the union
+ *   of the two live lists; pair_list holds that union, key tiles ascending,
+ *   from index row_ptr[(b*H + h)*nQt + 2m], one int32 per tile:
+ *   (key tile << 4) | bit 0 live for 2m | bit 1 FULL for 2m | bit 2 live for
+ *   2m + 1 | bit 3 FULL for 2m + 1; work_pairs [pairs]: pair ids by
+ *   pair_count descending, then id ascending.
  * ------------------------------------------------------------------------- */
 scfa_status scfa_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
                        const int32_t* q_hash, const int32_t* k_hash,
@@ -212,6 +219,9 @@ typedef struct {
   const uint8_t* cflags;
   const int32_t* work_fwd;
   const int32_t* work_bwd;
+  const int32_t* pair_count;
+  const int32_t* pair_list;
+  const int32_t* work_pairs;
   int n_q_tiles;   /* per head */
   int n_k_tiles;   /* per head */
 } scfa_tile_view;

@@ -94,7 +94,8 @@ def load() -> None:
 
 class TileView(ctypes.Structure):
     _fields_ = [("row_ptr", _P), ("cols", _P), ("fflags", _P), ("csc_ptr", _P), ("csc_rows", _P),
-                ("cflags", _P), ("work_fwd", _P), ("work_bwd", _P), ("n_q_tiles", _I), ("n_k_tiles", _I)]
+                ("cflags", _P), ("work_fwd", _P), ("work_bwd", _P), ("pair_count", _P), ("pair_list", _P),
+                ("work_pairs", _P), ("n_q_tiles", _I), ("n_k_tiles", _I)]
 
 
 def _ptr(t):

@@ -100,6 +100,7 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
   w.work_bwd = take(sizeof(int32_t) * w.n_ktiles);
   w.cursor = take(sizeof(int32_t) * (w.nQt + 2 * w.nKt + 3));
   w.pcount = take(sizeof(int32_t) * w.n_pairs);
+  w.ulist = take(sizeof(int32_t) * w.max_live);
   w.work_pairs = take(sizeof(int32_t) * w.n_pairs);
   if (backward) {
     w.dq_acc = take(sizeof(float) * static_cast<size_t>(BH) * Tq * D);
@@ -370,6 +371,9 @@ scfa_status scfa_tile_view_get(const void* ws, int mode, int B, int H, int Tq, i
   out->cflags = reinterpret_cast<const uint8_t*>(w + L.cflags);
   out->work_fwd = reinterpret_cast<const int32_t*>(w + L.work_fwd);
   out->work_bwd = reinterpret_cast<const int32_t*>(w + L.work_bwd);
+  out->pair_count = reinterpret_cast<const int32_t*>(w + L.pcount);
+  out->pair_list = reinterpret_cast<const int32_t*>(w + L.ulist);
+  out->work_pairs = reinterpret_cast<const int32_t*>(w + L.work_pairs);
   out->n_q_tiles = L.nQt;
   out->n_k_tiles = L.nKt;
   return SCFA_OK;

@@ -87,40 +87,11 @@ struct FwdParams {
   const uint8_t* fflags;
   const int32_t* work_pairs;
   const int32_t* pcount;
+  const int32_t* ulist;
   int n_pairs;
   uint16_t* o;
   float* lse;
   int* status;
-};
-
-// Merge walk over the live lists of query tiles 2m and 2m + 1 (ascending).
-struct PairWalk {
-  const int32_t* cols;
-  const uint8_t* ff;
-  int a, ae, b, be;
-  __device__ __forceinline__ void init(const FwdParams& p, long long g0, bool has1) {
-    cols = p.cols;
-    ff = p.fflags;
-    a = p.row_ptr[g0];
-    ae = p.row_ptr[g0 + 1];
-    b = has1 ? p.row_ptr[g0 + 1] : 0;
-    be = has1 ? p.row_ptr[g0 + 2] : 0;
-  }
-  // next union tile: key tile j; bits: 1 live for g=0, 2 FULL for g=0, 4 live for g=1, 8 FULL for g=1
-  __device__ __forceinline__ void next(int& j, int& bits) {
-    const int ja = a < ae ? cols[a] : INT_MAX;
-    const int jb = b < be ? cols[b] : INT_MAX;
-    j = min(ja, jb);
-    bits = 0;
-    if (ja == j) {
-      bits |= 1 | ((ff[a] & kFlagFull) ? 2 : 0);
-      ++a;
-    }
-    if (jb == j) {
-      bits |= 4 | ((ff[b] & kFlagFull) ? 8 : 0);
-      ++b;
-    }
-  }
 };
 
 template <int D>
@@ -182,12 +153,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (has1) tma_load_3d(sm.q[1][sub], &tm_q, &sm.q_full, sub * 64, (2 * m + 1) * kTile, bh);
         }
         last_q = item;
-        PairWalk wk;
-        wk.init(p, g0, has1);
+        const int32_t* ul = p.ulist + p.row_ptr[g0];
         bool ok = true;
         for (int t = 0; t < cnt; ++t) {
-          int j, bits;
-          wk.next(j, bits);
+          const int j = ul[t] >> 4;
           const int s = kv_it % kStages;
           const uint32_t ph = (kv_it / kStages) & 1;
           if (!mbar_wait(&sm.kv_empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
@@ -251,18 +220,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int cnt = p.pcount[pid];
         if (cnt == 0) continue;
         const int bh = pid / p.nPairs, m = pid % p.nPairs;
-        const bool has1 = 2 * m + 1 < p.nQt;
         const long long g0 = static_cast<long long>(bh) * p.nQt + 2 * m;
-        PairWalk wk;
-        wk.init(p, g0, has1);
-        int j_cur, bits_cur, j_nxt = 0, bits_nxt = 0;
-        wk.next(j_cur, bits_cur);
+        // union entries: current, next, and the one after, loaded two tiles
+        // ahead so the list read stays off the issue chain
+        const int32_t* ul = p.ulist + p.row_ptr[g0];
+        int bits_cur = ul[0] & 15;
+        int bits_nxt = cnt > 1 ? ul[1] & 15 : 0;
         if (!mbar_wait(&sm.q_full, item & 1, abort_flag, p.status)) break;
         if ((bits_cur & live_bit) && !issue_s(kv_it)) break;
         bool pv_first = true;
         for (int t = 0; t < cnt; ++t) {
           const bool more = t + 1 < cnt;
-          if (more) wk.next(j_nxt, bits_nxt);
+          const int bits_pre = t + 2 < cnt ? ul[t + 2] & 15 : 0;
           const bool s_next = more && (bits_nxt & live_bit);
           bool s_next_issued = false;
           const int s = kv_it % kStages;
@@ -295,8 +264,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tc_commit(&sm.kv_empty[s]);
           if (s_next && !s_next_issued && !issue_s(kv_it + 1)) { ok = false; break; }
           ++kv_it;
-          j_cur = j_nxt;
           bits_cur = bits_nxt;
+          bits_nxt = bits_pre;
         }
         if (!ok) break;
         if (!pv_first) {
@@ -322,14 +291,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t colS = 128u * grp, colO = 256u + D * grp;
     const uint32_t colP = kSepP ? 384u + 64u * grp : colS;
     int n_p = 0;  // P_g tiles written so far
-    const int live_bit = grp == 0 ? 1 : 4, full_bit = grp == 0 ? 2 : 8;
     int s_it = 0, o_it = 0;
     for (int w = blockIdx.x; w < p.n_pairs; w += gridDim.x) {
       const int pid = p.work_pairs[w];
-      const int cnt = p.pcount[pid];
       const int bh = pid / p.nPairs, m = pid % p.nPairs;
       const int i = 2 * m + grp;
-      const bool has1 = 2 * m + 1 < p.nQt;
       const long long g0 = static_cast<long long>(bh) * p.nQt + 2 * m;
       const int row = i * kTile + r;
       const bool valid = i < p.nQt && row < p.Tq;
@@ -339,27 +305,49 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         qi = (p.mode == SCFA_MODE_DENSE) ? row : p.q_idx[grow];
         if (p.mode == SCFA_MODE_HASH) qh = p.q_hash[grow];
       }
-      PairWalk wk;
-      wk.init(p, g0, has1);
+      // this query tile's own live list; column, flag and key metadata of the
+      // coming tiles are loaded ahead (column two tiles ahead, key index and
+      // bucket one tile ahead) so no global load sits on the tile chain
+      const int e_beg = i < p.nQt ? p.row_ptr[g0 + grp] : 0;
+      const int e_end = i < p.nQt ? p.row_ptr[g0 + grp + 1] : 0;
+      const long long kbase = static_cast<long long>(bh) * p.Tk;
+      auto key_meta = [&](int j, int f, int& kid, int& kh) {
+        kid = INT_MAX;
+        kh = INT_MIN;
+        if (f & kFlagFull) return;
+        const int col = j * kTile + tid;
+        const bool kv = col < p.Tk;
+        if (p.mode == SCFA_MODE_DENSE) kid = kv ? col : INT_MAX;
+        else kid = kv ? p.k_idx[kbase + col] : INT_MAX;
+        if (p.mode == SCFA_MODE_HASH) kh = kv ? p.k_hash[kbase + col] : INT_MIN;
+      };
+      int j_c = 0, f_c = 0, kid_c = INT_MAX, kh_c = INT_MIN, j_n = 0, f_n = 0;
+      if (e_beg < e_end) {
+        j_c = p.cols[e_beg];
+        f_c = p.fflags[e_beg];
+        key_meta(j_c, f_c, kid_c, kh_c);
+      }
+      if (e_beg + 1 < e_end) {
+        j_n = p.cols[e_beg + 1];
+        f_n = p.fflags[e_beg + 1];
+      }
       float m_used = -INFINITY, l = 0.f;
       bool ok = true, any = false;
-      for (int t = 0; t < cnt; ++t) {
-        int j, bits;
-        wk.next(j, bits);
-        if (!(bits & live_bit)) continue;
+      for (int e = e_beg; e < e_end; ++e) {
+        const bool full = (f_c & kFlagFull) != 0;
+        const int kid = kid_c, khv = kh_c;
+        int kid_n = INT_MAX, kh_n = INT_MIN, j_nn = 0, f_nn = 0;
+        if (e + 1 < e_end) key_meta(j_n, f_n, kid_n, kh_n);
+        if (e + 2 < e_end) {
+          j_nn = p.cols[e + 2];
+          f_nn = p.fflags[e + 2];
+        }
         const bool first_tile = !any;
         any = true;
-        const bool full = (bits & full_bit) != 0;
         const int b = s_it & 1;
         if (!full) {
-          const int col = j * kTile + tid;
-          const bool kv = col < p.Tk;
-          const long long gk = static_cast<long long>(bh) * p.Tk + col;
-          int kid;
-          if (p.mode == SCFA_MODE_DENSE) kid = kv ? col : INT_MAX;
-          else kid = kv ? p.k_idx[gk] : INT_MAX;
           sm.kidx[grp][b][tid] = kid;
-          if (p.mode == SCFA_MODE_HASH) sm.khash[grp][b][tid] = kv ? p.k_hash[gk] : INT_MIN;
+          if (p.mode == SCFA_MODE_HASH) sm.khash[grp][b][tid] = khv;
           named_bar_sync(bar_id, 128);
         }
         ok = mbar_wait(&sm.s_full[grp], s_it & 1, abort_flag, p.status);
@@ -459,6 +447,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_before();
         mbar_arrive(&sm.p_full[grp]);
         ++s_it;
+        j_c = j_n;
+        f_c = f_n;
+        kid_c = kid_n;
+        kh_c = kh_n;
+        j_n = j_nn;
+        f_n = f_nn;
       }
       if (!ok) break;
       if (!any) {
@@ -533,6 +527,7 @@ static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   p.nPairs = L.nPairs;
   p.work_pairs = reinterpret_cast<const int32_t*>(a.ws + L.work_pairs);
   p.pcount = reinterpret_cast<const int32_t*>(a.ws + L.pcount);
+  p.ulist = reinterpret_cast<const int32_t*>(a.ws + L.ulist);
   p.n_pairs = static_cast<int>(L.n_pairs);
   p.o = a.o_out;
   p.lse = a.lse_out;

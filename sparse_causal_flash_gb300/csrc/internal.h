@@ -30,6 +30,9 @@ struct AttnWs {
   int nPairs = 0;                        // per head
   long long n_pairs = 0;                 // over all heads
   size_t pcount = 0;                     // union size per pair
+  size_t ulist = 0;                      // union list of pair m of head bh at row_ptr[bh * nQt + 2m]:
+                                         // (key tile << 4) | bits (1 live for 2m, 2 FULL for 2m,
+                                         // 4 live for 2m + 1, 8 FULL for 2m + 1), key tiles ascending
   size_t work_pairs = 0;                 // pair ids by union size descending
   size_t dq_acc = 0;                     // backward: fp32 dQ accumulator [B,H,Tq,D]
   size_t drow = 0;                       // backward: fp32 rowsum(dO * O) [B,H,Tq]

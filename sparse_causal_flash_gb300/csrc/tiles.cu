@@ -208,8 +208,9 @@ __global__ void tile_fill_kernel(TileCtx c, long long n_q, long long n_k,
 
 // Live-list union size of each query-tile pair (2m, 2m + 1): a merge count of
 // the two ascending CSR rows.
-__global__ void pair_count_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cols,
-                                  int nQt, int nPairs, long long n_pairs, int32_t* __restrict__ pcount) {
+__global__ void pair_list_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cols,
+                                 const uint8_t* __restrict__ fflags, int nQt, int nPairs, long long n_pairs,
+                                 int32_t* __restrict__ pcount, int32_t* __restrict__ ulist) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long pid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; pid < n_pairs; pid += stride) {
     const long long bh = pid / nPairs;
@@ -221,13 +222,24 @@ __global__ void pair_count_kernel(const int32_t* __restrict__ row_ptr, const int
       b = row_ptr[g0 + 1];
       be = row_ptr[g0 + 2];
     }
+    // the union is no longer than the two lists together, so it fits in the
+    // slots of the two CSR rows, which start at row_ptr[g0]
+    int32_t* out = ulist + row_ptr[g0];
     int cnt = 0;
     while (a < ae || b < be) {
       const int ja = a < ae ? cols[a] : INT_MAX;
       const int jb = b < be ? cols[b] : INT_MAX;
-      if (ja <= jb) ++a;
-      if (jb <= ja) ++b;
-      ++cnt;
+      const int j = ja < jb ? ja : jb;
+      int bits = 0;
+      if (ja == j) {
+        bits |= 1 | ((fflags[a] & kFlagFull) ? 2 : 0);
+        ++a;
+      }
+      if (jb == j) {
+        bits |= 4 | ((fflags[b] & kFlagFull) ? 8 : 0);
+        ++b;
+      }
+      out[cnt++] = (j << 4) | bits;
     }
     pcount[pid] = cnt;
   }
@@ -325,9 +337,9 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
       c, L.n_qtiles, L.n_ktiles, row_ptr, reinterpret_cast<int32_t*>(ws + L.cols),
       reinterpret_cast<uint8_t*>(ws + L.fflags), csc_ptr, reinterpret_cast<int32_t*>(ws + L.csc_rows),
       reinterpret_cast<uint8_t*>(ws + L.cflags));
-  pair_count_kernel<<<grid_for(L.n_pairs, 128, sms * 16), 128, 0, st>>>(
-      row_ptr, reinterpret_cast<const int32_t*>(ws + L.cols), L.nQt, L.nPairs, L.n_pairs,
-      reinterpret_cast<int32_t*>(ws + L.pcount));
+  pair_list_kernel<<<grid_for(L.n_pairs, 128, sms * 16), 128, 0, st>>>(
+      row_ptr, reinterpret_cast<const int32_t*>(ws + L.cols), reinterpret_cast<const uint8_t*>(ws + L.fflags),
+      L.nQt, L.nPairs, L.n_pairs, reinterpret_cast<int32_t*>(ws + L.pcount), reinterpret_cast<int32_t*>(ws + L.ulist));
   const int smem_bins = 12 * 1024;  // 48 KB of shared memory; larger histograms use the workspace
   const int maxc = (L.nKt > L.nQt ? L.nKt : L.nQt) + 1;
   const size_t smem = static_cast<size_t>(maxc <= smem_bins ? maxc : 0) * sizeof(int32_t);

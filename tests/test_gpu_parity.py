@@ -109,12 +109,47 @@ def read_tiles(scfa, ws, mode, B, H, Tq, Tk, D):
         "csc_ptr": csc_ptr, "csc_rows": arr(tv.csc_rows, int(csc_ptr[-1]), np.int32),
         "cflags": arr(tv.cflags, int(csc_ptr[-1]), np.uint8),
         "work_fwd": arr(tv.work_fwd, nq, np.int32), "work_bwd": arr(tv.work_bwd, nk, np.int32),
+        "pair_count": arr(tv.pair_count, B * H * ((tv.n_q_tiles + 1) // 2), np.int32),
+        "pair_list": arr(tv.pair_list, nl, np.int32),
+        "work_pairs": arr(tv.work_pairs, B * H * ((tv.n_q_tiles + 1) // 2), np.int32),
+        "nQt": tv.n_q_tiles,
     }
+
+
+def expected_pairs(ref, nQt):
+    """Union lists of query-tile pairs (2m, 2m + 1), merged from the oracle's
+    CSR rows, and the pair order (union size descending, id ascending)."""
+    row_ptr, cols, ff = ref["row_ptr"], ref["cols"], ref["fflags"]
+    BH = (len(row_ptr) - 1) // nQt
+    nP = (nQt + 1) // 2
+    counts, lists = [], {}
+    for bh in range(BH):
+        for m in range(nP):
+            ent = {}
+            for g in range(2):
+                i = 2 * m + g
+                if i >= nQt:
+                    continue
+                r = bh * nQt + i
+                for c, f in zip(cols[row_ptr[r]:row_ptr[r + 1]], ff[row_ptr[r]:row_ptr[r + 1]]):
+                    ent[int(c)] = ent.get(int(c), 0) | ((1 | (2 if f & 1 else 0)) << (2 * g))
+            lists[bh * nP + m] = [(c << 4) | b for c, b in sorted(ent.items())]
+            counts.append(len(ent))
+    order = sorted(range(len(counts)), key=lambda q: (-counts[q], q))
+    return np.array(counts, np.int32), lists, np.array(order, np.int32)
 
 
 def compare_tiles(got, ref):
     for key in ("row_ptr", "cols", "fflags", "csc_ptr", "csc_rows", "cflags", "work_fwd", "work_bwd"):
         np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+    nQt = got["nQt"]
+    counts, lists, order = expected_pairs(ref, nQt)
+    np.testing.assert_array_equal(got["pair_count"], counts, err_msg="pair_count")
+    np.testing.assert_array_equal(got["work_pairs"], order, err_msg="work_pairs")
+    nP = (nQt + 1) // 2
+    for pid, want in lists.items():
+        start = ref["row_ptr"][(pid // nP) * nQt + 2 * (pid % nP)]
+        np.testing.assert_array_equal(got["pair_list"][start:start + len(want)], want, err_msg=f"pair_list {pid}")
 
 
 @pytest.mark.parametrize("T,keep", [(1000, 0.7), (3000, 0.3), (8192, 0.7)])
