@@ -60,8 +60,8 @@ struct __align__(1024) BwdSmem {
   uint8_t dqs[kSubBytes];         // dQ fp32 staging: one [128 rows x 32 floats] swizzled half at a time
   int32_t qidx[kQStages][kTile];
   int32_t qhash[kQStages][kTile];
-  float lse2[kQStages][kTile];    // LSE * log2(e)
-  float drs[kQStages][kTile];     // rowsum(dO * O) * scale
+  float lse2[kQStages][kTile];    // -LSE * log2(e)
+  float drs[kQStages][kTile];     // -rowsum(dO * O) * scale
   uint64_t kv_full, kv_empty;
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t s_full, st_empty, ds_full, pt_free, ds_free[2], dq_full, dq_empty, dkv_full, dkv_empty, drain;
@@ -202,8 +202,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int c = lane + 32 * u;
             sm.qidx[s][c] = qid[u];
             sm.qhash[s][c] = qhv[u];
-            sm.lse2[s][c] = lsev[u] * kLog2e;
-            sm.drs[s][c] = drv[u] * p.scale;
+            sm.lse2[s][c] = -(lsev[u] * kLog2e);
+            sm.drs[s][c] = -(drv[u] * p.scale);
           }
         }
         __threadfence_block();
@@ -368,7 +368,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float* drs = sm.drs[s] + grp * 64;
         const int* qid = sm.qidx[s] + grp * 64;
         const int* qhs = sm.qhash[s] + grp * 64;
-        // one 32-query chunk: P^T and dS^T as packed bf16 pairs
+        // one 32-query chunk: P^T and dS^T as packed bf16 pairs. The
+        // arithmetic runs on packed f32 pairs (same operations and rounding
+        // as the scalar form); tiles not flagged FULL then zero the pairs
+        // that are not admissible.
+        const uint64_t sl2 = f2(p.scale_log2, p.scale_log2), sc2 = f2(p.scale, p.scale);
         auto chunk = [&](int c, const uint32_t (&sr)[32], const uint32_t (&dr)[32], uint32_t (&pk)[16],
                          uint32_t (&dk16)[16]) {
 #pragma unroll
@@ -376,36 +380,40 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int e = e4 * 4;
             const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 32 + e);
             const float4 d4 = *reinterpret_cast<const float4*>(drs + c * 32 + e);
-            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dv[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float pe = ex2_approx(fmaf(__uint_as_float(sr[e + u]), p.scale_log2, -la[u]));
-              pv[u] = pe;
-              dv[u] = pe * fmaf(__uint_as_float(dr[e + u]), p.scale, -da[u]);
+            for (int u = 0; u < 4; u += 2) {
+              const uint64_t nl = u == 0 ? f2(l4.x, l4.y) : f2(l4.z, l4.w);
+              const uint64_t nd = u == 0 ? f2(d4.x, d4.y) : f2(d4.z, d4.w);
+              float a0, a1;
+              f2_split(fma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2, nl), a0, a1);
+              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+              const uint64_t t = fma2(f2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])), sc2, nd);
+              float d0, d1;
+              f2_split(mul2(f2(p0, p1), t), d0, d1);
+              pk[e4 * 2 + u / 2] = pack_bf16x2(p0, p1);
+              dk16[e4 * 2 + u / 2] = pack_bf16x2(d0, d1);
             }
-            if (!full) {
+          }
+          if (!full) {
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const int e = e4 * 4;
               const int4 q4 = *reinterpret_cast<const int4*>(qid + c * 32 + e);
-              const int qa[4] = {q4.x, q4.y, q4.z, q4.w};
-              int ha[4] = {0, 0, 0, 0};
+              bool adm[4] = {q4.x >= ki, q4.y >= ki, q4.z >= ki, q4.w >= ki};
               if (p.mode == SCFA_MODE_HASH) {
                 const int4 h4 = *reinterpret_cast<const int4*>(qhs + c * 32 + e);
-                ha[0] = h4.x; ha[1] = h4.y; ha[2] = h4.z; ha[3] = h4.w;
+                adm[0] = adm[0] && h4.x == kh;
+                adm[1] = adm[1] && h4.y == kh;
+                adm[2] = adm[2] && h4.z == kh;
+                adm[3] = adm[3] && h4.w == kh;
               }
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const bool adm = qa[u] >= ki && (p.mode != SCFA_MODE_HASH || ha[u] == kh);
-                if (!adm) {
-                  pv[u] = 0.f;
-                  dv[u] = 0.f;
-                }
+              for (int u = 0; u < 4; u += 2) {
+                const uint32_t keep = (adm[u] ? 0x0000ffffu : 0u) | (adm[u + 1] ? 0xffff0000u : 0u);
+                pk[e4 * 2 + u / 2] &= keep;
+                dk16[e4 * 2 + u / 2] &= keep;
               }
             }
-            pk[e4 * 2] = pack_bf16x2(pv[0], pv[1]);
-            pk[e4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-            dk16[e4 * 2] = pack_bf16x2(dv[0], dv[1]);
-            dk16[e4 * 2 + 1] = pack_bf16x2(dv[2], dv[3]);
           }
         };
         uint32_t pk[2][16], dsk[2][16];
