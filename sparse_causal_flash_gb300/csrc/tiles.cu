@@ -109,11 +109,13 @@ __device__ __forceinline__ void partner_range(const TileCtx& c, bool by_q, const
   if (self.w == INT_MAX) *hi = n;
 }
 
-// One thread per query tile (first B*H*nQt ids) or key tile (next B*H*nKt).
+// One warp per query tile (first B*H*nQt ids) or key tile (next B*H*nKt):
+// the lanes test 32 partner tiles at a time.
 __global__ void tile_count_kernel(TileCtx c, long long n_q, long long n_k,
                                   int32_t* __restrict__ qcount, int32_t* __restrict__ kcount) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n_q + n_k; t += stride) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < n_q + n_k; t += warps) {
     const bool by_q = t < n_q;
     const long long id = by_q ? t : t - n_q;
     const int nself = by_q ? c.nQt : c.nKt;
@@ -121,12 +123,18 @@ __global__ void tile_count_kernel(TileCtx c, long long n_q, long long n_k,
     const int4 self = (by_q ? c.qstat : c.kstat)[id];
     int lo, hi;
     partner_range(c, by_q, self, bh, &lo, &hi);
+    const int4* other = (by_q ? c.kstat : c.qstat) + bh * (by_q ? c.nKt : c.nQt);
     int cnt = 0;
-    for (int p = lo; p < hi; ++p) {
-      const int4 other = (by_q ? c.kstat : c.qstat)[bh * (by_q ? c.nKt : c.nQt) + p];
-      cnt += by_q ? tile_live(c, self, other) : tile_live(c, other, self);
+    for (int p0 = lo; p0 < hi; p0 += 32) {
+      const int p = p0 + lane;
+      bool live = false;
+      if (p < hi) {
+        const int4 o = other[p];
+        live = by_q ? tile_live(c, self, o) : tile_live(c, o, self);
+      }
+      cnt += __popc(__ballot_sync(0xffffffffu, live));
     }
-    (by_q ? qcount : kcount)[id] = cnt;
+    if (lane == 0) (by_q ? qcount : kcount)[id] = cnt;
   }
 }
 
@@ -172,13 +180,16 @@ __global__ void tile_scan_kernel(const int32_t* __restrict__ qcount, long long n
   }
 }
 
+// One warp per tile, as the count pass: live partners are written in
+// ascending order at ballot prefix positions.
 __global__ void tile_fill_kernel(TileCtx c, long long n_q, long long n_k,
                                  const int32_t* __restrict__ row_ptr, int32_t* __restrict__ cols,
                                  uint8_t* __restrict__ fflags,
                                  const int32_t* __restrict__ csc_ptr, int32_t* __restrict__ csc_rows,
                                  uint8_t* __restrict__ cflags) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n_q + n_k; t += stride) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < n_q + n_k; t += warps) {
     const bool by_q = t < n_q;
     const long long id = by_q ? t : t - n_q;
     const int nself = by_q ? c.nQt : c.nKt;
@@ -187,61 +198,93 @@ __global__ void tile_fill_kernel(TileCtx c, long long n_q, long long n_k,
     const int4 self = (by_q ? c.qstat : c.kstat)[id];
     int lo, hi;
     partner_range(c, by_q, self, bh, &lo, &hi);
+    const int4* other = (by_q ? c.kstat : c.qstat) + bh * (by_q ? c.nKt : c.nQt);
     long long pos = by_q ? row_ptr[id] : csc_ptr[id];
-    for (int p = lo; p < hi; ++p) {
-      const int4 other = (by_q ? c.kstat : c.qstat)[bh * (by_q ? c.nKt : c.nQt) + p];
-      const int4 qs = by_q ? self : other;
-      const int4 ks = by_q ? other : self;
-      if (!tile_live(c, qs, ks)) continue;
-      const uint8_t f = tile_full(c, by_q ? me : p, by_q ? p : me, qs, ks) ? kFlagFull : 0;
-      if (by_q) {
-        cols[pos] = p;
-        fflags[pos] = f;
-      } else {
-        csc_rows[pos] = p;
-        cflags[pos] = f;
+    for (int p0 = lo; p0 < hi; p0 += 32) {
+      const int p = p0 + lane;
+      bool live = false;
+      uint8_t f = 0;
+      if (p < hi) {
+        const int4 o = other[p];
+        const int4 qs = by_q ? self : o;
+        const int4 ks = by_q ? o : self;
+        live = tile_live(c, qs, ks);
+        f = tile_full(c, by_q ? me : p, by_q ? p : me, qs, ks) ? kFlagFull : 0;
       }
-      ++pos;
+      const unsigned m = __ballot_sync(0xffffffffu, live);
+      if (live) {
+        const long long at = pos + __popc(m & ((1u << lane) - 1u));
+        if (by_q) {
+          cols[at] = p;
+          fflags[at] = f;
+        } else {
+          csc_rows[at] = p;
+          cflags[at] = f;
+        }
+      }
+      pos += __popc(m);
     }
   }
 }
 
-// Live-list union size of each query-tile pair (2m, 2m + 1): a merge count of
-// the two ascending CSR rows.
+// Union list of each query-tile pair (2m, 2m + 1), one warp per pair. Both
+// CSR rows are strictly ascending; an entry's place in the union is its index
+// in its own row, plus the entries of the other row below it (binary search),
+// minus the columns common to both rows below it (a running ballot count in
+// row order). A common column is written once, from row 2m.
 __global__ void pair_list_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ cols,
                                  const uint8_t* __restrict__ fflags, int nQt, int nPairs, long long n_pairs,
                                  int32_t* __restrict__ pcount, int32_t* __restrict__ ulist) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long pid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; pid < n_pairs; pid += stride) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long pid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; pid < n_pairs;
+       pid += warps) {
     const long long bh = pid / nPairs;
     const int m = static_cast<int>(pid % nPairs);
     const long long g0 = bh * nQt + 2 * m;
-    int a = row_ptr[g0], ae = row_ptr[g0 + 1];
-    int b = 0, be = 0;
-    if (2 * m + 1 < nQt) {
-      b = row_ptr[g0 + 1];
-      be = row_ptr[g0 + 2];
-    }
-    // the union is no longer than the two lists together, so it fits in the
-    // slots of the two CSR rows, which start at row_ptr[g0]
-    int32_t* out = ulist + row_ptr[g0];
-    int cnt = 0;
-    while (a < ae || b < be) {
-      const int ja = a < ae ? cols[a] : INT_MAX;
-      const int jb = b < be ? cols[b] : INT_MAX;
-      const int j = ja < jb ? ja : jb;
-      int bits = 0;
-      if (ja == j) {
-        bits |= 1 | ((fflags[a] & kFlagFull) ? 2 : 0);
-        ++a;
+    const int a0 = row_ptr[g0], na = row_ptr[g0 + 1] - a0;
+    const bool has1 = 2 * m + 1 < nQt;
+    const int b0 = has1 ? row_ptr[g0 + 1] : 0, nb = has1 ? row_ptr[g0 + 2] - b0 : 0;
+    const int32_t* A = cols + a0;
+    const int32_t* Bc = cols + b0;
+    // the union is no longer than the two rows together, so it fits in their
+    // slots, which start at row_ptr[g0]
+    int32_t* out = ulist + a0;
+    int common = 0;
+    for (int c0 = 0; c0 < na; c0 += 32) {
+      const int ia = c0 + lane;
+      bool both = false;
+      int x = 0, kb = 0;
+      if (ia < na) {
+        x = A[ia];
+        kb = lower_bound_by(nb, x, [&](int t) { return Bc[t]; });
+        both = kb < nb && Bc[kb] == x;
       }
-      if (jb == j) {
-        bits |= 4 | ((fflags[b] & kFlagFull) ? 8 : 0);
-        ++b;
+      const unsigned mk = __ballot_sync(0xffffffffu, both);
+      if (ia < na) {
+        int bits = 1 | ((fflags[a0 + ia] & kFlagFull) ? 2 : 0);
+        if (both) bits |= 4 | ((fflags[b0 + kb] & kFlagFull) ? 8 : 0);
+        out[ia + kb - (common + __popc(mk & lt))] = (x << 4) | bits;
       }
-      out[cnt++] = (j << 4) | bits;
+      common += __popc(mk);
     }
-    pcount[pid] = cnt;
+    int common_b = 0;
+    for (int c0 = 0; c0 < nb; c0 += 32) {
+      const int ib = c0 + lane;
+      bool both = false;
+      int y = 0, ka = 0;
+      if (ib < nb) {
+        y = Bc[ib];
+        ka = lower_bound_by(na, y, [&](int t) { return A[t]; });
+        both = ka < na && A[ka] == y;
+      }
+      const unsigned mk = __ballot_sync(0xffffffffu, both);
+      if (ib < nb && !both)
+        out[ib + ka - (common_b + __popc(mk & lt))] = (y << 4) | 4 | ((fflags[b0 + ib] & kFlagFull) ? 8 : 0);
+      common_b += __popc(mk);
+    }
+    if (lane == 0) pcount[pid] = na + nb - common;
   }
 }
 
@@ -253,10 +296,13 @@ struct OrderList {
   int32_t* gcur;
 };
 
+constexpr int kOrderChunk = 4096;  // counts staged in shared memory per scatter round
+
 // Stable counting sort of ids by count, descending: block 0 builds the
 // forward order (query tiles), block 1 the backward order (key tiles), block
 // 2 the order of query-tile pairs. The whole block histograms; warp 0 scans
-// and scatters in id order (stable by construction).
+// and scatters in id order (stable by construction), reading the counts from
+// shared memory, where the whole block stages them one chunk at a time.
 __global__ void work_order_kernel(OrderList l0, OrderList l1, OrderList l2, int smem_bins) {
   extern __shared__ int32_t scur[];
   const OrderList L = blockIdx.x == 0 ? l0 : (blockIdx.x == 1 ? l1 : l2);
@@ -265,39 +311,48 @@ __global__ void work_order_kernel(OrderList l0, OrderList l1, OrderList l2, int 
   const int maxc = L.maxc;
   int32_t* out = L.out;
   int32_t* cur = (maxc + 1 <= smem_bins) ? scur : L.gcur;
+  int32_t* chunk = scur + smem_bins;
   for (int cc = threadIdx.x; cc <= maxc; cc += blockDim.x) cur[cc] = 0;
   __syncthreads();
   for (long long i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&cur[min(max(cnt[i], 0), maxc)], 1);
   __syncthreads();
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  // start[c] = number of ids with a larger count
-  int running = 0;
-  for (int base = maxc; base >= 0; base -= 32) {
-    const int cc = base - lane;
-    const int v = cc >= 0 ? cur[cc] : 0;
-    int x = v;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    // start[c] = number of ids with a larger count
+    int running = 0;
+    for (int base = maxc; base >= 0; base -= 32) {
+      const int cc = base - lane;
+      const int v = cc >= 0 ? cur[cc] : 0;
+      int x = v;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (cc >= 0) cur[cc] = running + x - v;
+      running += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (cc >= 0) cur[cc] = running + x - v;
-    running += __shfl_sync(0xffffffffu, x, 31);
   }
-  __syncwarp();
-  for (long long base = 0; base < n; base += 32) {
-    const long long i = base + lane;
-    const bool active = i < n;
-    const int cc = active ? min(max(cnt[i], 0), maxc) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, cc);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    const int start = active ? cur[cc] : 0;
-    __syncwarp();
-    if (active) {
-      out[start + rank] = static_cast<int32_t>(i);
-      if (rank == 0) cur[cc] = start + __popc(peers);
+  for (long long c0 = 0; c0 < n; c0 += kOrderChunk) {
+    const int len = static_cast<int>(min(static_cast<long long>(kOrderChunk), n - c0));
+    __syncthreads();  // the previous chunk is scattered (and the scan above is done)
+    for (int t = threadIdx.x; t < len; t += blockDim.x) chunk[t] = min(max(cnt[c0 + t], 0), maxc);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      for (int base = 0; base < len; base += 32) {
+        const int t = base + lane;
+        const bool active = t < len;
+        const int cc = active ? chunk[t] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, cc);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        const int start = active ? cur[cc] : 0;
+        __syncwarp();
+        if (active) {
+          out[start + rank] = static_cast<int32_t>(c0 + t);
+          if (rank == 0) cur[cc] = start + __popc(peers);
+        }
+        __syncwarp();
+      }
     }
-    __syncwarp();
   }
 }
 
@@ -331,18 +386,26 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
       mode, k_idx, k_hash, L.n_ktiles, Tk, L.nKt, kstat);
   TileCtx c{mode, flags, Tq, Tk, L.nQt, L.nKt, qstat, kstat};
   const long long nt = L.n_qtiles + L.n_ktiles;
-  tile_count_kernel<<<grid_for(nt, 128, sms * 16), 128, 0, st>>>(c, L.n_qtiles, L.n_ktiles, qcount, kcount);
+  tile_count_kernel<<<grid_for(nt * 32, 256, sms * 8), 256, 0, st>>>(c, L.n_qtiles, L.n_ktiles, qcount, kcount);
   tile_scan_kernel<<<2, 1024, 0, st>>>(qcount, L.n_qtiles, row_ptr, kcount, L.n_ktiles, csc_ptr, hdr);
-  tile_fill_kernel<<<grid_for(nt, 128, sms * 16), 128, 0, st>>>(
+  tile_fill_kernel<<<grid_for(nt * 32, 256, sms * 8), 256, 0, st>>>(
       c, L.n_qtiles, L.n_ktiles, row_ptr, reinterpret_cast<int32_t*>(ws + L.cols),
       reinterpret_cast<uint8_t*>(ws + L.fflags), csc_ptr, reinterpret_cast<int32_t*>(ws + L.csc_rows),
       reinterpret_cast<uint8_t*>(ws + L.cflags));
-  pair_list_kernel<<<grid_for(L.n_pairs, 128, sms * 16), 128, 0, st>>>(
+  pair_list_kernel<<<grid_for(L.n_pairs * 32, 256, sms * 8), 256, 0, st>>>(
       row_ptr, reinterpret_cast<const int32_t*>(ws + L.cols), reinterpret_cast<const uint8_t*>(ws + L.fflags),
       L.nQt, L.nPairs, L.n_pairs, reinterpret_cast<int32_t*>(ws + L.pcount), reinterpret_cast<int32_t*>(ws + L.ulist));
   const int smem_bins = 12 * 1024;  // 48 KB of shared memory; larger histograms use the workspace
-  const int maxc = (L.nKt > L.nQt ? L.nKt : L.nQt) + 1;
-  const size_t smem = static_cast<size_t>(maxc <= smem_bins ? maxc : 0) * sizeof(int32_t);
+  const size_t smem = static_cast<size_t>(smem_bins + kOrderChunk) * sizeof(int32_t);
+  static bool order_smem_set[64] = {};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !order_smem_set[dev]) {
+    e = cudaFuncSetAttribute(work_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) order_smem_set[dev] = true;
+  }
   int32_t* gcur = reinterpret_cast<int32_t*>(ws + L.cursor);
   OrderList lf{qcount, L.n_qtiles, L.nKt, reinterpret_cast<int32_t*>(ws + L.work_fwd), gcur};
   OrderList lb{kcount, L.n_ktiles, L.nQt, reinterpret_cast<int32_t*>(ws + L.work_bwd), gcur + L.nKt + 1};
