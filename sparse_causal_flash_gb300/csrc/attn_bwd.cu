@@ -149,7 +149,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------ producer warp
     int q_it = 0, item = 0, last_kv = -1;
-    for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+    for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
       const int g = p.work[w / kHalves];  // both halves load all of K, V, Q, dO
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
       if (n == 0) continue;
@@ -258,7 +258,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_commit(&sm.s_full);
         return true;
       };
-      for (int w = blockIdx.x; w < p.n_work && ok; w += gridDim.x) {
+      for (int rnd = 0, w = work_item(0); w < p.n_work && ok; w = work_item(++rnd)) {
         const int g = p.work[w / kHalves];
         const int hh = w % kHalves;
         const int n = p.csc_ptr[g + 1] - p.csc_ptr[g];
@@ -335,7 +335,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int kr = quarter * 32 + lane;    // key row = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0, q_it = 0, item = 0;
-    for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+    for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
       const int g = p.work[w / kHalves];
       const int hh = w % kHalves;  // which 64-column half of D
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
@@ -477,7 +477,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int tid = threadIdx.x - 320;   // 0..127
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0;
-    for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+    for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
       const int g = p.work[w / kHalves];
       const int hh = w % kHalves;  // which 64-column half of D
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;

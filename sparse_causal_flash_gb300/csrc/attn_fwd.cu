@@ -89,6 +89,8 @@ struct FwdParams {
   const int32_t* pcount;
   const int32_t* ulist;
   int n_pairs;
+  const int32_t* work;   // query tiles by live count descending (single-tile kernel)
+  int n_work;
   uint16_t* o;
   float* lse;
   int* status;
@@ -139,7 +141,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int kv_it = 0, item = 0, last_q = -1;
-      for (int w = blockIdx.x; w < p.n_pairs; w += gridDim.x) {
+      for (int rnd = 0, w = work_item(0); w < p.n_pairs; w = work_item(++rnd)) {
         const int pid = p.work_pairs[w];
         const int cnt = p.pcount[pid];
         if (cnt == 0) continue;
@@ -215,7 +217,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ++n_s;
         return true;
       };
-      for (int w = blockIdx.x; w < p.n_pairs && ok; w += gridDim.x) {
+      for (int rnd = 0, w = work_item(0); w < p.n_pairs && ok; w = work_item(++rnd)) {
         const int pid = p.work_pairs[w];
         const int cnt = p.pcount[pid];
         if (cnt == 0) continue;
@@ -292,7 +294,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t colP = kSepP ? 384u + 64u * grp : colS;
     int n_p = 0;  // P_g tiles written so far
     int s_it = 0, o_it = 0;
-    for (int w = blockIdx.x; w < p.n_pairs; w += gridDim.x) {
+    for (int rnd = 0, w = work_item(0); w < p.n_pairs; w = work_item(++rnd)) {
       const int pid = p.work_pairs[w];
       const int bh = pid / p.nPairs, m = pid % p.nPairs;
       const int i = 2 * m + grp;
@@ -499,6 +501,381 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+
+// ---------------------------------------------------------------------------
+// Single-query-tile forward for D = 64: two CTAs per SM, each walking its own
+// query tiles, so the two tiles an SM works on never wait on one another.
+// Roles (192 threads): warp 0 producer (TMA: Q double-buffered, K and V in
+// separate 2-stage rings so a K stage is released as soon as S has read it),
+// warp 1 MMA issuer and TMEM owner (256 columns: S [0,128), O [128,192),
+// P [192,256)), warps 2-5 softmax (thread = query row = TMEM lane). S(j+1) is
+// computed while the softmax works on S(j): the softmax frees S once it is in
+// registers and waits for PV(j-1) before overwriting P.
+// ---------------------------------------------------------------------------
+constexpr int kF1Threads = 192;
+constexpr int kF1Stages = 2;
+constexpr uint32_t kF1TmemCols = 256;
+
+struct __align__(1024) Fwd1Smem {
+  uint8_t q[2][kSubBytes];
+  uint8_t k[kF1Stages][kSubBytes];
+  uint8_t v[kF1Stages][kSubBytes];
+  int32_t kidx[2][kTile];
+  int32_t khash[2][kTile];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[kF1Stages], k_empty[kF1Stages], v_full[kF1Stages], v_empty[kF1Stages];
+  uint64_t s_full, s_free, p_full, pv_done, o_full, o_empty, kbar, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(kF1Threads, 2)
+attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  constexpr int D = 64;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  Fwd1Smem& sm = *reinterpret_cast<Fwd1Smem*>(smem_raw + pad);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.q_full[b], 1);
+      mbar_init(&sm.q_empty[b], 1);
+    }
+    for (int s = 0; s < kF1Stages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_free, 128);
+    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.pv_done, 1);
+    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.o_empty, 128);
+    mbar_init(&sm.kbar, 128);
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, kF1TmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+  constexpr uint32_t kColS = 0, kColO = 128, kColP = 192;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int item = 0, kv = 0;
+      for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
+        const int g = p.work[w];
+        const int e0 = p.row_ptr[g], n = p.row_ptr[g + 1] - e0;
+        if (n == 0) continue;
+        const int bh = g / p.nQt, i = g % p.nQt;
+        const int qb = item & 1;
+        if (!mbar_wait(&sm.q_empty[qb], ((item >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&sm.q_full[qb], D * kTile * 2);
+        tma_load_3d(sm.q[qb], &tm_q, &sm.q_full[qb], 0, i * kTile, bh);
+        bool ok = true;
+        for (int t = 0; t < n; ++t) {
+          const int j = p.cols[e0 + t];
+          const int s = kv % kF1Stages;
+          const uint32_t ph = ((kv / kF1Stages) & 1) ^ 1;
+          if (!mbar_wait(&sm.k_empty[s], ph, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.k_full[s], D * kTile * 2);
+          tma_load_3d(sm.k[s], &tm_k, &sm.k_full[s], 0, j * kTile, bh);
+          if (!mbar_wait(&sm.v_empty[s], ph, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.v_full[s], D * kTile * 2);
+          tma_load_3d(sm.v[s], &tm_v, &sm.v_full[s], 0, j * kTile, bh);
+          ++kv;
+        }
+        if (!ok) break;
+        ++item;
+      }
+      // drain: every copy issued by this thread has landed before the CTA exits
+      for (int d = 1; d <= kF1Stages && d <= kv; ++d) {
+        const int it = kv - d;
+        mbar_wait(&sm.k_full[it % kF1Stages], (it / kF1Stages) & 1, abort_flag, p.status);
+        mbar_wait(&sm.v_full[it % kF1Stages], (it / kF1Stages) & 1, abort_flag, p.status);
+      }
+      for (int d = 1; d <= 2 && d <= item; ++d) {
+        const int it = item - d;
+        mbar_wait(&sm.q_full[it & 1], (it >> 1) & 1, abort_flag, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kTile, D, 0, 1);
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t kdesc = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t vdesc = smem_desc_sw128(smem_u32(sm.v[0]), kSubBytes, 1024);
+      constexpr uint32_t kBuf16 = kSubBytes >> 4;
+      int item = 0, kv = 0, n_s = 0, p_it = 0, o_it = 0;
+      bool ok = true;
+      auto issue_s = [&](int kvi, int qb) -> bool {
+        const int s = kvi % kF1Stages;
+        if (n_s > 0 && !mbar_wait(&sm.s_free, (n_s - 1) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&sm.k_full[s], (kvi / kF1Stages) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint64_t a = qdesc + static_cast<uint64_t>(qb * kBuf16);
+        const uint64_t b = kdesc + static_cast<uint64_t>(s * kBuf16);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + kColS, a + kstep_off16(kk, kSubBytes), b + kstep_off16(kk, kSubBytes), idesc_s, kk > 0);
+        tc_commit(&sm.s_full);
+        tc_commit(&sm.k_empty[s]);  // K stage free once S has read it
+        ++n_s;
+        return true;
+      };
+      for (int rnd = 0, w = work_item(0); w < p.n_work && ok; w = work_item(++rnd)) {
+        const int g = p.work[w];
+        const int n = p.row_ptr[g + 1] - p.row_ptr[g];
+        if (n == 0) continue;
+        const int qb = item & 1;
+        if (!mbar_wait(&sm.q_full[qb], (item >> 1) & 1, abort_flag, p.status)) break;
+        if (!issue_s(kv, qb)) break;
+        for (int t = 0; t < n; ++t) {
+          const int s = kv % kF1Stages;
+          if (t + 1 < n && !issue_s(kv + 1, qb)) { ok = false; break; }
+          if (!mbar_wait(&sm.p_full, p_it & 1, abort_flag, p.status)) { ok = false; break; }
+          if (t == 0 && !mbar_wait(&sm.o_empty, (o_it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(&sm.v_full[s], (kv / kF1Stages) & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t vb = vdesc + static_cast<uint64_t>(s * kBuf16);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8, vb + static_cast<uint64_t>(kk * 128), idesc_o,
+                        (kk > 0 || t > 0) ? 1u : 0u);
+          tc_commit(&sm.pv_done);
+          tc_commit(&sm.v_empty[s]);
+          ++kv;
+          ++p_it;
+        }
+        if (!ok) break;
+        tc_commit(&sm.o_full);
+        tc_commit(&sm.q_empty[qb]);
+        ++o_it;
+        ++item;
+      }
+      tc_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0, abort_flag, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroup
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;          // row of the tile = TMEM lane
+    const int tid = (warp - 2) * 32 + lane;     // 0..127
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    int s_it = 0, o_it = 0, x_it = 0;
+    // the 128 softmax threads; a bounded wait (a broken pipeline ends in a
+    // status code, not a hang)
+    auto group_sync = [&]() -> bool {
+      mbar_arrive(&sm.kbar);
+      const bool r_ok = mbar_wait(&sm.kbar, x_it & 1, abort_flag, p.status);
+      ++x_it;
+      return __all_sync(0xffffffffu, r_ok);
+    };
+    for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
+      const int g = p.work[w];
+      const int e_beg = p.row_ptr[g], e_end = p.row_ptr[g + 1];
+      const int bh = g / p.nQt, i = g % p.nQt;
+      const int row = i * kTile + r;
+      const bool valid = row < p.Tq;
+      const long long grow = static_cast<long long>(bh) * p.Tq + row;
+      int qi = INT_MIN, qh = 0;
+      if (valid) {
+        qi = (p.mode == SCFA_MODE_DENSE) ? row : p.q_idx[grow];
+        if (p.mode == SCFA_MODE_HASH) qh = p.q_hash[grow];
+      }
+      const long long kbase = static_cast<long long>(bh) * p.Tk;
+      // key index / bucket of a masked tile, one per thread
+      auto key_meta = [&](int j, int f, int& kid, int& kh) {
+        kid = INT_MAX;
+        kh = INT_MIN;
+        if (f & kFlagFull) return;
+        const int col = j * kTile + tid;
+        const bool kvv = col < p.Tk;
+        if (p.mode == SCFA_MODE_DENSE) kid = kvv ? col : INT_MAX;
+        else kid = kvv ? p.k_idx[kbase + col] : INT_MAX;
+        if (p.mode == SCFA_MODE_HASH) kh = kvv ? p.k_hash[kbase + col] : INT_MIN;
+      };
+      // column / flag two tiles ahead, key metadata one tile ahead
+      int f_c = 0, j_n = 0, f_n = 0, kid_c = INT_MAX, kh_c = INT_MIN;
+      if (e_beg < e_end) {
+        f_c = p.fflags[e_beg];
+        key_meta(p.cols[e_beg], f_c, kid_c, kh_c);
+      }
+      if (e_beg + 1 < e_end) {
+        j_n = p.cols[e_beg + 1];
+        f_n = p.fflags[e_beg + 1];
+      }
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true, any = false;
+      for (int e = e_beg; e < e_end; ++e) {
+        const bool full = (f_c & kFlagFull) != 0;
+        int kid_n = INT_MAX, kh_n = INT_MIN, j_nn = 0, f_nn = 0;
+        if (e + 1 < e_end) key_meta(j_n, f_n, kid_n, kh_n);
+        if (e + 2 < e_end) {
+          j_nn = p.cols[e + 2];
+          f_nn = p.fflags[e + 2];
+        }
+        const bool first_tile = !any;
+        any = true;
+        const int b = s_it & 1;
+        if (!full) {
+          sm.kidx[b][tid] = kid_c;
+          if (p.mode == SCFA_MODE_HASH) sm.khash[b][tid] = kh_c;
+          if (!group_sync()) { ok = false; break; }
+        }
+        ok = mbar_wait(&sm.s_full, s_it & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[kTile];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          tmem_ld32(lane_base + kColS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+        tmem_wait_ld();
+        // S is in registers: the MMA warp may compute the next S
+        tc_fence_before();
+        mbar_arrive(&sm.s_free);
+        if (!full) {
+#pragma unroll
+          for (int c4 = 0; c4 < kTile / 4; ++c4) {
+            const int4 k4 = *reinterpret_cast<const int4*>(&sm.kidx[b][c4 * 4]);
+            bool adm[4] = {qi >= k4.x, qi >= k4.y, qi >= k4.z, qi >= k4.w};
+            if (p.mode == SCFA_MODE_HASH) {
+              const int4 h4 = *reinterpret_cast<const int4*>(&sm.khash[b][c4 * 4]);
+              adm[0] = adm[0] && qh == h4.x;
+              adm[1] = adm[1] && qh == h4.y;
+              adm[2] = adm[2] && qh == h4.z;
+              adm[3] = adm[3] && qh == h4.w;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (!adm[u]) sr[c4 * 4 + u] = 0xff800000u;  // -inf
+          }
+        }
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+        for (int c = 4; c < kTile; c += 8) {
+          mx0 = max3f(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+          mx1 = max3f(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+          mx2 = max3f(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+          mx3 = max3f(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+        }
+        const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+        const float m_new = fmaxf(m_used, mt);
+        const bool resc = m_new > m_used + kRescaleThreshold;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2_approx(m_used - m_new);
+          m_used = m_new;
+        }
+        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+        const uint64_t sl2 = f2(p.scale_log2, p.scale_log2), nm2 = f2(-msub, -msub);
+        if (s_it > 0) {
+          // the previous PV has read P (and finished adding into O)
+          ok = mbar_wait(&sm.pv_done, (s_it - 1) & 1, abort_flag, p.status);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+        }
+        uint64_t rsum2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const uint64_t arg = fma2(f2(__uint_as_float(sr[h * 32 + c]), __uint_as_float(sr[h * 32 + c + 1])), sl2, nm2);
+            float a0, a1;
+            f2_split(arg, a0, a1);
+            const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+            rsum2[(c >> 1) & 3] = add2(rsum2[(c >> 1) & 3], f2(e0, e1));
+            pk[c >> 1] = pack_bf16x2(e0, e1);
+          }
+          tmem_st16(lane_base + kColP + h * 16, pk);
+        }
+        const uint64_t rs2 = add2(add2(rsum2[0], rsum2[1]), add2(rsum2[2], rsum2[3]));
+        float rs_lo, rs_hi;
+        f2_split(rs2, rs_lo, rs_hi);
+        l = l * alpha + (rs_lo + rs_hi);
+        // rescale O (rare); the previous PV is complete (waited above)
+        if (!first_tile && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t orr[32];
+            tmem_ld32(lane_base + kColO + cc * 32, orr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e2 = 0; e2 < 32; ++e2) orr[e2] = __float_as_uint(__uint_as_float(orr[e2]) * alpha);
+            tmem_st32(lane_base + kColO + cc * 32, orr);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full);
+        ++s_it;
+        f_c = f_n;
+        kid_c = kid_n;
+        kh_c = kh_n;
+        j_n = j_nn;
+        f_n = f_nn;
+      }
+      if (!ok) break;
+      if (!any) {
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          p.lse[grow] = -INFINITY;
+        }
+        continue;
+      }
+      // epilogue: O / l, LSE
+      ok = mbar_wait(&sm.o_full, o_it & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint32_t orr[D / 32][32];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_base + kColO + cc * 32, orr[cc]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&sm.o_empty);
+      ++o_it;
+      if (valid) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const int e = c * 8;
+          uint4 u;
+          u.x = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 0) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 1) & 31]) * inv);
+          u.y = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 2) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 3) & 31]) * inv);
+          u.z = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 4) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 5) & 31]) * inv);
+          u.w = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 6) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 7) & 31]) * inv);
+          dst[c] = u;
+        }
+        p.lse[grow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kF1TmemCols);
+}
+
 }  // namespace
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, long long T, long long BH);
@@ -545,8 +922,48 @@ static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// D = 64: single-query-tile kernel, two CTAs per SM
+static cudaError_t launch_fwd1(const AttnArgs& a, cudaStream_t st) {
+  constexpr int D = 64;
+  const AttnWs& L = *a.L;
+  const long long BH = static_cast<long long>(a.B) * a.H;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, BH) || !make_tmap_bf16_3d(&tk, a.k, D, a.Tk, BH) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, BH))
+    return cudaErrorInvalidValue;
+  FwdParams p = {};
+  p.mode = a.mode;
+  p.Tq = a.Tq;
+  p.Tk = a.Tk;
+  p.nQt = L.nQt;
+  p.scale_log2 = a.scale * kLog2e;
+  p.q_idx = a.q_idx;
+  p.k_idx = a.k_idx;
+  p.q_hash = a.q_hash;
+  p.k_hash = a.k_hash;
+  p.row_ptr = reinterpret_cast<const int32_t*>(a.ws + L.row_ptr);
+  p.cols = reinterpret_cast<const int32_t*>(a.ws + L.cols);
+  p.fflags = reinterpret_cast<const uint8_t*>(a.ws + L.fflags);
+  p.work = reinterpret_cast<const int32_t*>(a.ws + L.work_fwd);
+  p.n_work = static_cast<int>(L.n_qtiles);
+  p.o = a.o_out;
+  p.lse = a.lse_out;
+  p.status = reinterpret_cast<int*>(a.ws + L.header);
+  const size_t smem = sizeof(Fwd1Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int grid = 2 * num_sms();
+  if (grid > p.n_work) grid = p.n_work;
+  if (grid < 1) grid = 1;
+  record_kernel_event(0, true, st);
+  attn_fwd1_kernel<<<grid, kF1Threads, smem, st>>>(tq, tk, tv, p);
+  record_kernel_event(0, false, st);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st) {
-  if (a.D == 64) return launch_fwd_d<64>(a, st);
+  if (a.D == 64) return launch_fwd1(a, st);
   if (a.D == 128) return launch_fwd_d<128>(a, st);
   return cudaErrorInvalidValue;
 }

@@ -82,6 +82,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Work item of round r for this CTA of a persistent grid walking a list sorted
+// by size, largest first: rounds alternate direction (CTA b takes item b of
+// round 0, item G - 1 - b of round 1, ...), so no CTA gets the largest item
+// of every round. Every role of a CTA calls it with the same r sequence.
+__device__ __forceinline__ int work_item(int r) {
+  const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  return r * G + ((r & 1) ? (G - 1 - b) : b);
+}
+
 // named barrier among `count` threads (ids 1..15; 0 is __syncthreads)
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
