@@ -91,6 +91,7 @@ struct FwdParams {
   int n_pairs;
   const int32_t* work;   // query tiles by live count descending (single-tile kernel)
   int n_work;
+  int* sched;            // [0] next item, [1] CTAs done (single-tile kernel)
   uint16_t* o;
   float* lse;
   int* status;
@@ -514,6 +515,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // ---------------------------------------------------------------------------
 constexpr int kF1Threads = 192;
 constexpr int kF1Stages = 2;
+constexpr int kF1Slots = 4;  // work items handed from the producer to the other roles
 constexpr uint32_t kF1TmemCols = 256;
 
 struct __align__(1024) Fwd1Smem {
@@ -522,6 +524,8 @@ struct __align__(1024) Fwd1Smem {
   uint8_t v[kF1Stages][kSubBytes];
   int32_t kidx[2][kTile];
   int32_t khash[2][kTile];
+  int32_t items[kF1Slots];
+  uint64_t item_full[kF1Slots], item_empty[kF1Slots];
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kF1Stages], k_empty[kF1Stages], v_full[kF1Stages], v_empty[kF1Stages];
   uint64_t s_full, s_free, p_full, pv_done, o_full, o_empty, kbar, drain;
@@ -549,6 +553,10 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
     }
+    for (int s = 0; s < kF1Slots; ++s) {
+      mbar_init(&sm.item_full[s], 1);
+      mbar_init(&sm.item_empty[s], 129);  // the MMA thread and the 128 softmax threads
+    }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_free, 128);
     mbar_init(&sm.p_full, 128);
@@ -574,8 +582,18 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int item = 0, kv = 0;
-      for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
+      // Work items are taken from a global counter in list order (largest
+      // first) as this CTA gets through its previous ones, and handed to the
+      // MMA and softmax roles through a small slot ring; -1 ends the walk.
+      int item = 0, kv = 0, slot_it = 0;
+      for (;;) {
+        const int slot = slot_it % kF1Slots;
+        if (!mbar_wait(&sm.item_empty[slot], ((slot_it / kF1Slots) & 1) ^ 1, abort_flag, p.status)) break;
+        const int w = atomicAdd(&p.sched[0], 1);
+        sm.items[slot] = w < p.n_work ? w : -1;
+        mbar_arrive(&sm.item_full[slot]);
+        ++slot_it;
+        if (w >= p.n_work) break;
         const int g = p.work[w];
         const int e0 = p.row_ptr[g], n = p.row_ptr[g + 1] - e0;
         if (n == 0) continue;
@@ -637,7 +655,12 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         ++n_s;
         return true;
       };
-      for (int rnd = 0, w = work_item(0); w < p.n_work && ok; w = work_item(++rnd)) {
+      for (int slot_it = 0; ok; ++slot_it) {
+        const int slot = slot_it % kF1Slots;
+        if (!mbar_wait(&sm.item_full[slot], (slot_it / kF1Slots) & 1, abort_flag, p.status)) break;
+        const int w = sm.items[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        if (w < 0) break;
         const int g = p.work[w];
         const int n = p.row_ptr[g + 1] - p.row_ptr[g];
         if (n == 0) continue;
@@ -685,7 +708,13 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       ++x_it;
       return __all_sync(0xffffffffu, r_ok);
     };
-    for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
+    for (int slot_it = 0;; ++slot_it) {
+      const int slot = slot_it % kF1Slots;
+      bool got = mbar_wait(&sm.item_full[slot], (slot_it / kF1Slots) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, got)) break;
+      const int w = sm.items[slot];
+      mbar_arrive(&sm.item_empty[slot]);
+      if (w < 0) break;
       const int g = p.work[w];
       const int e_beg = p.row_ptr[g], e_end = p.row_ptr[g + 1];
       const int bh = g / p.nQt, i = g % p.nQt;
@@ -874,6 +903,15 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kF1TmemCols);
+  // the last CTA to finish (every CTA has stopped taking items by then)
+  // leaves the counters at zero for the next launch on this workspace
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&p.sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(&p.sched[0], 0);
+      atomicExch(&p.sched[1], 0);
+    }
+  }
 }
 
 }  // namespace
@@ -946,6 +984,7 @@ static cudaError_t launch_fwd1(const AttnArgs& a, cudaStream_t st) {
   p.fflags = reinterpret_cast<const uint8_t*>(a.ws + L.fflags);
   p.work = reinterpret_cast<const int32_t*>(a.ws + L.work_fwd);
   p.n_work = static_cast<int>(L.n_qtiles);
+  p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched;
   p.o = a.o_out;
   p.lse = a.lse_out;
   p.status = reinterpret_cast<int*>(a.ws + L.header);

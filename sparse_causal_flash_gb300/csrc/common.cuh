@@ -19,7 +19,12 @@ constexpr uint32_t kFlagFull = 1u;     // tile flag bit: every pair admissible
 struct WsHeader {
   int status;       // SCFA_OK or the first device-side error
   int n_live;       // total live tiles (written by the tile pass)
-  int pad[62];
+  // work counters of the dynamically scheduled kernels: [0] next forward
+  // item, [1] forward CTAs done, [2] next backward item, [3] backward CTAs
+  // done; zeroed with the header by the tile pass and again by the last CTA
+  // of each launch
+  int sched[4];
+  int pad[58];
 };
 
 // ---------------------------------------------------------------------------
