@@ -46,6 +46,7 @@ constexpr int kSubBytes = kTile * 128;
 template <int D>
 constexpr int bwd_qstages() { return D == 64 ? 3 : 1; }
 constexpr int kBwdThreads = 448;
+constexpr int kBwdSlots = 4;  // work items handed from the producer to the other roles
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -65,6 +66,8 @@ struct __align__(1024) BwdSmem {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t s_full, st_empty, ds_full, pt_free, ds_free[2], dq_full, dq_empty, dkv_full, dkv_empty, drain;
+  int32_t items[kBwdSlots];
+  uint64_t item_full[kBwdSlots], item_empty[kBwdSlots];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -86,6 +89,7 @@ struct BwdParams {
   int n_work;
   uint16_t* dk;
   uint16_t* dv;
+  int* sched;  // [0] next work item, [1] CTAs done
   int* status;
 };
 
@@ -131,6 +135,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&sm.dkv_full, 1);
     mbar_init(&sm.dkv_empty, 256);
     mbar_init(&sm.drain, 1);
+    for (int s = 0; s < kBwdSlots; ++s) {
+      mbar_init(&sm.item_full[s], 1);
+      mbar_init(&sm.item_empty[s], 1 + 256 + 128);  // MMA thread, compute and dQ warpgroups
+    }
     sm.abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -148,8 +156,22 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer warp
+    // Work items come from a global counter in list order (largest first) as
+    // this CTA gets through its previous ones; lane 0 hands each to the other
+    // roles through a slot ring, -1 ending the walk.
     int q_it = 0, item = 0, last_kv = -1;
-    for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
+    for (int slot_it = 0;; ++slot_it) {
+      int w = INT_MAX;
+      if (lane == 0) {
+        const int slot = slot_it % kBwdSlots;
+        if (mbar_wait(&sm.item_empty[slot], ((slot_it / kBwdSlots) & 1) ^ 1, abort_flag, p.status)) {
+          w = atomicAdd(&p.sched[0], 1);
+          sm.items[slot] = w < p.n_work ? w : -1;
+          mbar_arrive(&sm.item_full[slot]);
+        }
+      }
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w >= p.n_work) break;
       const int g = p.work[w / kHalves];  // both halves load all of K, V, Q, dO
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
       if (n == 0) continue;
@@ -258,7 +280,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_commit(&sm.s_full);
         return true;
       };
-      for (int rnd = 0, w = work_item(0); w < p.n_work && ok; w = work_item(++rnd)) {
+      for (int slot_it = 0; ok; ++slot_it) {
+        const int slot = slot_it % kBwdSlots;
+        if (!mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status)) break;
+        const int w = sm.items[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        if (w < 0) break;
         const int g = p.work[w / kHalves];
         const int hh = w % kHalves;
         const int n = p.csc_ptr[g + 1] - p.csc_ptr[g];
@@ -335,7 +362,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int kr = quarter * 32 + lane;    // key row = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0, q_it = 0, item = 0;
-    for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
+    for (int slot_it = 0;; ++slot_it) {
+      const int slot = slot_it % kBwdSlots;
+      const bool got = mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, got)) break;
+      const int w = sm.items[slot];
+      mbar_arrive(&sm.item_empty[slot]);
+      if (w < 0) break;
       const int g = p.work[w / kHalves];
       const int hh = w % kHalves;  // which 64-column half of D
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
@@ -477,7 +510,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int tid = threadIdx.x - 320;   // 0..127
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     int it = 0;
-    for (int rnd = 0, w = work_item(0); w < p.n_work; w = work_item(++rnd)) {
+    for (int slot_it = 0;; ++slot_it) {
+      const int slot = slot_it % kBwdSlots;
+      const bool got = mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, got)) break;
+      const int w = sm.items[slot];
+      mbar_arrive(&sm.item_empty[slot]);
+      if (w < 0) break;
       const int g = p.work[w / kHalves];
       const int hh = w % kHalves;  // which 64-column half of D
       const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
@@ -523,6 +562,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  // the last CTA to finish (every CTA has stopped taking items by then)
+  // leaves the counters at zero for the next launch on this workspace
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&p.sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(&p.sched[0], 0);
+      atomicExch(&p.sched[1], 0);
+    }
+  }
 }
 
 // Drow[row] = sum_d dO * O (fp32) and dq_acc[row] = 0. D/8 lanes per row (one
@@ -622,6 +670,7 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   p.dk = a.dk;
   p.dv = a.dv;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
+  p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched + 2;
   const size_t smem = sizeof(BwdSmem<D>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
