@@ -303,7 +303,10 @@ scfa_status lsh_hash(const uint16_t* x, const uint16_t* R, int B, int H, int T, 
   if ((static_cast<size_t>(D) * ((n_buckets / 2 + 3) & ~3) + 256u * (D / 2 + 1)) * sizeof(float) > 200 * 1024)
     return SCFA_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(B) * H * T;
-  return finish(launch_lsh_hash(x, R, rows, D, n_buckets / 2, hash, static_cast<cudaStream_t>(stream)), 0, nullptr);
+  // no workspace here: a pipeline timeout lands in a library-owned status word
+  return finish(launch_lsh_hash(x, R, rows, D, n_buckets / 2, hash, lsh_scratch_status(),
+                                static_cast<cudaStream_t>(stream)),
+                0, nullptr);
 }
 
 scfa_status lsh_bucket_sort(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D, int n_buckets,
@@ -321,7 +324,8 @@ scfa_status lsh_bucket_sort(const uint16_t* x, const uint16_t* R, int B, int H, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* hash = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.hash);
   const long long rows = static_cast<long long>(B) * H * T;
-  cudaError_t e = launch_lsh_hash(x, R, rows, D, n_buckets / 2, hash, st);
+  cudaError_t e = launch_lsh_hash(x, R, rows, D, n_buckets / 2, hash,
+                                  reinterpret_cast<int*>(static_cast<char*>(ws) + L.header), st);
   if (e == cudaSuccess) e = launch_bucket_sort(hash, B * H, T, n_buckets, perm, hash_sorted, bucket_off, st);
   if (e == cudaSuccess && x_sorted) e = launch_gather(x, perm, B * H, T, D, x_sorted, false, st);
   return finish(e, flags, st);

@@ -58,8 +58,13 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
                          char* ws, const AttnWs& L, cudaStream_t st);
 
 // lsh.cu
+// status: a device int the tensor-core path may raise a timeout in (NULL keeps
+// the CUDA-core kernel)
 cudaError_t launch_lsh_hash(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
-                            int32_t* hash, cudaStream_t st);
+                            int32_t* hash, int* status, cudaStream_t st);
+int* lsh_scratch_status();  // device status word of the workspace-free lsh_hash call
+cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
+                                 int32_t* hash, cudaStream_t st);
 cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int n_buckets,
                                int32_t* perm, int32_t* hash_sorted, int32_t* bucket_off,
                                cudaStream_t st);

@@ -136,14 +136,12 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
 //     keeps the smallest index among exact ties.
 constexpr int kHashRows = 256;
 
-__global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __restrict__ x,
-                                                             const uint16_t* __restrict__ R, long long rows,
-                                                             int D, int m, int32_t* __restrict__ hash) {
+// R as fp32 [D][m4] in shared memory (zero columns appended), the largest
+// column norm ||R_c||_2 rounded up and the exponent range of R's nonzero
+// entries; every thread of the block calls it.
+__device__ void lsh_prologue(const uint16_t* __restrict__ R, int D, int m, float* sR, float* rnmax_out,
+                             int* r_emin_out, int* r_emax_out) {
   const int m4 = (m + 3) & ~3;
-  const int xs = D / 2 + 1;  // padded row stride of the staged rows, in 32-bit words
-  extern __shared__ float smem[];
-  float* sR = smem;                                                  // [D][m4]
-  uint32_t* sX = reinterpret_cast<uint32_t*>(smem + D * m4);         // [kHashRows][xs]
   for (int i = threadIdx.x; i < D * m4; i += blockDim.x) {
     const int d = i / m4, c = i % m4;
     sR[i] = c < m ? bf16_to_f32(R[d * m + c]) : 0.f;
@@ -191,12 +189,163 @@ __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __r
     }
   }
   __syncthreads();
-  const float rnmax = s_rn;
-  const int r_emin = s_remin, r_emax = s_remax;
+  *rnmax_out = s_rn;
+  *r_emin_out = s_remin;
+  *r_emax_out = s_remax;
+}
+
+// Exact bucket id of one row: fp32 screening with the certified bound, exact
+// re-evaluation of near ties. xrow: the row as bf16 pairs (32-bit words, in
+// shared or global memory); xr: the same row in global memory.
+__device__ int hash_row(const uint32_t* xrow, const uint16_t* __restrict__ xr, const float* sR,
+                        const uint16_t* __restrict__ R, int D, int m, float rnmax, int r_emin, int r_emax) {
+  const int m4 = (m + 3) & ~3;
   const float4* sR4 = reinterpret_cast<const float4*>(sR);
   // fp32 rounding bound of one dot product, doubled: 2 * gamma_D with gamma_D < (D+1) 2^-24
   const float rel = static_cast<float>(D + 1) * 0x1p-23f;
   const float absb = static_cast<float>(D) * 0x1p-148f;
+    auto xval = [&](int d) -> float {
+    const uint32_t w = xrow[d >> 1];
+    return __uint_as_float((d & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  };
+  // ||x||_2 rounded up: squares of bf16 are exact unless subnormal
+  // (covered by D 2^-148), the fp32 sum by the (D+2) 2^-22 factor
+  float l2sq = 0.f;
+  for (int d = 0; d < D; ++d) l2sq = fmaf(xval(d), xval(d), l2sq);
+  const float l2 = sqrtf(l2sq * (1.f + static_cast<float>(D + 2) * 0x1p-22f) + static_cast<float>(D) * 0x1p-148f) *
+                   1.000001f;
+  const float emax = l2 * rnmax * rel * 1.000001f + absb;
+  // the four best candidates (values t, candidate indices j)
+  float t0 = -INFINITY, t1 = -INFINITY, t2 = -INFINITY, t3 = -INFINITY;
+  int j0 = 0, j1 = 0, j2 = 0;
+  for (int c0 = 0; c0 < m4; c0 += 4) {
+    asm volatile("" ::: "memory");
+    float sv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int d2 = 0; d2 < D; d2 += 2) {
+      const uint32_t w = xrow[d2 >> 1];
+      const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+      const float4 ra = sR4[(d2 * m4 + c0) >> 2];
+      const float4 rb = sR4[((d2 + 1) * m4 + c0) >> 2];
+      sv[0] = fmaf(x1, rb.x, fmaf(x0, ra.x, sv[0]));
+      sv[1] = fmaf(x1, rb.y, fmaf(x0, ra.y, sv[1]));
+      sv[2] = fmaf(x1, rb.z, fmaf(x0, ra.z, sv[2]));
+      sv[3] = fmaf(x1, rb.w, fmaf(x0, ra.w, sv[3]));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u;
+      if (c >= m) break;
+      // candidate c (+s) and candidate m + c (-s)
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const float v = t ? -sv[u] : sv[u];
+        const int j = c + t * m;
+        if (v > t3) {
+          if (v > t2) {
+            t3 = t2;
+            if (v > t1) {
+              t2 = t1; j2 = j1;
+              if (v > t0) { t1 = t0; j1 = j0; t0 = v; j0 = j; } else { t1 = v; j1 = j; }
+            } else { t2 = v; j2 = j; }
+          } else { t3 = v; }
+        }
+      }
+    }
+  }
+  int h = j0;
+  const float thr = 2.f * emax * 1.0001f;
+  if (!(t0 - t1 > thr)) {
+    const bool few = (t0 - t3 > thr);  // every candidate within thr of the top is among the four
+    int cj[3];
+    int nc = 0;
+    if (few) {
+      cj[nc++] = j0;
+      if (t0 - t1 <= thr) cj[nc++] = j1;
+      if (t0 - t2 <= thr) cj[nc++] = j2;
+    }
+    // exponent span of the row's products
+    int xemin = INT_MAX, xemax = INT_MIN;
+    for (int d = 0; d < D; ++d) {
+      bool ng;
+      uint32_t M;
+      int E;
+      bf16_parts(static_cast<uint16_t>(__float_as_uint(xval(d)) >> 16), &ng, &M, &E);
+      if (M != 0) {
+        xemin = min(xemin, E);
+        xemax = max(xemax, E);
+      }
+    }
+    const bool any_term = xemin != INT_MAX && r_emin != INT_MAX;
+    const int ebase = any_term ? xemin + r_emin : 0;
+    const bool fits128 = !any_term || (xemax + r_emax) - ebase <= 100;
+    // exact sum of column c as an integer times 2^ebase (fits128 only)
+    auto exact128 = [&](int c) -> __int128 {
+      __int128 acc = 0;
+      if (!any_term) return acc;
+      for (int d = 0; d < D; ++d) {
+        bool nx, nr2;
+        uint32_t Mx, Mr;
+        int Ex, Er;
+        bf16_parts(static_cast<uint16_t>(__float_as_uint(xval(d)) >> 16), &nx, &Mx, &Ex);
+        bf16_parts(static_cast<uint16_t>(__float_as_uint(sR[d * m4 + c]) >> 16), &nr2, &Mr, &Er);
+        if (Mx == 0 || Mr == 0) continue;
+        const __int128 term = static_cast<__int128>(Mx * Mr) << (Ex + Er - ebase);
+        acc = (nx != nr2) ? acc - term : acc + term;
+      }
+      return acc;
+    };
+    auto is_cand = [&](int j) -> bool {
+      if (few) {
+        bool in = false;
+        for (int k = 0; k < nc; ++k) in = in || (cj[k] == j);
+        return in;
+      }
+      const int c = j < m ? j : j - m;
+      float sc = 0.f;
+      for (int d = 0; d < D; ++d) sc = fmaf(xval(d), sR[d * m4 + c], sc);
+      const float vj = j < m ? sc : -sc;
+      return (t0 - vj <= thr) || (vj != vj);
+    };
+    int best_j = -1;
+    if (fits128) {
+      __int128 best = 0;
+      for (int j = 0; j < 2 * m; ++j) {
+        if (!is_cand(j)) continue;
+        const __int128 v = (j < m) ? exact128(j) : -exact128(j - m);
+        if (best_j < 0 || v > best) {
+          best = v;
+          best_j = j;
+        }
+      }
+    } else {
+      Fix576 best, cur;
+      for (int j = 0; j < 2 * m; ++j) {
+        if (!is_cand(j)) continue;
+        fix_dot(xr, R, D, m, j < m ? j : j - m, cur);
+        if (j >= m) fix_negate(cur);
+        if (best_j < 0 || fix_greater(cur, best)) {
+          best = cur;
+          best_j = j;
+        }
+      }
+    }
+    h = best_j >= 0 ? best_j : j0;
+  }
+  return h;
+}
+
+__global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __restrict__ x,
+                                                             const uint16_t* __restrict__ R, long long rows,
+                                                             int D, int m, int32_t* __restrict__ hash) {
+  const int m4 = (m + 3) & ~3;
+  const int xs = D / 2 + 1;  // padded row stride of the staged rows, in 32-bit words
+  extern __shared__ float smem[];
+  float* sR = smem;                                                  // [D][m4]
+  uint32_t* sX = reinterpret_cast<uint32_t*>(smem + D * m4);         // [kHashRows][xs]
+  float rnmax;
+  int r_emin, r_emax;
+  lsh_prologue(R, D, m, sR, &rnmax, &r_emin, &r_emax);
   const int wpr = D / 2;  // 32-bit words per row
   for (long long r0 = static_cast<long long>(blockIdx.x) * kHashRows; r0 < rows;
        r0 += static_cast<long long>(gridDim.x) * kHashRows) {
@@ -207,138 +356,374 @@ __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __r
     __syncthreads();
     if (threadIdx.x >= nr) continue;
     const long long r = r0 + threadIdx.x;
-    const uint32_t* xrow = sX + threadIdx.x * xs;
-    auto xval = [&](int d) -> float {
-      const uint32_t w = xrow[d >> 1];
-      return __uint_as_float((d & 1) ? (w & 0xFFFF0000u) : (w << 16));
-    };
-    // ||x||_2 rounded up: squares of bf16 are exact unless subnormal
-    // (covered by D 2^-148), the fp32 sum by the (D+2) 2^-22 factor
-    float l2sq = 0.f;
-    for (int d = 0; d < D; ++d) l2sq = fmaf(xval(d), xval(d), l2sq);
-    const float l2 = sqrtf(l2sq * (1.f + static_cast<float>(D + 2) * 0x1p-22f) + static_cast<float>(D) * 0x1p-148f) *
-                     1.000001f;
-    const float emax = l2 * rnmax * rel * 1.000001f + absb;
-    // the four best candidates (values t, candidate indices j)
-    float t0 = -INFINITY, t1 = -INFINITY, t2 = -INFINITY, t3 = -INFINITY;
-    int j0 = 0, j1 = 0, j2 = 0;
-    for (int c0 = 0; c0 < m4; c0 += 4) {
-      asm volatile("" ::: "memory");
-      float sv[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-      for (int d2 = 0; d2 < D; d2 += 2) {
-        const uint32_t w = xrow[d2 >> 1];
-        const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
-        const float4 ra = sR4[(d2 * m4 + c0) >> 2];
-        const float4 rb = sR4[((d2 + 1) * m4 + c0) >> 2];
-        sv[0] = fmaf(x1, rb.x, fmaf(x0, ra.x, sv[0]));
-        sv[1] = fmaf(x1, rb.y, fmaf(x0, ra.y, sv[1]));
-        sv[2] = fmaf(x1, rb.z, fmaf(x0, ra.z, sv[2]));
-        sv[3] = fmaf(x1, rb.w, fmaf(x0, ra.w, sv[3]));
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = c0 + u;
-        if (c >= m) break;
-        // candidate c (+s) and candidate m + c (-s)
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const float v = t ? -sv[u] : sv[u];
-          const int j = c + t * m;
-          if (v > t3) {
-            if (v > t2) {
-              t3 = t2;
-              if (v > t1) {
-                t2 = t1; j2 = j1;
-                if (v > t0) { t1 = t0; j1 = j0; t0 = v; j0 = j; } else { t1 = v; j1 = j; }
-              } else { t2 = v; j2 = j; }
-            } else { t3 = v; }
-          }
-        }
-      }
-    }
-    int h = j0;
-    const float thr = 2.f * emax * 1.0001f;
-    if (!(t0 - t1 > thr)) {
+    hash[r] = hash_row(sX + threadIdx.x * xs, x + r * D, sR, R, D, m, rnmax, r_emin, r_emax);
+  }
+}
+
+// Second pass after the tensor-core pass: rows it left at -1 (near ties,
+// non-finite or subnormal values, huge magnitudes) get the certified
+// computation, one warp per row. Each warp scans 32 ids at a time and takes
+// the flagged rows one by one: the lanes share the row (staged as fp32 in
+// shared memory), screen the columns lane + 32 k in fp32 with the same bound
+// as the single-thread path (it holds for any summation order), and evaluate
+// every candidate within the threshold of the top exactly, in 128-bit
+// integers; the warp keeps the largest value, the smallest index on ties.
+// A row whose exponent span needs more than 128 bits goes to the
+// single-thread path (576-bit accumulator) on lane 0.
+constexpr int kFixWarps = 8;
+
+__global__ void __launch_bounds__(kFixWarps * 32) lsh_fix_kernel(const uint16_t* __restrict__ x,
+                                                                 const uint16_t* __restrict__ R, long long rows,
+                                                                 int D, int m, int32_t* __restrict__ hash) {
+  extern __shared__ float smem[];
+  const int m4 = (m + 3) & ~3;
+  float* sR = smem;                      // [D][m4]
+  float* sxall = smem + D * m4;          // [kFixWarps][D]
+  float rnmax;
+  int r_emin, r_emax;
+  lsh_prologue(R, D, m, sR, &rnmax, &r_emin, &r_emax);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* sx = sxall + warp * D;
+  const float rel = static_cast<float>(D + 1) * 0x1p-23f;
+  const float absb = static_cast<float>(D) * 0x1p-148f;
+  const long long nwarps = static_cast<long long>(gridDim.x) * kFixWarps;
+  for (long long base = (static_cast<long long>(blockIdx.x) * kFixWarps + warp) * 32; base < rows;
+       base += nwarps * 32) {
+    const long long rl = base + lane;
+    const bool flagged = rl < rows && hash[rl] < 0;
+    unsigned todo = __ballot_sync(0xffffffffu, flagged);
+    while (todo) {
+      const int bit = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const long long r = base + bit;
       const uint16_t* xr = x + r * D;
-      const bool few = (t0 - t3 > thr);  // every candidate within thr of the top is among the four
-      int cj[3];
-      int nc = 0;
-      if (few) {
-        cj[nc++] = j0;
-        if (t0 - t1 <= thr) cj[nc++] = j1;
-        if (t0 - t2 <= thr) cj[nc++] = j2;
-      }
-      // exponent span of the row's products
+      // stage the row; norm and exponent range of its nonzero entries
+      float l2sq = 0.f;
       int xemin = INT_MAX, xemax = INT_MIN;
-      for (int d = 0; d < D; ++d) {
+      for (int d = lane; d < D; d += 32) {
+        const uint16_t bb = xr[d];
+        const float v = bf16_to_f32(bb);
+        sx[d] = v;
+        l2sq = fmaf(v, v, l2sq);
         bool ng;
         uint32_t M;
         int E;
-        bf16_parts(static_cast<uint16_t>(__float_as_uint(xval(d)) >> 16), &ng, &M, &E);
+        bf16_parts(bb, &ng, &M, &E);
         if (M != 0) {
           xemin = min(xemin, E);
           xemax = max(xemax, E);
         }
       }
+      for (int o = 16; o; o >>= 1) {
+        l2sq += __shfl_xor_sync(0xffffffffu, l2sq, o);
+        xemin = min(xemin, __shfl_xor_sync(0xffffffffu, xemin, o));
+        xemax = max(xemax, __shfl_xor_sync(0xffffffffu, xemax, o));
+      }
+      __syncwarp();
+      const float l2 = sqrtf(l2sq * (1.f + static_cast<float>(D + 2) * 0x1p-22f) + static_cast<float>(D) * 0x1p-148f) *
+                       1.000001f;
+      const float emax = l2 * rnmax * rel * 1.000001f + absb;
+      const float thr = 2.f * emax * 1.0001f;
+      // fp32 values of this lane's columns; the warp's top value
+      float best_v = -INFINITY;
+      for (int c = lane; c < m; c += 32) {
+        float sc = 0.f;
+        for (int d = 0; d < D; ++d) sc = fmaf(sx[d], sR[d * m4 + c], sc);
+        best_v = fmaxf(best_v, fmaxf(sc, -sc));
+      }
+      float t0 = best_v;
+      for (int o = 16; o; o >>= 1) t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
+      // exact values of the candidates (within thr of the top, or NaN)
       const bool any_term = xemin != INT_MAX && r_emin != INT_MAX;
       const int ebase = any_term ? xemin + r_emin : 0;
       const bool fits128 = !any_term || (xemax + r_emax) - ebase <= 100;
-      // exact sum of column c as an integer times 2^ebase (fits128 only)
-      auto exact128 = [&](int c) -> __int128 {
-        __int128 acc = 0;
-        if (!any_term) return acc;
-        for (int d = 0; d < D; ++d) {
-          bool nx, nr2;
-          uint32_t Mx, Mr;
-          int Ex, Er;
-          bf16_parts(static_cast<uint16_t>(__float_as_uint(xval(d)) >> 16), &nx, &Mx, &Ex);
-          bf16_parts(static_cast<uint16_t>(__float_as_uint(sR[d * m4 + c]) >> 16), &nr2, &Mr, &Er);
-          if (Mx == 0 || Mr == 0) continue;
-          const __int128 term = static_cast<__int128>(Mx * Mr) << (Ex + Er - ebase);
-          acc = (nx != nr2) ? acc - term : acc + term;
-        }
-        return acc;
-      };
-      auto is_cand = [&](int j) -> bool {
-        if (few) {
-          bool in = false;
-          for (int k = 0; k < nc; ++k) in = in || (cj[k] == j);
-          return in;
-        }
-        const int c = j < m ? j : j - m;
-        float sc = 0.f;
-        for (int d = 0; d < D; ++d) sc = fmaf(xval(d), sR[d * m4 + c], sc);
-        const float vj = j < m ? sc : -sc;
-        return (t0 - vj <= thr) || (vj != vj);
-      };
-      int best_j = -1;
+      int h;
       if (fits128) {
-        __int128 best = 0;
-        for (int j = 0; j < 2 * m; ++j) {
-          if (!is_cand(j)) continue;
-          const __int128 v = (j < m) ? exact128(j) : -exact128(j - m);
-          if (best_j < 0 || v > best) {
-            best = v;
-            best_j = j;
+        bool have = false;
+        __int128 bv = 0;
+        int bj = 0;
+        for (int c = lane; c < m; c += 32) {
+          float sc = 0.f;
+          for (int d = 0; d < D; ++d) sc = fmaf(sx[d], sR[d * m4 + c], sc);
+          const bool cp = (t0 - sc <= thr) || (sc != sc);
+          const bool cn = (t0 + sc <= thr) || (sc != sc);
+          if (!cp && !cn) continue;
+          __int128 acc = 0;
+          if (any_term) {
+            for (int d = 0; d < D; ++d) {
+              bool nx, nr2;
+              uint32_t Mx, Mr;
+              int Ex, Er;
+              bf16_parts(static_cast<uint16_t>(__float_as_uint(sx[d]) >> 16), &nx, &Mx, &Ex);
+              bf16_parts(static_cast<uint16_t>(__float_as_uint(sR[d * m4 + c]) >> 16), &nr2, &Mr, &Er);
+              if (Mx == 0 || Mr == 0) continue;
+              const __int128 term = static_cast<__int128>(Mx * Mr) << (Ex + Er - ebase);
+              acc = (nx != nr2) ? acc - term : acc + term;
+            }
+          }
+          // candidate c (+s), then m + c (-s): this lane's columns ascend, so a
+          // strict comparison keeps the smallest index among its own ties
+          if (cp && (!have || acc > bv || (acc == bv && c < bj))) {
+            bv = acc;
+            bj = c;
+            have = true;
+          }
+          if (cn && (!have || -acc > bv || (-acc == bv && c + m < bj))) {
+            bv = -acc;
+            bj = c + m;
+            have = true;
           }
         }
+        // warp arg-max: larger value, then smaller index
+        for (int o = 16; o; o >>= 1) {
+          const unsigned long long lo = static_cast<unsigned long long>(bv);
+          const long long hi = static_cast<long long>(bv >> 64);
+          const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, o);
+          const long long ohi = __shfl_xor_sync(0xffffffffu, hi, o);
+          const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+          const int oh = __shfl_xor_sync(0xffffffffu, have ? 1 : 0, o);
+          const __int128 ov = (static_cast<__int128>(ohi) << 64) | static_cast<__int128>(olo);
+          if (oh && (!have || ov > bv || (ov == bv && oj < bj))) {
+            bv = ov;
+            bj = oj;
+            have = true;
+          }
+        }
+        h = bj;
       } else {
-        Fix576 best, cur;
-        for (int j = 0; j < 2 * m; ++j) {
-          if (!is_cand(j)) continue;
-          fix_dot(xr, R, D, m, j < m ? j : j - m, cur);
-          if (j >= m) fix_negate(cur);
-          if (best_j < 0 || fix_greater(cur, best)) {
-            best = cur;
-            best_j = j;
+        // exponent span beyond 128 bits: the single-thread path on lane 0
+        int hh = 0;
+        if (lane == 0) hh = hash_row(reinterpret_cast<const uint32_t*>(xr), xr, sR, R, D, m, rnmax, r_emin, r_emax);
+        h = __shfl_sync(0xffffffffu, hh, 0);
+      }
+      if (lane == 0) hash[r] = h;
+      __syncwarp();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core first pass (D = 64 or 128, m a multiple of 8, m <= 256):
+// X R for 128 rows at a time on tcgen05 (bf16 products are exact, fp32
+// accumulation in TMEM), then per row the best and second-best candidate of
+// [xR, -xR]. The row keeps the best when it leads by more than twice a bound
+// on the accumulation error, taken loose (2^-14 ||x||_2 max_c ||R_c||_2: 4x
+// D additions each losing 2^-23 of a partial sum at D = 128, 8x at D = 64);
+// every other row, and every row with a subnormal, non-finite or huge value,
+// is left at -1 for the certified second pass (lsh_fix_kernel).
+// Roles (192 threads): warp 0 TMA producer (x tiles, 4 stages), warp 1 MMA
+// issuer and TMEM owner (two accumulators of m_pad columns), warps 2-5
+// epilogue (thread = row = TMEM lane). R sits in shared memory for the whole
+// kernel as the MN-major B operand ([D][64]-column swizzled sub-tiles).
+// ---------------------------------------------------------------------------
+constexpr int kTcThreads = 192;
+constexpr int kTcStages = 4;
+constexpr float kTcRel = 0x1p-14f;
+
+template <int D>
+struct __align__(1024) LshTcSmem {
+  uint8_t x[kTcStages][D / 64][kTile * 128];  // [stage][64-column sub-tile][128 rows x 128 B]
+  uint8_t r[4][D * 128];                      // up to 4 sub-tiles of [D rows][64 columns]
+  uint64_t x_full[kTcStages], x_empty[kTcStages];
+  uint64_t acc_full[2], acc_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int r_bad;  // R holds a subnormal or non-finite value: every row goes to the second pass
+  float rnmax;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __restrict__ R, long long rows,
+                   int m, int m_pad, int32_t* __restrict__ hash, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  LshTcSmem<D>& sm = *reinterpret_cast<LshTcSmem<D>*>(smem_raw + pad);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long n_tiles = (rows + kTile - 1) / kTile;
+  const uint32_t acc_cols = m_pad < 32 ? 32u : static_cast<uint32_t>(m_pad);
+  const uint32_t tmem_cols = acc_cols * 2 <= 32 ? 32u : (acc_cols * 2 <= 64 ? 64u : (acc_cols * 2 <= 128 ? 128u : (acc_cols * 2 <= 256 ? 256u : 512u)));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&sm.x_full[s], 1);
+      mbar_init(&sm.x_empty[s], 1 + 128);  // the MMA commit and the 128 epilogue threads (row norms)
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], 128);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    sm.r_bad = 0;
+    sm.rnmax = 0.f;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_x);
+  }
+  __syncthreads();
+  // R -> shared memory in the swizzled MN-major layout: sub-tile c / 64, row d,
+  // 16-byte chunk (c % 64) / 8; columns past m are zero. Also the largest
+  // column norm (rounded up) and a check for subnormal / non-finite entries.
+  {
+    const int n_sub = (m_pad + 63) / 64;
+    for (int idx = threadIdx.x; idx < n_sub * D * 8; idx += blockDim.x) {
+      const int st = idx / (D * 8), d = (idx / 8) % D, ch = idx % 8;
+      uint32_t w[4];
+      for (int u = 0; u < 4; ++u) {
+        const int c0 = st * 64 + ch * 8 + 2 * u;
+        const uint32_t lo = c0 < m ? R[static_cast<long long>(d) * m + c0] : 0u;
+        const uint32_t hi = c0 + 1 < m ? R[static_cast<long long>(d) * m + c0 + 1] : 0u;
+        w[u] = lo | (hi << 16);
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t b = k ? hi : lo;
+          const uint32_t e = (b >> 7) & 0xFFu, mant = b & 0x7Fu;
+          if ((e == 0 && mant != 0) || e == 0xFFu) sm.r_bad = 1;
+        }
+      }
+      *reinterpret_cast<uint4*>(&sm.r[st][0] + sw128_offset(d, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  {
+    // column norms from the staged copy
+    float mx = 0.f;
+    for (int c = threadIdx.x; c < m; c += blockDim.x) {
+      const uint8_t* sub = &sm.r[c >> 6][0];
+      const int ch = (c & 63) >> 3, w16 = c & 7;
+      float ss = 0.f;
+      for (int d = 0; d < D; ++d) {
+        const uint16_t b = *reinterpret_cast<const uint16_t*>(sub + sw128_offset(d, ch) + 2 * w16);
+        const float v = bf16_to_f32(b);
+        ss = fmaf(v, v, ss);
+      }
+      mx = fmaxf(mx, sqrtf(ss * (1.f + static_cast<float>(D + 2) * 0x1p-22f)) * 1.000001f);
+    }
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) atomicMax(reinterpret_cast<int*>(&sm.rnmax), __float_as_int(mx));
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+        const int s = it % kTcStages;
+        if (!mbar_wait(&sm.x_empty[s], ((it / kTcStages) & 1) ^ 1, abort_flag, status)) break;
+        mbar_arrive_expect_tx(&sm.x_full[s], D * kTile * 2);
+        for (int sub = 0; sub < D / 64; ++sub)
+          tma_load_3d(sm.x[s][sub], &tm_x, &sm.x_full[s], sub * 64, static_cast<int>(t * kTile), 0);
+      }
+      for (int d = 1; d <= kTcStages && d <= it; ++d) {
+        const int i2 = it - d;
+        mbar_wait(&sm.x_full[i2 % kTcStages], (i2 / kTcStages) & 1, abort_flag, status);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kTile, m_pad, 0, 1);
+      const uint64_t xdesc = smem_desc_sw128(smem_u32(sm.x[0][0]), 16, 1024);
+      const uint64_t rdesc = smem_desc_sw128(smem_u32(sm.r[0]), D * 128, 1024);
+      constexpr uint32_t kStage16 = (D / 64) * kTile * 128 >> 4;
+      int it = 0;
+      for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+        const int s = it % kTcStages, b = it & 1;
+        if (!mbar_wait(&sm.acc_empty[b], ((it >> 1) & 1) ^ 1, abort_flag, status)) break;
+        if (!mbar_wait(&sm.x_full[s], (it / kTcStages) & 1, abort_flag, status)) break;
+        tc_fence_after();
+        const uint64_t a = xdesc + static_cast<uint64_t>(s * kStage16);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + acc_cols * b, a + kstep_off16(kk, kTile * 128), rdesc + static_cast<uint64_t>(kk * 128),
+                      idesc, kk > 0);
+        tc_commit(&sm.acc_full[b]);
+        tc_commit(&sm.x_empty[s]);
+      }
+      tc_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0, abort_flag, status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int rr = quarter * 32 + lane;  // row of the tile = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float rnmax = sm.rnmax;
+    const bool r_bad = sm.r_bad != 0;
+    int it = 0;
+    for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+      const int s = it % kTcStages, b = it & 1;
+      bool ok = mbar_wait(&sm.acc_full[b], (it >> 1) & 1, abort_flag, status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      // ||x||_2 of this row from the staged tile (rounded up), and a check
+      // for subnormal / non-finite entries
+      float l2sq = 0.f;
+      bool x_bad = false;
+#pragma unroll
+      for (int sub = 0; sub < D / 64; ++sub) {
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 q4 = *reinterpret_cast<const uint4*>(&sm.x[s][sub][0] + sw128_offset(rr, ch));
+          const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float lo = __uint_as_float(wv[u] << 16), hi = __uint_as_float(wv[u] & 0xFFFF0000u);
+            l2sq = fmaf(lo, lo, fmaf(hi, hi, l2sq));
+            const uint32_t e0 = (wv[u] >> 7) & 0xFFu, m0 = wv[u] & 0x7Fu;
+            const uint32_t e1 = (wv[u] >> 23) & 0xFFu, m1 = (wv[u] >> 16) & 0x7Fu;
+            x_bad = x_bad || (e0 == 0 && m0 != 0) || e0 == 0xFFu || (e1 == 0 && m1 != 0) || e1 == 0xFFu;
           }
         }
       }
-      h = best_j >= 0 ? best_j : j0;
+      mbar_arrive(&sm.x_empty[s]);
+      const float l2 = sqrtf(l2sq * (1.f + static_cast<float>(D + 2) * 0x1p-22f)) * 1.000001f;
+      const float emax = l2 * rnmax * kTcRel;
+      // best and second best of [s, -s] over the m real columns
+      float t0 = -INFINITY, t1 = -INFINITY;
+      int j0 = 0;
+      const uint32_t col0 = acc_cols * b;
+      for (int c0 = 0; c0 < m_pad; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + col0 + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int c = c0 + u;
+          if (c < m) {
+            const float sv = __uint_as_float(v[u]);
+            const float a = fmaxf(sv, -sv);
+            const int j = sv >= 0.f ? c : c + m;  // for sv == 0 both tie: the smaller index, c
+            const float bmin = fminf(sv, -sv);    // the other sign of the same column
+            // the pair (a, bmin) enters the running top two
+            if (a > t0) {
+              t1 = fmaxf(t0, bmin);
+              t0 = a;
+              j0 = j;
+            } else {
+              t1 = fmaxf(t1, a);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.acc_empty[b]);
+      const long long row = t * kTile + rr;
+      if (row < rows) {
+        const bool clear = !r_bad && !x_bad && l2 < 0x1p60f && rnmax < 0x1p60f && (t0 - t1 > 2.f * emax * 1.0001f);
+        hash[row] = clear ? j0 : -1;
+      }
     }
-    hash[r] = h;
   }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, tmem_cols);
 }
 
 // Stable counting sort of one (b,h) row of bucket ids per CTA. Warp w owns a
@@ -439,8 +824,58 @@ __global__ void row_move_kernel(const uint4* __restrict__ x, const int32_t* __re
 
 }  // namespace
 
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, long long T, long long BH);
+
+__device__ int g_lsh_status;
+
+int* lsh_scratch_status() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_lsh_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+template <int D>
+static cudaError_t launch_lsh_tc(const uint16_t* x, const uint16_t* R, long long rows, int m, int32_t* hash,
+                                 int* status, cudaStream_t st) {
+  CUtensorMap tm;
+  if (!make_tmap_bf16_3d(&tm, x, D, rows, 1)) return cudaErrorInvalidValue;
+  const int m_pad = (m + 15) / 16 * 16;
+  const size_t smem = sizeof(LshTcSmem<D>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(lsh_hash_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long n_tiles = (rows + kTile - 1) / kTile;
+  long long g = num_sms();
+  if (g > n_tiles) g = n_tiles;
+  if (g < 1) g = 1;
+  lsh_hash_tc_kernel<D><<<static_cast<int>(g), kTcThreads, smem, st>>>(tm, R, rows, m, m_pad, hash, status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // certified second pass over the rows the first pass left at -1
+  const size_t smem2 = static_cast<size_t>(D) * (((m + 3) & ~3) + kFixWarps) * sizeof(float);
+  e = cudaFuncSetAttribute(lsh_fix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem2));
+  if (e != cudaSuccess) return e;
+  long long g2 = (rows + kFixWarps * 32 - 1) / (kFixWarps * 32);
+  if (g2 > static_cast<long long>(num_sms()) * 2) g2 = static_cast<long long>(num_sms()) * 2;
+  if (g2 < 1) g2 = 1;
+  lsh_fix_kernel<<<static_cast<int>(g2), kFixWarps * 32, smem2, st>>>(x, R, rows, D, m, hash);
+  return cudaGetLastError();
+}
+
+// The tensor-core path needs D = 64 or 128, m a multiple of 8 (16-byte rows of
+// R), m <= 256 (one accumulator fits twice in TMEM) and a 16-byte aligned x;
+// other shapes take the CUDA-core kernel.
 cudaError_t launch_lsh_hash(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
-                            int32_t* hash, cudaStream_t st) {
+                            int32_t* hash, int* status, cudaStream_t st) {
+  const bool tc_ok = (D == 64 || D == 128) && m % 8 == 0 && m >= 8 && m <= 256 && status != nullptr &&
+                     (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && rows < (1ll << 31);
+  if (tc_ok) return D == 64 ? launch_lsh_tc<64>(x, R, rows, m, hash, status, st)
+                            : launch_lsh_tc<128>(x, R, rows, m, hash, status, st);
+  return launch_lsh_hash_cuda(x, R, rows, D, m, hash, st);
+}
+
+cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
+                                 int32_t* hash, cudaStream_t st) {
   const size_t smem = (static_cast<size_t>(D) * ((m + 3) & ~3) + static_cast<size_t>(kHashRows) * (D / 2 + 1)) *
                       sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(lsh_hash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

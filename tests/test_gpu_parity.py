@@ -62,6 +62,33 @@ def test_lsh_hash_exact_ties_and_cancellation(scfa):
         np.testing.assert_array_equal(h.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("D,m", [(64, 8), (128, 16), (128, 256)])
+def test_lsh_hash_tensor_core_path_ties_and_edges(scfa, D, m):
+    # shapes that take the tensor-core first pass (D 64 / 128, m a multiple of
+    # 8): exact column ties, all-zero rows, cancellation beyond fp32, a
+    # subnormal entry and huge magnitudes must all come out as the oracle says
+    rng = np.random.default_rng(6 + D + m)
+    c0 = torch.from_numpy(rng.standard_normal(D)).to(torch.bfloat16)
+    cols = [c0, c0, -c0, torch.zeros(D, dtype=torch.bfloat16)]
+    cols += [torch.from_numpy(rng.standard_normal(D)).to(torch.bfloat16) for _ in range(m - 4)]
+    R = torch.stack(cols, dim=1)
+    rows = [torch.zeros(D, dtype=torch.bfloat16)]
+    rows += [synth.normal_bf16(10 + D, 1, (D,)) for _ in range(300)]
+    big = torch.zeros(D, dtype=torch.bfloat16)
+    big[0], big[1], big[2] = 2.0**60, 1.0, -(2.0**60)
+    rows.append(big)
+    tiny = synth.normal_bf16(11, 1, (D,)).clone()
+    tiny[3] = torch.tensor(2.0**-130).to(torch.bfloat16)   # subnormal in bf16
+    rows.append(tiny)
+    huge = synth.normal_bf16(12, 1, (D,)) * 2.0**100
+    rows.append(huge.to(torch.bfloat16))
+    x = torch.stack(rows)[None, None]
+    h = torch.empty((1, 1, x.shape[2]), dtype=torch.int32, device="cuda")
+    scfa.lsh_hash(cuda(x), cuda(R), 2 * m, h)
+    ref = lsh.lsh_hash(x.double().numpy(), R.double().numpy())
+    np.testing.assert_array_equal(h.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("B,H,T,D,nb", [(1, 2, 512, 64, 4), (2, 3, 1000, 64, 16), (1, 1, 5000, 64, 512)])
 def test_bucket_sort_and_gather_bitexact(scfa, B, H, T, D, nb):
     x = synth.normal_bf16(78, 2, (B, H, T, D))
