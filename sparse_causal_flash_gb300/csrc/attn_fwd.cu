@@ -528,7 +528,8 @@ struct __align__(1024) Fwd1Smem {
   uint64_t item_full[kF1Slots], item_empty[kF1Slots];
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kF1Stages], k_empty[kF1Stages], v_full[kF1Stages], v_empty[kF1Stages];
-  uint64_t s_full, s_free, p_full, pv_done, o_full, o_empty, kbar, drain;
+  uint64_t s_full, s_free, o_full, o_empty, kbar, drain;
+  uint64_t p_full[2], pv_done[2];  // per key half: keys 0-63 (P columns 0-31), keys 64-127
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -559,8 +560,10 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_free, 128);
-    mbar_init(&sm.p_full, 128);
-    mbar_init(&sm.pv_done, 1);
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(&sm.p_full[hf], 128);
+      mbar_init(&sm.pv_done[hf], 1);
+    }
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.o_empty, 128);
     mbar_init(&sm.kbar, 128);
@@ -670,16 +673,24 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int t = 0; t < n; ++t) {
           const int s = kv % kF1Stages;
           if (t + 1 < n && !issue_s(kv + 1, qb)) { ok = false; break; }
-          if (!mbar_wait(&sm.p_full, p_it & 1, abort_flag, p.status)) { ok = false; break; }
           if (t == 0 && !mbar_wait(&sm.o_empty, (o_it & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
           if (!mbar_wait(&sm.v_full[s], (kv / kF1Stages) & 1, abort_flag, p.status)) { ok = false; break; }
-          tc_fence_after();
           const uint64_t vb = vdesc + static_cast<uint64_t>(s * kBuf16);
+          // PV in two halves of 64 keys, each as soon as the softmax has
+          // written that half of P
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8, vb + static_cast<uint64_t>(kk * 128), idesc_o,
-                        (kk > 0 || t > 0) ? 1u : 0u);
-          tc_commit(&sm.pv_done);
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait(&sm.p_full[hf], p_it & 1, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+              const int kk = hf * 4 + kq;
+              mma_bf16_ts(tmem + kColO, tmem + kColP + kk * 8, vb + static_cast<uint64_t>(kk * 128), idesc_o,
+                          (kk > 0 || t > 0) ? 1u : 0u);
+            }
+            tc_commit(&sm.pv_done[hf]);
+          }
+          if (!ok) break;
           tc_commit(&sm.v_empty[s]);
           ++kv;
           ++p_it;
@@ -813,46 +824,57 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
         const uint64_t sl2 = f2(p.scale_log2, p.scale_log2), nm2 = f2(-msub, -msub);
-        if (s_it > 0) {
-          // the previous PV has read P (and finished adding into O)
-          ok = mbar_wait(&sm.pv_done, (s_it - 1) & 1, abort_flag, p.status);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-        }
+        // P in two halves of 64 keys: each half waits for the previous PV's
+        // half that read it, and is handed to the MMA warp as soon as written
         uint64_t rsum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const uint64_t arg = fma2(f2(__uint_as_float(sr[h * 32 + c]), __uint_as_float(sr[h * 32 + c + 1])), sl2, nm2);
-            float a0, a1;
-            f2_split(arg, a0, a1);
-            const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
-            rsum2[(c >> 1) & 3] = add2(rsum2[(c >> 1) & 3], f2(e0, e1));
-            pk[c >> 1] = pack_bf16x2(e0, e1);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (s_it > 0) {
+            ok = mbar_wait(&sm.pv_done[hf], (s_it - 1) & 1, abort_flag, p.status);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
           }
-          tmem_st16(lane_base + kColP + h * 16, pk);
+#pragma unroll
+          for (int hq = 0; hq < 2; ++hq) {
+            const int h = hf * 2 + hq;
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const uint64_t arg = fma2(f2(__uint_as_float(sr[h * 32 + c]), __uint_as_float(sr[h * 32 + c + 1])), sl2, nm2);
+              float a0, a1;
+              f2_split(arg, a0, a1);
+              const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+              rsum2[(c >> 1) & 3] = add2(rsum2[(c >> 1) & 3], f2(e0, e1));
+              pk[c >> 1] = pack_bf16x2(e0, e1);
+            }
+            tmem_st16(lane_base + kColP + h * 16, pk);
+          }
+          // rescale O (rare) before the first half goes to the MMA warp; both
+          // halves of the previous PV are complete (the second was waited for
+          // only if needed here)
+          if (hf == 0 && !first_tile && __any_sync(0xffffffffu, resc)) {
+            ok = mbar_wait(&sm.pv_done[1], (s_it - 1) & 1, abort_flag, p.status);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t orr[32];
+              tmem_ld32(lane_base + kColO + cc * 32, orr);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e2 = 0; e2 < 32; ++e2) orr[e2] = __float_as_uint(__uint_as_float(orr[e2]) * alpha);
+              tmem_st32(lane_base + kColO + cc * 32, orr);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&sm.p_full[hf]);
         }
+        if (!ok) break;
         const uint64_t rs2 = add2(add2(rsum2[0], rsum2[1]), add2(rsum2[2], rsum2[3]));
         float rs_lo, rs_hi;
         f2_split(rs2, rs_lo, rs_hi);
         l = l * alpha + (rs_lo + rs_hi);
-        // rescale O (rare); the previous PV is complete (waited above)
-        if (!first_tile && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t orr[32];
-            tmem_ld32(lane_base + kColO + cc * 32, orr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e2 = 0; e2 < 32; ++e2) orr[e2] = __float_as_uint(__uint_as_float(orr[e2]) * alpha);
-            tmem_st32(lane_base + kColO + cc * 32, orr);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&sm.p_full);
         ++s_it;
         f_c = f_n;
         kid_c = kid_n;
