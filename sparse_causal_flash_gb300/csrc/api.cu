@@ -126,6 +126,11 @@ bool lsh_ws_layout(int B, int H, int T, int n_buckets, LshWs* L) {
   off = align_up(off + sizeof(WsHeader), 256);
   w.hash = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * H * T, 256);
+  w.chunk = off;
+  if (T > kSortChunk) {
+    const size_t chunks = (static_cast<size_t>(T) + kSortChunk - 1) / kSortChunk;
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * H * chunks * n_buckets, 256);
+  }
   w.total = off;
   *L = w;
   return true;
@@ -326,7 +331,9 @@ scfa_status lsh_bucket_sort(const uint16_t* x, const uint16_t* R, int B, int H, 
   const long long rows = static_cast<long long>(B) * H * T;
   cudaError_t e = launch_lsh_hash(x, R, rows, D, n_buckets / 2, hash,
                                   reinterpret_cast<int*>(static_cast<char*>(ws) + L.header), st);
-  if (e == cudaSuccess) e = launch_bucket_sort(hash, B * H, T, n_buckets, perm, hash_sorted, bucket_off, st);
+  if (e == cudaSuccess)
+    e = launch_bucket_sort(hash, B * H, T, n_buckets, perm, hash_sorted, bucket_off,
+                           reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.chunk), st);
   if (e == cudaSuccess && x_sorted) e = launch_gather(x, perm, B * H, T, D, x_sorted, false, st);
   return finish(e, flags, st);
 }

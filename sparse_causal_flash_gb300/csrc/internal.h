@@ -45,8 +45,10 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
 struct LshWs {
   size_t header = 0;
   size_t hash = 0;    // int32 [B,H,T], original order
+  size_t chunk = 0;   // int32 [B*H][chunks][n_buckets]: per-chunk counts, then scatter bases (long rows)
   size_t total = 0;
 };
+constexpr int kSortChunk = 8192;  // rows longer than this are sorted by several CTAs
 bool lsh_ws_layout(int B, int H, int T, int n_buckets, LshWs* L);
 
 int num_sms();
@@ -65,9 +67,10 @@ cudaError_t launch_lsh_hash(const uint16_t* x, const uint16_t* R, long long rows
 int* lsh_scratch_status();  // device status word of the workspace-free lsh_hash call
 cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
                                  int32_t* hash, cudaStream_t st);
+// chunk_ws: the workspace's chunk array (used when T > kSortChunk)
 cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int n_buckets,
                                int32_t* perm, int32_t* hash_sorted, int32_t* bucket_off,
-                               cudaStream_t st);
+                               int32_t* chunk_ws, cudaStream_t st);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int BH, int T, int D,
                           uint16_t* out, bool unsort, cudaStream_t st);
 

@@ -730,21 +730,33 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
 // contiguous slice of the row; per-warp histograms give each warp its start
 // in every bucket, and the warp then scatters its slice in order, ranking
 // equal ids inside each 32-element step with __match_any_sync.
+//
+// Rows longer than kSortChunk: CTA (row, chunk) sorts its chunk the same way,
+// in three launches: mode 1 writes the chunk's bucket counts, mode 2 (one
+// CTA per row, bucket_scan_kernel) turns them into the chunk's first output
+// position per bucket and writes bucket_off, mode 2 scatters from those
+// bases. Mode 0 is the whole row in one CTA.
 __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int nb,
                                    int32_t* __restrict__ perm, int32_t* __restrict__ hash_sorted,
-                                   int32_t* __restrict__ bucket_off) {
+                                   int32_t* __restrict__ bucket_off, int mode, int chunk, int n_chunks,
+                                   int32_t* __restrict__ chunk_ws) {
   extern __shared__ int32_t hist[];  // [nwarps][nb], then [nb] totals
   const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long bh = blockIdx.x;
+  const long long bh = mode == 0 ? blockIdx.x : blockIdx.x / n_chunks;
+  const int ci = mode == 0 ? 0 : static_cast<int>(blockIdx.x % n_chunks);
   const int32_t* hrow = hash + bh * T;
   int32_t* prow = perm + bh * T;
   int32_t* srow = hash_sorted + bh * T;
   int32_t* orow = bucket_off + bh * (nb + 1);
+  int32_t* cws = chunk_ws + (bh * n_chunks + ci) * nb;
   int32_t* tot = hist + nw * nb;
   for (int i = threadIdx.x; i < (nw + 1) * nb; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  const int per = ((T + nw - 1) / nw + 31) / 32 * 32;
-  const int b0 = min(T, w * per), b1 = min(T, b0 + per);
+  const int c_begin = mode == 0 ? 0 : min(T, ci * chunk);
+  const int c_end = mode == 0 ? T : min(T, c_begin + chunk);
+  const int len = c_end - c_begin;
+  const int per = ((len + nw - 1) / nw + 31) / 32 * 32;
+  const int b0 = c_begin + min(len, w * per), b1 = c_begin + min(len, w * per + per);
   int32_t* my = hist + w * nb;
   for (int base = b0; base < b1; base += 32) {
     const int i = base + lane;
@@ -765,8 +777,14 @@ __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int 
     tot[c] = run;
   }
   __syncthreads();
-  // exclusive scan of the totals over buckets (warp 0), written to bucket_off
-  if (w == 0) {
+  if (mode == 1) {
+    for (int c = threadIdx.x; c < nb; c += blockDim.x) cws[c] = tot[c];
+    return;
+  }
+  if (mode == 2) {
+    for (int c = threadIdx.x; c < nb; c += blockDim.x) tot[c] = cws[c];
+  } else if (w == 0) {
+    // exclusive scan of the totals over buckets (warp 0), written to bucket_off
     int run = 0;
     for (int base = 0; base < nb; base += 32) {
       const int c = base + lane;
@@ -803,6 +821,51 @@ __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int 
       if (rank == 0) my[h] = start + __popc(peers);
     }
     __syncwarp();
+  }
+}
+
+// Per row (one CTA): bucket_off = exclusive scan over buckets of the summed
+// chunk counts; each chunk's count is replaced by its first output position
+// in that bucket (bucket start + counts of the earlier chunks).
+__global__ void bucket_scan_kernel(int nb, int n_chunks, int32_t* __restrict__ chunk_ws,
+                                   int32_t* __restrict__ bucket_off) {
+  extern __shared__ int32_t tot2[];  // [nb]
+  const long long bh = blockIdx.x;
+  int32_t* cws = chunk_ws + bh * n_chunks * nb;
+  int32_t* orow = bucket_off + bh * (nb + 1);
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+    int run = 0;
+    for (int k = 0; k < n_chunks; ++k) {
+      const int t = cws[k * nb + c];
+      cws[k * nb + c] = run;
+      run += t;
+    }
+    tot2[c] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int run = 0;
+    for (int base = 0; base < nb; base += 32) {
+      const int c = base + lane;
+      const int v = c < nb ? tot2[c] : 0;
+      int x = v;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (c < nb) {
+        tot2[c] = run + x - v;
+        orow[c] = run + x - v;
+      }
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) orow[nb] = run;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+    const int start = tot2[c];
+    for (int k = 0; k < n_chunks; ++k) cws[k * nb + c] += start;
   }
 }
 
@@ -890,7 +953,8 @@ cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long
 }
 
 cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int nb,
-                               int32_t* perm, int32_t* hash_sorted, int32_t* bucket_off, cudaStream_t st) {
+                               int32_t* perm, int32_t* hash_sorted, int32_t* bucket_off, int32_t* chunk_ws,
+                               cudaStream_t st) {
   const size_t budget = 160 * 1024;
   int nw = static_cast<int>(budget / (static_cast<size_t>(nb) * sizeof(int32_t))) - 1;
   if (nw > 32) nw = 32;
@@ -899,7 +963,21 @@ cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int nb,
   cudaError_t e = cudaFuncSetAttribute(bucket_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  bucket_sort_kernel<<<BH, nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off);
+  if (T <= kSortChunk || chunk_ws == nullptr) {
+    bucket_sort_kernel<<<BH, nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off, 0, T, 1, nullptr);
+    return cudaGetLastError();
+  }
+  const int n_chunks = (T + kSortChunk - 1) / kSortChunk;
+  const long long g = static_cast<long long>(BH) * n_chunks;
+  bucket_sort_kernel<<<static_cast<int>(g), nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off, 1,
+                                                                  kSortChunk, n_chunks, chunk_ws);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bucket_scan_kernel<<<BH, 256, static_cast<size_t>(nb) * sizeof(int32_t), st>>>(nb, n_chunks, chunk_ws, bucket_off);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bucket_sort_kernel<<<static_cast<int>(g), nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off, 2,
+                                                                  kSortChunk, n_chunks, chunk_ws);
   return cudaGetLastError();
 }
 

@@ -89,7 +89,8 @@ def test_lsh_hash_tensor_core_path_ties_and_edges(scfa, D, m):
     np.testing.assert_array_equal(h.cpu().numpy(), ref)
 
 
-@pytest.mark.parametrize("B,H,T,D,nb", [(1, 2, 512, 64, 4), (2, 3, 1000, 64, 16), (1, 1, 5000, 64, 512)])
+@pytest.mark.parametrize("B,H,T,D,nb", [(1, 2, 512, 64, 4), (2, 3, 1000, 64, 16), (1, 1, 5000, 64, 512),
+                                        (1, 2, 20000, 64, 64), (1, 1, 40000, 128, 512)])
 def test_bucket_sort_and_gather_bitexact(scfa, B, H, T, D, nb):
     x = synth.normal_bf16(78, 2, (B, H, T, D))
     R = synth.rotation_bf16(78, D, nb // 2)
