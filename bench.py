@@ -407,7 +407,9 @@ def main():
     if bwd_ms >= fwd_ms:
         dom, dom_ms, dom_flops, src = "attn_bwd_kernel", bwd_ms, 10.0 * D * pairs, "attn_bwd.cu"
     else:
-        dom, dom_ms, dom_flops, src = "attn_fwd_kernel", fwd_ms, 4.0 * D * pairs, "attn_fwd.cu"
+        # D = 64 runs the single-query-tile kernel, D = 128 the query-tile-pair kernel
+        dom = "attn_fwd1_kernel" if D == 64 else "attn_fwd_kernel"
+        dom_ms, dom_flops, src = fwd_ms, 4.0 * D * pairs, "attn_fwd.cu"
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     tr = load_traffic(dom)
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
