@@ -96,11 +96,15 @@ def admissible_pairs(wl, prob, step=None) -> int:
     return total
 
 
-def kernels_per_step(mode: str) -> int:
-    tiles = 6            # tile stats (q, k), count, scan, fill, work order
+def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0) -> int:
+    """Library kernels launched per step (the library's own launch sequence)."""
+    tiles = 7            # tile stats (q, k), count, scan, fill, pair union lists, work order
     attn = 1 + 3         # forward; backward pre-pass, backward, dQ finalise
     if mode == "hash":
-        return tiles + attn + 2 * 3 + 2 + 4   # 2 x (hash, sort, gather), gather V / dO, 4 unsorts
+        m = n_buckets // 2
+        lsh = 2 if (D in (64, 128) and m % 8 == 0 and 8 <= m <= 256) else 1  # tensor-core pass + certified pass
+        sort = 3 if T > 8192 else 1                                          # chunk counts, scan, scatter
+        return tiles + attn + 2 * (lsh + sort + 1) + 2 + 4   # per q / k: hash, sort, gather; gather V / dO; 4 unsorts
     return tiles + attn
 
 
@@ -479,7 +483,8 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
             "pct_of_bf16_peak": 100.0 * (value / world) / peak,
             "dense": dense, "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
-            "gpu_launches": kernels_per_step(wl.mode) * args.steps, "clocks": clocks,
+            "gpu_launches": kernels_per_step(wl.mode, wl.D, wl.T, getattr(wl, "n_buckets", 0)) * args.steps,
+            "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
