@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __r
 // single-thread path (576-bit accumulator) on lane 0.
 constexpr int kFixWarps = 8;
 
-__global__ void __launch_bounds__(kFixWarps * 32) lsh_fix_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(kFixWarps * 32, 1) lsh_fix_kernel(const uint16_t* __restrict__ x,
                                                                  const uint16_t* __restrict__ R, long long rows,
                                                                  int D, int m, int32_t* __restrict__ hash) {
   extern __shared__ float smem[];
@@ -424,13 +424,23 @@ __global__ void __launch_bounds__(kFixWarps * 32) lsh_fix_kernel(const uint16_t*
                        1.000001f;
       const float emax = l2 * rnmax * rel * 1.000001f + absb;
       const float thr = 2.f * emax * 1.0001f;
-      // fp32 values of this lane's columns; the warp's top value
-      float best_v = -INFINITY;
-      for (int c = lane; c < m; c += 32) {
-        float sc = 0.f;
-        for (int d = 0; d < D; ++d) sc = fmaf(sx[d], sR[d * m4 + c], sc);
-        best_v = fmaxf(best_v, fmaxf(sc, -sc));
+      // fp32 values of this lane's columns c = lane + 32 k (m <= 256: k < 8),
+      // each summed over d in order; the warp's top value
+      float scv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) scv[k] = 0.f;
+      for (int d = 0; d < D; ++d) {
+        const float xv = sx[d];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c = lane + 32 * k;
+          if (c < m) scv[k] = fmaf(xv, sR[d * m4 + c], scv[k]);
+        }
       }
+      float best_v = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (lane + 32 * k < m) best_v = fmaxf(best_v, fmaxf(scv[k], -scv[k]));
       float t0 = best_v;
       for (int o = 16; o; o >>= 1) t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
       // exact values of the candidates (within thr of the top, or NaN)
@@ -442,9 +452,11 @@ __global__ void __launch_bounds__(kFixWarps * 32) lsh_fix_kernel(const uint16_t*
         bool have = false;
         __int128 bv = 0;
         int bj = 0;
-        for (int c = lane; c < m; c += 32) {
-          float sc = 0.f;
-          for (int d = 0; d < D; ++d) sc = fmaf(sx[d], sR[d * m4 + c], sc);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c = lane + 32 * k;
+          if (c >= m) continue;
+          const float sc = scv[k];
           const bool cp = (t0 - sc <= thr) || (sc != sc);
           const bool cn = (t0 + sc <= thr) || (sc != sc);
           if (!cp && !cn) continue;
@@ -511,12 +523,12 @@ __global__ void __launch_bounds__(kFixWarps * 32) lsh_fix_kernel(const uint16_t*
 // D additions each losing 2^-23 of a partial sum at D = 128, 8x at D = 64);
 // every other row, and every row with a subnormal, non-finite or huge value,
 // is left at -1 for the certified second pass (lsh_fix_kernel).
-// Roles (192 threads): warp 0 TMA producer (x tiles, 4 stages), warp 1 MMA
-// issuer and TMEM owner (two accumulators of m_pad columns), warps 2-5
-// epilogue (thread = row = TMEM lane). R sits in shared memory for the whole
+// Roles (320 threads): warp 0 TMA producer (x tiles, 4 stages), warp 1 MMA
+// issuer and TMEM owner (two accumulators of m_pad columns), warps 2-5 and
+// 6-9 epilogue for even / odd tiles (thread = row = TMEM lane). R sits in shared memory for the whole
 // kernel as the MN-major B operand ([D][64]-column swizzled sub-tiles).
 // ---------------------------------------------------------------------------
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;  // producer, MMA, two epilogue warpgroups (alternate tiles)
 constexpr int kTcStages = 4;
 constexpr float kTcRel = 0x1p-14f;
 
@@ -650,12 +662,14 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
+    const int eg = (warp - 2) >> 2;      // epilogue warpgroup: tiles it with it % 2 == eg
     const int rr = quarter * 32 + lane;  // row of the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float rnmax = sm.rnmax;
     const bool r_bad = sm.r_bad != 0;
-    int it = 0;
-    for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+    int it = eg;
+    for (long long t = blockIdx.x + static_cast<long long>(eg) * gridDim.x; t < n_tiles;
+         t += 2ll * gridDim.x, it += 2) {
       const int s = it % kTcStages, b = it & 1;
       bool ok = mbar_wait(&sm.acc_full[b], (it >> 1) & 1, abort_flag, status);
       if (!__all_sync(0xffffffffu, ok)) break;
