@@ -6,7 +6,10 @@ sparse attention forward and backward on the sorted rows, and puts O, dQ, dK
 and dV back in original order ("Faster Causal Attention Over Large Sequences
 Through Sparse Flash Attention", deep-paper.org, sections "动态稀疏性为何会破坏它"
 and "SCFA 解决方案" part 2). LSE stays in sorted query order (the backward
-consumes it there). Buffers are allocated once per shape and reused.
+consumes it there). Buffers are allocated once per shape and reused. The
+query side and the key side of the hash step are independent until the
+attention, so the key side runs on a second stream (and so do the unsorts
+of dK and dV), joined by events.
 """
 from __future__ import annotations
 
@@ -40,6 +43,9 @@ class Step:
         if mode == MODE_HASH:
             T = Tq
             self.ws_l = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
+            self.ws_lk = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
+            self.side = torch.cuda.Stream(device=dev)
+            self.ev = [torch.cuda.Event() for _ in range(4)]
             self.qh = torch.empty((B, H, T), **i32)
             self.kh = torch.empty((B, H, T), **i32)
             self.pq = torch.empty((B, H, T), **i32)
@@ -68,16 +74,27 @@ class Step:
                         fr, stream)
         else:
             nb = self.nb
-            lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, stream)
-            lsh_bucket_sort(k, R, nb, self.kh, self.pk, self.offk, self.k_s, self.ws_l, 0, stream)
-            lsh_gather(v, self.pk, self.v_s, stream)
+            main = stream if stream is not None else torch.cuda.current_stream()
+            side = self.side
+            # key side (hash, sort, K and V gathers) on the second stream
+            self.ev[0].record(main)
+            side.wait_event(self.ev[0])
+            lsh_bucket_sort(k, R, nb, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
+            lsh_gather(v, self.pk, self.v_s, side)
+            self.ev[1].record(side)
+            lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
+            lsh_gather(do, self.pq, self.do_s, main)
+            main.wait_event(self.ev[1])
             scfa_hash_fwd(self.q_s, self.k_s, self.v_s, self.pq, self.pk, self.qh, self.kh, scale, self.o_s,
-                          self.lse, self.ws_f, f, stream)
-            lsh_gather(do, self.pq, self.do_s, stream)
+                          self.lse, self.ws_f, f, main)
             scfa_hash_bwd(self.q_s, self.k_s, self.v_s, self.o_s, self.lse, self.do_s, self.pq, self.pk, self.qh,
-                          self.kh, scale, self.dq_s, self.dk_s, self.dv_s, self.ws_b, fr, stream)
-            lsh_unsort(self.o_s, self.pq, self.o, stream)
-            lsh_unsort(self.dq_s, self.pq, self.dq, stream)
-            lsh_unsort(self.dk_s, self.pk, self.dk, stream)
-            lsh_unsort(self.dv_s, self.pk, self.dv, stream)
+                          self.kh, scale, self.dq_s, self.dk_s, self.dv_s, self.ws_b, fr, main)
+            self.ev[2].record(main)
+            side.wait_event(self.ev[2])
+            lsh_unsort(self.dk_s, self.pk, self.dk, side)
+            lsh_unsort(self.dv_s, self.pk, self.dv, side)
+            self.ev[3].record(side)
+            lsh_unsort(self.o_s, self.pq, self.o, main)
+            lsh_unsort(self.dq_s, self.pq, self.dq, main)
+            main.wait_event(self.ev[3])
         return self
