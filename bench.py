@@ -98,7 +98,7 @@ def admissible_pairs(wl, prob, step=None) -> int:
 
 def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0) -> int:
     """Library kernels launched per step (the library's own launch sequence)."""
-    tiles = 7            # tile stats (q, k), count, scan, fill, pair union lists, work order
+    tiles = 6 + (1 if D == 128 else 0)  # tile stats (q, k), count, scan, fill, work order (+ pair lists at D = 128)
     attn = 1 + 3         # forward; backward pre-pass, backward, dQ finalise
     if mode == "hash":
         m = n_buckets // 2

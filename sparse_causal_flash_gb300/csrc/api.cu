@@ -183,7 +183,7 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   char* w = static_cast<char*>(ws);
   cudaError_t e = cudaSuccess;
   if (!(flags & SCFA_FLAG_REUSE_TILES)) {
-    e = launch_tiles(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, flags, w, L, st);
+    e = launch_tiles(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, flags, w, L, st, D == 128);
     if (e != cudaSuccess) return SCFA_ERR_CUDA;
   }
   AttnArgs a;

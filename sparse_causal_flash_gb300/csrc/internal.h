@@ -54,10 +54,12 @@ bool lsh_ws_layout(int B, int H, int T, int n_buckets, LshWs* L);
 int num_sms();
 
 // tiles.cu
+// with_pairs: also build the union lists and order of query-tile pairs (the
+// head-dimension-128 forward walks those)
 cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
                          const int32_t* q_hash, const int32_t* k_hash,
                          int B, int H, int Tq, int Tk, unsigned flags,
-                         char* ws, const AttnWs& L, cudaStream_t st);
+                         char* ws, const AttnWs& L, cudaStream_t st, bool with_pairs = true);
 
 // lsh.cu
 // status: a device int the tensor-core path may raise a timeout in (NULL keeps

@@ -296,7 +296,8 @@ struct OrderList {
   int32_t* gcur;
 };
 
-constexpr int kOrderChunk = 4096;  // counts staged in shared memory per scatter round
+constexpr int kOrderChunk = 4096;     // counts staged in shared memory per scatter round
+constexpr int kOrderWarpBins = 8192;  // per-warp bin offsets (few distinct counts)
 
 // Stable counting sort of ids by count, descending: block 0 builds the
 // forward order (query tiles), block 1 the backward order (key tiles), block
@@ -332,10 +333,55 @@ __global__ void work_order_kernel(OrderList l0, OrderList l1, OrderList l2, int 
       running += __shfl_sync(0xffffffffu, x, 31);
     }
   }
+  // few distinct counts: all 32 warps scatter, each a contiguous slice of the
+  // chunk, from per-warp bin offsets (earlier slices first: stable)
+  const int nwarps = static_cast<int>(blockDim.x >> 5), wid = static_cast<int>(threadIdx.x >> 5);
+  int32_t* hw = chunk + kOrderChunk;  // [nwarps][maxc + 1]
+  const bool parallel = (maxc + 1) * nwarps <= kOrderWarpBins;
   for (long long c0 = 0; c0 < n; c0 += kOrderChunk) {
     const int len = static_cast<int>(min(static_cast<long long>(kOrderChunk), n - c0));
     __syncthreads();  // the previous chunk is scattered (and the scan above is done)
     for (int t = threadIdx.x; t < len; t += blockDim.x) chunk[t] = min(max(cnt[c0 + t], 0), maxc);
+    if (parallel) {
+      for (int i = threadIdx.x; i < (maxc + 1) * nwarps; i += blockDim.x) hw[i] = 0;
+      __syncthreads();
+      const int per = (len + nwarps - 1) / nwarps;
+      const int s0 = min(len, wid * per), s1 = min(len, s0 + per);
+      int32_t* my = hw + wid * (maxc + 1);
+      for (int base = s0; base < s1; base += 32) {
+        const int t = base + lane;
+        const int cc = t < s1 ? chunk[t] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, cc);
+        if (cc >= 0 && (peers & ((1u << lane) - 1u)) == 0) my[cc] += __popc(peers);
+        __syncwarp();
+      }
+      __syncthreads();
+      for (int c = threadIdx.x; c <= maxc; c += blockDim.x) {
+        int run = cur[c];
+        for (int w = 0; w < nwarps; ++w) {
+          const int t = hw[w * (maxc + 1) + c];
+          hw[w * (maxc + 1) + c] = run;
+          run += t;
+        }
+        cur[c] = run;
+      }
+      __syncthreads();
+      for (int base = s0; base < s1; base += 32) {
+        const int t = base + lane;
+        const bool active = t < s1;
+        const int cc = active ? chunk[t] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, cc);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        const int start = active ? my[cc] : 0;
+        __syncwarp();
+        if (active) {
+          out[start + rank] = static_cast<int32_t>(c0 + t);
+          if (rank == 0) my[cc] = start + __popc(peers);
+        }
+        __syncwarp();
+      }
+      continue;
+    }
     __syncthreads();
     if (threadIdx.x < 32) {
       for (int base = 0; base < len; base += 32) {
@@ -368,7 +414,7 @@ inline int grid_for(long long work, int block, int max_blocks) {
 cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
                          const int32_t* q_hash, const int32_t* k_hash,
                          int B, int H, int Tq, int Tk, unsigned flags,
-                         char* ws, const AttnWs& L, cudaStream_t st) {
+                         char* ws, const AttnWs& L, cudaStream_t st, bool with_pairs) {
   const int sms = num_sms();
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
   int4* qstat = reinterpret_cast<int4*>(ws + L.qstat);
@@ -392,11 +438,12 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
       c, L.n_qtiles, L.n_ktiles, row_ptr, reinterpret_cast<int32_t*>(ws + L.cols),
       reinterpret_cast<uint8_t*>(ws + L.fflags), csc_ptr, reinterpret_cast<int32_t*>(ws + L.csc_rows),
       reinterpret_cast<uint8_t*>(ws + L.cflags));
-  pair_list_kernel<<<grid_for(L.n_pairs * 32, 256, sms * 8), 256, 0, st>>>(
+  if (with_pairs)
+    pair_list_kernel<<<grid_for(L.n_pairs * 32, 256, sms * 8), 256, 0, st>>>(
       row_ptr, reinterpret_cast<const int32_t*>(ws + L.cols), reinterpret_cast<const uint8_t*>(ws + L.fflags),
       L.nQt, L.nPairs, L.n_pairs, reinterpret_cast<int32_t*>(ws + L.pcount), reinterpret_cast<int32_t*>(ws + L.ulist));
   const int smem_bins = 12 * 1024;  // 48 KB of shared memory; larger histograms use the workspace
-  const size_t smem = static_cast<size_t>(smem_bins + kOrderChunk) * sizeof(int32_t);
+  const size_t smem = static_cast<size_t>(smem_bins + kOrderChunk + kOrderWarpBins) * sizeof(int32_t);
   static bool order_smem_set[64] = {};
   int dev = 0;
   e = cudaGetDevice(&dev);
@@ -409,7 +456,7 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
   int32_t* gcur = reinterpret_cast<int32_t*>(ws + L.cursor);
   OrderList lf{qcount, L.n_qtiles, L.nKt, reinterpret_cast<int32_t*>(ws + L.work_fwd), gcur};
   OrderList lb{kcount, L.n_ktiles, L.nQt, reinterpret_cast<int32_t*>(ws + L.work_bwd), gcur + L.nKt + 1};
-  OrderList lp{reinterpret_cast<const int32_t*>(ws + L.pcount), L.n_pairs, L.nKt,
+  OrderList lp{reinterpret_cast<const int32_t*>(ws + L.pcount), with_pairs ? L.n_pairs : 0, L.nKt,
                reinterpret_cast<int32_t*>(ws + L.work_pairs), gcur + L.nKt + L.nQt + 2};
   work_order_kernel<<<3, 1024, smem, st>>>(lf, lb, lp, smem_bins);
   return cudaGetLastError();
