@@ -933,7 +933,7 @@ static cudaError_t launch_lsh_tc(const uint16_t* x, const uint16_t* R, long long
   e = cudaFuncSetAttribute(lsh_fix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem2));
   if (e != cudaSuccess) return e;
   long long g2 = (rows + kFixWarps * 32 - 1) / (kFixWarps * 32);
-  if (g2 > static_cast<long long>(num_sms()) * 2) g2 = static_cast<long long>(num_sms()) * 2;
+  if (g2 > static_cast<long long>(num_sms())) g2 = static_cast<long long>(num_sms());  // one wave
   if (g2 < 1) g2 = 1;
   lsh_fix_kernel<<<static_cast<int>(g2), kFixWarps * 32, smem2, st>>>(x, R, rows, D, m, hash);
   return cudaGetLastError();
