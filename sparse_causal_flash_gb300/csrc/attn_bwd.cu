@@ -66,6 +66,7 @@ struct __align__(1024) BwdSmem {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t s_full, st_empty, ds_full, pt_free, ds_free[2], dq_full, dq_empty, dkv_full, dkv_empty, drain;
+  uint64_t dq_sync;  // the 128 threads of the dQ warpgroup around the staging tile
   int32_t items[kBwdSlots];
   uint64_t item_full[kBwdSlots], item_empty[kBwdSlots];
   uint32_t tmem_base;
@@ -135,6 +136,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&sm.dkv_full, 1);
     mbar_init(&sm.dkv_empty, 256);
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.dq_sync, 128);
     for (int s = 0; s < kBwdSlots; ++s) {
       mbar_init(&sm.item_full[s], 1);
       mbar_init(&sm.item_empty[s], 1 + 256 + 128);  // MMA thread, compute and dQ warpgroups
@@ -509,7 +511,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int qr = quarter * 32 + lane;  // query row = TMEM lane
     const int tid = threadIdx.x - 320;   // 0..127
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    int it = 0;
+    int it = 0, x_it = 0;
+    // bounded sync of the dQ warpgroup (a broken pipeline ends in a status
+    // code instead of a hang at a named barrier)
+    auto dq_group_sync = [&]() -> bool {
+      mbar_arrive(&sm.dq_sync);
+      const bool r_ok = mbar_wait(&sm.dq_sync, x_it & 1, abort_flag, p.status);
+      ++x_it;
+      return __all_sync(0xffffffffu, r_ok);
+    };
     for (int slot_it = 0;; ++slot_it) {
       const int slot = slot_it % kBwdSlots;
       const bool got = mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status);
@@ -539,18 +549,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (tid == 0) bulk_wait_group_read0();
-          named_bar_sync(2, 128);
+          if (!dq_group_sync()) { ok = false; break; }
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(sm.dqs + sw128_offset(qr, c)) =
                 make_uint4(qv[h][c * 4], qv[h][c * 4 + 1], qv[h][c * 4 + 2], qv[h][c * 4 + 3]);
           fence_proxy_async_smem();
-          named_bar_sync(2, 128);
+          if (!dq_group_sync()) { ok = false; break; }
           if (tid == 0) {
             tma_reduce_add_3d(&tm_dq, sm.dqs, 64 * hh + h * 32, i * kTile, bh);
             bulk_commit_group();
           }
         }
+        if (!ok) break;
         ++it;
       }
       if (!ok) break;

@@ -70,6 +70,7 @@ struct __align__(1024) FwdSmem {
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2], drain[2];
   uint64_t s_free[2], pv_done[2];  // used when P has its own TMEM columns
+  uint64_t kbar[2];                // the 128 softmax threads of query tile g around masked-tile keys
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -122,6 +123,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&sm.o_empty[g], 128);
       mbar_init(&sm.s_free[g], 128);
       mbar_init(&sm.pv_done[g], 1);
+      mbar_init(&sm.kbar[g], 128);
     }
     mbar_init(&sm.drain[0], 1);
     mbar_init(&sm.drain[1], 1);
@@ -288,9 +290,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;          // row of the tile = TMEM lane
     const int tid = (warp - 2 - 4 * grp) * 32 + lane;  // 0..127 for cooperative staging
-    const int bar_id = 1 + grp;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     constexpr bool kSepP = fwd_separate_p<D>();
+    int x_it = 0;
+    // bounded sync of this query tile's 128 softmax threads (a broken
+    // pipeline ends in a status code instead of a hang at a named barrier)
+    auto group_sync = [&]() -> bool {
+      mbar_arrive(&sm.kbar[grp]);
+      const bool r_ok = mbar_wait(&sm.kbar[grp], x_it & 1, abort_flag, p.status);
+      ++x_it;
+      return __all_sync(0xffffffffu, r_ok);
+    };
     const uint32_t colS = 128u * grp, colO = 256u + D * grp;
     const uint32_t colP = kSepP ? 384u + 64u * grp : colS;
     int n_p = 0;  // P_g tiles written so far
@@ -351,7 +361,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!full) {
           sm.kidx[grp][b][tid] = kid;
           if (p.mode == SCFA_MODE_HASH) sm.khash[grp][b][tid] = khv;
-          named_bar_sync(bar_id, 128);
+          if (!group_sync()) { ok = false; break; }
         }
         ok = mbar_wait(&sm.s_full[grp], s_it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
