@@ -409,7 +409,9 @@ def main():
     long_region = (t1 - t0) > 1.0
     peak = peak_sus if long_region else peak_burst
     if bwd_ms >= fwd_ms:
-        dom, dom_ms, dom_flops, src = "attn_bwd_kernel", bwd_ms, 10.0 * D * pairs, "attn_bwd.cu"
+        # D = 128 runs the full-D key-tile kernel
+        dom = "attn_bwd_kernel" if D == 64 else "attn_bwd128_kernel"
+        dom_ms, dom_flops, src = bwd_ms, 10.0 * D * pairs, "attn_bwd.cu"
     else:
         # D = 64 runs the single-query-tile kernel, D = 128 the query-tile-pair kernel
         dom = "attn_fwd1_kernel" if D == 64 else "attn_fwd_kernel"

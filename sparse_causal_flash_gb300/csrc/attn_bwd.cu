@@ -584,6 +584,464 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Head dimension 128, one work item per key tile (the whole of D). TMEM:
+// S^T [0,128) with P^T overwriting its first 64 columns once both compute
+// warpgroups have read S^T; dP^T [128,256) with dQ overwriting it once read;
+// dV [256,384) and dK [384,512) accumulate over the key tile's query tiles.
+// Per query tile the MMA warp issues S^T and dP^T (dP^T after the dQ
+// warpgroup has read the previous dQ), then dV, dK, dQ; one thread's MMAs run
+// in order, so S^T(t+1) cannot overtake dV(t) reading P^T. Q and dO have one
+// stage each, released separately (dO after dV, Q after dK), so the next
+// tile's dO load starts while dK and dQ still run. dQ leaves TMEM in two
+// rounds of 64 columns through two 16 KB staging tiles and TMA reduce-adds.
+// ---------------------------------------------------------------------------
+struct __align__(1024) Bwd128Smem {
+  uint8_t k[2][kSubBytes];
+  uint8_t v[2][kSubBytes];
+  uint8_t q[2][kSubBytes];
+  uint8_t dO[2][kSubBytes];
+  uint8_t dst[2][kSubBytes];   // dS^T [query half][128 keys x 64 queries]
+  uint8_t dqs[2][kSubBytes];   // dQ staging: [128 rows x 32 floats] each
+  int32_t qidx[2][kTile];      // query metadata by step parity
+  int32_t qhash[2][kTile];
+  float lse2[2][kTile];        // -LSE * log2(e)
+  float drs[2][kTile];         // -rowsum(dO * O) * scale
+  uint64_t kv_full, kv_empty, q_full, q_empty, do_empty, s_full, loaded, ds_full;
+  uint64_t dq_full, dq_empty, dkv_full, dkv_empty, drain, dq_sync;
+  int32_t items[kBwdSlots];
+  uint64_t item_full[kBwdSlots], item_empty[kBwdSlots];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(kBwdThreads, 1)
+attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  Bwd128Smem& sm = *reinterpret_cast<Bwd128Smem*>(smem_raw + pad);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr uint32_t kColS = 0, kColPT = 0, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK = 384;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.kv_full, 1);
+    mbar_init(&sm.kv_empty, 1);
+    mbar_init(&sm.q_full, 2);
+    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.do_empty, 1);
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.loaded, 256);
+    mbar_init(&sm.ds_full, 256);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_empty, 128);
+    mbar_init(&sm.dkv_full, 1);
+    mbar_init(&sm.dkv_empty, 256);
+    mbar_init(&sm.drain, 1);
+    mbar_init(&sm.dq_sync, 128);
+    for (int s = 0; s < kBwdSlots; ++s) {
+      mbar_init(&sm.item_full[s], 1);
+      mbar_init(&sm.item_empty[s], 1 + 256 + 128);
+    }
+    sm.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
+  }
+  if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer warp
+    int qt = 0, item = 0, last_kv = -1;
+    for (int slot_it = 0;; ++slot_it) {
+      int w = INT_MAX;
+      if (lane == 0) {
+        const int slot = slot_it % kBwdSlots;
+        if (mbar_wait(&sm.item_empty[slot], ((slot_it / kBwdSlots) & 1) ^ 1, abort_flag, p.status)) {
+          w = atomicAdd(&p.sched[0], 1);
+          sm.items[slot] = w < p.n_work ? w : -1;
+          mbar_arrive(&sm.item_full[slot]);
+        }
+      }
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w >= p.n_work) break;
+      const int g = p.work[w];
+      const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
+      if (n == 0) continue;
+      const int bh = g / p.nKt, j = g % p.nKt;
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&sm.kv_empty, (item & 1) ^ 1, abort_flag, p.status);
+        if (ok) {
+          mbar_arrive_expect_tx(&sm.kv_full, 2 * D * kTile * 2);
+          for (int sub = 0; sub < 2; ++sub) {
+            tma_load_3d(sm.k[sub], &tm_k, &sm.kv_full, sub * 64, j * kTile, bh);
+            tma_load_3d(sm.v[sub], &tm_v, &sm.kv_full, sub * 64, j * kTile, bh);
+          }
+          last_kv = item;
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      for (int t = 0; t < n; ++t) {
+        const int i = p.csc_rows[start + t];
+        const int mb = qt & 1;
+        if (lane == 0) {
+          // dO once dV of the previous tile has read it, Q once dK has
+          ok = mbar_wait(&sm.do_empty, (qt & 1) ^ 1, abort_flag, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.q_full, 2 * D * kTile * 2);
+            for (int sub = 0; sub < 2; ++sub) tma_load_3d(sm.dO[sub], &tm_do, &sm.q_full, sub * 64, i * kTile, bh);
+            ok = mbar_wait(&sm.q_empty, (qt & 1) ^ 1, abort_flag, p.status);
+            if (ok)
+              for (int sub = 0; sub < 2; ++sub) tma_load_3d(sm.q[sub], &tm_q, &sm.q_full, sub * 64, i * kTile, bh);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+        {
+          int qid[4], qhv[4];
+          float lsev[4], drv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = lane + 32 * u;
+            const int qrow = i * kTile + c;
+            const bool qv = qrow < p.Tq;
+            const long long gq = static_cast<long long>(bh) * p.Tq + (qv ? qrow : 0);
+            qid[u] = (p.mode == SCFA_MODE_DENSE) ? (qv ? qrow : INT_MIN) : (qv ? p.q_idx[gq] : INT_MIN);
+            qhv[u] = (p.mode == SCFA_MODE_HASH && qv) ? p.q_hash[gq] : 0;
+            lsev[u] = qv ? p.lse[gq] : 0.f;
+            drv[u] = qv ? p.drow[gq] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = lane + 32 * u;
+            sm.qidx[mb][c] = qid[u];
+            sm.qhash[mb][c] = qhv[u];
+            sm.lse2[mb][c] = -(lsev[u] * kLog2e);
+            sm.drs[mb][c] = -(drv[u] * p.scale);
+          }
+        }
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.q_full);
+        ++qt;
+      }
+      if (!ok) break;
+      ++item;
+    }
+    if (lane == 0) {
+      if (qt > 0) mbar_wait(&sm.q_full, (qt - 1) & 1, abort_flag, p.status);
+      if (last_kv >= 0) mbar_wait(&sm.kv_full, last_kv & 1, abort_flag, p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
+      constexpr uint32_t idesc_kv = idesc_bf16_f32(kTile, D, 0, 1);  // dV, dK: N = D, B MN-major
+      constexpr uint32_t idesc_q = idesc_bf16_f32(kTile, D, 1, 1);   // dQ: A = dS (MN-major), B = K (MN-major)
+      const uint64_t kdesc_k = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t vdesc_k = smem_desc_sw128(smem_u32(sm.v[0]), 16, 1024);
+      const uint64_t kdesc_mn = smem_desc_sw128(smem_u32(sm.k[0]), kSubBytes, 1024);
+      const uint64_t qdesc_k = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t qdesc_mn = smem_desc_sw128(smem_u32(sm.q[0]), kSubBytes, 1024);
+      const uint64_t odesc_k = smem_desc_sw128(smem_u32(sm.dO[0]), 16, 1024);
+      const uint64_t odesc_mn = smem_desc_sw128(smem_u32(sm.dO[0]), kSubBytes, 1024);
+      const uint64_t sdesc_k = smem_desc_sw128(smem_u32(sm.dst[0]), 16, 1024);
+      const uint64_t sdesc_mn = smem_desc_sw128(smem_u32(sm.dst[0]), kSubBytes, 1024);
+      int it = 0, item = 0;
+      bool ok = true;
+      for (int slot_it = 0; ok; ++slot_it) {
+        const int slot = slot_it % kBwdSlots;
+        if (!mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status)) break;
+        const int w = sm.items[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        if (w < 0) break;
+        const int g = p.work[w];
+        const int n = p.csc_ptr[g + 1] - p.csc_ptr[g];
+        if (n == 0) continue;
+        if (!mbar_wait(&sm.kv_full, item & 1, abort_flag, p.status)) break;
+        for (int t = 0; t < n; ++t) {
+          // S^T = K Q^T, then dP^T = V dO^T once dQ of the previous tile is out of TMEM
+          if (!mbar_wait(&sm.q_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(tmem + kColS, kdesc_k + kstep_off16(kk, kSubBytes), qdesc_k + kstep_off16(kk, kSubBytes),
+                        idesc_s, kk > 0);
+          if (it > 0 && !mbar_wait(&sm.dq_empty, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(tmem + kColDP, vdesc_k + kstep_off16(kk, kSubBytes), odesc_k + kstep_off16(kk, kSubBytes),
+                        idesc_s, kk > 0);
+          tc_commit(&sm.s_full);
+          // P^T in TMEM and dS^T in shared memory from the compute warps
+          if (!mbar_wait(&sm.ds_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+          if (t == 0 && !mbar_wait(&sm.dkv_empty, (item & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t acc0 = t > 0 ? 1u : 0u;
+          // dV += P^T dO (A = P^T in TMEM)
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ts(tmem + kColDV, tmem + kColPT + kk * 8, odesc_mn + static_cast<uint64_t>(kk * 128), idesc_kv,
+                        kk > 0 ? 1u : acc0);
+          tc_commit(&sm.do_empty);
+          // dK += dS^T Q
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss(tmem + kColDK, sdesc_k + kstep_off16(kk, kSubBytes), qdesc_mn + static_cast<uint64_t>(kk * 128),
+                        idesc_kv, kk > 0 ? 1u : acc0);
+          tc_commit(&sm.q_empty);
+          // dQ_i = dS K into the dP^T columns (read by now)
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_bf16_ss(tmem + kColDQ, sdesc_mn + static_cast<uint64_t>(kk * 128),
+                        kdesc_mn + static_cast<uint64_t>(kk * 128), idesc_q, kk > 0 ? 1u : 0u);
+          tc_commit(&sm.dq_full);
+          ++it;
+        }
+        if (!ok) break;
+        tc_commit(&sm.dkv_full);
+        tc_commit(&sm.kv_empty);
+        ++item;
+      }
+      tc_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0, abort_flag, p.status);
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ P^T / dS^T warpgroups
+    const int grp = (warp - 2) >> 2;       // 0: query columns 0-63, 1: 64-127
+    const int quarter = warp & 3;
+    const int kr = quarter * 32 + lane;    // key row = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    int it = 0, item = 0;
+    for (int slot_it = 0;; ++slot_it) {
+      const int slot = slot_it % kBwdSlots;
+      const bool got = mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, got)) break;
+      const int w = sm.items[slot];
+      mbar_arrive(&sm.item_empty[slot]);
+      if (w < 0) break;
+      const int g = p.work[w];
+      const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
+      const int bh = g / p.nKt, j = g % p.nKt;
+      const int key = j * kTile + kr;
+      const bool kvalid = key < p.Tk;
+      const long long gk = static_cast<long long>(bh) * p.Tk + key;
+      if (n == 0) {
+        if (kvalid) {
+          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + gk * D);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) a[c] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      int ki, kh = 0;
+      if (p.mode == SCFA_MODE_DENSE) ki = kvalid ? key : INT_MAX;
+      else ki = kvalid ? p.k_idx[gk] : INT_MAX;
+      if (p.mode == SCFA_MODE_HASH && kvalid) kh = p.k_hash[gk];
+      bool ok = true;
+      for (int t = 0; t < n; ++t) {
+        const bool full = (p.cflags[start + t] & kFlagFull) != 0;
+        const int mb = it & 1;
+        ok = mbar_wait(&sm.q_full, it & 1, abort_flag, p.status) &&
+             mbar_wait(&sm.s_full, it & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        const float* lse2 = sm.lse2[mb] + grp * 64;
+        const float* drs = sm.drs[mb] + grp * 64;
+        const int* qid = sm.qidx[mb] + grp * 64;
+        const int* qhs = sm.qhash[mb] + grp * 64;
+        const uint64_t sl2 = f2(p.scale_log2, p.scale_log2), sc2 = f2(p.scale, p.scale);
+        auto chunk = [&](int c, const uint32_t (&sr)[32], const uint32_t (&dr)[32], uint32_t (&pk)[16],
+                         uint32_t (&dk16)[16]) {
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const int e = e4 * 4;
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 32 + e);
+            const float4 d4 = *reinterpret_cast<const float4*>(drs + c * 32 + e);
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              const uint64_t nl = u == 0 ? f2(l4.x, l4.y) : f2(l4.z, l4.w);
+              const uint64_t nd = u == 0 ? f2(d4.x, d4.y) : f2(d4.z, d4.w);
+              float a0, a1;
+              f2_split(fma2(f2(__uint_as_float(sr[e + u]), __uint_as_float(sr[e + u + 1])), sl2, nl), a0, a1);
+              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+              const uint64_t tt = fma2(f2(__uint_as_float(dr[e + u]), __uint_as_float(dr[e + u + 1])), sc2, nd);
+              float d0, d1;
+              f2_split(mul2(f2(p0, p1), tt), d0, d1);
+              pk[e4 * 2 + u / 2] = pack_bf16x2(p0, p1);
+              dk16[e4 * 2 + u / 2] = pack_bf16x2(d0, d1);
+            }
+          }
+          if (!full) {
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const int e = e4 * 4;
+              const int4 q4 = *reinterpret_cast<const int4*>(qid + c * 32 + e);
+              bool adm[4] = {q4.x >= ki, q4.y >= ki, q4.z >= ki, q4.w >= ki};
+              if (p.mode == SCFA_MODE_HASH) {
+                const int4 h4 = *reinterpret_cast<const int4*>(qhs + c * 32 + e);
+                adm[0] = adm[0] && h4.x == kh;
+                adm[1] = adm[1] && h4.y == kh;
+                adm[2] = adm[2] && h4.z == kh;
+                adm[3] = adm[3] && h4.w == kh;
+              }
+#pragma unroll
+              for (int u = 0; u < 4; u += 2) {
+                const uint32_t keep = (adm[u] ? 0x0000ffffu : 0u) | (adm[u + 1] ? 0xffff0000u : 0u);
+                pk[e4 * 2 + u / 2] &= keep;
+                dk16[e4 * 2 + u / 2] &= keep;
+              }
+            }
+          }
+        };
+        uint32_t pk[2][16], dsk[2][16];
+        {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(lane_base + kColS + grp * 64, sr);
+          tmem_ld32(lane_base + kColDP + grp * 64, dr);
+          tmem_wait_ld();
+          chunk(0, sr, dr, pk[0], dsk[0]);
+        }
+        {
+          uint32_t sr[32], dr[32];
+          tmem_ld32(lane_base + kColS + grp * 64 + 32, sr);
+          tmem_ld32(lane_base + kColDP + grp * 64 + 32, dr);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&sm.loaded);  // this thread's S^T / dP^T columns are in registers
+          chunk(1, sr, dr, pk[1], dsk[1]);
+        }
+        // P^T overwrites S^T columns 0-63: both warpgroups must have read them
+        ok = mbar_wait(&sm.loaded, it & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* dsh = sm.dst[grp];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_st16(lane_base + kColPT + grp * 32 + c * 16, pk[c]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(dsh + sw128_offset(kr, c * 4 + u)) =
+                make_uint4(dsk[c][u * 4], dsk[c][u * 4 + 1], dsk[c][u * 4 + 2], dsk[c][u * 4 + 3]);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&sm.ds_full);
+        ++it;
+      }
+      if (!ok) break;
+      // item epilogue: group 0 writes dV, group 1 writes dK, 64 columns at a time
+      ok = mbar_wait(&sm.dkv_full, item & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t col = grp == 0 ? kColDV : kColDK;
+      uint16_t* orow = (grp == 0 ? p.dv : p.dk) + gk * D;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t acc[2][32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) tmem_ld32(lane_base + col + hf * 64 + cc * 32, acc[cc]);
+        tmem_wait_ld();
+        if (hf == 1) {
+          tc_fence_before();
+          mbar_arrive(&sm.dkv_empty);
+        }
+        if (kvalid) store_row_bf16(orow + 64 * hf, &acc[0][0], 64);
+      }
+      ++item;
+    }
+  } else {
+    // ------------------------------------------------------------ dQ warpgroup
+    const int quarter = warp & 3;
+    const int qr = quarter * 32 + lane;  // query row = TMEM lane
+    const int tid = threadIdx.x - 320;   // 0..127
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    int it = 0, x_it = 0;
+    auto dq_group_sync = [&]() -> bool {
+      mbar_arrive(&sm.dq_sync);
+      const bool r_ok = mbar_wait(&sm.dq_sync, x_it & 1, abort_flag, p.status);
+      ++x_it;
+      return __all_sync(0xffffffffu, r_ok);
+    };
+    for (int slot_it = 0;; ++slot_it) {
+      const int slot = slot_it % kBwdSlots;
+      const bool got = mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, got)) break;
+      const int w = sm.items[slot];
+      mbar_arrive(&sm.item_empty[slot]);
+      if (w < 0) break;
+      const int g = p.work[w];
+      const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
+      if (n == 0) continue;
+      const int bh = g / p.nKt;
+      bool ok = true;
+      for (int t = 0; t < n; ++t) {
+        const int i = p.csc_rows[start + t];
+        ok = mbar_wait(&sm.dq_full, it & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        // two rounds of 64 columns; the second round's loads free the TMEM
+#pragma unroll
+        for (int rd = 0; rd < 2; ++rd) {
+          uint32_t qv[2][32];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) tmem_ld32(lane_base + kColDQ + rd * 64 + cc * 32, qv[cc]);
+          tmem_wait_ld();
+          if (rd == 1) {
+            tc_fence_before();
+            mbar_arrive(&sm.dq_empty);
+          }
+          // the staging tiles are free once the previous reduces have read them
+          if (tid == 0) bulk_wait_group_read0();
+          if (!dq_group_sync()) { ok = false; break; }
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(&sm.dqs[h][0] + sw128_offset(qr, c)) =
+                  make_uint4(qv[h][c * 4], qv[h][c * 4 + 1], qv[h][c * 4 + 2], qv[h][c * 4 + 3]);
+          fence_proxy_async_smem();
+          if (!dq_group_sync()) { ok = false; break; }
+          if (tid == 0) {
+            tma_reduce_add_3d(&tm_dq, &sm.dqs[0][0], rd * 64, i * kTile, bh);
+            tma_reduce_add_3d(&tm_dq, &sm.dqs[1][0], rd * 64 + 32, i * kTile, bh);
+            bulk_commit_group();
+          }
+        }
+        if (!ok) break;
+        ++it;
+      }
+      if (!ok) break;
+    }
+    if (tid == 0) bulk_wait_group0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&p.sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(&p.sched[0], 0);
+      atomicExch(&p.sched[1], 0);
+    }
+  }
+}
+
 // Drow[row] = sum_d dO * O (fp32) and dq_acc[row] = 0. D/8 lanes per row (one
 // 16-byte chunk each), 32 / (D/8) rows per warp step; the loop is warp-uniform
 // so the shuffle reduction always has the whole warp.
@@ -677,20 +1135,23 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   p.csc_rows = reinterpret_cast<const int32_t*>(a.ws + L.csc_rows);
   p.cflags = reinterpret_cast<const uint8_t*>(a.ws + L.cflags);
   p.work = reinterpret_cast<const int32_t*>(a.ws + L.work_bwd);
-  p.n_work = static_cast<int>(L.n_ktiles) * (D / 64);
+  p.n_work = static_cast<int>(L.n_ktiles) * (D == 128 ? 1 : D / 64);
   p.dk = a.dk;
   p.dv = a.dv;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched + 2;
-  const size_t smem = sizeof(BwdSmem<D>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  const size_t smem = (D == 128 ? sizeof(Bwd128Smem) : sizeof(BwdSmem<D>)) + 1024;
+  cudaError_t e = D == 128 ? cudaFuncSetAttribute(attn_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(smem))
+                           : cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int grid = sms;
   if (grid > p.n_work) grid = p.n_work;
   if (grid < 1) grid = 1;
   record_kernel_event(1, true, st);
-  attn_bwd_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
+  if (D == 128) attn_bwd128_kernel<<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
+  else attn_bwd_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
   record_kernel_event(1, false, st);
   {
     const long long n8 = qrows * D / 8;
