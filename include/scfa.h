@@ -196,7 +196,9 @@ scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int
  *   row_ptr [B*H*nQt+1], cols, fflags (CSR over q tiles, columns ascending);
  *   csc_ptr [B*H*nKt+1], csc_rows, cflags (CSC over k tiles, rows ascending);
  *   flag bit 0 = FULL; work_fwd [B*H*nQt] and work_bwd [B*H*nKt]: every tile
- *   id sorted by live count descending, then id ascending.
+ *   id sorted by live count descending, then id ascending, except that
+ *   work_bwd keeps the natural id order when its summed live counts reach
+ *   4096 times its largest count.
  *   Forward schedule over pairs of query tiles (2m, 2m + 1) of one head, pair
  *   id = (b*H + h) * ceil(nQt / 2) + m: pair_count [pairs] = size of the union
  *   of the two live lists; pair_list holds that union, key tiles ascending,

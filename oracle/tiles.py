@@ -70,6 +70,21 @@ def head_tiles(mode: str, Tq: int, Tk: int, q_idx=None, k_idx=None, q_hash=None,
     return live, full
 
 
+NATURAL_ORDER_RATIO = 4096
+
+
+def work_order(counts, may_keep_natural=False):
+    """Order in which the tiles of a list are handed out (a scheduling choice,
+    not part of the method): tile ids by live count descending, then id
+    ascending; but a list that may keep its natural order (the key-tile list)
+    does so when its total count is at least NATURAL_ORDER_RATIO times its
+    largest count."""
+    counts = [max(int(c), 0) for c in counts]
+    if may_keep_natural and counts and max(counts) * NATURAL_ORDER_RATIO <= sum(counts):
+        return list(range(len(counts)))
+    return sorted(range(len(counts)), key=lambda t: (-counts[t], t))
+
+
 def live_list(mode: str, B: int, H: int, Tq: int, Tk: int,
               q_idx=None, k_idx=None, q_hash=None, k_hash=None):
     """The whole work list over all heads.
@@ -109,8 +124,8 @@ def live_list(mode: str, B: int, H: int, Tq: int, Tk: int,
                 cflags.extend([FLAG_FULL if full[i, j] else 0 for i in is_])
                 csc_ptr.append(csc_ptr[-1] + len(is_))
                 kcount[g * nKt + j] = len(is_)
-    work_fwd = sorted(range(B * H * nQt), key=lambda t: (-qcount[t], t))
-    work_bwd = sorted(range(B * H * nKt), key=lambda t: (-kcount[t], t))
+    work_fwd = work_order(qcount)
+    work_bwd = work_order(kcount, may_keep_natural=True)
     i32 = lambda a: np.asarray(a, dtype=np.int32)
     return {
         "nQt": nQt, "nKt": nKt,

@@ -590,26 +590,28 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // S^T [0,128) with P^T overwriting its first 64 columns once both compute
 // warpgroups have read S^T; dP^T [128,256) with dQ overwriting it once read;
 // dV [256,384) and dK [384,512) accumulate over the key tile's query tiles.
-// Per query tile the MMA warp issues S^T and dP^T (dP^T after the dQ
-// warpgroup has read the previous dQ), then dV, dK, dQ; one thread's MMAs run
-// in order, so S^T(t+1) cannot overtake dV(t) reading P^T. Q and dO have one
-// stage each, released separately (dO after dV, Q after dK), so the next
-// tile's dO load starts while dK and dQ still run. dQ leaves TMEM in two
-// rounds of 64 columns through two 16 KB staging tiles and TMA reduce-adds.
+// Per query tile the MMA warp issues S^T (once dV of the previous tile has
+// read P^T) and dP^T (once the dQ warpgroup has read the previous dQ), then
+// dV, dK, dQ. Q has two stages, so the next tile's Q is in place a whole step
+// ahead; dO has one, refilled as soon as dV has read it (dV runs first). The
+// producer loads each tile's row metadata before it waits for a stage. dQ
+// leaves TMEM in two rounds of 64 columns through two 16 KB staging tiles and
+// TMA reduce-adds; the staging tiles share their shared memory with dS^T (the
+// next dS^T is written once the reduces have read the staged dQ).
 // ---------------------------------------------------------------------------
 struct __align__(1024) Bwd128Smem {
   uint8_t k[2][kSubBytes];
   uint8_t v[2][kSubBytes];
-  uint8_t q[2][kSubBytes];
+  uint8_t q[2][2][kSubBytes];  // [stage][64-column half of D]
   uint8_t dO[2][kSubBytes];
-  uint8_t dst[2][kSubBytes];   // dS^T [query half][128 keys x 64 queries]
-  uint8_t dqs[2][kSubBytes];   // dQ staging: [128 rows x 32 floats] each
+  uint8_t dsq[2][kSubBytes];   // dS^T [query half][128 keys x 64 queries] (bf16), then
+                               // the dQ staging tiles [128 rows x 32 floats] (fp32)
   int32_t qidx[2][kTile];      // query metadata by step parity
   int32_t qhash[2][kTile];
   float lse2[2][kTile];        // -LSE * log2(e)
   float drs[2][kTile];         // -rowsum(dO * O) * scale
-  uint64_t kv_full, kv_empty, q_full, q_empty, do_empty, s_full, loaded, ds_full;
-  uint64_t dq_full, dq_empty, dkv_full, dkv_empty, drain, dq_sync;
+  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, loaded, ds_full;
+  uint64_t dq_full, dq_empty, dqs_free, dkv_full, dkv_empty, drain, dq_sync;
   int32_t items[kBwdSlots];
   uint64_t item_full[kBwdSlots], item_empty[kBwdSlots];
   uint32_t tmem_base;
@@ -630,14 +632,18 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   if (threadIdx.x == 0) {
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
-    mbar_init(&sm.q_full, 2);
-    mbar_init(&sm.q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+    }
+    mbar_init(&sm.do_full, 2);
     mbar_init(&sm.do_empty, 1);
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.loaded, 256);
     mbar_init(&sm.ds_full, 256);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_empty, 128);
+    mbar_init(&sm.dqs_free, 1);
     mbar_init(&sm.dkv_full, 1);
     mbar_init(&sm.dkv_empty, 256);
     mbar_init(&sm.drain, 1);
@@ -695,20 +701,9 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       for (int t = 0; t < n; ++t) {
         const int i = p.csc_rows[start + t];
-        const int mb = qt & 1;
-        if (lane == 0) {
-          // dO once dV of the previous tile has read it, Q once dK has
-          ok = mbar_wait(&sm.do_empty, (qt & 1) ^ 1, abort_flag, p.status);
-          if (ok) {
-            mbar_arrive_expect_tx(&sm.q_full, 2 * D * kTile * 2);
-            for (int sub = 0; sub < 2; ++sub) tma_load_3d(sm.dO[sub], &tm_do, &sm.q_full, sub * 64, i * kTile, bh);
-            ok = mbar_wait(&sm.q_empty, (qt & 1) ^ 1, abort_flag, p.status);
-            if (ok)
-              for (int sub = 0; sub < 2; ++sub) tma_load_3d(sm.q[sub], &tm_q, &sm.q_full, sub * 64, i * kTile, bh);
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+        const int mb = qt & 1, s = qt & 1;
         {
+          // row metadata first (plain loads, in flight during the waits below)
           int qid[4], qhv[4];
           float lsev[4], drv[4];
 #pragma unroll
@@ -722,6 +717,22 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             lsev[u] = qv ? p.lse[gq] : 0.f;
             drv[u] = qv ? p.drow[gq] : 0.f;
           }
+          if (lane == 0) {
+            // Q into its stage once dK two tiles back has read it, dO once dV
+            // of the previous tile has
+            ok = mbar_wait(&sm.q_empty[s], ((qt >> 1) & 1) ^ 1, abort_flag, p.status);
+            if (ok) {
+              mbar_arrive_expect_tx(&sm.q_full[s], D * kTile * 2);
+              for (int sub = 0; sub < 2; ++sub)
+                tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
+              ok = mbar_wait(&sm.do_empty, (qt & 1) ^ 1, abort_flag, p.status);
+            }
+            if (ok) {
+              mbar_arrive_expect_tx(&sm.do_full, D * kTile * 2);
+              for (int sub = 0; sub < 2; ++sub) tma_load_3d(sm.dO[sub], &tm_do, &sm.do_full, sub * 64, i * kTile, bh);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int c = lane + 32 * u;
@@ -733,14 +744,19 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         __threadfence_block();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.q_full);
+        if (lane == 0) mbar_arrive(&sm.do_full);
         ++qt;
       }
       if (!ok) break;
       ++item;
     }
     if (lane == 0) {
-      if (qt > 0) mbar_wait(&sm.q_full, (qt - 1) & 1, abort_flag, p.status);
+      // no load may still be in flight when the CTA exits
+      if (qt > 0) {
+        mbar_wait(&sm.do_full, (qt - 1) & 1, abort_flag, p.status);
+        mbar_wait(&sm.q_full[(qt - 1) & 1], ((qt - 1) >> 1) & 1, abort_flag, p.status);
+      }
+      if (qt > 1) mbar_wait(&sm.q_full[(qt - 2) & 1], ((qt - 2) >> 1) & 1, abort_flag, p.status);
       if (last_kv >= 0) mbar_wait(&sm.kv_full, last_kv & 1, abort_flag, p.status);
     }
   } else if (warp == 1) {
@@ -752,12 +768,13 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const uint64_t kdesc_k = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
       const uint64_t vdesc_k = smem_desc_sw128(smem_u32(sm.v[0]), 16, 1024);
       const uint64_t kdesc_mn = smem_desc_sw128(smem_u32(sm.k[0]), kSubBytes, 1024);
-      const uint64_t qdesc_k = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
-      const uint64_t qdesc_mn = smem_desc_sw128(smem_u32(sm.q[0]), kSubBytes, 1024);
+      const uint64_t qdesc_k = smem_desc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
+      const uint64_t qdesc_mn = smem_desc_sw128(smem_u32(sm.q[0][0]), kSubBytes, 1024);
+      constexpr uint32_t kQStage16 = (2 * kSubBytes) >> 4;
       const uint64_t odesc_k = smem_desc_sw128(smem_u32(sm.dO[0]), 16, 1024);
       const uint64_t odesc_mn = smem_desc_sw128(smem_u32(sm.dO[0]), kSubBytes, 1024);
-      const uint64_t sdesc_k = smem_desc_sw128(smem_u32(sm.dst[0]), 16, 1024);
-      const uint64_t sdesc_mn = smem_desc_sw128(smem_u32(sm.dst[0]), kSubBytes, 1024);
+      const uint64_t sdesc_k = smem_desc_sw128(smem_u32(sm.dsq[0]), 16, 1024);
+      const uint64_t sdesc_mn = smem_desc_sw128(smem_u32(sm.dsq[0]), kSubBytes, 1024);
       int it = 0, item = 0;
       bool ok = true;
       for (int slot_it = 0; ok; ++slot_it) {
@@ -771,13 +788,19 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (n == 0) continue;
         if (!mbar_wait(&sm.kv_full, item & 1, abort_flag, p.status)) break;
         for (int t = 0; t < n; ++t) {
-          // S^T = K Q^T, then dP^T = V dO^T once dQ of the previous tile is out of TMEM
-          if (!mbar_wait(&sm.q_full, it & 1, abort_flag, p.status)) { ok = false; break; }
+          // S^T = K Q^T once dV of the previous tile has read P^T (the same
+          // columns), then dP^T = V dO^T once dQ of the previous tile is out
+          // of TMEM
+          const int s = it & 1;
+          const uint64_t qs16 = static_cast<uint64_t>(s * kQStage16);
+          if (!mbar_wait(&sm.q_full[s], (it >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (it > 0 && !mbar_wait(&sm.do_empty, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_bf16_ss(tmem + kColS, kdesc_k + kstep_off16(kk, kSubBytes), qdesc_k + kstep_off16(kk, kSubBytes),
-                        idesc_s, kk > 0);
+            mma_bf16_ss(tmem + kColS, kdesc_k + kstep_off16(kk, kSubBytes),
+                        qdesc_k + qs16 + kstep_off16(kk, kSubBytes), idesc_s, kk > 0);
+          if (!mbar_wait(&sm.do_full, it & 1, abort_flag, p.status)) { ok = false; break; }
           if (it > 0 && !mbar_wait(&sm.dq_empty, (it - 1) & 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -799,9 +822,9 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           // dK += dS^T Q
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ss(tmem + kColDK, sdesc_k + kstep_off16(kk, kSubBytes), qdesc_mn + static_cast<uint64_t>(kk * 128),
-                        idesc_kv, kk > 0 ? 1u : acc0);
-          tc_commit(&sm.q_empty);
+            mma_bf16_ss(tmem + kColDK, sdesc_k + kstep_off16(kk, kSubBytes),
+                        qdesc_mn + qs16 + static_cast<uint64_t>(kk * 128), idesc_kv, kk > 0 ? 1u : acc0);
+          tc_commit(&sm.q_empty[s]);
           // dQ_i = dS K into the dP^T columns (read by now)
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
@@ -854,7 +877,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       for (int t = 0; t < n; ++t) {
         const bool full = (p.cflags[start + t] & kFlagFull) != 0;
         const int mb = it & 1;
-        ok = mbar_wait(&sm.q_full, it & 1, abort_flag, p.status) &&
+        ok = mbar_wait(&sm.do_full, it & 1, abort_flag, p.status) &&
              mbar_wait(&sm.s_full, it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -927,10 +950,14 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         ok = mbar_wait(&sm.loaded, it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        uint8_t* dsh = sm.dst[grp];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) tmem_st16(lane_base + kColPT + grp * 32 + c * 16, pk[c]);
+        // dS^T replaces the previous tile's staged dQ once its reduces have read it
+        ok = mbar_wait(&sm.dqs_free, (it & 1) ^ 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        uint8_t* dsh = sm.dsq[grp];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          tmem_st16(lane_base + kColPT + grp * 32 + c * 16, pk[c]);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             *reinterpret_cast<uint4*>(dsh + sw128_offset(kr, c * 4 + u)) =
@@ -1004,24 +1031,29 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc_fence_before();
             mbar_arrive(&sm.dq_empty);
           }
-          // the staging tiles are free once the previous reduces have read them
+          // the staging tiles are free once the first round's reduces have read them
           if (tid == 0) bulk_wait_group_read0();
           if (!dq_group_sync()) { ok = false; break; }
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(&sm.dqs[h][0] + sw128_offset(qr, c)) =
+              *reinterpret_cast<uint4*>(&sm.dsq[h][0] + sw128_offset(qr, c)) =
                   make_uint4(qv[h][c * 4], qv[h][c * 4 + 1], qv[h][c * 4 + 2], qv[h][c * 4 + 3]);
           fence_proxy_async_smem();
           if (!dq_group_sync()) { ok = false; break; }
           if (tid == 0) {
-            tma_reduce_add_3d(&tm_dq, &sm.dqs[0][0], rd * 64, i * kTile, bh);
-            tma_reduce_add_3d(&tm_dq, &sm.dqs[1][0], rd * 64 + 32, i * kTile, bh);
+            tma_reduce_add_3d(&tm_dq, &sm.dsq[0][0], rd * 64, i * kTile, bh);
+            tma_reduce_add_3d(&tm_dq, &sm.dsq[1][0], rd * 64 + 32, i * kTile, bh);
             bulk_commit_group();
           }
         }
         if (!ok) break;
+        // the staging tiles go back to dS^T once the reduces have read them
+        if (tid == 0) {
+          bulk_wait_group_read0();
+          mbar_arrive(&sm.dqs_free);
+        }
         ++it;
       }
       if (!ok) break;

@@ -294,9 +294,16 @@ struct OrderList {
   int maxc;
   int32_t* out;
   int32_t* gcur;
+  bool may_keep_natural;
 };
 
 constexpr int kOrderChunk = 4096;     // counts staged in shared memory per scatter round
+// A key-tile list whose total work is at least this many times its largest
+// item keeps the natural (head, tile) order: the tail left by the largest item
+// is then small, and key tiles taken at the same time share their query tiles
+// in L2. (The forward lists stay sorted: the query-tile-pair forward hands its
+// items out in fixed rounds, where the sorted order balances better.)
+constexpr long long kNaturalOrderRatio = 4096;
 constexpr int kOrderWarpBins = 8192;  // per-warp bin offsets (few distinct counts)
 
 // Stable counting sort of ids by count, descending: block 0 builds the
@@ -313,6 +320,36 @@ __global__ void work_order_kernel(OrderList l0, OrderList l1, OrderList l2, int 
   int32_t* out = L.out;
   int32_t* cur = (maxc + 1 <= smem_bins) ? scur : L.gcur;
   int32_t* chunk = scur + smem_bins;
+  if (L.may_keep_natural) {
+    __shared__ unsigned long long s_total;
+    __shared__ int s_max;
+    if (threadIdx.x == 0) {
+      s_total = 0;
+      s_max = 0;
+    }
+    __syncthreads();
+    unsigned long long tot = 0;
+    int mx = 0;
+    for (long long i = threadIdx.x; i < n; i += blockDim.x) {
+      const int c = max(cnt[i], 0);
+      tot += static_cast<unsigned long long>(c);
+      mx = max(mx, c);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+      atomicAdd(&s_total, tot);
+      atomicMax(&s_max, mx);
+    }
+    __syncthreads();
+    const bool natural = n > 0 && static_cast<unsigned long long>(s_max) * kNaturalOrderRatio <= s_total;
+    if (natural) {
+      for (long long i = threadIdx.x; i < n; i += blockDim.x) out[i] = static_cast<int32_t>(i);
+      return;
+    }
+  }
   for (int cc = threadIdx.x; cc <= maxc; cc += blockDim.x) cur[cc] = 0;
   __syncthreads();
   for (long long i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&cur[min(max(cnt[i], 0), maxc)], 1);
@@ -454,10 +491,10 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
     if (dev >= 0 && dev < 64) order_smem_set[dev] = true;
   }
   int32_t* gcur = reinterpret_cast<int32_t*>(ws + L.cursor);
-  OrderList lf{qcount, L.n_qtiles, L.nKt, reinterpret_cast<int32_t*>(ws + L.work_fwd), gcur};
-  OrderList lb{kcount, L.n_ktiles, L.nQt, reinterpret_cast<int32_t*>(ws + L.work_bwd), gcur + L.nKt + 1};
+  OrderList lf{qcount, L.n_qtiles, L.nKt, reinterpret_cast<int32_t*>(ws + L.work_fwd), gcur, false};
+  OrderList lb{kcount, L.n_ktiles, L.nQt, reinterpret_cast<int32_t*>(ws + L.work_bwd), gcur + L.nKt + 1, true};
   OrderList lp{reinterpret_cast<const int32_t*>(ws + L.pcount), with_pairs ? L.n_pairs : 0, L.nKt,
-               reinterpret_cast<int32_t*>(ws + L.work_pairs), gcur + L.nKt + L.nQt + 2};
+               reinterpret_cast<int32_t*>(ws + L.work_pairs), gcur + L.nKt + L.nQt + 2, false};
   work_order_kernel<<<3, 1024, smem, st>>>(lf, lb, lp, smem_bins);
   return cudaGetLastError();
 }

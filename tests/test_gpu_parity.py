@@ -163,7 +163,7 @@ def expected_pairs(ref, nQt):
                     ent[int(c)] = ent.get(int(c), 0) | ((1 | (2 if f & 1 else 0)) << (2 * g))
             lists[bh * nP + m] = [(c << 4) | b for c, b in sorted(ent.items())]
             counts.append(len(ent))
-    order = sorted(range(len(counts)), key=lambda q: (-counts[q], q))
+    order = tiles.work_order(counts)
     return np.array(counts, np.int32), lists, np.array(order, np.int32)
 
 
@@ -205,6 +205,23 @@ def test_tiles_hash_bitexact(scfa, T, nb):
     scfa.scfa_tiles(scfa.MODE_HASH, t(pq), t(pk), t(qs), t(ks), B, H, T, T, 64, ws)
     got = read_tiles(scfa, ws, scfa.MODE_HASH, B, H, T, T, 64)
     compare_tiles(got, tiles.live_list("hash", B, H, T, T, pq, pk, qs, ks))
+
+
+def test_tiles_natural_order(scfa):
+    # 4096 key tiles that each see one query tile (buckets of exactly 128
+    # rows): the summed live counts reach 4096 x the largest, so the key-tile
+    # work list keeps the natural order
+    B, H, T = 1, 4, 131072
+    pos = np.broadcast_to(np.arange(T, dtype=np.int32), (B, H, T))
+    qs = np.broadcast_to((np.arange(T) // 128).astype(np.int32), (B, H, T))
+    ks = np.broadcast_to((np.arange(T) // 128).astype(np.int32), (B, H, T))
+    ws = scfa.workspace(scfa.attn_workspace_size(scfa.MODE_HASH, 1, B, H, T, T, 64))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    scfa.scfa_tiles(scfa.MODE_HASH, t(pos), t(pos), t(qs), t(ks), B, H, T, T, 64, ws)
+    got = read_tiles(scfa, ws, scfa.MODE_HASH, B, H, T, T, 64)
+    ref = tiles.live_list("hash", B, H, T, T, pos, pos, qs, ks)
+    np.testing.assert_array_equal(ref["work_bwd"], np.arange(B * H * (T // 128)))
+    compare_tiles(got, ref)
 
 
 @pytest.mark.parametrize("T", [1, 130, 1000])

@@ -130,3 +130,18 @@ def test_csr_csc_work_order_consistency():
     assert sorted(L["work_fwd"].tolist()) == list(range(B * H * nQt))
     keys = [(-cnt[t], t) for t in L["work_fwd"]]
     assert keys == sorted(keys)
+
+
+def test_work_order_rule():
+    # largest first (ties by id) while one item is a sizeable share of the list
+    assert tiles.work_order([1, 3, 0, 3, 2]) == [1, 3, 4, 0, 2]
+    assert tiles.work_order([]) == []
+    # boundary of the natural-order rule: total >= 4096 x largest
+    heavy_last = [1] * 4095 + [2]                  # 4097 < 8192: sorted
+    order = tiles.work_order(heavy_last, may_keep_natural=True)
+    assert order[0] == 4095 and order[1:] == list(range(4095))
+    many = [1] * 8191 + [2]                        # 8193 >= 8192: natural
+    assert tiles.work_order(many, may_keep_natural=True) == list(range(8192))
+    order = tiles.work_order(many)                 # lists that always sort
+    assert order[0] == 8191 and order[1:] == list(range(8191))
+    assert tiles.work_order([0, 0, 0], may_keep_natural=True) == [0, 1, 2]
