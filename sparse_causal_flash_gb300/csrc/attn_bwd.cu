@@ -9,19 +9,19 @@
 // the mask, L = sum(O * dO): dV = P^T dO, dP = dO V^T,
 // dS = P * (dP - rowsum(dO * O)), dQ = scale * dS K, dK = scale * dS^T Q.
 //
-// GB300 design: persistent CTAs walk the backward work order (key tiles by
-// live count, longest first); each work item keeps K_j, V_j resident and
+// GB300 design: persistent CTAs take key tiles from the backward work order
+// through a global counter; each work item keeps K_j, V_j resident and
 // streams the live query tiles i of its CSC column. Per query tile:
 //   A(i): S^T = K Q_i^T and dP^T = V dO_i^T      (tcgen05, TMEM, keys on lanes)
 //   compute(i): P^T = exp2(S^T - LSE) under the mask -> TMEM (bf16, the A
 //         operand of the dV MMA); dS^T = P^T (dP^T - Drow) scale -> shared
 //         memory (bf16, double-buffered)
 //   B(i): dV += P^T dO_i (A from TMEM), dK += dS^T Q_i, dQ_i = dS K
-// The MMA warp issues A(i+1) as soon as compute(i) has read S^T / dP^T out of
-// TMEM, so the tensor core runs A(i+1) and B(i-1) while compute(i) works.
-// Roles (448 threads):
+// Head dimension 64 (attn_bwd_kernel<64>): the MMA warp issues A(i+1) as
+// soon as compute(i) has read S^T / dP^T out of TMEM, so the tensor core runs
+// A(i+1) and B(i-1) while compute(i) works. Roles (448 threads):
 //   warp 0       producer: lane 0 issues the TMA loads of K_j, V_j (once per
-//                item) and Q_i, dO_i (2-stage ring); all 32 lanes stage the
+//                item) and Q_i, dO_i (3-stage ring); all 32 lanes stage the
 //                query metadata (position, bucket, LSE in log2 units,
 //                rowsum * scale) of tile i next to it.
 //   warp 1       TMEM owner (512 columns); lane 0 issues every tcgen05.mma.
@@ -31,7 +31,11 @@
 //                swizzled fp32 shared tile, then one TMA reduce-add per
 //                64-column half into the fp32 accumulator in the workspace.
 // TMEM columns: S^T [0,128) dP^T [128,256) dV [256,320) dK [320,384)
-// dQ [384,448) P^T (bf16 pairs) [448,512). Every wait is bounded.
+// dQ [384,448) P^T (bf16 pairs) [448,512).
+// Head dimension 128 (attn_bwd128_kernel): the same roles, but dV and dK
+// take 128 TMEM columns each, so P^T and dQ overwrite S^T and dP^T once they
+// have been read, and A(i+1) follows B(i); described at the kernel.
+// Every wait is bounded.
 #include <climits>
 
 #include "common.cuh"
@@ -41,10 +45,13 @@ namespace scfa {
 namespace {
 
 constexpr int kSubBytes = kTile * 128;
-// Q / dO / query-metadata ring depth: 3 at D = 64; 1 at D = 128, where the
-// 64 KB Q + dO stage leaves no room for a second one
+// Q / dO / query-metadata ring depth of attn_bwd_kernel (head dimension 64;
+// head dimension 128 runs attn_bwd128_kernel)
 template <int D>
-constexpr int bwd_qstages() { return D == 64 ? 3 : 1; }
+constexpr int bwd_qstages() {
+  static_assert(D == 64, "attn_bwd_kernel is built for head dimension 64");
+  return 3;
+}
 constexpr int kBwdThreads = 448;
 constexpr int kBwdSlots = 4;  // work items handed from the producer to the other roles
 constexpr uint32_t kTmemCols = 512;
@@ -1167,24 +1174,31 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   p.csc_rows = reinterpret_cast<const int32_t*>(a.ws + L.csc_rows);
   p.cflags = reinterpret_cast<const uint8_t*>(a.ws + L.cflags);
   p.work = reinterpret_cast<const int32_t*>(a.ws + L.work_bwd);
-  p.n_work = static_cast<int>(L.n_ktiles) * (D == 128 ? 1 : D / 64);
+  p.n_work = static_cast<int>(L.n_ktiles);  // one work item per key tile
   p.dk = a.dk;
   p.dv = a.dv;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched + 2;
-  const size_t smem = (D == 128 ? sizeof(Bwd128Smem) : sizeof(BwdSmem<D>)) + 1024;
-  cudaError_t e = D == 128 ? cudaFuncSetAttribute(attn_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(smem))
-                           : cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
   int grid = sms;
   if (grid > p.n_work) grid = p.n_work;
   if (grid < 1) grid = 1;
-  record_kernel_event(1, true, st);
-  if (D == 128) attn_bwd128_kernel<<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
-  else attn_bwd_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
-  record_kernel_event(1, false, st);
+  if constexpr (D == 128) {
+    const size_t smem = sizeof(Bwd128Smem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    record_kernel_event(1, true, st);
+    attn_bwd128_kernel<<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
+    record_kernel_event(1, false, st);
+  } else {
+    const size_t smem = sizeof(BwdSmem<D>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    record_kernel_event(1, true, st);
+    attn_bwd_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
+    record_kernel_event(1, false, st);
+  }
   {
     const long long n8 = qrows * D / 8;
     long long g = (n8 + 255) / 256;
