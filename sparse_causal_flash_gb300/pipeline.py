@@ -9,7 +9,8 @@ and "SCFA 解决方案" part 2). LSE stays in sorted query order (the backward
 consumes it there). Buffers are allocated once per shape and reused. The
 query side and the key side of the hash step are independent until the
 attention, so the key side runs on a second stream (and so do the unsorts
-of dK and dV), joined by events.
+of dK and dV), joined by events. HostPipeline runs steps on batches held in
+pinned host memory with the host/device copies overlapped with the kernels.
 """
 from __future__ import annotations
 
@@ -98,3 +99,83 @@ class Step:
             lsh_unsort(self.dq_s, self.pq, self.dq, main)
             main.wait_event(self.ev[3])
         return self
+
+
+class HostPipeline:
+    """Fwd+bwd steps on batches held in pinned host memory, with the copies
+    hidden under the kernels.
+
+    Two Steps (two sets of device inputs, outputs and workspaces) alternate:
+    while step t runs on the compute stream, a host-to-device stream fills the
+    other slot with the inputs of step t+1 and a device-to-host stream drains
+    the results of step t-1. Events order the three streams (call order only,
+    no arithmetic). Results of each step are copied into the host tensors
+    passed with it; `synchronize()` waits for everything submitted.
+    """
+
+    INPUTS = ("q", "k", "v", "do", "q_idx", "k_idx", "R")
+
+    def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
+                 device="cuda", flags: int = 0):
+        self.device = torch.device(device)
+        self.steps = [Step(mode, B, H, Tq, Tk, D, n_buckets=n_buckets, device=self.device, flags=flags)
+                      for _ in range(2)]
+        self.h2d = torch.cuda.Stream(device=self.device)
+        self.d2h = torch.cuda.Stream(device=self.device)
+        self.inputs = [None, None]
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.drained = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+        self.n = 0
+
+    def submit(self, host_inputs: dict, host_outputs, scale: float, stream=None, before=None):
+        """Queue one step and return at once.
+
+        host_inputs: pinned CPU tensors by name (q, k, v, do, and q_idx / k_idx
+        / R where the mode has them; None or absent otherwise). host_outputs:
+        pinned CPU tensors for o, lse, dq, dk, dv, in that order. stream: the
+        compute stream (default: the current one). before(stream): called on
+        the compute stream just before the step's kernels.
+        """
+        s = self.n & 1
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if self.inputs[s] is None:
+            self.inputs[s] = {n: (torch.empty(t.shape, dtype=t.dtype, device=self.device) if t is not None else None)
+                              for n in self.INPUTS for t in [host_inputs.get(n)]}
+        dst = self.inputs[s]
+        if self.used[s]:
+            self.h2d.wait_event(self.computed[s])  # the step two calls back has read this slot
+        with torch.cuda.stream(self.h2d):
+            for n in self.INPUTS:
+                src = host_inputs.get(n)
+                if src is not None:
+                    dst[n].copy_(src, non_blocking=True)
+        self.in_ready[s].record(self.h2d)
+        main.wait_event(self.in_ready[s])
+        if self.used[s]:
+            main.wait_event(self.drained[s])  # this slot's previous results have reached the host
+        if before is not None:
+            before(main)
+        st = self.steps[s]
+        st.run(dst["q"], dst["k"], dst["v"], dst["do"], scale, q_idx=dst["q_idx"], k_idx=dst["k_idx"], R=dst["R"],
+               stream=main)
+        self.computed[s].record(main)
+        self.d2h.wait_event(self.computed[s])
+        with torch.cuda.stream(self.d2h):
+            for h, o in zip(host_outputs, (st.o, st.lse, st.dq, st.dk, st.dv)):
+                h.copy_(o, non_blocking=True)
+        self.drained[s].record(self.d2h)
+        self.used[s] = True
+        self.n += 1
+        return st
+
+    def wait_copies(self, stream):
+        """Make `stream` wait for every copy submitted so far."""
+        stream.wait_stream(self.h2d)
+        stream.wait_stream(self.d2h)
+
+    def synchronize(self):
+        self.h2d.synchronize()
+        self.d2h.synchronize()
+        torch.cuda.synchronize(self.device)
