@@ -7,8 +7,10 @@
 // positions and of the bucket ids over its valid rows, tests every candidate
 // (query tile, key tile) pair, and emits CSR (by query tile), CSC (by key
 // tile), a FULL flag per entry (all 128 x 128 pairs admissible: no element
-// mask needed), and the work order (tile ids by live count descending, then
-// id ascending) that the persistent attention kernels walk.
+// mask needed), and the work orders that the persistent attention kernels
+// walk: tile ids by live count descending, then id ascending, except that the
+// key-tile list keeps its natural order when its total work is at least
+// 4,096 times its largest item.
 //
 // All passes are integer and tiny next to the attention itself. In hash mode
 // the bucket ids are non-decreasing along the sorted rows, so the key tiles
