@@ -105,7 +105,7 @@ def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0) -> 
         m = n_buckets // 2
         lsh = 2 if (D in (64, 128) and m % 8 == 0 and 8 <= m <= 256) else 1  # tensor-core pass + certified pass
         sort = 3 if T > 8192 else 1                                          # chunk counts, scan, scatter
-        return tiles + attn + 2 * (lsh + sort + 1) + 2 + 4   # per q / k: hash, sort, gather; gather V / dO; 4 unsorts
+        return tiles + attn + 2 * (lsh + sort + 1) + 2   # per q / k: hash, sort, gather; gather V / dO
     return tiles + attn
 
 

@@ -69,12 +69,22 @@ enum { SCFA_MODE_DENSE = 0, SCFA_MODE_QK = 1, SCFA_MODE_HASH = 2 };
 enum {
   SCFA_FLAG_NO_PRUNE = 1,    /* treat every tile as live (results unchanged) */
   SCFA_FLAG_DEBUG_SYNC = 4,  /* synchronise the stream after every launch */
-  SCFA_FLAG_REUSE_TILES = 8  /* the workspace already holds the live-tile list
-                                of these exact indices and shape (built by
-                                scfa_tiles or an earlier call on the same
-                                workspace): skip the metadata pass. One
-                                backward-sized workspace may then serve the
-                                forward and the backward call of a step. */
+  SCFA_FLAG_REUSE_TILES = 8,  /* the workspace already holds the live-tile list
+                                 of these exact indices and shape (built by
+                                 scfa_tiles or an earlier call on the same
+                                 workspace): skip the metadata pass. One
+                                 backward-sized workspace may then serve the
+                                 forward and the backward call of a step. */
+  SCFA_FLAG_ORIGINAL_ORDER = 16  /* hash mode only: the row tensors o (forward
+                                 output and backward input), dq, dk and dv are
+                                 in ORIGINAL row order: sorted query row s of
+                                 head (b,h) is row q_idx[b,h,s] of o and dq,
+                                 sorted key row s is row k_idx[b,h,s] of dk and
+                                 dv (q_idx / k_idx must then be permutations of
+                                 [0, T) per head; rows whose index falls outside
+                                 [0, T) are not written, and read as zero).
+                                 q, k, v, do, lse stay in sorted order. This
+                                 replaces the lsh_unsort passes. */
 };
 
 /* Tiles are SCFA_TILE rows of queries by SCFA_TILE rows of keys. */
@@ -133,7 +143,9 @@ scfa_status scfa_qk_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * k_s, v_s, dk_s, dv_s the key order. q_idx / k_idx [B,H,T] are the original
  * positions of the sorted rows (the perm of lsh_bucket_sort) and q_hash /
  * k_hash [B,H,T] their bucket ids, non-decreasing within each (b,h).
- * Put results back in original order with lsh_unsort. D = 64 or 128.
+ * Put results back in original order with lsh_unsort, or pass
+ * SCFA_FLAG_ORIGINAL_ORDER to have the kernels write o / dq / dk / dv (and
+ * read o) in original order directly. D = 64 or 128.
  * ------------------------------------------------------------------------- */
 scfa_status scfa_hash_fwd(const uint16_t* q_s, const uint16_t* k_s, const uint16_t* v_s,
                           const int32_t* q_idx, const int32_t* k_idx,

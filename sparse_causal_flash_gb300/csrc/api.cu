@@ -169,6 +169,7 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return SCFA_ERR_INVALID;
   if (mode != SCFA_MODE_DENSE && (!q_idx || !k_idx)) return SCFA_ERR_INVALID;
   if (mode == SCFA_MODE_HASH && (!q_hash || !k_hash)) return SCFA_ERR_INVALID;
+  if ((flags & SCFA_FLAG_ORIGINAL_ORDER) && (mode != SCFA_MODE_HASH || Tq != Tk)) return SCFA_ERR_INVALID;
   if (!backward) {
     if (!o || !lse || !aligned16(o)) return SCFA_ERR_INVALID;
   } else {
@@ -209,6 +210,9 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  const bool original = (flags & SCFA_FLAG_ORIGINAL_ORDER) != 0;
+  a.q_rows = original ? q_idx : nullptr;
+  a.k_rows = original ? k_idx : nullptr;
   a.ws = w;
   a.L = &L;
   e = backward ? launch_attn_bwd(a, st) : launch_attn_fwd(a, st);

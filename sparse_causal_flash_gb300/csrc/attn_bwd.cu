@@ -97,6 +97,7 @@ struct BwdParams {
   int n_work;
   uint16_t* dk;
   uint16_t* dv;
+  const int32_t* k_rows;  // null, or the original row of each sorted key row
   int* sched;  // [0] next work item, [1] CTAs done
   int* status;
 };
@@ -385,9 +386,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int key = j * kTile + kr;
       const bool kvalid = key < p.Tk;
       const long long gk = static_cast<long long>(bh) * p.Tk + key;
+      // dK / dV row within the head (-1: not written)
+      const int kro = !kvalid ? -1 : (p.k_rows == nullptr ? key : p.k_rows[gk]);
       if (n == 0) {
-        if (kvalid) {
-          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + gk * D + 64 * hh);
+        if (kro >= 0 && kro < p.Tk) {
+          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + (gk - key + kro) * D + 64 * hh);
 #pragma unroll
           for (int c = 0; c < 8; ++c) a[c] = make_uint4(0, 0, 0, 0);
         }
@@ -509,7 +512,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&sm.dkv_empty);
-      if (kvalid) store_row_bf16((grp == 0 ? p.dv : p.dk) + gk * D + 64 * hh, &acc[0][0], 64);
+      if (kro >= 0 && kro < p.Tk)
+        store_row_bf16((grp == 0 ? p.dv : p.dk) + (gk - key + kro) * D + 64 * hh, &acc[0][0], 64);
       ++item;
     }
   } else {
@@ -868,9 +872,10 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const int key = j * kTile + kr;
       const bool kvalid = key < p.Tk;
       const long long gk = static_cast<long long>(bh) * p.Tk + key;
+      const long long gko = kvalid ? mapped_row(p.k_rows, gk, key, p.Tk) : -1;  // dK / dV row
       if (n == 0) {
-        if (kvalid) {
-          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + gk * D);
+        if (gko >= 0) {
+          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + gko * D);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) a[c] = make_uint4(0, 0, 0, 0);
         }
@@ -982,7 +987,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t col = grp == 0 ? kColDV : kColDK;
-      uint16_t* orow = (grp == 0 ? p.dv : p.dk) + gk * D;
+      uint16_t* orow = (grp == 0 ? p.dv : p.dk) + (gko >= 0 ? gko : 0) * D;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t acc[2][32];
@@ -993,7 +998,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tc_fence_before();
           mbar_arrive(&sm.dkv_empty);
         }
-        if (kvalid) store_row_bf16(orow + 64 * hf, &acc[0][0], 64);
+        if (gko >= 0) store_row_bf16(orow + 64 * hf, &acc[0][0], 64);
       }
       ++item;
     }
@@ -1086,7 +1091,8 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // so the shuffle reduction always has the whole warp.
 template <int D>
 __global__ void bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dO, long long rows,
-                               float* __restrict__ drow, float* __restrict__ dq_acc) {
+                               float* __restrict__ drow, float* __restrict__ dq_acc,
+                               const int32_t* __restrict__ o_rows, int T) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = threadIdx.x & 31;
@@ -1098,7 +1104,9 @@ __global__ void bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* _
     const bool active = row < rows;
     float s = 0.f;
     if (active) {
-      const uint4 a = reinterpret_cast<const uint4*>(o + row * D)[ch];
+      // O may be stored in original row order (o_rows maps sorted -> original)
+      const long long orow = mapped_row(o_rows, row, static_cast<int>(row % T), T);
+      const uint4 a = orow >= 0 ? reinterpret_cast<const uint4*>(o + orow * D)[ch] : make_uint4(0, 0, 0, 0);
       const uint4 b = reinterpret_cast<const uint4*>(dO + row * D)[ch];
       const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -1118,9 +1126,18 @@ __global__ void bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* _
   }
 }
 
-__global__ void dq_finalize_kernel(const float* __restrict__ dq_acc, long long n8, uint16_t* __restrict__ dq) {
+__global__ void dq_finalize_kernel(const float* __restrict__ dq_acc, long long n8, uint16_t* __restrict__ dq,
+                                   const int32_t* __restrict__ q_rows, int T, int chunks) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
+    // dQ may be stored in original row order (q_rows maps sorted -> original)
+    long long out = t;
+    if (q_rows != nullptr) {
+      const long long row = t / chunks;
+      const long long orow = mapped_row(q_rows, row, static_cast<int>(row % T), T);
+      if (orow < 0) continue;
+      out = orow * chunks + (t - row * chunks);
+    }
     const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * t];
     const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * t + 1];
     uint4 u;
@@ -1128,7 +1145,7 @@ __global__ void dq_finalize_kernel(const float* __restrict__ dq_acc, long long n
     u.y = pack_bf16x2(a.z, a.w);
     u.z = pack_bf16x2(b.x, b.y);
     u.w = pack_bf16x2(b.z, b.w);
-    reinterpret_cast<uint4*>(dq)[t] = u;
+    reinterpret_cast<uint4*>(dq)[out] = u;
   }
 }
 
@@ -1150,7 +1167,7 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
     long long g = (work + 255) / 256;
     if (g > sms * 16LL) g = sms * 16LL;
     if (g < 1) g = 1;
-    bwd_pre_kernel<D><<<static_cast<int>(g), 256, 0, st>>>(a.o, a.do_, qrows, drow, dq_acc);
+    bwd_pre_kernel<D><<<static_cast<int>(g), 256, 0, st>>>(a.o, a.do_, qrows, drow, dq_acc, a.q_rows, a.Tq);
   }
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, BH) || !make_tmap_bf16_3d(&tk, a.k, D, a.Tk, BH) ||
@@ -1177,6 +1194,7 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   p.n_work = static_cast<int>(L.n_ktiles);  // one work item per key tile
   p.dk = a.dk;
   p.dv = a.dv;
+  p.k_rows = a.k_rows;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched + 2;
   int grid = sms;
@@ -1204,7 +1222,7 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
     long long g = (n8 + 255) / 256;
     if (g > sms * 16LL) g = sms * 16LL;
     if (g < 1) g = 1;
-    dq_finalize_kernel<<<static_cast<int>(g), 256, 0, st>>>(dq_acc, n8, a.dq);
+    dq_finalize_kernel<<<static_cast<int>(g), 256, 0, st>>>(dq_acc, n8, a.dq, a.q_rows, a.Tq, D / 8);
   }
   return cudaGetLastError();
 }

@@ -94,6 +94,7 @@ struct FwdParams {
   int n_work;
   int* sched;            // [0] next item, [1] CTAs done (single-tile kernel)
   uint16_t* o;
+  const int32_t* o_rows;  // null, or the original row of each sorted query row
   float* lse;
   int* status;
 };
@@ -470,9 +471,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (!ok) break;
       if (!any) {
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
+          const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
+          if (orow >= 0) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          }
           p.lse[grow] = -INFINITY;
         }
         continue;
@@ -490,7 +494,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ++o_it;
       if (valid) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
+        const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (orow >= 0 ? orow : grow) * D);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
           const int e = c * 8;
@@ -499,7 +504,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           u.y = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 2) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 3) & 31]) * inv);
           u.z = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 4) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 5) & 31]) * inv);
           u.w = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 6) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 7) & 31]) * inv);
-          dst[c] = u;
+          if (orow >= 0) dst[c] = u;
         }
         p.lse[grow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       }
@@ -895,9 +900,12 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!ok) break;
       if (!any) {
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
+          const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
+          if (orow >= 0) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          }
           p.lse[grow] = -INFINITY;
         }
         continue;
@@ -915,7 +923,8 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       ++o_it;
       if (valid) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D);
+        const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (orow >= 0 ? orow : grow) * D);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
           const int e = c * 8;
@@ -924,7 +933,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           u.y = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 2) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 3) & 31]) * inv);
           u.z = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 4) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 5) & 31]) * inv);
           u.w = pack_bf16x2(__uint_as_float(orr[e >> 5][(e + 6) & 31]) * inv, __uint_as_float(orr[e >> 5][(e + 7) & 31]) * inv);
-          dst[c] = u;
+          if (orow >= 0) dst[c] = u;
         }
         p.lse[grow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       }
@@ -977,6 +986,7 @@ static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   p.ulist = reinterpret_cast<const int32_t*>(a.ws + L.ulist);
   p.n_pairs = static_cast<int>(L.n_pairs);
   p.o = a.o_out;
+  p.o_rows = a.q_rows;
   p.lse = a.lse_out;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
@@ -1018,6 +1028,7 @@ static cudaError_t launch_fwd1(const AttnArgs& a, cudaStream_t st) {
   p.n_work = static_cast<int>(L.n_qtiles);
   p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched;
   p.o = a.o_out;
+  p.o_rows = a.q_rows;
   p.lse = a.lse_out;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   const size_t smem = sizeof(Fwd1Smem) + 1024;

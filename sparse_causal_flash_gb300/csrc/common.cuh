@@ -96,6 +96,15 @@ __device__ __forceinline__ int work_item(int r) {
   return r * G + ((r & 1) ? (G - 1 - b) : b);
 }
 
+// Output row of the row `grow` = (head base + r) of a sorted tensor: grow
+// itself without a row map, else head base + rows[grow]; -1 when the map
+// points outside [0, T) (such rows are neither written nor read).
+__device__ __forceinline__ long long mapped_row(const int32_t* rows, long long grow, int r, int T) {
+  if (rows == nullptr) return grow;
+  const int t = rows[grow];
+  return (t >= 0 && t < T) ? grow - r + t : -1;
+}
+
 // named barrier among `count` threads (ids 1..15; 0 is __syncthreads)
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");

@@ -87,6 +87,9 @@ struct AttnArgs {
   uint16_t* o_out;
   float* lse_out;
   uint16_t *dq, *dk, *dv;
+  // hash mode with SCFA_FLAG_ORIGINAL_ORDER: destination row (within the
+  // head) of each sorted query / key row; null = rows stay in place
+  const int32_t *q_rows, *k_rows;
   char* ws;
   const AttnWs* L;
 };

@@ -1,24 +1,25 @@
 """One fwd+bwd step of each SCFA mode, composed from C-ABI calls.
 
 Call order only (no arithmetic): the hash-sparse step hashes and
-bucket-sorts queries and keys, gathers V and dO into sorted order, runs the
-sparse attention forward and backward on the sorted rows, and puts O, dQ, dK
-and dV back in original order ("Faster Causal Attention Over Large Sequences
-Through Sparse Flash Attention", deep-paper.org, sections "动态稀疏性为何会破坏它"
-and "SCFA 解决方案" part 2). LSE stays in sorted query order (the backward
-consumes it there). Buffers are allocated once per shape and reused. The
-query side and the key side of the hash step are independent until the
-attention, so the key side runs on a second stream (and so do the unsorts
-of dK and dV), joined by events. HostPipeline runs steps on batches held in
+bucket-sorts queries and keys, gathers V and dO into sorted order, and runs
+the sparse attention forward and backward on the sorted rows, whose kernels
+write O, dQ, dK and dV straight back to original row order
+(SCFA_FLAG_ORIGINAL_ORDER; "Faster Causal Attention Over Large Sequences
+Through Sparse Flash Attention", deep-paper.org, sections
+"动态稀疏性为何会破坏它" and "SCFA 解决方案" part 2). LSE stays in sorted query
+order (the backward consumes it there). Buffers are allocated once per shape
+and reused. The query side and the key side of the hash step are independent
+until the attention, so the key side runs on a second stream, joined by an
+event. HostPipeline runs steps on batches held in
 pinned host memory with the host/device copies overlapped with the kernels.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size, lsh_bucket_sort, lsh_gather,
-               lsh_unsort, lsh_workspace_size, scfa_dense_bwd, scfa_dense_fwd, scfa_hash_bwd, scfa_hash_fwd,
-               scfa_qk_bwd, scfa_qk_fwd, workspace)
+from . import (FLAG_ORIGINAL_ORDER, FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size,
+               lsh_bucket_sort, lsh_gather, lsh_workspace_size, scfa_dense_bwd, scfa_dense_fwd, scfa_hash_bwd,
+               scfa_hash_fwd, scfa_qk_bwd, scfa_qk_fwd, workspace)
 
 
 class Step:
@@ -46,7 +47,7 @@ class Step:
             self.ws_l = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
             self.ws_lk = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
             self.side = torch.cuda.Stream(device=dev)
-            self.ev = [torch.cuda.Event() for _ in range(4)]
+            self.ev = [torch.cuda.Event() for _ in range(2)]
             self.qh = torch.empty((B, H, T), **i32)
             self.kh = torch.empty((B, H, T), **i32)
             self.pq = torch.empty((B, H, T), **i32)
@@ -57,10 +58,6 @@ class Step:
             self.k_s = torch.empty((B, H, T, D), **bf)
             self.v_s = torch.empty((B, H, T, D), **bf)
             self.do_s = torch.empty((B, H, T, D), **bf)
-            self.o_s = torch.empty((B, H, T, D), **bf)
-            self.dq_s = torch.empty((B, H, T, D), **bf)
-            self.dk_s = torch.empty((B, H, T, D), **bf)
-            self.dv_s = torch.empty((B, H, T, D), **bf)
 
     def run(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None, stream=None):
         """Forward + backward. Results land in self.o/lse/dq/dk/dv."""
@@ -86,18 +83,13 @@ class Step:
             lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
             lsh_gather(do, self.pq, self.do_s, main)
             main.wait_event(self.ev[1])
-            scfa_hash_fwd(self.q_s, self.k_s, self.v_s, self.pq, self.pk, self.qh, self.kh, scale, self.o_s,
-                          self.lse, self.ws_f, f, main)
-            scfa_hash_bwd(self.q_s, self.k_s, self.v_s, self.o_s, self.lse, self.do_s, self.pq, self.pk, self.qh,
-                          self.kh, scale, self.dq_s, self.dk_s, self.dv_s, self.ws_b, fr, main)
-            self.ev[2].record(main)
-            side.wait_event(self.ev[2])
-            lsh_unsort(self.dk_s, self.pk, self.dk, side)
-            lsh_unsort(self.dv_s, self.pk, self.dv, side)
-            self.ev[3].record(side)
-            lsh_unsort(self.o_s, self.pq, self.o, main)
-            lsh_unsort(self.dq_s, self.pq, self.dq, main)
-            main.wait_event(self.ev[3])
+            # O, dQ, dK, dV go straight to original row order (pq / pk map
+            # sorted rows to original ones); LSE stays in sorted order
+            fo = f | FLAG_ORIGINAL_ORDER
+            scfa_hash_fwd(self.q_s, self.k_s, self.v_s, self.pq, self.pk, self.qh, self.kh, scale, self.o,
+                          self.lse, self.ws_f, fo, main)
+            scfa_hash_bwd(self.q_s, self.k_s, self.v_s, self.o, self.lse, self.do_s, self.pq, self.pk, self.qh,
+                          self.kh, scale, self.dq, self.dk, self.dv, self.ws_b, fr | FLAG_ORIGINAL_ORDER, main)
         return self
 
 

@@ -54,6 +54,8 @@ def test_host_validation_without_gpu(scfa):
     assert lib.scfa_dense_fwd(bad, fake, fake, 1, 1, 128, 64, 0.1, fake, fake, fake, 1 << 30, 0, None) == 1
     # workspace too small
     assert lib.scfa_dense_fwd(fake, fake, fake, 1, 1, 128, 64, 0.1, fake, fake, fake, 16, 0, None) == 3
+    # rows in original order exist only for hash mode
+    assert lib.scfa_dense_fwd(fake, fake, fake, 1, 1, 128, 64, 0.1, fake, fake, fake, 1 << 30, 16, None) == 1
     # odd bucket count
     assert lib.lsh_hash(fake, fake, 1, 1, 16, 64, 5, fake, None) == 1
     assert scfa.status_string(5) == "device pipeline wait timed out"

@@ -275,6 +275,38 @@ def test_hash_parity(scfa, B, H, T, D, nb, seed):
     compare_heads(st, ref, ref.keys(), lse_perm=pq)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_hash_sorted_order_entry_points(scfa, D):
+    """The hash step writes O / dQ / dK / dV in original order from inside the
+    kernels; the same entry points without SCFA_FLAG_ORIGINAL_ORDER keep every
+    row tensor in sorted order, and lsh_unsort then gives the same results.
+    16 buckets keep every output below 8 in magnitude, where a bf16 half-ulp
+    (at most 2^-6) is within the 2e-2 absolute bound (with 8 buckets some dV
+    entries pass 8 and their correct bf16 rounding alone exceeds it)."""
+    nb = 16
+    p = synth.make_problem(synth.Workload("hs", "hash", 1, 2, 900, D, 31 + D, n_buckets=nb))
+    st = run_step(scfa, p, scfa.MODE_HASH)
+    B, H, T, _ = p.q.shape
+    e = lambda: torch.empty((B, H, T, D), dtype=torch.bfloat16, device="cuda")
+    o_s, dq_s, dk_s, dv_s = e(), e(), e(), e()
+    lse_s = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    ws = scfa.workspace(scfa.attn_workspace_size(scfa.MODE_HASH, 1, B, H, T, T, D))
+    scfa.scfa_hash_fwd(st.q_s, st.k_s, st.v_s, st.pq, st.pk, st.qh, st.kh, p.wl.scale, o_s, lse_s, ws)
+    scfa.scfa_hash_bwd(st.q_s, st.k_s, st.v_s, o_s, lse_s, st.do_s, st.pq, st.pk, st.qh, st.kh, p.wl.scale,
+                       dq_s, dk_s, dv_s, ws, scfa.FLAG_REUSE_TILES)
+    back = {}
+    for name, y_s, perm in (("o", o_s, st.pq), ("dq", dq_s, st.pq), ("dk", dk_s, st.pk), ("dv", dv_s, st.pk)):
+        back[name] = e()
+        scfa.lsh_unsort(y_s, perm, back[name])
+    torch.cuda.synchronize()
+    assert torch.equal(lse_s, st.lse)
+    assert torch.equal(back["o"].view(torch.int16), st.o.view(torch.int16))  # the forward is deterministic
+    ref, qh, _ = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, p.wl.scale)
+    for (b, h), r in ref.items():
+        for key in ("o", "dq", "dk", "dv"):
+            check_close(f"sorted-order {key}[{b},{h}]", back[key][b, h], r[key])
+
+
 @pytest.mark.parametrize("B,H,T,D", [(1, 2, 700, 64), (2, 1, 128, 64), (1, 1, 1, 64), (1, 2, 900, 128)])
 def test_dense_parity(scfa, B, H, T, D):
     p = synth.make_problem(synth.Workload("d", "dense", B, H, T, D, 31))
