@@ -269,8 +269,9 @@ scfa_status scfa_get_device_status(const void* ws, void* stream);
  * workspace: the forward's scratch (the live-tile metadata) is a
  * SCFA_NOALLOC_SCRATCH_BYTES array compiled into the library, which every GPU
  * that loads the library keeps until the process exits. For callers that may
- * not call cudaMalloc where they run attention: inside CUDA graph capture,
- * under a fixed-pool allocator, or in a host framework's callbacks. The call
+ * not call cudaMalloc where they run attention: servers whose allocator hands
+ * out one fixed pool at start-up and refuses later requests, and plugins in a
+ * host framework that forbids allocation inside its callbacks. The call
  * allocates nothing (no cudaMalloc / cudaFree, no allocating library call).
  *
  * - Shapes whose forward scratch exceeds SCFA_NOALLOC_SCRATCH_BYTES (see

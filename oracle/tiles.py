@@ -70,18 +70,10 @@ def head_tiles(mode: str, Tq: int, Tk: int, q_idx=None, k_idx=None, q_hash=None,
     return live, full
 
 
-NATURAL_ORDER_RATIO = 4096
-
-
-def work_order(counts, may_keep_natural=False):
-    """Order in which the tiles of a list are handed out (a scheduling choice,
-    not part of the method): tile ids by live count descending, then id
-    ascending; but a list that may keep its natural order (the key-tile list)
-    does so when its total count is at least NATURAL_ORDER_RATIO times its
-    largest count."""
+def work_order(counts):
+    """Work order of a tile list: tile ids sorted by live count descending,
+    then by id ascending (every id appears, zero counts last)."""
     counts = [max(int(c), 0) for c in counts]
-    if may_keep_natural and counts and max(counts) * NATURAL_ORDER_RATIO <= sum(counts):
-        return list(range(len(counts)))
     return sorted(range(len(counts)), key=lambda t: (-counts[t], t))
 
 
@@ -125,7 +117,7 @@ def live_list(mode: str, B: int, H: int, Tq: int, Tk: int,
                 csc_ptr.append(csc_ptr[-1] + len(is_))
                 kcount[g * nKt + j] = len(is_)
     work_fwd = work_order(qcount)
-    work_bwd = work_order(kcount, may_keep_natural=True)
+    work_bwd = work_order(kcount)
     i32 = lambda a: np.asarray(a, dtype=np.int32)
     return {
         "nQt": nQt, "nKt": nKt,

@@ -1,12 +1,12 @@
 // Allocation-free QK-sparse forward.
 //
-// Some callers cannot allocate device memory where they run attention: code
-// that runs while a CUDA graph is being captured (cudaMalloc is not a stream
-// operation and cannot be recorded), serving processes whose allocator hands
-// out one fixed pool at start-up and refuses later requests, and plugins
-// hosted by a framework that forbids allocation inside its callbacks. For
-// them scfa_qk_fwd_noalloc takes no workspace: its scratch (the live-tile
-// metadata of the forward pass) lives in an array compiled into this library.
+// Some callers cannot allocate device memory where they run attention:
+// serving processes whose allocator hands out one fixed pool at start-up and
+// refuses every later request (so a per-call workspace cannot be had), and
+// plugins hosted by a framework that forbids allocation inside its callbacks
+// (an allocation there can block or fail). For them scfa_qk_fwd_noalloc takes
+// no workspace: its scratch (the live-tile metadata of the forward pass)
+// lives in an array compiled into this library.
 //
 // The array has a fixed size, SCFA_NOALLOC_SCRATCH_BYTES; every GPU that
 // loads the library holds it until the process exits. All calls on a device

@@ -135,6 +135,9 @@ class HostPipeline:
         if self.inputs[s] is None:
             self.inputs[s] = {n: (torch.empty(t.shape, dtype=t.dtype, device=self.device) if t is not None else None)
                               for n in self.INPUTS for t in [host_inputs.get(n)]}
+            # the blocks were allocated on the compute stream, whose earlier
+            # kernels may still use that memory: the uploads wait for them
+            self.h2d.wait_stream(main)
         dst = self.inputs[s]
         if self.used[s]:
             self.h2d.wait_event(self.computed[s])  # the step two calls back has read this slot

@@ -1,7 +1,8 @@
 """The allocation-free QK-sparse forward, scfa_qk_fwd_noalloc.
 
 It exists for callers that may not call cudaMalloc where they run attention
-(graph capture, fixed-pool allocators, host-framework callbacks): it takes no
+(servers with one fixed memory pool, plugins whose host framework forbids
+allocation inside its callbacks): it takes no
 workspace and uses a scratch array compiled into the library. These tests call
 it through the C ABI and compare it with scfa_qk_fwd (caller workspace) on two
 calls in a row, and check that a shape too large for the array is refused on
