@@ -75,7 +75,7 @@ enum {
                                  workspace): skip the metadata pass. One
                                  backward-sized workspace may then serve the
                                  forward and the backward call of a step. */
-  SCFA_FLAG_ORIGINAL_ORDER = 16  /* hash mode only: the row tensors o (forward
+  SCFA_FLAG_ORIGINAL_ORDER = 16, /* hash mode only: the row tensors o (forward
                                  output and backward input), dq, dk and dv are
                                  in ORIGINAL row order: sorted query row s of
                                  head (b,h) is row q_idx[b,h,s] of o and dq,
@@ -85,6 +85,14 @@ enum {
                                  [0, T) are not written, and read as zero).
                                  q, k, v, do, lse stay in sorted order. This
                                  replaces the lsh_unsort passes. */
+  SCFA_FLAG_KEEP_O32 = 32        /* forward: also store O in fp32 in the
+                                 workspace, which must then be sized for the
+                                 backward (scfa_attn_workspace_size(mode, 1,
+                                 ...)); backward: take rowsum(dO * O) from that
+                                 copy instead of the bf16 o. Pass it to the
+                                 forward and the backward of one step on the
+                                 same workspace. The bf16 rounding of O is
+                                 otherwise the largest error term of dS. */
 };
 
 /* Tiles are SCFA_TILE rows of queries by SCFA_TILE rows of keys. */
@@ -242,6 +250,34 @@ typedef struct {
 
 scfa_status scfa_tile_view_get(const void* ws, int mode, int B, int H, int Tq, int Tk, int D,
                                scfa_tile_view* out);
+
+/* ----------------------------------------------------------------------------
+ * Pair counts (page section "实验与结果": SCFA hash-sparse attention covers
+ * 100% of the bucket collisions, Reformer's chunked attention does not). A
+ * pair (query row r, key row c) is admissible when the mode's element mask
+ * keeps it: q_idx[r] >= k_idx[c] (QK), r >= c (dense), and in hash mode also
+ * q_hash[r] == k_hash[c]. Results are written to *count, a DEVICE uint64,
+ * asynchronously on `stream`.
+ *
+ * scfa_count_pairs: admissible pairs inside the live tiles of the list that
+ *   `ws` holds (built by scfa_tiles or by an attention call with the same
+ *   mode, indices and shape; ws sized for that mode). With full coverage this
+ *   is the number of admissible pairs of the whole problem, the basis of the
+ *   useful-FLOP count (4 D forward, 10 D backward per pair).
+ * scfa_count_chunked_pairs: hash mode on bucket-sorted rows (q_idx / k_idx the
+ *   original positions, q_hash / k_hash the sorted bucket ids, [B,H,T]):
+ *   admissible pairs whose key's sorted slot lies in the query's chunk of
+ *   `chunk` slots or in the chunk before it, i.e. the pairs a Reformer-style
+ *   chunked attention over the same sort would see.
+ * ------------------------------------------------------------------------- */
+scfa_status scfa_count_pairs(int mode, const int32_t* q_idx, const int32_t* k_idx,
+                             const int32_t* q_hash, const int32_t* k_hash,
+                             int B, int H, int Tq, int Tk, int D, const void* ws, size_t ws_bytes,
+                             unsigned long long* count, void* stream);
+scfa_status scfa_count_chunked_pairs(const int32_t* q_idx, const int32_t* k_idx,
+                                     const int32_t* q_hash, const int32_t* k_hash,
+                                     int B, int H, int T, int chunk,
+                                     unsigned long long* count, void* stream);
 
 /* ----------------------------------------------------------------------------
  * Profiling hook: when set, every later attention call records

@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libscfa.so")
 
 MODE_DENSE, MODE_QK, MODE_HASH = 0, 1, 2
-FLAG_NO_PRUNE, FLAG_DEBUG_SYNC, FLAG_REUSE_TILES, FLAG_ORIGINAL_ORDER = 1, 4, 8, 16
+FLAG_NO_PRUNE, FLAG_DEBUG_SYNC, FLAG_REUSE_TILES, FLAG_ORIGINAL_ORDER, FLAG_KEEP_O32 = 1, 4, 8, 16, 32
 TILE = 128
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "CUDA error", 5: "device timeout"}
 
@@ -54,6 +54,8 @@ _SIGS = {
     "scfa_tiles": ([_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _U, _P], _I),
     "scfa_tile_view_get": ([_P, _I, _I, _I, _I, _I, _I, _P], _I),
     "scfa_get_device_status": ([_P, _P], _I),
+    "scfa_count_pairs": ([_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P], _I),
+    "scfa_count_chunked_pairs": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
     "scfa_set_kernel_events": ([_I, _P, _P], _I),
 }
 EXPORTED = tuple(_SIGS)
@@ -209,6 +211,22 @@ def scfa_tile_view_get(ws, mode, B, H, Tq, Tk, D) -> TileView:
     tv = TileView()
     _check("scfa_tile_view_get", _lib.scfa_tile_view_get(_ptr(ws), mode, B, H, Tq, Tk, D, ctypes.byref(tv)))
     return tv
+
+
+def scfa_count_pairs(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, D, ws, count, stream=None):
+    """Admissible pairs inside the live tiles held by `ws`, into the int64 CUDA tensor `count`."""
+    _need(count, torch.int64, "count")
+    _check("scfa_count_pairs", _lib.scfa_count_pairs(mode, _ptr(q_idx), _ptr(k_idx), _ptr(q_hash), _ptr(k_hash), B, H,
+                                                     Tq, Tk, D, _ptr(ws), ws.numel(), _ptr(count), _stream(stream)))
+
+
+def scfa_count_chunked_pairs(q_idx, k_idx, q_hash, k_hash, chunk, count, stream=None):
+    """Admissible hash-mode pairs within a query's chunk or the chunk before, into `count`."""
+    _need(count, torch.int64, "count")
+    B, H, T = q_idx.shape
+    _check("scfa_count_chunked_pairs", _lib.scfa_count_chunked_pairs(_ptr(q_idx), _ptr(k_idx), _ptr(q_hash),
+                                                                     _ptr(k_hash), B, H, T, chunk, _ptr(count),
+                                                                     _stream(stream)))
 
 
 def scfa_get_device_status(ws, stream=None) -> int:

@@ -104,7 +104,7 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
   w.work_pairs = take(sizeof(int32_t) * w.n_pairs);
   if (backward) {
     w.dq_acc = take(sizeof(float) * static_cast<size_t>(BH) * Tq * D);
-    w.drow = take(sizeof(float) * static_cast<size_t>(BH) * Tq);
+    w.qmeta = take(4 * sizeof(float) * static_cast<size_t>(BH) * w.nQt * kTile);
   }
   w.total = off;
   *L = w;
@@ -177,8 +177,11 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
     if (!aligned16(o_in) || !aligned16(do_) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
       return SCFA_ERR_INVALID;
   }
+  // with SCFA_FLAG_KEEP_O32 the forward also needs the backward's workspace
+  // (its fp32 copy of O lives where the backward keeps the dQ accumulator)
+  const bool keep_o32 = (flags & SCFA_FLAG_KEEP_O32) != 0;
   AttnWs L;
-  if (!attn_ws_layout(mode, backward ? 1 : 0, B, H, Tq, Tk, D, &L)) return SCFA_ERR_UNSUPPORTED;
+  if (!attn_ws_layout(mode, (backward || keep_o32) ? 1 : 0, B, H, Tq, Tk, D, &L)) return SCFA_ERR_UNSUPPORTED;
   if (!aligned256(ws) || ws_bytes < L.total) return SCFA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
@@ -213,6 +216,7 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   const bool original = (flags & SCFA_FLAG_ORIGINAL_ORDER) != 0;
   a.q_rows = original ? q_idx : nullptr;
   a.k_rows = original ? k_idx : nullptr;
+  a.o32 = keep_o32 ? reinterpret_cast<float*>(w + L.dq_acc) : nullptr;
   a.ws = w;
   a.L = &L;
   e = backward ? launch_attn_bwd(a, st) : launch_attn_fwd(a, st);

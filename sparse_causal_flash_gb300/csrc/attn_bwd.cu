@@ -53,6 +53,7 @@ constexpr int bwd_qstages() {
   return 3;
 }
 constexpr int kBwdThreads = 448;
+
 constexpr int kBwdSlots = 4;  // work items handed from the producer to the other roles
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -66,10 +67,10 @@ struct __align__(1024) BwdSmem {
   uint8_t dO[kQStages][D / 64][kSubBytes];
   uint8_t dst[2][2][kSubBytes];   // dS^T [buffer][query half][128 keys x 64 queries]
   uint8_t dqs[kSubBytes];         // dQ fp32 staging: one [128 rows x 32 floats] swizzled half at a time
-  int32_t qidx[kQStages][kTile];
-  int32_t qhash[kQStages][kTile];
-  float lse2[kQStages][kTile];    // -LSE * log2(e)
-  float drs[kQStages][kTile];     // -rowsum(dO * O) * scale
+  alignas(16) int32_t qidx[kQStages][kTile];
+  alignas(16) int32_t qhash[kQStages][kTile];
+  alignas(16) float lse2[kQStages][kTile];    // -LSE * log2(e)
+  alignas(16) float drs[kQStages][kTile];     // -rowsum(dO * O) * scale
   uint64_t kv_full, kv_empty;
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t s_full, st_empty, ds_full, pt_free, ds_free[2], dq_full, dq_empty, dkv_full, dkv_empty, drain;
@@ -88,8 +89,11 @@ struct BwdParams {
   const int32_t* k_idx;
   const int32_t* q_hash;
   const int32_t* k_hash;
-  const float* lse;
-  const float* drow;
+  // per-query metadata (bwd_pre_kernel), four arrays of qm_n entries padded to
+  // whole tiles (Tqp rows per head): -LSE*log2(e), -rowsum(dO*O)*scale, position, bucket
+  const float* qm;
+  long long qm_n;
+  int Tqp;
   const int32_t* csc_ptr;
   const int32_t* csc_rows;
   const uint8_t* cflags;
@@ -131,7 +135,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
     for (int s = 0; s < kQStages; ++s) {
-      mbar_init(&sm.q_full[s], 2);
+      mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) mbar_init(&sm.ds_free[s], 1);
@@ -205,42 +209,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (lane == 0) {
           ok = mbar_wait(&sm.q_empty[s], ((q_it / kQStages) & 1) ^ 1, abort_flag, p.status);
           if (ok) {
-            mbar_arrive_expect_tx(&sm.q_full[s], 2 * D * kTile * 2);
+            // Q_i, dO_i and the query metadata of tile i (four 512-byte rows
+            // of the padded arrays) land on one barrier
+            mbar_arrive_expect_tx(&sm.q_full[s], 2 * D * kTile * 2 + 4 * kTile * 4);
             for (int sub = 0; sub < D / 64; ++sub) {
               tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
               tma_load_3d(sm.dO[s][sub], &tm_do, &sm.q_full[s], sub * 64, i * kTile, bh);
             }
+            const float* m = p.qm + static_cast<long long>(bh) * p.Tqp + i * kTile;
+            bulk_load(sm.lse2[s], m, kTile * 4, &sm.q_full[s]);
+            bulk_load(sm.drs[s], m + p.qm_n, kTile * 4, &sm.q_full[s]);
+            bulk_load(sm.qidx[s], m + 2 * p.qm_n, kTile * 4, &sm.q_full[s]);
+            bulk_load(sm.qhash[s], m + 3 * p.qm_n, kTile * 4, &sm.q_full[s]);
           }
         }
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
-        // query metadata of tile i, next to its Q / dO stage: every lane issues
-        // its 16 loads before any store, so the warp pays one memory latency
-        {
-          int qid[4], qhv[4];
-          float lsev[4], drv[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = lane + 32 * u;
-            const int qrow = i * kTile + c;
-            const bool qv = qrow < p.Tq;
-            const long long gq = static_cast<long long>(bh) * p.Tq + (qv ? qrow : 0);
-            qid[u] = (p.mode == SCFA_MODE_DENSE) ? (qv ? qrow : INT_MIN) : (qv ? p.q_idx[gq] : INT_MIN);
-            qhv[u] = (p.mode == SCFA_MODE_HASH && qv) ? p.q_hash[gq] : 0;
-            lsev[u] = qv ? p.lse[gq] : 0.f;
-            drv[u] = qv ? p.drow[gq] : 0.f;
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = lane + 32 * u;
-            sm.qidx[s][c] = qid[u];
-            sm.qhash[s][c] = qhv[u];
-            sm.lse2[s][c] = -(lsev[u] * kLog2e);
-            sm.drs[s][c] = -(drv[u] * p.scale);
-          }
-        }
-        __threadfence_block();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.q_full[s]);
         ++q_it;
       }
       if (!ok) break;
@@ -617,10 +600,10 @@ struct __align__(1024) Bwd128Smem {
   uint8_t dO[2][kSubBytes];
   uint8_t dsq[2][kSubBytes];   // dS^T [query half][128 keys x 64 queries] (bf16), then
                                // the dQ staging tiles [128 rows x 32 floats] (fp32)
-  int32_t qidx[2][kTile];      // query metadata by step parity
-  int32_t qhash[2][kTile];
-  float lse2[2][kTile];        // -LSE * log2(e)
-  float drs[2][kTile];         // -rowsum(dO * O) * scale
+  alignas(16) int32_t qidx[2][kTile];      // query metadata by step parity
+  alignas(16) int32_t qhash[2][kTile];
+  alignas(16) float lse2[2][kTile];        // -LSE * log2(e)
+  alignas(16) float drs[2][kTile];         // -rowsum(dO * O) * scale
   uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, loaded, ds_full;
   uint64_t dq_full, dq_empty, dqs_free, dkv_full, dkv_empty, drain, dq_sync;
   int32_t items[kBwdSlots];
@@ -647,7 +630,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
     }
-    mbar_init(&sm.do_full, 2);
+    mbar_init(&sm.do_full, 1);
     mbar_init(&sm.do_empty, 1);
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.loaded, 256);
@@ -713,49 +696,28 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       for (int t = 0; t < n; ++t) {
         const int i = p.csc_rows[start + t];
         const int mb = qt & 1, s = qt & 1;
-        {
-          // row metadata first (plain loads, in flight during the waits below)
-          int qid[4], qhv[4];
-          float lsev[4], drv[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = lane + 32 * u;
-            const int qrow = i * kTile + c;
-            const bool qv = qrow < p.Tq;
-            const long long gq = static_cast<long long>(bh) * p.Tq + (qv ? qrow : 0);
-            qid[u] = (p.mode == SCFA_MODE_DENSE) ? (qv ? qrow : INT_MIN) : (qv ? p.q_idx[gq] : INT_MIN);
-            qhv[u] = (p.mode == SCFA_MODE_HASH && qv) ? p.q_hash[gq] : 0;
-            lsev[u] = qv ? p.lse[gq] : 0.f;
-            drv[u] = qv ? p.drow[gq] : 0.f;
+        if (lane == 0) {
+          // Q into its stage once dK two tiles back has read it; dO and the
+          // query metadata (four 512-byte rows of the padded arrays, kept by
+          // step parity) once dV of the previous tile has read dO
+          ok = mbar_wait(&sm.q_empty[s], ((qt >> 1) & 1) ^ 1, abort_flag, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.q_full[s], D * kTile * 2);
+            for (int sub = 0; sub < 2; ++sub)
+              tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
+            ok = mbar_wait(&sm.do_empty, (qt & 1) ^ 1, abort_flag, p.status);
           }
-          if (lane == 0) {
-            // Q into its stage once dK two tiles back has read it, dO once dV
-            // of the previous tile has
-            ok = mbar_wait(&sm.q_empty[s], ((qt >> 1) & 1) ^ 1, abort_flag, p.status);
-            if (ok) {
-              mbar_arrive_expect_tx(&sm.q_full[s], D * kTile * 2);
-              for (int sub = 0; sub < 2; ++sub)
-                tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
-              ok = mbar_wait(&sm.do_empty, (qt & 1) ^ 1, abort_flag, p.status);
-            }
-            if (ok) {
-              mbar_arrive_expect_tx(&sm.do_full, D * kTile * 2);
-              for (int sub = 0; sub < 2; ++sub) tma_load_3d(sm.dO[sub], &tm_do, &sm.do_full, sub * 64, i * kTile, bh);
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = lane + 32 * u;
-            sm.qidx[mb][c] = qid[u];
-            sm.qhash[mb][c] = qhv[u];
-            sm.lse2[mb][c] = -(lsev[u] * kLog2e);
-            sm.drs[mb][c] = -(drv[u] * p.scale);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.do_full, D * kTile * 2 + 4 * kTile * 4);
+            for (int sub = 0; sub < 2; ++sub) tma_load_3d(sm.dO[sub], &tm_do, &sm.do_full, sub * 64, i * kTile, bh);
+            const float* m = p.qm + static_cast<long long>(bh) * p.Tqp + i * kTile;
+            bulk_load(sm.lse2[mb], m, kTile * 4, &sm.do_full);
+            bulk_load(sm.drs[mb], m + p.qm_n, kTile * 4, &sm.do_full);
+            bulk_load(sm.qidx[mb], m + 2 * p.qm_n, kTile * 4, &sm.do_full);
+            bulk_load(sm.qhash[mb], m + 3 * p.qm_n, kTile * 4, &sm.do_full);
           }
         }
-        __threadfence_block();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.do_full);
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
         ++qt;
       }
       if (!ok) break;
@@ -1086,40 +1048,92 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   }
 }
 
-// Drow[row] = sum_d dO * O (fp32) and dq_acc[row] = 0. D/8 lanes per row (one
-// 16-byte chunk each), 32 / (D/8) rows per warp step; the loop is warp-uniform
-// so the shuffle reduction always has the whole warp.
+// Per query row: Drow = sum_d dO * O (fp32) and dq_acc[row] = 0, and the
+// metadata that the backward's producer copies next to each Q / dO tile,
+// written into four arrays padded to whole tiles of 128 rows (Tqp rows per
+// head): -LSE * log2(e), -Drow * scale, the position (the row itself in dense
+// mode) and the bucket id. Padding rows get position INT_MIN (never
+// admissible) and zeros. D/8 lanes per row (one 16-byte chunk each),
+// 32 / (D/8) rows per warp step; the loop is warp-uniform so the shuffle
+// reduction always has the whole warp.
+// With o32 (the forward's fp32 copy of O, kept in the dQ accumulator's place)
+// the sum is taken from it instead of the bf16 o: the bf16 store of O is the
+// largest error term of dS otherwise. Each lane reads its chunk of o32 before
+// zeroing it.
+struct PreParams {
+  const uint16_t* o;
+  const uint16_t* dO;
+  const float* o32;
+  const int32_t* o_rows;
+  const float* lse;
+  const int32_t* q_idx;
+  const int32_t* q_hash;
+  float* dq_acc;
+  float* qm;          // four arrays of n_pad entries
+  long long n_pad;    // B*H*Tqp
+  int Tq, Tqp, mode;
+  float scale;
+};
+
 template <int D>
-__global__ void bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dO, long long rows,
-                               float* __restrict__ drow, float* __restrict__ dq_acc,
-                               const int32_t* __restrict__ o_rows, int T) {
+__global__ void bwd_pre_kernel(const PreParams p) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = threadIdx.x & 31;
   const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   for (long long wg = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       wg * kRowsPerWarp < rows; wg += warps) {
-    const long long row = wg * kRowsPerWarp + lane / kLanesPerRow;
+       wg * kRowsPerWarp < p.n_pad; wg += warps) {
+    const long long rp = wg * kRowsPerWarp + lane / kLanesPerRow;  // padded row
     const int ch = lane % kLanesPerRow;
-    const bool active = row < rows;
+    const long long bh = rp / p.Tqp;
+    const int r = static_cast<int>(rp - bh * p.Tqp);
+    const bool inside = rp < p.n_pad;
+    const bool active = inside && r < p.Tq;
+    const long long row = bh * p.Tq + r;
     float s = 0.f;
     if (active) {
-      // O may be stored in original row order (o_rows maps sorted -> original)
-      const long long orow = mapped_row(o_rows, row, static_cast<int>(row % T), T);
-      const uint4 a = orow >= 0 ? reinterpret_cast<const uint4*>(o + orow * D)[ch] : make_uint4(0, 0, 0, 0);
-      const uint4 b = reinterpret_cast<const uint4*>(dO + row * D)[ch];
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+      const uint4 b = reinterpret_cast<const uint4*>(p.dO + row * D)[ch];
+      const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+      if (p.o32 != nullptr) {
+        const float4 a0 = reinterpret_cast<const float4*>(p.o32 + row * D)[ch * 2];
+        const float4 a1 = reinterpret_cast<const float4*>(p.o32 + row * D)[ch * 2 + 1];
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        s = fmaf(__uint_as_float(aw[u] << 16), __uint_as_float(bw[u] << 16), s);
-        s = fmaf(__uint_as_float(aw[u] & 0xFFFF0000u), __uint_as_float(bw[u] & 0xFFFF0000u), s);
+        for (int u = 0; u < 4; ++u) {
+          s = fmaf(av[2 * u], __uint_as_float(bw[u] << 16), s);
+          s = fmaf(av[2 * u + 1], __uint_as_float(bw[u] & 0xFFFF0000u), s);
+        }
+      } else {
+        // O may be stored in original row order (o_rows maps sorted -> original)
+        const long long orow = mapped_row(p.o_rows, row, r, p.Tq);
+        const uint4 a = orow >= 0 ? reinterpret_cast<const uint4*>(p.o + orow * D)[ch] : make_uint4(0, 0, 0, 0);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          s = fmaf(__uint_as_float(aw[u] << 16), __uint_as_float(bw[u] << 16), s);
+          s = fmaf(__uint_as_float(aw[u] & 0xFFFF0000u), __uint_as_float(bw[u] & 0xFFFF0000u), s);
+        }
       }
     }
 #pragma unroll
     for (int off = kLanesPerRow / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (inside && ch == 0) {
+      float* m = p.qm + rp;
+      int32_t* mi = reinterpret_cast<int32_t*>(p.qm) + rp;
+      if (active) {
+        m[0] = -(p.lse[row] * kLog2e);
+        m[p.n_pad] = -(s * p.scale);
+        mi[2 * p.n_pad] = p.mode == SCFA_MODE_DENSE ? r : p.q_idx[row];
+        mi[3 * p.n_pad] = p.mode == SCFA_MODE_HASH ? p.q_hash[row] : 0;
+      } else {
+        m[0] = 0.f;
+        m[p.n_pad] = 0.f;
+        mi[2 * p.n_pad] = INT_MIN;
+        mi[3 * p.n_pad] = 0;
+      }
+    }
     if (active) {
-      if (ch == 0) drow[row] = s;
-      float4* z = reinterpret_cast<float4*>(dq_acc + row * D) + ch * 2;
+      float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D) + ch * 2;
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -1160,14 +1174,31 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   const long long BH = static_cast<long long>(a.B) * a.H;
   const int sms = num_sms();
   float* dq_acc = reinterpret_cast<float*>(a.ws + L.dq_acc);
-  float* drow = reinterpret_cast<float*>(a.ws + L.drow);
+  float* qm = reinterpret_cast<float*>(a.ws + L.qmeta);
+  const int Tqp = L.nQt * kTile;
   const long long qrows = BH * a.Tq;
+  const long long n_pad = BH * Tqp;
   {
-    const long long work = (qrows * (D / 8) + 31) / 32 * 32;
+    PreParams pp;
+    pp.o = a.o;
+    pp.dO = a.do_;
+    pp.o32 = a.o32;
+    pp.o_rows = a.q_rows;
+    pp.lse = a.lse_in;
+    pp.q_idx = a.q_idx;
+    pp.q_hash = a.q_hash;
+    pp.dq_acc = dq_acc;
+    pp.qm = qm;
+    pp.n_pad = n_pad;
+    pp.Tq = a.Tq;
+    pp.Tqp = Tqp;
+    pp.mode = a.mode;
+    pp.scale = a.scale;
+    const long long work = (n_pad * (D / 8) + 31) / 32 * 32;
     long long g = (work + 255) / 256;
     if (g > sms * 16LL) g = sms * 16LL;
     if (g < 1) g = 1;
-    bwd_pre_kernel<D><<<static_cast<int>(g), 256, 0, st>>>(a.o, a.do_, qrows, drow, dq_acc, a.q_rows, a.Tq);
+    bwd_pre_kernel<D><<<static_cast<int>(g), 256, 0, st>>>(pp);
   }
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, BH) || !make_tmap_bf16_3d(&tk, a.k, D, a.Tk, BH) ||
@@ -1185,8 +1216,9 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   p.k_idx = a.k_idx;
   p.q_hash = a.q_hash;
   p.k_hash = a.k_hash;
-  p.lse = a.lse_in;
-  p.drow = drow;
+  p.qm = qm;
+  p.qm_n = n_pad;
+  p.Tqp = Tqp;
   p.csc_ptr = reinterpret_cast<const int32_t*>(a.ws + L.csc_ptr);
   p.csc_rows = reinterpret_cast<const int32_t*>(a.ws + L.csc_rows);
   p.cflags = reinterpret_cast<const uint8_t*>(a.ws + L.cflags);

@@ -75,6 +75,26 @@ struct __align__(1024) FwdSmem {
   int abort_flag;
 };
 
+// fp32 copy of one O row (thread = row) for the backward's rowsum(dO * O);
+// `scale` 0 writes zeros (a row with no admissible key, or one whose output
+// row is outside [0, T) and therefore reads as zero)
+template <int D>
+__device__ __forceinline__ void store_o32_row(float* dst, const uint32_t (&orr)[D / 32][32], float scale) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int c = 0; c < D / 4; ++c) {
+    const int e = c * 4;
+    d[c] = make_float4(__uint_as_float(orr[e >> 5][(e + 0) & 31]) * scale, __uint_as_float(orr[e >> 5][(e + 1) & 31]) * scale,
+                       __uint_as_float(orr[e >> 5][(e + 2) & 31]) * scale, __uint_as_float(orr[e >> 5][(e + 3) & 31]) * scale);
+  }
+}
+template <int D>
+__device__ __forceinline__ void zero_o32_row(float* dst) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int c = 0; c < D / 4; ++c) d[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 struct FwdParams {
   int mode;
   int Tq, Tk, nQt, nPairs;
@@ -96,6 +116,7 @@ struct FwdParams {
   uint16_t* o;
   const int32_t* o_rows;  // null, or the original row of each sorted query row
   float* lse;
+  float* o32;             // null, or an fp32 copy of O [B,H,Tq,D] in row order of q
   int* status;
 };
 
@@ -346,6 +367,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         f_n = p.fflags[e_beg + 1];
       }
       float m_used = -INFINITY, l = 0.f;
+      float m_top = -INFINITY;  // largest score of the row so far (log2 units)
       bool ok = true, any = false;
       for (int e = e_beg; e < e_end; ++e) {
         const bool full = (f_c & kFlagFull) != 0;
@@ -407,6 +429,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
         const float m_new = fmaxf(m_used, mt);
+        m_top = fmaxf(m_top, mt);
         const bool resc = m_new > m_used + kRescaleThreshold;
         float alpha = 1.f;
         if (resc) {
@@ -478,6 +501,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
           }
           p.lse[grow] = -INFINITY;
+          if (p.o32) zero_o32_row<D>(p.o32 + grow * D);
         }
         continue;
       }
@@ -493,7 +517,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_arrive(&sm.o_empty[grp]);
       ++o_it;
       if (valid) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        // O is normalised by the row sum as PV saw it for the largest score:
+        // with the lazy rescale its weight 2^(m_top - m_used) need not be 1,
+        // and PV used its bf16 rounding. Swapping that one term of l for the
+        // rounded value makes a row with a single key return V exactly and
+        // removes the largest coherent error of O on rows with few keys. LSE
+        // keeps the unrounded sum (the backward recomputes P from it).
+        float l_o = l;
+        if (l > 0.f) {
+          const float pm = ex2_approx(m_top - m_used);
+          l_o = l - pm + __bfloat162float(__float2bfloat16_rn(pm));
+        }
+        const float inv = l_o > 0.f ? 1.f / l_o : 0.f;
         const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
         uint4* dst = reinterpret_cast<uint4*>(p.o + (orow >= 0 ? orow : grow) * D);
 #pragma unroll
@@ -507,6 +542,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (orow >= 0) dst[c] = u;
         }
         p.lse[grow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+        if (p.o32) store_o32_row<D>(p.o32 + grow * D, orr, orow >= 0 ? inv : 0.f);
       }
     }
   }
@@ -775,6 +811,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         f_n = p.fflags[e_beg + 1];
       }
       float m_used = -INFINITY, l = 0.f;
+      float m_top = -INFINITY;  // largest score of the row so far (log2 units)
       bool ok = true, any = false;
       for (int e = e_beg; e < e_end; ++e) {
         const bool full = (f_c & kFlagFull) != 0;
@@ -831,6 +868,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
         const float m_new = fmaxf(m_used, mt);
+        m_top = fmaxf(m_top, mt);
         const bool resc = m_new > m_used + kRescaleThreshold;
         float alpha = 1.f;
         if (resc) {
@@ -907,6 +945,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
           }
           p.lse[grow] = -INFINITY;
+          if (p.o32) zero_o32_row<D>(p.o32 + grow * D);
         }
         continue;
       }
@@ -922,7 +961,18 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_arrive(&sm.o_empty);
       ++o_it;
       if (valid) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        // O is normalised by the row sum as PV saw it for the largest score:
+        // with the lazy rescale its weight 2^(m_top - m_used) need not be 1,
+        // and PV used its bf16 rounding. Swapping that one term of l for the
+        // rounded value makes a row with a single key return V exactly and
+        // removes the largest coherent error of O on rows with few keys. LSE
+        // keeps the unrounded sum (the backward recomputes P from it).
+        float l_o = l;
+        if (l > 0.f) {
+          const float pm = ex2_approx(m_top - m_used);
+          l_o = l - pm + __bfloat162float(__float2bfloat16_rn(pm));
+        }
+        const float inv = l_o > 0.f ? 1.f / l_o : 0.f;
         const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
         uint4* dst = reinterpret_cast<uint4*>(p.o + (orow >= 0 ? orow : grow) * D);
 #pragma unroll
@@ -936,6 +986,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           if (orow >= 0) dst[c] = u;
         }
         p.lse[grow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+        if (p.o32) store_o32_row<D>(p.o32 + grow * D, orr, orow >= 0 ? inv : 0.f);
       }
     }
   }
@@ -988,6 +1039,7 @@ static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   p.o = a.o_out;
   p.o_rows = a.q_rows;
   p.lse = a.lse_out;
+  p.o32 = a.o32;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1030,6 +1082,7 @@ static cudaError_t launch_fwd1(const AttnArgs& a, cudaStream_t st) {
   p.o = a.o_out;
   p.o_rows = a.q_rows;
   p.lse = a.lse_out;
+  p.o32 = a.o32;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   const size_t smem = sizeof(Fwd1Smem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -35,7 +35,9 @@ struct AttnWs {
                                          // 4 live for 2m + 1, 8 FULL for 2m + 1), key tiles ascending
   size_t work_pairs = 0;                 // pair ids by union size descending
   size_t dq_acc = 0;                     // backward: fp32 dQ accumulator [B,H,Tq,D]
-  size_t drow = 0;                       // backward: fp32 rowsum(dO * O) [B,H,Tq]
+  size_t qmeta = 0;                      // backward: per-query metadata padded to whole tiles, four
+                                         // [B*H][nQt*128] arrays: -LSE*log2(e) and -rowsum(dO*O)*scale
+                                         // (fp32), position and bucket id (int32)
   size_t total = 0;
 };
 
@@ -90,6 +92,9 @@ struct AttnArgs {
   // hash mode with SCFA_FLAG_ORIGINAL_ORDER: destination row (within the
   // head) of each sorted query / key row; null = rows stay in place
   const int32_t *q_rows, *k_rows;
+  // SCFA_FLAG_KEEP_O32: the fp32 copy of O in the workspace (the forward
+  // writes it, the backward pre-pass reads it); null otherwise
+  float* o32;
   char* ws;
   const AttnWs* L;
 };

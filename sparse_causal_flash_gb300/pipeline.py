@@ -17,7 +17,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (FLAG_ORIGINAL_ORDER, FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size,
+from . import (FLAG_KEEP_O32, FLAG_ORIGINAL_ORDER, FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size,
                lsh_bucket_sort, lsh_gather, lsh_workspace_size, scfa_dense_bwd, scfa_dense_fwd, scfa_hash_bwd,
                scfa_hash_fwd, scfa_qk_bwd, scfa_qk_fwd, workspace)
 
@@ -61,7 +61,9 @@ class Step:
 
     def run(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None, stream=None):
         """Forward + backward. Results land in self.o/lse/dq/dk/dv."""
-        f = self.flags
+        # the forward keeps O in fp32 in the shared workspace for the
+        # backward's rowsum(dO * O); the backward reuses the live-tile list
+        f = self.flags | FLAG_KEEP_O32
         fr = f | FLAG_REUSE_TILES
         if self.mode == MODE_DENSE:
             scfa_dense_fwd(q, k, v, scale, self.o, self.lse, self.ws_f, f, stream)

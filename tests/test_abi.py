@@ -56,6 +56,9 @@ def test_host_validation_without_gpu(scfa):
     assert lib.scfa_dense_fwd(fake, fake, fake, 1, 1, 128, 64, 0.1, fake, fake, fake, 16, 0, None) == 3
     # rows in original order exist only for hash mode
     assert lib.scfa_dense_fwd(fake, fake, fake, 1, 1, 128, 64, 0.1, fake, fake, fake, 1 << 30, 16, None) == 1
+    # an fp32 copy of O needs the backward-sized workspace, even in the forward
+    fwd_ws = scfa.attn_workspace_size(scfa.MODE_DENSE, 0, 1, 1, 128, 128, 64)
+    assert lib.scfa_dense_fwd(fake, fake, fake, 1, 1, 128, 64, 0.1, fake, fake, fake, fwd_ws, 32, None) == 3
     # odd bucket count
     assert lib.lsh_hash(fake, fake, 1, 1, 16, 64, 5, fake, None) == 1
     assert scfa.status_string(5) == "device pipeline wait timed out"

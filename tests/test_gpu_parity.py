@@ -12,7 +12,7 @@ import torch
 
 import synth
 from harness import check_close, check_lse, to_np
-from oracle import attention, lsh, pipelines, tiles
+from oracle import attention, coverage, lsh, pipelines, tiles
 
 pytestmark = pytest.mark.gpu
 
@@ -246,6 +246,61 @@ def test_tiles_dense_bitexact(scfa, T):
     compare_tiles(got, tiles.live_list("dense", 1, 2, T, T))
 
 
+# ------------------------------------------------------------------ pair counts
+def device_count(scfa, mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, ws):
+    c = torch.zeros(1, dtype=torch.int64, device="cuda")
+    scfa.scfa_count_pairs(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, 64, ws, c)
+    torch.cuda.synchronize()
+    return int(c.item())
+
+
+@pytest.mark.parametrize("mode,T,arg", [("qk", 3000, 0.6), ("qk", 1000, 0.2), ("hash", 2000, 8), ("hash", 700, 1),
+                                        ("dense", 700, None), ("dense", 1, None)])
+def test_count_pairs_equals_all_admissible_pairs(scfa, mode, T, arg):
+    """The on-device count of admissible pairs inside the live tiles equals
+    the oracle's count over the whole explicit mask (the page's 100%
+    coverage), exactly."""
+    B, H = 2, 3
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    if mode == "qk":
+        p = synth.make_problem(synth.Workload("c", "qk", B, H, T, 64, 80, p_keep=arg))
+        qi, ki = p.q_idx.numpy(), p.k_idx.numpy()
+        Tq, Tk = qi.shape[2], ki.shape[2]
+        args = (scfa.MODE_QK, t32(qi), t32(ki), None, None)
+        want = sum(attention.admissible_pairs(attention.mask_qk(qi[b, h], ki[b, h])) for b in range(B) for h in range(H))
+    elif mode == "hash":
+        rng = np.random.default_rng(T + arg)
+        pq, qs, _ = pipelines.hash_sort_view(rng.integers(0, arg, (B, H, T)), arg)
+        pk, ks, _ = pipelines.hash_sort_view(rng.integers(0, arg, (B, H, T)), arg)
+        Tq = Tk = T
+        args = (scfa.MODE_HASH, t32(pq), t32(pk), t32(qs), t32(ks))
+        want = sum(attention.admissible_pairs(attention.mask_hash(qs[b, h], ks[b, h], q_pos=pq[b, h], k_pos=pk[b, h]))
+                   for b in range(B) for h in range(H))
+    else:
+        Tq = Tk = T
+        args = (scfa.MODE_DENSE, None, None, None, None)
+        want = B * H * attention.admissible_pairs(attention.mask_dense(T))
+    ws = scfa.workspace(scfa.attn_workspace_size(args[0], 1, B, H, Tq, Tk, 64))
+    scfa.scfa_tiles(*args, B, H, Tq, Tk, 64, ws)
+    assert device_count(scfa, *args, B, H, Tq, Tk, ws) == want
+
+
+@pytest.mark.parametrize("chunk", [32, 128, 300, 2048])
+def test_count_chunked_pairs_bitexact(scfa, chunk):
+    """Reformer-style chunk coverage on the bucket-sorted rows, counted on the
+    device, equals the oracle's count for every head."""
+    B, H, T, nb = 2, 2, 2000, 8
+    rng = np.random.default_rng(90 + chunk)
+    pq, qs, _ = pipelines.hash_sort_view(rng.integers(0, nb, (B, H, T)), nb)
+    pk, ks, _ = pipelines.hash_sort_view(rng.integers(0, nb, (B, H, T)), nb)
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    c = torch.zeros(1, dtype=torch.int64, device="cuda")
+    scfa.scfa_count_chunked_pairs(t32(pq), t32(pk), t32(qs), t32(ks), chunk, c)
+    torch.cuda.synchronize()
+    want = sum(coverage.chunked_pairs(qs[b, h], ks[b, h], pq[b, h], pk[b, h], chunk) for b in range(B) for h in range(H))
+    assert int(c.item()) == want
+
+
 # ------------------------------------------------------------------ attention
 def run_step(scfa, p, mode, flags=0):
     from sparse_causal_flash_gb300.pipeline import Step
@@ -304,9 +359,10 @@ def test_hash_sorted_order_entry_points(scfa, D):
     o_s, dq_s, dk_s, dv_s = e(), e(), e(), e()
     lse_s = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
     ws = scfa.workspace(scfa.attn_workspace_size(scfa.MODE_HASH, 1, B, H, T, T, D))
-    scfa.scfa_hash_fwd(st.q_s, st.k_s, st.v_s, st.pq, st.pk, st.qh, st.kh, p.wl.scale, o_s, lse_s, ws)
+    k32 = scfa.FLAG_KEEP_O32
+    scfa.scfa_hash_fwd(st.q_s, st.k_s, st.v_s, st.pq, st.pk, st.qh, st.kh, p.wl.scale, o_s, lse_s, ws, k32)
     scfa.scfa_hash_bwd(st.q_s, st.k_s, st.v_s, o_s, lse_s, st.do_s, st.pq, st.pk, st.qh, st.kh, p.wl.scale,
-                       dq_s, dk_s, dv_s, ws, scfa.FLAG_REUSE_TILES)
+                       dq_s, dk_s, dv_s, ws, scfa.FLAG_REUSE_TILES | k32)
     back = {}
     for name, y_s, perm in (("o", o_s, st.pq), ("dq", dq_s, st.pq), ("dk", dk_s, st.pk), ("dv", dv_s, st.pk)):
         back[name] = e()
@@ -341,7 +397,7 @@ def test_original_order_skips_rows_outside_range(scfa, D):
     o, dq, dk, dv = nan(), nan(), nan(), nan()
     lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
     ws = scfa.workspace(scfa.attn_workspace_size(scfa.MODE_HASH, 1, B, H, T, T, D))
-    oo = scfa.FLAG_ORIGINAL_ORDER
+    oo = scfa.FLAG_ORIGINAL_ORDER | scfa.FLAG_KEEP_O32
     scfa.scfa_hash_fwd(st.q_s, st.k_s, st.v_s, gpq, gpk, st.qh, st.kh, p.wl.scale, o, lse, ws, oo)
     scfa.scfa_hash_bwd(st.q_s, st.k_s, st.v_s, o, lse, st.do_s, gpq, gpk, st.qh, st.kh, p.wl.scale,
                        dq, dk, dv, ws, oo | scfa.FLAG_REUSE_TILES)
@@ -428,6 +484,12 @@ def test_full_qk_8k_sampled_heads(scfa):
     heads = [(0, 0), (3, 11)]
     ref = pipelines.run_qk(p.q, p.k, p.v, p.do, p.q_idx.numpy(), p.k_idx.numpy(), wl.scale, heads=heads)
     compare_heads(st, ref, heads)
+    # the bench's unit count: admissible pairs inside the live tiles, on the device
+    B, H, Tq, _ = p.q.shape
+    qi, ki = p.q_idx.numpy(), p.k_idx.numpy()
+    want = sum(attention.admissible_pairs(attention.mask_qk(qi[b, h], ki[b, h])) for b in range(B) for h in range(H))
+    assert device_count(scfa, scfa.MODE_QK, cuda(p.q_idx), cuda(p.k_idx), None, None, B, H, Tq, p.k.shape[2],
+                        st.ws_b) == want
 
 
 def test_full_hash_8k_sampled_heads(scfa):
@@ -441,6 +503,11 @@ def test_full_hash_8k_sampled_heads(scfa):
     ref, _, _ = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, wl.scale, heads=heads, q_hash=qh, k_hash=kh)
     pq, _, _ = pipelines.hash_sort_view(qh, wl.n_buckets)
     compare_heads(st, ref, heads, lse_perm=pq)
+    # the bench's unit count: admissible pairs inside the live tiles (device)
+    # against the oracle's hash mask over every head, from the oracle's ids
+    want = sum(attention.admissible_pairs(attention.mask_hash(qh[b, h], kh[b, h]))
+               for b in range(wl.B) for h in range(wl.H))
+    assert device_count(scfa, scfa.MODE_HASH, st.pq, st.pk, st.qh, st.kh, wl.B, wl.H, wl.T, wl.T, st.ws_b) == want
 
 
 def test_full_hash_16k_sampled_heads(scfa):
