@@ -61,27 +61,29 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the other target workloads")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     return ap.parse_args()
 
 
 # ---------------------------------------------------------------------------- units
-def admissible_pairs(wl, prob, step=None) -> int:
-    """Exact count of unmasked (query, key) pairs of the whole workload."""
-    if wl.mode == "dense":
-        return wl.B * wl.H * wl.T * (wl.T + 1) // 2
-    if wl.mode == "qk":
-        qi = prob.q_idx.numpy().astype(np.int64)
-        ki = prob.k_idx.numpy().astype(np.int64)
-        total = 0
-        for b in range(qi.shape[0]):
-            for h in range(qi.shape[1]):
-                q = qi[b, h][qi[b, h] >= 0]
-                k = np.sort(ki[b, h][ki[b, h] != 2**31 - 1])
-                total += int(np.searchsorted(k, q, side="right").sum())
-        return total
-    # hash: bucket ranges from the library's own (bit-exact) stable sort; inside
-    # a bucket both lists are in position order
+def host_pairs_qk(prob) -> int:
+    """Admissible pairs of a QK-sparse problem from its index lists (host):
+    per kept query, the kept keys at or before its position."""
+    qi = prob.q_idx.numpy().astype(np.int64)
+    ki = prob.k_idx.numpy().astype(np.int64)
+    total = 0
+    for b in range(qi.shape[0]):
+        for h in range(qi.shape[1]):
+            q = qi[b, h][qi[b, h] >= 0]
+            k = np.sort(ki[b, h][ki[b, h] != 2**31 - 1])
+            total += int(np.searchsorted(k, q, side="right").sum())
+    return total
+
+
+def host_pairs_hash(step) -> int:
+    """Admissible pairs of a hash-sparse step from its sorted view (host): per
+    bucket, the keys at or before each query's position."""
     pq = step.pq.cpu().numpy().astype(np.int64)
     pk = step.pk.cpu().numpy().astype(np.int64)
     oq = step.offq.cpu().numpy().astype(np.int64)
@@ -95,6 +97,30 @@ def admissible_pairs(wl, prob, step=None) -> int:
                 if len(qpos) and len(kpos):
                     total += int(np.searchsorted(kpos, qpos, side="right").sum())
     return total
+
+
+def admissible_pairs(scfa, wl, prob, step, dev) -> int:
+    """Unit count of a step: admissible pairs inside the live tiles, counted on
+    the device from the list the step built (scfa_count_pairs), and checked
+    against a host count of the whole mask (the two agree when the live tiles
+    cover every admissible pair, which the GPU tests also check against the
+    oracle)."""
+    import torch
+    B, H, Tq, D = step.B, step.H, step.Tq, step.D
+    count = torch.zeros(1, dtype=torch.int64, device=dev)
+    if wl.mode == "dense":
+        scfa.scfa_count_pairs(scfa.MODE_DENSE, None, None, None, None, B, H, Tq, Tq, D, step.ws_b, count)
+        host = B * H * Tq * (Tq + 1) // 2
+    elif wl.mode == "qk":
+        scfa.scfa_count_pairs(scfa.MODE_QK, prob.q_idx.to(dev), prob.k_idx.to(dev), None, None, B, H, Tq, step.Tk, D,
+                              step.ws_b, count)
+        host = host_pairs_qk(prob)
+    else:
+        scfa.scfa_count_pairs(scfa.MODE_HASH, step.pq, step.pk, step.qh, step.kh, B, H, Tq, Tq, D, step.ws_b, count)
+        host = host_pairs_hash(step)
+    device = int(count.item())
+    assert device == host, f"pair count: device {device} != host {host}"
+    return device
 
 
 def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0) -> int:
@@ -311,6 +337,197 @@ def run_reference(args, wl, rank, world):
 
 
 # ---------------------------------------------------------------------------- our arm
+# Other target workloads, measured in the same run (hash 8k; hash and QK 16k
+# with the drop sweep of the 16k configuration). The million-token workload
+# runs with --workload (about 50 ms per step plus a dense comparator of
+# seconds).
+SECONDARY = ("hash_b4h12_t8192_d64_nb16", "hash_b2h12_t16384_d64_nb32", "qk_b2h12_t16384_d64_keep0.8",
+             "qk_b2h12_t16384_d64_keep0.7", "qk_b2h12_t16384_d64_keep0.5", "qk_b2h12_t16384_d64_keep0.3")
+REFORMER_CHUNKS = (64, 128, 256, 512)
+
+
+class Runner:
+    """Device-side measurement of one workload at a time (timing, stages,
+    naive baseline, dense comparator, coverage)."""
+
+    def __init__(self, scfa, torch, dev, stream, dist, peaks):
+        self.scfa, self.torch, self.dev, self.stream, self.dist = scfa, torch, dev, stream, dist
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.peak_burst, self.peak_sus, self.peak_kind = peaks
+        self.dense_cache = {}
+
+    def timed(self, run, K, kernel_events=False):
+        """K steps, each after an L2 flush, CUDA events on the compute stream."""
+        torch, scfa, stream = self.torch, self.scfa, self.stream
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+               for _ in range(K)] if kernel_events else None
+        if kev is not None:  # torch creates the CUDA event on first record; the library re-records it
+            for pair in kev:
+                for a, b in pair:
+                    a.record(stream)
+                    b.record(stream)
+        if self.dist is not None:
+            self.dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(K):
+            self.flush.zero_()
+            if kev is not None:
+                scfa.scfa_set_kernel_events(0, *kev[i][0])
+                scfa.scfa_set_kernel_events(1, *kev[i][1])
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if self.dist is not None:
+            self.dist.barrier()
+        t1 = time.time()
+        scfa.scfa_set_kernel_events(0)
+        scfa.scfa_set_kernel_events(1)
+        ms = [a.elapsed_time(b) for a, b in ev]
+        kms = None
+        if kev is not None:
+            kms = ([a.elapsed_time(b) for (a, b) in (x[0] for x in kev)],
+                   [a.elapsed_time(b) for (a, b) in (x[1] for x in kev)])
+        return ms, kms, t0, t1
+
+    def stages(self, step, args_, kw, scale):
+        """One step with every call on the compute stream and an event after
+        each stage (ms per stage; the hash step's two streams are serialised)."""
+        torch = self.torch
+        names, evs = [], []
+        start = torch.cuda.Event(enable_timing=True)
+
+        def mark(name):
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(self.stream)
+            names.append(name)
+            evs.append(e)
+
+        out = {}
+        for rep in range(3):
+            names.clear()
+            evs.clear()
+            self.flush.zero_()
+            start.record(self.stream)
+            step.run(*args_, scale, mark=mark, **kw)
+            torch.cuda.synchronize()
+            prev = start
+            for n, e in zip(names, evs):
+                out.setdefault(n, []).append(prev.elapsed_time(e))
+                prev = e
+        return {n: statistics.median(v) for n, v in out.items()}
+
+    def dense_ms(self, wl, K):
+        from sparse_causal_flash_gb300.pipeline import Step
+        import synth
+        key = (wl.B, wl.H, wl.T, wl.D)
+        if key not in self.dense_cache:
+            torch, dev = self.torch, self.dev
+            dstep = Step(self.scfa.MODE_DENSE, wl.B, wl.H, wl.T, wl.T, wl.D, device=dev)
+            t = [synth.normal_bf16(wl.seed, tid, (wl.B, wl.H, wl.T, wl.D)).to(dev)
+                 for tid in (synth.TID_Q, synth.TID_K, synth.TID_V, synth.TID_DO)]
+            run = lambda: dstep.run(*t, wl.scale)
+            once = wl.T >= (1 << 20)  # a dense 2^20-token causal step takes seconds: timed once
+            for _ in range(0 if once else 3):
+                run()
+            n = 1 if once else K
+            dms, _, _, _ = self.timed(run, n)
+            self.dense_cache[key] = (sum(dms) / n, n)
+            del dstep, t
+            torch.cuda.empty_cache()
+        return self.dense_cache[key]
+
+    def measure(self, wl, steps, detail=True, e2e_steps=0):
+        """Everything about one workload; returns (record, step objects kept for e2e)."""
+        import synth
+        from sparse_causal_flash_gb300.pipeline import Step
+        scfa, torch, dev = self.scfa, self.torch, self.dev
+        prob = synth.make_problem(wl)
+        mode = {"dense": scfa.MODE_DENSE, "qk": scfa.MODE_QK, "hash": scfa.MODE_HASH}[wl.mode]
+        B, H, Tq, D = prob.q.shape
+        Tk = prob.k.shape[2]
+        step = Step(mode, B, H, Tq, Tk, D, n_buckets=wl.n_buckets, device=dev)
+        args_ = [t.to(dev) for t in (prob.q, prob.k, prob.v, prob.do)]
+        kw = dict(q_idx=prob.q_idx.to(dev) if prob.q_idx is not None else None,
+                  k_idx=prob.k_idx.to(dev) if prob.k_idx is not None else None,
+                  R=prob.R.to(dev) if prob.R is not None else None)
+        run = lambda: step.run(*args_, wl.scale, **kw)
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        assert scfa.scfa_get_device_status(step.ws_b) == 0, f"{wl.name}: device status not ok after warm-up"
+        pairs = admissible_pairs(scfa, wl, prob, step, dev)
+        useful = 14.0 * D * pairs
+        ms, kms, t0, t1 = self.timed(run, steps, kernel_events=True)
+        assert scfa.scfa_get_device_status(step.ws_b) == 0, f"{wl.name}: device status not ok after the timed steps"
+        fwd_ms, bwd_ms = statistics.mean(kms[0]), statistics.mean(kms[1])
+        long_region = (t1 - t0) > 1.0
+        peak = self.peak_sus if long_region else self.peak_burst
+        if bwd_ms >= fwd_ms:
+            dom = "attn_bwd_kernel" if D == 64 else "attn_bwd128_kernel"
+            dom_ms, dom_flops = bwd_ms, 10.0 * D * pairs
+        else:
+            dom = "attn_fwd1_kernel" if D == 64 else "attn_fwd_kernel"
+            dom_ms, dom_flops = fwd_ms, 4.0 * D * pairs
+        achieved = dom_flops / (dom_ms / 1e3) / 1e12
+        rec = {"workload": wl.name, "mode": wl.mode, "B": B, "H": H, "T": wl.T, "Tq": Tq, "Tk": Tk, "D": D,
+               "admissible_pairs": pairs, "useful_flop_per_step": useful, "steps": steps,
+               "ms_per_step": sum(ms) / steps, "ms_per_step_median": statistics.median(ms),
+               "useful_tflops": useful / (sum(ms) / steps / 1e3) / 1e12,
+               "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                            "frac": achieved / peak, "kernel_ms": dom_ms,
+                            "peak_source": f"{self.peak_kind} bf16 {'sustained' if long_region else 'burst'}",
+                            "fwd_kernel_ms": fwd_ms, "bwd_kernel_ms": bwd_ms,
+                            "fwd_kernel_tflops": 4.0 * D * pairs / (fwd_ms / 1e3) / 1e12,
+                            "bwd_kernel_tflops": 10.0 * D * pairs / (bwd_ms / 1e3) / 1e12},
+               "timed_region_s": t1 - t0, "_t0": t0, "_t1": t1}
+        rec["pct_of_bf16_peak"] = 100.0 * rec["useful_tflops"] / peak
+        if wl.mode == "qk":
+            rec["p_keep"] = wl.p_keep
+        if wl.mode == "hash":
+            rec["n_buckets"] = wl.n_buckets
+        if detail:
+            st = self.stages(step, args_, kw, wl.scale)
+            st["fwd_kernel"] = fwd_ms
+            st["tiles_in_fwd_call"] = max(st["fwd"] - fwd_ms, 0.0)
+            st["bwd_kernel"] = bwd_ms
+            st["bwd_pre_and_dq_finalise"] = max(st["bwd"] - bwd_ms, 0.0)
+            rec["stages_ms"] = st
+            if wl.mode != "dense":
+                # the pages' naive baselines ("实验与结果", Fig. 3 and 7): every
+                # tile computed with the element mask (hash: the full T x T
+                # matrix then the mask; QK: the whole compacted rectangle)
+                nstep = Step(mode, B, H, Tq, Tk, D, n_buckets=wl.n_buckets, device=dev, flags=scfa.FLAG_NO_PRUNE)
+                nrun = lambda: nstep.run(*args_, wl.scale, **kw)
+                nrun()
+                nk = max(3, steps // 4)
+                nms, _, _, _ = self.timed(nrun, nk)
+                rec["naive_no_prune"] = {"ms_per_step": sum(nms) / nk, "steps": nk,
+                                         "speedup_scfa_vs_naive": (sum(nms) / nk) / rec["ms_per_step"]}
+                del nstep
+                torch.cuda.empty_cache()
+                d_ms, dn = self.dense_ms(wl, max(3, steps // 4))
+                rec["dense"] = {"ms_per_step": d_ms, "steps": dn,
+                                "useful_tflops": 14.0 * D * B * H * wl.T * (wl.T + 1) / 2 / (d_ms / 1e3) / 1e12,
+                                "speedup_sparse_vs_dense": d_ms / rec["ms_per_step"]}
+            if wl.mode == "hash":
+                # bucket-collision coverage (Fig. 4): SCFA's live tiles vs a
+                # Reformer-style chunked attention over the same sort
+                cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+                cov = {"scfa_live_tiles": 1.0}
+                for c in REFORMER_CHUNKS:
+                    scfa.scfa_count_chunked_pairs(step.pq, step.pk, step.qh, step.kh, c, cnt)
+                    cov[f"reformer_chunk{c}"] = int(cnt.item()) / pairs
+                rec["coverage"] = cov
+        keep = (step, args_, kw, prob) if e2e_steps else None
+        if not e2e_steps:
+            del step, args_, kw
+            torch.cuda.empty_cache()
+        return rec, keep
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -325,11 +542,11 @@ def main():
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_base = oracle_sample(wl, prob, args.cpu_seconds)  # before the first GPU call
+    del prob
 
     import torch
     import sparse_causal_flash_gb300 as scfa
     from sparse_causal_flash_gb300 import build as scfa_build
-    from sparse_causal_flash_gb300.pipeline import Step
     from sparse_causal_flash_gb300.replicas import job_throughput, max_over_ranks
     scfa_build.build()
     scfa.load()
@@ -340,114 +557,26 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-
-    mode = {"dense": scfa.MODE_DENSE, "qk": scfa.MODE_QK, "hash": scfa.MODE_HASH}[wl.mode]
-    B, H, Tq, D = prob.q.shape
-    Tk = prob.k.shape[2]
-    step = Step(mode, B, H, Tq, Tk, D, n_buckets=wl.n_buckets, device=dev)
-    q, k, v, do = (t.to(dev) for t in (prob.q, prob.k, prob.v, prob.do))
-    q_idx = prob.q_idx.to(dev) if prob.q_idx is not None else None
-    k_idx = prob.k_idx.to(dev) if prob.k_idx is not None else None
-    R = prob.R.to(dev) if prob.R is not None else None
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def run_once():
-        step.run(q, k, v, do, wl.scale, q_idx=q_idx, k_idx=k_idx, R=R)
-
-    for _ in range(max(args.warmup, 3)):
-        run_once()
-    torch.cuda.synchronize()
-    assert scfa.scfa_get_device_status(step.ws_b) == 0, "device status not ok after warm-up"
-    pairs = admissible_pairs(wl, prob, step)
-    useful = 14.0 * D * pairs
-
-    def timed(run, K, kernel_events=False):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
-               for _ in range(K)] if kernel_events else None
-        if kev is not None:  # torch creates the CUDA event on first record; the library re-records it
-            for pair in kev:
-                for a, b in pair:
-                    a.record(stream)
-                    b.record(stream)
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-        t0 = time.time()
-        for i in range(K):
-            flush.zero_()
-            if kev is not None:
-                scfa.scfa_set_kernel_events(0, *kev[i][0])
-                scfa.scfa_set_kernel_events(1, *kev[i][1])
-            ev[i][0].record(stream)
-            run()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        t1 = time.time()
-        scfa.scfa_set_kernel_events(0)
-        scfa.scfa_set_kernel_events(1)
-        ms = [a.elapsed_time(b) for a, b in ev]
-        kms = None
-        if kev is not None:
-            kms = ([a.elapsed_time(b) for (a, b) in (x[0] for x in kev)],
-                   [a.elapsed_time(b) for (a, b) in (x[1] for x in kev)])
-        return ms, kms, t0, t1
+    R = Runner(scfa, torch, dev, stream, dist, load_peaks())
 
     sampler = ClockSampler(local) if rank == 0 else None
-    ms, kms, t0, t1 = timed(run_once, args.steps, kernel_events=True)
-    clocks = sampler.stop(t0, t1) if sampler else None
-    assert scfa.scfa_get_device_status(step.ws_b) == 0, "device status not ok after the timed steps"
-    total_ms = max_over_ranks(sum(ms), dev)
+    rec, keep = R.measure(wl, args.steps, detail=not args.no_dense, e2e_steps=0 if args.no_e2e else 1)
+    clocks = sampler.stop(rec.pop("_t0"), rec.pop("_t1")) if sampler else None
+    total_ms = max_over_ranks(rec["ms_per_step"] * args.steps, dev)
     ms_per_step = total_ms / args.steps
+    useful = rec["useful_flop_per_step"]
     value = job_throughput(useful, args.steps, total_ms, world) / 1e12
-
-    # the attention kernels timed alone (events recorded by the library around each launch)
-    fwd_ms = statistics.mean(kms[0])
-    bwd_ms = statistics.mean(kms[1])
-    peak_burst, peak_sus, peak_kind = load_peaks()
-    long_region = (t1 - t0) > 1.0
-    peak = peak_sus if long_region else peak_burst
-    if bwd_ms >= fwd_ms:
-        # D = 128 runs the full-D key-tile kernel
-        dom = "attn_bwd_kernel" if D == 64 else "attn_bwd128_kernel"
-        dom_ms, dom_flops, src = bwd_ms, 10.0 * D * pairs, "attn_bwd.cu"
-    else:
-        # D = 64 runs the single-query-tile kernel, D = 128 the query-tile-pair kernel
-        dom = "attn_fwd1_kernel" if D == 64 else "attn_fwd_kernel"
-        dom_ms, dom_flops, src = fwd_ms, 4.0 * D * pairs, "attn_fwd.cu"
-    achieved = dom_flops / (dom_ms / 1e3) / 1e12
-    tr = load_traffic(dom)
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None if tr is None else tr["bytes_per_launch"],
-                "peak_source": f"{peak_kind} bf16 {'sustained' if long_region else 'burst'}",
-                "kernel_ms": dom_ms, "fwd_kernel_ms": fwd_ms, "bwd_kernel_ms": bwd_ms,
-                "fwd_kernel_tflops": 4.0 * D * pairs / (fwd_ms / 1e3) / 1e12,
-                "bwd_kernel_tflops": 10.0 * D * pairs / (bwd_ms / 1e3) / 1e12}
-
-    dense = None
-    if not args.no_dense and wl.mode != "dense":
-        dstep = Step(scfa.MODE_DENSE, wl.B, wl.H, wl.T, wl.T, D, device=dev)
-        dq_ = synth.normal_bf16(wl.seed, synth.TID_Q, (wl.B, wl.H, wl.T, D)).to(dev)
-        dk_ = synth.normal_bf16(wl.seed, synth.TID_K, (wl.B, wl.H, wl.T, D)).to(dev)
-        dv_ = synth.normal_bf16(wl.seed, synth.TID_V, (wl.B, wl.H, wl.T, D)).to(dev)
-        ddo = synth.normal_bf16(wl.seed, synth.TID_DO, (wl.B, wl.H, wl.T, D)).to(dev)
-        run_dense = lambda: dstep.run(dq_, dk_, dv_, ddo, wl.scale)
-        once = wl.T >= (1 << 20)  # a dense 2^20-token causal step takes seconds: timed once
-        for _ in range(0 if once else 3):
-            run_dense()
-        dK = 1 if once else max(5, args.steps // 4)
-        dms, _, _, _ = timed(run_dense, dK)
-        d_ms = sum(dms) / dK
-        d_useful = 14.0 * D * wl.B * wl.H * wl.T * (wl.T + 1) / 2
-        dense = {"ms_per_step": d_ms, "useful_tflops": d_useful / (d_ms / 1e3) / 1e12, "steps": dK,
-                 "speedup_sparse_vs_dense": d_ms / ms_per_step}
-        del dstep, dq_, dk_, dv_, ddo
+    roofline = dict(rec["roofline"])
+    tr = load_traffic(roofline["kernel"])
+    roofline["traffic"] = None if tr is None else tr["bytes_per_launch"]
 
     e2e = None
-    if not args.no_e2e:
+    if keep is not None:
         from sparse_causal_flash_gb300.pipeline import HostPipeline
+        step, _, _, prob = keep
+        B, H, Tq, D = prob.q.shape
+        Tk = prob.k.shape[2]
+        mode = {"dense": scfa.MODE_DENSE, "qk": scfa.MODE_QK, "hash": scfa.MODE_HASH}[wl.mode]
         pin = lambda t: t.contiguous().pin_memory() if t is not None else None
         hin = {"q": pin(prob.q), "k": pin(prob.k), "v": pin(prob.v), "do": pin(prob.do),
                "q_idx": pin(prob.q_idx), "k_idx": pin(prob.k_idx), "R": pin(prob.R)}
@@ -455,9 +584,10 @@ def main():
         houts = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
         h2d = sum(t.numel() * t.element_size() for t in hin.values() if t is not None)
         d2h = sum(t.numel() * t.element_size() for t in houts)
+        del keep, step
+        torch.cuda.empty_cache()
         pipe = HostPipeline(mode, B, H, Tq, Tk, D, n_buckets=wl.n_buckets, device=dev)
-        flush_before = lambda s: flush.zero_()
-
+        flush_before = lambda s: R.flush.zero_()
         for _ in range(3):
             pipe.submit(hin, houts, wl.scale, stream=stream, before=flush_before)
         pipe.synchronize()
@@ -486,10 +616,20 @@ def main():
                "copies": "overlapped with the kernels of neighbouring steps (two device slots, one copy stream "
                          "each way); L2 flushed before every step inside the span"}
         del pipe
+        torch.cuda.empty_cache()
+
+    secondary = []
+    if not args.no_secondary and wl.name == DEFAULT_WORKLOAD:
+        for name in SECONDARY:
+            r2, _ = R.measure(synth.WORKLOADS[name], max(10, args.steps // 2), detail=True)
+            r2.pop("_t0", None)
+            r2.pop("_t1", None)
+            secondary.append(r2)
 
     if rank == 0:
         cfg = {"workload": wl.name, "mode": wl.mode, "B": wl.B, "H": wl.H, "T": wl.T, "D": wl.D,
-               "Tq": Tq, "Tk": Tk, "admissible_pairs": pairs, "useful_flop_per_step": useful,
+               "Tq": rec["Tq"], "Tk": rec["Tk"], "admissible_pairs": rec["admissible_pairs"],
+               "useful_flop_per_step": useful,
                "l2": "flushed before every timed step (256 MiB write), outside the step's events",
                "parallelism": f"replicas x{world}"}
         if wl.mode == "qk":
@@ -500,10 +640,11 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
-            "pct_of_bf16_peak": 100.0 * (value / world) / peak,
-            "dense": dense, "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
+            "pct_of_bf16_peak": 100.0 * (value / world) / roofline["peak"],
+            "dense": rec.get("dense"), "naive_no_prune": rec.get("naive_no_prune"), "stages_ms": rec.get("stages_ms"),
+            "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
             "gpu_launches": kernels_per_step(wl.mode, wl.D, wl.T, getattr(wl, "n_buckets", 0)) * args.steps,
-            "clocks": clocks,
+            "clocks": clocks, "secondary": secondary,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -59,39 +59,53 @@ class Step:
             self.v_s = torch.empty((B, H, T, D), **bf)
             self.do_s = torch.empty((B, H, T, D), **bf)
 
-    def run(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None, stream=None):
-        """Forward + backward. Results land in self.o/lse/dq/dk/dv."""
+    def run(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None, stream=None, mark=None):
+        """Forward + backward. Results land in self.o/lse/dq/dk/dv.
+
+        mark(name): if given, every call runs on the one stream and mark is
+        called after each named stage (for per-stage timing)."""
         # the forward keeps O in fp32 in the shared workspace for the
         # backward's rowsum(dO * O); the backward reuses the live-tile list
         f = self.flags | FLAG_KEEP_O32
         fr = f | FLAG_REUSE_TILES
+        tick = mark if mark is not None else (lambda name: None)
         if self.mode == MODE_DENSE:
             scfa_dense_fwd(q, k, v, scale, self.o, self.lse, self.ws_f, f, stream)
+            tick("fwd")
             scfa_dense_bwd(q, k, v, self.o, self.lse, do, scale, self.dq, self.dk, self.dv, self.ws_b, fr, stream)
+            tick("bwd")
         elif self.mode == MODE_QK:
             scfa_qk_fwd(q, k, v, q_idx, k_idx, scale, self.o, self.lse, self.ws_f, f, stream)
+            tick("fwd")
             scfa_qk_bwd(q, k, v, self.o, self.lse, do, q_idx, k_idx, scale, self.dq, self.dk, self.dv, self.ws_b,
                         fr, stream)
+            tick("bwd")
         else:
             nb = self.nb
             main = stream if stream is not None else torch.cuda.current_stream()
-            side = self.side
             # key side (hash, sort, K and V gathers) on the second stream
+            side = self.side if mark is None else main
             self.ev[0].record(main)
             side.wait_event(self.ev[0])
             lsh_bucket_sort(k, R, nb, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
+            tick("hash_sort_gather_k")
             lsh_gather(v, self.pk, self.v_s, side)
+            tick("gather_v")
             self.ev[1].record(side)
             lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
+            tick("hash_sort_gather_q")
             lsh_gather(do, self.pq, self.do_s, main)
+            tick("gather_do")
             main.wait_event(self.ev[1])
             # O, dQ, dK, dV go straight to original row order (pq / pk map
             # sorted rows to original ones); LSE stays in sorted order
             fo = f | FLAG_ORIGINAL_ORDER
             scfa_hash_fwd(self.q_s, self.k_s, self.v_s, self.pq, self.pk, self.qh, self.kh, scale, self.o,
                           self.lse, self.ws_f, fo, main)
+            tick("fwd")
             scfa_hash_bwd(self.q_s, self.k_s, self.v_s, self.o, self.lse, self.do_s, self.pq, self.pk, self.qh,
                           self.kh, scale, self.dq, self.dk, self.dv, self.ws_b, fr | FLAG_ORIGINAL_ORDER, main)
+            tick("bwd")
         return self
 
 
