@@ -288,26 +288,26 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int t = 0; t < n; ++t) {
           const int s = q_it % kQStages;
           const int db = it & 1;
-          // Issue A(t+1) as soon as its inputs are ready, but never let B(t)
-          // wait behind it: poll both until B(t) can go.
+          // A(t+1) before B(t) when it can go early: the compute warps free
+          // the S^T / dP^T columns (st_empty) early in their step, long
+          // before dS^T(t) is ready (ds_full), so wait for that first (the
+          // thread sleeps in the barrier), and issue A(t+1) if its Q / dO have
+          // landed; if they have not, B(t) goes first and A(t+1) after it.
           bool a_next = (t + 1 >= n);
-          {
-            WaitClock wc;
-            const int s1 = (q_it + 1) % kQStages;
-            for (;;) {
-              if (!a_next && mbar_test(&sm.q_full[s1], ((q_it + 1) / kQStages) & 1) &&
-                  mbar_test(&sm.st_empty, ((it + 1) & 1) ^ 1)) {
-                if (!issue_a(q_it + 1, it + 1)) { ok = false; break; }
-                a_next = true;
-              }
-              if (mbar_test(&sm.ds_full, it & 1) &&
-                  (t > 0 || mbar_test(&sm.dkv_empty, (item & 1) ^ 1)) &&
-                  mbar_test(&sm.dq_empty, (it & 1) ^ 1))
-                break;
-              if (!wc.tick(abort_flag, p.status)) { ok = false; break; }
-              __nanosleep(32);  // leave issue slots to the compute warps sharing this SMSP
+          if (!a_next) {
+            if (!mbar_wait(&sm.st_empty, ((it + 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+            if (mbar_test(&sm.q_full[(q_it + 1) % kQStages], ((q_it + 1) / kQStages) & 1)) {
+              if (!issue_a(q_it + 1, it + 1)) { ok = false; break; }
+              a_next = true;
             }
-            if (!ok) break;
+          }
+          // B(t): dS^T(t) written, dK / dV accumulators free at an item's
+          // first tile, the previous dQ read out of TMEM
+          if (!mbar_wait(&sm.ds_full, it & 1, abort_flag, p.status) ||
+              (t == 0 && !mbar_wait(&sm.dkv_empty, (item & 1) ^ 1, abort_flag, p.status)) ||
+              !mbar_wait(&sm.dq_empty, (it & 1) ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
           }
           tc_fence_after();
           const uint64_t half16 = static_cast<uint64_t>(hh * (kSubBytes >> 4));

@@ -185,25 +185,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
-// Deadline helper for polling loops that test several barriers: returns false
-// (after raising the status word and the abort flag) once the limit passes.
-struct WaitClock {
-  uint64_t t0 = 0;
-  uint32_t it = 0;
-  __device__ __forceinline__ bool tick(volatile int* abort_flag, int* status) {
-    if (((++it) & 63u) != 0) return true;
-    if (*abort_flag) return false;
-    const uint64_t now = global_timer_ns();
-    if (t0 == 0) t0 = now;
-    if (now - t0 > kWaitLimitNs) {
-      raise_status(status, SCFA_ERR_TIMEOUT);
-      *abort_flag = 1;
-      return false;
-    }
-    return true;
-  }
-};
-
 // ---------------------------------------------------------------------------
 // TMA (tensor copies, global -> shared), completion counted on an mbarrier
 // ---------------------------------------------------------------------------
