@@ -68,6 +68,14 @@ enum { SCFA_MODE_DENSE = 0, SCFA_MODE_QK = 1, SCFA_MODE_HASH = 2 };
 /* flags */
 enum {
   SCFA_FLAG_NO_PRUNE = 1,    /* treat every tile as live (results unchanged) */
+  SCFA_FLAG_VALIDATE = 2,    /* check the index contracts on the device first and
+                                raise SCFA_ERR_INVALID in the status word on a
+                                violation (the call still runs; its results are
+                                then undefined): QK: per head the kept positions
+                                strictly ascending, sentinels only after them;
+                                hash: q_hash / k_hash non-decreasing and >= 0,
+                                and with SCFA_FLAG_ORIGINAL_ORDER no index in
+                                [0, T) twice. */
   SCFA_FLAG_DEBUG_SYNC = 4,  /* synchronise the stream after every launch */
   SCFA_FLAG_REUSE_TILES = 8,  /* the workspace already holds the live-tile list
                                  of these exact indices and shape (built by
@@ -85,7 +93,7 @@ enum {
                                  [0, T) are not written, and read as zero).
                                  q, k, v, do, lse stay in sorted order. This
                                  replaces the lsh_unsort passes. */
-  SCFA_FLAG_KEEP_O32 = 32        /* forward: also store O in fp32 in the
+  SCFA_FLAG_KEEP_O32 = 32,       /* forward: also store O in fp32 in the
                                  workspace, which must then be sized for the
                                  backward (scfa_attn_workspace_size(mode, 1,
                                  ...)); backward: take rowsum(dO * O) from that
@@ -93,6 +101,15 @@ enum {
                                  forward and the backward of one step on the
                                  same workspace. The bf16 rounding of O is
                                  otherwise the largest error term of dS. */
+  SCFA_FLAG_DEBUG_STALL = 64     /* debug: the main attention kernel of the call
+                                 withholds the first K / V load of every CTA,
+                                 so its pipeline waits on a barrier that
+                                 nothing completes; each wait gives up after
+                                 its limit (1 s), the status word reads
+                                 SCFA_ERR_TIMEOUT and the results are invalid.
+                                 For testing the timeout path: the CTAs drain
+                                 their issued copies and MMAs and exit, and the
+                                 device stays usable. */
 };
 
 /* Tiles are SCFA_TILE rows of queries by SCFA_TILE rows of keys. */

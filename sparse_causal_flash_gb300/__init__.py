@@ -20,7 +20,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libscfa.so")
 
 MODE_DENSE, MODE_QK, MODE_HASH = 0, 1, 2
-FLAG_NO_PRUNE, FLAG_DEBUG_SYNC, FLAG_REUSE_TILES, FLAG_ORIGINAL_ORDER, FLAG_KEEP_O32 = 1, 4, 8, 16, 32
+FLAG_NO_PRUNE, FLAG_VALIDATE, FLAG_DEBUG_SYNC, FLAG_REUSE_TILES, FLAG_ORIGINAL_ORDER = 1, 2, 4, 8, 16
+FLAG_KEEP_O32, FLAG_DEBUG_STALL = 32, 64
 TILE = 128
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "CUDA error", 5: "device timeout"}
 

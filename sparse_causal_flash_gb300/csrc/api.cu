@@ -102,6 +102,8 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
   w.pcount = take(sizeof(int32_t) * w.n_pairs);
   w.ulist = take(sizeof(int32_t) * w.max_live);
   w.work_pairs = take(sizeof(int32_t) * w.n_pairs);
+  w.vbits_bytes = sizeof(uint32_t) * static_cast<size_t>(BH) * ((Tq + 31) / 32 + (Tk + 31) / 32);
+  w.vbits = take(w.vbits_bytes);
   if (backward) {
     w.dq_acc = take(sizeof(float) * static_cast<size_t>(BH) * Tq * D);
     w.qmeta = take(4 * sizeof(float) * static_cast<size_t>(BH) * w.nQt * kTile);
@@ -187,7 +189,13 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   char* w = static_cast<char*>(ws);
   cudaError_t e = cudaSuccess;
   if (!(flags & SCFA_FLAG_REUSE_TILES)) {
+    // (clears the status word first)
     e = launch_tiles(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, flags, w, L, st, D == 128);
+    if (e != cudaSuccess) return SCFA_ERR_CUDA;
+  }
+  if (flags & SCFA_FLAG_VALIDATE) {
+    e = launch_validate(mode, (flags & SCFA_FLAG_ORIGINAL_ORDER) != 0, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, w,
+                        L, st);
     if (e != cudaSuccess) return SCFA_ERR_CUDA;
   }
   AttnArgs a;
@@ -217,6 +225,7 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   a.q_rows = original ? q_idx : nullptr;
   a.k_rows = original ? k_idx : nullptr;
   a.o32 = keep_o32 ? reinterpret_cast<float*>(w + L.dq_acc) : nullptr;
+  a.stall = (flags & SCFA_FLAG_DEBUG_STALL) ? 1 : 0;
   a.ws = w;
   a.L = &L;
   e = backward ? launch_attn_bwd(a, st) : launch_attn_fwd(a, st);

@@ -102,6 +102,7 @@ struct BwdParams {
   uint16_t* dk;
   uint16_t* dv;
   const int32_t* k_rows;  // null, or the original row of each sorted key row
+  int stall;   // SCFA_FLAG_DEBUG_STALL: withhold the first K / V load
   int* sched;  // [0] next work item, [1] CTAs done
   int* status;
 };
@@ -191,7 +192,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (n == 0) continue;
       const int bh = g / p.nKt, j = g % p.nKt;
       bool ok = true;
-      if (lane == 0) {
+      const bool stall = p.stall && item == 0;  // debug stall: K / V never arrive
+      if (lane == 0 && !stall) {
         ok = mbar_wait(&sm.kv_empty, (item & 1) ^ 1, abort_flag, p.status);
         if (ok) {
           mbar_arrive_expect_tx(&sm.kv_full, 2 * D * kTile * 2);
@@ -203,7 +205,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      for (int t = 0; t < n; ++t) {
+      for (int t = 0; t < (stall ? min(n, kQStages) : n); ++t) {
         const int i = p.csc_rows[start + t];
         const int s = q_it % kQStages;
         if (lane == 0) {
@@ -226,15 +228,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
         ++q_it;
       }
-      if (!ok) break;
+      if (!ok || stall) break;
       ++item;
     }
     if (lane == 0) {
+      // every copy issued by this thread lands before the CTA exits, also
+      // after an abort (q_it counts the stages actually loaded)
       for (int d = 1; d <= kQStages && d <= q_it; ++d) {
         const int it = q_it - d;
-        mbar_wait(&sm.q_full[it % kQStages], (it / kQStages) & 1, abort_flag, p.status);
+        mbar_wait_drain(&sm.q_full[it % kQStages], (it / kQStages) & 1, p.status);
       }
-      if (last_kv >= 0) mbar_wait(&sm.kv_full, last_kv & 1, abort_flag, p.status);
+      if (last_kv >= 0) mbar_wait_drain(&sm.kv_full, last_kv & 1, p.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -346,7 +350,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ++item;
       }
       tc_commit(&sm.drain);
-      mbar_wait(&sm.drain, 0, abort_flag, p.status);
+      mbar_wait_drain(&sm.drain, 0, p.status);
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------ P^T / dS^T warpgroups
@@ -664,6 +668,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   if (warp == 0) {
     // ------------------------------------------------------------ producer warp
     int qt = 0, item = 0, last_kv = -1;
+    int q_issued = 0, do_issued = 0;  // loads issued, for the drain
     for (int slot_it = 0;; ++slot_it) {
       int w = INT_MAX;
       if (lane == 0) {
@@ -681,7 +686,8 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (n == 0) continue;
       const int bh = g / p.nKt, j = g % p.nKt;
       bool ok = true;
-      if (lane == 0) {
+      const bool stall = p.stall && item == 0;  // debug stall: K / V never arrive
+      if (lane == 0 && !stall) {
         ok = mbar_wait(&sm.kv_empty, (item & 1) ^ 1, abort_flag, p.status);
         if (ok) {
           mbar_arrive_expect_tx(&sm.kv_full, 2 * D * kTile * 2);
@@ -693,7 +699,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      for (int t = 0; t < n; ++t) {
+      for (int t = 0; t < (stall ? 1 : n); ++t) {
         const int i = p.csc_rows[start + t];
         const int mb = qt & 1, s = qt & 1;
         if (lane == 0) {
@@ -705,6 +711,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_arrive_expect_tx(&sm.q_full[s], D * kTile * 2);
             for (int sub = 0; sub < 2; ++sub)
               tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
+            q_issued = qt + 1;
             ok = mbar_wait(&sm.do_empty, (qt & 1) ^ 1, abort_flag, p.status);
           }
           if (ok) {
@@ -715,22 +722,24 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             bulk_load(sm.drs[mb], m + p.qm_n, kTile * 4, &sm.do_full);
             bulk_load(sm.qidx[mb], m + 2 * p.qm_n, kTile * 4, &sm.do_full);
             bulk_load(sm.qhash[mb], m + 3 * p.qm_n, kTile * 4, &sm.do_full);
+            do_issued = qt + 1;
           }
         }
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
         ++qt;
       }
-      if (!ok) break;
+      if (!ok || stall) break;
       ++item;
     }
     if (lane == 0) {
-      // no load may still be in flight when the CTA exits
-      if (qt > 0) {
-        mbar_wait(&sm.do_full, (qt - 1) & 1, abort_flag, p.status);
-        mbar_wait(&sm.q_full[(qt - 1) & 1], ((qt - 1) >> 1) & 1, abort_flag, p.status);
+      // no load may still be in flight when the CTA exits, also after an
+      // abort (the counts are of loads actually issued)
+      if (do_issued > 0) mbar_wait_drain(&sm.do_full, (do_issued - 1) & 1, p.status);
+      for (int d = 1; d <= 2 && d <= q_issued; ++d) {
+        const int it = q_issued - d;
+        mbar_wait_drain(&sm.q_full[it & 1], (it >> 1) & 1, p.status);
       }
-      if (qt > 1) mbar_wait(&sm.q_full[(qt - 2) & 1], ((qt - 2) >> 1) & 1, abort_flag, p.status);
-      if (last_kv >= 0) mbar_wait(&sm.kv_full, last_kv & 1, abort_flag, p.status);
+      if (last_kv >= 0) mbar_wait_drain(&sm.kv_full, last_kv & 1, p.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -812,7 +821,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         ++item;
       }
       tc_commit(&sm.drain);
-      mbar_wait(&sm.drain, 0, abort_flag, p.status);
+      mbar_wait_drain(&sm.drain, 0, p.status);
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------ P^T / dS^T warpgroups
@@ -1227,6 +1236,7 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   p.dk = a.dk;
   p.dv = a.dv;
   p.k_rows = a.k_rows;
+  p.stall = a.stall;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched + 2;
   int grid = sms;

@@ -117,6 +117,7 @@ struct FwdParams {
   const int32_t* o_rows;  // null, or the original row of each sorted query row
   float* lse;
   float* o32;             // null, or an fp32 copy of O [B,H,Tq,D] in row order of q
+  int stall;              // SCFA_FLAG_DEBUG_STALL: withhold the first K / V load
   int* status;
 };
 
@@ -181,8 +182,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         last_q = item;
         const int32_t* ul = p.ulist + p.row_ptr[g0];
-        bool ok = true;
-        for (int t = 0; t < cnt; ++t) {
+        bool ok = !(p.stall && kv_it == 0);  // debug stall: no K / V load ever arrives
+        for (int t = 0; t < cnt && ok; ++t) {
           const int j = ul[t] >> 4;
           const int s = kv_it % kStages;
           const uint32_t ph = (kv_it / kStages) & 1;
@@ -196,15 +197,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!ok) break;
         ++item;
       }
-      // drain: every copy issued by this thread has landed before the CTA exits
+      // drain: every copy issued by this thread has landed before the CTA
+      // exits, also after an abort (K and V of one stage are issued together)
       for (int d = 1; d <= kStages && d <= kv_it; ++d) {
         const int it = kv_it - d;
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        mbar_wait(&sm.k_full[s], ph, abort_flag, p.status);
-        mbar_wait(&sm.v_full[s], ph, abort_flag, p.status);
+        mbar_wait_drain(&sm.k_full[s], ph, p.status);
+        mbar_wait_drain(&sm.v_full[s], ph, p.status);
       }
-      if (last_q >= 0) mbar_wait(&sm.q_full, last_q & 1, abort_flag, p.status);
+      if (last_q >= 0) mbar_wait_drain(&sm.q_full, last_q & 1, p.status);
     }
   } else if (warp == 1 || warp == 10) {
     // ------------------------------------------------------------ MMA issuers
@@ -304,7 +306,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       // drain: all MMAs issued by this thread are complete before TMEM is freed
       tc_commit(&sm.drain[g]);
-      mbar_wait(&sm.drain[g], 0, abort_flag, p.status);
+      mbar_wait_drain(&sm.drain[g], 0, p.status);
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
@@ -640,6 +642,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       // first) as this CTA gets through its previous ones, and handed to the
       // MMA and softmax roles through a small slot ring; -1 ends the walk.
       int item = 0, kv = 0, slot_it = 0;
+      int k_issued = 0, v_issued = 0, q_issued = 0;  // loads issued, for the drain
       for (;;) {
         const int slot = slot_it % kF1Slots;
         if (!mbar_wait(&sm.item_empty[slot], ((slot_it / kF1Slots) & 1) ^ 1, abort_flag, p.status)) break;
@@ -656,31 +659,38 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (!mbar_wait(&sm.q_empty[qb], ((item >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&sm.q_full[qb], D * kTile * 2);
         tma_load_3d(sm.q[qb], &tm_q, &sm.q_full[qb], 0, i * kTile, bh);
-        bool ok = true;
-        for (int t = 0; t < n; ++t) {
+        q_issued = item + 1;
+        bool ok = !(p.stall && kv == 0);  // debug stall: no K / V load ever arrives
+        for (int t = 0; t < n && ok; ++t) {
           const int j = p.cols[e0 + t];
           const int s = kv % kF1Stages;
           const uint32_t ph = ((kv / kF1Stages) & 1) ^ 1;
           if (!mbar_wait(&sm.k_empty[s], ph, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&sm.k_full[s], D * kTile * 2);
           tma_load_3d(sm.k[s], &tm_k, &sm.k_full[s], 0, j * kTile, bh);
+          k_issued = kv + 1;
           if (!mbar_wait(&sm.v_empty[s], ph, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&sm.v_full[s], D * kTile * 2);
           tma_load_3d(sm.v[s], &tm_v, &sm.v_full[s], 0, j * kTile, bh);
+          v_issued = kv + 1;
           ++kv;
         }
         if (!ok) break;
         ++item;
       }
-      // drain: every copy issued by this thread has landed before the CTA exits
-      for (int d = 1; d <= kF1Stages && d <= kv; ++d) {
-        const int it = kv - d;
-        mbar_wait(&sm.k_full[it % kF1Stages], (it / kF1Stages) & 1, abort_flag, p.status);
-        mbar_wait(&sm.v_full[it % kF1Stages], (it / kF1Stages) & 1, abort_flag, p.status);
+      // drain: every copy issued by this thread has landed before the CTA
+      // exits, also after an abort (the counts are of loads actually issued)
+      for (int d = 1; d <= kF1Stages && d <= k_issued; ++d) {
+        const int it = k_issued - d;
+        mbar_wait_drain(&sm.k_full[it % kF1Stages], (it / kF1Stages) & 1, p.status);
       }
-      for (int d = 1; d <= 2 && d <= item; ++d) {
-        const int it = item - d;
-        mbar_wait(&sm.q_full[it & 1], (it >> 1) & 1, abort_flag, p.status);
+      for (int d = 1; d <= kF1Stages && d <= v_issued; ++d) {
+        const int it = v_issued - d;
+        mbar_wait_drain(&sm.v_full[it % kF1Stages], (it / kF1Stages) & 1, p.status);
+      }
+      for (int d = 1; d <= 2 && d <= q_issued; ++d) {
+        const int it = q_issued - d;
+        mbar_wait_drain(&sm.q_full[it & 1], (it >> 1) & 1, p.status);
       }
     }
   } else if (warp == 1) {
@@ -753,7 +763,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         ++item;
       }
       tc_commit(&sm.drain);
-      mbar_wait(&sm.drain, 0, abort_flag, p.status);
+      mbar_wait_drain(&sm.drain, 0, p.status);
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroup
@@ -1040,6 +1050,7 @@ static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   p.o_rows = a.q_rows;
   p.lse = a.lse_out;
   p.o32 = a.o32;
+  p.stall = a.stall;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1083,6 +1094,7 @@ static cudaError_t launch_fwd1(const AttnArgs& a, cudaStream_t st) {
   p.o_rows = a.q_rows;
   p.lse = a.lse_out;
   p.o32 = a.o32;
+  p.stall = a.stall;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   const size_t smem = sizeof(Fwd1Smem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -185,6 +185,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Wait used when a role leaves: for copies and MMAs this thread has already
+// issued, which complete on their own. It ignores the abort flag (so a CTA
+// that is aborting still lets its in-flight TMA loads land and its MMAs
+// finish before it releases shared memory and TMEM) and is bounded by the
+// same limit.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      raise_status(status, SCFA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tensor copies, global -> shared), completion counted on an mbarrier
 // ---------------------------------------------------------------------------

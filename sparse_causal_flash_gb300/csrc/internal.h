@@ -35,6 +35,7 @@ struct AttnWs {
                                          // 4 live for 2m + 1, 8 FULL for 2m + 1), key tiles ascending
   size_t work_pairs = 0;                 // pair ids by union size descending
   size_t dq_acc = 0;                     // backward: fp32 dQ accumulator [B,H,Tq,D]
+  size_t vbits = 0, vbits_bytes = 0;     // SCFA_FLAG_VALIDATE: one bit per row of q and of k
   size_t qmeta = 0;                      // backward: per-query metadata padded to whole tiles, four
                                          // [B*H][nQt*128] arrays: -LSE*log2(e) and -rowsum(dO*O)*scale
                                          // (fp32), position and bucket id (int32)
@@ -62,6 +63,11 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
                          const int32_t* q_hash, const int32_t* k_hash,
                          int B, int H, int Tq, int Tk, unsigned flags,
                          char* ws, const AttnWs& L, cudaStream_t st, bool with_pairs = true);
+
+// SCFA_FLAG_VALIDATE: contract checks of the index inputs into the status word
+cudaError_t launch_validate(int mode, bool original, const int32_t* q_idx, const int32_t* k_idx,
+                            const int32_t* q_hash, const int32_t* k_hash, int B, int H, int Tq, int Tk,
+                            char* ws, const AttnWs& L, cudaStream_t st);
 
 // lsh.cu
 // status: a device int the tensor-core path may raise a timeout in (NULL keeps
@@ -95,6 +101,7 @@ struct AttnArgs {
   // SCFA_FLAG_KEEP_O32: the fp32 copy of O in the workspace (the forward
   // writes it, the backward pre-pass reads it); null otherwise
   float* o32;
+  int stall;  // SCFA_FLAG_DEBUG_STALL
   char* ws;
   const AttnWs* L;
 };

@@ -633,7 +633,7 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
       }
       for (int d = 1; d <= kTcStages && d <= it; ++d) {
         const int i2 = it - d;
-        mbar_wait(&sm.x_full[i2 % kTcStages], (i2 / kTcStages) & 1, abort_flag, status);
+        mbar_wait_drain(&sm.x_full[i2 % kTcStages], (i2 / kTcStages) & 1, status);
       }
     }
   } else if (warp == 1) {
@@ -657,7 +657,7 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
         tc_commit(&sm.x_empty[s]);
       }
       tc_commit(&sm.drain);
-      mbar_wait(&sm.drain, 0, abort_flag, status);
+      mbar_wait_drain(&sm.drain, 0, status);
     }
   } else {
     // ------------------------------------------------------------ epilogue

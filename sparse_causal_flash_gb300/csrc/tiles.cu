@@ -441,6 +441,55 @@ __global__ void work_order_kernel(OrderList l0, OrderList l1, OrderList l2, int 
   }
 }
 
+// SCFA_FLAG_VALIDATE: checks the documented contracts of the index inputs and
+// raises SCFA_ERR_INVALID in the status word on the first violation (nothing
+// traps; the attention still runs and its results are then undefined).
+//   QK: per head, the kept positions (q_idx >= 0, k_idx < INT32_MAX) strictly
+//       ascending, padding sentinels (-1 / INT32_MAX) only after them.
+//   hash: per head, q_hash and k_hash non-decreasing and >= 0; with
+//       `original` (SCFA_FLAG_ORIGINAL_ORDER) no index in [0, T) twice
+//       (two rows would write the same output row), checked with one bit per
+//       row in `bits` (zeroed by the caller).
+__global__ void validate_kernel(int mode, int original, const int32_t* __restrict__ q_idx,
+                                const int32_t* __restrict__ k_idx, const int32_t* __restrict__ q_hash,
+                                const int32_t* __restrict__ k_hash, long long BH, int Tq, int Tk,
+                                uint32_t* __restrict__ bits, int* status) {
+  const long long nq = BH * Tq, n = nq + BH * Tk;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n; t += stride) {
+    const bool is_q = t < nq;
+    const long long u = is_q ? t : t - nq;
+    const int T = is_q ? Tq : Tk;
+    const long long bh = u / T;
+    const int r = static_cast<int>(u - bh * T);
+    const int32_t* idx = (is_q ? q_idx : k_idx) + bh * T;
+    bool bad = false;
+    if (mode == SCFA_MODE_QK) {
+      const int32_t sent = is_q ? -1 : INT_MAX;
+      const int32_t v = idx[r];
+      if (v != sent && v < 0) bad = true;
+      if (r > 0) {
+        const int32_t w = idx[r - 1];
+        if (w == sent && v != sent) bad = true;         // a kept row after padding
+        if (w != sent && v != sent && w >= v) bad = true;  // not strictly ascending
+      }
+    } else if (mode == SCFA_MODE_HASH) {
+      const int32_t* h = (is_q ? q_hash : k_hash) + bh * T;
+      if (h[r] < 0 || (r > 0 && h[r - 1] > h[r])) bad = true;
+      if (original) {
+        const int32_t v = idx[r];
+        if (v >= 0 && v < T) {
+          const long long words = (static_cast<long long>(T) + 31) / 32;
+          uint32_t* b = bits + (is_q ? 0 : BH * ((static_cast<long long>(Tq) + 31) / 32)) + bh * words + v / 32;
+          const uint32_t m = 1u << (v & 31);
+          if (atomicOr(b, m) & m) bad = true;  // this index seen before in this head
+        }
+      }
+    }
+    if (bad) raise_status(status, SCFA_ERR_INVALID);
+  }
+}
+
 inline int grid_for(long long work, int block, int max_blocks) {
   long long g = (work + block - 1) / block;
   if (g < 1) g = 1;
@@ -449,6 +498,23 @@ inline int grid_for(long long work, int block, int max_blocks) {
 }
 
 }  // namespace
+
+cudaError_t launch_validate(int mode, bool original, const int32_t* q_idx, const int32_t* k_idx,
+                            const int32_t* q_hash, const int32_t* k_hash, int B, int H, int Tq, int Tk,
+                            char* ws, const AttnWs& L, cudaStream_t st) {
+  if (mode == SCFA_MODE_DENSE) return cudaSuccess;
+  const long long BH = static_cast<long long>(B) * H;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(ws + L.vbits);
+  if (original) {
+    cudaError_t e = cudaMemsetAsync(bits, 0, L.vbits_bytes, st);
+    if (e != cudaSuccess) return e;
+  }
+  const long long n = BH * (static_cast<long long>(Tq) + Tk);
+  validate_kernel<<<grid_for(n, 256, num_sms() * 8), 256, 0, st>>>(mode, original ? 1 : 0, q_idx, k_idx, q_hash,
+                                                                    k_hash, BH, Tq, Tk, bits,
+                                                                    reinterpret_cast<int*>(ws + L.header));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
                          const int32_t* q_hash, const int32_t* k_hash,
