@@ -126,6 +126,37 @@ const char* scfa_status_string(scfa_status s);
  * ------------------------------------------------------------------------- */
 size_t scfa_attn_workspace_size(int mode, int backward, int B, int H, int Tq, int Tk, int D);
 
+/* The live-tile lists of a workspace hold as many entries as fit past its
+ * fixed part; scfa_attn_workspace_size leaves room for every tile pair (the
+ * worst case), which at long T dominates (8 heads of 2^20 tokens: 7.5 GB).
+ * The layout of a workspace depends on its size alone, never on the call: a
+ * workspace that holds the backward's fixed part (the fp32 dQ accumulator
+ * and the per-row metadata) lays them out for every call, forward included,
+ * and the lists follow them; so a forward and a SCFA_FLAG_REUSE_TILES
+ * backward on one workspace always agree on where the lists are. (So a
+ * forward-only workspace grown past that fixed part holds fewer entries than
+ * one just below it; the sizes returned below never fall in that gap.)
+ * scfa_attn_workspace_size_live sizes a workspace whose lists hold n_live
+ * entries for a call of the given kind; scfa_attn_workspace_capacity returns
+ * how many entries a workspace of ws_bytes holds (-1: not even the fixed part
+ * the call needs fits). Both are host-only arithmetic. scfa_tiles_count writes
+ * the live count of a problem (an int32 on the DEVICE, asynchronously on
+ * `stream`) using a workspace of at least
+ * scfa_attn_workspace_size_live(mode, 0, ..., 0) bytes. A call whose lists
+ * need more entries than its workspace holds leaves every list empty, so no
+ * tile is computed and nothing is read or written past the lists, and raises
+ * SCFA_ERR_WORKSPACE in the status word. A call that reuses a list
+ * (SCFA_FLAG_REUSE_TILES) finds it where the building call recorded it in
+ * the workspace header. */
+size_t scfa_attn_workspace_size_live(int mode, int backward, int B, int H, int Tq, int Tk, int D,
+                                     long long n_live);
+long long scfa_attn_workspace_capacity(int mode, int backward, int B, int H, int Tq, int Tk, int D,
+                                       size_t ws_bytes);
+scfa_status scfa_tiles_count(int mode, const int32_t* q_idx, const int32_t* k_idx,
+                             const int32_t* q_hash, const int32_t* k_hash,
+                             int B, int H, int Tq, int Tk, void* ws, size_t ws_bytes,
+                             int32_t* n_live, void* stream);
+
 /* ----------------------------------------------------------------------------
  * Dense causal attention (comparator; page section "FlashAttention 的兴起":
  * a token sees only earlier tokens). q, k, v, o, do_, dq, dk, dv: [B,H,T,D]
@@ -229,7 +260,8 @@ scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int
  *   hash: live(i,j) = bucket ranges overlap AND max q_idx(i) >= min k_idx(j).
  *   FULL(i,j) (no element mask needed): both tiles have 128 valid rows, min
  *   q_idx(i) >= max k_idx(j) and, in hash mode, all four bucket bounds equal.
- * scfa_tile_view_get fills device pointers into the workspace:
+ * scfa_tile_view_get fills device pointers into the workspace (it reads the
+ * workspace header, synchronously, to find the lists):
  *   row_ptr [B*H*nQt+1], cols, fflags (CSR over q tiles, columns ascending);
  *   csc_ptr [B*H*nKt+1], csc_rows, cflags (CSC over k tiles, rows ascending);
  *   flag bit 0 = FULL; work_fwd [B*H*nQt] and work_bwd [B*H*nKt]: every tile

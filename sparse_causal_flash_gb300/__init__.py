@@ -41,6 +41,9 @@ _U = ctypes.c_uint
 _SIGS = {
     "scfa_status_string": ([_I], ctypes.c_char_p),
     "scfa_attn_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _S),
+    "scfa_attn_workspace_size_live": ([_I, _I, _I, _I, _I, _I, _I, ctypes.c_longlong], _S),
+    "scfa_attn_workspace_capacity": ([_I, _I, _I, _I, _I, _I, _I, _S], ctypes.c_longlong),
+    "scfa_tiles_count": ([_I, _P, _P, _P, _P, _I, _I, _I, _I, _P, _S, _P, _P], _I),
     "scfa_dense_fwd": ([_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _S, _U, _P], _I),
     "scfa_dense_bwd": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _S, _U, _P], _I),
     "scfa_qk_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _U, _P], _I),
@@ -123,6 +126,23 @@ def _need(t, dtype, name):
 
 def attn_workspace_size(mode, backward, B, H, Tq, Tk, D) -> int:
     return int(_lib.scfa_attn_workspace_size(mode, int(backward), B, H, Tq, Tk, D))
+
+
+def attn_workspace_size_live(mode, backward, B, H, Tq, Tk, D, n_live) -> int:
+    """Bytes of a workspace whose live-tile lists hold n_live entries."""
+    return int(_lib.scfa_attn_workspace_size_live(mode, int(backward), B, H, Tq, Tk, D, int(n_live)))
+
+
+def attn_workspace_capacity(mode, backward, B, H, Tq, Tk, D, ws_bytes) -> int:
+    """Live-tile list entries a workspace of ws_bytes holds (-1: too small)."""
+    return int(_lib.scfa_attn_workspace_capacity(mode, int(backward), B, H, Tq, Tk, D, int(ws_bytes)))
+
+
+def scfa_tiles_count(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, ws, n_live, stream=None):
+    """Live-tile count of a problem into the int32 CUDA tensor n_live (asynchronous)."""
+    _need(n_live, torch.int32, "n_live")
+    _check("scfa_tiles_count", _lib.scfa_tiles_count(mode, _ptr(q_idx), _ptr(k_idx), _ptr(q_hash), _ptr(k_hash), B, H,
+                                                     Tq, Tk, _ptr(ws), ws.numel(), _ptr(n_live), _stream(stream)))
 
 
 def lsh_workspace_size(B, H, T, n_buckets) -> int:

@@ -66,7 +66,7 @@ bool make_tmap_f32_3d(CUtensorMap* map, void* base, int D, long long T, long lon
   return r == CUDA_SUCCESS;
 }
 
-bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D, AttnWs* L) {
+bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D, AttnWs* L, long long cap) {
   if (mode < SCFA_MODE_DENSE || mode > SCFA_MODE_HASH) return false;
   if (B < 1 || H < 1 || Tq < 1 || Tk < 1 || D < 1) return false;
   AttnWs w;
@@ -79,6 +79,7 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
   w.n_pairs = BH * w.nPairs;
   w.max_live = w.n_qtiles * w.nKt;
   if (w.max_live >= INT_MAX || w.n_qtiles >= INT_MAX / 2 || w.n_ktiles >= INT_MAX / 2) return false;
+  w.cap = (cap < 0 || cap > w.max_live) ? w.max_live : cap;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -92,15 +93,10 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
   w.kcount = take(sizeof(int32_t) * w.n_ktiles);
   w.row_ptr = take(sizeof(int32_t) * (w.n_qtiles + 1));
   w.csc_ptr = take(sizeof(int32_t) * (w.n_ktiles + 1));
-  w.cols = take(sizeof(int32_t) * w.max_live);
-  w.csc_rows = take(sizeof(int32_t) * w.max_live);
-  w.fflags = take(w.max_live);
-  w.cflags = take(w.max_live);
   w.work_fwd = take(sizeof(int32_t) * w.n_qtiles);
   w.work_bwd = take(sizeof(int32_t) * w.n_ktiles);
   w.cursor = take(sizeof(int32_t) * (w.nQt + 2 * w.nKt + 3));
   w.pcount = take(sizeof(int32_t) * w.n_pairs);
-  w.ulist = take(sizeof(int32_t) * w.max_live);
   w.work_pairs = take(sizeof(int32_t) * w.n_pairs);
   w.vbits_bytes = sizeof(uint32_t) * static_cast<size_t>(BH) * ((Tq + 31) / 32 + (Tk + 31) / 32);
   w.vbits = take(w.vbits_bytes);
@@ -108,9 +104,48 @@ bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D,
     w.dq_acc = take(sizeof(float) * static_cast<size_t>(BH) * Tq * D);
     w.qmeta = take(4 * sizeof(float) * static_cast<size_t>(BH) * w.nQt * kTile);
   }
+  w.cols = take(sizeof(int32_t) * w.cap);
+  w.csc_rows = take(sizeof(int32_t) * w.cap);
+  w.ulist = take(sizeof(int32_t) * w.cap);
+  w.fflags = take(w.cap);
+  w.cflags = take(w.cap);
   w.total = off;
   *L = w;
   return true;
+}
+
+// The layout of a `ws_bytes` workspace depends on its size alone, not on the
+// call: a workspace that holds the backward's fixed part always lays out the
+// backward's arrays, so a forward and a SCFA_FLAG_REUSE_TILES backward on it
+// agree on where the lists are. The lists take the largest entry count that
+// fits after that (at most every tile pair).
+bool attn_ws_fit(int mode, int backward, int B, int H, int Tq, int Tk, int D, size_t ws_bytes, AttnWs* L) {
+  AttnWs w;
+  if (!attn_ws_layout(mode, 1, B, H, Tq, Tk, D, &w, 0)) return false;
+  const int kind = ws_bytes >= w.total ? 1 : 0;
+  if (backward && kind == 0) return false;
+  if (!attn_ws_layout(mode, kind, B, H, Tq, Tk, D, &w, 0) || ws_bytes < w.total) return false;
+  // largest cap in [0, max_live] whose layout fits (total grows with cap)
+  long long lo = 0, hi = w.max_live;
+  while (lo < hi) {
+    const long long mid = lo + (hi - lo + 1) / 2;
+    AttnWs t;
+    if (attn_ws_layout(mode, kind, B, H, Tq, Tk, D, &t, mid) && t.total <= ws_bytes) lo = mid;
+    else hi = mid - 1;
+  }
+  if (!attn_ws_layout(mode, kind, B, H, Tq, Tk, D, &w, lo)) return false;
+  *L = w;
+  return true;
+}
+
+// Bytes of a workspace whose lists hold `cap` entries for a call of the given
+// kind: a forward-only layout that would reach past the backward's fixed part
+// takes the backward's layout instead (see attn_ws_fit).
+size_t attn_ws_bytes(int mode, int backward, int B, int H, int Tq, int Tk, int D, long long cap) {
+  AttnWs w, f1;
+  if (!attn_ws_layout(mode, backward, B, H, Tq, Tk, D, &w, cap)) return 0;
+  if (backward || !attn_ws_layout(mode, 1, B, H, Tq, Tk, D, &f1, 0) || w.total < f1.total) return w.total;
+  return attn_ws_layout(mode, 1, B, H, Tq, Tk, D, &w, cap) ? w.total : 0;
 }
 
 static cudaEvent_t g_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
@@ -182,9 +217,12 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   // with SCFA_FLAG_KEEP_O32 the forward also needs the backward's workspace
   // (its fp32 copy of O lives where the backward keeps the dQ accumulator)
   const bool keep_o32 = (flags & SCFA_FLAG_KEEP_O32) != 0;
+  const int kind = (backward || keep_o32) ? 1 : 0;
   AttnWs L;
-  if (!attn_ws_layout(mode, (backward || keep_o32) ? 1 : 0, B, H, Tq, Tk, D, &L)) return SCFA_ERR_UNSUPPORTED;
-  if (!aligned256(ws) || ws_bytes < L.total) return SCFA_ERR_WORKSPACE;
+  if (!attn_ws_layout(mode, kind, B, H, Tq, Tk, D, &L, 0)) return SCFA_ERR_UNSUPPORTED;
+  // the live-tile lists get whatever the workspace holds past its fixed part
+  // (a list that does not fit is reported on the device, see scfa.h)
+  if (!aligned256(ws) || !attn_ws_fit(mode, kind, B, H, Tq, Tk, D, ws_bytes, &L)) return SCFA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   cudaError_t e = cudaSuccess;
@@ -249,9 +287,19 @@ const char* scfa_status_string(scfa_status s) {
 }
 
 size_t scfa_attn_workspace_size(int mode, int backward, int B, int H, int Tq, int Tk, int D) {
+  return attn_ws_bytes(mode, backward, B, H, Tq, Tk, D, -1);
+}
+
+size_t scfa_attn_workspace_size_live(int mode, int backward, int B, int H, int Tq, int Tk, int D, long long n_live) {
+  if (n_live < 0) return 0;
+  return attn_ws_bytes(mode, backward, B, H, Tq, Tk, D, n_live);
+}
+
+long long scfa_attn_workspace_capacity(int mode, int backward, int B, int H, int Tq, int Tk, int D,
+                                       size_t ws_bytes) {
   AttnWs L;
-  if (!attn_ws_layout(mode, backward, B, H, Tq, Tk, D, &L)) return 0;
-  return L.total;
+  if (!attn_ws_fit(mode, backward, B, H, Tq, Tk, D, ws_bytes, &L)) return -1;
+  return L.cap;
 }
 
 scfa_status scfa_dense_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, int B, int H, int T, int D,
@@ -379,28 +427,49 @@ scfa_status scfa_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx, con
   if (mode != SCFA_MODE_DENSE && (!q_idx || !k_idx)) return SCFA_ERR_INVALID;
   if (mode == SCFA_MODE_HASH && (!q_hash || !k_hash)) return SCFA_ERR_INVALID;
   AttnWs L;
-  if (!attn_ws_layout(mode, 1, B, H, Tq, Tk, D, &L)) return SCFA_ERR_INVALID;
-  if (!aligned256(ws) || ws_bytes < L.total) return SCFA_ERR_WORKSPACE;
+  if (!attn_ws_layout(mode, 0, B, H, Tq, Tk, D, &L, 0)) return SCFA_ERR_INVALID;
+  if (!aligned256(ws) || !attn_ws_fit(mode, 0, B, H, Tq, Tk, D, ws_bytes, &L)) return SCFA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return finish(launch_tiles(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, flags, static_cast<char*>(ws), L, st),
                 flags, st);
 }
 
+scfa_status scfa_tiles_count(int mode, const int32_t* q_idx, const int32_t* k_idx, const int32_t* q_hash,
+                             const int32_t* k_hash, int B, int H, int Tq, int Tk, void* ws, size_t ws_bytes,
+                             int32_t* n_live, void* stream) {
+  if (!ws || !n_live || B < 1 || H < 1 || Tq < 1 || Tk < 1) return SCFA_ERR_INVALID;
+  if (mode != SCFA_MODE_DENSE && (!q_idx || !k_idx)) return SCFA_ERR_INVALID;
+  if (mode == SCFA_MODE_HASH && (!q_hash || !k_hash)) return SCFA_ERR_INVALID;
+  AttnWs L;
+  if (!attn_ws_layout(mode, 0, B, H, Tq, Tk, 64, &L, 0)) return SCFA_ERR_INVALID;
+  if (!aligned256(ws) || ws_bytes < L.total) return SCFA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  cudaError_t e = launch_tiles(mode, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, 0, w, L, st, false, true);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(n_live, &reinterpret_cast<WsHeader*>(w + L.header)->n_live, sizeof(int32_t),
+                        cudaMemcpyDeviceToDevice, st);
+  return e == cudaSuccess ? SCFA_OK : SCFA_ERR_CUDA;
+}
+
 scfa_status scfa_tile_view_get(const void* ws, int mode, int B, int H, int Tq, int Tk, int D, scfa_tile_view* out) {
   if (!ws || !out) return SCFA_ERR_INVALID;
   AttnWs L;
-  if (!attn_ws_layout(mode, 1, B, H, Tq, Tk, D, &L)) return SCFA_ERR_INVALID;
+  if (!attn_ws_layout(mode, 1, B, H, Tq, Tk, D, &L, 0)) return SCFA_ERR_INVALID;
+  // the lists are where the call that built them recorded them
+  WsHeader h;
+  if (cudaMemcpy(&h, ws, sizeof(WsHeader), cudaMemcpyDeviceToHost) != cudaSuccess) return SCFA_ERR_CUDA;
   const char* w = static_cast<const char*>(ws);
   out->row_ptr = reinterpret_cast<const int32_t*>(w + L.row_ptr);
-  out->cols = reinterpret_cast<const int32_t*>(w + L.cols);
-  out->fflags = reinterpret_cast<const uint8_t*>(w + L.fflags);
+  out->cols = reinterpret_cast<const int32_t*>(w + h.list_off[kListCols]);
+  out->fflags = reinterpret_cast<const uint8_t*>(w + h.list_off[kListFflags]);
   out->csc_ptr = reinterpret_cast<const int32_t*>(w + L.csc_ptr);
-  out->csc_rows = reinterpret_cast<const int32_t*>(w + L.csc_rows);
-  out->cflags = reinterpret_cast<const uint8_t*>(w + L.cflags);
+  out->csc_rows = reinterpret_cast<const int32_t*>(w + h.list_off[kListCscRows]);
+  out->cflags = reinterpret_cast<const uint8_t*>(w + h.list_off[kListCflags]);
   out->work_fwd = reinterpret_cast<const int32_t*>(w + L.work_fwd);
   out->work_bwd = reinterpret_cast<const int32_t*>(w + L.work_bwd);
   out->pair_count = reinterpret_cast<const int32_t*>(w + L.pcount);
-  out->pair_list = reinterpret_cast<const int32_t*>(w + L.ulist);
+  out->pair_list = reinterpret_cast<const int32_t*>(w + h.list_off[kListPairs]);
   out->work_pairs = reinterpret_cast<const int32_t*>(w + L.work_pairs);
   out->n_q_tiles = L.nQt;
   out->n_k_tiles = L.nKt;

@@ -95,8 +95,6 @@ struct BwdParams {
   long long qm_n;
   int Tqp;
   const int32_t* csc_ptr;
-  const int32_t* csc_rows;
-  const uint8_t* cflags;
   const int32_t* work;
   int n_work;
   uint16_t* dk;
@@ -130,6 +128,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   constexpr int kQStages = BwdSmem<D>::kQStages;
   constexpr int kHalves = D / 64;  // a work item = (key tile, 64-column half of D)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // live-tile lists where the call that built them put them
+  const int32_t* const csc_rows = ws_list<int32_t>(p.status, kListCscRows);
+  const uint8_t* const cflags = ws_list<uint8_t>(p.status, kListCflags);
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384, kColPT = 448;
 
   if (threadIdx.x == 0) {
@@ -206,7 +207,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       for (int t = 0; t < (stall ? min(n, kQStages) : n); ++t) {
-        const int i = p.csc_rows[start + t];
+        const int i = csc_rows[start + t];
         const int s = q_it % kQStages;
         if (lane == 0) {
           ok = mbar_wait(&sm.q_empty[s], ((q_it / kQStages) & 1) ^ 1, abort_flag, p.status);
@@ -389,7 +390,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (p.mode == SCFA_MODE_HASH && kvalid) kh = p.k_hash[gk];
       bool ok = true;
       for (int t = 0; t < n; ++t) {
-        const bool full = (p.cflags[start + t] & kFlagFull) != 0;
+        const bool full = (cflags[start + t] & kFlagFull) != 0;
         const int s = q_it % kQStages;
         const int db = it & 1;
         ok = mbar_wait(&sm.q_full[s], (q_it / kQStages) & 1, abort_flag, p.status) &&
@@ -454,6 +455,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_ld32(lane_base + kColS + grp * 64, sr);
           tmem_ld32(lane_base + kColDP + grp * 64, dr);
           tmem_wait_ld();
+          tmem_ld_fence(sr);
+          tmem_ld_fence(dr);
           chunk(0, sr, dr, pk[0], dsk[0]);
         }
         {
@@ -461,6 +464,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_ld32(lane_base + kColS + grp * 64 + 32, sr);
           tmem_ld32(lane_base + kColDP + grp * 64 + 32, dr);
           tmem_wait_ld();
+          tmem_ld_fence(sr);
+          tmem_ld_fence(dr);
           tc_fence_before();
           mbar_arrive(&sm.st_empty);  // S^T / dP^T may now be overwritten by the next A
           chunk(1, sr, dr, pk[1], dsk[1]);
@@ -497,6 +502,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) tmem_ld32(lane_base + (grp == 0 ? kColDV : kColDK) + cc * 32, acc[cc]);
       tmem_wait_ld();
+      tmem_ld_fence(acc[0]);
+      tmem_ld_fence(acc[1]);
       tc_fence_before();
       mbar_arrive(&sm.dkv_empty);
       if (kro >= 0 && kro < p.Tk)
@@ -532,7 +539,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int bh = g / p.nKt;
       bool ok = true;
       for (int t = 0; t < n; ++t) {
-        const int i = p.csc_rows[start + t];
+        const int i = csc_rows[start + t];
         ok = mbar_wait(&sm.dq_full, it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -540,6 +547,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) tmem_ld32(lane_base + kColDQ + cc * 32, qv[cc]);
         tmem_wait_ld();
+        tmem_ld_fence(qv[0]);
+        tmem_ld_fence(qv[1]);
         tc_fence_before();
         mbar_arrive(&sm.dq_empty);
         // the two 32-column halves go through one 16 KB staging tile; the
@@ -625,6 +634,9 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   Bwd128Smem& sm = *reinterpret_cast<Bwd128Smem*>(smem_raw + pad);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // live-tile lists where the call that built them put them
+  const int32_t* const csc_rows = ws_list<int32_t>(p.status, kListCscRows);
+  const uint8_t* const cflags = ws_list<uint8_t>(p.status, kListCflags);
   constexpr uint32_t kColS = 0, kColPT = 0, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK = 384;
 
   if (threadIdx.x == 0) {
@@ -700,7 +712,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       for (int t = 0; t < (stall ? 1 : n); ++t) {
-        const int i = p.csc_rows[start + t];
+        const int i = csc_rows[start + t];
         const int mb = qt & 1, s = qt & 1;
         if (lane == 0) {
           // Q into its stage once dK two tiles back has read it; dO and the
@@ -858,7 +870,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (p.mode == SCFA_MODE_HASH && kvalid) kh = p.k_hash[gk];
       bool ok = true;
       for (int t = 0; t < n; ++t) {
-        const bool full = (p.cflags[start + t] & kFlagFull) != 0;
+        const bool full = (cflags[start + t] & kFlagFull) != 0;
         const int mb = it & 1;
         ok = mbar_wait(&sm.do_full, it & 1, abort_flag, p.status) &&
              mbar_wait(&sm.s_full, it & 1, abort_flag, p.status);
@@ -918,6 +930,8 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tmem_ld32(lane_base + kColS + grp * 64, sr);
           tmem_ld32(lane_base + kColDP + grp * 64, dr);
           tmem_wait_ld();
+          tmem_ld_fence(sr);
+          tmem_ld_fence(dr);
           chunk(0, sr, dr, pk[0], dsk[0]);
         }
         {
@@ -925,6 +939,8 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tmem_ld32(lane_base + kColS + grp * 64 + 32, sr);
           tmem_ld32(lane_base + kColDP + grp * 64 + 32, dr);
           tmem_wait_ld();
+          tmem_ld_fence(sr);
+          tmem_ld_fence(dr);
           tc_fence_before();
           mbar_arrive(&sm.loaded);  // this thread's S^T / dP^T columns are in registers
           chunk(1, sr, dr, pk[1], dsk[1]);
@@ -965,6 +981,8 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) tmem_ld32(lane_base + col + hf * 64 + cc * 32, acc[cc]);
         tmem_wait_ld();
+        tmem_ld_fence(acc[0]);
+        tmem_ld_fence(acc[1]);
         if (hf == 1) {
           tc_fence_before();
           mbar_arrive(&sm.dkv_empty);
@@ -999,7 +1017,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const int bh = g / p.nKt;
       bool ok = true;
       for (int t = 0; t < n; ++t) {
-        const int i = p.csc_rows[start + t];
+        const int i = csc_rows[start + t];
         ok = mbar_wait(&sm.dq_full, it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -1010,6 +1028,8 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) tmem_ld32(lane_base + kColDQ + rd * 64 + cc * 32, qv[cc]);
           tmem_wait_ld();
+          tmem_ld_fence(qv[0]);
+          tmem_ld_fence(qv[1]);
           if (rd == 1) {
             tc_fence_before();
             mbar_arrive(&sm.dq_empty);
@@ -1229,8 +1249,6 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   p.qm_n = n_pad;
   p.Tqp = Tqp;
   p.csc_ptr = reinterpret_cast<const int32_t*>(a.ws + L.csc_ptr);
-  p.csc_rows = reinterpret_cast<const int32_t*>(a.ws + L.csc_rows);
-  p.cflags = reinterpret_cast<const uint8_t*>(a.ws + L.cflags);
   p.work = reinterpret_cast<const int32_t*>(a.ws + L.work_bwd);
   p.n_work = static_cast<int>(L.n_ktiles);  // one work item per key tile
   p.dk = a.dk;

@@ -104,11 +104,8 @@ struct FwdParams {
   const int32_t* q_hash;
   const int32_t* k_hash;
   const int32_t* row_ptr;
-  const int32_t* cols;
-  const uint8_t* fflags;
   const int32_t* work_pairs;
   const int32_t* pcount;
-  const int32_t* ulist;
   int n_pairs;
   const int32_t* work;   // query tiles by live count descending (single-tile kernel)
   int n_work;
@@ -130,6 +127,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(smem_raw + pad);
   constexpr int kStages = FwdSmem<D>::kStages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // live-tile lists where the call that built them put them
+  const int32_t* const cols = ws_list<int32_t>(p.status, kListCols);
+  const uint8_t* const fflags = ws_list<uint8_t>(p.status, kListFflags);
+  const int32_t* const ulist = ws_list<int32_t>(p.status, kListPairs);
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
@@ -181,7 +182,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (has1) tma_load_3d(sm.q[1][sub], &tm_q, &sm.q_full, sub * 64, (2 * m + 1) * kTile, bh);
         }
         last_q = item;
-        const int32_t* ul = p.ulist + p.row_ptr[g0];
+        const int32_t* ul = ulist + p.row_ptr[g0];
         bool ok = !(p.stall && kv_it == 0);  // debug stall: no K / V load ever arrives
         for (int t = 0; t < cnt && ok; ++t) {
           const int j = ul[t] >> 4;
@@ -252,7 +253,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const long long g0 = static_cast<long long>(bh) * p.nQt + 2 * m;
         // union entries: current, next, and the one after, loaded two tiles
         // ahead so the list read stays off the issue chain
-        const int32_t* ul = p.ulist + p.row_ptr[g0];
+        const int32_t* ul = ulist + p.row_ptr[g0];
         int bits_cur = ul[0] & 15;
         int bits_nxt = cnt > 1 ? ul[1] & 15 : 0;
         if (!mbar_wait(&sm.q_full, item & 1, abort_flag, p.status)) break;
@@ -360,13 +361,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       };
       int j_c = 0, f_c = 0, kid_c = INT_MAX, kh_c = INT_MIN, j_n = 0, f_n = 0;
       if (e_beg < e_end) {
-        j_c = p.cols[e_beg];
-        f_c = p.fflags[e_beg];
+        j_c = cols[e_beg];
+        f_c = fflags[e_beg];
         key_meta(j_c, f_c, kid_c, kh_c);
       }
       if (e_beg + 1 < e_end) {
-        j_n = p.cols[e_beg + 1];
-        f_n = p.fflags[e_beg + 1];
+        j_n = cols[e_beg + 1];
+        f_n = fflags[e_beg + 1];
       }
       float m_used = -INFINITY, l = 0.f;
       float m_top = -INFINITY;  // largest score of the row so far (log2 units)
@@ -377,8 +378,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int kid_n = INT_MAX, kh_n = INT_MIN, j_nn = 0, f_nn = 0;
         if (e + 1 < e_end) key_meta(j_n, f_n, kid_n, kh_n);
         if (e + 2 < e_end) {
-          j_nn = p.cols[e + 2];
-          f_nn = p.fflags[e + 2];
+          j_nn = cols[e + 2];
+          f_nn = fflags[e + 2];
         }
         const bool first_tile = !any;
         any = true;
@@ -397,6 +398,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int cc = 0; cc < 4; ++cc)
           tmem_ld32(lane_base + colS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
         tmem_wait_ld();
+        tmem_ld_fence(sr);
         if (kSepP) {
           // S_g is in registers: the MMA warp may compute the next S_g
           tc_fence_before();
@@ -477,6 +479,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             uint32_t orr[32];
             tmem_ld32(lane_base + colO + cc * 32, orr);
             tmem_wait_ld();
+            tmem_ld_fence(orr);
 #pragma unroll
             for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
             tmem_st32(lane_base + colO + cc * 32, orr);
@@ -515,6 +518,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_base + colO + cc * 32, orr[cc]);
       tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld_fence(orr[cc]);
       tc_fence_before();
       mbar_arrive(&sm.o_empty[grp]);
       ++o_it;
@@ -595,6 +600,9 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   Fwd1Smem& sm = *reinterpret_cast<Fwd1Smem*>(smem_raw + pad);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // live-tile lists where the call that built them put them
+  const int32_t* const cols = ws_list<int32_t>(p.status, kListCols);
+  const uint8_t* const fflags = ws_list<uint8_t>(p.status, kListFflags);
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -662,7 +670,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         q_issued = item + 1;
         bool ok = !(p.stall && kv == 0);  // debug stall: no K / V load ever arrives
         for (int t = 0; t < n && ok; ++t) {
-          const int j = p.cols[e0 + t];
+          const int j = cols[e0 + t];
           const int s = kv % kF1Stages;
           const uint32_t ph = ((kv / kF1Stages) & 1) ^ 1;
           if (!mbar_wait(&sm.k_empty[s], ph, abort_flag, p.status)) { ok = false; break; }
@@ -813,12 +821,12 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       // column / flag two tiles ahead, key metadata one tile ahead
       int f_c = 0, j_n = 0, f_n = 0, kid_c = INT_MAX, kh_c = INT_MIN;
       if (e_beg < e_end) {
-        f_c = p.fflags[e_beg];
-        key_meta(p.cols[e_beg], f_c, kid_c, kh_c);
+        f_c = fflags[e_beg];
+        key_meta(cols[e_beg], f_c, kid_c, kh_c);
       }
       if (e_beg + 1 < e_end) {
-        j_n = p.cols[e_beg + 1];
-        f_n = p.fflags[e_beg + 1];
+        j_n = cols[e_beg + 1];
+        f_n = fflags[e_beg + 1];
       }
       float m_used = -INFINITY, l = 0.f;
       float m_top = -INFINITY;  // largest score of the row so far (log2 units)
@@ -828,8 +836,8 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         int kid_n = INT_MAX, kh_n = INT_MIN, j_nn = 0, f_nn = 0;
         if (e + 1 < e_end) key_meta(j_n, f_n, kid_n, kh_n);
         if (e + 2 < e_end) {
-          j_nn = p.cols[e + 2];
-          f_nn = p.fflags[e + 2];
+          j_nn = cols[e + 2];
+          f_nn = fflags[e + 2];
         }
         const bool first_tile = !any;
         any = true;
@@ -847,6 +855,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int cc = 0; cc < 4; ++cc)
           tmem_ld32(lane_base + kColS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
         tmem_wait_ld();
+        tmem_ld_fence(sr);
         // S is in registers: the MMA warp may compute the next S
         tc_fence_before();
         mbar_arrive(&sm.s_free);
@@ -924,6 +933,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               uint32_t orr[32];
               tmem_ld32(lane_base + kColO + cc * 32, orr);
               tmem_wait_ld();
+              tmem_ld_fence(orr);
 #pragma unroll
               for (int e2 = 0; e2 < 32; ++e2) orr[e2] = __float_as_uint(__uint_as_float(orr[e2]) * alpha);
               tmem_st32(lane_base + kColO + cc * 32, orr);
@@ -967,6 +977,8 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_base + kColO + cc * 32, orr[cc]);
       tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) tmem_ld_fence(orr[cc]);
       tc_fence_before();
       mbar_arrive(&sm.o_empty);
       ++o_it;
@@ -1039,12 +1051,9 @@ static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   p.q_hash = a.q_hash;
   p.k_hash = a.k_hash;
   p.row_ptr = reinterpret_cast<const int32_t*>(a.ws + L.row_ptr);
-  p.cols = reinterpret_cast<const int32_t*>(a.ws + L.cols);
-  p.fflags = reinterpret_cast<const uint8_t*>(a.ws + L.fflags);
   p.nPairs = L.nPairs;
   p.work_pairs = reinterpret_cast<const int32_t*>(a.ws + L.work_pairs);
   p.pcount = reinterpret_cast<const int32_t*>(a.ws + L.pcount);
-  p.ulist = reinterpret_cast<const int32_t*>(a.ws + L.ulist);
   p.n_pairs = static_cast<int>(L.n_pairs);
   p.o = a.o_out;
   p.o_rows = a.q_rows;
@@ -1085,8 +1094,6 @@ static cudaError_t launch_fwd1(const AttnArgs& a, cudaStream_t st) {
   p.q_hash = a.q_hash;
   p.k_hash = a.k_hash;
   p.row_ptr = reinterpret_cast<const int32_t*>(a.ws + L.row_ptr);
-  p.cols = reinterpret_cast<const int32_t*>(a.ws + L.cols);
-  p.fflags = reinterpret_cast<const uint8_t*>(a.ws + L.fflags);
   p.work = reinterpret_cast<const int32_t*>(a.ws + L.work_fwd);
   p.n_work = static_cast<int>(L.n_qtiles);
   p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched;

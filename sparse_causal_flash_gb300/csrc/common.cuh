@@ -24,8 +24,20 @@ struct WsHeader {
   // done; zeroed with the header by the tile pass and again by the last CTA
   // of each launch
   int sched[4];
-  int pad[58];
+  // where the call that built the live-tile lists put them (byte offsets from
+  // the workspace start: cols, csc_rows, fflags, cflags, pair lists) and how
+  // many entries each holds; calls that reuse the lists read them from here
+  long long list_off[5];
+  long long list_cap;
+  int pad[46];
 };
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+enum { kListCols = 0, kListCscRows = 1, kListFflags = 2, kListCflags = 3, kListPairs = 4 };
+template <typename T>
+__device__ __forceinline__ const T* ws_list(const int* status, int which) {
+  const WsHeader* h = reinterpret_cast<const WsHeader*>(status);
+  return reinterpret_cast<const T*>(reinterpret_cast<const char*>(h) + h->list_off[which]);
+}
 
 // ---------------------------------------------------------------------------
 // Generic helpers
@@ -50,12 +62,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// three-input maximum (one instruction on sm_100 and later)
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
+// maximum of three. Written as two fmaxf so that the compiler picks the
+// instruction: a hand-written three-input max.f32 on scores fresh from a TMEM
+// load returned stale values in the softmax loop (a row whose every key was
+// masked got a tiny denormal instead of -inf as its tile maximum), which made
+// the low bits of O and LSE depend on the launch.
+__device__ __forceinline__ float max3f(float a, float b, float c) { return fmaxf(fmaxf(a, b), c); }
 
 // packed pairs of f32: one instruction does two lanes' worth of FMA / add / mul
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
@@ -365,6 +377,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// tcgen05.ld fills its destination registers asynchronously, but to the
+// compiler they are defined when the load issues: register-only arithmetic on
+// them (a max, an FMA) may be scheduled above tcgen05.wait::ld and then reads
+// values the load has not written yet. After each wait, pass every register
+// loaded since the previous wait through this empty volatile asm: it comes
+// after the wait (volatile asm keeps its order) and redefines the registers,
+// so every use of them follows it.
+template <int N>
+__device__ __forceinline__ void tmem_ld_fence(uint32_t (&r)[N]) {
+  static_assert(N % 8 == 0, "fence registers in groups of 8");
+#pragma unroll
+  for (int i = 0; i < N; i += 8)
+    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]),
+                 "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Offset of element (row, col) of a [rows][64] bf16 tile stored with the

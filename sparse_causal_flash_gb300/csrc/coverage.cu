@@ -32,7 +32,8 @@ __global__ void __launch_bounds__(kCountWarps * 32)
 count_live_pairs_kernel(int mode, const int32_t* __restrict__ q_idx, const int32_t* __restrict__ k_idx,
                         const int32_t* __restrict__ q_hash, const int32_t* __restrict__ k_hash,
                         int Tq, int Tk, int nQt, long long n_qtiles, const int32_t* __restrict__ row_ptr,
-                        const int32_t* __restrict__ cols, unsigned long long* __restrict__ count) {
+                        const int* ws_header, unsigned long long* __restrict__ count) {
+  const int32_t* const cols = ws_list<int32_t>(ws_header, kListCols);
   __shared__ int32_t kid[kCountWarps][kTile];
   __shared__ int32_t khs[kCountWarps][kTile];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -111,8 +112,8 @@ extern "C" scfa_status scfa_count_pairs(int mode, const int32_t* q_idx, const in
   if (!ws || !count || B < 1 || H < 1 || Tq < 1 || Tk < 1) return SCFA_ERR_INVALID;
   if (mode != SCFA_MODE_DENSE && (!q_idx || !k_idx)) return SCFA_ERR_INVALID;
   if (mode == SCFA_MODE_HASH && (!q_hash || !k_hash)) return SCFA_ERR_INVALID;
-  AttnWs L;
-  if (!attn_ws_layout(mode, 0, B, H, Tq, Tk, D, &L)) return SCFA_ERR_INVALID;
+  AttnWs L;  // row pointers at their fixed place; the lists where the builder recorded them
+  if (!attn_ws_layout(mode, 0, B, H, Tq, Tk, D, &L, 0)) return SCFA_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < L.total) return SCFA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const char* w = static_cast<const char*>(ws);
@@ -121,7 +122,7 @@ extern "C" scfa_status scfa_count_pairs(int mode, const int32_t* q_idx, const in
   if (blocks > 16LL * num_sms()) blocks = 16LL * num_sms();
   count_live_pairs_kernel<<<static_cast<int>(blocks), kCountWarps * 32, 0, st>>>(
       mode, q_idx, k_idx, q_hash, k_hash, Tq, Tk, L.nQt, L.n_qtiles, reinterpret_cast<const int32_t*>(w + L.row_ptr),
-      reinterpret_cast<const int32_t*>(w + L.cols), count);
+      reinterpret_cast<const int*>(w + L.header), count);
   return cudaGetLastError() == cudaSuccess ? SCFA_OK : SCFA_ERR_CUDA;
 }
 

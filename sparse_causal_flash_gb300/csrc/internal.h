@@ -16,7 +16,8 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct AttnWs {
   int nQt = 0, nKt = 0;
   long long n_qtiles = 0, n_ktiles = 0;  // over all heads
-  long long max_live = 0;                // capacity of the live lists
+  long long max_live = 0;                // every (query tile, key tile) pair
+  long long cap = 0;                     // entries the live lists hold (<= max_live)
   size_t header = 0;
   size_t qstat = 0, kstat = 0;           // int4 per tile: min idx, max idx, min hash, max hash
   size_t qcount = 0, kcount = 0;         // live count per q tile / k tile
@@ -42,8 +43,16 @@ struct AttnWs {
   size_t total = 0;
 };
 
-// Returns false if the sizes are out of range.
-bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D, AttnWs* L);
+// Layout with lists of `cap` entries (cap < 0: every tile pair); returns false
+// if the sizes are out of range. The live-tile lists come last, after the
+// backward's arrays.
+bool attn_ws_layout(int mode, int backward, int B, int H, int Tq, int Tk, int D, AttnWs* L, long long cap = -1);
+// The layout of a `ws_bytes` workspace, the same for every call on it: the
+// backward's arrays whenever it holds them, then lists as long as fit (at most
+// every tile pair). False if the fixed part the call needs does not fit.
+bool attn_ws_fit(int mode, int backward, int B, int H, int Tq, int Tk, int D, size_t ws_bytes, AttnWs* L);
+// Workspace bytes for lists of `cap` entries (cap < 0: every tile pair).
+size_t attn_ws_bytes(int mode, int backward, int B, int H, int Tq, int Tk, int D, long long cap);
 
 struct LshWs {
   size_t header = 0;
@@ -59,10 +68,13 @@ int num_sms();
 // tiles.cu
 // with_pairs: also build the union lists and order of query-tile pairs (the
 // head-dimension-128 forward walks those)
+// count_only: per-tile statistics, live counts and their scan only (the
+// header's n_live then holds the total; no lists are written)
 cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
                          const int32_t* q_hash, const int32_t* k_hash,
                          int B, int H, int Tq, int Tk, unsigned flags,
-                         char* ws, const AttnWs& L, cudaStream_t st, bool with_pairs = true);
+                         char* ws, const AttnWs& L, cudaStream_t st, bool with_pairs = true,
+                         bool count_only = false);
 
 // SCFA_FLAG_VALIDATE: contract checks of the index inputs into the status word
 cudaError_t launch_validate(int mode, bool original, const int32_t* q_idx, const int32_t* k_idx,

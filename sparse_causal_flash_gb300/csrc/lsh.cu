@@ -705,6 +705,7 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
         uint32_t v[16];
         tmem_ld16(lane_base + col0 + c0, v);
         tmem_wait_ld();
+        tmem_ld_fence(v);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int c = c0 + u;

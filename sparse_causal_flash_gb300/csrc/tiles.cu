@@ -140,10 +140,13 @@ __global__ void tile_count_kernel(TileCtx c, long long n_q, long long n_k,
   }
 }
 
-// Exclusive scans: block 0 -> row_ptr from qcount, block 1 -> csc_ptr from kcount.
+// Exclusive scans: block 0 -> row_ptr from qcount, block 1 -> csc_ptr from
+// kcount. If the total exceeds the lists' capacity `cap`, every pointer is 0
+// (all lists empty, so nothing reads or writes past them) and the status word
+// says SCFA_ERR_WORKSPACE.
 __global__ void tile_scan_kernel(const int32_t* __restrict__ qcount, long long n_q, int32_t* __restrict__ row_ptr,
                                  const int32_t* __restrict__ kcount, long long n_k, int32_t* __restrict__ csc_ptr,
-                                 WsHeader* hdr) {
+                                 WsHeader* hdr, long long cap) {
   const int32_t* in = blockIdx.x == 0 ? qcount : kcount;
   int32_t* out = blockIdx.x == 0 ? row_ptr : csc_ptr;
   const long long n = blockIdx.x == 0 ? n_q : n_k;
@@ -171,14 +174,18 @@ __global__ void tile_scan_kernel(const int32_t* __restrict__ qcount, long long n
     wsum[lane] = s;  // inclusive over warps
   }
   __syncthreads();
-  long long run = x - sum + (w > 0 ? wsum[w - 1] : 0);
+  const bool over = wsum[(nt >> 5) - 1] > cap;
+  long long run = over ? 0 : x - sum + (w > 0 ? wsum[w - 1] : 0);
   for (long long i = b; i < e; ++i) {
     out[i] = static_cast<int32_t>(run);
-    run += in[i];
+    if (!over) run += in[i];
   }
   if (tid == nt - 1) {
     out[n] = static_cast<int32_t>(run);
-    if (blockIdx.x == 0) hdr->n_live = static_cast<int>(run);
+    if (blockIdx.x == 0) {
+      hdr->n_live = static_cast<int>(run);
+      if (over) raise_status(&hdr->status, SCFA_ERR_WORKSPACE);
+    }
   }
 }
 
@@ -201,7 +208,10 @@ __global__ void tile_fill_kernel(TileCtx c, long long n_q, long long n_k,
     int lo, hi;
     partner_range(c, by_q, self, bh, &lo, &hi);
     const int4* other = (by_q ? c.kstat : c.qstat) + bh * (by_q ? c.nKt : c.nQt);
-    long long pos = by_q ? row_ptr[id] : csc_ptr[id];
+    const long long first = by_q ? row_ptr[id] : csc_ptr[id];
+    // entries this tile may write (0 for every tile when the lists overflowed)
+    const long long budget = (by_q ? row_ptr[id + 1] : csc_ptr[id + 1]) - first;
+    long long pos = first;
     for (int p0 = lo; p0 < hi; p0 += 32) {
       const int p = p0 + lane;
       bool live = false;
@@ -214,7 +224,7 @@ __global__ void tile_fill_kernel(TileCtx c, long long n_q, long long n_k,
         f = tile_full(c, by_q ? me : p, by_q ? p : me, qs, ks) ? kFlagFull : 0;
       }
       const unsigned m = __ballot_sync(0xffffffffu, live);
-      if (live) {
+      if (live && pos + __popc(m & ((1u << lane) - 1u)) - first < budget) {
         const long long at = pos + __popc(m & ((1u << lane) - 1u));
         if (by_q) {
           cols[at] = p;
@@ -490,6 +500,23 @@ __global__ void validate_kernel(int mode, int original, const int32_t* __restric
   }
 }
 
+// Clears the status word, counters and schedule, and records where this call
+// puts the live-tile lists and how many entries they hold.
+__global__ void ws_header_init_kernel(WsHeader* hdr, long long c0, long long c1, long long c2, long long c3,
+                                      long long c4, long long cap) {
+  if (threadIdx.x == 0) {
+    hdr->status = 0;
+    hdr->n_live = 0;
+    for (int i = 0; i < 4; ++i) hdr->sched[i] = 0;
+    hdr->list_off[kListCols] = c0;
+    hdr->list_off[kListCscRows] = c1;
+    hdr->list_off[kListFflags] = c2;
+    hdr->list_off[kListCflags] = c3;
+    hdr->list_off[kListPairs] = c4;
+    hdr->list_cap = cap;
+  }
+}
+
 inline int grid_for(long long work, int block, int max_blocks) {
   long long g = (work + block - 1) / block;
   if (g < 1) g = 1;
@@ -519,7 +546,7 @@ cudaError_t launch_validate(int mode, bool original, const int32_t* q_idx, const
 cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
                          const int32_t* q_hash, const int32_t* k_hash,
                          int B, int H, int Tq, int Tk, unsigned flags,
-                         char* ws, const AttnWs& L, cudaStream_t st, bool with_pairs) {
+                         char* ws, const AttnWs& L, cudaStream_t st, bool with_pairs, bool count_only) {
   const int sms = num_sms();
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
   int4* qstat = reinterpret_cast<int4*>(ws + L.qstat);
@@ -529,8 +556,10 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
   int32_t* row_ptr = reinterpret_cast<int32_t*>(ws + L.row_ptr);
   int32_t* csc_ptr = reinterpret_cast<int32_t*>(ws + L.csc_ptr);
 
-  cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st);
-  if (e != cudaSuccess) return e;
+  ws_header_init_kernel<<<1, 32, 0, st>>>(hdr, static_cast<long long>(L.cols), static_cast<long long>(L.csc_rows),
+                                         static_cast<long long>(L.fflags), static_cast<long long>(L.cflags),
+                                         static_cast<long long>(L.ulist), L.cap);
+  cudaError_t e = cudaSuccess;
   tile_stats_kernel<<<grid_for(L.n_qtiles * 32, 256, sms * 8), 256, 0, st>>>(
       mode, q_idx, q_hash, L.n_qtiles, Tq, L.nQt, qstat);
   tile_stats_kernel<<<grid_for(L.n_ktiles * 32, 256, sms * 8), 256, 0, st>>>(
@@ -538,7 +567,9 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
   TileCtx c{mode, flags, Tq, Tk, L.nQt, L.nKt, qstat, kstat};
   const long long nt = L.n_qtiles + L.n_ktiles;
   tile_count_kernel<<<grid_for(nt * 32, 256, sms * 8), 256, 0, st>>>(c, L.n_qtiles, L.n_ktiles, qcount, kcount);
-  tile_scan_kernel<<<2, 1024, 0, st>>>(qcount, L.n_qtiles, row_ptr, kcount, L.n_ktiles, csc_ptr, hdr);
+  tile_scan_kernel<<<2, 1024, 0, st>>>(qcount, L.n_qtiles, row_ptr, kcount, L.n_ktiles, csc_ptr, hdr,
+                                       count_only ? LLONG_MAX : L.cap);
+  if (count_only) return cudaGetLastError();
   tile_fill_kernel<<<grid_for(nt * 32, 256, sms * 8), 256, 0, st>>>(
       c, L.n_qtiles, L.n_ktiles, row_ptr, reinterpret_cast<int32_t*>(ws + L.cols),
       reinterpret_cast<uint8_t*>(ws + L.fflags), csc_ptr, reinterpret_cast<int32_t*>(ws + L.csc_rows),

@@ -18,8 +18,12 @@ from __future__ import annotations
 import torch
 
 from . import (FLAG_KEEP_O32, FLAG_ORIGINAL_ORDER, FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size,
-               lsh_bucket_sort, lsh_gather, lsh_workspace_size, scfa_dense_bwd, scfa_dense_fwd, scfa_hash_bwd,
-               scfa_hash_fwd, scfa_qk_bwd, scfa_qk_fwd, workspace)
+               attn_workspace_size_live, lsh_bucket_sort, lsh_gather, lsh_workspace_size, scfa_dense_bwd,
+               scfa_dense_fwd, scfa_hash_bwd, scfa_hash_fwd, scfa_qk_bwd, scfa_qk_fwd, scfa_tiles_count, workspace)
+
+# Above this many bytes of worst-case live-tile lists (every tile pair), the
+# hash step sizes its lists for the live count of each batch instead.
+LIVE_SIZED_ABOVE = 256 << 20
 
 
 class Step:
@@ -40,7 +44,18 @@ class Step:
         self.dv = torch.empty((B, H, Tk, D), **bf)
         # one backward-sized workspace: the forward call builds the live-tile
         # list in it and the backward call reuses that list
-        self.ws_b = workspace(attn_workspace_size(mode, 1, B, H, Tq, Tk, D), dev)
+        self.device = dev
+        worst = attn_workspace_size(mode, 1, B, H, Tq, Tk, D)
+        fixed = attn_workspace_size_live(mode, 1, B, H, Tq, Tk, D, 0)
+        self.live_sized = mode == MODE_HASH and worst - fixed > LIVE_SIZED_ABOVE
+        if self.live_sized:
+            # lists sized per batch from its live-tile count (scfa_tiles_count)
+            self.ws_count = workspace(attn_workspace_size_live(mode, 0, B, H, Tq, Tk, D, 0), dev)
+            self.n_live = torch.zeros(1, dtype=torch.int32, device=dev)
+            self.list_cap = 0
+            self.ws_b = None
+        else:
+            self.ws_b = workspace(worst, dev)
         self.ws_f = self.ws_b
         if mode == MODE_HASH:
             T = Tq
@@ -97,6 +112,8 @@ class Step:
             lsh_gather(do, self.pq, self.do_s, main)
             tick("gather_do")
             main.wait_event(self.ev[1])
+            if self.live_sized:
+                self._size_lists(main)
             # O, dQ, dK, dV go straight to original row order (pq / pk map
             # sorted rows to original ones); LSE stays in sorted order
             fo = f | FLAG_ORIGINAL_ORDER
@@ -107,6 +124,21 @@ class Step:
                           self.kh, scale, self.dq, self.dk, self.dv, self.ws_b, fr | FLAG_ORIGINAL_ORDER, main)
             tick("bwd")
         return self
+
+
+    def _size_lists(self, stream):
+        """Count this batch's live tiles (reads one int back) and grow the
+        workspace if its lists cannot hold them (with an eighth to spare)."""
+        scfa_tiles_count(MODE_HASH, self.pq, self.pk, self.qh, self.kh, self.B, self.H, self.Tq, self.Tq,
+                         self.ws_count, self.n_live, stream)
+        stream.synchronize()
+        need = int(self.n_live.item())
+        if self.ws_b is None or need > self.list_cap:
+            self.list_cap = need + need // 8 + 1024
+            self.ws_b = None
+            self.ws_b = workspace(attn_workspace_size_live(MODE_HASH, 1, self.B, self.H, self.Tq, self.Tq, self.D,
+                                                           self.list_cap), self.device)
+            self.ws_f = self.ws_b
 
 
 class HostPipeline:

@@ -5,6 +5,8 @@ import os
 import re
 import subprocess
 
+import numpy as np
+
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -21,7 +23,7 @@ def scfa():
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "scfa.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\*?\s+\*?([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    names = re.findall(r"^\s*(?:const\s+)?(?:long\s+)?[A-Za-z_][A-Za-z0-9_]*\*?\s+\*?([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
     return sorted(set(names))
 
 
@@ -71,3 +73,41 @@ def test_workspace_sizes_grow_with_shape(scfa):
     assert 0 < a < b < c
     assert b - a >= 1000 * 64 * 4  # the fp32 dQ accumulator
     assert scfa.attn_workspace_size(scfa.MODE_QK, 0, 0, 1, 10, 10, 64) == 0
+
+
+@pytest.mark.parametrize("mode,B,H,T,D", [(0, 1, 2, 1000, 64), (1, 2, 3, 3000, 64), (2, 1, 3, 3000, 128),
+                                          (2, 1, 8, 1 << 16, 64), (1, 1, 1, 1 << 19, 64)])
+def test_workspace_capacity_is_exact_and_the_same_for_every_call(scfa, mode, B, H, T, D):
+    """Host arithmetic only. A workspace of scfa_attn_workspace_size_live(n)
+    bytes holds at least n list entries and one byte less holds fewer; the
+    layout depends on the size alone, so a forward and a backward on the
+    same workspace see the same lists; the worst-case sizes hold every tile
+    pair."""
+    n_t = (T + 127) // 128
+    max_live = B * H * n_t * n_t
+    cap = lambda kind, nbytes: scfa.attn_workspace_capacity(mode, kind, B, H, T, T, D, nbytes)
+    for kind in (0, 1):
+        worst = scfa.attn_workspace_size(mode, kind, B, H, T, T, D)
+        assert cap(kind, worst) == max_live
+        fixed = scfa.attn_workspace_size_live(mode, kind, B, H, T, T, D, 0)
+        assert cap(kind, fixed) >= 0 and cap(kind, fixed - 1) == -1
+        for n in sorted({x for x in (0, 1, 35, 36, 100, 326, 4095, 4096, max_live // 3, max_live - 1, max_live)
+                         if 0 <= x <= max_live}):
+            size = scfa.attn_workspace_size_live(mode, kind, B, H, T, T, D, n)
+            assert cap(kind, size) >= n, (kind, n)
+            if n > 0:
+                assert cap(kind, size - 1) < n, (kind, n)
+            for nbytes in (size - 1, size, size + 1000):
+                if cap(1, nbytes) >= 0:
+                    assert cap(0, nbytes) == cap(1, nbytes), (n, nbytes)
+        # more bytes never hold fewer entries, except where a forward-only
+        # workspace grows past the backward's fixed part and takes its layout
+        t1 = scfa.attn_workspace_size_live(mode, 1, B, H, T, T, D, 0)
+        for lo, hi in ((fixed, t1 - 1), (t1, worst + 4096)):
+            if hi <= lo:
+                continue
+            caps = [cap(kind, int(x)) for x in np.linspace(lo, hi, 257).astype(np.int64)]
+            assert all(a <= b for a, b in zip(caps, caps[1:]))
+    # a forward-only workspace never holds fewer lists than its size promises,
+    # also where it is large enough to take the backward's layout
+    assert scfa.attn_workspace_size(mode, 0, B, H, T, T, D) <= scfa.attn_workspace_size(mode, 1, B, H, T, T, D)

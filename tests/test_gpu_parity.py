@@ -238,6 +238,52 @@ def test_tiles_natural_order(scfa):
     np.testing.assert_array_equal(got["work_bwd"], np.arange(B * H * (T // 128)))
 
 
+def test_live_sized_workspace(scfa):
+    """Lists sized for the live count (scfa_tiles_count +
+    scfa_attn_workspace_size_live) give the same lists and the same results
+    as the worst-case workspace; one entry short, every list stays empty and
+    the status word says SCFA_ERR_WORKSPACE."""
+    B, H, T, D, nb = 1, 3, 3000, 64, 8
+    p = synth.make_problem(synth.Workload("ls", "hash", B, H, T, D, 150, n_buckets=nb))
+    from sparse_causal_flash_gb300.pipeline import Step
+    st = Step(scfa.MODE_HASH, B, H, T, T, D, n_buckets=nb)
+    st.run(p.q.cuda(), p.k.cuda(), p.v.cuda(), p.do.cuda(), p.wl.scale, R=p.R.cuda())
+    n_live = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wc = scfa.workspace(scfa.attn_workspace_size_live(scfa.MODE_HASH, 0, B, H, T, T, D, 0))
+    scfa.scfa_tiles_count(scfa.MODE_HASH, st.pq, st.pk, st.qh, st.kh, B, H, T, T, wc, n_live)
+    torch.cuda.synchronize()
+    nl = int(n_live.item())
+    ref = tiles.live_list("hash", B, H, T, T, st.pq.cpu().numpy(), st.pk.cpu().numpy(), st.qh.cpu().numpy(),
+                          st.kh.cpu().numpy())
+    assert nl == int(ref["row_ptr"][-1])
+    worst = scfa.attn_workspace_size(scfa.MODE_HASH, 1, B, H, T, T, D)
+    live = scfa.attn_workspace_size_live(scfa.MODE_HASH, 1, B, H, T, T, D, nl)
+    assert live < worst
+    e = lambda: torch.empty((B, H, T, D), dtype=torch.bfloat16, device="cuda")
+    flags = scfa.FLAG_ORIGINAL_ORDER | scfa.FLAG_KEEP_O32
+    outs = {}
+    # one byte short of the live size holds fewer than nl entries
+    assert scfa.attn_workspace_capacity(scfa.MODE_HASH, 1, B, H, T, T, D, live - 1) < nl
+    for name, size in (("worst", worst), ("live", live), ("short", live - 1)):
+        ws = scfa.workspace(size)
+        o, dq, dk, dv = e(), e(), e(), e()
+        lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+        scfa.scfa_hash_fwd(st.q_s, st.k_s, st.v_s, st.pq, st.pk, st.qh, st.kh, p.wl.scale, o, lse, ws, flags)
+        scfa.scfa_hash_bwd(st.q_s, st.k_s, st.v_s, o, lse, st.do_s, st.pq, st.pk, st.qh, st.kh, p.wl.scale,
+                           dq, dk, dv, ws, flags | scfa.FLAG_REUSE_TILES)
+        torch.cuda.synchronize()
+        outs[name] = (scfa.scfa_get_device_status(ws), o, lse, dk, dv, ws)
+    assert outs["worst"][0] == 0 and outs["live"][0] == 0
+    got = read_tiles(scfa, outs["live"][5], scfa.MODE_HASH, B, H, T, T, D)
+    for key in ("row_ptr", "cols", "fflags", "csc_ptr", "csc_rows", "cflags"):  # (no pair lists at D = 64)
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+    for i, name in ((1, "O"), (2, "LSE"), (3, "dK"), (4, "dV")):
+        assert torch.equal(outs["worst"][i], outs["live"][i]), name
+    assert outs["short"][0] == 3  # SCFA_ERR_WORKSPACE
+    tv = read_tiles(scfa, outs["short"][5], scfa.MODE_HASH, B, H, T, T, D)
+    assert not tv["row_ptr"].any() and not tv["csc_ptr"].any()
+
+
 @pytest.mark.parametrize("T", [1, 130, 1000])
 def test_tiles_dense_bitexact(scfa, T):
     ws = scfa.workspace(scfa.attn_workspace_size(scfa.MODE_DENSE, 1, 1, 2, T, T, 64))
@@ -311,6 +357,7 @@ def run_step(scfa, p, mode, flags=0):
            q_idx=None if p.q_idx is None else cuda(p.q_idx), k_idx=None if p.k_idx is None else cuda(p.k_idx),
            R=None if p.R is None else cuda(p.R))
     torch.cuda.synchronize()
+    assert scfa.STATUS.get(scfa.scfa_get_device_status(st.ws_b)) == "ok"
     return st
 
 
@@ -570,6 +617,11 @@ def test_full_hash_1m_sampled_buckets(scfa):
     p = synth.make_problem(wl)
     st = run_step(scfa, p, scfa.MODE_HASH)
     assert scfa.scfa_get_device_status(st.ws_b) == 0
+    # the lists are sized for the live tiles, not for every tile pair
+    assert st.live_sized
+    fixed = scfa.attn_workspace_size_live(scfa.MODE_HASH, 1, wl.B, wl.H, wl.T, wl.T, wl.D, 0)
+    assert st.ws_b.numel() - fixed < 64 << 20
+    assert scfa.attn_workspace_size(scfa.MODE_HASH, 1, wl.B, wl.H, wl.T, wl.T, wl.D) - fixed > 7e9
     h0 = 5
     q, k, v, do = (t[0, h0] for t in (p.q, p.k, p.v, p.do))
     R = p.R.double().numpy()
