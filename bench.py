@@ -82,20 +82,29 @@ def host_pairs_qk(prob) -> int:
 
 
 def host_pairs_hash(step) -> int:
-    """Admissible pairs of a hash-sparse step from its sorted view (host): per
-    bucket, the keys at or before each query's position."""
-    pq = step.pq.cpu().numpy().astype(np.int64)
-    pk = step.pk.cpu().numpy().astype(np.int64)
-    oq = step.offq.cpu().numpy().astype(np.int64)
-    ok = step.offk.cpu().numpy().astype(np.int64)
+    """Admissible pairs of a hash-sparse step (host): the (position, bucket)
+    of every token, read from the sorted arrays whatever their layout (rows
+    that name no token are skipped), then per bucket the keys at or before
+    each query's position."""
+    T = step.Tq
+    pq, qh = step.pq.cpu().numpy().astype(np.int64), step.qh.cpu().numpy().astype(np.int64)
+    pk, kh = step.pk.cpu().numpy().astype(np.int64), step.kh.cpu().numpy().astype(np.int64)
     total = 0
     for b in range(pq.shape[0]):
         for h in range(pq.shape[1]):
-            for c in range(oq.shape[2] - 1):
-                qpos = pq[b, h, oq[b, h, c]:oq[b, h, c + 1]]
-                kpos = pk[b, h, ok[b, h, c]:ok[b, h, c + 1]]
-                if len(qpos) and len(kpos):
-                    total += int(np.searchsorted(kpos, qpos, side="right").sum())
+            qi = (pq[b, h] >= 0) & (pq[b, h] < T)
+            ki = (pk[b, h] >= 0) & (pk[b, h] < T)
+            assert qi.sum() == T and ki.sum() == T
+            qb = np.empty(T, np.int64)
+            kb = np.empty(T, np.int64)
+            qb[pq[b, h][qi]] = qh[b, h][qi]
+            kb[pk[b, h][ki]] = kh[b, h][ki]
+            nb = int(max(qb.max(), kb.max())) + 1
+            kpos = [np.nonzero(kb == c)[0] for c in range(nb)]
+            for c in range(nb):
+                qpos = np.nonzero(qb == c)[0]
+                if len(qpos) and len(kpos[c]):
+                    total += int(np.searchsorted(kpos[c], qpos, side="right").sum())
     return total
 
 
@@ -116,21 +125,23 @@ def admissible_pairs(scfa, wl, prob, step, dev) -> int:
                               step.ws_b, count)
         host = host_pairs_qk(prob)
     else:
-        scfa.scfa_count_pairs(scfa.MODE_HASH, step.pq, step.pk, step.qh, step.kh, B, H, Tq, Tq, D, step.ws_b, count)
+        scfa.scfa_count_pairs(scfa.MODE_HASH, step.pq, step.pk, step.qh, step.kh, B, H, step.Ts, step.Ts, D,
+                              step.ws_b, count)
         host = host_pairs_hash(step)
     device = int(count.item())
     assert device == host, f"pair count: device {device} != host {host}"
     return device
 
 
-def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0) -> int:
+def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0, tiled: bool = True) -> int:
     """Library kernels launched per step (the library's own launch sequence)."""
-    tiles = 6 + (1 if D == 128 else 0)  # tile stats (q, k), count, scan, fill, work order (+ pair lists at D = 128)
+    # header init, tile stats (q, k), count, scan, fill, work order (+ pair lists at D = 128)
+    tiles = 7 + (1 if D == 128 else 0)
     attn = 1 + 3         # forward; backward pre-pass, backward, dQ finalise
     if mode == "hash":
         m = n_buckets // 2
         lsh = 2 if (D in (64, 128) and m % 8 == 0 and 8 <= m <= 256) else 1  # tensor-core pass + certified pass
-        sort = 3 if T > 8192 else 1                                          # chunk counts, scan, scatter
+        sort = (3 if T > 8192 else 1) + (2 if tiled else 0)  # chunk counts, scan, scatter; bucket starts, spread
         return tiles + attn + 2 * (lsh + sort + 1) + 2   # per q / k: hash, sort, gather; gather V / dO
     return tiles + attn
 
@@ -499,7 +510,8 @@ class Runner:
                 # the pages' naive baselines ("实验与结果", Fig. 3 and 7): every
                 # tile computed with the element mask (hash: the full T x T
                 # matrix then the mask; QK: the whole compacted rectangle)
-                nstep = Step(mode, B, H, Tq, Tk, D, n_buckets=wl.n_buckets, device=dev, flags=scfa.FLAG_NO_PRUNE)
+                nstep = Step(mode, B, H, Tq, Tk, D, n_buckets=wl.n_buckets, device=dev, flags=scfa.FLAG_NO_PRUNE,
+                             tiled=False)
                 nrun = lambda: nstep.run(*args_, wl.scale, **kw)
                 nrun()
                 nk = max(3, steps // 4)
@@ -515,10 +527,20 @@ class Runner:
             if wl.mode == "hash":
                 # bucket-collision coverage (Fig. 4): SCFA's live tiles vs a
                 # Reformer-style chunked attention over the same sort
+                # (Reformer chunks the plain sorted sequence: sorted again here
+                # without the tile-aligned padding)
                 cnt = torch.zeros(1, dtype=torch.int64, device=dev)
                 cov = {"scfa_live_tiles": 1.0}
+                i32 = dict(dtype=torch.int32, device=dev)
+                plain = {}
+                for side, x in (("q", prob.q), ("k", prob.k)):
+                    hs, pm = torch.empty((B, H, Tq), **i32), torch.empty((B, H, Tq), **i32)
+                    off = torch.empty((B, H, wl.n_buckets + 1), **i32)
+                    wsl = scfa.workspace(scfa.lsh_workspace_size(B, H, Tq, wl.n_buckets), dev)
+                    scfa.lsh_bucket_sort(x.to(dev), kw["R"], wl.n_buckets, hs, pm, off, None, wsl)
+                    plain[side] = (hs, pm)
                 for c in REFORMER_CHUNKS:
-                    scfa.scfa_count_chunked_pairs(step.pq, step.pk, step.qh, step.kh, c, cnt)
+                    scfa.scfa_count_chunked_pairs(plain["q"][1], plain["k"][1], plain["q"][0], plain["k"][0], c, cnt)
                     cov[f"reformer_chunk{c}"] = int(cnt.item()) / pairs
                 rec["coverage"] = cov
         keep = (step, args_, kw, prob) if e2e_steps else None

@@ -88,9 +88,10 @@ enum {
                                  in ORIGINAL row order: sorted query row s of
                                  head (b,h) is row q_idx[b,h,s] of o and dq,
                                  sorted key row s is row k_idx[b,h,s] of dk and
-                                 dv (q_idx / k_idx must then be permutations of
-                                 [0, T) per head; rows whose index falls outside
-                                 [0, T) are not written, and read as zero).
+                                 dv (within each head, the q_idx / k_idx that
+                                 fall in [0, T_orig) must be distinct; rows
+                                 whose index falls outside are not written,
+                                 and read as zero).
                                  q, k, v, do, lse stay in sorted order. This
                                  replaces the lsh_unsort passes. */
   SCFA_FLAG_KEEP_O32 = 32,       /* forward: also store O in fp32 in the
@@ -199,21 +200,25 @@ scfa_status scfa_qk_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
  * k_s, v_s, dk_s, dv_s the key order. q_idx / k_idx [B,H,T] are the original
  * positions of the sorted rows (the perm of lsh_bucket_sort) and q_hash /
  * k_hash [B,H,T] their bucket ids, non-decreasing within each (b,h).
+ * T is the row count per head of the sorted tensors; T_orig that of the
+ * original-order tensors (T_orig <= T; equal to T unless the sorted layout
+ * has padding rows, as lsh_bucket_sort_tiled's does).
  * Put results back in original order with lsh_unsort, or pass
  * SCFA_FLAG_ORIGINAL_ORDER to have the kernels write o / dq / dk / dv (and
- * read o) in original order directly. D = 64 or 128.
+ * read o) in original order directly, as [B,H,T_orig,D] tensors. Without
+ * that flag T_orig must equal T. D = 64 or 128.
  * ------------------------------------------------------------------------- */
 scfa_status scfa_hash_fwd(const uint16_t* q_s, const uint16_t* k_s, const uint16_t* v_s,
                           const int32_t* q_idx, const int32_t* k_idx,
                           const int32_t* q_hash, const int32_t* k_hash,
-                          int B, int H, int T, int D, float scale,
+                          int B, int H, int T, int T_orig, int D, float scale,
                           uint16_t* o_s, float* lse_s,
                           void* ws, size_t ws_bytes, unsigned flags, void* stream);
 scfa_status scfa_hash_bwd(const uint16_t* q_s, const uint16_t* k_s, const uint16_t* v_s,
                           const uint16_t* o_s, const float* lse_s, const uint16_t* do_s,
                           const int32_t* q_idx, const int32_t* k_idx,
                           const int32_t* q_hash, const int32_t* k_hash,
-                          int B, int H, int T, int D, float scale,
+                          int B, int H, int T, int T_orig, int D, float scale,
                           uint16_t* dq_s, uint16_t* dk_s, uint16_t* dv_s,
                           void* ws, size_t ws_bytes, unsigned flags, void* stream);
 
@@ -233,9 +238,26 @@ scfa_status scfa_hash_bwd(const uint16_t* q_s, const uint16_t* k_s, const uint16
  *   [B,H,n_buckets+1]: number of tokens with a smaller bucket id; x_sorted
  *   (nullable) [B,H,T,D] = x gathered by perm. Workspace:
  *   lsh_workspace_size.
- * lsh_gather: x_sorted[b,h,s,:] = x[b,h,perm[b,h,s],:].
+ * lsh_bucket_sort_tiled: the same order, laid out so that every bucket
+ *   starts on a multiple of 128 rows (the attention tile height): no tile then
+ *   holds two buckets, so far fewer (query tile, key tile) pairs stay live.
+ *   Bucket b's n_b rows start at bucket_start[b,h,b] = the sum over c < b of
+ *   n_c rounded up to a multiple of 128; bucket_start[b,h,n_buckets] is where
+ *   the last bucket's tiles end. The rows between a bucket's n_b rows and its
+ *   next multiple of 128, and all rows after the last bucket up to T_sorted,
+ *   are padding: perm = pad, hash_sorted = the bucket's id (n_buckets - 1
+ *   after the last bucket) and x_sorted a zero row. pad must lie outside
+ *   [0, T): pass -1 for queries (a query row that sees no key) and INT32_MAX
+ *   for keys (a key row no query sees), the QK-mode sentinels. perm,
+ *   hash_sorted [B,H,T_sorted]; x_sorted [B,H,T_sorted,D];
+ *   T_sorted >= scfa_tiled_rows(T, n_buckets), the largest such layout
+ *   (T + 127 per non-empty bucket, rounded up to 128). Same workspace as
+ *   lsh_bucket_sort.
+ * lsh_gather: x_sorted[b,h,s,:] = x[b,h,perm[b,h,s],:] for the T_sorted rows
+ *   s of each head (x has T rows per head); a zero row where perm[b,h,s] is
+ *   outside [0, T).
  * lsh_unsort: y[b,h,perm[b,h,s],:] = y_sorted[b,h,s,:]. Rows whose perm entry
- *   is out of [0, T) are skipped.
+ *   is out of [0, T) are skipped. Pass T_sorted = T for the plain layout.
  * ------------------------------------------------------------------------- */
 size_t lsh_workspace_size(int B, int H, int T, int n_buckets);
 scfa_status lsh_hash(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D,
@@ -244,10 +266,15 @@ scfa_status lsh_bucket_sort(const uint16_t* x, const uint16_t* R, int B, int H, 
                             int n_buckets, int32_t* hash_sorted, int32_t* perm,
                             int32_t* bucket_off, uint16_t* x_sorted,
                             void* ws, size_t ws_bytes, unsigned flags, void* stream);
-scfa_status lsh_gather(const uint16_t* x, const int32_t* perm, int B, int H, int T, int D,
-                       uint16_t* x_sorted, void* stream);
-scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int H, int T, int D,
-                       uint16_t* y, void* stream);
+int scfa_tiled_rows(int T, int n_buckets);
+scfa_status lsh_bucket_sort_tiled(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D,
+                                  int n_buckets, int T_sorted, int32_t pad, int32_t* hash_sorted,
+                                  int32_t* perm, int32_t* bucket_start, uint16_t* x_sorted,
+                                  void* ws, size_t ws_bytes, unsigned flags, void* stream);
+scfa_status lsh_gather(const uint16_t* x, const int32_t* perm, int B, int H, int T, int T_sorted,
+                       int D, uint16_t* x_sorted, void* stream);
+scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int H, int T, int T_sorted,
+                       int D, uint16_t* y, void* stream);
 
 /* ----------------------------------------------------------------------------
  * Tile metadata and the live-tile work list (page section "SCFA 解决方案":

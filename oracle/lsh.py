@@ -16,6 +16,11 @@ Readings:
     x is a positive scaling, which leaves the exact argmax unchanged, so it is
     not applied. A zero vector gets bucket 0.
   * The sort is stable: key (bucket, original position).
+  * Tile-aligned layout (tile_aligned): the same sorted order with each
+    bucket starting on a multiple of the attention tile height, the gaps
+    filled with padding rows that name no token. The page sorts by bucket
+    but leaves the row layout open; padding keeps every tile inside one
+    bucket, so no tile pair straddles two buckets.
 """
 from __future__ import annotations
 
@@ -104,9 +109,46 @@ def bucket_sort(h, n_buckets: int):
     return perm, h[perm].astype(np.int32), off
 
 
+def tile_aligned(perm, bucket_off, n_rows: int, tile: int, pad: int):
+    """One head's sorted order re-laid so that every bucket starts on a
+    multiple of `tile` rows.
+
+    Bucket b (n_b = bucket_off[b+1] - bucket_off[b] tokens, in their sorted
+    order) occupies rows start[b] .. start[b] + n_b - 1, where start[0] = 0 and
+    start[b+1] = start[b] + n_b rounded up to a multiple of tile. Every other
+    row up to n_rows is padding: position `pad`, and the bucket id of the
+    rows around it (bucket n_buckets - 1 after the last bucket). Returns
+    (perm_t, h_t, start) with start of length n_buckets + 1.
+    """
+    off = np.asarray(bucket_off, dtype=np.int64)
+    nb = len(off) - 1
+    start = np.zeros(nb + 1, dtype=np.int64)
+    for b in range(nb):
+        n_b = off[b + 1] - off[b]
+        start[b + 1] = start[b] + -(-n_b // tile) * tile
+    assert start[nb] <= n_rows
+    perm_t = np.full(n_rows, pad, dtype=np.int64)
+    h_t = np.full(n_rows, nb - 1, dtype=np.int64)
+    for b in range(nb):
+        n_b = off[b + 1] - off[b]
+        h_t[start[b]:start[b + 1]] = b
+        perm_t[start[b]:start[b] + n_b] = np.asarray(perm)[off[b]:off[b + 1]]
+    return perm_t.astype(np.int32), h_t.astype(np.int32), start.astype(np.int32)
+
+
 def gather_rows(x, perm):
     """x_sorted[s] = x[perm[s]] (row copy)."""
     return np.asarray(x)[np.asarray(perm, dtype=np.int64)]
+
+
+def gather_rows_padded(x, perm):
+    """x_sorted[s] = x[perm[s]], a zero row where perm[s] names no row."""
+    x = np.asarray(x)
+    perm = np.asarray(perm, dtype=np.int64)
+    inside = (perm >= 0) & (perm < x.shape[0])
+    out = np.zeros((perm.shape[0],) + x.shape[1:], dtype=x.dtype)
+    out[inside] = x[perm[inside]]
+    return out
 
 
 def unsort_rows(y_sorted, perm):

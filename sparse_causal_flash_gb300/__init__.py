@@ -48,13 +48,16 @@ _SIGS = {
     "scfa_dense_bwd": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _S, _U, _P], _I),
     "scfa_qk_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _U, _P], _I),
     "scfa_qk_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _S, _U, _P], _I),
-    "scfa_hash_fwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _S, _U, _P], _I),
-    "scfa_hash_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _S, _U, _P], _I),
+    "scfa_hash_fwd": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _S, _U, _P], _I),
+    "scfa_hash_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _S, _U, _P],
+                      _I),
     "lsh_workspace_size": ([_I, _I, _I, _I], _S),
     "lsh_hash": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "lsh_bucket_sort": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _U, _P], _I),
-    "lsh_gather": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
-    "lsh_unsort": ([_P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "scfa_tiled_rows": ([_I, _I], _I),
+    "lsh_bucket_sort_tiled": ([_P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P, _P, _S, _U, _P], _I),
+    "lsh_gather": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "lsh_unsort": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "scfa_tiles": ([_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _U, _P], _I),
     "scfa_tile_view_get": ([_P, _I, _I, _I, _I, _I, _I, _P], _I),
     "scfa_get_device_status": ([_P, _P], _I),
@@ -184,19 +187,22 @@ def scfa_qk_bwd(q, k, v, o, lse, do, q_idx, k_idx, scale, dq, dk, dv, ws, flags=
 
 
 def scfa_hash_fwd(q_s, k_s, v_s, q_idx, k_idx, q_hash, k_hash, scale, o_s, lse_s, ws, flags=0, stream=None):
+    """o_s: [B,H,T,D] in sorted order, or [B,H,T_orig,D] in original order
+    with FLAG_ORIGINAL_ORDER (its row count is passed as T_orig)."""
     B, H, T, D = q_s.shape
     _check("scfa_hash_fwd", _lib.scfa_hash_fwd(_ptr(q_s), _ptr(k_s), _ptr(v_s), _ptr(q_idx), _ptr(k_idx),
-                                               _ptr(q_hash), _ptr(k_hash), B, H, T, D, scale, _ptr(o_s), _ptr(lse_s),
-                                               _ptr(ws), ws.numel(), flags, _stream(stream)))
+                                               _ptr(q_hash), _ptr(k_hash), B, H, T, o_s.shape[2], D, scale,
+                                               _ptr(o_s), _ptr(lse_s), _ptr(ws), ws.numel(), flags,
+                                               _stream(stream)))
 
 
 def scfa_hash_bwd(q_s, k_s, v_s, o_s, lse_s, do_s, q_idx, k_idx, q_hash, k_hash, scale, dq_s, dk_s, dv_s, ws,
                   flags=0, stream=None):
     B, H, T, D = q_s.shape
     _check("scfa_hash_bwd", _lib.scfa_hash_bwd(_ptr(q_s), _ptr(k_s), _ptr(v_s), _ptr(o_s), _ptr(lse_s), _ptr(do_s),
-                                               _ptr(q_idx), _ptr(k_idx), _ptr(q_hash), _ptr(k_hash), B, H, T, D,
-                                               scale, _ptr(dq_s), _ptr(dk_s), _ptr(dv_s), _ptr(ws), ws.numel(),
-                                               flags, _stream(stream)))
+                                               _ptr(q_idx), _ptr(k_idx), _ptr(q_hash), _ptr(k_hash), B, H, T,
+                                               dq_s.shape[2], D, scale, _ptr(dq_s), _ptr(dk_s), _ptr(dv_s),
+                                               _ptr(ws), ws.numel(), flags, _stream(stream)))
 
 
 # ---------------------------------------------------------------- LSH / sort / gather
@@ -212,14 +218,34 @@ def lsh_bucket_sort(x, R, n_buckets, hash_sorted, perm, bucket_off, x_sorted, ws
                                                    ws.numel(), flags, _stream(stream)))
 
 
-def lsh_gather(x, perm, x_sorted, stream=None):
+def scfa_tiled_rows(T, n_buckets) -> int:
+    """Rows per head of the tile-aligned sorted layout (lsh_bucket_sort_tiled)."""
+    return int(_lib.scfa_tiled_rows(int(T), int(n_buckets)))
+
+
+def lsh_bucket_sort_tiled(x, R, n_buckets, pad, hash_sorted, perm, bucket_start, x_sorted, ws, flags=0,
+                          stream=None):
+    """Bucket sort with every bucket starting on a 128-row boundary; perm,
+    hash_sorted [B,H,T_sorted], bucket_start [B,H,n_buckets+1], x_sorted
+    [B,H,T_sorted,D] or None. pad: the perm value of padding rows (-1 for
+    queries, 2**31 - 1 for keys)."""
     B, H, T, D = x.shape
-    _check("lsh_gather", _lib.lsh_gather(_ptr(x), _ptr(perm), B, H, T, D, _ptr(x_sorted), _stream(stream)))
+    _check("lsh_bucket_sort_tiled", _lib.lsh_bucket_sort_tiled(
+        _ptr(x), _ptr(R), B, H, T, D, n_buckets, perm.shape[2], int(pad), _ptr(hash_sorted), _ptr(perm),
+        _ptr(bucket_start), _ptr(x_sorted), _ptr(ws), ws.numel(), flags, _stream(stream)))
+
+
+def lsh_gather(x, perm, x_sorted, stream=None):
+    """x_sorted[b,h,s] = x[b,h,perm[b,h,s]] (a zero row where perm is outside [0, T))."""
+    B, H, T, D = x.shape
+    _check("lsh_gather", _lib.lsh_gather(_ptr(x), _ptr(perm), B, H, T, x_sorted.shape[2], D, _ptr(x_sorted),
+                                         _stream(stream)))
 
 
 def lsh_unsort(y_sorted, perm, y, stream=None):
-    B, H, T, D = y_sorted.shape
-    _check("lsh_unsort", _lib.lsh_unsort(_ptr(y_sorted), _ptr(perm), B, H, T, D, _ptr(y), _stream(stream)))
+    B, H, T, D = y.shape
+    _check("lsh_unsort", _lib.lsh_unsort(_ptr(y_sorted), _ptr(perm), B, H, T, y_sorted.shape[2], D, _ptr(y),
+                                         _stream(stream)))
 
 
 # ---------------------------------------------------------------- tiles

@@ -168,6 +168,12 @@ bool lsh_ws_layout(int B, int H, int T, int n_buckets, LshWs* L) {
     const size_t chunks = (static_cast<size_t>(T) + kSortChunk - 1) / kSortChunk;
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * H * chunks * n_buckets, 256);
   }
+  w.perm_u = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * H * T, 256);
+  w.hs_u = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * H * T, 256);
+  w.off_u = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(B) * H * (n_buckets + 1), 256);
   w.total = off;
   *L = w;
   return true;
@@ -196,7 +202,7 @@ inline scfa_status finish(cudaError_t e, unsigned flags, cudaStream_t st) {
 scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                           const uint16_t* o_in, const float* lse_in, const uint16_t* do_,
                           const int32_t* q_idx, const int32_t* k_idx, const int32_t* q_hash, const int32_t* k_hash,
-                          int B, int H, int Tq, int Tk, int D, float scale,
+                          int B, int H, int Tq, int Tk, int To, int D, float scale,
                           uint16_t* o, float* lse, uint16_t* dq, uint16_t* dk, uint16_t* dv,
                           void* ws, size_t ws_bytes, unsigned flags, void* stream) {
   if (!q || !k || !v || !ws) return SCFA_ERR_INVALID;
@@ -207,6 +213,9 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   if (mode != SCFA_MODE_DENSE && (!q_idx || !k_idx)) return SCFA_ERR_INVALID;
   if (mode == SCFA_MODE_HASH && (!q_hash || !k_hash)) return SCFA_ERR_INVALID;
   if ((flags & SCFA_FLAG_ORIGINAL_ORDER) && (mode != SCFA_MODE_HASH || Tq != Tk)) return SCFA_ERR_INVALID;
+  // original-order tensors have To rows per head (at most the sorted count);
+  // without a row map they are the sorted tensors themselves
+  if ((flags & SCFA_FLAG_ORIGINAL_ORDER) ? (To < 1 || To > Tq) : To != Tq) return SCFA_ERR_INVALID;
   if (!backward) {
     if (!o || !lse || !aligned16(o)) return SCFA_ERR_INVALID;
   } else {
@@ -232,7 +241,7 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
     if (e != cudaSuccess) return SCFA_ERR_CUDA;
   }
   if (flags & SCFA_FLAG_VALIDATE) {
-    e = launch_validate(mode, (flags & SCFA_FLAG_ORIGINAL_ORDER) != 0, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, w,
+    e = launch_validate(mode, (flags & SCFA_FLAG_ORIGINAL_ORDER) != 0, q_idx, k_idx, q_hash, k_hash, B, H, Tq, Tk, To, w,
                         L, st);
     if (e != cudaSuccess) return SCFA_ERR_CUDA;
   }
@@ -262,6 +271,7 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   const bool original = (flags & SCFA_FLAG_ORIGINAL_ORDER) != 0;
   a.q_rows = original ? q_idx : nullptr;
   a.k_rows = original ? k_idx : nullptr;
+  a.To = To;
   a.o32 = keep_o32 ? reinterpret_cast<float*>(w + L.dq_acc) : nullptr;
   a.stall = (flags & SCFA_FLAG_DEBUG_STALL) ? 1 : 0;
   a.ws = w;
@@ -306,7 +316,8 @@ scfa_status scfa_dense_fwd(const uint16_t* q, const uint16_t* k, const uint16_t*
                            float scale, uint16_t* o, float* lse, void* ws, size_t ws_bytes, unsigned flags,
                            void* stream) {
   return run_attention(SCFA_MODE_DENSE, false, q, k, v, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                       nullptr, B, H, T, T, D, scale, o, lse, nullptr, nullptr, nullptr, ws, ws_bytes, flags, stream);
+                       nullptr, B, H, T, T, T, D, scale, o, lse, nullptr, nullptr, nullptr, ws, ws_bytes, flags,
+                       stream);
 }
 
 scfa_status scfa_dense_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o,
@@ -314,40 +325,40 @@ scfa_status scfa_dense_bwd(const uint16_t* q, const uint16_t* k, const uint16_t*
                            uint16_t* dq, uint16_t* dk, uint16_t* dv, void* ws, size_t ws_bytes, unsigned flags,
                            void* stream) {
   return run_attention(SCFA_MODE_DENSE, true, q, k, v, o, lse, do_, nullptr, nullptr, nullptr, nullptr, B, H, T,
-                       T, D, scale, nullptr, nullptr, dq, dk, dv, ws, ws_bytes, flags, stream);
+                       T, T, D, scale, nullptr, nullptr, dq, dk, dv, ws, ws_bytes, flags, stream);
 }
 
 scfa_status scfa_qk_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* q_idx,
                         const int32_t* k_idx, int B, int H, int Tq, int Tk, int D, float scale, uint16_t* o,
                         float* lse, void* ws, size_t ws_bytes, unsigned flags, void* stream) {
   return run_attention(SCFA_MODE_QK, false, q, k, v, nullptr, nullptr, nullptr, q_idx, k_idx, nullptr, nullptr, B,
-                       H, Tq, Tk, D, scale, o, lse, nullptr, nullptr, nullptr, ws, ws_bytes, flags, stream);
+                       H, Tq, Tk, Tq, D, scale, o, lse, nullptr, nullptr, nullptr, ws, ws_bytes, flags, stream);
 }
 
 scfa_status scfa_qk_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o,
                         const float* lse, const uint16_t* do_, const int32_t* q_idx, const int32_t* k_idx, int B,
                         int H, int Tq, int Tk, int D, float scale, uint16_t* dq, uint16_t* dk, uint16_t* dv,
                         void* ws, size_t ws_bytes, unsigned flags, void* stream) {
-  return run_attention(SCFA_MODE_QK, true, q, k, v, o, lse, do_, q_idx, k_idx, nullptr, nullptr, B, H, Tq, Tk, D,
-                       scale, nullptr, nullptr, dq, dk, dv, ws, ws_bytes, flags, stream);
+  return run_attention(SCFA_MODE_QK, true, q, k, v, o, lse, do_, q_idx, k_idx, nullptr, nullptr, B, H, Tq, Tk, Tq,
+                       D, scale, nullptr, nullptr, dq, dk, dv, ws, ws_bytes, flags, stream);
 }
 
 scfa_status scfa_hash_fwd(const uint16_t* q_s, const uint16_t* k_s, const uint16_t* v_s, const int32_t* q_idx,
                           const int32_t* k_idx, const int32_t* q_hash, const int32_t* k_hash, int B, int H, int T,
-                          int D, float scale, uint16_t* o_s, float* lse_s, void* ws, size_t ws_bytes,
+                          int T_orig, int D, float scale, uint16_t* o_s, float* lse_s, void* ws, size_t ws_bytes,
                           unsigned flags, void* stream) {
   return run_attention(SCFA_MODE_HASH, false, q_s, k_s, v_s, nullptr, nullptr, nullptr, q_idx, k_idx, q_hash,
-                       k_hash, B, H, T, T, D, scale, o_s, lse_s, nullptr, nullptr, nullptr, ws, ws_bytes, flags,
-                       stream);
+                       k_hash, B, H, T, T, T_orig, D, scale, o_s, lse_s, nullptr, nullptr, nullptr, ws, ws_bytes,
+                       flags, stream);
 }
 
 scfa_status scfa_hash_bwd(const uint16_t* q_s, const uint16_t* k_s, const uint16_t* v_s, const uint16_t* o_s,
                           const float* lse_s, const uint16_t* do_s, const int32_t* q_idx, const int32_t* k_idx,
-                          const int32_t* q_hash, const int32_t* k_hash, int B, int H, int T, int D, float scale,
-                          uint16_t* dq_s, uint16_t* dk_s, uint16_t* dv_s, void* ws, size_t ws_bytes,
+                          const int32_t* q_hash, const int32_t* k_hash, int B, int H, int T, int T_orig, int D,
+                          float scale, uint16_t* dq_s, uint16_t* dk_s, uint16_t* dv_s, void* ws, size_t ws_bytes,
                           unsigned flags, void* stream) {
   return run_attention(SCFA_MODE_HASH, true, q_s, k_s, v_s, o_s, lse_s, do_s, q_idx, k_idx, q_hash, k_hash, B, H,
-                       T, T, D, scale, nullptr, nullptr, dq_s, dk_s, dv_s, ws, ws_bytes, flags, stream);
+                       T, T, T_orig, D, scale, nullptr, nullptr, dq_s, dk_s, dv_s, ws, ws_bytes, flags, stream);
 }
 
 size_t lsh_workspace_size(int B, int H, int T, int n_buckets) {
@@ -399,25 +410,66 @@ scfa_status lsh_bucket_sort(const uint16_t* x, const uint16_t* R, int B, int H, 
   if (e == cudaSuccess)
     e = launch_bucket_sort(hash, B * H, T, n_buckets, perm, hash_sorted, bucket_off,
                            reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.chunk), st);
-  if (e == cudaSuccess && x_sorted) e = launch_gather(x, perm, B * H, T, D, x_sorted, false, st);
+  if (e == cudaSuccess && x_sorted) e = launch_gather(x, perm, B * H, T, T, D, x_sorted, false, st);
   return finish(e, flags, st);
 }
 
-scfa_status lsh_gather(const uint16_t* x, const int32_t* perm, int B, int H, int T, int D, uint16_t* x_sorted,
-                       void* stream) {
-  if (!x || !perm || !x_sorted || B < 1 || H < 1 || T < 1) return SCFA_ERR_INVALID;
-  if (D < 8 || (D % 8) != 0) return SCFA_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(x_sorted)) return SCFA_ERR_INVALID;
-  return finish(launch_gather(x, perm, B * H, T, D, x_sorted, false, static_cast<cudaStream_t>(stream)), 0,
-                nullptr);
+int scfa_tiled_rows(int T, int n_buckets) {
+  if (T < 1 || n_buckets < 1) return -1;
+  // every non-empty bucket rounds up by less than one tile
+  const long long nb = n_buckets < T ? n_buckets : T;
+  const long long rows = (static_cast<long long>(T) + nb * (kTile - 1) + kTile - 1) / kTile * kTile;
+  return rows > INT_MAX ? -1 : static_cast<int>(rows);
 }
 
-scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int H, int T, int D, uint16_t* y,
-                       void* stream) {
-  if (!y_sorted || !perm || !y || B < 1 || H < 1 || T < 1) return SCFA_ERR_INVALID;
+scfa_status lsh_bucket_sort_tiled(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D, int n_buckets,
+                                  int T_sorted, int32_t pad, int32_t* hash_sorted, int32_t* perm,
+                                  int32_t* bucket_start, uint16_t* x_sorted, void* ws, size_t ws_bytes,
+                                  unsigned flags, void* stream) {
+  scfa_status s = check_lsh_args(x, R, B, H, T, D, n_buckets);
+  if (s != SCFA_OK) return s;
+  if (!hash_sorted || !perm || !bucket_start || !ws) return SCFA_ERR_INVALID;
+  if (x_sorted && !aligned16(x_sorted)) return SCFA_ERR_INVALID;
+  const int need = scfa_tiled_rows(T, n_buckets);
+  if (need < 0 || T_sorted < need) return SCFA_ERR_INVALID;
+  if (pad >= 0 && pad < T) return SCFA_ERR_INVALID;  // a padding row must not name a real row
+  if ((static_cast<size_t>(D) * ((n_buckets / 2 + 3) & ~3) + 256u * (D / 2 + 1)) * sizeof(float) > 200 * 1024)
+    return SCFA_ERR_UNSUPPORTED;
+  LshWs L;
+  if (!lsh_ws_layout(B, H, T, n_buckets, &L)) return SCFA_ERR_INVALID;
+  if (!aligned256(ws) || ws_bytes < L.total) return SCFA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  int32_t* hash = reinterpret_cast<int32_t*>(w + L.hash);
+  int32_t* perm_u = reinterpret_cast<int32_t*>(w + L.perm_u);
+  int32_t* off_u = reinterpret_cast<int32_t*>(w + L.off_u);
+  const long long rows = static_cast<long long>(B) * H * T;
+  cudaError_t e = launch_lsh_hash(x, R, rows, D, n_buckets / 2, hash, reinterpret_cast<int*>(w + L.header), st);
+  if (e == cudaSuccess)
+    e = launch_bucket_sort(hash, B * H, T, n_buckets, perm_u, reinterpret_cast<int32_t*>(w + L.hs_u), off_u,
+                           reinterpret_cast<int32_t*>(w + L.chunk), st);
+  if (e == cudaSuccess)
+    e = launch_tiled_layout(perm_u, off_u, B * H, T, T_sorted, n_buckets, pad, perm, hash_sorted, bucket_start, st);
+  if (e == cudaSuccess && x_sorted) e = launch_gather(x, perm, B * H, T_sorted, T, D, x_sorted, false, st);
+  return finish(e, flags, st);
+}
+
+scfa_status lsh_gather(const uint16_t* x, const int32_t* perm, int B, int H, int T, int T_sorted, int D,
+                       uint16_t* x_sorted, void* stream) {
+  if (!x || !perm || !x_sorted || B < 1 || H < 1 || T < 1 || T_sorted < T) return SCFA_ERR_INVALID;
+  if (D < 8 || (D % 8) != 0) return SCFA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(x_sorted)) return SCFA_ERR_INVALID;
+  return finish(launch_gather(x, perm, B * H, T_sorted, T, D, x_sorted, false, static_cast<cudaStream_t>(stream)),
+                0, nullptr);
+}
+
+scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int H, int T, int T_sorted, int D,
+                       uint16_t* y, void* stream) {
+  if (!y_sorted || !perm || !y || B < 1 || H < 1 || T < 1 || T_sorted < T) return SCFA_ERR_INVALID;
   if (D < 8 || (D % 8) != 0) return SCFA_ERR_UNSUPPORTED;
   if (!aligned16(y_sorted) || !aligned16(y)) return SCFA_ERR_INVALID;
-  return finish(launch_gather(y_sorted, perm, B * H, T, D, y, true, static_cast<cudaStream_t>(stream)), 0, nullptr);
+  return finish(launch_gather(y_sorted, perm, B * H, T_sorted, T, D, y, true, static_cast<cudaStream_t>(stream)), 0,
+                nullptr);
 }
 
 scfa_status scfa_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx, const int32_t* q_hash,

@@ -100,6 +100,7 @@ struct BwdParams {
   uint16_t* dk;
   uint16_t* dv;
   const int32_t* k_rows;  // null, or the original row of each sorted key row
+  int To;                 // rows per head of dk / dv when k_rows is set
   int stall;   // SCFA_FLAG_DEBUG_STALL: withhold the first K / V load
   int* sched;  // [0] next work item, [1] CTAs done
   int* status;
@@ -375,10 +376,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const bool kvalid = key < p.Tk;
       const long long gk = static_cast<long long>(bh) * p.Tk + key;
       // dK / dV row within the head (-1: not written)
-      const int kro = !kvalid ? -1 : (p.k_rows == nullptr ? key : p.k_rows[gk]);
+      const long long gko = kvalid ? mapped_row(p.k_rows, gk, bh, p.To) : -1;
       if (n == 0) {
-        if (kro >= 0 && kro < p.Tk) {
-          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + (gk - key + kro) * D + 64 * hh);
+        if (gko >= 0) {
+          uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + gko * D + 64 * hh);
 #pragma unroll
           for (int c = 0; c < 8; ++c) a[c] = make_uint4(0, 0, 0, 0);
         }
@@ -506,8 +507,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tmem_ld_fence(acc[1]);
       tc_fence_before();
       mbar_arrive(&sm.dkv_empty);
-      if (kro >= 0 && kro < p.Tk)
-        store_row_bf16((grp == 0 ? p.dv : p.dk) + (gk - key + kro) * D + 64 * hh, &acc[0][0], 64);
+      if (gko >= 0)
+        store_row_bf16((grp == 0 ? p.dv : p.dk) + gko * D + 64 * hh, &acc[0][0], 64);
       ++item;
     }
   } else {
@@ -855,7 +856,7 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const int key = j * kTile + kr;
       const bool kvalid = key < p.Tk;
       const long long gk = static_cast<long long>(bh) * p.Tk + key;
-      const long long gko = kvalid ? mapped_row(p.k_rows, gk, key, p.Tk) : -1;  // dK / dV row
+      const long long gko = kvalid ? mapped_row(p.k_rows, gk, bh, p.To) : -1;  // dK / dV row
       if (n == 0) {
         if (gko >= 0) {
           uint4* a = reinterpret_cast<uint4*>((grp == 0 ? p.dv : p.dk) + gko * D);
@@ -1094,6 +1095,7 @@ struct PreParams {
   const uint16_t* dO;
   const float* o32;
   const int32_t* o_rows;
+  int To;             // rows per head of o when o_rows is set
   const float* lse;
   const int32_t* q_idx;
   const int32_t* q_hash;
@@ -1134,7 +1136,7 @@ __global__ void bwd_pre_kernel(const PreParams p) {
         }
       } else {
         // O may be stored in original row order (o_rows maps sorted -> original)
-        const long long orow = mapped_row(p.o_rows, row, r, p.Tq);
+        const long long orow = mapped_row(p.o_rows, row, bh, p.To);
         const uint4 a = orow >= 0 ? reinterpret_cast<const uint4*>(p.o + orow * D)[ch] : make_uint4(0, 0, 0, 0);
         const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
@@ -1170,14 +1172,14 @@ __global__ void bwd_pre_kernel(const PreParams p) {
 }
 
 __global__ void dq_finalize_kernel(const float* __restrict__ dq_acc, long long n8, uint16_t* __restrict__ dq,
-                                   const int32_t* __restrict__ q_rows, int T, int chunks) {
+                                   const int32_t* __restrict__ q_rows, int T, int To, int chunks) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += stride) {
     // dQ may be stored in original row order (q_rows maps sorted -> original)
     long long out = t;
     if (q_rows != nullptr) {
       const long long row = t / chunks;
-      const long long orow = mapped_row(q_rows, row, static_cast<int>(row % T), T);
+      const long long orow = mapped_row(q_rows, row, row / T, To);
       if (orow < 0) continue;
       out = orow * chunks + (t - row * chunks);
     }
@@ -1213,6 +1215,7 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
     pp.dO = a.do_;
     pp.o32 = a.o32;
     pp.o_rows = a.q_rows;
+    pp.To = a.To;
     pp.lse = a.lse_in;
     pp.q_idx = a.q_idx;
     pp.q_hash = a.q_hash;
@@ -1254,6 +1257,7 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   p.dk = a.dk;
   p.dv = a.dv;
   p.k_rows = a.k_rows;
+  p.To = a.To;
   p.stall = a.stall;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched + 2;
@@ -1282,7 +1286,7 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
     long long g = (n8 + 255) / 256;
     if (g > sms * 16LL) g = sms * 16LL;
     if (g < 1) g = 1;
-    dq_finalize_kernel<<<static_cast<int>(g), 256, 0, st>>>(dq_acc, n8, a.dq, a.q_rows, a.Tq, D / 8);
+    dq_finalize_kernel<<<static_cast<int>(g), 256, 0, st>>>(dq_acc, n8, a.dq, a.q_rows, a.Tq, a.To, D / 8);
   }
   return cudaGetLastError();
 }

@@ -112,6 +112,7 @@ struct FwdParams {
   int* sched;            // [0] next item, [1] CTAs done (single-tile kernel)
   uint16_t* o;
   const int32_t* o_rows;  // null, or the original row of each sorted query row
+  int To;                 // rows per head of o when o_rows is set
   float* lse;
   float* o32;             // null, or an fp32 copy of O [B,H,Tq,D] in row order of q
   int stall;              // SCFA_FLAG_DEBUG_STALL: withhold the first K / V load
@@ -499,7 +500,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (!ok) break;
       if (!any) {
         if (valid) {
-          const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
+          const long long orow = mapped_row(p.o_rows, grow, bh, p.To);
           if (orow >= 0) {
             uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
 #pragma unroll
@@ -536,7 +537,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           l_o = l - pm + __bfloat162float(__float2bfloat16_rn(pm));
         }
         const float inv = l_o > 0.f ? 1.f / l_o : 0.f;
-        const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
+        const long long orow = mapped_row(p.o_rows, grow, bh, p.To);
         uint4* dst = reinterpret_cast<uint4*>(p.o + (orow >= 0 ? orow : grow) * D);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -958,7 +959,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!ok) break;
       if (!any) {
         if (valid) {
-          const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
+          const long long orow = mapped_row(p.o_rows, grow, bh, p.To);
           if (orow >= 0) {
             uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
 #pragma unroll
@@ -995,7 +996,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           l_o = l - pm + __bfloat162float(__float2bfloat16_rn(pm));
         }
         const float inv = l_o > 0.f ? 1.f / l_o : 0.f;
-        const long long orow = mapped_row(p.o_rows, grow, row, p.Tq);
+        const long long orow = mapped_row(p.o_rows, grow, bh, p.To);
         uint4* dst = reinterpret_cast<uint4*>(p.o + (orow >= 0 ? orow : grow) * D);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
@@ -1057,6 +1058,7 @@ static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   p.n_pairs = static_cast<int>(L.n_pairs);
   p.o = a.o_out;
   p.o_rows = a.q_rows;
+  p.To = a.To;
   p.lse = a.lse_out;
   p.o32 = a.o32;
   p.stall = a.stall;
@@ -1099,6 +1101,7 @@ static cudaError_t launch_fwd1(const AttnArgs& a, cudaStream_t st) {
   p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched;
   p.o = a.o_out;
   p.o_rows = a.q_rows;
+  p.To = a.To;
   p.lse = a.lse_out;
   p.o32 = a.o32;
   p.stall = a.stall;

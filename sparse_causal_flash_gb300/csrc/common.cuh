@@ -108,13 +108,14 @@ __device__ __forceinline__ int work_item(int r) {
   return r * G + ((r & 1) ? (G - 1 - b) : b);
 }
 
-// Output row of the row `grow` = (head base + r) of a sorted tensor: grow
-// itself without a row map, else head base + rows[grow]; -1 when the map
-// points outside [0, T) (such rows are neither written nor read).
-__device__ __forceinline__ long long mapped_row(const int32_t* rows, long long grow, int r, int T) {
+// Output row of the row `grow` of head `bh` of a sorted tensor: grow itself
+// without a row map, else row rows[grow] of that head in an original-order
+// tensor of To rows per head; -1 when the map points outside [0, To) (such
+// rows are neither written nor read).
+__device__ __forceinline__ long long mapped_row(const int32_t* rows, long long grow, long long bh, int To) {
   if (rows == nullptr) return grow;
   const int t = rows[grow];
-  return (t >= 0 && t < T) ? grow - r + t : -1;
+  return (t >= 0 && t < To) ? bh * To + t : -1;
 }
 
 // named barrier among `count` threads (ids 1..15; 0 is __syncthreads)

@@ -58,6 +58,8 @@ struct LshWs {
   size_t header = 0;
   size_t hash = 0;    // int32 [B,H,T], original order
   size_t chunk = 0;   // int32 [B*H][chunks][n_buckets]: per-chunk counts, then scatter bases (long rows)
+  size_t perm_u = 0, hs_u = 0;  // int32 [B,H,T]: the plain sorted order (tile-aligned sort)
+  size_t off_u = 0;             // int32 [B,H,n_buckets+1]
   size_t total = 0;
 };
 constexpr int kSortChunk = 8192;  // rows longer than this are sorted by several CTAs
@@ -78,7 +80,7 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
 
 // SCFA_FLAG_VALIDATE: contract checks of the index inputs into the status word
 cudaError_t launch_validate(int mode, bool original, const int32_t* q_idx, const int32_t* k_idx,
-                            const int32_t* q_hash, const int32_t* k_hash, int B, int H, int Tq, int Tk,
+                            const int32_t* q_hash, const int32_t* k_hash, int B, int H, int Tq, int Tk, int To,
                             char* ws, const AttnWs& L, cudaStream_t st);
 
 // lsh.cu
@@ -93,8 +95,12 @@ cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long
 cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int n_buckets,
                                int32_t* perm, int32_t* hash_sorted, int32_t* bucket_off,
                                int32_t* chunk_ws, cudaStream_t st);
-cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int BH, int T, int D,
+// Ts rows per head in the sorted tensor, To in the original-order one
+cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int BH, int Ts, int To, int D,
                           uint16_t* out, bool unsort, cudaStream_t st);
+// plain sorted order (perm_u, off_u) -> tile-aligned order of Ts rows per head
+cudaError_t launch_tiled_layout(const int32_t* perm_u, const int32_t* off_u, int BH, int T, int Ts, int nb, int pad,
+                                int32_t* perm, int32_t* hash_sorted, int32_t* start, cudaStream_t st);
 
 // attn_fwd.cu / attn_bwd.cu
 struct AttnArgs {
@@ -110,6 +116,7 @@ struct AttnArgs {
   // hash mode with SCFA_FLAG_ORIGINAL_ORDER: destination row (within the
   // head) of each sorted query / key row; null = rows stay in place
   const int32_t *q_rows, *k_rows;
+  int To;  // rows per head of the original-order tensors (= Tq without a row map)
   // SCFA_FLAG_KEEP_O32: the fp32 copy of O in the workspace (the forward
   // writes it, the backward pre-pass reads it); null otherwise
   float* o32;

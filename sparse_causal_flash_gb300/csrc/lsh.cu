@@ -884,19 +884,26 @@ __global__ void bucket_scan_kernel(int nb, int n_chunks, int32_t* __restrict__ c
   }
 }
 
-// 16-byte vector row moves. gather: out[s] = x[perm[s]]; unsort: out[perm[s]] = x[s].
+// 16-byte vector row moves between a sorted tensor of Ts rows per head and an
+// original-order one of To rows per head. gather: sorted[s] = x[perm[s]], a
+// zero row where perm[s] is outside [0, To) (a padding row); unsort:
+// out[perm[s]] = sorted[s], skipping such rows.
 __global__ void row_move_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
-                                long long rows, int T, int chunks, uint4* __restrict__ out, int unsort) {
+                                long long rows, int Ts, int To, int chunks, uint4* __restrict__ out, int unsort) {
   const long long n = rows * chunks;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n; g += stride) {
-    const long long row = g / chunks;
+    const long long row = g / chunks;  // sorted row over all heads
     const int ch = static_cast<int>(g - row * chunks);
-    const long long head0 = row - row % T;
+    const long long bh = row / Ts;
     const int p = perm[row];
-    if (p < 0 || p >= T) continue;
-    if (unsort) out[(head0 + p) * chunks + ch] = x[g];
-    else out[g] = x[(head0 + p) * chunks + ch];
+    const bool in = p >= 0 && p < To;
+    const long long orig = (bh * To + p) * chunks + ch;
+    if (unsort) {
+      if (in) out[orig] = x[g];
+    } else {
+      out[g] = in ? x[orig] : make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 }
 
@@ -996,18 +1003,89 @@ cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int nb,
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int BH, int T, int D,
+// Tile-aligned sorted layout. One warp per head: bucket b starts at row
+// start[b] = sum over c < b of n_c rounded up to a multiple of kTile, so no
+// tile holds two buckets; start[nb] is the end of the last bucket's tiles.
+__global__ void tiled_offsets_kernel(const int32_t* __restrict__ off, int BH, int nb,
+                                     int32_t* __restrict__ start) {
+  const int lane = threadIdx.x & 31;
+  const long long bh = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (bh >= BH) return;
+  const int32_t* o = off + bh * (nb + 1);
+  int32_t* s = start + bh * (nb + 1);
+  int run = 0;
+  for (int base = 0; base < nb; base += 32) {
+    const int b = base + lane;
+    const int v = b < nb ? (o[b + 1] - o[b] + kTile - 1) / kTile * kTile : 0;
+    int x = v;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    if (b < nb) s[b] = run + x - v;
+    run += __shfl_sync(0xffffffffu, x, 31);
+  }
+  if (lane == 0) s[nb] = run;
+}
+
+// Row p of the tile-aligned layout (Ts rows per head): the bucket b whose
+// tiles hold p (the last start <= p), its rank r = p - start[b], and then
+// either the r-th row of the bucket in the plain sorted order or, past the
+// bucket's n_b rows and after the last bucket, a padding row: position `pad`
+// and bucket id b (nb - 1 after the last bucket), so tile ranges keep one
+// bucket each.
+__global__ void tiled_spread_kernel(const int32_t* __restrict__ perm_u, const int32_t* __restrict__ off,
+                                    const int32_t* __restrict__ start, int BH, int T, int Ts, int nb, int pad,
+                                    int32_t* __restrict__ perm, int32_t* __restrict__ hash_sorted) {
+  const long long n = static_cast<long long>(BH) * Ts;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < n; g += stride) {
+    const long long bh = g / Ts;
+    const int p = static_cast<int>(g - bh * Ts);
+    const int32_t* s = start + bh * (nb + 1);
+    const int32_t* o = off + bh * (nb + 1);
+    int lo = 0, hi = nb - 1;  // last b in [0, nb) with s[b] <= p (s[0] = 0)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s[mid] <= p) lo = mid;
+      else hi = mid - 1;
+    }
+    const int r = p - s[lo];
+    const int n_b = o[lo + 1] - o[lo];
+    perm[g] = r < n_b ? perm_u[bh * T + o[lo] + r] : pad;
+    hash_sorted[g] = lo;
+  }
+}
+
+cudaError_t launch_tiled_layout(const int32_t* perm_u, const int32_t* off_u, int BH, int T, int Ts, int nb, int pad,
+                                int32_t* perm, int32_t* hash_sorted, int32_t* start, cudaStream_t st) {
+  const int warps_per_block = 8;
+  tiled_offsets_kernel<<<(BH + warps_per_block - 1) / warps_per_block, warps_per_block * 32, 0, st>>>(off_u, BH, nb,
+                                                                                                      start);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long n = static_cast<long long>(BH) * Ts;
+  long long g = (n + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms()) * 16;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  tiled_spread_kernel<<<static_cast<int>(g), 256, 0, st>>>(perm_u, off_u, start, BH, T, Ts, nb, pad, perm,
+                                                           hash_sorted);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int BH, int Ts, int To, int D,
                           uint16_t* out, bool unsort, cudaStream_t st) {
   const int chunks = D / 8;
-  const long long rows = static_cast<long long>(BH) * T;
+  const long long rows = static_cast<long long>(BH) * Ts;
   const long long n = rows * chunks;
   const int block = 256;
   long long g = (n + block - 1) / block;
   const long long cap = static_cast<long long>(num_sms()) * 16;
   if (g > cap) g = cap;
   if (g < 1) g = 1;
-  row_move_kernel<<<static_cast<int>(g), block, 0, st>>>(reinterpret_cast<const uint4*>(x), perm, rows, T, chunks,
-                                                         reinterpret_cast<uint4*>(out), unsort ? 1 : 0);
+  row_move_kernel<<<static_cast<int>(g), block, 0, st>>>(reinterpret_cast<const uint4*>(x), perm, rows, Ts, To,
+                                                         chunks, reinterpret_cast<uint4*>(out), unsort ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -462,7 +462,7 @@ __global__ void work_order_kernel(OrderList l0, OrderList l1, OrderList l2, int 
 //       row in `bits` (zeroed by the caller).
 __global__ void validate_kernel(int mode, int original, const int32_t* __restrict__ q_idx,
                                 const int32_t* __restrict__ k_idx, const int32_t* __restrict__ q_hash,
-                                const int32_t* __restrict__ k_hash, long long BH, int Tq, int Tk,
+                                const int32_t* __restrict__ k_hash, long long BH, int Tq, int Tk, int To,
                                 uint32_t* __restrict__ bits, int* status) {
   const long long nq = BH * Tq, n = nq + BH * Tk;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -488,7 +488,7 @@ __global__ void validate_kernel(int mode, int original, const int32_t* __restric
       if (h[r] < 0 || (r > 0 && h[r - 1] > h[r])) bad = true;
       if (original) {
         const int32_t v = idx[r];
-        if (v >= 0 && v < T) {
+        if (v >= 0 && v < To) {  // ids outside [0, To) are rows that are not written
           const long long words = (static_cast<long long>(T) + 31) / 32;
           uint32_t* b = bits + (is_q ? 0 : BH * ((static_cast<long long>(Tq) + 31) / 32)) + bh * words + v / 32;
           const uint32_t m = 1u << (v & 31);
@@ -527,7 +527,7 @@ inline int grid_for(long long work, int block, int max_blocks) {
 }  // namespace
 
 cudaError_t launch_validate(int mode, bool original, const int32_t* q_idx, const int32_t* k_idx,
-                            const int32_t* q_hash, const int32_t* k_hash, int B, int H, int Tq, int Tk,
+                            const int32_t* q_hash, const int32_t* k_hash, int B, int H, int Tq, int Tk, int To,
                             char* ws, const AttnWs& L, cudaStream_t st) {
   if (mode == SCFA_MODE_DENSE) return cudaSuccess;
   const long long BH = static_cast<long long>(B) * H;
@@ -538,7 +538,7 @@ cudaError_t launch_validate(int mode, bool original, const int32_t* q_idx, const
   }
   const long long n = BH * (static_cast<long long>(Tq) + Tk);
   validate_kernel<<<grid_for(n, 256, num_sms() * 8), 256, 0, st>>>(mode, original ? 1 : 0, q_idx, k_idx, q_hash,
-                                                                    k_hash, BH, Tq, Tk, bits,
+                                                                    k_hash, BH, Tq, Tk, To, bits,
                                                                     reinterpret_cast<int*>(ws + L.header));
   return cudaGetLastError();
 }

@@ -18,39 +18,53 @@ from __future__ import annotations
 import torch
 
 from . import (FLAG_KEEP_O32, FLAG_ORIGINAL_ORDER, FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size,
-               attn_workspace_size_live, lsh_bucket_sort, lsh_gather, lsh_workspace_size, scfa_dense_bwd,
+               attn_workspace_size_live, lsh_bucket_sort, lsh_bucket_sort_tiled, lsh_gather, lsh_workspace_size,
+               scfa_dense_bwd, scfa_tiled_rows,
                scfa_dense_fwd, scfa_hash_bwd, scfa_hash_fwd, scfa_qk_bwd, scfa_qk_fwd, scfa_tiles_count, workspace)
 
 # Above this many bytes of worst-case live-tile lists (every tile pair), the
 # hash step sizes its lists for the live count of each batch instead.
 LIVE_SIZED_ABOVE = 256 << 20
+# position of the padding rows of the tile-aligned sorted layout: a query that
+# sees no key, a key that no query sees
+Q_PAD, K_PAD = -1, 2**31 - 1
 
 
 class Step:
     """Buffers and the launch sequence of one fwd+bwd step for a fixed shape."""
 
     def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
-                 device="cuda", flags: int = 0):
+                 device="cuda", flags: int = 0, tiled=None):
+        """tiled (hash mode; the default): sort into the tile-aligned layout,
+        every bucket starting on a tile boundary (lsh_bucket_sort_tiled); the
+        sorted tensors then have Ts = scfa_tiled_rows(T, n_buckets) rows per
+        head. tiled=False keeps the plain sorted order (Ts = T)."""
         self.mode, self.B, self.H, self.Tq, self.Tk, self.D = mode, B, H, Tq, Tk, D
         self.nb = n_buckets
         self.flags = flags
+        self.tiled = mode == MODE_HASH and (tiled is None or bool(tiled))
+        # rows per head of the sorted tensors (hash mode) or of q / k
+        self.Ts = scfa_tiled_rows(Tq, n_buckets) if self.tiled else Tq
         dev = torch.device(device)
         bf = dict(dtype=torch.bfloat16, device=dev)
         i32 = dict(dtype=torch.int32, device=dev)
         self.o = torch.empty((B, H, Tq, D), **bf)
-        self.lse = torch.empty((B, H, Tq), dtype=torch.float32, device=dev)
+        # LSE stays in sorted order (with its padding rows in the tiled layout)
+        self.lse = torch.empty((B, H, self.Ts), dtype=torch.float32, device=dev)
         self.dq = torch.empty((B, H, Tq, D), **bf)
         self.dk = torch.empty((B, H, Tk, D), **bf)
         self.dv = torch.empty((B, H, Tk, D), **bf)
         # one backward-sized workspace: the forward call builds the live-tile
         # list in it and the backward call reuses that list
         self.device = dev
-        worst = attn_workspace_size(mode, 1, B, H, Tq, Tk, D)
-        fixed = attn_workspace_size_live(mode, 1, B, H, Tq, Tk, D, 0)
+        Ta, Tb = (self.Ts, self.Ts) if mode == MODE_HASH else (Tq, Tk)  # rows the attention calls see
+        self.Ta = Ta
+        worst = attn_workspace_size(mode, 1, B, H, Ta, Tb, D)
+        fixed = attn_workspace_size_live(mode, 1, B, H, Ta, Tb, D, 0)
         self.live_sized = mode == MODE_HASH and worst - fixed > LIVE_SIZED_ABOVE
         if self.live_sized:
             # lists sized per batch from its live-tile count (scfa_tiles_count)
-            self.ws_count = workspace(attn_workspace_size_live(mode, 0, B, H, Tq, Tk, D, 0), dev)
+            self.ws_count = workspace(attn_workspace_size_live(mode, 0, B, H, Ta, Tb, D, 0), dev)
             self.n_live = torch.zeros(1, dtype=torch.int32, device=dev)
             self.list_cap = 0
             self.ws_b = None
@@ -58,21 +72,21 @@ class Step:
             self.ws_b = workspace(worst, dev)
         self.ws_f = self.ws_b
         if mode == MODE_HASH:
-            T = Tq
+            T, Ts = Tq, self.Ts
             self.ws_l = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
             self.ws_lk = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
             self.side = torch.cuda.Stream(device=dev)
             self.ev = [torch.cuda.Event() for _ in range(2)]
-            self.qh = torch.empty((B, H, T), **i32)
-            self.kh = torch.empty((B, H, T), **i32)
-            self.pq = torch.empty((B, H, T), **i32)
-            self.pk = torch.empty((B, H, T), **i32)
+            self.qh = torch.empty((B, H, Ts), **i32)
+            self.kh = torch.empty((B, H, Ts), **i32)
+            self.pq = torch.empty((B, H, Ts), **i32)
+            self.pk = torch.empty((B, H, Ts), **i32)
             self.offq = torch.empty((B, H, n_buckets + 1), **i32)
             self.offk = torch.empty((B, H, n_buckets + 1), **i32)
-            self.q_s = torch.empty((B, H, T, D), **bf)
-            self.k_s = torch.empty((B, H, T, D), **bf)
-            self.v_s = torch.empty((B, H, T, D), **bf)
-            self.do_s = torch.empty((B, H, T, D), **bf)
+            self.q_s = torch.empty((B, H, Ts, D), **bf)
+            self.k_s = torch.empty((B, H, Ts, D), **bf)
+            self.v_s = torch.empty((B, H, Ts, D), **bf)
+            self.do_s = torch.empty((B, H, Ts, D), **bf)
 
     def run(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None, stream=None, mark=None):
         """Forward + backward. Results land in self.o/lse/dq/dk/dv.
@@ -102,12 +116,18 @@ class Step:
             side = self.side if mark is None else main
             self.ev[0].record(main)
             side.wait_event(self.ev[0])
-            lsh_bucket_sort(k, R, nb, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
+            if self.tiled:
+                lsh_bucket_sort_tiled(k, R, nb, K_PAD, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
+            else:
+                lsh_bucket_sort(k, R, nb, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
             tick("hash_sort_gather_k")
             lsh_gather(v, self.pk, self.v_s, side)
             tick("gather_v")
             self.ev[1].record(side)
-            lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
+            if self.tiled:
+                lsh_bucket_sort_tiled(q, R, nb, Q_PAD, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
+            else:
+                lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
             tick("hash_sort_gather_q")
             lsh_gather(do, self.pq, self.do_s, main)
             tick("gather_do")
@@ -129,14 +149,14 @@ class Step:
     def _size_lists(self, stream):
         """Count this batch's live tiles (reads one int back) and grow the
         workspace if its lists cannot hold them (with an eighth to spare)."""
-        scfa_tiles_count(MODE_HASH, self.pq, self.pk, self.qh, self.kh, self.B, self.H, self.Tq, self.Tq,
+        scfa_tiles_count(MODE_HASH, self.pq, self.pk, self.qh, self.kh, self.B, self.H, self.Ts, self.Ts,
                          self.ws_count, self.n_live, stream)
         stream.synchronize()
         need = int(self.n_live.item())
         if self.ws_b is None or need > self.list_cap:
             self.list_cap = need + need // 8 + 1024
             self.ws_b = None
-            self.ws_b = workspace(attn_workspace_size_live(MODE_HASH, 1, self.B, self.H, self.Tq, self.Tq, self.D,
+            self.ws_b = workspace(attn_workspace_size_live(MODE_HASH, 1, self.B, self.H, self.Ts, self.Ts, self.D,
                                                            self.list_cap), self.device)
             self.ws_f = self.ws_b
 
@@ -156,9 +176,10 @@ class HostPipeline:
     INPUTS = ("q", "k", "v", "do", "q_idx", "k_idx", "R")
 
     def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
-                 device="cuda", flags: int = 0):
+                 device="cuda", flags: int = 0, tiled=None):
         self.device = torch.device(device)
-        self.steps = [Step(mode, B, H, Tq, Tk, D, n_buckets=n_buckets, device=self.device, flags=flags)
+        self.steps = [Step(mode, B, H, Tq, Tk, D, n_buckets=n_buckets, device=self.device, flags=flags,
+                           tiled=tiled)
                       for _ in range(2)]
         self.h2d = torch.cuda.Stream(device=self.device)
         self.d2h = torch.cuda.Stream(device=self.device)

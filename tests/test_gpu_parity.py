@@ -31,6 +31,34 @@ def cuda(t):
     return t.contiguous().cuda()
 
 
+Q_PAD, K_PAD = -1, 2**31 - 1  # positions of padding rows in the tile-aligned layout
+
+
+def sorted_views(x_hash, nb, Ts=None, pad=Q_PAD):
+    """The oracle's sorted view of [B,H,T] bucket ids: the plain stable sort,
+    or (Ts given) its tile-aligned layout of Ts rows per head."""
+    perm, hs, off = pipelines.hash_sort_view(x_hash, nb)
+    if Ts is None:
+        return perm, hs, off
+    B, H, _ = perm.shape
+    out = [np.empty((B, H, Ts), np.int32), np.empty((B, H, Ts), np.int32), np.empty((B, H, nb + 1), np.int32)]
+    for b in range(B):
+        for h in range(H):
+            for a, v in zip(out, lsh.tile_aligned(perm[b, h], off[b, h], Ts, 128, pad)):
+                a[b, h] = v
+    return tuple(out)
+
+
+def check_lse_sorted(name, got, ref, perm):
+    """LSE in sorted order against the oracle's LSE in original order; rows
+    whose perm entry names no token (padding) must be -inf."""
+    perm = np.asarray(perm)
+    inside = (perm >= 0) & (perm < len(ref))
+    m = torch.from_numpy(inside).to(got.device)
+    check_lse(name, got[m], np.asarray(ref)[perm[inside]])
+    assert bool(torch.all(torch.isneginf(got[~m]))), f"{name}: a padding row is not -inf"
+
+
 # ------------------------------------------------------------------ LSH + sort
 @pytest.mark.parametrize("B,H,T,D,nb", [(1, 2, 512, 64, 4), (2, 3, 1000, 64, 16), (1, 2, 700, 128, 64),
                                         (2, 3, 1000, 64, 32)])
@@ -116,6 +144,41 @@ def test_bucket_sort_and_gather_bitexact(scfa, B, H, T, D, nb):
     g = torch.empty_like(xs)
     scfa.lsh_gather(cuda(x), perm, g)
     assert torch.equal(g.cpu().view(torch.int16), xs_ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("B,H,T,D,nb", [(1, 2, 512, 64, 4), (2, 3, 1000, 64, 16), (1, 1, 5000, 64, 512),
+                                        (1, 2, 20000, 64, 64), (1, 1, 3000, 128, 32), (1, 1, 130, 64, 256)])
+def test_bucket_sort_tiled_bitexact(scfa, B, H, T, D, nb):
+    """lsh_bucket_sort_tiled: perm, bucket ids, bucket starts and gathered rows
+    bit for bit against the oracle's tile-aligned view of its own sort, for
+    queries (padding position -1) and keys (padding position INT32_MAX);
+    padding rows are zero, and unsort puts every real row back."""
+    x = synth.normal_bf16(79, 2, (B, H, T, D))
+    R = synth.rotation_bf16(79, D, nb // 2)
+    Ts = scfa.scfa_tiled_rows(T, nb)
+    assert Ts % 128 == 0 and Ts >= T
+    href = lsh.lsh_hash(x.double().numpy(), R.double().numpy())
+    ws = scfa.workspace(scfa.lsh_workspace_size(B, H, T, nb))
+    dev = dict(dtype=torch.int32, device="cuda")
+    for pad in (Q_PAD, K_PAD):
+        hs = torch.empty((B, H, Ts), **dev)
+        perm = torch.empty((B, H, Ts), **dev)
+        start = torch.empty((B, H, nb + 1), **dev)
+        xs = torch.full((B, H, Ts, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        scfa.lsh_bucket_sort_tiled(cuda(x), cuda(R), nb, pad, hs, perm, start, xs, ws)
+        pr, hr, sr = sorted_views(href, nb, Ts, pad)
+        np.testing.assert_array_equal(perm.cpu().numpy(), pr)
+        np.testing.assert_array_equal(hs.cpu().numpy(), hr)
+        np.testing.assert_array_equal(start.cpu().numpy(), sr)
+        xs_ref = np.stack([np.stack([lsh.gather_rows_padded(x[b, h].view(torch.int16).numpy(), pr[b, h])
+                                     for h in range(H)]) for b in range(B)])
+        np.testing.assert_array_equal(xs.cpu().view(torch.int16).numpy(), xs_ref)
+        back = torch.zeros_like(cuda(x))
+        scfa.lsh_unsort(xs, perm, back)
+        assert torch.equal(back.cpu().view(torch.int16), x.view(torch.int16))
+        g = torch.full_like(xs, float("nan"))
+        scfa.lsh_gather(cuda(x), perm, g)
+        assert torch.equal(g.view(torch.int16), xs.view(torch.int16))
 
 
 # ------------------------------------------------------------------ tiles
@@ -248,39 +311,40 @@ def test_live_sized_workspace(scfa):
     from sparse_causal_flash_gb300.pipeline import Step
     st = Step(scfa.MODE_HASH, B, H, T, T, D, n_buckets=nb)
     st.run(p.q.cuda(), p.k.cuda(), p.v.cuda(), p.do.cuda(), p.wl.scale, R=p.R.cuda())
+    Ts = st.Ts  # rows of the sorted (tile-aligned) tensors
     n_live = torch.zeros(1, dtype=torch.int32, device="cuda")
-    wc = scfa.workspace(scfa.attn_workspace_size_live(scfa.MODE_HASH, 0, B, H, T, T, D, 0))
-    scfa.scfa_tiles_count(scfa.MODE_HASH, st.pq, st.pk, st.qh, st.kh, B, H, T, T, wc, n_live)
+    wc = scfa.workspace(scfa.attn_workspace_size_live(scfa.MODE_HASH, 0, B, H, Ts, Ts, D, 0))
+    scfa.scfa_tiles_count(scfa.MODE_HASH, st.pq, st.pk, st.qh, st.kh, B, H, Ts, Ts, wc, n_live)
     torch.cuda.synchronize()
     nl = int(n_live.item())
-    ref = tiles.live_list("hash", B, H, T, T, st.pq.cpu().numpy(), st.pk.cpu().numpy(), st.qh.cpu().numpy(),
+    ref = tiles.live_list("hash", B, H, Ts, Ts, st.pq.cpu().numpy(), st.pk.cpu().numpy(), st.qh.cpu().numpy(),
                           st.kh.cpu().numpy())
     assert nl == int(ref["row_ptr"][-1])
-    worst = scfa.attn_workspace_size(scfa.MODE_HASH, 1, B, H, T, T, D)
-    live = scfa.attn_workspace_size_live(scfa.MODE_HASH, 1, B, H, T, T, D, nl)
+    worst = scfa.attn_workspace_size(scfa.MODE_HASH, 1, B, H, Ts, Ts, D)
+    live = scfa.attn_workspace_size_live(scfa.MODE_HASH, 1, B, H, Ts, Ts, D, nl)
     assert live < worst
     e = lambda: torch.empty((B, H, T, D), dtype=torch.bfloat16, device="cuda")
     flags = scfa.FLAG_ORIGINAL_ORDER | scfa.FLAG_KEEP_O32
     outs = {}
     # one byte short of the live size holds fewer than nl entries
-    assert scfa.attn_workspace_capacity(scfa.MODE_HASH, 1, B, H, T, T, D, live - 1) < nl
+    assert scfa.attn_workspace_capacity(scfa.MODE_HASH, 1, B, H, Ts, Ts, D, live - 1) < nl
     for name, size in (("worst", worst), ("live", live), ("short", live - 1)):
         ws = scfa.workspace(size)
         o, dq, dk, dv = e(), e(), e(), e()
-        lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+        lse = torch.empty((B, H, Ts), dtype=torch.float32, device="cuda")
         scfa.scfa_hash_fwd(st.q_s, st.k_s, st.v_s, st.pq, st.pk, st.qh, st.kh, p.wl.scale, o, lse, ws, flags)
         scfa.scfa_hash_bwd(st.q_s, st.k_s, st.v_s, o, lse, st.do_s, st.pq, st.pk, st.qh, st.kh, p.wl.scale,
                            dq, dk, dv, ws, flags | scfa.FLAG_REUSE_TILES)
         torch.cuda.synchronize()
         outs[name] = (scfa.scfa_get_device_status(ws), o, lse, dk, dv, ws)
     assert outs["worst"][0] == 0 and outs["live"][0] == 0
-    got = read_tiles(scfa, outs["live"][5], scfa.MODE_HASH, B, H, T, T, D)
+    got = read_tiles(scfa, outs["live"][5], scfa.MODE_HASH, B, H, Ts, Ts, D)
     for key in ("row_ptr", "cols", "fflags", "csc_ptr", "csc_rows", "cflags"):  # (no pair lists at D = 64)
         np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
     for i, name in ((1, "O"), (2, "LSE"), (3, "dK"), (4, "dV")):
         assert torch.equal(outs["worst"][i], outs["live"][i]), name
     assert outs["short"][0] == 3  # SCFA_ERR_WORKSPACE
-    tv = read_tiles(scfa, outs["short"][5], scfa.MODE_HASH, B, H, T, T, D)
+    tv = read_tiles(scfa, outs["short"][5], scfa.MODE_HASH, B, H, Ts, Ts, D)
     assert not tv["row_ptr"].any() and not tv["csc_ptr"].any()
 
 
@@ -348,11 +412,11 @@ def test_count_chunked_pairs_bitexact(scfa, chunk):
 
 
 # ------------------------------------------------------------------ attention
-def run_step(scfa, p, mode, flags=0):
+def run_step(scfa, p, mode, flags=0, tiled=False):
     from sparse_causal_flash_gb300.pipeline import Step
     B, H, Tq, D = p.q.shape
     Tk = p.k.shape[2]
-    st = Step(mode, B, H, Tq, Tk, D, n_buckets=p.wl.n_buckets, flags=flags)
+    st = Step(mode, B, H, Tq, Tk, D, n_buckets=p.wl.n_buckets, flags=flags, tiled=tiled)
     st.run(cuda(p.q), cuda(p.k), cuda(p.v), cuda(p.do), p.wl.scale,
            q_idx=None if p.q_idx is None else cuda(p.q_idx), k_idx=None if p.k_idx is None else cuda(p.k_idx),
            R=None if p.R is None else cuda(p.R))
@@ -365,8 +429,10 @@ def compare_heads(st, ref, heads, lse_perm=None):
     for (b, h) in heads:
         r = ref[(b, h)]
         check_close(f"O[{b},{h}]", st.o[b, h], r["o"])
-        lse_ref = r["lse"] if lse_perm is None else r["lse"][lse_perm[b, h]]
-        check_lse(f"LSE[{b},{h}]", st.lse[b, h], lse_ref)
+        if lse_perm is None:
+            check_lse(f"LSE[{b},{h}]", st.lse[b, h], r["lse"])
+        else:
+            check_lse_sorted(f"LSE[{b},{h}]", st.lse[b, h], r["lse"], lse_perm[b, h])
         check_close(f"dQ[{b},{h}]", st.dq[b, h], r["dq"])
         check_close(f"dK[{b},{h}]", st.dk[b, h], r["dk"])
         check_close(f"dV[{b},{h}]", st.dv[b, h], r["dv"])
@@ -389,6 +455,28 @@ def test_hash_parity(scfa, B, H, T, D, nb, seed):
     ref, qh, kh = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, p.wl.scale)
     pq, _, _ = pipelines.hash_sort_view(qh, nb)
     compare_heads(st, ref, ref.keys(), lse_perm=pq)
+
+
+@pytest.mark.parametrize("B,H,T,D,nb,seed", [(1, 2, 512, 64, 4, 1001), (1, 2, 1000, 64, 8, 21),
+                                             (1, 1, 1000, 64, 64, 24), (1, 2, 1300, 128, 8, 23)])
+def test_hash_parity_tiled(scfa, B, H, T, D, nb, seed):
+    """The hash step on the tile-aligned sorted layout (padding rows between
+    buckets): results in original order within tolerance, LSE in the padded
+    sorted order (padding rows -inf), and the live-tile lists of the padded
+    index arrays bit for bit."""
+    p = synth.make_problem(synth.Workload("ht", "hash", B, H, T, D, seed, n_buckets=nb))
+    st = run_step(scfa, p, scfa.MODE_HASH, tiled=True)
+    assert st.Ts == scfa.scfa_tiled_rows(T, nb) and st.q_s.shape[2] == st.Ts
+    ref, qh, kh = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, p.wl.scale)
+    pq, qs, _ = sorted_views(qh, nb, st.Ts, Q_PAD)
+    pk, ks, _ = sorted_views(kh, nb, st.Ts, K_PAD)
+    np.testing.assert_array_equal(st.pq.cpu().numpy(), pq)
+    np.testing.assert_array_equal(st.pk.cpu().numpy(), pk)
+    compare_heads(st, ref, ref.keys(), lse_perm=pq)
+    got = read_tiles(scfa, st.ws_b, scfa.MODE_HASH, B, H, st.Ts, st.Ts, D)
+    want = tiles.live_list("hash", B, H, st.Ts, st.Ts, pq, pk, qs, ks)
+    for key in ("row_ptr", "cols", "fflags", "csc_ptr", "csc_rows", "cflags"):
+        np.testing.assert_array_equal(got[key], want[key], err_msg=key)
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -539,38 +627,42 @@ def test_full_qk_8k_sampled_heads(scfa):
                         st.ws_b) == want
 
 
-def test_full_hash_8k_sampled_heads(scfa):
+@pytest.mark.parametrize("tiled", [False, True])
+def test_full_hash_8k_sampled_heads(scfa, tiled):
     wl = synth.WORKLOADS["hash_b4h12_t8192_d64_nb16"]
     p = synth.make_problem(wl)
-    st = run_step(scfa, p, scfa.MODE_HASH)
+    st = run_step(scfa, p, scfa.MODE_HASH, tiled=tiled)
     heads = [(0, 0), (1, 5), (2, 9), (3, 11)]
     qh = lsh.lsh_hash(p.q.double().numpy(), p.R.double().numpy())
     kh = lsh.lsh_hash(p.k.double().numpy(), p.R.double().numpy())
-    np.testing.assert_array_equal(st.qh.cpu().numpy(), pipelines.hash_sort_view(qh, wl.n_buckets)[1])
+    pq, qs, _ = sorted_views(qh, wl.n_buckets, st.Ts if tiled else None, Q_PAD)
+    np.testing.assert_array_equal(st.qh.cpu().numpy(), qs)
+    np.testing.assert_array_equal(st.pq.cpu().numpy(), pq)
     ref, _, _ = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, wl.scale, heads=heads, q_hash=qh, k_hash=kh)
-    pq, _, _ = pipelines.hash_sort_view(qh, wl.n_buckets)
     compare_heads(st, ref, heads, lse_perm=pq)
     # the bench's unit count: admissible pairs inside the live tiles (device)
     # against the oracle's hash mask over every head, from the oracle's ids
     want = sum(attention.admissible_pairs(attention.mask_hash(qh[b, h], kh[b, h]))
                for b in range(wl.B) for h in range(wl.H))
-    assert device_count(scfa, scfa.MODE_HASH, st.pq, st.pk, st.qh, st.kh, wl.B, wl.H, wl.T, wl.T, st.ws_b) == want
+    assert device_count(scfa, scfa.MODE_HASH, st.pq, st.pk, st.qh, st.kh, wl.B, wl.H, st.Ts, st.Ts, st.ws_b) == want
 
 
-def test_full_hash_16k_sampled_heads(scfa):
+@pytest.mark.parametrize("tiled", [False, True])
+def test_full_hash_16k_sampled_heads(scfa, tiled):
     """Hash-sparse B2 H12 T16384 D64 with 32 buckets, in the bench's launch
     configuration: bucket ids and sorted views of every head bit-exact, and
     three whole heads within tolerance (the oracle evaluates each head bucket
     by bucket, exact because the hash mask never pairs two buckets)."""
     wl = synth.WORKLOADS["hash_b2h12_t16384_d64_nb32"]
     p = synth.make_problem(wl)
-    st = run_step(scfa, p, scfa.MODE_HASH)
+    st = run_step(scfa, p, scfa.MODE_HASH, tiled=tiled)
     assert scfa.scfa_get_device_status(st.ws_b) == 0
     R = p.R.double().numpy()
     qh = lsh.lsh_hash(p.q.double().numpy(), R)
     kh = lsh.lsh_hash(p.k.double().numpy(), R)
-    pq, qs, oq = pipelines.hash_sort_view(qh, wl.n_buckets)
-    pk, ks, ok_ = pipelines.hash_sort_view(kh, wl.n_buckets)
+    Ts = st.Ts if tiled else None
+    pq, qs, oq = sorted_views(qh, wl.n_buckets, Ts, Q_PAD)
+    pk, ks, ok_ = sorted_views(kh, wl.n_buckets, Ts, K_PAD)
     np.testing.assert_array_equal(st.pq.cpu().numpy(), pq)
     np.testing.assert_array_equal(st.qh.cpu().numpy(), qs)
     np.testing.assert_array_equal(st.offq.cpu().numpy(), oq)
@@ -588,7 +680,7 @@ def test_full_hash_16k_sampled_heads(scfa):
             o[qp], dq[qp], lse[r["q_pos"]] = torch.from_numpy(r["o"]), torch.from_numpy(r["dq"]), r["lse"]
             dk[kp], dv[kp] = torch.from_numpy(r["dk"]), torch.from_numpy(r["dv"])
         check_close(f"O[{b},{h}]", st.o[b, h], o.numpy())
-        check_lse(f"LSE[{b},{h}]", st.lse[b, h], lse[pq[b, h]])
+        check_lse_sorted(f"LSE[{b},{h}]", st.lse[b, h], lse, pq[b, h])
         check_close(f"dQ[{b},{h}]", st.dq[b, h], dq.numpy())
         check_close(f"dK[{b},{h}]", st.dk[b, h], dk.numpy())
         check_close(f"dV[{b},{h}]", st.dv[b, h], dv.numpy())
@@ -615,20 +707,23 @@ def test_full_hash_1m_sampled_buckets(scfa):
     buckets (the hash mask is block-diagonal by bucket) within tolerance."""
     wl = synth.WORKLOADS["hash_b1h8_t1048576_d128_nb512"]
     p = synth.make_problem(wl)
-    st = run_step(scfa, p, scfa.MODE_HASH)
+    st = run_step(scfa, p, scfa.MODE_HASH, tiled=True)
+    Ts = st.Ts
     assert scfa.scfa_get_device_status(st.ws_b) == 0
     # the lists are sized for the live tiles, not for every tile pair
     assert st.live_sized
-    fixed = scfa.attn_workspace_size_live(scfa.MODE_HASH, 1, wl.B, wl.H, wl.T, wl.T, wl.D, 0)
+    fixed = scfa.attn_workspace_size_live(scfa.MODE_HASH, 1, wl.B, wl.H, Ts, Ts, wl.D, 0)
     assert st.ws_b.numel() - fixed < 64 << 20
-    assert scfa.attn_workspace_size(scfa.MODE_HASH, 1, wl.B, wl.H, wl.T, wl.T, wl.D) - fixed > 7e9
+    assert scfa.attn_workspace_size(scfa.MODE_HASH, 1, wl.B, wl.H, Ts, Ts, wl.D) - fixed > 7e9
     h0 = 5
     q, k, v, do = (t[0, h0] for t in (p.q, p.k, p.v, p.do))
     R = p.R.double().numpy()
     qh = lsh.lsh_hash(q.double().numpy(), R)
     kh = lsh.lsh_hash(k.double().numpy(), R)
-    pq, qs, _ = lsh.bucket_sort(qh, wl.n_buckets)
-    pk, ks, _ = lsh.bucket_sort(kh, wl.n_buckets)
+    pq, qs, oq = lsh.bucket_sort(qh, wl.n_buckets)
+    pk, ks, ok_ = lsh.bucket_sort(kh, wl.n_buckets)
+    pq, qs, _ = lsh.tile_aligned(pq, oq, Ts, 128, Q_PAD)
+    pk, ks, _ = lsh.tile_aligned(pk, ok_, Ts, 128, K_PAD)
     np.testing.assert_array_equal(st.pq[0, h0].cpu().numpy(), pq)
     np.testing.assert_array_equal(st.qh[0, h0].cpu().numpy(), qs)
     np.testing.assert_array_equal(st.pk[0, h0].cpu().numpy(), pk)
@@ -636,8 +731,9 @@ def test_full_hash_1m_sampled_buckets(scfa):
     counts = np.bincount(qh, minlength=wl.n_buckets)
     buckets = sorted({int(np.argmax(counts)), int(qh[-1]), 7})
     ref = pipelines.run_hash_buckets(q, k, v, do, wl.scale, qh, kh, buckets)
-    inv_q = np.empty_like(pq)
-    inv_q[pq] = np.arange(len(pq))
+    inv_q = np.empty(wl.T, dtype=np.int64)  # sorted row of each query position
+    real = pq != Q_PAD
+    inv_q[pq[real]] = np.nonzero(real)[0]
     o, dq, dk, dv = (t[0, h0].cpu() for t in (st.o, st.dq, st.dk, st.dv))
     lse_sorted = st.lse[0, h0].cpu().numpy()
     for c, r in ref.items():
@@ -658,8 +754,9 @@ def test_host_pipeline_overlapped_copies(scfa):
     from sparse_causal_flash_gb300.pipeline import HostPipeline
     B, H, T, D, nb = 1, 2, 640, 64, 4
     pipe = HostPipeline(scfa.MODE_HASH, B, H, T, T, D, n_buckets=nb)
+    Ts = pipe.steps[0].Ts  # LSE stays in the (tile-aligned) sorted order
     probs, hins, houts = [], [], []
-    shapes = [((B, H, T, D), torch.bfloat16), ((B, H, T), torch.float32)] + [((B, H, T, D), torch.bfloat16)] * 3
+    shapes = [((B, H, T, D), torch.bfloat16), ((B, H, Ts), torch.float32)] + [((B, H, T, D), torch.bfloat16)] * 3
     for i in range(3):
         p = synth.make_problem(synth.Workload("hp", "hash", B, H, T, D, 70 + i, n_buckets=nb))
         hin = {n: getattr(p, n).contiguous().pin_memory() for n in ("q", "k", "v", "do", "R")}
@@ -671,10 +768,10 @@ def test_host_pipeline_overlapped_copies(scfa):
     pipe.synchronize()
     for i, (p, (o, lse, dq, dk, dv)) in enumerate(zip(probs, houts)):
         ref, qh, _ = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, p.wl.scale)
-        pq, _, _ = pipelines.hash_sort_view(qh, nb)
+        pq, _, _ = sorted_views(qh, nb, Ts, Q_PAD)
         for (b, h), r in ref.items():
             check_close(f"step {i} O[{b},{h}]", o[b, h], r["o"])
-            check_lse(f"step {i} LSE[{b},{h}]", lse[b, h], r["lse"][pq[b, h]])
+            check_lse_sorted(f"step {i} LSE[{b},{h}]", lse[b, h], r["lse"], pq[b, h])
             check_close(f"step {i} dQ[{b},{h}]", dq[b, h], r["dq"])
             check_close(f"step {i} dK[{b},{h}]", dk[b, h], r["dk"])
             check_close(f"step {i} dV[{b},{h}]", dv[b, h], r["dv"])

@@ -88,7 +88,7 @@ def hash_forward(scfa, q_s, k_s, v_s, pq, pk, qh, kh, scale, flags):
 def test_validate_hash_contracts(scfa):
     from sparse_causal_flash_gb300.pipeline import Step
     p = synth.make_problem(synth.Workload("vh", "hash", 1, 2, 700, 64, 121, n_buckets=8))
-    st = Step(scfa.MODE_HASH, 1, 2, 700, 700, 64, n_buckets=8)
+    st = Step(scfa.MODE_HASH, 1, 2, 700, 700, 64, n_buckets=8, tiled=False)
     st.run(p.q.cuda(), p.k.cuda(), p.v.cuda(), p.do.cuda(), p.wl.scale, R=p.R.cuda())
     torch.cuda.synchronize()
     args = (st.q_s, st.k_s, st.v_s)

@@ -93,3 +93,45 @@ def test_gather_unsort_round_trip():
     for s in range(64):
         np.testing.assert_array_equal(xs[s], x[perm[s]])
     np.testing.assert_array_equal(lsh.unsort_rows(xs, perm), x)
+
+
+def test_tile_aligned_hand_worked():
+    # ids [1, 0, 1, 1, 0], two buckets, tile height 2, 8 rows:
+    # plain order perm [1, 4, 0, 2, 3], offsets [0, 2, 5]; bucket 0 keeps rows
+    # 0-1, bucket 1 starts at row 2 and its 3 tokens round up to 4 rows (2-5),
+    # rows 6-7 follow the last bucket
+    perm, hs, off = lsh.bucket_sort(np.array([1, 0, 1, 1, 0]), 2)
+    np.testing.assert_array_equal(perm, [1, 4, 0, 2, 3])
+    pt, ht, start = lsh.tile_aligned(perm, off, 8, 2, -1)
+    np.testing.assert_array_equal(pt, [1, 4, 0, 2, 3, -1, -1, -1])
+    np.testing.assert_array_equal(ht, [0, 0, 1, 1, 1, 1, 1, 1])
+    np.testing.assert_array_equal(start, [0, 2, 6])
+
+
+@pytest.mark.parametrize("T,nb,tile", [(1, 4, 128), (300, 64, 128), (1000, 8, 128), (5000, 512, 128), (97, 6, 5)])
+def test_tile_aligned_properties(T, nb, tile):
+    rng = np.random.default_rng(T + nb)
+    h = rng.integers(0, nb, size=T)
+    h[: T // 3] = rng.integers(0, max(1, nb // 4), size=T // 3)  # uneven, some buckets empty
+    perm, hs, off = lsh.bucket_sort(h, nb)
+    nonempty = int((np.diff(off) > 0).sum())
+    n_rows = -(-(T + nonempty * (tile - 1)) // tile) * tile  # the bound the product allocates
+    pt, ht, start = lsh.tile_aligned(perm, off, n_rows, tile, 2**31 - 1)
+    real = pt != 2**31 - 1
+    # every token appears once, in the plain sorted order
+    np.testing.assert_array_equal(pt[real], perm)
+    # bucket ids are non-decreasing, each bucket starts on a tile boundary and
+    # holds exactly its tokens followed by padding
+    assert np.all(np.diff(ht) >= 0)
+    for b in range(nb):
+        assert start[b] % tile == 0
+        rows = np.nonzero(ht == b)[0]
+        n_b = off[b + 1] - off[b]
+        if n_b:
+            assert rows[0] == start[b] and np.all(real[start[b]:start[b] + n_b])
+            assert not np.any(real[start[b] + n_b:start[b + 1]])
+            np.testing.assert_array_equal(h[pt[start[b]:start[b] + n_b]], b)
+    # no tile holds two buckets
+    for t0 in range(0, n_rows, tile):
+        assert len(set(ht[t0:t0 + tile].tolist())) == 1
+    assert not np.any(real[start[nb]:])
