@@ -193,6 +193,19 @@ scfa_status scfa_qk_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                         uint16_t* dq, uint16_t* dk, uint16_t* dv,
                         void* ws, size_t ws_bytes, unsigned flags, void* stream);
 
+/* The selection step in front of QK-sparse attention (same page section:
+ * dropped queries and keys leave compacted Q/K/V with their original
+ * positions). keep [B,H,T] uint8 (nonzero = kept; the policy that sets it is
+ * the caller's). idx [B,H,Tc] int32: the positions of the kept tokens of
+ * each head in ascending order, then `sentinel` (which must lie outside
+ * [0, T): -1 for queries, INT32_MAX for keys); count [B,H] int32: the kept
+ * count, also when it exceeds Tc (then only the first Tc positions are
+ * written: size Tc to the largest count). The rows move with lsh_gather
+ * (x_c = x gathered by idx, zero rows at the sentinels: T = T, T_sorted =
+ * Tc) and gradients go back to full length with lsh_unsort. */
+scfa_status scfa_qk_select(const uint8_t* keep, int B, int H, int T, int Tc, int32_t sentinel,
+                           int32_t* idx, int32_t* count, void* stream);
+
 /* ----------------------------------------------------------------------------
  * Hash-sparse attention on bucket-sorted rows (page section "SCFA 解决方案",
  * part 2 "Hash-Sparse"). All row tensors are in SORTED order, as produced by
@@ -253,11 +266,22 @@ scfa_status scfa_hash_bwd(const uint16_t* q_s, const uint16_t* k_s, const uint16
  *   T_sorted >= scfa_tiled_rows(T, n_buckets), the largest such layout
  *   (T + 127 per non-empty bucket, rounded up to 128). Same workspace as
  *   lsh_bucket_sort.
+ * lsh_sort_ids: the stable sort of bucket ids given by the caller (hash
+ *   [B,H,T] in original order, each in [0, n_buckets); 1 <= n_buckets <=
+ *   32768), without hashing: T_sorted == T gives the plain layout of
+ *   lsh_bucket_sort (bucket_start = bucket_off, pad unused), T_sorted >=
+ *   scfa_tiled_rows(T, n_buckets) the tile-aligned one of
+ *   lsh_bucket_sort_tiled. Shared-QK hashing sorts the keys by their queries'
+ *   ids this way. An id outside [0, n_buckets) raises SCFA_ERR_INVALID in the
+ *   workspace's status word (scfa_get_device_status) and takes no slot; the
+ *   outputs are then undefined. Same workspace as lsh_bucket_sort.
  * lsh_gather: x_sorted[b,h,s,:] = x[b,h,perm[b,h,s],:] for the T_sorted rows
  *   s of each head (x has T rows per head); a zero row where perm[b,h,s] is
  *   outside [0, T).
  * lsh_unsort: y[b,h,perm[b,h,s],:] = y_sorted[b,h,s,:]. Rows whose perm entry
- *   is out of [0, T) are skipped. Pass T_sorted = T for the plain layout.
+ *   is out of [0, T) are skipped. T_sorted (rows per head of the sorted
+ *   tensor and of perm) may be anything >= 1: T for the plain layout, more
+ *   for the tile-aligned one, fewer for a QK compaction (scfa_qk_select).
  * ------------------------------------------------------------------------- */
 size_t lsh_workspace_size(int B, int H, int T, int n_buckets);
 scfa_status lsh_hash(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D,
@@ -271,6 +295,9 @@ scfa_status lsh_bucket_sort_tiled(const uint16_t* x, const uint16_t* R, int B, i
                                   int n_buckets, int T_sorted, int32_t pad, int32_t* hash_sorted,
                                   int32_t* perm, int32_t* bucket_start, uint16_t* x_sorted,
                                   void* ws, size_t ws_bytes, unsigned flags, void* stream);
+scfa_status lsh_sort_ids(const int32_t* hash, int B, int H, int T, int n_buckets, int T_sorted,
+                         int32_t pad, int32_t* hash_sorted, int32_t* perm, int32_t* bucket_start,
+                         void* ws, size_t ws_bytes, unsigned flags, void* stream);
 scfa_status lsh_gather(const uint16_t* x, const int32_t* perm, int B, int H, int T, int T_sorted,
                        int D, uint16_t* x_sorted, void* stream);
 scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int H, int T, int T_sorted,

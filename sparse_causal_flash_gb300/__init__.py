@@ -56,6 +56,8 @@ _SIGS = {
     "lsh_bucket_sort": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _U, _P], _I),
     "scfa_tiled_rows": ([_I, _I], _I),
     "lsh_bucket_sort_tiled": ([_P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P, _P, _S, _U, _P], _I),
+    "lsh_sort_ids": ([_P, _I, _I, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P, _S, _U, _P], _I),
+    "scfa_qk_select": ([_P, _I, _I, _I, _I, ctypes.c_int32, _P, _P, _P], _I),
     "lsh_gather": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "lsh_unsort": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "scfa_tiles": ([_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _U, _P], _I),
@@ -233,6 +235,23 @@ def lsh_bucket_sort_tiled(x, R, n_buckets, pad, hash_sorted, perm, bucket_start,
     _check("lsh_bucket_sort_tiled", _lib.lsh_bucket_sort_tiled(
         _ptr(x), _ptr(R), B, H, T, D, n_buckets, perm.shape[2], int(pad), _ptr(hash_sorted), _ptr(perm),
         _ptr(bucket_start), _ptr(x_sorted), _ptr(ws), ws.numel(), flags, _stream(stream)))
+
+
+def lsh_sort_ids(hash_, n_buckets, pad, hash_sorted, perm, bucket_start, ws, flags=0, stream=None):
+    """Stable sort of given bucket ids [B,H,T]: plain layout when perm has T
+    rows per head, tile-aligned when it has scfa_tiled_rows(T, n_buckets)."""
+    B, H, T = hash_.shape
+    _check("lsh_sort_ids", _lib.lsh_sort_ids(_ptr(hash_), B, H, T, n_buckets, perm.shape[2], int(pad),
+                                             _ptr(hash_sorted), _ptr(perm), _ptr(bucket_start), _ptr(ws),
+                                             ws.numel(), flags, _stream(stream)))
+
+
+def scfa_qk_select(keep, sentinel, idx, count, stream=None):
+    """Positions of the kept tokens of each head (ascending), then the
+    sentinel: keep [B,H,T] uint8 -> idx [B,H,Tc] int32, count [B,H] int32."""
+    B, H, T = keep.shape
+    _check("scfa_qk_select", _lib.scfa_qk_select(_ptr(keep), B, H, T, idx.shape[2], int(sentinel), _ptr(idx),
+                                                 _ptr(count), _stream(stream)))
 
 
 def lsh_gather(x, perm, x_sorted, stream=None):

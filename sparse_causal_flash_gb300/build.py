@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(os.path.dirname(HERE), "_build")
 LIB = os.path.join(HERE, "libscfa.so")
-SOURCES = ["api.cu", "tiles.cu", "lsh.cu", "attn_fwd.cu", "attn_bwd.cu", "coverage.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "tiles.cu", "lsh.cu", "attn_fwd.cu", "attn_bwd.cu", "coverage.cu", "noalloc.cu", "select.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]

@@ -454,9 +454,41 @@ scfa_status lsh_bucket_sort_tiled(const uint16_t* x, const uint16_t* R, int B, i
   return finish(e, flags, st);
 }
 
+scfa_status lsh_sort_ids(const int32_t* hash, int B, int H, int T, int n_buckets, int T_sorted, int32_t pad,
+                         int32_t* hash_sorted, int32_t* perm, int32_t* bucket_start, void* ws, size_t ws_bytes,
+                         unsigned flags, void* stream) {
+  if (!hash || !hash_sorted || !perm || !bucket_start || !ws || B < 1 || H < 1 || T < 1) return SCFA_ERR_INVALID;
+  if (n_buckets < 1 || n_buckets > kMaxBuckets) return SCFA_ERR_INVALID;
+  const bool tiled = T_sorted != T;
+  if (tiled) {
+    const int need = scfa_tiled_rows(T, n_buckets);
+    if (need < 0 || T_sorted < need || (pad >= 0 && pad < T)) return SCFA_ERR_INVALID;
+  }
+  LshWs L;
+  if (!lsh_ws_layout(B, H, T, n_buckets, &L)) return SCFA_ERR_INVALID;
+  if (!aligned256(ws) || ws_bytes < L.total) return SCFA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  int* status = reinterpret_cast<int*>(w + L.header);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = launch_ids_check(hash, static_cast<long long>(B) * H * T, n_buckets, status, st);
+  int32_t* chunk = reinterpret_cast<int32_t*>(w + L.chunk);
+  if (e == cudaSuccess && !tiled) e = launch_bucket_sort(hash, B * H, T, n_buckets, perm, hash_sorted, bucket_start,
+                                                         chunk, st);
+  if (e == cudaSuccess && tiled) {
+    int32_t* perm_u = reinterpret_cast<int32_t*>(w + L.perm_u);
+    int32_t* off_u = reinterpret_cast<int32_t*>(w + L.off_u);
+    e = launch_bucket_sort(hash, B * H, T, n_buckets, perm_u, reinterpret_cast<int32_t*>(w + L.hs_u), off_u, chunk,
+                           st);
+    if (e == cudaSuccess)
+      e = launch_tiled_layout(perm_u, off_u, B * H, T, T_sorted, n_buckets, pad, perm, hash_sorted, bucket_start, st);
+  }
+  return finish(e, flags, st);
+}
+
 scfa_status lsh_gather(const uint16_t* x, const int32_t* perm, int B, int H, int T, int T_sorted, int D,
                        uint16_t* x_sorted, void* stream) {
-  if (!x || !perm || !x_sorted || B < 1 || H < 1 || T < 1 || T_sorted < T) return SCFA_ERR_INVALID;
+  if (!x || !perm || !x_sorted || B < 1 || H < 1 || T < 1 || T_sorted < 1) return SCFA_ERR_INVALID;
   if (D < 8 || (D % 8) != 0) return SCFA_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(x_sorted)) return SCFA_ERR_INVALID;
   return finish(launch_gather(x, perm, B * H, T_sorted, T, D, x_sorted, false, static_cast<cudaStream_t>(stream)),
@@ -465,7 +497,7 @@ scfa_status lsh_gather(const uint16_t* x, const int32_t* perm, int B, int H, int
 
 scfa_status lsh_unsort(const uint16_t* y_sorted, const int32_t* perm, int B, int H, int T, int T_sorted, int D,
                        uint16_t* y, void* stream) {
-  if (!y_sorted || !perm || !y || B < 1 || H < 1 || T < 1 || T_sorted < T) return SCFA_ERR_INVALID;
+  if (!y_sorted || !perm || !y || B < 1 || H < 1 || T < 1 || T_sorted < 1) return SCFA_ERR_INVALID;
   if (D < 8 || (D % 8) != 0) return SCFA_ERR_UNSUPPORTED;
   if (!aligned16(y_sorted) || !aligned16(y)) return SCFA_ERR_INVALID;
   return finish(launch_gather(y_sorted, perm, B * H, T_sorted, T, D, y, true, static_cast<cudaStream_t>(stream)), 0,

@@ -98,6 +98,8 @@ cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int n_buckets
 // Ts rows per head in the sorted tensor, To in the original-order one
 cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int BH, int Ts, int To, int D,
                           uint16_t* out, bool unsort, cudaStream_t st);
+// bucket ids outside [0, nb) -> SCFA_ERR_INVALID in *status
+cudaError_t launch_ids_check(const int32_t* ids, long long n, int nb, int* status, cudaStream_t st);
 // plain sorted order (perm_u, off_u) -> tile-aligned order of Ts rows per head
 cudaError_t launch_tiled_layout(const int32_t* perm_u, const int32_t* off_u, int BH, int T, int Ts, int nb, int pad,
                                 int32_t* perm, int32_t* hash_sorted, int32_t* start, cudaStream_t st);

@@ -775,7 +775,8 @@ __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int 
   int32_t* my = hist + w * nb;
   for (int base = b0; base < b1; base += 32) {
     const int i = base + lane;
-    const int h = i < b1 ? hrow[i] : -1;
+    int h = i < b1 ? hrow[i] : -1;
+    if (h >= nb) h = -1;  // an id outside [0, nb) takes no slot (the id check reports it)
     const unsigned peers = __match_any_sync(0xffffffffu, h);
     if (h >= 0 && (peers & ((1u << lane) - 1u)) == 0) my[h] += __popc(peers);
     __syncwarp();
@@ -825,7 +826,8 @@ __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int 
   __syncthreads();
   for (int base = b0; base < b1; base += 32) {
     const int i = base + lane;
-    const int h = i < b1 ? hrow[i] : -1;
+    int h = i < b1 ? hrow[i] : -1;
+    if (h >= nb) h = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, h);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const int start = h >= 0 ? my[h] : 0;
@@ -1000,6 +1002,24 @@ cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int nb,
   if (e != cudaSuccess) return e;
   bucket_sort_kernel<<<static_cast<int>(g), nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off, 2,
                                                                   kSortChunk, n_chunks, chunk_ws);
+  return cudaGetLastError();
+}
+
+// Bucket ids given by the caller: any outside [0, nb) raises the status word.
+__global__ void ids_check_kernel(const int32_t* __restrict__ ids, long long n, int nb, int* status) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    bad |= ids[i] < 0 || ids[i] >= nb;
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) raise_status(status, SCFA_ERR_INVALID);
+}
+
+cudaError_t launch_ids_check(const int32_t* ids, long long n, int nb, int* status, cudaStream_t st) {
+  long long g = (n + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  ids_check_kernel<<<static_cast<int>(g), 256, 0, st>>>(ids, n, nb, status);
   return cudaGetLastError();
 }
 

@@ -18,7 +18,8 @@ from __future__ import annotations
 import torch
 
 from . import (FLAG_KEEP_O32, FLAG_ORIGINAL_ORDER, FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size,
-               attn_workspace_size_live, lsh_bucket_sort, lsh_bucket_sort_tiled, lsh_gather, lsh_workspace_size,
+               attn_workspace_size_live, lsh_bucket_sort, lsh_bucket_sort_tiled, lsh_gather, lsh_hash, lsh_sort_ids,
+               lsh_workspace_size,
                scfa_dense_bwd, scfa_tiled_rows,
                scfa_dense_fwd, scfa_hash_bwd, scfa_hash_fwd, scfa_qk_bwd, scfa_qk_fwd, scfa_tiles_count, workspace)
 
@@ -34,15 +35,19 @@ class Step:
     """Buffers and the launch sequence of one fwd+bwd step for a fixed shape."""
 
     def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
-                 device="cuda", flags: int = 0, tiled=None):
+                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False):
         """tiled (hash mode; the default): sort into the tile-aligned layout,
         every bucket starting on a tile boundary (lsh_bucket_sort_tiled); the
         sorted tensors then have Ts = scfa_tiled_rows(T, n_buckets) rows per
-        head. tiled=False keeps the plain sorted order (Ts = T)."""
+        head. tiled=False keeps the plain sorted order (Ts = T).
+        shared_qk (hash mode): one hash per token, of its query, for both its
+        query and its key (Reformer's shared-QK hashing); keys are sorted by
+        those ids (lsh_sort_ids), so every token shares a bucket with itself."""
         self.mode, self.B, self.H, self.Tq, self.Tk, self.D = mode, B, H, Tq, Tk, D
         self.nb = n_buckets
         self.flags = flags
         self.tiled = mode == MODE_HASH and (tiled is None or bool(tiled))
+        self.shared_qk = mode == MODE_HASH and bool(shared_qk)
         # rows per head of the sorted tensors (hash mode) or of q / k
         self.Ts = scfa_tiled_rows(Tq, n_buckets) if self.tiled else Tq
         dev = torch.device(device)
@@ -87,6 +92,8 @@ class Step:
             self.k_s = torch.empty((B, H, Ts, D), **bf)
             self.v_s = torch.empty((B, H, Ts, D), **bf)
             self.do_s = torch.empty((B, H, Ts, D), **bf)
+            if self.shared_qk:
+                self.ids = torch.empty((B, H, T), **i32)  # bucket ids in original order
 
     def run(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None, stream=None, mark=None):
         """Forward + backward. Results land in self.o/lse/dq/dk/dv.
@@ -110,27 +117,13 @@ class Step:
                         fr, stream)
             tick("bwd")
         else:
-            nb = self.nb
             main = stream if stream is not None else torch.cuda.current_stream()
             # key side (hash, sort, K and V gathers) on the second stream
             side = self.side if mark is None else main
-            self.ev[0].record(main)
-            side.wait_event(self.ev[0])
-            if self.tiled:
-                lsh_bucket_sort_tiled(k, R, nb, K_PAD, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
+            if self.shared_qk:
+                self._shared_qk_sorts(q, k, v, do, R, main, side, tick)
             else:
-                lsh_bucket_sort(k, R, nb, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
-            tick("hash_sort_gather_k")
-            lsh_gather(v, self.pk, self.v_s, side)
-            tick("gather_v")
-            self.ev[1].record(side)
-            if self.tiled:
-                lsh_bucket_sort_tiled(q, R, nb, Q_PAD, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
-            else:
-                lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
-            tick("hash_sort_gather_q")
-            lsh_gather(do, self.pq, self.do_s, main)
-            tick("gather_do")
+                self._sorts(q, k, v, do, R, main, side, tick)
             main.wait_event(self.ev[1])
             if self.live_sized:
                 self._size_lists(main)
@@ -145,6 +138,41 @@ class Step:
             tick("bwd")
         return self
 
+    def _shared_qk_sorts(self, q, k, v, do, R, main, side, tick):
+        nb = self.nb
+        lsh_hash(q, R, nb, self.ids, main)
+        tick("hash_q")
+        self.ev[0].record(main)
+        side.wait_event(self.ev[0])
+        lsh_sort_ids(self.ids, nb, K_PAD, self.kh, self.pk, self.offk, self.ws_lk, 0, side)
+        lsh_gather(k, self.pk, self.k_s, side)
+        lsh_gather(v, self.pk, self.v_s, side)
+        tick("sort_gather_k_v")
+        self.ev[1].record(side)
+        lsh_sort_ids(self.ids, nb, Q_PAD, self.qh, self.pq, self.offq, self.ws_l, 0, main)
+        lsh_gather(q, self.pq, self.q_s, main)
+        lsh_gather(do, self.pq, self.do_s, main)
+        tick("sort_gather_q_do")
+
+    def _sorts(self, q, k, v, do, R, main, side, tick):
+        nb = self.nb
+        self.ev[0].record(main)
+        side.wait_event(self.ev[0])
+        if self.tiled:
+            lsh_bucket_sort_tiled(k, R, nb, K_PAD, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
+        else:
+            lsh_bucket_sort(k, R, nb, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
+        tick("hash_sort_gather_k")
+        lsh_gather(v, self.pk, self.v_s, side)
+        tick("gather_v")
+        self.ev[1].record(side)
+        if self.tiled:
+            lsh_bucket_sort_tiled(q, R, nb, Q_PAD, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
+        else:
+            lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
+        tick("hash_sort_gather_q")
+        lsh_gather(do, self.pq, self.do_s, main)
+        tick("gather_do")
 
     def _size_lists(self, stream):
         """Count this batch's live tiles (reads one int back) and grow the
@@ -176,10 +204,10 @@ class HostPipeline:
     INPUTS = ("q", "k", "v", "do", "q_idx", "k_idx", "R")
 
     def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
-                 device="cuda", flags: int = 0, tiled=None):
+                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False):
         self.device = torch.device(device)
         self.steps = [Step(mode, B, H, Tq, Tk, D, n_buckets=n_buckets, device=self.device, flags=flags,
-                           tiled=tiled)
+                           tiled=tiled, shared_qk=shared_qk)
                       for _ in range(2)]
         self.h2d = torch.cuda.Stream(device=self.device)
         self.d2h = torch.cuda.Stream(device=self.device)

@@ -775,3 +775,101 @@ def test_host_pipeline_overlapped_copies(scfa):
             check_close(f"step {i} dQ[{b},{h}]", dq[b, h], r["dq"])
             check_close(f"step {i} dK[{b},{h}]", dk[b, h], r["dk"])
             check_close(f"step {i} dV[{b},{h}]", dv[b, h], r["dv"])
+
+
+# ------------------------------------------------------------------ NEXT-3 variants
+@pytest.mark.parametrize("B,H,T,p_keep,seed", [(2, 3, 1000, 0.7, 91), (1, 2, 20000, 0.3, 92), (1, 4, 300, 1.0, 93)])
+def test_qk_select_and_compaction_bitexact(scfa, B, H, T, p_keep, seed):
+    """The selection step on the device: kept positions and counts bit for
+    bit against the oracle; the compaction through them (lsh_gather) equals
+    the workload's own compacted Q/K/V/dO and positions; lsh_unsort puts the
+    kept rows back and leaves the dropped ones alone; an all-dropped head and
+    a too-short Tc are reported through the counts."""
+    from oracle import qk_select
+    D = 64
+    wl = synth.Workload("sel", "qk", B, H, T, D, seed, p_keep=p_keep)
+    prob = synth.make_problem(wl)
+    full = {n: synth.normal_bf16(seed, tid, (B, H, T, D)) for n, tid in
+            (("q", synth.TID_Q), ("k", synth.TID_K), ("v", synth.TID_V), ("do", synth.TID_DO))}
+    masks = {"q": synth.keep_mask(seed, synth.TID_KEEP_Q, B, H, T, p_keep),
+             "k": synth.keep_mask(seed, synth.TID_KEEP_K, B, H, T, p_keep)}
+    for side, sent, rows, want_idx in (("q", Q_PAD, ("q", "do"), prob.q_idx), ("k", K_PAD, ("k", "v"), prob.k_idx)):
+        Tc = want_idx.shape[2]
+        keep = torch.from_numpy(masks[side].astype(np.uint8)).cuda()
+        idx = torch.empty((B, H, Tc), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((B, H), dtype=torch.int32, device="cuda")
+        scfa.scfa_qk_select(keep, sent, idx, cnt)
+        ref_idx, ref_cnt = qk_select.select_positions(masks[side], Tc, sent)
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+        np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
+        np.testing.assert_array_equal(idx.cpu().numpy(), want_idx.numpy())
+        for n in rows:
+            xc = torch.full((B, H, Tc, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+            scfa.lsh_gather(cuda(full[n]), idx, xc)
+            assert torch.equal(xc.cpu().view(torch.int16), getattr(prob, n).view(torch.int16)), n
+            back = torch.zeros((B, H, T, D), dtype=torch.bfloat16, device="cuda")
+            scfa.lsh_unsort(xc, idx, back)
+            kept = torch.from_numpy(masks[side])[..., None]
+            want = torch.where(kept, full[n], torch.zeros_like(full[n]))
+            assert torch.equal(back.cpu().view(torch.int16), want.view(torch.int16)), n
+    # one head keeps nothing, and a Tc shorter than the largest count
+    keep = torch.from_numpy(masks["q"].astype(np.uint8)).cuda()
+    keep[0, 0] = 0
+    Tc = max(1, int(keep.sum(-1).max()) // 2)
+    idx = torch.empty((B, H, Tc), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((B, H), dtype=torch.int32, device="cuda")
+    scfa.scfa_qk_select(keep, Q_PAD, idx, cnt)
+    ref_idx, ref_cnt = qk_select.select_positions(keep.cpu().numpy(), Tc, Q_PAD)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
+    assert int(cnt[0, 0]) == 0 and bool(torch.all(idx[0, 0] == Q_PAD))
+
+
+def test_lsh_sort_ids_layouts_and_bad_ids(scfa):
+    """Sorting given bucket ids (no hashing): the plain layout and the
+    tile-aligned one bit for bit against the oracle; an id outside
+    [0, n_buckets) is reported in the status word (it takes no slot)."""
+    B, H, T, nb = 2, 3, 3000, 37
+    rng = np.random.default_rng(95)
+    ids = rng.integers(0, nb, (B, H, T)).astype(np.int32)
+    ids[0, 1, :900] = 5  # one large bucket
+    g = torch.from_numpy(ids).cuda()
+    ws = scfa.workspace(scfa.lsh_workspace_size(B, H, T, nb))
+    dev = dict(dtype=torch.int32, device="cuda")
+    for Ts, pad in ((T, 0), (scfa.scfa_tiled_rows(T, nb), K_PAD)):
+        hs, perm = torch.empty((B, H, Ts), **dev), torch.empty((B, H, Ts), **dev)
+        start = torch.empty((B, H, nb + 1), **dev)
+        scfa.lsh_sort_ids(g, nb, pad, hs, perm, start, ws)
+        want = sorted_views(ids, nb, None if Ts == T else Ts, pad)
+        for got, ref in zip((perm, hs, start), want):
+            np.testing.assert_array_equal(got.cpu().numpy(), ref)
+        assert scfa.scfa_get_device_status(ws) == 0
+    bad = g.clone()
+    bad[1, 2, 17] = nb
+    hs, perm = torch.empty((B, H, T), **dev), torch.empty((B, H, T), **dev)
+    start = torch.empty((B, H, nb + 1), **dev)
+    scfa.lsh_sort_ids(bad, nb, 0, hs, perm, start, ws)
+    assert scfa.scfa_get_device_status(ws) == 1  # SCFA_ERR_INVALID
+
+
+@pytest.mark.parametrize("tiled", [False, True])
+def test_shared_qk_hash_parity(scfa, tiled):
+    """Shared-QK hashing: one bucket id per token, from its query, used for
+    its key too (keys sorted by their queries' ids). Against the oracle's
+    hash-sparse attention with k_hash = q_hash."""
+    from sparse_causal_flash_gb300.pipeline import Step
+    B, H, T, D, nb = 1, 2, 1000, 64, 8
+    p = synth.make_problem(synth.Workload("sq", "hash", B, H, T, D, 97, n_buckets=nb))
+    st = Step(scfa.MODE_HASH, B, H, T, T, D, n_buckets=nb, tiled=tiled, shared_qk=True)
+    st.run(cuda(p.q), cuda(p.k), cuda(p.v), cuda(p.do), p.wl.scale, R=cuda(p.R))
+    torch.cuda.synchronize()
+    assert scfa.scfa_get_device_status(st.ws_b) == 0
+    qh = lsh.lsh_hash(p.q.double().numpy(), p.R.double().numpy())
+    Ts = st.Ts if tiled else None
+    pq, qs, _ = sorted_views(qh, nb, Ts, Q_PAD)
+    pk, ks, _ = sorted_views(qh, nb, Ts, K_PAD)
+    np.testing.assert_array_equal(st.pq.cpu().numpy(), pq)
+    np.testing.assert_array_equal(st.pk.cpu().numpy(), pk)
+    np.testing.assert_array_equal(st.kh.cpu().numpy(), ks)
+    ref, _, _ = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, p.wl.scale, q_hash=qh, k_hash=qh)
+    compare_heads(st, ref, ref.keys(), lse_perm=pq)
