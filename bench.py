@@ -366,6 +366,7 @@ class Runner:
         self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
         self.peak_burst, self.peak_sus, self.peak_kind = peaks
         self.dense_cache = {}
+        self.graphs = []  # captured steps alive while they are timed
 
     def timed(self, run, K, kernel_events=False):
         """K steps, each after an L2 flush, CUDA events on the compute stream."""
@@ -430,6 +431,18 @@ class Runner:
                 prev = e
         return {n: statistics.median(v) for n, v in out.items()}
 
+    def graph_run(self, step, args_, kw, scale):
+        """The step as one CUDA graph (graph.replay per step), or None when it
+        cannot be captured (live-sized lists are read back every step)."""
+        if getattr(step, "live_sized", False):
+            return None
+        g = step.capture(*args_, scale, **kw)
+        self.graphs.append(g)
+        for _ in range(3):
+            g.replay()
+        self.torch.cuda.synchronize()
+        return g.replay
+
     def dense_ms(self, wl, K):
         from sparse_causal_flash_gb300.pipeline import Step
         import synth
@@ -443,10 +456,13 @@ class Runner:
             once = wl.T >= (1 << 20)  # a dense 2^20-token causal step takes seconds: timed once
             for _ in range(0 if once else 3):
                 run()
+            if not once:
+                run = self.graph_run(dstep, t, {}, wl.scale) or run
             n = 1 if once else K
             dms, _, _, _ = self.timed(run, n)
             self.dense_cache[key] = (sum(dms) / n, n)
-            del dstep, t
+            self.graphs.clear()
+            del dstep, t, run
             torch.cuda.empty_cache()
         return self.dense_cache[key]
 
@@ -471,10 +487,23 @@ class Runner:
         assert scfa.scfa_get_device_status(step.ws_b) == 0, f"{wl.name}: device status not ok after warm-up"
         pairs = admissible_pairs(scfa, wl, prob, step, dev)
         useful = 14.0 * D * pairs
-        ms, kms, t0, t1 = self.timed(run, steps, kernel_events=True)
+        # kernel times: eager steps with the library's events around the two
+        # attention kernels
+        ms_eager, kms, t0e, t1e = self.timed(run, steps, kernel_events=True)
         assert scfa.scfa_get_device_status(step.ws_b) == 0, f"{wl.name}: device status not ok after the timed steps"
         fwd_ms, bwd_ms = statistics.mean(kms[0]), statistics.mean(kms[1])
-        long_region = (t1 - t0) > 1.0
+        long_region = (t1e - t0e) > 1.0
+        # the step time: the whole step as one CUDA graph replayed per step (no
+        # per-launch gaps), eager where the step cannot be captured
+        grun = self.graph_run(step, args_, kw, wl.scale)
+        graphed = grun is not None
+        if graphed:
+            ms, _, t0, t1 = self.timed(grun, steps)
+            assert scfa.scfa_get_device_status(step.ws_b) == 0, f"{wl.name}: device status not ok after the graph steps"
+            self.graphs.clear()
+            del grun
+        else:
+            ms, t0, t1 = ms_eager, t0e, t1e
         peak = self.peak_sus if long_region else self.peak_burst
         if bwd_ms >= fwd_ms:
             dom = "attn_bwd_kernel" if D == 64 else "attn_bwd128_kernel"
@@ -493,7 +522,9 @@ class Runner:
                             "fwd_kernel_ms": fwd_ms, "bwd_kernel_ms": bwd_ms,
                             "fwd_kernel_tflops": 4.0 * D * pairs / (fwd_ms / 1e3) / 1e12,
                             "bwd_kernel_tflops": 10.0 * D * pairs / (bwd_ms / 1e3) / 1e12},
-               "timed_region_s": t1 - t0, "_t0": t0, "_t1": t1}
+               "timed_region_s": t1 - t0, "_t0": t0, "_t1": t1,
+               "launch": "one CUDA graph per step (graph.replay)" if graphed else "eager",
+               "ms_per_step_eager": sum(ms_eager) / steps}
         rec["pct_of_bf16_peak"] = 100.0 * rec["useful_tflops"] / peak
         if wl.mode == "qk":
             rec["p_keep"] = wl.p_keep
@@ -514,11 +545,13 @@ class Runner:
                              tiled=False)
                 nrun = lambda: nstep.run(*args_, wl.scale, **kw)
                 nrun()
+                nrun = self.graph_run(nstep, args_, kw, wl.scale) or nrun
                 nk = max(3, steps // 4)
                 nms, _, _, _ = self.timed(nrun, nk)
                 rec["naive_no_prune"] = {"ms_per_step": sum(nms) / nk, "steps": nk,
                                          "speedup_scfa_vs_naive": (sum(nms) / nk) / rec["ms_per_step"]}
-                del nstep
+                self.graphs.clear()
+                del nstep, nrun
                 torch.cuda.empty_cache()
                 d_ms, dn = self.dense_ms(wl, max(3, steps // 4))
                 rec["dense"] = {"ms_per_step": d_ms, "steps": dn,
@@ -663,6 +696,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
             "pct_of_bf16_peak": 100.0 * (value / world) / roofline["peak"],
+            "launch": rec.get("launch"), "ms_per_step_eager": rec.get("ms_per_step_eager"),
             "dense": rec.get("dense"), "naive_no_prune": rec.get("naive_no_prune"), "stages_ms": rec.get("stages_ms"),
             "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
             "gpu_launches": kernels_per_step(wl.mode, wl.D, wl.T, getattr(wl, "n_buckets", 0)) * args.steps,

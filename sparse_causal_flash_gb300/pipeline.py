@@ -138,6 +138,21 @@ class Step:
             tick("bwd")
         return self
 
+    def capture(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None):
+        """One whole step (every kernel of run(), both streams joined by
+        events) as a CUDA graph on these input tensors, which must stay
+        alive and in place: graph.replay() reruns it without per-launch
+        overhead. Live-sized steps read the live count back on the host every
+        step and cannot be captured."""
+        if self.live_sized:
+            raise RuntimeError("a live-sized step reads its live count on the host and cannot be captured")
+        self.run(q, k, v, do, scale, q_idx=q_idx, k_idx=k_idx, R=R)  # attributes and modules set up
+        torch.cuda.synchronize(self.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(q, k, v, do, scale, q_idx=q_idx, k_idx=k_idx, R=R)
+        return g
+
     def _shared_qk_sorts(self, q, k, v, do, R, main, side, tick):
         nb = self.nb
         lsh_hash(q, R, nb, self.ids, main)
@@ -204,11 +219,16 @@ class HostPipeline:
     INPUTS = ("q", "k", "v", "do", "q_idx", "k_idx", "R")
 
     def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
-                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False):
+                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False, graphs: bool = True):
         self.device = torch.device(device)
         self.steps = [Step(mode, B, H, Tq, Tk, D, n_buckets=n_buckets, device=self.device, flags=flags,
                            tiled=tiled, shared_qk=shared_qk)
                       for _ in range(2)]
+        # graphs: from its second use on, a slot's step runs as one CUDA graph
+        # captured on the slot's device input buffers (not for live-sized
+        # steps, which read their live count back every step)
+        self.use_graphs = bool(graphs)
+        self.graphs = [None, None]
         self.h2d = torch.cuda.Stream(device=self.device)
         self.d2h = torch.cuda.Stream(device=self.device)
         self.inputs = [None, None]
@@ -250,8 +270,19 @@ class HostPipeline:
         if before is not None:
             before(main)
         st = self.steps[s]
-        st.run(dst["q"], dst["k"], dst["v"], dst["do"], scale, q_idx=dst["q_idx"], k_idx=dst["k_idx"], R=dst["R"],
-               stream=main)
+        ins = (dst["q"], dst["k"], dst["v"], dst["do"], scale)
+        kw = dict(q_idx=dst["q_idx"], k_idx=dst["k_idx"], R=dst["R"])
+        if self.use_graphs and self.used[s] and hasattr(st, "capture") and not getattr(st, "live_sized", False):
+            with torch.cuda.stream(main):
+                if self.graphs[s] is None:
+                    self.graphs[s] = (st.capture(*ins, **kw), scale)
+                g, g_scale = self.graphs[s]
+                if g_scale != scale:  # the scale is part of the captured step
+                    st.run(*ins, stream=main, **kw)
+                else:
+                    g.replay()
+        else:
+            st.run(*ins, stream=main, **kw)
         self.computed[s].record(main)
         self.d2h.wait_event(self.computed[s])
         with torch.cuda.stream(self.d2h):
