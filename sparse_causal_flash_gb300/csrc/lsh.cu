@@ -162,6 +162,7 @@ __device__ void lsh_prologue(const uint16_t* __restrict__ R, int D, int m, float
     float mx = 0.f;
     for (int c = threadIdx.x; c < m; c += blockDim.x) {
       float ss = 0.f;
+#pragma unroll 8
       for (int d = 0; d < D; ++d) ss = fmaf(sR[d * m4 + c], sR[d * m4 + c], ss);
       mx = fmaxf(mx, sqrtf(ss * (1.f + static_cast<float>(D + 2) * 0x1p-22f) + static_cast<float>(D) * 0x1p-148f) *
                          1.000001f);
@@ -362,17 +363,20 @@ __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __r
 
 // Second pass after the tensor-core pass: rows it left at -1 (near ties,
 // non-finite or subnormal values, huge magnitudes) get the certified
-// computation, one warp per row. Each warp scans 32 ids at a time and takes
-// the flagged rows one by one: the lanes share the row (staged as fp32 in
-// shared memory), screen the columns lane + 32 k in fp32 with the same bound
-// as the single-thread path (it holds for any summation order), and evaluate
-// every candidate within the threshold of the top exactly, in 128-bit
-// integers; the warp keeps the largest value, the smallest index on ties.
-// A row whose exponent span needs more than 128 bits goes to the
+// computation, one warp per row. A CTA takes kFixSeg consecutive rows at a
+// time: its threads scan the ids, collect the flagged rows (a fraction of a
+// percent) in a shared list, and the warps then share that list evenly. Per
+// row the lanes share the row (staged as fp32 in shared memory), screen the
+// columns lane + 32 k in fp32 with the same bound as the single-thread path
+// (it holds for any summation order), and evaluate every candidate within
+// the threshold of the top exactly in 128-bit integers, one candidate at a
+// time split over the lanes; the largest value wins, the smallest index on
+// ties. A row whose exponent span needs more than 128 bits goes to the
 // single-thread path (576-bit accumulator) on lane 0.
 constexpr int kFixWarps = 8;
+constexpr int kFixSeg = 2048;  // rows per CTA step; the shared list holds up to this many
 
-__global__ void __launch_bounds__(kFixWarps * 32, 1) lsh_fix_kernel(const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(kFixWarps * 32, 2) lsh_fix_kernel(const uint16_t* __restrict__ x,
                                                                  const uint16_t* __restrict__ R, long long rows,
                                                                  int D, int m, int32_t* __restrict__ hash) {
   extern __shared__ float smem[];
@@ -386,16 +390,19 @@ __global__ void __launch_bounds__(kFixWarps * 32, 1) lsh_fix_kernel(const uint16
   float* sx = sxall + warp * D;
   const float rel = static_cast<float>(D + 1) * 0x1p-23f;
   const float absb = static_cast<float>(D) * 0x1p-148f;
-  const long long nwarps = static_cast<long long>(gridDim.x) * kFixWarps;
-  for (long long base = (static_cast<long long>(blockIdx.x) * kFixWarps + warp) * 32; base < rows;
-       base += nwarps * 32) {
-    const long long rl = base + lane;
-    const bool flagged = rl < rows && hash[rl] < 0;
-    unsigned todo = __ballot_sync(0xffffffffu, flagged);
-    while (todo) {
-      const int bit = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const long long r = base + bit;
+  __shared__ int s_n;
+  __shared__ int s_list[kFixSeg];  // offsets of the flagged rows in the segment
+  for (long long seg = static_cast<long long>(blockIdx.x) * kFixSeg; seg < rows;
+       seg += static_cast<long long>(gridDim.x) * kFixSeg) {
+    __syncthreads();  // the previous segment's list is consumed
+    if (threadIdx.x == 0) s_n = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < kFixSeg; i += blockDim.x)
+      if (seg + i < rows && hash[seg + i] < 0) s_list[atomicAdd(&s_n, 1)] = i;
+    __syncthreads();
+    const int n_flag = s_n;
+    for (int li = warp; li < n_flag; li += kFixWarps) {
+      const long long r = seg + s_list[li];
       const uint16_t* xr = x + r * D;
       // stage the row; norm and exponent range of its nonzero entries
       float l2sq = 0.f;
@@ -429,6 +436,7 @@ __global__ void __launch_bounds__(kFixWarps * 32, 1) lsh_fix_kernel(const uint16
       float scv[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) scv[k] = 0.f;
+#pragma unroll 4
       for (int d = 0; d < D; ++d) {
         const float xv = sx[d];
 #pragma unroll
@@ -449,56 +457,56 @@ __global__ void __launch_bounds__(kFixWarps * 32, 1) lsh_fix_kernel(const uint16
       const bool fits128 = !any_term || (xemax + r_emax) - ebase <= 100;
       int h;
       if (fits128) {
+        // candidates (column, sign) one at a time, each summed exactly by the
+        // whole warp: lane l takes d = l, l + 32, ... (an integer sum, so the
+        // order does not matter), then a butterfly of the 128-bit partials
         bool have = false;
         __int128 bv = 0;
         int bj = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int c = lane + 32 * k;
-          if (c >= m) continue;
-          const float sc = scv[k];
-          const bool cp = (t0 - sc <= thr) || (sc != sc);
-          const bool cn = (t0 + sc <= thr) || (sc != sc);
-          if (!cp && !cn) continue;
-          __int128 acc = 0;
-          if (any_term) {
-            for (int d = 0; d < D; ++d) {
-              bool nx, nr2;
-              uint32_t Mx, Mr;
-              int Ex, Er;
-              bf16_parts(static_cast<uint16_t>(__float_as_uint(sx[d]) >> 16), &nx, &Mx, &Ex);
-              bf16_parts(static_cast<uint16_t>(__float_as_uint(sR[d * m4 + c]) >> 16), &nr2, &Mr, &Er);
-              if (Mx == 0 || Mr == 0) continue;
-              const __int128 term = static_cast<__int128>(Mx * Mr) << (Ex + Er - ebase);
-              acc = (nx != nr2) ? acc - term : acc + term;
+          const float sc = c < m ? scv[k] : 0.f;
+          const bool cp = c < m && ((t0 - sc <= thr) || (sc != sc));
+          const bool cn = c < m && ((t0 + sc <= thr) || (sc != sc));
+          unsigned todo_c = __ballot_sync(0xffffffffu, cp || cn);
+          const unsigned pos_mask = __ballot_sync(0xffffffffu, cp), neg_mask = __ballot_sync(0xffffffffu, cn);
+          while (todo_c) {
+            const int bit = __ffs(todo_c) - 1;
+            todo_c &= todo_c - 1;
+            const int cc = bit + 32 * k;
+            __int128 acc = 0;
+            if (any_term) {
+              for (int d = lane; d < D; d += 32) {
+                bool nx, nr2;
+                uint32_t Mx, Mr;
+                int Ex, Er;
+                bf16_parts(static_cast<uint16_t>(__float_as_uint(sx[d]) >> 16), &nx, &Mx, &Ex);
+                bf16_parts(static_cast<uint16_t>(__float_as_uint(sR[d * m4 + cc]) >> 16), &nr2, &Mr, &Er);
+                if (Mx == 0 || Mr == 0) continue;
+                const __int128 term = static_cast<__int128>(Mx * Mr) << (Ex + Er - ebase);
+                acc = (nx != nr2) ? acc - term : acc + term;
+              }
             }
-          }
-          // candidate c (+s), then m + c (-s): this lane's columns ascend, so a
-          // strict comparison keeps the smallest index among its own ties
-          if (cp && (!have || acc > bv || (acc == bv && c < bj))) {
-            bv = acc;
-            bj = c;
-            have = true;
-          }
-          if (cn && (!have || -acc > bv || (-acc == bv && c + m < bj))) {
-            bv = -acc;
-            bj = c + m;
-            have = true;
-          }
-        }
-        // warp arg-max: larger value, then smaller index
-        for (int o = 16; o; o >>= 1) {
-          const unsigned long long lo = static_cast<unsigned long long>(bv);
-          const long long hi = static_cast<long long>(bv >> 64);
-          const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, o);
-          const long long ohi = __shfl_xor_sync(0xffffffffu, hi, o);
-          const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-          const int oh = __shfl_xor_sync(0xffffffffu, have ? 1 : 0, o);
-          const __int128 ov = (static_cast<__int128>(ohi) << 64) | static_cast<__int128>(olo);
-          if (oh && (!have || ov > bv || (ov == bv && oj < bj))) {
-            bv = ov;
-            bj = oj;
-            have = true;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+              const unsigned long long lo = static_cast<unsigned long long>(acc);
+              const long long hi = static_cast<long long>(acc >> 64);
+              const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, o);
+              const long long ohi = __shfl_xor_sync(0xffffffffu, hi, o);
+              acc += (static_cast<__int128>(ohi) << 64) | static_cast<__int128>(olo);
+            }
+            // (+) column cc, then (-) column cc + m: larger value, then smaller index
+            if (((pos_mask >> bit) & 1u) && (!have || acc > bv || (acc == bv && cc < bj))) {
+              bv = acc;
+              bj = cc;
+              have = true;
+            }
+            if (((neg_mask >> bit) & 1u) && (!have || -acc > bv || (-acc == bv && cc + m < bj))) {
+              bv = -acc;
+              bj = cc + m;
+              have = true;
+            }
           }
         }
         h = bj;
@@ -675,9 +683,13 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       // ||x||_2 of this row from the staged tile (rounded up), and a check
-      // for subnormal / non-finite entries
+      // for subnormal entries. Both bf16 halves of a word at once: with a
+      // the magnitude bits of a half, a + 0x7F80 reaches bit 15 iff the
+      // exponent is nonzero, a + 0x7FFF iff a != 0 (neither carries out of
+      // the half). A non-finite entry makes l2sq inf or NaN, which the
+      // l2 < 2^60 test below turns away.
       float l2sq = 0.f;
-      bool x_bad = false;
+      uint32_t sub_bits = 0;
 #pragma unroll
       for (int sub = 0; sub < D / 64; ++sub) {
 #pragma unroll
@@ -688,12 +700,12 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
           for (int u = 0; u < 4; ++u) {
             const float lo = __uint_as_float(wv[u] << 16), hi = __uint_as_float(wv[u] & 0xFFFF0000u);
             l2sq = fmaf(lo, lo, fmaf(hi, hi, l2sq));
-            const uint32_t e0 = (wv[u] >> 7) & 0xFFu, m0 = wv[u] & 0x7Fu;
-            const uint32_t e1 = (wv[u] >> 23) & 0xFFu, m1 = (wv[u] >> 16) & 0x7Fu;
-            x_bad = x_bad || (e0 == 0 && m0 != 0) || e0 == 0xFFu || (e1 == 0 && m1 != 0) || e1 == 0xFFu;
+            const uint32_t a = wv[u] & 0x7FFF7FFFu;
+            sub_bits |= (a + 0x7FFF7FFFu) & ~(a + 0x7F807F80u);
           }
         }
       }
+      const bool x_bad = (sub_bits & 0x80008000u) != 0;
       mbar_arrive(&sm.x_empty[s]);
       const float l2 = sqrtf(l2sq * (1.f + static_cast<float>(D + 2) * 0x1p-22f)) * 1.000001f;
       const float emax = l2 * rnmax * kTcRel;
@@ -942,8 +954,8 @@ static cudaError_t launch_lsh_tc(const uint16_t* x, const uint16_t* R, long long
   const size_t smem2 = static_cast<size_t>(D) * (((m + 3) & ~3) + kFixWarps) * sizeof(float);
   e = cudaFuncSetAttribute(lsh_fix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem2));
   if (e != cudaSuccess) return e;
-  long long g2 = (rows + kFixWarps * 32 - 1) / (kFixWarps * 32);
-  if (g2 > static_cast<long long>(num_sms())) g2 = static_cast<long long>(num_sms());  // one wave
+  long long g2 = (rows + kFixSeg - 1) / kFixSeg;
+  if (g2 > 2LL * num_sms()) g2 = 2LL * num_sms();  // two CTAs per SM
   if (g2 < 1) g2 = 1;
   lsh_fix_kernel<<<static_cast<int>(g2), kFixWarps * 32, smem2, st>>>(x, R, rows, D, m, hash);
   return cudaGetLastError();

@@ -118,6 +118,20 @@ def test_lsh_hash_tensor_core_path_ties_and_edges(scfa, D, m):
     np.testing.assert_array_equal(h.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("D,m,T", [(64, 8, 3001), (128, 64, 500)])
+def test_lsh_hash_every_row_certified(scfa, D, m, T):
+    # every column of R appears twice, once negated: each row's top value is
+    # an exact tie, so every row goes through the certified second pass with
+    # several candidates; spread over many warps and CTAs
+    half = synth.rotation_bf16(91, D, m // 2)
+    R = torch.cat([half, -half.flip(1)], dim=1)
+    x = synth.normal_bf16(92, 1, (1, 2, T, D))
+    h = torch.empty((1, 2, T), dtype=torch.int32, device="cuda")
+    scfa.lsh_hash(cuda(x), cuda(R), 2 * m, h)
+    ref = lsh.lsh_hash(x.double().numpy(), R.double().numpy())
+    np.testing.assert_array_equal(h.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("B,H,T,D,nb", [(1, 2, 512, 64, 4), (2, 3, 1000, 64, 16), (1, 1, 5000, 64, 512),
                                         (1, 2, 20000, 64, 64), (1, 1, 40000, 128, 512)])
 def test_bucket_sort_and_gather_bitexact(scfa, B, H, T, D, nb):
