@@ -133,8 +133,11 @@ def admissible_pairs(scfa, wl, prob, step, dev) -> int:
     return device
 
 
-def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0, tiled: bool = True) -> int:
-    """Library kernels launched per step (the library's own launch sequence)."""
+def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0, tiled: bool = True,
+                     gather_kv: bool = True) -> int:
+    """Library kernels launched per step (the library's own launch sequence).
+    gather_kv: the attention kernels read K and V rows through the key
+    permutation (the tile-aligned step's default), so neither is moved."""
     # header init, tile stats (q, k), count, scan, fill, work order (+ pair lists at D = 128)
     tiles = 7 + (1 if D == 128 else 0)
     attn = 1 + 3         # forward; backward pre-pass, backward, dQ finalise
@@ -142,7 +145,8 @@ def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0, til
         m = n_buckets // 2
         lsh = 2 if (D in (64, 128) and m % 8 == 0 and 8 <= m <= 256) else 1  # tensor-core pass + certified pass
         sort = (3 if T > 8192 else 1) + (2 if tiled else 0)  # chunk counts, scan, scatter; bucket starts, spread
-        return tiles + attn + 2 * (lsh + sort + 1) + 2   # per q / k: hash, sort, gather; gather V / dO
+        moves = 2 if (tiled and gather_kv) else 4  # Q, dO (and K, V) into sorted order
+        return tiles + attn + 2 * (lsh + sort) + moves  # per q / k: hash, sort
     return tiles + attn
 
 
@@ -530,6 +534,10 @@ class Runner:
             rec["p_keep"] = wl.p_keep
         if wl.mode == "hash":
             rec["n_buckets"] = wl.n_buckets
+            # which row tensors the attention kernels gather through the
+            # sort's permutations instead of reading sorted copies
+            rec["row_gathers"] = ("q, dO" if step.gq else "") + (", " if step.gq and step.gkv else "") + \
+                ("k, v" if step.gkv else "")
         if detail:
             st = self.stages(step, args_, kw, wl.scale)
             st["fwd_kernel"] = fwd_ms

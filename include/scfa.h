@@ -102,7 +102,7 @@ enum {
                                  forward and the backward of one step on the
                                  same workspace. The bf16 rounding of O is
                                  otherwise the largest error term of dS. */
-  SCFA_FLAG_DEBUG_STALL = 64     /* debug: the main attention kernel of the call
+  SCFA_FLAG_DEBUG_STALL = 64,    /* debug: the main attention kernel of the call
                                  withholds the first K / V load of every CTA,
                                  so its pipeline waits on a barrier that
                                  nothing completes; each wait gives up after
@@ -111,6 +111,20 @@ enum {
                                  For testing the timeout path: the CTAs drain
                                  their issued copies and MMAs and exit, and the
                                  device stays usable. */
+  SCFA_FLAG_GATHER_Q = 128,      /* hash mode, with SCFA_FLAG_ORIGINAL_ORDER:
+                                 q (and do in the backward) are also in
+                                 ORIGINAL row order, [B,H,T_orig,D]; the
+                                 attention kernels load sorted query row s of
+                                 head (b,h) from row q_idx[b,h,s] (tile-row
+                                 gathers), so no sorted copy is made. A sorted
+                                 row whose index falls outside [0, T_orig)
+                                 (padding) reads some row of the same head:
+                                 its scores are masked, so for finite inputs
+                                 the results equal those computed from sorted
+                                 copies with zero padding rows. Needs
+                                 B*H*T_orig < 2^31. lse stays in sorted
+                                 order. */
+  SCFA_FLAG_GATHER_KV = 256      /* the same for k and v, through k_idx. */
 };
 
 /* Tiles are SCFA_TILE rows of queries by SCFA_TILE rows of keys. */

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libscfa.so")
 
 MODE_DENSE, MODE_QK, MODE_HASH = 0, 1, 2
 FLAG_NO_PRUNE, FLAG_VALIDATE, FLAG_DEBUG_SYNC, FLAG_REUSE_TILES, FLAG_ORIGINAL_ORDER = 1, 2, 4, 8, 16
-FLAG_KEEP_O32, FLAG_DEBUG_STALL = 32, 64
+FLAG_KEEP_O32, FLAG_DEBUG_STALL, FLAG_GATHER_Q, FLAG_GATHER_KV = 32, 64, 128, 256
 TILE = 128
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "CUDA error", 5: "device timeout"}
 
@@ -190,8 +190,11 @@ def scfa_qk_bwd(q, k, v, o, lse, do, q_idx, k_idx, scale, dq, dk, dv, ws, flags=
 
 def scfa_hash_fwd(q_s, k_s, v_s, q_idx, k_idx, q_hash, k_hash, scale, o_s, lse_s, ws, flags=0, stream=None):
     """o_s: [B,H,T,D] in sorted order, or [B,H,T_orig,D] in original order
-    with FLAG_ORIGINAL_ORDER (its row count is passed as T_orig)."""
-    B, H, T, D = q_s.shape
+    with FLAG_ORIGINAL_ORDER (its row count is passed as T_orig); with
+    FLAG_GATHER_Q q_s, with FLAG_GATHER_KV k_s and v_s are the original-order
+    [B,H,T_orig,D] tensors. T is the sorted row count, from q_idx [B,H,T]."""
+    B, H, T = q_idx.shape
+    D = q_s.shape[3]
     _check("scfa_hash_fwd", _lib.scfa_hash_fwd(_ptr(q_s), _ptr(k_s), _ptr(v_s), _ptr(q_idx), _ptr(k_idx),
                                                _ptr(q_hash), _ptr(k_hash), B, H, T, o_s.shape[2], D, scale,
                                                _ptr(o_s), _ptr(lse_s), _ptr(ws), ws.numel(), flags,
@@ -200,7 +203,8 @@ def scfa_hash_fwd(q_s, k_s, v_s, q_idx, k_idx, q_hash, k_hash, scale, o_s, lse_s
 
 def scfa_hash_bwd(q_s, k_s, v_s, o_s, lse_s, do_s, q_idx, k_idx, q_hash, k_hash, scale, dq_s, dk_s, dv_s, ws,
                   flags=0, stream=None):
-    B, H, T, D = q_s.shape
+    B, H, T = q_idx.shape
+    D = q_s.shape[3]
     _check("scfa_hash_bwd", _lib.scfa_hash_bwd(_ptr(q_s), _ptr(k_s), _ptr(v_s), _ptr(o_s), _ptr(lse_s), _ptr(do_s),
                                                _ptr(q_idx), _ptr(k_idx), _ptr(q_hash), _ptr(k_hash), B, H, T,
                                                dq_s.shape[2], D, scale, _ptr(dq_s), _ptr(dk_s), _ptr(dv_s),

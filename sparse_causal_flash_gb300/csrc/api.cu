@@ -51,6 +51,19 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, long long T, l
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_bf16_rows(CUtensorMap* map, const void* base, int D, long long rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D map over a [BH][T][D] fp32 tensor; box = 32 columns x 128 rows x 1
 // head, 128-byte swizzle (used by TMA reduce-add; rows past T are skipped).
 bool make_tmap_f32_3d(CUtensorMap* map, void* base, int D, long long T, long long BH) {
@@ -216,6 +229,12 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   // original-order tensors have To rows per head (at most the sorted count);
   // without a row map they are the sorted tensors themselves
   if ((flags & SCFA_FLAG_ORIGINAL_ORDER) ? (To < 1 || To > Tq) : To != Tq) return SCFA_ERR_INVALID;
+  // row gathers read original-order inputs through the row maps (the gather
+  // coordinates are 32-bit row numbers)
+  const bool gather_q = (flags & SCFA_FLAG_GATHER_Q) != 0, gather_kv = (flags & SCFA_FLAG_GATHER_KV) != 0;
+  if ((gather_q || gather_kv) &&
+      (!(flags & SCFA_FLAG_ORIGINAL_ORDER) || static_cast<long long>(B) * H * To >= (1ll << 31)))
+    return SCFA_ERR_INVALID;
   if (!backward) {
     if (!o || !lse || !aligned16(o)) return SCFA_ERR_INVALID;
   } else {
@@ -274,6 +293,8 @@ scfa_status run_attention(int mode, bool backward, const uint16_t* q, const uint
   a.To = To;
   a.o32 = keep_o32 ? reinterpret_cast<float*>(w + L.dq_acc) : nullptr;
   a.stall = (flags & SCFA_FLAG_DEBUG_STALL) ? 1 : 0;
+  a.gather_q = gather_q ? 1 : 0;
+  a.gather_kv = gather_kv ? 1 : 0;
   a.ws = w;
   a.L = &L;
   e = backward ? launch_attn_bwd(a, st) : launch_attn_fwd(a, st);

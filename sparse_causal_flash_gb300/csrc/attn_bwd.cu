@@ -102,6 +102,8 @@ struct BwdParams {
   const int32_t* k_rows;  // null, or the original row of each sorted key row
   int To;                 // rows per head of dk / dv when k_rows is set
   int stall;   // SCFA_FLAG_DEBUG_STALL: withhold the first K / V load
+  int gather_q;   // q and do are original-order tensors read by row gathers through q_idx (To rows per head)
+  int gather_kv;  // k and v likewise through k_idx
   int* sched;  // [0] next work item, [1] CTAs done
   int* status;
 };
@@ -195,30 +197,51 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int bh = g / p.nKt, j = g % p.nKt;
       bool ok = true;
       const bool stall = p.stall && item == 0;  // debug stall: K / V never arrive
+      // the item's query tiles are read 32 at a time (one per lane); with
+      // row gathers (p.gather_q, p.gather_kv) every lane issues four rows of each tile, the
+      // source rows of a tile loaded a tile ahead, before the stage wait
+      int cq = lane < n ? csc_rows[start + lane] : 0;
+      int rr[4], rq[4] = {0, 0, 0, 0}, rn[4] = {0, 0, 0, 0};
+      if (p.gather_kv) gather_rows(p.k_idx, bh, p.Tk, p.To, j * kTile, lane, rr);
+      if (p.gather_q) gather_rows(p.q_idx, bh, p.Tq, p.To, __shfl_sync(0xffffffffu, cq, 0) * kTile, lane, rq);
       if (lane == 0 && !stall) {
         ok = mbar_wait(&sm.kv_empty, (item & 1) ^ 1, abort_flag, p.status);
         if (ok) {
           mbar_arrive_expect_tx(&sm.kv_full, 2 * D * kTile * 2);
-          for (int sub = 0; sub < D / 64; ++sub) {
-            tma_load_3d(sm.k[sub], &tm_k, &sm.kv_full, sub * 64, j * kTile, bh);
-            tma_load_3d(sm.v[sub], &tm_v, &sm.kv_full, sub * 64, j * kTile, bh);
+          if (!p.gather_kv) {
+            for (int sub = 0; sub < D / 64; ++sub) {
+              tma_load_3d(sm.k[sub], &tm_k, &sm.kv_full, sub * 64, j * kTile, bh);
+              tma_load_3d(sm.v[sub], &tm_v, &sm.kv_full, sub * 64, j * kTile, bh);
+            }
           }
           last_kv = item;
         }
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      for (int t = 0; t < (stall ? min(n, kQStages) : n); ++t) {
-        const int i = csc_rows[start + t];
+      if (p.gather_kv && !stall) {
+        gather_issue(sm.k[0], kSubBytes, D / 64, &tm_k, &sm.kv_full, rr, lane);
+        gather_issue(sm.v[0], kSubBytes, D / 64, &tm_v, &sm.kv_full, rr, lane);
+      }
+      const int n_steps = stall ? min(n, kQStages) : n;
+      for (int t = 0; t < n_steps; ++t) {
+        const int i = __shfl_sync(0xffffffffu, cq, t & 31);
         const int s = q_it % kQStages;
+        if (t + 1 < n_steps) {
+          if (((t + 1) & 31) == 0) cq = t + 1 + lane < n ? csc_rows[start + t + 1 + lane] : 0;
+          if (p.gather_q)  // Q and dO rows of the next tile
+            gather_rows(p.q_idx, bh, p.Tq, p.To, __shfl_sync(0xffffffffu, cq, (t + 1) & 31) * kTile, lane, rn);
+        }
         if (lane == 0) {
           ok = mbar_wait(&sm.q_empty[s], ((q_it / kQStages) & 1) ^ 1, abort_flag, p.status);
           if (ok) {
             // Q_i, dO_i and the query metadata of tile i (four 512-byte rows
             // of the padded arrays) land on one barrier
             mbar_arrive_expect_tx(&sm.q_full[s], 2 * D * kTile * 2 + 4 * kTile * 4);
-            for (int sub = 0; sub < D / 64; ++sub) {
-              tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
-              tma_load_3d(sm.dO[s][sub], &tm_do, &sm.q_full[s], sub * 64, i * kTile, bh);
+            if (!p.gather_q) {
+              for (int sub = 0; sub < D / 64; ++sub) {
+                tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
+                tma_load_3d(sm.dO[s][sub], &tm_do, &sm.q_full[s], sub * 64, i * kTile, bh);
+              }
             }
             const float* m = p.qm + static_cast<long long>(bh) * p.Tqp + i * kTile;
             bulk_load(sm.lse2[s], m, kTile * 4, &sm.q_full[s]);
@@ -228,6 +251,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+        if (p.gather_q) {
+          gather_issue(sm.q[s][0], kSubBytes, D / 64, &tm_q, &sm.q_full[s], rq, lane);
+          gather_issue(sm.dO[s][0], kSubBytes, D / 64, &tm_do, &sm.q_full[s], rq, lane);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) rq[u] = rn[u];
+        }
         ++q_it;
       }
       if (!ok || stall) break;
@@ -700,36 +729,62 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const int bh = g / p.nKt, j = g % p.nKt;
       bool ok = true;
       const bool stall = p.stall && item == 0;  // debug stall: K / V never arrive
+      // the item's query tiles are read 32 at a time (one per lane); with
+      // row gathers (p.gather_q, p.gather_kv) every lane issues four rows of each tile, the
+      // source rows of a tile loaded a tile ahead, before the stage wait
+      int cq = lane < n ? csc_rows[start + lane] : 0;
+      int rr[4], rq[4] = {0, 0, 0, 0}, rn[4] = {0, 0, 0, 0};
+      if (p.gather_kv) gather_rows(p.k_idx, bh, p.Tk, p.To, j * kTile, lane, rr);
+      if (p.gather_q) gather_rows(p.q_idx, bh, p.Tq, p.To, __shfl_sync(0xffffffffu, cq, 0) * kTile, lane, rq);
       if (lane == 0 && !stall) {
         ok = mbar_wait(&sm.kv_empty, (item & 1) ^ 1, abort_flag, p.status);
         if (ok) {
           mbar_arrive_expect_tx(&sm.kv_full, 2 * D * kTile * 2);
-          for (int sub = 0; sub < 2; ++sub) {
-            tma_load_3d(sm.k[sub], &tm_k, &sm.kv_full, sub * 64, j * kTile, bh);
-            tma_load_3d(sm.v[sub], &tm_v, &sm.kv_full, sub * 64, j * kTile, bh);
+          if (!p.gather_kv) {
+            for (int sub = 0; sub < 2; ++sub) {
+              tma_load_3d(sm.k[sub], &tm_k, &sm.kv_full, sub * 64, j * kTile, bh);
+              tma_load_3d(sm.v[sub], &tm_v, &sm.kv_full, sub * 64, j * kTile, bh);
+            }
           }
           last_kv = item;
         }
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      for (int t = 0; t < (stall ? 1 : n); ++t) {
-        const int i = csc_rows[start + t];
+      if (p.gather_kv && !stall) {
+        gather_issue(sm.k[0], kSubBytes, 2, &tm_k, &sm.kv_full, rr, lane);
+        gather_issue(sm.v[0], kSubBytes, 2, &tm_v, &sm.kv_full, rr, lane);
+      }
+      const int n_steps = stall ? 1 : n;
+      for (int t = 0; t < n_steps; ++t) {
+        const int i = __shfl_sync(0xffffffffu, cq, t & 31);
         const int mb = qt & 1, s = qt & 1;
+        if (t + 1 < n_steps) {
+          if (((t + 1) & 31) == 0) cq = t + 1 + lane < n ? csc_rows[start + t + 1 + lane] : 0;
+          if (p.gather_q)  // Q and dO rows of the next tile
+            gather_rows(p.q_idx, bh, p.Tq, p.To, __shfl_sync(0xffffffffu, cq, (t + 1) & 31) * kTile, lane, rn);
+        }
         if (lane == 0) {
-          // Q into its stage once dK two tiles back has read it; dO and the
-          // query metadata (four 512-byte rows of the padded arrays, kept by
-          // step parity) once dV of the previous tile has read dO
+          // Q into its stage once dK two tiles back has read it
           ok = mbar_wait(&sm.q_empty[s], ((qt >> 1) & 1) ^ 1, abort_flag, p.status);
           if (ok) {
             mbar_arrive_expect_tx(&sm.q_full[s], D * kTile * 2);
-            for (int sub = 0; sub < 2; ++sub)
-              tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
+            if (!p.gather_q)
+              for (int sub = 0; sub < 2; ++sub)
+                tma_load_3d(sm.q[s][sub], &tm_q, &sm.q_full[s], sub * 64, i * kTile, bh);
             q_issued = qt + 1;
-            ok = mbar_wait(&sm.do_empty, (qt & 1) ^ 1, abort_flag, p.status);
           }
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+        if (p.gather_q) gather_issue(sm.q[s][0], kSubBytes, 2, &tm_q, &sm.q_full[s], rq, lane);
+        if (lane == 0) {
+          // dO and the query metadata (four 512-byte rows of the padded
+          // arrays, kept by step parity) once dV of the previous tile has
+          // read dO
+          ok = mbar_wait(&sm.do_empty, (qt & 1) ^ 1, abort_flag, p.status);
           if (ok) {
             mbar_arrive_expect_tx(&sm.do_full, D * kTile * 2 + 4 * kTile * 4);
-            for (int sub = 0; sub < 2; ++sub) tma_load_3d(sm.dO[sub], &tm_do, &sm.do_full, sub * 64, i * kTile, bh);
+            if (!p.gather_q)
+              for (int sub = 0; sub < 2; ++sub) tma_load_3d(sm.dO[sub], &tm_do, &sm.do_full, sub * 64, i * kTile, bh);
             const float* m = p.qm + static_cast<long long>(bh) * p.Tqp + i * kTile;
             bulk_load(sm.lse2[mb], m, kTile * 4, &sm.do_full);
             bulk_load(sm.drs[mb], m + p.qm_n, kTile * 4, &sm.do_full);
@@ -739,6 +794,11 @@ attn_bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           }
         }
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+        if (p.gather_q) {
+          gather_issue(sm.dO[0], kSubBytes, 2, &tm_do, &sm.do_full, rq, lane);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) rq[u] = rn[u];
+        }
         ++qt;
       }
       if (!ok || stall) break;
@@ -1095,7 +1155,8 @@ struct PreParams {
   const uint16_t* dO;
   const float* o32;
   const int32_t* o_rows;
-  int To;             // rows per head of o when o_rows is set
+  const int32_t* do_rows;  // null, or the original row of each sorted row of dO (row gathers)
+  int To;             // rows per head of o (and dO) when o_rows (do_rows) is set
   const float* lse;
   const int32_t* q_idx;
   const int32_t* q_hash;
@@ -1123,7 +1184,8 @@ __global__ void bwd_pre_kernel(const PreParams p) {
     const long long row = bh * p.Tq + r;
     float s = 0.f;
     if (active) {
-      const uint4 b = reinterpret_cast<const uint4*>(p.dO + row * D)[ch];
+      const long long drow = mapped_row(p.do_rows, row, bh, p.To);
+      const uint4 b = drow >= 0 ? reinterpret_cast<const uint4*>(p.dO + drow * D)[ch] : make_uint4(0, 0, 0, 0);
       const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
       if (p.o32 != nullptr) {
         const float4 a0 = reinterpret_cast<const float4*>(p.o32 + row * D)[ch * 2];
@@ -1215,6 +1277,7 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
     pp.dO = a.do_;
     pp.o32 = a.o32;
     pp.o_rows = a.q_rows;
+    pp.do_rows = a.gather_q ? a.q_idx : nullptr;
     pp.To = a.To;
     pp.lse = a.lse_in;
     pp.q_idx = a.q_idx;
@@ -1233,10 +1296,14 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
     bwd_pre_kernel<D><<<static_cast<int>(g), 256, 0, st>>>(pp);
   }
   CUtensorMap tq, tk, tv, tdo, tdq;
-  if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, BH) || !make_tmap_bf16_3d(&tk, a.k, D, a.Tk, BH) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, BH) || !make_tmap_bf16_3d(&tdo, a.do_, D, a.Tq, BH) ||
-      !make_tmap_f32_3d(&tdq, dq_acc, D, a.Tq, BH))
-    return cudaErrorInvalidValue;
+  // tiled maps over the sorted q, k, v, dO, or row-gather maps over the
+  // original-order ones
+  const bool maps_ok =
+      (a.gather_q ? (make_tmap_bf16_rows(&tq, a.q, D, BH * a.To) && make_tmap_bf16_rows(&tdo, a.do_, D, BH * a.To))
+                  : (make_tmap_bf16_3d(&tq, a.q, D, a.Tq, BH) && make_tmap_bf16_3d(&tdo, a.do_, D, a.Tq, BH))) &&
+      (a.gather_kv ? (make_tmap_bf16_rows(&tk, a.k, D, BH * a.To) && make_tmap_bf16_rows(&tv, a.v, D, BH * a.To))
+                   : (make_tmap_bf16_3d(&tk, a.k, D, a.Tk, BH) && make_tmap_bf16_3d(&tv, a.v, D, a.Tk, BH)));
+  if (!maps_ok || !make_tmap_f32_3d(&tdq, dq_acc, D, a.Tq, BH)) return cudaErrorInvalidValue;
   BwdParams p;
   p.mode = a.mode;
   p.Tq = a.Tq;
@@ -1259,6 +1326,8 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
   p.k_rows = a.k_rows;
   p.To = a.To;
   p.stall = a.stall;
+  p.gather_q = a.gather_q;
+  p.gather_kv = a.gather_kv;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   p.sched = reinterpret_cast<WsHeader*>(a.ws + L.header)->sched + 2;
   int grid = sms;

@@ -116,6 +116,8 @@ struct FwdParams {
   float* lse;
   float* o32;             // null, or an fp32 copy of O [B,H,Tq,D] in row order of q
   int stall;              // SCFA_FLAG_DEBUG_STALL: withhold the first K / V load
+  int gather_q;           // q is an original-order tensor read by row gathers through q_idx (To rows per head)
+  int gather_kv;          // k and v likewise through k_idx
   int* status;
 };
 
@@ -167,39 +169,72 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int kv_it = 0, item = 0, last_q = -1;
-      for (int rnd = 0, w = work_item(0); w < p.n_pairs; w = work_item(++rnd)) {
-        const int pid = p.work_pairs[w];
-        const int cnt = p.pcount[pid];
-        if (cnt == 0) continue;
-        const int bh = pid / p.nPairs, m = pid % p.nPairs;
-        const bool has1 = 2 * m + 1 < p.nQt;
-        const long long g0 = static_cast<long long>(bh) * p.nQt + 2 * m;
-        if (!mbar_wait(&sm.q_empty, (item & 1) ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&sm.q_full, (has1 ? 2 : 1) * D * kTile * 2);
-        for (int sub = 0; sub < D / 64; ++sub) {
-          tma_load_3d(sm.q[0][sub], &tm_q, &sm.q_full, sub * 64, 2 * m * kTile, bh);
-          if (has1) tma_load_3d(sm.q[1][sub], &tm_q, &sm.q_full, sub * 64, (2 * m + 1) * kTile, bh);
-        }
-        last_q = item;
-        const int32_t* ul = ulist + p.row_ptr[g0];
-        bool ok = !(p.stall && kv_it == 0);  // debug stall: no K / V load ever arrives
-        for (int t = 0; t < cnt && ok; ++t) {
-          const int j = ul[t] >> 4;
-          const int s = kv_it % kStages;
-          const uint32_t ph = (kv_it / kStages) & 1;
-          if (!mbar_wait(&sm.kv_empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&sm.k_full[s], D * kTile * 2);
-          for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(sm.k[s][sub], &tm_k, &sm.k_full[s], sub * 64, j * kTile, bh);
-          mbar_arrive_expect_tx(&sm.v_full[s], D * kTile * 2);
-          for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(sm.v[s][sub], &tm_v, &sm.v_full[s], sub * 64, j * kTile, bh);
-          ++kv_it;
-        }
-        if (!ok) break;
-        ++item;
+    // Lane 0 waits on the stages and issues tiled loads; with row gathers
+    // (p.gather_q, p.gather_kv) every lane issues four rows of each tile, their source rows
+    // loaded before the stage wait.
+    int kv_it = 0, item = 0, last_q = -1;
+    for (int rnd = 0, w = work_item(0); w < p.n_pairs; w = work_item(++rnd)) {
+      const int pid = p.work_pairs[w];
+      const int cnt = p.pcount[pid];
+      if (cnt == 0) continue;
+      const int bh = pid / p.nPairs, m = pid % p.nPairs;
+      const bool has1 = 2 * m + 1 < p.nQt;
+      const long long g0 = static_cast<long long>(bh) * p.nQt + 2 * m;
+      int r0[4], r1[4];
+      if (p.gather_q) {
+        gather_rows(p.q_idx, bh, p.Tq, p.To, 2 * m * kTile, lane, r0);
+        if (has1) gather_rows(p.q_idx, bh, p.Tq, p.To, (2 * m + 1) * kTile, lane, r1);
       }
-      // drain: every copy issued by this thread has landed before the CTA
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&sm.q_empty, (item & 1) ^ 1, abort_flag, p.status);
+        if (ok) {
+          mbar_arrive_expect_tx(&sm.q_full, (has1 ? 2 : 1) * D * kTile * 2);
+          if (!p.gather_q) {
+            for (int sub = 0; sub < D / 64; ++sub) {
+              tma_load_3d(sm.q[0][sub], &tm_q, &sm.q_full, sub * 64, 2 * m * kTile, bh);
+              if (has1) tma_load_3d(sm.q[1][sub], &tm_q, &sm.q_full, sub * 64, (2 * m + 1) * kTile, bh);
+            }
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      if (p.gather_q) {
+        gather_issue(sm.q[0][0], kSubBytes, D / 64, &tm_q, &sm.q_full, r0, lane);
+        if (has1) gather_issue(sm.q[1][0], kSubBytes, D / 64, &tm_q, &sm.q_full, r1, lane);
+      }
+      last_q = item;
+      const int32_t* ul = ulist + p.row_ptr[g0];
+      ok = !(p.stall && kv_it == 0);  // debug stall: no K / V load ever arrives
+      for (int t = 0; t < cnt && ok; ++t) {
+        const int j = ul[t] >> 4;
+        const int s = kv_it % kStages;
+        const uint32_t ph = (kv_it / kStages) & 1;
+        int rr[4];
+        if (p.gather_kv) gather_rows(p.k_idx, bh, p.Tk, p.To, j * kTile, lane, rr);  // K and V rows
+        if (lane == 0) {
+          ok = mbar_wait(&sm.kv_empty[s], ph ^ 1, abort_flag, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.k_full[s], D * kTile * 2);
+            if (!p.gather_kv)
+              for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(sm.k[s][sub], &tm_k, &sm.k_full[s], sub * 64, j * kTile, bh);
+            mbar_arrive_expect_tx(&sm.v_full[s], D * kTile * 2);
+            if (!p.gather_kv)
+              for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(sm.v[s][sub], &tm_v, &sm.v_full[s], sub * 64, j * kTile, bh);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+        if (p.gather_kv) {
+          gather_issue(sm.k[s][0], kSubBytes, D / 64, &tm_k, &sm.k_full[s], rr, lane);
+          gather_issue(sm.v[s][0], kSubBytes, D / 64, &tm_v, &sm.v_full[s], rr, lane);
+        }
+        ++kv_it;
+      }
+      if (!ok) break;
+      ++item;
+    }
+    if (lane == 0) {
+      // drain: every copy issued by this warp has landed before the CTA
       // exits, also after an abort (K and V of one stage are issued together)
       for (int d = 1; d <= kStages && d <= kv_it; ++d) {
         const int it = kv_it - d;
@@ -646,48 +681,89 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      // Work items are taken from a global counter in list order (largest
-      // first) as this CTA gets through its previous ones, and handed to the
-      // MMA and softmax roles through a small slot ring; -1 ends the walk.
-      int item = 0, kv = 0, slot_it = 0;
-      int k_issued = 0, v_issued = 0, q_issued = 0;  // loads issued, for the drain
-      for (;;) {
-        const int slot = slot_it % kF1Slots;
-        if (!mbar_wait(&sm.item_empty[slot], ((slot_it / kF1Slots) & 1) ^ 1, abort_flag, p.status)) break;
-        const int w = atomicAdd(&p.sched[0], 1);
+    // Work items are taken from a global counter in list order (largest
+    // first) as this CTA gets through its previous ones, and handed to the
+    // MMA and softmax roles through a small slot ring; -1 ends the walk.
+    // Lane 0 waits on the stages and issues tiled loads; with row gathers
+    // (p.gather_q, p.gather_kv) every lane issues four rows of each tile, their source rows
+    // loaded before the stage wait.
+    int item = 0, kv = 0, slot_it = 0;
+    int k_issued = 0, v_issued = 0, q_issued = 0;  // loads issued, for the drain
+    for (;;) {
+      const int slot = slot_it % kF1Slots;
+      int w = INT_MAX;
+      if (lane == 0 && mbar_wait(&sm.item_empty[slot], ((slot_it / kF1Slots) & 1) ^ 1, abort_flag, p.status)) {
+        w = atomicAdd(&p.sched[0], 1);
         sm.items[slot] = w < p.n_work ? w : -1;
         mbar_arrive(&sm.item_full[slot]);
-        ++slot_it;
-        if (w >= p.n_work) break;
-        const int g = p.work[w];
-        const int e0 = p.row_ptr[g], n = p.row_ptr[g + 1] - e0;
-        if (n == 0) continue;
-        const int bh = g / p.nQt, i = g % p.nQt;
-        const int qb = item & 1;
-        if (!mbar_wait(&sm.q_empty[qb], ((item >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&sm.q_full[qb], D * kTile * 2);
-        tma_load_3d(sm.q[qb], &tm_q, &sm.q_full[qb], 0, i * kTile, bh);
-        q_issued = item + 1;
-        bool ok = !(p.stall && kv == 0);  // debug stall: no K / V load ever arrives
-        for (int t = 0; t < n && ok; ++t) {
-          const int j = cols[e0 + t];
-          const int s = kv % kF1Stages;
-          const uint32_t ph = ((kv / kF1Stages) & 1) ^ 1;
-          if (!mbar_wait(&sm.k_empty[s], ph, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&sm.k_full[s], D * kTile * 2);
-          tma_load_3d(sm.k[s], &tm_k, &sm.k_full[s], 0, j * kTile, bh);
-          k_issued = kv + 1;
-          if (!mbar_wait(&sm.v_empty[s], ph, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&sm.v_full[s], D * kTile * 2);
-          tma_load_3d(sm.v[s], &tm_v, &sm.v_full[s], 0, j * kTile, bh);
-          v_issued = kv + 1;
-          ++kv;
-        }
-        if (!ok) break;
-        ++item;
       }
-      // drain: every copy issued by this thread has landed before the CTA
+      w = __shfl_sync(0xffffffffu, w, 0);
+      ++slot_it;
+      if (w >= p.n_work) break;
+      const int g = p.work[w];
+      const int e0 = p.row_ptr[g], n = p.row_ptr[g + 1] - e0;
+      if (n == 0) continue;
+      const int bh = g / p.nQt, i = g % p.nQt;
+      const int qb = item & 1;
+      int rr[4];
+      if (p.gather_q) gather_rows(p.q_idx, bh, p.Tq, p.To, i * kTile, lane, rr);
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&sm.q_empty[qb], ((item >> 1) & 1) ^ 1, abort_flag, p.status);
+        if (ok) {
+          mbar_arrive_expect_tx(&sm.q_full[qb], D * kTile * 2);
+          if (!p.gather_q) tma_load_3d(sm.q[qb], &tm_q, &sm.q_full[qb], 0, i * kTile, bh);
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      if (p.gather_q) gather_issue(sm.q[qb], 0, 1, &tm_q, &sm.q_full[qb], rr, lane);
+      q_issued = item + 1;
+      ok = !(p.stall && kv == 0);  // debug stall: no K / V load ever arrives
+      // the item's key tiles are read 32 at a time (one per lane); with row
+      // gathers the source rows of a tile are loaded a tile ahead
+      int cj = lane < n ? cols[e0 + lane] : 0;
+      int rk[4] = {0, 0, 0, 0};
+      if (p.gather_kv) gather_rows(p.k_idx, bh, p.Tk, p.To, __shfl_sync(0xffffffffu, cj, 0) * kTile, lane, rk);
+      for (int t = 0; t < n && ok; ++t) {
+        const int j = __shfl_sync(0xffffffffu, cj, t & 31);
+        const int s = kv % kF1Stages;
+        const uint32_t ph = ((kv / kF1Stages) & 1) ^ 1;
+        if (t + 1 < n) {
+          if (((t + 1) & 31) == 0) cj = t + 1 + lane < n ? cols[e0 + t + 1 + lane] : 0;
+          if (p.gather_kv)  // K and V rows of the next tile
+            gather_rows(p.k_idx, bh, p.Tk, p.To, __shfl_sync(0xffffffffu, cj, (t + 1) & 31) * kTile, lane, rr);
+        }
+        if (lane == 0) {
+          ok = mbar_wait(&sm.k_empty[s], ph, abort_flag, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.k_full[s], D * kTile * 2);
+            if (!p.gather_kv) tma_load_3d(sm.k[s], &tm_k, &sm.k_full[s], 0, j * kTile, bh);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+        if (p.gather_kv) gather_issue(sm.k[s], 0, 1, &tm_k, &sm.k_full[s], rk, lane);
+        k_issued = kv + 1;
+        if (lane == 0) {
+          ok = mbar_wait(&sm.v_empty[s], ph, abort_flag, p.status);
+          if (ok) {
+            mbar_arrive_expect_tx(&sm.v_full[s], D * kTile * 2);
+            if (!p.gather_kv) tma_load_3d(sm.v[s], &tm_v, &sm.v_full[s], 0, j * kTile, bh);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { ok = false; break; }
+        if (p.gather_kv) {
+          gather_issue(sm.v[s], 0, 1, &tm_v, &sm.v_full[s], rk, lane);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) rk[u] = rr[u];
+        }
+        v_issued = kv + 1;
+        ++kv;
+      }
+      if (!ok) break;
+      ++item;
+    }
+    if (lane == 0) {
+      // drain: every copy issued by this warp has landed before the CTA
       // exits, also after an abort (the counts are of loads actually issued)
       for (int d = 1; d <= kF1Stages && d <= k_issued; ++d) {
         const int it = k_issued - d;
@@ -1033,14 +1109,22 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int D, long long T, long long BH);
 
+// tiled maps over the sorted q, k, v, or row-gather maps over the
+// original-order ones
+static bool make_fwd_maps(const AttnArgs& a, int D, long long BH, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv) {
+  const bool q_ok = a.gather_q ? make_tmap_bf16_rows(tq, a.q, D, BH * a.To) : make_tmap_bf16_3d(tq, a.q, D, a.Tq, BH);
+  const bool kv_ok = a.gather_kv
+                         ? make_tmap_bf16_rows(tk, a.k, D, BH * a.To) && make_tmap_bf16_rows(tv, a.v, D, BH * a.To)
+                         : make_tmap_bf16_3d(tk, a.k, D, a.Tk, BH) && make_tmap_bf16_3d(tv, a.v, D, a.Tk, BH);
+  return q_ok && kv_ok;
+}
+
 template <int D>
 static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   const AttnWs& L = *a.L;
   const long long BH = static_cast<long long>(a.B) * a.H;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, BH) || !make_tmap_bf16_3d(&tk, a.k, D, a.Tk, BH) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, BH))
-    return cudaErrorInvalidValue;
+  if (!make_fwd_maps(a, D, BH, &tq, &tk, &tv)) return cudaErrorInvalidValue;
   FwdParams p;
   p.mode = a.mode;
   p.Tq = a.Tq;
@@ -1062,6 +1146,8 @@ static cudaError_t launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   p.lse = a.lse_out;
   p.o32 = a.o32;
   p.stall = a.stall;
+  p.gather_q = a.gather_q;
+  p.gather_kv = a.gather_kv;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1082,9 +1168,7 @@ static cudaError_t launch_fwd1(const AttnArgs& a, cudaStream_t st) {
   const AttnWs& L = *a.L;
   const long long BH = static_cast<long long>(a.B) * a.H;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16_3d(&tq, a.q, D, a.Tq, BH) || !make_tmap_bf16_3d(&tk, a.k, D, a.Tk, BH) ||
-      !make_tmap_bf16_3d(&tv, a.v, D, a.Tk, BH))
-    return cudaErrorInvalidValue;
+  if (!make_fwd_maps(a, D, BH, &tq, &tk, &tv)) return cudaErrorInvalidValue;
   FwdParams p = {};
   p.mode = a.mode;
   p.Tq = a.Tq;
@@ -1105,6 +1189,8 @@ static cudaError_t launch_fwd1(const AttnArgs& a, cudaStream_t st) {
   p.lse = a.lse_out;
   p.o32 = a.o32;
   p.stall = a.stall;
+  p.gather_q = a.gather_q;
+  p.gather_kv = a.gather_kv;
   p.status = reinterpret_cast<int*>(a.ws + L.header);
   const size_t smem = sizeof(Fwd1Smem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

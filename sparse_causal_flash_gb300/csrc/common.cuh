@@ -231,6 +231,46 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// four rows of a 2-D map whose box is one row high (tile::gather4): rows
+// r0..r3, columns x .. x + box width, landing as consecutive box rows at
+// smem_dst with the map's swizzle (the same bytes a tiled load of those rows
+// would write there)
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int r0,
+                                            int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      :: "r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2),
+         "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Row gathers of one 128-row tile by a whole warp, from an original-order
+// tensor (a 2-D map over its BH * To rows, 64-column boxes one row high):
+// sorted slot row0 + r of head bh is row idx[bh * Ts + row0 + r] of that
+// head. A slot at or past Ts, or whose index falls outside [0, To), is a
+// padding row and reads the head's first row instead (every score against a
+// padding row is masked, so its values only ever meet exact zeros).
+// gather_rows: lane l's four source rows 4l .. 4l + 3 (loaded ahead of the
+// stage wait); gather_issue: lane l's gathers into each 64-column sub-tile
+// (sub-tiles sub_bytes apart), completing on `bar`, whose expected byte
+// count the caller has set.
+__device__ __forceinline__ void gather_rows(const int32_t* __restrict__ idx, long long bh, int Ts, int To, int row0,
+                                            int lane, int (&rr)[4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int slot = row0 + 4 * lane + u;
+    int src = slot < Ts ? __ldg(idx + bh * Ts + slot) : -1;
+    if (src < 0 || src >= To) src = 0;
+    rr[u] = static_cast<int>(bh * To + src);
+  }
+}
+__device__ __forceinline__ void gather_issue(uint8_t* dst, uint32_t sub_bytes, int n_sub, const CUtensorMap* map,
+                                             uint64_t* bar, const int (&rr)[4], int lane) {
+  for (int sub = 0; sub < n_sub; ++sub)
+    tma_gather4(dst + sub * sub_bytes + 512 * lane, map, bar, sub * 64, rr[0], rr[1], rr[2], rr[3]);
+}
+
 // untiled bulk copy global -> shared of `bytes` bytes (both addresses 16-byte
 // aligned, bytes a multiple of 16), completion counted on `bar`
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {

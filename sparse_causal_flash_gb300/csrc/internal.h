@@ -123,9 +123,16 @@ struct AttnArgs {
   // writes it, the backward pre-pass reads it); null otherwise
   float* o32;
   int stall;  // SCFA_FLAG_DEBUG_STALL
+  // SCFA_FLAG_GATHER_Q: q and do, SCFA_FLAG_GATHER_KV: k and v are
+  // original-order [B,H,To,D] tensors whose rows the kernels gather through
+  // q_idx / k_idx
+  int gather_q, gather_kv;
   char* ws;
   const AttnWs* L;
 };
+// 2-D map over `rows` rows of a bf16 [rows][D] tensor; box = 64 columns x 1
+// row (for tile::gather4), 128-byte swizzle
+bool make_tmap_bf16_rows(CUtensorMap* map, const void* base, int D, long long rows);
 cudaError_t launch_attn_fwd(const AttnArgs& a, cudaStream_t st);
 
 // profiling hook: events recorded around the main fwd (0) / bwd (1) kernel

@@ -17,7 +17,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (FLAG_KEEP_O32, FLAG_ORIGINAL_ORDER, FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size,
+from . import (FLAG_GATHER_KV, FLAG_GATHER_Q, FLAG_KEEP_O32, FLAG_ORIGINAL_ORDER, FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size,
                attn_workspace_size_live, lsh_bucket_sort, lsh_bucket_sort_tiled, lsh_gather, lsh_hash, lsh_sort_ids,
                lsh_workspace_size,
                scfa_dense_bwd, scfa_tiled_rows,
@@ -35,19 +35,33 @@ class Step:
     """Buffers and the launch sequence of one fwd+bwd step for a fixed shape."""
 
     def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
-                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False):
+                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False, gather=None):
         """tiled (hash mode; the default): sort into the tile-aligned layout,
         every bucket starting on a tile boundary (lsh_bucket_sort_tiled); the
         sorted tensors then have Ts = scfa_tiled_rows(T, n_buckets) rows per
         head. tiled=False keeps the plain sorted order (Ts = T).
         shared_qk (hash mode): one hash per token, of its query, for both its
         query and its key (Reformer's shared-QK hashing); keys are sorted by
-        those ids (lsh_sort_ids), so every token shares a bucket with itself."""
+        those ids (lsh_sort_ids), so every token shares a bucket with itself.
+        gather (hash mode): "q" (q and dO), "kv" (k and v), True (all four)
+        or False: no sorted copies of those tensors; the attention kernels
+        read their rows through the sort's permutations (SCFA_FLAG_GATHER_Q,
+        SCFA_FLAG_GATHER_KV). The default, None, is "kv" on the tile-aligned
+        layout (the fastest on GB300: the backward's query-tile ring waits on
+        gathered rows, its resident key tile does not) and False on the plain
+        one."""
         self.mode, self.B, self.H, self.Tq, self.Tk, self.D = mode, B, H, Tq, Tk, D
         self.nb = n_buckets
         self.flags = flags
         self.tiled = mode == MODE_HASH and (tiled is None or bool(tiled))
         self.shared_qk = mode == MODE_HASH and bool(shared_qk)
+        if gather is None:
+            gather = "kv" if self.tiled else False
+        g = "qkv" if gather is True else (gather or "")
+        if g not in ("", "q", "kv", "qkv"):
+            raise ValueError(f"gather must be False, True, 'q', 'kv' or 'qkv', not {gather!r}")
+        self.gq = mode == MODE_HASH and "q" in g
+        self.gkv = mode == MODE_HASH and "kv" in g
         # rows per head of the sorted tensors (hash mode) or of q / k
         self.Ts = scfa_tiled_rows(Tq, n_buckets) if self.tiled else Tq
         dev = torch.device(device)
@@ -81,17 +95,21 @@ class Step:
             self.ws_l = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
             self.ws_lk = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
             self.side = torch.cuda.Stream(device=dev)
-            self.ev = [torch.cuda.Event() for _ in range(2)]
+            self.ev = [torch.cuda.Event() for _ in range(3)]
             self.qh = torch.empty((B, H, Ts), **i32)
             self.kh = torch.empty((B, H, Ts), **i32)
             self.pq = torch.empty((B, H, Ts), **i32)
             self.pk = torch.empty((B, H, Ts), **i32)
             self.offq = torch.empty((B, H, n_buckets + 1), **i32)
             self.offk = torch.empty((B, H, n_buckets + 1), **i32)
-            self.q_s = torch.empty((B, H, Ts, D), **bf)
-            self.k_s = torch.empty((B, H, Ts, D), **bf)
-            self.v_s = torch.empty((B, H, Ts, D), **bf)
-            self.do_s = torch.empty((B, H, Ts, D), **bf)
+            # sorted copies of the tensors the kernels do not gather themselves
+            self.q_s = self.do_s = self.k_s = self.v_s = None
+            if not self.gq:
+                self.q_s = torch.empty((B, H, Ts, D), **bf)
+                self.do_s = torch.empty((B, H, Ts, D), **bf)
+            if not self.gkv:
+                self.k_s = torch.empty((B, H, Ts, D), **bf)
+                self.v_s = torch.empty((B, H, Ts, D), **bf)
             if self.shared_qk:
                 self.ids = torch.empty((B, H, T), **i32)  # bucket ids in original order
 
@@ -129,12 +147,16 @@ class Step:
                 self._size_lists(main)
             # O, dQ, dK, dV go straight to original row order (pq / pk map
             # sorted rows to original ones); LSE stays in sorted order
-            fo = f | FLAG_ORIGINAL_ORDER
-            scfa_hash_fwd(self.q_s, self.k_s, self.v_s, self.pq, self.pk, self.qh, self.kh, scale, self.o,
-                          self.lse, self.ws_f, fo, main)
+            # the kernels gather the rows of q, dO through pq and of k, v
+            # through pk where they have no sorted copies
+            g = FLAG_ORIGINAL_ORDER | (FLAG_GATHER_Q if self.gq else 0) | (FLAG_GATHER_KV if self.gkv else 0)
+            xq, xdo = (q, do) if self.gq else (self.q_s, self.do_s)
+            xk, xv = (k, v) if self.gkv else (self.k_s, self.v_s)
+            scfa_hash_fwd(xq, xk, xv, self.pq, self.pk, self.qh, self.kh, scale, self.o, self.lse, self.ws_f, f | g,
+                          main)
             tick("fwd")
-            scfa_hash_bwd(self.q_s, self.k_s, self.v_s, self.o, self.lse, self.do_s, self.pq, self.pk, self.qh,
-                          self.kh, scale, self.dq, self.dk, self.dv, self.ws_b, fr | FLAG_ORIGINAL_ORDER, main)
+            scfa_hash_bwd(xq, xk, xv, self.o, self.lse, xdo, self.pq, self.pk, self.qh, self.kh, scale, self.dq,
+                          self.dk, self.dv, self.ws_b, fr | g, main)
             tick("bwd")
         return self
 
@@ -160,33 +182,47 @@ class Step:
         self.ev[0].record(main)
         side.wait_event(self.ev[0])
         lsh_sort_ids(self.ids, nb, K_PAD, self.kh, self.pk, self.offk, self.ws_lk, 0, side)
-        lsh_gather(k, self.pk, self.k_s, side)
-        lsh_gather(v, self.pk, self.v_s, side)
+        if not self.gkv:
+            lsh_gather(k, self.pk, self.k_s, side)
+            lsh_gather(v, self.pk, self.v_s, side)
         tick("sort_gather_k_v")
         self.ev[1].record(side)
         lsh_sort_ids(self.ids, nb, Q_PAD, self.qh, self.pq, self.offq, self.ws_l, 0, main)
-        lsh_gather(q, self.pq, self.q_s, main)
-        lsh_gather(do, self.pq, self.do_s, main)
+        if not self.gq:
+            lsh_gather(q, self.pq, self.q_s, main)
+            lsh_gather(do, self.pq, self.do_s, main)
         tick("sort_gather_q_do")
 
     def _sorts(self, q, k, v, do, R, main, side, tick):
         nb = self.nb
         self.ev[0].record(main)
         side.wait_event(self.ev[0])
-        if self.tiled:
-            lsh_bucket_sort_tiled(k, R, nb, K_PAD, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
-        else:
-            lsh_bucket_sort(k, R, nb, self.kh, self.pk, self.offk, self.k_s, self.ws_lk, 0, side)
+
+        def sort(x, pad, hs, perm, off, x_sorted, ws, st):
+            if self.tiled:
+                lsh_bucket_sort_tiled(x, R, nb, pad, hs, perm, off, x_sorted, ws, 0, st)
+            else:
+                lsh_bucket_sort(x, R, nb, hs, perm, off, x_sorted, ws, 0, st)
+
+        # with query-side gathers alone the query stream has time to spare:
+        # it moves V once the key sort is done, the key stream moves K
+        split = self.gq and not self.gkv
+        sort(k, K_PAD, self.kh, self.pk, self.offk, None if (self.gkv or split) else self.k_s, self.ws_lk, side)
         tick("hash_sort_gather_k")
-        lsh_gather(v, self.pk, self.v_s, side)
+        if split:
+            self.ev[2].record(side)
+            lsh_gather(k, self.pk, self.k_s, side)
+        elif not self.gkv:
+            lsh_gather(v, self.pk, self.v_s, side)
         tick("gather_v")
         self.ev[1].record(side)
-        if self.tiled:
-            lsh_bucket_sort_tiled(q, R, nb, Q_PAD, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
-        else:
-            lsh_bucket_sort(q, R, nb, self.qh, self.pq, self.offq, self.q_s, self.ws_l, 0, main)
+        sort(q, Q_PAD, self.qh, self.pq, self.offq, None if self.gq else self.q_s, self.ws_l, main)
         tick("hash_sort_gather_q")
-        lsh_gather(do, self.pq, self.do_s, main)
+        if split:
+            main.wait_event(self.ev[2])
+            lsh_gather(v, self.pk, self.v_s, main)
+        if not self.gq:
+            lsh_gather(do, self.pq, self.do_s, main)
         tick("gather_do")
 
     def _size_lists(self, stream):
@@ -219,10 +255,11 @@ class HostPipeline:
     INPUTS = ("q", "k", "v", "do", "q_idx", "k_idx", "R")
 
     def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
-                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False, graphs: bool = True):
+                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False, gather=None,
+                 graphs: bool = True):
         self.device = torch.device(device)
         self.steps = [Step(mode, B, H, Tq, Tk, D, n_buckets=n_buckets, device=self.device, flags=flags,
-                           tiled=tiled, shared_qk=shared_qk)
+                           tiled=tiled, shared_qk=shared_qk, gather=gather)
                       for _ in range(2)]
         # graphs: from its second use on, a slot's step runs as one CUDA graph
         # captured on the slot's device input buffers (not for live-sized

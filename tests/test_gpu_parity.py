@@ -323,7 +323,7 @@ def test_live_sized_workspace(scfa):
     B, H, T, D, nb = 1, 3, 3000, 64, 8
     p = synth.make_problem(synth.Workload("ls", "hash", B, H, T, D, 150, n_buckets=nb))
     from sparse_causal_flash_gb300.pipeline import Step
-    st = Step(scfa.MODE_HASH, B, H, T, T, D, n_buckets=nb)
+    st = Step(scfa.MODE_HASH, B, H, T, T, D, n_buckets=nb, gather=False)  # sorted copies of all four
     st.run(p.q.cuda(), p.k.cuda(), p.v.cuda(), p.do.cuda(), p.wl.scale, R=p.R.cuda())
     Ts = st.Ts  # rows of the sorted (tile-aligned) tensors
     n_live = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -426,11 +426,12 @@ def test_count_chunked_pairs_bitexact(scfa, chunk):
 
 
 # ------------------------------------------------------------------ attention
-def run_step(scfa, p, mode, flags=0, tiled=False):
+def run_step(scfa, p, mode, flags=0, tiled=False, gather=False, shared_qk=False):
     from sparse_causal_flash_gb300.pipeline import Step
     B, H, Tq, D = p.q.shape
     Tk = p.k.shape[2]
-    st = Step(mode, B, H, Tq, Tk, D, n_buckets=p.wl.n_buckets, flags=flags, tiled=tiled)
+    st = Step(mode, B, H, Tq, Tk, D, n_buckets=p.wl.n_buckets, flags=flags, tiled=tiled, gather=gather,
+              shared_qk=shared_qk)
     st.run(cuda(p.q), cuda(p.k), cuda(p.v), cuda(p.do), p.wl.scale,
            q_idx=None if p.q_idx is None else cuda(p.q_idx), k_idx=None if p.k_idx is None else cuda(p.k_idx),
            R=None if p.R is None else cuda(p.R))
@@ -491,6 +492,39 @@ def test_hash_parity_tiled(scfa, B, H, T, D, nb, seed):
     want = tiles.live_list("hash", B, H, st.Ts, st.Ts, pq, pk, qs, ks)
     for key in ("row_ptr", "cols", "fflags", "csc_ptr", "csc_rows", "cflags"):
         np.testing.assert_array_equal(got[key], want[key], err_msg=key)
+
+
+@pytest.mark.parametrize("tiled,gather", [(False, True), (True, True), (True, "q"), (True, "kv"), (False, "q")])
+@pytest.mark.parametrize("B,H,T,D,nb,seed", [(1, 2, 1000, 64, 8, 21), (2, 1, 1500, 64, 2, 22),
+                                             (1, 1, 1000, 64, 64, 24), (1, 2, 1300, 128, 8, 23),
+                                             (1, 1, 77, 64, 4, 25)])
+def test_hash_parity_gather(scfa, B, H, T, D, nb, seed, tiled, gather):
+    """Row gathers inside the attention kernels (SCFA_FLAG_GATHER_Q: q, dO;
+    SCFA_FLAG_GATHER_KV: k, v; read in original order through the sort's
+    permutations): results within tolerance of the oracle, and equal to
+    those of the step that materialises the sorted copies (padding rows are
+    masked either way)."""
+    p = synth.make_problem(synth.Workload("hg", "hash", B, H, T, D, seed, n_buckets=nb))
+    st = run_step(scfa, p, scfa.MODE_HASH, tiled=tiled, gather=gather)
+    assert (st.q_s is None) == (gather in (True, "q")) and (st.k_s is None) == (gather in (True, "kv"))
+    ref, qh, kh = pipelines.run_hash(p.q, p.k, p.v, p.do, p.R, p.wl.scale)
+    pq, _, _ = sorted_views(qh, nb, st.Ts if tiled else None, Q_PAD)
+    np.testing.assert_array_equal(st.pq.cpu().numpy(), pq)
+    compare_heads(st, ref, ref.keys(), lse_perm=pq)
+    st0 = run_step(scfa, p, scfa.MODE_HASH, tiled=tiled, gather=False)
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        a, b = getattr(st, name), getattr(st0, name)
+        assert torch.equal(a, b), f"{name}: gathered rows differ from the sorted copies"
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_hash_shared_qk_gather(scfa, D):
+    """Shared-QK hashing with row gathers equals the same step on sorted copies."""
+    p = synth.make_problem(synth.Workload("hsg", "hash", 1, 2, 900, D, 26, n_buckets=8))
+    st = run_step(scfa, p, scfa.MODE_HASH, tiled=True, gather=True, shared_qk=True)
+    st0 = run_step(scfa, p, scfa.MODE_HASH, tiled=True, gather=False, shared_qk=True)
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(getattr(st, name), getattr(st0, name)), name
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -641,11 +675,11 @@ def test_full_qk_8k_sampled_heads(scfa):
                         st.ws_b) == want
 
 
-@pytest.mark.parametrize("tiled", [False, True])
-def test_full_hash_8k_sampled_heads(scfa, tiled):
+@pytest.mark.parametrize("tiled,gather", [(False, False), (True, False), (True, True)])
+def test_full_hash_8k_sampled_heads(scfa, tiled, gather):
     wl = synth.WORKLOADS["hash_b4h12_t8192_d64_nb16"]
     p = synth.make_problem(wl)
-    st = run_step(scfa, p, scfa.MODE_HASH, tiled=tiled)
+    st = run_step(scfa, p, scfa.MODE_HASH, tiled=tiled, gather=gather)
     heads = [(0, 0), (1, 5), (2, 9), (3, 11)]
     qh = lsh.lsh_hash(p.q.double().numpy(), p.R.double().numpy())
     kh = lsh.lsh_hash(p.k.double().numpy(), p.R.double().numpy())
@@ -661,15 +695,15 @@ def test_full_hash_8k_sampled_heads(scfa, tiled):
     assert device_count(scfa, scfa.MODE_HASH, st.pq, st.pk, st.qh, st.kh, wl.B, wl.H, st.Ts, st.Ts, st.ws_b) == want
 
 
-@pytest.mark.parametrize("tiled", [False, True])
-def test_full_hash_16k_sampled_heads(scfa, tiled):
+@pytest.mark.parametrize("tiled,gather", [(False, False), (True, False), (True, True)])
+def test_full_hash_16k_sampled_heads(scfa, tiled, gather):
     """Hash-sparse B2 H12 T16384 D64 with 32 buckets, in the bench's launch
     configuration: bucket ids and sorted views of every head bit-exact, and
     three whole heads within tolerance (the oracle evaluates each head bucket
     by bucket, exact because the hash mask never pairs two buckets)."""
     wl = synth.WORKLOADS["hash_b2h12_t16384_d64_nb32"]
     p = synth.make_problem(wl)
-    st = run_step(scfa, p, scfa.MODE_HASH, tiled=tiled)
+    st = run_step(scfa, p, scfa.MODE_HASH, tiled=tiled, gather=gather)
     assert scfa.scfa_get_device_status(st.ws_b) == 0
     R = p.R.double().numpy()
     qh = lsh.lsh_hash(p.q.double().numpy(), R)
