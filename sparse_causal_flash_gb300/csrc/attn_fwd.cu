@@ -167,11 +167,57 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
 
-  if (warp == 0) {
+  if (warp == 0 && !p.gather_q && !p.gather_kv) {
     // ------------------------------------------------------------ producer
-    // Lane 0 waits on the stages and issues tiled loads; with row gathers
-    // (p.gather_q, p.gather_kv) every lane issues four rows of each tile, their source rows
-    // loaded before the stage wait.
+    if (lane == 0) {
+      int kv_it = 0, item = 0, last_q = -1;
+      for (int rnd = 0, w = work_item(0); w < p.n_pairs; w = work_item(++rnd)) {
+        const int pid = p.work_pairs[w];
+        const int cnt = p.pcount[pid];
+        if (cnt == 0) continue;
+        const int bh = pid / p.nPairs, m = pid % p.nPairs;
+        const bool has1 = 2 * m + 1 < p.nQt;
+        const long long g0 = static_cast<long long>(bh) * p.nQt + 2 * m;
+        if (!mbar_wait(&sm.q_empty, (item & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&sm.q_full, (has1 ? 2 : 1) * D * kTile * 2);
+        for (int sub = 0; sub < D / 64; ++sub) {
+          tma_load_3d(sm.q[0][sub], &tm_q, &sm.q_full, sub * 64, 2 * m * kTile, bh);
+          if (has1) tma_load_3d(sm.q[1][sub], &tm_q, &sm.q_full, sub * 64, (2 * m + 1) * kTile, bh);
+        }
+        last_q = item;
+        const int32_t* ul = ulist + p.row_ptr[g0];
+        bool ok = !(p.stall && kv_it == 0);  // debug stall: no K / V load ever arrives
+        for (int t = 0; t < cnt && ok; ++t) {
+          const int j = ul[t] >> 4;
+          const int s = kv_it % kStages;
+          const uint32_t ph = (kv_it / kStages) & 1;
+          if (!mbar_wait(&sm.kv_empty[s], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.k_full[s], D * kTile * 2);
+          for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(sm.k[s][sub], &tm_k, &sm.k_full[s], sub * 64, j * kTile, bh);
+          mbar_arrive_expect_tx(&sm.v_full[s], D * kTile * 2);
+          for (int sub = 0; sub < D / 64; ++sub) tma_load_3d(sm.v[s][sub], &tm_v, &sm.v_full[s], sub * 64, j * kTile, bh);
+          ++kv_it;
+        }
+        if (!ok) break;
+        ++item;
+      }
+      // drain: every copy issued by this thread has landed before the CTA
+      // exits, also after an abort (K and V of one stage are issued together)
+      for (int d = 1; d <= kStages && d <= kv_it; ++d) {
+        const int it = kv_it - d;
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        mbar_wait_drain(&sm.k_full[s], ph, p.status);
+        mbar_wait_drain(&sm.v_full[s], ph, p.status);
+      }
+      if (last_q >= 0) mbar_wait_drain(&sm.q_full, last_q & 1, p.status);
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer (row gathers)
+    // The same walk with the whole warp: lane 0 waits on the stages and
+    // issues the tiled loads, every lane issues four rows of each gathered
+    // tile (p.gather_q: Q; p.gather_kv: K, V), their source rows loaded
+    // before the stage wait.
     int kv_it = 0, item = 0, last_q = -1;
     for (int rnd = 0, w = work_item(0); w < p.n_pairs; w = work_item(++rnd)) {
       const int pid = p.work_pairs[w];
@@ -679,14 +725,71 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   volatile int* abort_flag = &sm.abort_flag;
   constexpr uint32_t kColS = 0, kColO = 128, kColP = 192;
 
-  if (warp == 0) {
+  if (warp == 0 && !p.gather_q && !p.gather_kv) {
     // ------------------------------------------------------------ producer
-    // Work items are taken from a global counter in list order (largest
-    // first) as this CTA gets through its previous ones, and handed to the
-    // MMA and softmax roles through a small slot ring; -1 ends the walk.
-    // Lane 0 waits on the stages and issues tiled loads; with row gathers
-    // (p.gather_q, p.gather_kv) every lane issues four rows of each tile, their source rows
-    // loaded before the stage wait.
+    if (lane == 0) {
+      // Work items are taken from a global counter in list order (largest
+      // first) as this CTA gets through its previous ones, and handed to the
+      // MMA and softmax roles through a small slot ring; -1 ends the walk.
+      int item = 0, kv = 0, slot_it = 0;
+      int k_issued = 0, v_issued = 0, q_issued = 0;  // loads issued, for the drain
+      for (;;) {
+        const int slot = slot_it % kF1Slots;
+        if (!mbar_wait(&sm.item_empty[slot], ((slot_it / kF1Slots) & 1) ^ 1, abort_flag, p.status)) break;
+        const int w = atomicAdd(&p.sched[0], 1);
+        sm.items[slot] = w < p.n_work ? w : -1;
+        mbar_arrive(&sm.item_full[slot]);
+        ++slot_it;
+        if (w >= p.n_work) break;
+        const int g = p.work[w];
+        const int e0 = p.row_ptr[g], n = p.row_ptr[g + 1] - e0;
+        if (n == 0) continue;
+        const int bh = g / p.nQt, i = g % p.nQt;
+        const int qb = item & 1;
+        if (!mbar_wait(&sm.q_empty[qb], ((item >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&sm.q_full[qb], D * kTile * 2);
+        tma_load_3d(sm.q[qb], &tm_q, &sm.q_full[qb], 0, i * kTile, bh);
+        q_issued = item + 1;
+        bool ok = !(p.stall && kv == 0);  // debug stall: no K / V load ever arrives
+        for (int t = 0; t < n && ok; ++t) {
+          const int j = cols[e0 + t];
+          const int s = kv % kF1Stages;
+          const uint32_t ph = ((kv / kF1Stages) & 1) ^ 1;
+          if (!mbar_wait(&sm.k_empty[s], ph, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.k_full[s], D * kTile * 2);
+          tma_load_3d(sm.k[s], &tm_k, &sm.k_full[s], 0, j * kTile, bh);
+          k_issued = kv + 1;
+          if (!mbar_wait(&sm.v_empty[s], ph, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.v_full[s], D * kTile * 2);
+          tma_load_3d(sm.v[s], &tm_v, &sm.v_full[s], 0, j * kTile, bh);
+          v_issued = kv + 1;
+          ++kv;
+        }
+        if (!ok) break;
+        ++item;
+      }
+      // drain: every copy issued by this thread has landed before the CTA
+      // exits, also after an abort (the counts are of loads actually issued)
+      for (int d = 1; d <= kF1Stages && d <= k_issued; ++d) {
+        const int it = k_issued - d;
+        mbar_wait_drain(&sm.k_full[it % kF1Stages], (it / kF1Stages) & 1, p.status);
+      }
+      for (int d = 1; d <= kF1Stages && d <= v_issued; ++d) {
+        const int it = v_issued - d;
+        mbar_wait_drain(&sm.v_full[it % kF1Stages], (it / kF1Stages) & 1, p.status);
+      }
+      for (int d = 1; d <= 2 && d <= q_issued; ++d) {
+        const int it = q_issued - d;
+        mbar_wait_drain(&sm.q_full[it & 1], (it >> 1) & 1, p.status);
+      }
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer (row gathers)
+    // The same walk with the whole warp: lane 0 waits on the stages and
+    // issues the tiled loads, every lane issues four rows of each gathered
+    // tile (p.gather_q: Q; p.gather_kv: K, V), their source rows loaded a
+    // tile ahead, before the stage wait. (Without gathers the single-lane
+    // producer above is kept: the warp-wide loop cost the QK forward 4%.)
     int item = 0, kv = 0, slot_it = 0;
     int k_issued = 0, v_issued = 0, q_issued = 0;  // loads issued, for the drain
     for (;;) {
