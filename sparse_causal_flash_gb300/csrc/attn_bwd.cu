@@ -46,11 +46,13 @@ namespace {
 
 constexpr int kSubBytes = kTile * 128;
 // Q / dO / query-metadata ring depth of attn_bwd_kernel (head dimension 64;
-// head dimension 128 runs attn_bwd128_kernel)
-template <int D>
+// head dimension 128 runs attn_bwd128_kernel): three stages with one K / V
+// buffer, two with two K / V buffers (shared memory holds one or the other)
+template <int D, int KVB>
 constexpr int bwd_qstages() {
   static_assert(D == 64, "attn_bwd_kernel is built for head dimension 64");
-  return 3;
+  static_assert(KVB == 1 || KVB == 2, "one or two K / V buffers");
+  return KVB == 1 ? 3 : 2;
 }
 constexpr int kBwdThreads = 448;
 
@@ -58,11 +60,11 @@ constexpr int kBwdSlots = 4;  // work items handed from the producer to the othe
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+template <int D, int KVB>
 struct __align__(1024) BwdSmem {
-  static constexpr int kQStages = bwd_qstages<D>();
-  uint8_t k[D / 64][kSubBytes];
-  uint8_t v[D / 64][kSubBytes];
+  static constexpr int kQStages = bwd_qstages<D, KVB>();
+  uint8_t k[KVB][D / 64][kSubBytes];  // K / V of work item n in buffer n % KVB
+  uint8_t v[KVB][D / 64][kSubBytes];
   uint8_t q[kQStages][D / 64][kSubBytes];
   uint8_t dO[kQStages][D / 64][kSubBytes];
   uint8_t dst[2][2][kSubBytes];   // dS^T [buffer][query half][128 keys x 64 queries]
@@ -71,7 +73,7 @@ struct __align__(1024) BwdSmem {
   alignas(16) int32_t qhash[kQStages][kTile];
   alignas(16) float lse2[kQStages][kTile];    // -LSE * log2(e)
   alignas(16) float drs[kQStages][kTile];     // -rowsum(dO * O) * scale
-  uint64_t kv_full, kv_empty;
+  uint64_t kv_full[KVB], kv_empty[KVB];
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t s_full, st_empty, ds_full, pt_free, ds_free[2], dq_full, dq_empty, dkv_full, dkv_empty, drain;
   uint64_t dq_sync;  // the 128 threads of the dQ warpgroup around the staging tile
@@ -120,15 +122,15 @@ __device__ __forceinline__ void store_row_bf16(uint16_t* dst_row, const uint32_t
   }
 }
 
-template <int D>
+template <int D, int KVB>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw + pad);
-  constexpr int kQStages = BwdSmem<D>::kQStages;
+  BwdSmem<D, KVB>& sm = *reinterpret_cast<BwdSmem<D, KVB>*>(smem_raw + pad);
+  constexpr int kQStages = BwdSmem<D, KVB>::kQStages;
   constexpr int kHalves = D / 64;  // a work item = (key tile, 64-column half of D)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // live-tile lists where the call that built them put them
@@ -137,8 +139,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384, kColPT = 448;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sm.kv_full, 1);
-    mbar_init(&sm.kv_empty, 1);
+    for (int b = 0; b < KVB; ++b) {
+      mbar_init(&sm.kv_full[b], 1);
+      mbar_init(&sm.kv_empty[b], 1);
+    }
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
@@ -204,14 +208,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       int rr[4], rq[4] = {0, 0, 0, 0}, rn[4] = {0, 0, 0, 0};
       if (p.gather_kv) gather_rows(p.k_idx, bh, p.Tk, p.To, j * kTile, lane, rr);
       if (p.gather_q) gather_rows(p.q_idx, bh, p.Tq, p.To, __shfl_sync(0xffffffffu, cq, 0) * kTile, lane, rq);
+      const int kb = item % KVB;
       if (lane == 0 && !stall) {
-        ok = mbar_wait(&sm.kv_empty, (item & 1) ^ 1, abort_flag, p.status);
+        ok = mbar_wait(&sm.kv_empty[kb], ((item / KVB) & 1) ^ 1, abort_flag, p.status);
         if (ok) {
-          mbar_arrive_expect_tx(&sm.kv_full, 2 * D * kTile * 2);
+          mbar_arrive_expect_tx(&sm.kv_full[kb], 2 * D * kTile * 2);
           if (!p.gather_kv) {
             for (int sub = 0; sub < D / 64; ++sub) {
-              tma_load_3d(sm.k[sub], &tm_k, &sm.kv_full, sub * 64, j * kTile, bh);
-              tma_load_3d(sm.v[sub], &tm_v, &sm.kv_full, sub * 64, j * kTile, bh);
+              tma_load_3d(sm.k[kb][sub], &tm_k, &sm.kv_full[kb], sub * 64, j * kTile, bh);
+              tma_load_3d(sm.v[kb][sub], &tm_v, &sm.kv_full[kb], sub * 64, j * kTile, bh);
             }
           }
           last_kv = item;
@@ -219,8 +224,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
       if (p.gather_kv && !stall) {
-        gather_issue(sm.k[0], kSubBytes, D / 64, &tm_k, &sm.kv_full, rr, lane);
-        gather_issue(sm.v[0], kSubBytes, D / 64, &tm_v, &sm.kv_full, rr, lane);
+        gather_issue(sm.k[kb][0], kSubBytes, D / 64, &tm_k, &sm.kv_full[kb], rr, lane);
+        gather_issue(sm.v[kb][0], kSubBytes, D / 64, &tm_v, &sm.kv_full[kb], rr, lane);
       }
       const int n_steps = stall ? min(n, kQStages) : n;
       for (int t = 0; t < n_steps; ++t) {
@@ -269,7 +274,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int it = q_it - d;
         mbar_wait_drain(&sm.q_full[it % kQStages], (it / kQStages) & 1, p.status);
       }
-      if (last_kv >= 0) mbar_wait_drain(&sm.kv_full, last_kv & 1, p.status);
+      // (items load their K / V in order, so the last KVB loads are the
+      // ones that can still be in flight)
+      for (int d = 0; d < KVB && last_kv - d >= 0; ++d) {
+        const int it = last_kv - d;
+        mbar_wait_drain(&sm.kv_full[it % KVB], (it / KVB) & 1, p.status);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -279,9 +289,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       constexpr uint32_t idesc_q = idesc_bf16_f32(kTile, 64, 1, 1);   // dQ: one 64-column half of D
       // descriptors built once; steps, stages and buffers are constant adds
       constexpr uint32_t kStage16 = (D / 64) * kSubBytes >> 4;
-      const uint64_t kdesc_k = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);           // K, K-major
-      const uint64_t vdesc_k = smem_desc_sw128(smem_u32(sm.v[0]), 16, 1024);           // V, K-major
-      const uint64_t kdesc_mn = smem_desc_sw128(smem_u32(sm.k[0]), kSubBytes, 1024);   // K, MN-major
+      const uint64_t kdesc_k0 = smem_desc_sw128(smem_u32(sm.k[0][0]), 16, 1024);           // K, K-major
+      const uint64_t vdesc_k0 = smem_desc_sw128(smem_u32(sm.v[0][0]), 16, 1024);           // V, K-major
+      const uint64_t kdesc_mn0 = smem_desc_sw128(smem_u32(sm.k[0][0]), kSubBytes, 1024);   // K, MN-major
+      constexpr uint32_t kKvBuf16 = (D / 64) * kSubBytes >> 4;  // one K (or V) buffer
+      uint64_t kdesc_k = kdesc_k0, vdesc_k = vdesc_k0, kdesc_mn = kdesc_mn0;  // this item's buffer
       const uint64_t qdesc_k = smem_desc_sw128(smem_u32(sm.q[0][0]), 16, 1024);
       const uint64_t qdesc_mn = smem_desc_sw128(smem_u32(sm.q[0][0]), kSubBytes, 1024);
       const uint64_t odesc_k = smem_desc_sw128(smem_u32(sm.dO[0][0]), 16, 1024);
@@ -318,7 +330,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int hh = w % kHalves;
         const int n = p.csc_ptr[g + 1] - p.csc_ptr[g];
         if (n == 0) continue;
-        if (!mbar_wait(&sm.kv_full, item & 1, abort_flag, p.status)) break;
+        const int kb = item % KVB;
+        if (!mbar_wait(&sm.kv_full[kb], (item / KVB) & 1, abort_flag, p.status)) break;
+        kdesc_k = kdesc_k0 + static_cast<uint64_t>(kb * kKvBuf16);
+        vdesc_k = vdesc_k0 + static_cast<uint64_t>(kb * kKvBuf16);
+        kdesc_mn = kdesc_mn0 + static_cast<uint64_t>(kb * kKvBuf16);
         if (!issue_a(q_it, it)) break;
         for (int t = 0; t < n; ++t) {
           const int s = q_it % kQStages;
@@ -377,7 +393,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         if (!ok) break;
         tc_commit(&sm.dkv_full);
-        tc_commit(&sm.kv_empty);
+        tc_commit(&sm.kv_empty[item % KVB]);
         ++item;
       }
       tc_commit(&sm.drain);
@@ -1342,12 +1358,18 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
     attn_bwd128_kernel<<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
     record_kernel_event(1, false, st);
   } else {
-    const size_t smem = sizeof(BwdSmem<D>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    // hash mode: about three query tiles per key tile, so a second K / V
+    // buffer (loaded while the previous item runs) is worth a Q / dO stage;
+    // the long columns of the other modes keep the deeper query ring
+    static_assert(sizeof(BwdSmem<D, 2>) + 1024 <= 227 * 1024 && sizeof(BwdSmem<D, 1>) + 1024 <= 227 * 1024,
+                  "shared memory per CTA");
+    const bool two_kv = a.mode == SCFA_MODE_HASH;
+    const size_t smem = (two_kv ? sizeof(BwdSmem<D, 2>) : sizeof(BwdSmem<D, 1>)) + 1024;
+    auto kern = two_kv ? attn_bwd_kernel<D, 2> : attn_bwd_kernel<D, 1>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     record_kernel_event(1, true, st);
-    attn_bwd_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
+    kern<<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdq, p);
     record_kernel_event(1, false, st);
   }
   {
