@@ -300,6 +300,11 @@ scfa_status scfa_hash_bwd(const uint16_t* q_s, const uint16_t* k_s, const uint16
 size_t lsh_workspace_size(int B, int H, int T, int n_buckets);
 scfa_status lsh_hash(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D,
                      int n_buckets, int32_t* hash, void* stream);
+/* lsh_hash_heads: lsh_hash with one rotation per head: R is [H][D][n_buckets/2]
+ * bf16 and head h of every batch is hashed with R[h] (the same construction,
+ * the same exact argmax). Sort the ids with lsh_sort_ids. */
+scfa_status lsh_hash_heads(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D,
+                           int n_buckets, int32_t* hash, void* stream);
 scfa_status lsh_bucket_sort(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D,
                             int n_buckets, int32_t* hash_sorted, int32_t* perm,
                             int32_t* bucket_off, uint16_t* x_sorted,

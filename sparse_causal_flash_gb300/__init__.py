@@ -53,6 +53,7 @@ _SIGS = {
                       _I),
     "lsh_workspace_size": ([_I, _I, _I, _I], _S),
     "lsh_hash": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "lsh_hash_heads": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "lsh_bucket_sort": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _U, _P], _I),
     "scfa_tiled_rows": ([_I, _I], _I),
     "lsh_bucket_sort_tiled": ([_P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_int32, _P, _P, _P, _P, _P, _S, _U, _P], _I),
@@ -215,6 +216,15 @@ def scfa_hash_bwd(q_s, k_s, v_s, o_s, lse_s, do_s, q_idx, k_idx, q_hash, k_hash,
 def lsh_hash(x, R, n_buckets, hash_out, stream=None):
     B, H, T, D = x.shape
     _check("lsh_hash", _lib.lsh_hash(_ptr(x), _ptr(R), B, H, T, D, n_buckets, _ptr(hash_out), _stream(stream)))
+
+
+def lsh_hash_heads(x, R, n_buckets, hash_out, stream=None):
+    """One rotation per head: R [H, D, n_buckets // 2]; hash_out [B,H,T]."""
+    B, H, T, D = x.shape
+    if R.dim() != 3 or R.shape[0] != H or R.shape[1] != D:
+        raise ValueError(f"lsh_hash_heads: R must be [H={H}, D={D}, m], got {tuple(R.shape)}")
+    _check("lsh_hash_heads", _lib.lsh_hash_heads(_ptr(x), _ptr(R), B, H, T, D, n_buckets, _ptr(hash_out),
+                                                 _stream(stream)))
 
 
 def lsh_bucket_sort(x, R, n_buckets, hash_sorted, perm, bucket_off, x_sorted, ws, flags=0, stream=None):

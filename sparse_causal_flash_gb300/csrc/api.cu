@@ -411,6 +411,18 @@ scfa_status lsh_hash(const uint16_t* x, const uint16_t* R, int B, int H, int T, 
                 0, nullptr);
 }
 
+scfa_status lsh_hash_heads(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D, int n_buckets,
+                           int32_t* hash, void* stream) {
+  scfa_status s = check_lsh_args(x, R, B, H, T, D, n_buckets);
+  if (s != SCFA_OK) return s;
+  if (!hash) return SCFA_ERR_INVALID;
+  if ((static_cast<size_t>(D) * ((n_buckets / 2 + 3) & ~3) + 256u * (D / 2 + 1)) * sizeof(float) > 200 * 1024)
+    return SCFA_ERR_UNSUPPORTED;
+  return finish(launch_lsh_hash_heads(x, R, B, H, T, D, n_buckets / 2, hash, lsh_scratch_status(),
+                                      static_cast<cudaStream_t>(stream)),
+                0, nullptr);
+}
+
 scfa_status lsh_bucket_sort(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D, int n_buckets,
                             int32_t* hash_sorted, int32_t* perm, int32_t* bucket_off, uint16_t* x_sorted, void* ws,
                             size_t ws_bytes, unsigned flags, void* stream) {

@@ -88,6 +88,9 @@ cudaError_t launch_validate(int mode, bool original, const int32_t* q_idx, const
 // the CUDA-core kernel)
 cudaError_t launch_lsh_hash(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
                             int32_t* hash, int* status, cudaStream_t st);
+// one rotation per head: R is [H][D][m], head h of x ([B,H,T,D]) uses R[h]
+cudaError_t launch_lsh_hash_heads(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D, int m,
+                                  int32_t* hash, int* status, cudaStream_t st);
 int* lsh_scratch_status();  // device status word of the workspace-free lsh_hash call
 cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
                                  int32_t* hash, cudaStream_t st);

@@ -136,6 +136,28 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
 //     keeps the smallest index among exact ties.
 constexpr int kHashRows = 256;
 
+// The rows of x as n_seg x n_heads segments of seg_rows rows, segment (s, h)
+// starting at row (s * n_heads + h) * seg_rows: with one rotation per head
+// ([B,H,T,D] rows, seg_rows = T, n_seg = B, n_heads = H) the CTAs with
+// blockIdx.y = h stage rotation h (R + h * r_stride) and take the chunks of
+// head h's segments; with one shared rotation the rows are one segment.
+struct LshSegs {
+  long long seg_rows;
+  int n_seg, n_heads;
+  long long r_stride;
+};
+// chunk u (of n_seg * ceil(seg_rows / chunk)) of head h: first row, row count
+__device__ __forceinline__ void seg_chunk(const LshSegs& g, int h, long long u, int chunk, long long* r0, int* nr) {
+  const long long nc = (g.seg_rows + chunk - 1) / chunk;
+  const long long sgi = u / nc, c = u - sgi * nc;
+  *r0 = (sgi * g.n_heads + h) * g.seg_rows + c * chunk;
+  const long long left = g.seg_rows - c * chunk;
+  *nr = static_cast<int>(left < chunk ? left : chunk);
+}
+__host__ __device__ __forceinline__ long long seg_units(const LshSegs& g, int chunk) {
+  return static_cast<long long>(g.n_seg) * ((g.seg_rows + chunk - 1) / chunk);
+}
+
 // R as fp32 [D][m4] in shared memory (zero columns appended), the largest
 // column norm ||R_c||_2 rounded up and the exponent range of R's nonzero
 // entries; every thread of the block calls it.
@@ -337,7 +359,7 @@ __device__ int hash_row(const uint32_t* xrow, const uint16_t* __restrict__ xr, c
 }
 
 __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __restrict__ x,
-                                                             const uint16_t* __restrict__ R, long long rows,
+                                                             const uint16_t* __restrict__ R, LshSegs sg,
                                                              int D, int m, int32_t* __restrict__ hash) {
   const int m4 = (m + 3) & ~3;
   const int xs = D / 2 + 1;  // padded row stride of the staged rows, in 32-bit words
@@ -346,11 +368,14 @@ __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __r
   uint32_t* sX = reinterpret_cast<uint32_t*>(smem + D * m4);         // [kHashRows][xs]
   float rnmax;
   int r_emin, r_emax;
+  R += blockIdx.y * sg.r_stride;
   lsh_prologue(R, D, m, sR, &rnmax, &r_emin, &r_emax);
   const int wpr = D / 2;  // 32-bit words per row
-  for (long long r0 = static_cast<long long>(blockIdx.x) * kHashRows; r0 < rows;
-       r0 += static_cast<long long>(gridDim.x) * kHashRows) {
-    const int nr = static_cast<int>(rows - r0 < kHashRows ? rows - r0 : kHashRows);
+  const long long n_units = seg_units(sg, kHashRows);
+  for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+    long long r0;
+    int nr;
+    seg_chunk(sg, blockIdx.y, u, kHashRows, &r0, &nr);
     __syncthreads();
     const uint32_t* gx = reinterpret_cast<const uint32_t*>(x + r0 * D);
     for (int i = threadIdx.x; i < nr * wpr; i += blockDim.x) sX[(i / wpr) * xs + (i % wpr)] = gx[i];
@@ -377,7 +402,7 @@ constexpr int kFixWarps = 8;
 constexpr int kFixSeg = 2048;  // rows per CTA step; the shared list holds up to this many
 
 __global__ void __launch_bounds__(kFixWarps * 32, 2) lsh_fix_kernel(const uint16_t* __restrict__ x,
-                                                                 const uint16_t* __restrict__ R, long long rows,
+                                                                 const uint16_t* __restrict__ R, LshSegs sg,
                                                                  int D, int m, int32_t* __restrict__ hash) {
   extern __shared__ float smem[];
   const int m4 = (m + 3) & ~3;
@@ -385,6 +410,7 @@ __global__ void __launch_bounds__(kFixWarps * 32, 2) lsh_fix_kernel(const uint16
   float* sxall = smem + D * m4;          // [kFixWarps][D]
   float rnmax;
   int r_emin, r_emax;
+  R += blockIdx.y * sg.r_stride;
   lsh_prologue(R, D, m, sR, &rnmax, &r_emin, &r_emax);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* sx = sxall + warp * D;
@@ -392,13 +418,16 @@ __global__ void __launch_bounds__(kFixWarps * 32, 2) lsh_fix_kernel(const uint16
   const float absb = static_cast<float>(D) * 0x1p-148f;
   __shared__ int s_n;
   __shared__ int s_list[kFixSeg];  // offsets of the flagged rows in the segment
-  for (long long seg = static_cast<long long>(blockIdx.x) * kFixSeg; seg < rows;
-       seg += static_cast<long long>(gridDim.x) * kFixSeg) {
+  const long long n_units = seg_units(sg, kFixSeg);
+  for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+    long long seg;
+    int nseg;
+    seg_chunk(sg, blockIdx.y, u, kFixSeg, &seg, &nseg);
     __syncthreads();  // the previous segment's list is consumed
     if (threadIdx.x == 0) s_n = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < kFixSeg; i += blockDim.x)
-      if (seg + i < rows && hash[seg + i] < 0) s_list[atomicAdd(&s_n, 1)] = i;
+    for (int i = threadIdx.x; i < nseg; i += blockDim.x)
+      if (hash[seg + i] < 0) s_list[atomicAdd(&s_n, 1)] = i;
     __syncthreads();
     const int n_flag = s_n;
     for (int li = warp; li < n_flag; li += kFixWarps) {
@@ -554,13 +583,16 @@ struct __align__(1024) LshTcSmem {
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
-lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __restrict__ R, long long rows,
+lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __restrict__ R, LshSegs sg,
                    int m, int m_pad, int32_t* __restrict__ hash, int* status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   LshTcSmem<D>& sm = *reinterpret_cast<LshTcSmem<D>*>(smem_raw + pad);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long n_tiles = (rows + kTile - 1) / kTile;
+  // tiles: 128-row chunks of this head's segments (rotation blockIdx.y)
+  const long long n_tiles = seg_units(sg, kTile);
+  const int hd = blockIdx.y;
+  R += hd * sg.r_stride;
   const uint32_t acc_cols = m_pad < 32 ? 32u : static_cast<uint32_t>(m_pad);
   const uint32_t tmem_cols = acc_cols * 2 <= 32 ? 32u : (acc_cols * 2 <= 64 ? 64u : (acc_cols * 2 <= 128 ? 128u : (acc_cols * 2 <= 256 ? 256u : 512u)));
 
@@ -634,10 +666,13 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
       int it = 0;
       for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
         const int s = it % kTcStages;
+        long long r0;
+        int nr;
+        seg_chunk(sg, hd, t, kTile, &r0, &nr);
         if (!mbar_wait(&sm.x_empty[s], ((it / kTcStages) & 1) ^ 1, abort_flag, status)) break;
         mbar_arrive_expect_tx(&sm.x_full[s], D * kTile * 2);
         for (int sub = 0; sub < D / 64; ++sub)
-          tma_load_3d(sm.x[s][sub], &tm_x, &sm.x_full[s], sub * 64, static_cast<int>(t * kTile), 0);
+          tma_load_3d(sm.x[s][sub], &tm_x, &sm.x_full[s], sub * 64, static_cast<int>(r0), 0);
       }
       for (int d = 1; d <= kTcStages && d <= it; ++d) {
         const int i2 = it - d;
@@ -739,8 +774,11 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
       }
       tc_fence_before();
       mbar_arrive(&sm.acc_empty[b]);
-      const long long row = t * kTile + rr;
-      if (row < rows) {
+      long long r0;
+      int nr;
+      seg_chunk(sg, hd, t, kTile, &r0, &nr);
+      const long long row = r0 + rr;
+      if (rr < nr) {
         const bool clear = !r_bad && !x_bad && l2 < 0x1p60f && rnmax < 0x1p60f && (t0 - t1 > 2.f * emax * 1.0001f);
         hash[row] = clear ? j0 : -1;
       }
@@ -934,8 +972,8 @@ int* lsh_scratch_status() {
 }
 
 template <int D>
-static cudaError_t launch_lsh_tc(const uint16_t* x, const uint16_t* R, long long rows, int m, int32_t* hash,
-                                 int* status, cudaStream_t st) {
+static cudaError_t launch_lsh_tc(const uint16_t* x, const uint16_t* R, long long rows, const LshSegs& sg, int m,
+                                 int32_t* hash, int* status, cudaStream_t st) {
   CUtensorMap tm;
   if (!make_tmap_bf16_3d(&tm, x, D, rows, 1)) return cudaErrorInvalidValue;
   const int m_pad = (m + 15) / 16 * 16;
@@ -943,49 +981,65 @@ static cudaError_t launch_lsh_tc(const uint16_t* x, const uint16_t* R, long long
   cudaError_t e = cudaFuncSetAttribute(lsh_hash_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long n_tiles = (rows + kTile - 1) / kTile;
-  long long g = num_sms();
+  // about one CTA per SM in all, split over the rotations
+  const long long n_tiles = seg_units(sg, kTile);
+  long long g = num_sms() / sg.n_heads;
   if (g > n_tiles) g = n_tiles;
   if (g < 1) g = 1;
-  lsh_hash_tc_kernel<D><<<static_cast<int>(g), kTcThreads, smem, st>>>(tm, R, rows, m, m_pad, hash, status);
+  lsh_hash_tc_kernel<D><<<dim3(static_cast<unsigned>(g), sg.n_heads), kTcThreads, smem, st>>>(tm, R, sg, m, m_pad,
+                                                                                            hash, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // certified second pass over the rows the first pass left at -1
   const size_t smem2 = static_cast<size_t>(D) * (((m + 3) & ~3) + kFixWarps) * sizeof(float);
   e = cudaFuncSetAttribute(lsh_fix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem2));
   if (e != cudaSuccess) return e;
-  long long g2 = (rows + kFixSeg - 1) / kFixSeg;
-  if (g2 > 2LL * num_sms()) g2 = 2LL * num_sms();  // two CTAs per SM
+  long long g2 = seg_units(sg, kFixSeg);
+  const long long cap2 = 2LL * num_sms() / sg.n_heads;  // two CTAs per SM
+  if (g2 > cap2) g2 = cap2;
   if (g2 < 1) g2 = 1;
-  lsh_fix_kernel<<<static_cast<int>(g2), kFixWarps * 32, smem2, st>>>(x, R, rows, D, m, hash);
+  lsh_fix_kernel<<<dim3(static_cast<unsigned>(g2), sg.n_heads), kFixWarps * 32, smem2, st>>>(x, R, sg, D, m, hash);
   return cudaGetLastError();
 }
 
-// The tensor-core path needs D = 64 or 128, m a multiple of 8 (16-byte rows of
-// R), m <= 256 (one accumulator fits twice in TMEM) and a 16-byte aligned x;
-// other shapes take the CUDA-core kernel.
-cudaError_t launch_lsh_hash(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
-                            int32_t* hash, int* status, cudaStream_t st) {
+static cudaError_t launch_lsh_segs(const uint16_t* x, const uint16_t* R, long long rows, const LshSegs& sg, int D,
+                                   int m, int32_t* hash, int* status, cudaStream_t st) {
+  // The tensor-core path needs D = 64 or 128, m a multiple of 8 (16-byte rows
+  // of R), m <= 256 (one accumulator fits twice in TMEM) and a 16-byte aligned
+  // x; other shapes take the CUDA-core kernel.
   const bool tc_ok = (D == 64 || D == 128) && m % 8 == 0 && m >= 8 && m <= 256 && status != nullptr &&
                      (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && rows < (1ll << 31);
-  if (tc_ok) return D == 64 ? launch_lsh_tc<64>(x, R, rows, m, hash, status, st)
-                            : launch_lsh_tc<128>(x, R, rows, m, hash, status, st);
-  return launch_lsh_hash_cuda(x, R, rows, D, m, hash, st);
-}
-
-cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
-                                 int32_t* hash, cudaStream_t st) {
+  if (tc_ok) return D == 64 ? launch_lsh_tc<64>(x, R, rows, sg, m, hash, status, st)
+                            : launch_lsh_tc<128>(x, R, rows, sg, m, hash, status, st);
   const size_t smem = (static_cast<size_t>(D) * ((m + 3) & ~3) + static_cast<size_t>(kHashRows) * (D / 2 + 1)) *
                       sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(lsh_hash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  long long g = (rows + kHashRows - 1) / kHashRows;
-  const long long cap = static_cast<long long>(num_sms()) * 8;
+  long long g = seg_units(sg, kHashRows);
+  const long long cap = static_cast<long long>(num_sms()) * 8 / sg.n_heads;
   if (g > cap) g = cap;
   if (g < 1) g = 1;
-  lsh_hash_kernel<<<static_cast<int>(g), kHashRows, smem, st>>>(x, R, rows, D, m, hash);
+  lsh_hash_kernel<<<dim3(static_cast<unsigned>(g), sg.n_heads), kHashRows, smem, st>>>(x, R, sg, D, m, hash);
   return cudaGetLastError();
+}
+
+cudaError_t launch_lsh_hash(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
+                            int32_t* hash, int* status, cudaStream_t st) {
+  const LshSegs sg = {rows, 1, 1, 0};  // one rotation for every row
+  return launch_lsh_segs(x, R, rows, sg, D, m, hash, status, st);
+}
+
+cudaError_t launch_lsh_hash_heads(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D, int m,
+                                  int32_t* hash, int* status, cudaStream_t st) {
+  const LshSegs sg = {T, B, H, static_cast<long long>(D) * m};  // rotation h for the rows of head h
+  return launch_lsh_segs(x, R, static_cast<long long>(B) * H * T, sg, D, m, hash, status, st);
+}
+
+cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long rows, int D, int m,
+                                 int32_t* hash, cudaStream_t st) {
+  const LshSegs sg = {rows, 1, 1, 0};
+  return launch_lsh_segs(x, R, rows, sg, D, m, hash, nullptr, st);
 }
 
 cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int nb,

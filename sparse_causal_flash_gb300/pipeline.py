@@ -18,7 +18,8 @@ from __future__ import annotations
 import torch
 
 from . import (FLAG_GATHER_KV, FLAG_GATHER_Q, FLAG_KEEP_O32, FLAG_ORIGINAL_ORDER, FLAG_REUSE_TILES, MODE_DENSE, MODE_HASH, MODE_QK, attn_workspace_size,
-               attn_workspace_size_live, lsh_bucket_sort, lsh_bucket_sort_tiled, lsh_gather, lsh_hash, lsh_sort_ids,
+               attn_workspace_size_live, lsh_bucket_sort, lsh_bucket_sort_tiled, lsh_gather, lsh_hash, lsh_hash_heads,
+               lsh_sort_ids,
                lsh_workspace_size,
                scfa_dense_bwd, scfa_tiled_rows,
                scfa_dense_fwd, scfa_hash_bwd, scfa_hash_fwd, scfa_qk_bwd, scfa_qk_fwd, scfa_tiles_count, workspace)
@@ -35,7 +36,8 @@ class Step:
     """Buffers and the launch sequence of one fwd+bwd step for a fixed shape."""
 
     def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
-                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False, gather=None):
+                 device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False, gather=None,
+                 per_head_r: bool = False):
         """tiled (hash mode; the default): sort into the tile-aligned layout,
         every bucket starting on a tile boundary (lsh_bucket_sort_tiled); the
         sorted tensors then have Ts = scfa_tiled_rows(T, n_buckets) rows per
@@ -49,12 +51,15 @@ class Step:
         SCFA_FLAG_GATHER_KV). The default, None, is "kv" on the tile-aligned
         layout (the fastest on GB300: the backward's query-tile ring waits on
         gathered rows, its resident key tile does not) and False on the plain
-        one."""
+        one.
+        per_head_r (hash mode): one rotation per head, R [H, D, n_buckets // 2]
+        (lsh_hash_heads); the ids are then sorted with lsh_sort_ids."""
         self.mode, self.B, self.H, self.Tq, self.Tk, self.D = mode, B, H, Tq, Tk, D
         self.nb = n_buckets
         self.flags = flags
         self.tiled = mode == MODE_HASH and (tiled is None or bool(tiled))
         self.shared_qk = mode == MODE_HASH and bool(shared_qk)
+        self.per_head_r = mode == MODE_HASH and bool(per_head_r)
         if gather is None:
             gather = "kv" if self.tiled else False
         g = "qkv" if gather is True else (gather or "")
@@ -110,8 +115,10 @@ class Step:
             if not self.gkv:
                 self.k_s = torch.empty((B, H, Ts, D), **bf)
                 self.v_s = torch.empty((B, H, Ts, D), **bf)
-            if self.shared_qk:
+            if self.shared_qk or self.per_head_r:
                 self.ids = torch.empty((B, H, T), **i32)  # bucket ids in original order
+            if self.per_head_r and not self.shared_qk:
+                self.kids = torch.empty((B, H, T), **i32)
 
     def run(self, q, k, v, do, scale, q_idx=None, k_idx=None, R=None, stream=None, mark=None):
         """Forward + backward. Results land in self.o/lse/dq/dk/dv.
@@ -140,6 +147,8 @@ class Step:
             side = self.side if mark is None else main
             if self.shared_qk:
                 self._shared_qk_sorts(q, k, v, do, R, main, side, tick)
+            elif self.per_head_r:
+                self._per_head_sorts(q, k, v, do, R, main, side, tick)
             else:
                 self._sorts(q, k, v, do, R, main, side, tick)
             main.wait_event(self.ev[1])
@@ -175,9 +184,12 @@ class Step:
             self.run(q, k, v, do, scale, q_idx=q_idx, k_idx=k_idx, R=R)
         return g
 
+    def _hash(self, x, R, ids, stream):
+        (lsh_hash_heads if self.per_head_r else lsh_hash)(x, R, self.nb, ids, stream)
+
     def _shared_qk_sorts(self, q, k, v, do, R, main, side, tick):
         nb = self.nb
-        lsh_hash(q, R, nb, self.ids, main)
+        self._hash(q, R, self.ids, main)
         tick("hash_q")
         self.ev[0].record(main)
         side.wait_event(self.ev[0])
@@ -225,6 +237,24 @@ class Step:
             lsh_gather(do, self.pq, self.do_s, main)
         tick("gather_do")
 
+    def _per_head_sorts(self, q, k, v, do, R, main, side, tick):
+        nb = self.nb
+        self.ev[0].record(main)
+        side.wait_event(self.ev[0])
+        lsh_hash_heads(k, R, nb, self.kids, side)
+        lsh_sort_ids(self.kids, nb, K_PAD, self.kh, self.pk, self.offk, self.ws_lk, 0, side)
+        if not self.gkv:
+            lsh_gather(k, self.pk, self.k_s, side)
+            lsh_gather(v, self.pk, self.v_s, side)
+        tick("hash_sort_k_v")
+        self.ev[1].record(side)
+        lsh_hash_heads(q, R, nb, self.ids, main)
+        lsh_sort_ids(self.ids, nb, Q_PAD, self.qh, self.pq, self.offq, self.ws_l, 0, main)
+        if not self.gq:
+            lsh_gather(q, self.pq, self.q_s, main)
+            lsh_gather(do, self.pq, self.do_s, main)
+        tick("hash_sort_q_do")
+
     def _size_lists(self, stream):
         """Count this batch's live tiles (reads one int back) and grow the
         workspace if its lists cannot hold them (with an eighth to spare)."""
@@ -256,10 +286,10 @@ class HostPipeline:
 
     def __init__(self, mode: int, B: int, H: int, Tq: int, Tk: int, D: int, n_buckets: int = 0,
                  device="cuda", flags: int = 0, tiled=None, shared_qk: bool = False, gather=None,
-                 graphs: bool = True):
+                 per_head_r: bool = False, graphs: bool = True):
         self.device = torch.device(device)
         self.steps = [Step(mode, B, H, Tq, Tk, D, n_buckets=n_buckets, device=self.device, flags=flags,
-                           tiled=tiled, shared_qk=shared_qk, gather=gather)
+                           tiled=tiled, shared_qk=shared_qk, gather=gather, per_head_r=per_head_r)
                       for _ in range(2)]
         # graphs: from its second use on, a slot's step runs as one CUDA graph
         # captured on the slot's device input buffers (not for live-sized
