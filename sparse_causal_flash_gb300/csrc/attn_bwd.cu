@@ -1196,8 +1196,11 @@ __global__ void bwd_pre_kernel(const PreParams p) {
     const long long bh = rp / p.Tqp;
     const int r = static_cast<int>(rp - bh * p.Tqp);
     const bool inside = rp < p.n_pad;
-    const bool active = inside && r < p.Tq;
     const long long row = bh * p.Tq + r;
+    // with original-order outputs a sorted row whose index falls outside
+    // [0, To) (a padding row) has no output: no dO / O reads and no dQ reset
+    // for it, and metadata that masks it (position INT_MIN)
+    const bool active = inside && r < p.Tq && (p.o_rows == nullptr || mapped_row(p.o_rows, row, bh, p.To) >= 0);
     float s = 0.f;
     if (active) {
       const long long drow = mapped_row(p.do_rows, row, bh, p.To);
