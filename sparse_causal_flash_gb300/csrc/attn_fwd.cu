@@ -588,7 +588,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
           }
           p.lse[grow] = -INFINITY;
-          if (p.o32) zero_o32_row<D>(p.o32 + grow * D);
+          if (p.o32 && orow >= 0) zero_o32_row<D>(p.o32 + grow * D);
         }
         continue;
       }
@@ -631,7 +631,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (orow >= 0) dst[c] = u;
         }
         p.lse[grow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
-        if (p.o32) store_o32_row<D>(p.o32 + grow * D, orr, orow >= 0 ? inv : 0.f);
+        // (a padding row of an original-order step has no O32 row: the
+        // backward pre-pass skips it)
+        if (p.o32 && orow >= 0) store_o32_row<D>(p.o32 + grow * D, orr, inv);
       }
     }
   }
@@ -1145,7 +1147,7 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
           }
           p.lse[grow] = -INFINITY;
-          if (p.o32) zero_o32_row<D>(p.o32 + grow * D);
+          if (p.o32 && orow >= 0) zero_o32_row<D>(p.o32 + grow * D);
         }
         continue;
       }
@@ -1188,7 +1190,9 @@ attn_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           if (orow >= 0) dst[c] = u;
         }
         p.lse[grow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
-        if (p.o32) store_o32_row<D>(p.o32 + grow * D, orr, orow >= 0 ? inv : 0.f);
+        // (a padding row of an original-order step has no O32 row: the
+        // backward pre-pass skips it)
+        if (p.o32 && orow >= 0) store_o32_row<D>(p.o32 + grow * D, orr, inv);
       }
     }
   }
