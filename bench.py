@@ -138,8 +138,9 @@ def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0, til
     """Library kernels launched per step (the library's own launch sequence).
     gather_kv: the attention kernels read K and V rows through the key
     permutation (the tile-aligned step's default), so neither is moved."""
-    # header init, tile stats (q, k), count, scan, fill, work order (+ pair lists at D = 128)
-    tiles = 7 + (1 if D == 128 else 0)
+    # header init with the tile stats of both sides, count, scans with the
+    # work orders, fill (+ pair lists and their order at D = 128)
+    tiles = 4 + (2 if D == 128 else 0)
     attn = 1 + 3         # forward; backward pre-pass, backward, dQ finalise
     if mode == "hash":
         m = n_buckets // 2

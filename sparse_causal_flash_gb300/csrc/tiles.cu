@@ -33,24 +33,50 @@ __device__ __forceinline__ int warp_max(int v) {
   return v;
 }
 
-// One warp per tile: {min idx, max idx, min hash, max hash} over valid rows.
-__global__ void tile_stats_kernel(int mode, const int32_t* __restrict__ idx,
-                                  const int32_t* __restrict__ hash,
-                                  long long n_tiles, int T, int nT, int4* __restrict__ out) {
+// One side of the tile statistics pass: index and bucket arrays, tiles.
+struct StatSide {
+  const int32_t* idx;
+  const int32_t* hash;
+  long long n_tiles;
+  int T, nT;
+  int4* out;
+};
+// Where the call puts the live-tile lists and how many entries they hold.
+struct HdrInit {
+  long long off[5];
+  long long cap;
+};
+
+// One warp per tile: {min idx, max idx, min hash, max hash} over valid rows,
+// query tiles first, then key tiles. Thread 0 of block 0 also clears the
+// status word, counters and schedule and records the list layout (the
+// header is read only by later launches).
+__global__ void tile_stats_kernel(int mode, StatSide qs, StatSide ks, WsHeader* hdr, HdrInit hi) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    hdr->status = 0;
+    hdr->n_live = 0;
+    for (int i = 0; i < 4; ++i) hdr->sched[i] = 0;
+    for (int i = 0; i < 5; ++i) hdr->list_off[i] = hi.off[i];
+    hdr->list_cap = hi.cap;
+  }
   const int lane = threadIdx.x & 31;
   const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  for (long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < n_tiles; t += warps) {
-    const long long bh = t / nT;
-    const int r0 = static_cast<int>(t % nT) * kTile;
-    const int rows = min(kTile, T - r0);
+  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < qs.n_tiles + ks.n_tiles;
+       w += warps) {
+    const bool q_side = w < qs.n_tiles;
+    const StatSide& sd = q_side ? qs : ks;
+    const long long t = q_side ? w : w - qs.n_tiles;
+    const long long bh = t / sd.nT;
+    const int r0 = static_cast<int>(t % sd.nT) * kTile;
+    const int rows = min(kTile, sd.T - r0);
     int mn = INT_MAX, mx = INT_MIN, hmn = INT_MAX, hmx = INT_MIN;
     for (int r = lane; r < rows; r += 32) {
-      const long long g = bh * T + r0 + r;
-      const int id = (mode == SCFA_MODE_DENSE) ? (r0 + r) : idx[g];
+      const long long g = bh * sd.T + r0 + r;
+      const int id = (mode == SCFA_MODE_DENSE) ? (r0 + r) : sd.idx[g];
       mn = min(mn, id);
       mx = max(mx, id);
       if (mode == SCFA_MODE_HASH) {
-        const int h = hash[g];
+        const int h = sd.hash[g];
         hmn = min(hmn, h);
         hmx = max(hmx, h);
       }
@@ -59,7 +85,7 @@ __global__ void tile_stats_kernel(int mode, const int32_t* __restrict__ idx,
     mx = warp_max(mx);
     hmn = warp_min(hmn);
     hmx = warp_max(hmx);
-    if (lane == 0) out[t] = make_int4(mn, mx, hmn, hmx);
+    if (lane == 0) sd.out[t] = make_int4(mn, mx, hmn, hmx);
   }
 }
 
@@ -144,12 +170,22 @@ __global__ void tile_count_kernel(TileCtx c, long long n_q, long long n_k,
 // kcount. If the total exceeds the lists' capacity `cap`, every pointer is 0
 // (all lists empty, so nothing reads or writes past them) and the status word
 // says SCFA_ERR_WORKSPACE.
-__global__ void tile_scan_kernel(const int32_t* __restrict__ qcount, long long n_q, int32_t* __restrict__ row_ptr,
-                                 const int32_t* __restrict__ kcount, long long n_k, int32_t* __restrict__ csc_ptr,
-                                 WsHeader* hdr, long long cap) {
-  const int32_t* in = blockIdx.x == 0 ? qcount : kcount;
-  int32_t* out = blockIdx.x == 0 ? row_ptr : csc_ptr;
-  const long long n = blockIdx.x == 0 ? n_q : n_k;
+struct ScanArgs {
+  const int32_t* qcount;
+  long long n_q;
+  int32_t* row_ptr;
+  const int32_t* kcount;
+  long long n_k;
+  int32_t* csc_ptr;
+  WsHeader* hdr;
+  long long cap;
+};
+__device__ void tile_scan_block(const ScanArgs& a, int blk) {
+  const int32_t* in = blk == 0 ? a.qcount : a.kcount;
+  int32_t* out = blk == 0 ? a.row_ptr : a.csc_ptr;
+  const long long n = blk == 0 ? a.n_q : a.n_k;
+  WsHeader* hdr = a.hdr;
+  const long long cap = a.cap;
   const int tid = threadIdx.x, nt = blockDim.x;
   const long long per = (n + nt - 1) / nt;
   const long long b = min(n, per * tid), e = min(n, b + per);
@@ -182,7 +218,7 @@ __global__ void tile_scan_kernel(const int32_t* __restrict__ qcount, long long n
   }
   if (tid == nt - 1) {
     out[n] = static_cast<int32_t>(run);
-    if (blockIdx.x == 0) {
+    if (blk == 0) {
       hdr->n_live = static_cast<int>(run);
       if (over) raise_status(&hdr->status, SCFA_ERR_WORKSPACE);
     }
@@ -323,9 +359,8 @@ constexpr int kOrderWarpBins = 8192;  // per-warp bin offsets (few distinct coun
 // 2 the order of query-tile pairs. The whole block histograms; warp 0 scans
 // and scatters in id order (stable by construction), reading the counts from
 // shared memory, where the whole block stages them one chunk at a time.
-__global__ void work_order_kernel(OrderList l0, OrderList l1, OrderList l2, int smem_bins) {
+__device__ void work_order_block(const OrderList& L, int smem_bins) {
   extern __shared__ int32_t scur[];
-  const OrderList L = blockIdx.x == 0 ? l0 : (blockIdx.x == 1 ? l1 : l2);
   const int32_t* cnt = L.count;
   const long long n = L.n;
   const int maxc = L.maxc;
@@ -451,6 +486,22 @@ __global__ void work_order_kernel(OrderList l0, OrderList l1, OrderList l2, int 
   }
 }
 
+// The two exclusive scans (blocks 0 and 1: row_ptr, csc_ptr) and the work
+// orders of the query and key tiles (blocks 2 and 3) in one launch: the
+// orders read only the counts, so they need not wait for the scans. A launch
+// of two blocks runs the scans alone.
+__global__ void tile_scan_order_kernel(ScanArgs sa, OrderList lq, OrderList lk, int smem_bins) {
+  if (blockIdx.x < 2) {
+    tile_scan_block(sa, blockIdx.x);
+  } else {
+    work_order_block(blockIdx.x == 2 ? lq : lk, smem_bins);
+  }
+}
+
+// The order of the query-tile pairs (head dimension 128), once their union
+// lists are counted.
+__global__ void pair_order_kernel(OrderList lp, int smem_bins) { work_order_block(lp, smem_bins); }
+
 // SCFA_FLAG_VALIDATE: checks the documented contracts of the index inputs and
 // raises SCFA_ERR_INVALID in the status word on the first violation (nothing
 // traps; the attention still runs and its results are then undefined).
@@ -500,23 +551,6 @@ __global__ void validate_kernel(int mode, int original, const int32_t* __restric
   }
 }
 
-// Clears the status word, counters and schedule, and records where this call
-// puts the live-tile lists and how many entries they hold.
-__global__ void ws_header_init_kernel(WsHeader* hdr, long long c0, long long c1, long long c2, long long c3,
-                                      long long c4, long long cap) {
-  if (threadIdx.x == 0) {
-    hdr->status = 0;
-    hdr->n_live = 0;
-    for (int i = 0; i < 4; ++i) hdr->sched[i] = 0;
-    hdr->list_off[kListCols] = c0;
-    hdr->list_off[kListCscRows] = c1;
-    hdr->list_off[kListFflags] = c2;
-    hdr->list_off[kListCflags] = c3;
-    hdr->list_off[kListPairs] = c4;
-    hdr->list_cap = cap;
-  }
-}
-
 inline int grid_for(long long work, int block, int max_blocks) {
   long long g = (work + block - 1) / block;
   if (g < 1) g = 1;
@@ -556,45 +590,49 @@ cudaError_t launch_tiles(int mode, const int32_t* q_idx, const int32_t* k_idx,
   int32_t* row_ptr = reinterpret_cast<int32_t*>(ws + L.row_ptr);
   int32_t* csc_ptr = reinterpret_cast<int32_t*>(ws + L.csc_ptr);
 
-  ws_header_init_kernel<<<1, 32, 0, st>>>(hdr, static_cast<long long>(L.cols), static_cast<long long>(L.csc_rows),
-                                         static_cast<long long>(L.fflags), static_cast<long long>(L.cflags),
-                                         static_cast<long long>(L.ulist), L.cap);
-  cudaError_t e = cudaSuccess;
-  tile_stats_kernel<<<grid_for(L.n_qtiles * 32, 256, sms * 8), 256, 0, st>>>(
-      mode, q_idx, q_hash, L.n_qtiles, Tq, L.nQt, qstat);
-  tile_stats_kernel<<<grid_for(L.n_ktiles * 32, 256, sms * 8), 256, 0, st>>>(
-      mode, k_idx, k_hash, L.n_ktiles, Tk, L.nKt, kstat);
-  TileCtx c{mode, flags, Tq, Tk, L.nQt, L.nKt, qstat, kstat};
+  // header + tile statistics of both sides; counts; scans with the two
+  // work orders; lists (+ pair unions and their order at D = 128)
+  const HdrInit hi{{static_cast<long long>(L.cols), static_cast<long long>(L.csc_rows),
+                    static_cast<long long>(L.fflags), static_cast<long long>(L.cflags),
+                    static_cast<long long>(L.ulist)},
+                   L.cap};
+  const StatSide sq{q_idx, q_hash, L.n_qtiles, Tq, L.nQt, qstat};
+  const StatSide sk{k_idx, k_hash, L.n_ktiles, Tk, L.nKt, kstat};
   const long long nt = L.n_qtiles + L.n_ktiles;
+  tile_stats_kernel<<<grid_for(nt * 32, 256, sms * 8), 256, 0, st>>>(mode, sq, sk, hdr, hi);
+  TileCtx c{mode, flags, Tq, Tk, L.nQt, L.nKt, qstat, kstat};
   tile_count_kernel<<<grid_for(nt * 32, 256, sms * 8), 256, 0, st>>>(c, L.n_qtiles, L.n_ktiles, qcount, kcount);
-  tile_scan_kernel<<<2, 1024, 0, st>>>(qcount, L.n_qtiles, row_ptr, kcount, L.n_ktiles, csc_ptr, hdr,
-                                       count_only ? LLONG_MAX : L.cap);
-  if (count_only) return cudaGetLastError();
-  tile_fill_kernel<<<grid_for(nt * 32, 256, sms * 8), 256, 0, st>>>(
-      c, L.n_qtiles, L.n_ktiles, row_ptr, reinterpret_cast<int32_t*>(ws + L.cols),
-      reinterpret_cast<uint8_t*>(ws + L.fflags), csc_ptr, reinterpret_cast<int32_t*>(ws + L.csc_rows),
-      reinterpret_cast<uint8_t*>(ws + L.cflags));
-  if (with_pairs)
-    pair_list_kernel<<<grid_for(L.n_pairs * 32, 256, sms * 8), 256, 0, st>>>(
-      row_ptr, reinterpret_cast<const int32_t*>(ws + L.cols), reinterpret_cast<const uint8_t*>(ws + L.fflags),
-      L.nQt, L.nPairs, L.n_pairs, reinterpret_cast<int32_t*>(ws + L.pcount), reinterpret_cast<int32_t*>(ws + L.ulist));
+  const ScanArgs sa{qcount, L.n_qtiles, row_ptr, kcount, L.n_ktiles, csc_ptr, hdr, count_only ? LLONG_MAX : L.cap};
   const int smem_bins = 12 * 1024;  // 48 KB of shared memory; larger histograms use the workspace
   const size_t smem = static_cast<size_t>(smem_bins + kOrderChunk + kOrderWarpBins) * sizeof(int32_t);
   static bool order_smem_set[64] = {};
   int dev = 0;
-  e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !order_smem_set[dev]) {
-    e = cudaFuncSetAttribute(work_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(tile_scan_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(pair_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) order_smem_set[dev] = true;
   }
   int32_t* gcur = reinterpret_cast<int32_t*>(ws + L.cursor);
   OrderList lf{qcount, L.n_qtiles, L.nKt, reinterpret_cast<int32_t*>(ws + L.work_fwd), gcur, false};
   OrderList lb{kcount, L.n_ktiles, L.nQt, reinterpret_cast<int32_t*>(ws + L.work_bwd), gcur + L.nKt + 1, true};
-  OrderList lp{reinterpret_cast<const int32_t*>(ws + L.pcount), with_pairs ? L.n_pairs : 0, L.nKt,
-               reinterpret_cast<int32_t*>(ws + L.work_pairs), gcur + L.nKt + L.nQt + 2, false};
-  work_order_kernel<<<3, 1024, smem, st>>>(lf, lb, lp, smem_bins);
+  tile_scan_order_kernel<<<count_only ? 2 : 4, 1024, smem, st>>>(sa, lf, lb, smem_bins);
+  if (count_only) return cudaGetLastError();
+  tile_fill_kernel<<<grid_for(nt * 32, 256, sms * 8), 256, 0, st>>>(
+      c, L.n_qtiles, L.n_ktiles, row_ptr, reinterpret_cast<int32_t*>(ws + L.cols),
+      reinterpret_cast<uint8_t*>(ws + L.fflags), csc_ptr, reinterpret_cast<int32_t*>(ws + L.csc_rows),
+      reinterpret_cast<uint8_t*>(ws + L.cflags));
+  if (with_pairs) {
+    pair_list_kernel<<<grid_for(L.n_pairs * 32, 256, sms * 8), 256, 0, st>>>(
+        row_ptr, reinterpret_cast<const int32_t*>(ws + L.cols), reinterpret_cast<const uint8_t*>(ws + L.fflags),
+        L.nQt, L.nPairs, L.n_pairs, reinterpret_cast<int32_t*>(ws + L.pcount), reinterpret_cast<int32_t*>(ws + L.ulist));
+    OrderList lp{reinterpret_cast<const int32_t*>(ws + L.pcount), L.n_pairs, L.nKt,
+                 reinterpret_cast<int32_t*>(ws + L.work_pairs), gcur + L.nKt + L.nQt + 2, false};
+    pair_order_kernel<<<1, 1024, smem, st>>>(lp, smem_bins);
+  }
   return cudaGetLastError();
 }
 
