@@ -100,7 +100,7 @@ class Step:
             self.ws_l = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
             self.ws_lk = workspace(lsh_workspace_size(B, H, T, n_buckets), dev)
             self.side = torch.cuda.Stream(device=dev)
-            self.ev = [torch.cuda.Event() for _ in range(3)]
+            self.ev = [torch.cuda.Event() for _ in range(5)]
             self.qh = torch.empty((B, H, Ts), **i32)
             self.kh = torch.empty((B, H, Ts), **i32)
             self.pq = torch.empty((B, H, Ts), **i32)
@@ -164,6 +164,8 @@ class Step:
             scfa_hash_fwd(xq, xk, xv, self.pq, self.pk, self.qh, self.kh, scale, self.o, self.lse, self.ws_f, f | g,
                           main)
             tick("fwd")
+            if not self.gq:
+                main.wait_event(self.ev[4])  # dO in sorted order (moved during the forward)
             scfa_hash_bwd(xq, xk, xv, self.o, self.lse, xdo, self.pq, self.pk, self.qh, self.kh, scale, self.dq,
                           self.dk, self.dv, self.ws_b, fr | g, main)
             tick("bwd")
@@ -202,7 +204,7 @@ class Step:
         lsh_sort_ids(self.ids, nb, Q_PAD, self.qh, self.pq, self.offq, self.ws_l, 0, main)
         if not self.gq:
             lsh_gather(q, self.pq, self.q_s, main)
-            lsh_gather(do, self.pq, self.do_s, main)
+        self._move_do_late(do, main, side)
         tick("sort_gather_q_do")
 
     def _sorts(self, q, k, v, do, R, main, side, tick):
@@ -233,8 +235,7 @@ class Step:
         if split:
             main.wait_event(self.ev[2])
             lsh_gather(v, self.pk, self.v_s, main)
-        if not self.gq:
-            lsh_gather(do, self.pq, self.do_s, main)
+        self._move_do_late(do, main, side)
         tick("gather_do")
 
     def _per_head_sorts(self, q, k, v, do, R, main, side, tick):
@@ -252,8 +253,19 @@ class Step:
         lsh_sort_ids(self.ids, nb, Q_PAD, self.qh, self.pq, self.offq, self.ws_l, 0, main)
         if not self.gq:
             lsh_gather(q, self.pq, self.q_s, main)
-            lsh_gather(do, self.pq, self.do_s, main)
+        self._move_do_late(do, main, side)
         tick("hash_sort_q_do")
+
+    def _move_do_late(self, do, main, side):
+        """dO into sorted order on the second stream once the query sort is
+        done: only the backward reads it, so the move runs under the forward
+        (run() waits for it before the backward)."""
+        if self.gq:
+            return
+        self.ev[3].record(main)
+        side.wait_event(self.ev[3])
+        lsh_gather(do, self.pq, self.do_s, side)
+        self.ev[4].record(side)
 
     def _size_lists(self, stream):
         """Count this batch's live tiles (reads one int back) and grow the
