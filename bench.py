@@ -137,7 +137,8 @@ def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0, til
                      gather_kv: bool = True) -> int:
     """Library kernels launched per step (the library's own launch sequence).
     gather_kv: the attention kernels read K and V rows through the key
-    permutation (the tile-aligned step's default), so neither is moved."""
+    permutation (the tile-aligned step's default at D = 64), so neither is
+    moved."""
     # header init with the tile stats of both sides, count, scans with the
     # work orders, fill (+ pair lists and their order at D = 128)
     tiles = 4 + (2 if D == 128 else 0)
@@ -146,7 +147,7 @@ def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0, til
         m = n_buckets // 2
         lsh = 2 if (D in (64, 128) and m % 8 == 0 and 8 <= m <= 256) else 1  # tensor-core pass + certified pass
         sort = (3 if T > 8192 else 1) + (2 if tiled else 0)  # chunk counts, scan, scatter; bucket starts, spread
-        moves = 2 if (tiled and gather_kv) else 4  # Q, dO (and K, V) into sorted order
+        moves = 2 if (tiled and gather_kv and D == 64) else 4  # Q, dO (and K, V) into sorted order
         return tiles + attn + 2 * (lsh + sort) + moves  # per q / k: hash, sort
     return tiles + attn
 

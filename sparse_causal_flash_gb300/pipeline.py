@@ -48,10 +48,11 @@ class Step:
         gather (hash mode): "q" (q and dO), "kv" (k and v), True (all four)
         or False: no sorted copies of those tensors; the attention kernels
         read their rows through the sort's permutations (SCFA_FLAG_GATHER_Q,
-        SCFA_FLAG_GATHER_KV). The default, None, is "kv" on the tile-aligned
-        layout (the fastest on GB300: the backward's query-tile ring waits on
-        gathered rows, its resident key tile does not) and False on the plain
-        one.
+        SCFA_FLAG_GATHER_KV). The default, None, is "kv" at D = 64 on the
+        tile-aligned layout (the fastest there on GB300: the backward's
+        query-tile ring waits on gathered rows, its resident key tile does
+        not) and False otherwise (at D = 128 the two-tile forward is slower
+        with gathered key tiles).
         per_head_r (hash mode): one rotation per head, R [H, D, n_buckets // 2]
         (lsh_hash_heads); the ids are then sorted with lsh_sort_ids."""
         self.mode, self.B, self.H, self.Tq, self.Tk, self.D = mode, B, H, Tq, Tk, D
@@ -61,7 +62,7 @@ class Step:
         self.shared_qk = mode == MODE_HASH and bool(shared_qk)
         self.per_head_r = mode == MODE_HASH and bool(per_head_r)
         if gather is None:
-            gather = "kv" if self.tiled else False
+            gather = "kv" if (self.tiled and D == 64) else False
         g = "qkv" if gather is True else (gather or "")
         if g not in ("", "q", "kv", "qkv"):
             raise ValueError(f"gather must be False, True, 'q', 'kv' or 'qkv', not {gather!r}")
