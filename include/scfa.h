@@ -441,7 +441,10 @@ scfa_status scfa_get_device_status(const void* ws, void* stream);
  * - Every call shares the one array: calls that overlap on the GPU (e.g. on
  *   two unordered streams) race. Each call clears and rewrites all the
  *   scratch it reads.
- * - The device status word lives in the array and is not exposed.
+ * - The device status word lives in the array: scfa_qk_fwd_noalloc_status
+ *   synchronises `stream` and returns it (SCFA_OK, or the SCFA_ERR_* a
+ *   device-side check or a pipeline timeout of the last call raised), as
+ *   scfa_get_device_status does for a workspace.
  * ------------------------------------------------------------------------- */
 #define SCFA_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -449,6 +452,7 @@ scfa_status scfa_qk_fwd_noalloc(const uint16_t* q, const uint16_t* k, const uint
                                 const int32_t* q_idx, const int32_t* k_idx,
                                 int B, int H, int Tq, int Tk, int D, float scale,
                                 uint16_t* o, float* lse, void* stream);
+scfa_status scfa_qk_fwd_noalloc_status(void* stream);
 
 #ifdef __cplusplus
 }

@@ -57,3 +57,12 @@ extern "C" scfa_status scfa_qk_fwd_noalloc(const uint16_t* q, const uint16_t* k,
   return scfa_qk_fwd(q, k, v, q_idx, k_idx, B, H, Tq, Tk, D, scale, o, lse, ws, SCFA_NOALLOC_SCRATCH_BYTES, 0,
                      stream);
 }
+
+// The status word of the array (its first int, as in every workspace), after
+// the stream's work: SCFA_ERR_TIMEOUT, SCFA_ERR_WORKSPACE or SCFA_ERR_INVALID
+// raised on the device by the last call, or SCFA_OK.
+extern "C" scfa_status scfa_qk_fwd_noalloc_status(void* stream) {
+  void* ws = nullptr;
+  if (noalloc_scratch_address(&ws) != cudaSuccess) return SCFA_ERR_CUDA;
+  return scfa_get_device_status(ws, stream);
+}

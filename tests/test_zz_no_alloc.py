@@ -54,6 +54,12 @@ def test_noalloc_matches_workspace_entry_point(lib):
         lse = torch.full((B, H, Tq), float("nan"), dtype=torch.float32, device="cuda")
         rc = fn(_p(q), _p(k), _p(v), _p(qi), _p(ki), B, H, Tq, Tk, 64, p.wl.scale, _p(o), _p(lse), stream)
         assert rc == 0, scfa.status_string(rc)
+        # the device status word of the compiled-in scratch: the call's
+        # pipeline and list checks passed
+        st_fn = scfa._lib.scfa_qk_fwd_noalloc_status
+        st_fn.argtypes = [ctypes.c_void_p]
+        st_fn.restype = ctypes.c_int
+        assert st_fn(stream) == 0
         torch.cuda.synchronize()
         check_close("O noalloc", o, to_np(o_ref))
         check_lse("LSE noalloc", lse, to_np(lse_ref))
