@@ -46,13 +46,21 @@ namespace {
 
 constexpr int kSubBytes = kTile * 128;
 // Q / dO / query-metadata ring depth of attn_bwd_kernel (head dimension 64;
-// head dimension 128 runs attn_bwd128_kernel): three stages with one K / V
-// buffer, two with two K / V buffers (shared memory holds one or the other)
+// head dimension 128 runs attn_bwd128_kernel), with one or two K / V buffers
 template <int D, int KVB>
 constexpr int bwd_qstages() {
   static_assert(D == 64, "attn_bwd_kernel is built for head dimension 64");
   static_assert(KVB == 1 || KVB == 2, "one or two K / V buffers");
-  return KVB == 1 ? 3 : 2;
+  return 3;
+}
+// dS^T buffers: two with one K / V buffer; with two K / V buffers shared
+// memory holds one, and the compute warps write dS^T(t) once the MMAs of
+// tile t - 1 have read it (mostly done by the time tile t's math ends).
+// Measured: the long QK columns need the second dS^T buffer, hash mode's
+// short ones the second K / V buffer and the third query stage.
+template <int KVB>
+constexpr int bwd_dsbufs() {
+  return KVB == 1 ? 2 : 1;
 }
 constexpr int kBwdThreads = 448;
 
@@ -63,11 +71,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D, int KVB>
 struct __align__(1024) BwdSmem {
   static constexpr int kQStages = bwd_qstages<D, KVB>();
+  static constexpr int kDsBufs = bwd_dsbufs<KVB>();
   uint8_t k[KVB][D / 64][kSubBytes];  // K / V of work item n in buffer n % KVB
   uint8_t v[KVB][D / 64][kSubBytes];
   uint8_t q[kQStages][D / 64][kSubBytes];
   uint8_t dO[kQStages][D / 64][kSubBytes];
-  uint8_t dst[2][2][kSubBytes];   // dS^T [buffer][query half][128 keys x 64 queries]
+  uint8_t dst[kDsBufs][2][kSubBytes];   // dS^T [buffer][query half][128 keys x 64 queries]
   uint8_t dqs[kSubBytes];         // dQ fp32 staging: one [128 rows x 32 floats] swizzled half at a time
   alignas(16) int32_t qidx[kQStages][kTile];
   alignas(16) int32_t qhash[kQStages][kTile];
@@ -75,7 +84,7 @@ struct __align__(1024) BwdSmem {
   alignas(16) float drs[kQStages][kTile];     // -rowsum(dO * O) * scale
   uint64_t kv_full[KVB], kv_empty[KVB];
   uint64_t q_full[kQStages], q_empty[kQStages];
-  uint64_t s_full, st_empty, ds_full, pt_free, ds_free[2], dq_full, dq_empty, dkv_full, dkv_empty, drain;
+  uint64_t s_full, st_empty, ds_full, pt_free, ds_free[kDsBufs], dq_full, dq_empty, dkv_full, dkv_empty, drain;
   uint64_t dq_sync;  // the 128 threads of the dQ warpgroup around the staging tile
   int32_t items[kBwdSlots];
   uint64_t item_full[kBwdSlots], item_empty[kBwdSlots];
@@ -131,6 +140,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   BwdSmem<D, KVB>& sm = *reinterpret_cast<BwdSmem<D, KVB>*>(smem_raw + pad);
   constexpr int kQStages = BwdSmem<D, KVB>::kQStages;
+  constexpr int kDsBufs = BwdSmem<D, KVB>::kDsBufs;
   constexpr int kHalves = D / 64;  // a work item = (key tile, 64-column half of D)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // live-tile lists where the call that built them put them
@@ -147,7 +157,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(&sm.ds_free[s], 1);
+    for (int s = 0; s < kDsBufs; ++s) mbar_init(&sm.ds_free[s], 1);
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.st_empty, 256);
     mbar_init(&sm.ds_full, 256);
@@ -338,7 +348,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!issue_a(q_it, it)) break;
         for (int t = 0; t < n; ++t) {
           const int s = q_it % kQStages;
-          const int db = it & 1;
+          const int db = kDsBufs == 1 ? 0 : (it & 1);
           // A(t+1) before B(t) when it can go early: the compute warps free
           // the S^T / dP^T columns (st_empty) early in their step, long
           // before dS^T(t) is ready (ds_full), so wait for that first (the
@@ -438,7 +448,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int t = 0; t < n; ++t) {
         const bool full = (cflags[start + t] & kFlagFull) != 0;
         const int s = q_it % kQStages;
-        const int db = it & 1;
+        const int db = kDsBufs == 1 ? 0 : (it & 1);
         ok = mbar_wait(&sm.q_full[s], (q_it / kQStages) & 1, abort_flag, p.status) &&
              mbar_wait(&sm.s_full, it & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -516,9 +526,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           mbar_arrive(&sm.st_empty);  // S^T / dP^T may now be overwritten by the next A
           chunk(1, sr, dr, pk[1], dsk[1]);
         }
-        // the previous dV MMA must have read P^T, the MMAs two tiles back dS^T[db]
+        // the previous dV MMA must have read P^T, the MMAs kDsBufs tiles back dS^T[db]
         ok = mbar_wait(&sm.pt_free, (it & 1) ^ 1, abort_flag, p.status) &&
-             mbar_wait(&sm.ds_free[db], ((it >> 1) & 1) ^ 1, abort_flag, p.status);
+             mbar_wait(&sm.ds_free[db], (kDsBufs == 1 ? (it & 1) : ((it >> 1) & 1)) ^ 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         uint8_t* dsh = sm.dst[db][grp];
@@ -1362,8 +1372,8 @@ static cudaError_t launch_bwd_d(const AttnArgs& a, cudaStream_t st) {
     record_kernel_event(1, false, st);
   } else {
     // hash mode: about three query tiles per key tile, so a second K / V
-    // buffer (loaded while the previous item runs) is worth a Q / dO stage;
-    // the long columns of the other modes keep the deeper query ring
+    // buffer (loaded while the previous item runs) is worth the second dS^T
+    // buffer; the long columns of the other modes keep that one
     static_assert(sizeof(BwdSmem<D, 2>) + 1024 <= 227 * 1024 && sizeof(BwdSmem<D, 1>) + 1024 <= 227 * 1024,
                   "shared memory per CTA");
     const bool two_kv = a.mode == SCFA_MODE_HASH;
