@@ -720,7 +720,7 @@ def test_full_qk_8k_sampled_heads(scfa):
                         st.ws_b) == want
 
 
-@pytest.mark.parametrize("tiled,gather", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("tiled,gather", [(False, False), (True, False), (True, True), (True, "kv")])
 def test_full_hash_8k_sampled_heads(scfa, tiled, gather):
     wl = synth.WORKLOADS["hash_b4h12_t8192_d64_nb16"]
     p = synth.make_problem(wl)
@@ -740,7 +740,7 @@ def test_full_hash_8k_sampled_heads(scfa, tiled, gather):
     assert device_count(scfa, scfa.MODE_HASH, st.pq, st.pk, st.qh, st.kh, wl.B, wl.H, st.Ts, st.Ts, st.ws_b) == want
 
 
-@pytest.mark.parametrize("tiled,gather", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("tiled,gather", [(False, False), (True, False), (True, True), (True, "kv")])
 def test_full_hash_16k_sampled_heads(scfa, tiled, gather):
     """Hash-sparse B2 H12 T16384 D64 with 32 buckets, in the bench's launch
     configuration: bucket ids and sorted views of every head bit-exact, and
