@@ -560,12 +560,12 @@ __global__ void __launch_bounds__(kFixWarps * 32, 2) lsh_fix_kernel(const uint16
 // D additions each losing 2^-23 of a partial sum at D = 128, 8x at D = 64);
 // every other row, and every row with a subnormal, non-finite or huge value,
 // is left at -1 for the certified second pass (lsh_fix_kernel).
-// Roles (320 threads): warp 0 TMA producer (x tiles, 4 stages), warp 1 MMA
-// issuer and TMEM owner (two accumulators of m_pad columns), warps 2-5 and
-// 6-9 epilogue for even / odd tiles (thread = row = TMEM lane). R sits in shared memory for the whole
-// kernel as the MN-major B operand ([D][64]-column swizzled sub-tiles).
+// Roles: warp 0 TMA producer (x tiles, 4 stages), warp 1 MMA issuer and
+// TMEM owner (one accumulator of m_pad columns per epilogue warpgroup), then
+// two or four epilogue warpgroups taking the tiles in turn (thread = row =
+// TMEM lane). R sits in shared memory for the whole kernel as the MN-major B
+// operand ([D][64]-column swizzled sub-tiles).
 // ---------------------------------------------------------------------------
-constexpr int kTcThreads = 320;  // producer, MMA, two epilogue warpgroups (alternate tiles)
 constexpr int kTcStages = 4;
 constexpr float kTcRel = 0x1p-14f;
 
@@ -574,15 +574,17 @@ struct __align__(1024) LshTcSmem {
   uint8_t x[kTcStages][D / 64][kTile * 128];  // [stage][64-column sub-tile][128 rows x 128 B]
   uint8_t r[4][D * 128];                      // up to 4 sub-tiles of [D rows][64 columns]
   uint64_t x_full[kTcStages], x_empty[kTcStages];
-  uint64_t acc_full[2], acc_empty[2], drain;
+  uint64_t acc_full[4], acc_empty[4], drain;  // one accumulator per epilogue warpgroup
   uint32_t tmem_base;
   int abort_flag;
   int r_bad;  // R holds a subnormal or non-finite value: every row goes to the second pass
   float rnmax;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// G epilogue warpgroups take the tiles in turn, each with its own TMEM
+// accumulator: four when four accumulators fit in TMEM (m <= 128), else two.
+template <int D, int G>
+__global__ void __launch_bounds__(64 + 128 * G, 1)
 lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __restrict__ R, LshSegs sg,
                    int m, int m_pad, int32_t* __restrict__ hash, int* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -594,14 +596,15 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
   const int hd = blockIdx.y;
   R += hd * sg.r_stride;
   const uint32_t acc_cols = m_pad < 32 ? 32u : static_cast<uint32_t>(m_pad);
-  const uint32_t tmem_cols = acc_cols * 2 <= 32 ? 32u : (acc_cols * 2 <= 64 ? 64u : (acc_cols * 2 <= 128 ? 128u : (acc_cols * 2 <= 256 ? 256u : 512u)));
+  const uint32_t need = acc_cols * G;
+  const uint32_t tmem_cols = need <= 32 ? 32u : (need <= 64 ? 64u : (need <= 128 ? 128u : (need <= 256 ? 256u : 512u)));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&sm.x_full[s], 1);
       mbar_init(&sm.x_empty[s], 1 + 128);  // the MMA commit and the 128 epilogue threads (row norms)
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < G; ++b) {
       mbar_init(&sm.acc_full[b], 1);
       mbar_init(&sm.acc_empty[b], 128);
     }
@@ -687,8 +690,8 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
       constexpr uint32_t kStage16 = (D / 64) * kTile * 128 >> 4;
       int it = 0;
       for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
-        const int s = it % kTcStages, b = it & 1;
-        if (!mbar_wait(&sm.acc_empty[b], ((it >> 1) & 1) ^ 1, abort_flag, status)) break;
+        const int s = it % kTcStages, b = it % G;
+        if (!mbar_wait(&sm.acc_empty[b], ((it / G) & 1) ^ 1, abort_flag, status)) break;
         if (!mbar_wait(&sm.x_full[s], (it / kTcStages) & 1, abort_flag, status)) break;
         tc_fence_after();
         const uint64_t a = xdesc + static_cast<uint64_t>(s * kStage16);
@@ -705,16 +708,16 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
-    const int eg = (warp - 2) >> 2;      // epilogue warpgroup: tiles it with it % 2 == eg
+    const int eg = (warp - 2) >> 2;      // epilogue warpgroup: tiles it with it % G == eg
     const int rr = quarter * 32 + lane;  // row of the tile = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float rnmax = sm.rnmax;
     const bool r_bad = sm.r_bad != 0;
     int it = eg;
     for (long long t = blockIdx.x + static_cast<long long>(eg) * gridDim.x; t < n_tiles;
-         t += 2ll * gridDim.x, it += 2) {
-      const int s = it % kTcStages, b = it & 1;
-      bool ok = mbar_wait(&sm.acc_full[b], (it >> 1) & 1, abort_flag, status);
+         t += static_cast<long long>(G) * gridDim.x, it += G) {
+      const int s = it % kTcStages, b = it % G;
+      bool ok = mbar_wait(&sm.acc_full[b], (it / G) & 1, abort_flag, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       // ||x||_2 of this row from the staged tile (rounded up), and a check
@@ -978,16 +981,19 @@ static cudaError_t launch_lsh_tc(const uint16_t* x, const uint16_t* R, long long
   if (!make_tmap_bf16_3d(&tm, x, D, rows, 1)) return cudaErrorInvalidValue;
   const int m_pad = (m + 15) / 16 * 16;
   const size_t smem = sizeof(LshTcSmem<D>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(lsh_hash_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  // four epilogue warpgroups when four accumulators fit in TMEM
+  const int acc_cols = m_pad < 32 ? 32 : m_pad;
+  const bool four = acc_cols * 4 <= 512;
+  auto kern = four ? lsh_hash_tc_kernel<D, 4> : lsh_hash_tc_kernel<D, 2>;
+  const int threads = 64 + 128 * (four ? 4 : 2);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // about one CTA per SM in all, split over the rotations
   const long long n_tiles = seg_units(sg, kTile);
   long long g = num_sms() / sg.n_heads;
   if (g > n_tiles) g = n_tiles;
   if (g < 1) g = 1;
-  lsh_hash_tc_kernel<D><<<dim3(static_cast<unsigned>(g), sg.n_heads), kTcThreads, smem, st>>>(tm, R, sg, m, m_pad,
-                                                                                            hash, status);
+  kern<<<dim3(static_cast<unsigned>(g), sg.n_heads), threads, smem, st>>>(tm, R, sg, m, m_pad, hash, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // certified second pass over the rows the first pass left at -1
