@@ -426,8 +426,18 @@ __global__ void __launch_bounds__(kFixWarps * 32, 2) lsh_fix_kernel(const uint16
     __syncthreads();  // the previous segment's list is consumed
     if (threadIdx.x == 0) s_n = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < nseg; i += blockDim.x)
-      if (hash[seg + i] < 0) s_list[atomicAdd(&s_n, 1)] = i;
+    // all eight ids of this thread are loaded before any is tested (one
+    // memory latency, not eight)
+    constexpr int kPer = kFixSeg / (kFixWarps * 32);
+    int hv[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = threadIdx.x + j * kFixWarps * 32;
+      hv[j] = i < nseg ? hash[seg + i] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (hv[j] < 0) s_list[atomicAdd(&s_n, 1)] = threadIdx.x + j * kFixWarps * 32;
     __syncthreads();
     const int n_flag = s_n;
     for (int li = warp; li < n_flag; li += kFixWarps) {
