@@ -836,13 +836,25 @@ __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int 
   const int per = ((len + nw - 1) / nw + 31) / 32 * 32;
   const int b0 = c_begin + min(len, w * per), b1 = c_begin + min(len, w * per + per);
   int32_t* my = hist + w * nb;
-  for (int base = b0; base < b1; base += 32) {
-    const int i = base + lane;
-    int h = i < b1 ? hrow[i] : -1;
-    if (h >= nb) h = -1;  // an id outside [0, nb) takes no slot (the id check reports it)
-    const unsigned peers = __match_any_sync(0xffffffffu, h);
-    if (h >= 0 && (peers & ((1u << lane) - 1u)) == 0) my[h] += __popc(peers);
-    __syncwarp();
+  // the slice in steps of 32 ids, eight steps' ids loaded at once (one
+  // memory latency per eight steps); an id outside [0, nb) takes no slot
+  // (the id check reports it)
+  constexpr int kSteps = 8;
+  for (int base0 = b0; base0 < b1; base0 += 32 * kSteps) {
+    int hv[kSteps];
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+      const int i = base0 + u * 32 + lane;
+      const int h = i < b1 ? hrow[i] : -1;
+      hv[u] = h >= nb ? -1 : h;
+    }
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+      const int h = hv[u];
+      const unsigned peers = __match_any_sync(0xffffffffu, h);
+      if (h >= 0 && (peers & ((1u << lane) - 1u)) == 0) my[h] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
   // per bucket: exclusive prefix over warps; totals
@@ -887,20 +899,29 @@ __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int 
     for (int ww = 0; ww < nw; ++ww) hist[ww * nb + c] += base;
   }
   __syncthreads();
-  for (int base = b0; base < b1; base += 32) {
-    const int i = base + lane;
-    int h = i < b1 ? hrow[i] : -1;
-    if (h >= nb) h = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, h);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    const int start = h >= 0 ? my[h] : 0;
-    __syncwarp();
-    if (h >= 0) {
-      prow[start + rank] = i;
-      srow[start + rank] = h;
-      if (rank == 0) my[h] = start + __popc(peers);
+  for (int base0 = b0; base0 < b1; base0 += 32 * kSteps) {
+    int hv[kSteps];
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+      const int i = base0 + u * 32 + lane;
+      const int h = i < b1 ? hrow[i] : -1;
+      hv[u] = h >= nb ? -1 : h;
     }
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+      const int i = base0 + u * 32 + lane;
+      const int h = hv[u];
+      const unsigned peers = __match_any_sync(0xffffffffu, h);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int start = h >= 0 ? my[h] : 0;
+      __syncwarp();
+      if (h >= 0) {
+        prow[start + rank] = i;
+        srow[start + rank] = h;
+        if (rank == 0) my[h] = start + __popc(peers);
+      }
+      __syncwarp();
+    }
   }
 }
 
