@@ -455,6 +455,21 @@ int scfa_tiled_rows(int T, int n_buckets) {
   return rows > INT_MAX ? -1 : static_cast<int>(rows);
 }
 
+// The tile-aligned layout straight from the sort kernel, or from the plain
+// sort plus the layout pass: the former needs heads of one CTA and room for
+// three shared histograms' worth of buckets.
+static cudaError_t sort_tiled(const int32_t* hash, int BH, int T, int nb, int T_sorted, int32_t pad, int32_t* perm,
+                              int32_t* hash_sorted, int32_t* bucket_start, char* w, const LshWs& L, cudaStream_t st) {
+  if (T <= kSortChunk && static_cast<size_t>(nb) * 3 * sizeof(int32_t) <= 160 * 1024)
+    return launch_bucket_sort(hash, BH, T, nb, perm, hash_sorted, bucket_start, nullptr, st, T_sorted, pad);
+  int32_t* perm_u = reinterpret_cast<int32_t*>(w + L.perm_u);
+  int32_t* off_u = reinterpret_cast<int32_t*>(w + L.off_u);
+  cudaError_t e = launch_bucket_sort(hash, BH, T, nb, perm_u, reinterpret_cast<int32_t*>(w + L.hs_u), off_u,
+                                     reinterpret_cast<int32_t*>(w + L.chunk), st);
+  if (e == cudaSuccess) e = launch_tiled_layout(perm_u, off_u, BH, T, T_sorted, nb, pad, perm, hash_sorted, bucket_start, st);
+  return e;
+}
+
 scfa_status lsh_bucket_sort_tiled(const uint16_t* x, const uint16_t* R, int B, int H, int T, int D, int n_buckets,
                                   int T_sorted, int32_t pad, int32_t* hash_sorted, int32_t* perm,
                                   int32_t* bucket_start, uint16_t* x_sorted, void* ws, size_t ws_bytes,
@@ -474,15 +489,10 @@ scfa_status lsh_bucket_sort_tiled(const uint16_t* x, const uint16_t* R, int B, i
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   int32_t* hash = reinterpret_cast<int32_t*>(w + L.hash);
-  int32_t* perm_u = reinterpret_cast<int32_t*>(w + L.perm_u);
-  int32_t* off_u = reinterpret_cast<int32_t*>(w + L.off_u);
   const long long rows = static_cast<long long>(B) * H * T;
   cudaError_t e = launch_lsh_hash(x, R, rows, D, n_buckets / 2, hash, reinterpret_cast<int*>(w + L.header), st);
   if (e == cudaSuccess)
-    e = launch_bucket_sort(hash, B * H, T, n_buckets, perm_u, reinterpret_cast<int32_t*>(w + L.hs_u), off_u,
-                           reinterpret_cast<int32_t*>(w + L.chunk), st);
-  if (e == cudaSuccess)
-    e = launch_tiled_layout(perm_u, off_u, B * H, T, T_sorted, n_buckets, pad, perm, hash_sorted, bucket_start, st);
+    e = sort_tiled(hash, B * H, T, n_buckets, T_sorted, pad, perm, hash_sorted, bucket_start, w, L, st);
   if (e == cudaSuccess && x_sorted) e = launch_gather(x, perm, B * H, T_sorted, T, D, x_sorted, false, st);
   return finish(e, flags, st);
 }
@@ -508,14 +518,8 @@ scfa_status lsh_sort_ids(const int32_t* hash, int B, int H, int T, int n_buckets
   int32_t* chunk = reinterpret_cast<int32_t*>(w + L.chunk);
   if (e == cudaSuccess && !tiled) e = launch_bucket_sort(hash, B * H, T, n_buckets, perm, hash_sorted, bucket_start,
                                                          chunk, st);
-  if (e == cudaSuccess && tiled) {
-    int32_t* perm_u = reinterpret_cast<int32_t*>(w + L.perm_u);
-    int32_t* off_u = reinterpret_cast<int32_t*>(w + L.off_u);
-    e = launch_bucket_sort(hash, B * H, T, n_buckets, perm_u, reinterpret_cast<int32_t*>(w + L.hs_u), off_u, chunk,
-                           st);
-    if (e == cudaSuccess)
-      e = launch_tiled_layout(perm_u, off_u, B * H, T, T_sorted, n_buckets, pad, perm, hash_sorted, bucket_start, st);
-  }
+  if (e == cudaSuccess && tiled)
+    e = sort_tiled(hash, B * H, T, n_buckets, T_sorted, pad, perm, hash_sorted, bucket_start, w, L, st);
   return finish(e, flags, st);
 }
 

@@ -97,7 +97,7 @@ cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long
 // chunk_ws: the workspace's chunk array (used when T > kSortChunk)
 cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int n_buckets,
                                int32_t* perm, int32_t* hash_sorted, int32_t* bucket_off,
-                               int32_t* chunk_ws, cudaStream_t st);
+                               int32_t* chunk_ws, cudaStream_t st, int Ts = 0, int pad = 0);
 // Ts rows per head in the sorted tensor, To in the original-order one
 cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int BH, int Ts, int To, int D,
                           uint16_t* out, bool unsort, cudaStream_t st);

@@ -814,20 +814,30 @@ lsh_hash_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const uint16_t* __r
 // CTA per row, bucket_scan_kernel) turns them into the chunk's first output
 // position per bucket and writes bucket_off, mode 2 scatters from those
 // bases. Mode 0 is the whole row in one CTA.
+//
+// Ts > 0 (mode 0 only): the output is the tile-aligned layout directly (Ts
+// rows per head): bucket b's rows start at bucket_off[b] = the sum over c < b
+// of n_c rounded up to kTile, and the rows between a bucket's n_b rows and
+// its next tile boundary, and all rows after the last bucket's tiles, are
+// padding rows (position `pad`, bucket id b, nb - 1 after the last bucket).
 __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int nb,
                                    int32_t* __restrict__ perm, int32_t* __restrict__ hash_sorted,
                                    int32_t* __restrict__ bucket_off, int mode, int chunk, int n_chunks,
-                                   int32_t* __restrict__ chunk_ws) {
-  extern __shared__ int32_t hist[];  // [nwarps][nb], then [nb] totals
+                                   int32_t* __restrict__ chunk_ws, int Ts, int pad) {
+  extern __shared__ int32_t hist[];  // [nwarps][nb], then [nb] totals, then [nb] counts (tile-aligned)
+  __shared__ int s_end;              // tile-aligned: end of the last bucket's tiles
   const int nw = blockDim.x >> 5, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool tiled = mode == 0 && Ts > 0;
+  const int rs = tiled ? Ts : T;  // output rows per head
   const long long bh = mode == 0 ? blockIdx.x : blockIdx.x / n_chunks;
   const int ci = mode == 0 ? 0 : static_cast<int>(blockIdx.x % n_chunks);
   const int32_t* hrow = hash + bh * T;
-  int32_t* prow = perm + bh * T;
-  int32_t* srow = hash_sorted + bh * T;
+  int32_t* prow = perm + bh * rs;
+  int32_t* srow = hash_sorted + bh * rs;
   int32_t* orow = bucket_off + bh * (nb + 1);
   int32_t* cws = chunk_ws + (bh * n_chunks + ci) * nb;
   int32_t* tot = hist + nw * nb;
+  int32_t* cnt = tot + nb;
   for (int i = threadIdx.x; i < (nw + 1) * nb; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int c_begin = mode == 0 ? 0 : min(T, ci * chunk);
@@ -875,11 +885,13 @@ __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int 
   if (mode == 2) {
     for (int c = threadIdx.x; c < nb; c += blockDim.x) tot[c] = cws[c];
   } else if (w == 0) {
-    // exclusive scan of the totals over buckets (warp 0), written to bucket_off
+    // exclusive scan of the totals over buckets (warp 0), written to
+    // bucket_off; tile-aligned, of the totals rounded up to kTile
     int run = 0;
     for (int base = 0; base < nb; base += 32) {
       const int c = base + lane;
-      const int v = c < nb ? tot[c] : 0;
+      const int n_c = c < nb ? tot[c] : 0;
+      const int v = tiled ? (n_c + kTile - 1) / kTile * kTile : n_c;
       int x = v;
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -888,10 +900,14 @@ __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int 
       if (c < nb) {
         tot[c] = run + x - v;
         orow[c] = run + x - v;
+        if (tiled) cnt[c] = n_c;
       }
       run += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (lane == 0) orow[nb] = run;
+    if (lane == 0) {
+      orow[nb] = run;
+      s_end = run;
+    }
   }
   __syncthreads();
   for (int c = threadIdx.x; c < nb; c += blockDim.x) {
@@ -921,6 +937,20 @@ __global__ void bucket_sort_kernel(const int32_t* __restrict__ hash, int T, int 
         if (rank == 0) my[h] = start + __popc(peers);
       }
       __syncwarp();
+    }
+  }
+  if (tiled) {
+    // padding rows: the rest of each bucket's last tile, then the tail
+    for (int c = w; c < nb; c += nw) {
+      const int a = tot[c] + cnt[c], e = tot[c] + (cnt[c] + kTile - 1) / kTile * kTile;
+      for (int p = a + lane; p < e; p += 32) {
+        prow[p] = pad;
+        srow[p] = c;
+      }
+    }
+    for (int p = s_end + threadIdx.x; p < Ts; p += blockDim.x) {
+      prow[p] = pad;
+      srow[p] = nb - 1;
     }
   }
 }
@@ -1081,30 +1111,39 @@ cudaError_t launch_lsh_hash_cuda(const uint16_t* x, const uint16_t* R, long long
 
 cudaError_t launch_bucket_sort(const int32_t* hash, int BH, int T, int nb,
                                int32_t* perm, int32_t* hash_sorted, int32_t* bucket_off, int32_t* chunk_ws,
-                               cudaStream_t st) {
+                               cudaStream_t st, int Ts, int pad) {
+  // per-warp histograms, the totals and (tile-aligned) the counts
+  const int extra = Ts > 0 ? 2 : 1;
   const size_t budget = 160 * 1024;
-  int nw = static_cast<int>(budget / (static_cast<size_t>(nb) * sizeof(int32_t))) - 1;
+  int nw = static_cast<int>(budget / (static_cast<size_t>(nb) * sizeof(int32_t))) - extra;
   if (nw > 32) nw = 32;
   if (nw < 1) nw = 1;
-  const size_t smem = static_cast<size_t>(nw + 1) * nb * sizeof(int32_t);
+  const size_t smem = static_cast<size_t>(nw + extra) * nb * sizeof(int32_t);
   cudaError_t e = cudaFuncSetAttribute(bucket_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  if (Ts > 0) {
+    // the tile-aligned layout straight from the sort: heads of one CTA only
+    if (T > kSortChunk) return cudaErrorInvalidValue;
+    bucket_sort_kernel<<<BH, nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off, 0, T, 1, nullptr, Ts,
+                                                  pad);
+    return cudaGetLastError();
+  }
   if (T <= kSortChunk || chunk_ws == nullptr) {
-    bucket_sort_kernel<<<BH, nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off, 0, T, 1, nullptr);
+    bucket_sort_kernel<<<BH, nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off, 0, T, 1, nullptr, 0, 0);
     return cudaGetLastError();
   }
   const int n_chunks = (T + kSortChunk - 1) / kSortChunk;
   const long long g = static_cast<long long>(BH) * n_chunks;
   bucket_sort_kernel<<<static_cast<int>(g), nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off, 1,
-                                                                  kSortChunk, n_chunks, chunk_ws);
+                                                                  kSortChunk, n_chunks, chunk_ws, 0, 0);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   bucket_scan_kernel<<<BH, 256, static_cast<size_t>(nb) * sizeof(int32_t), st>>>(nb, n_chunks, chunk_ws, bucket_off);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   bucket_sort_kernel<<<static_cast<int>(g), nw * 32, smem, st>>>(hash, T, nb, perm, hash_sorted, bucket_off, 2,
-                                                                  kSortChunk, n_chunks, chunk_ws);
+                                                                  kSortChunk, n_chunks, chunk_ws, 0, 0);
   return cudaGetLastError();
 }
 
