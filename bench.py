@@ -147,8 +147,8 @@ def kernels_per_step(mode: str, D: int = 64, T: int = 0, n_buckets: int = 0, til
         m = n_buckets // 2
         lsh = 2 if (D in (64, 128) and m % 8 == 0 and 8 <= m <= 256) else 1  # tensor-core pass + certified pass
         # chunk counts, scan, scatter; bucket starts and spread (heads of up
-        # to 8,192 rows get the tile-aligned layout from the sort itself)
-        sort = (3 if T > 8192 else 1) + (2 if (tiled and T > 8192) else 0)
+        # to 16,384 rows get the tile-aligned layout from the sort itself)
+        sort = (3 if T > 16384 else 1) + (2 if (tiled and T > 16384) else 0)
         moves = 2 if (tiled and gather_kv and D == 64) else 4  # Q, dO (and K, V) into sorted order
         return tiles + attn + 2 * (lsh + sort) + moves  # per q / k: hash, sort
     return tiles + attn

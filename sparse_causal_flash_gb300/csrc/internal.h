@@ -62,7 +62,7 @@ struct LshWs {
   size_t off_u = 0;             // int32 [B,H,n_buckets+1]
   size_t total = 0;
 };
-constexpr int kSortChunk = 8192;  // rows longer than this are sorted by several CTAs
+constexpr int kSortChunk = 16384;  // rows longer than this are sorted by several CTAs
 bool lsh_ws_layout(int B, int H, int T, int n_buckets, LshWs* L);
 
 int num_sms();
