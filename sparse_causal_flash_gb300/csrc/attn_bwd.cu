@@ -87,6 +87,7 @@ struct __align__(1024) BwdSmem {
   uint64_t s_full, st_empty, ds_full, pt_free, ds_free[kDsBufs], dq_full, dq_empty, dkv_full, dkv_empty, drain;
   uint64_t dq_sync;  // the 128 threads of the dQ warpgroup around the staging tile
   int32_t items[kBwdSlots];
+  int4 imeta[kBwdSlots];  // two K/V buffers (hash mode): the item's {key tile, first CSC entry, count}
   uint64_t item_full[kBwdSlots], item_empty[kBwdSlots];
   uint32_t tmem_base;
   int abort_flag;
@@ -200,6 +201,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (mbar_wait(&sm.item_empty[slot], ((slot_it / kBwdSlots) & 1) ^ 1, abort_flag, p.status)) {
           w = atomicAdd(&p.sched[0], 1);
           sm.items[slot] = w < p.n_work ? w : -1;
+          if constexpr (KVB == 2) {
+            // short hash-mode items: the other roles take the item's key
+            // tile and CSC range from the slot instead of loading them
+            if (w < p.n_work) {
+              const int gg = p.work[w / kHalves];
+              const int s0 = p.csc_ptr[gg];
+              sm.imeta[slot] = make_int4(gg, s0, p.csc_ptr[gg + 1] - s0, 0);
+            }
+          }
           mbar_arrive(&sm.item_full[slot]);
         }
       }
@@ -334,11 +344,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int slot = slot_it % kBwdSlots;
         if (!mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status)) break;
         const int w = sm.items[slot];
+        int4 im = make_int4(0, 0, 0, 0);
+        if constexpr (KVB == 2) im = sm.imeta[slot];
         mbar_arrive(&sm.item_empty[slot]);
         if (w < 0) break;
-        const int g = p.work[w / kHalves];
         const int hh = w % kHalves;
-        const int n = p.csc_ptr[g + 1] - p.csc_ptr[g];
+        int n;
+        if constexpr (KVB == 2) {
+          n = im.z;
+        } else {
+          const int g = p.work[w / kHalves];
+          n = p.csc_ptr[g + 1] - p.csc_ptr[g];
+        }
         if (n == 0) continue;
         const int kb = item % KVB;
         if (!mbar_wait(&sm.kv_full[kb], (item / KVB) & 1, abort_flag, p.status)) break;
@@ -421,11 +438,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const bool got = mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, got)) break;
       const int w = sm.items[slot];
+      int4 im = make_int4(0, 0, 0, 0);
+      if constexpr (KVB == 2) im = sm.imeta[slot];
       mbar_arrive(&sm.item_empty[slot]);
       if (w < 0) break;
-      const int g = p.work[w / kHalves];
+      int g, start, n;
+      if constexpr (KVB == 2) {
+        g = im.x;
+        start = im.y;
+        n = im.z;
+      } else {
+        g = p.work[w / kHalves];
+        start = p.csc_ptr[g];
+        n = p.csc_ptr[g + 1] - start;
+      }
       const int hh = w % kHalves;  // which 64-column half of D
-      const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
       const int bh = g / p.nKt, j = g % p.nKt;
       const int key = j * kTile + kr;
       const bool kvalid = key < p.Tk;
@@ -586,11 +613,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const bool got = mbar_wait(&sm.item_full[slot], (slot_it / kBwdSlots) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, got)) break;
       const int w = sm.items[slot];
+      int4 im = make_int4(0, 0, 0, 0);
+      if constexpr (KVB == 2) im = sm.imeta[slot];
       mbar_arrive(&sm.item_empty[slot]);
       if (w < 0) break;
-      const int g = p.work[w / kHalves];
+      int g, start, n;
+      if constexpr (KVB == 2) {
+        g = im.x;
+        start = im.y;
+        n = im.z;
+      } else {
+        g = p.work[w / kHalves];
+        start = p.csc_ptr[g];
+        n = p.csc_ptr[g + 1] - start;
+      }
       const int hh = w % kHalves;  // which 64-column half of D
-      const int start = p.csc_ptr[g], n = p.csc_ptr[g + 1] - start;
       if (n == 0) continue;
       const int bh = g / p.nKt;
       bool ok = true;
