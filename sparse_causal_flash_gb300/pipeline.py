@@ -1,9 +1,12 @@
 """One fwd+bwd step of each SCFA mode, composed from C-ABI calls.
 
 Call order only (no arithmetic): the hash-sparse step hashes and
-bucket-sorts queries and keys, gathers V and dO into sorted order, and runs
-the sparse attention forward and backward on the sorted rows, whose kernels
-write O, dQ, dK and dV straight back to original row order
+bucket-sorts queries and keys, moves into sorted order the rows of q, k, v
+and dO that the attention kernels do not gather themselves through the
+permutations (by default at head dimension 64: q and dO are moved, k and v
+are gathered in the kernels), and runs the sparse attention forward and
+backward in sorted order, whose kernels write O, dQ, dK and dV straight back
+to original row order
 (SCFA_FLAG_ORIGINAL_ORDER; "Faster Causal Attention Over Large Sequences
 Through Sparse Flash Attention", deep-paper.org, sections
 "动态稀疏性为何会破坏它" and "SCFA 解决方案" part 2). LSE stays in sorted query
