@@ -6,6 +6,8 @@ within max abs 2e-2 and relative L2 5e-3; LSE within 2e-3 (and -inf exactly).
 Sizes span several 128-row tiles with ragged tails; the full-size workloads
 are checked on sampled heads.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -688,6 +690,41 @@ def test_empty_rows_output_zero(scfa):
     assert torch.all(st.dq[0, 0, :150] == 0)
     ref = pipelines.run_qk(q, k, v, do, q_idx.numpy(), k_idx.numpy(), p.wl.scale)
     compare_heads(st, ref, ref.keys())
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_query_tiles_without_live_key_tile(scfa, D):
+    """Whole query tiles that see no key (every position before the first
+    key's) have no backward work item: their dQ rows are written as zero all
+    the same, like O = 0 and LSE = -inf. Outputs start as NaN and the call
+    goes straight through the C-ABI; a ragged last tile and a second head
+    whose every tile is live ride along."""
+    B, H, Tq, Tk = 1, 2, 300, 333
+    q_idx = torch.arange(Tq, dtype=torch.int32).repeat(B, H, 1).contiguous()
+    k_idx = torch.arange(Tk, dtype=torch.int32).repeat(B, H, 1).contiguous()
+    k_idx[0, 0] += 260  # head 0: queries 0..259 (query tiles 0 and 1) see no key
+    q = synth.normal_bf16(5, 1, (B, H, Tq, D))
+    k = synth.normal_bf16(5, 2, (B, H, Tk, D))
+    v = synth.normal_bf16(5, 3, (B, H, Tk, D))
+    do = synth.normal_bf16(5, 4, (B, H, Tq, D))
+    scale = 1.0 / math.sqrt(D)
+    nan = lambda t: torch.full(t, float("nan"), dtype=torch.bfloat16, device="cuda")
+    o, dq, dk, dv = nan((B, H, Tq, D)), nan((B, H, Tq, D)), nan((B, H, Tk, D)), nan((B, H, Tk, D))
+    lse = torch.empty((B, H, Tq), dtype=torch.float32, device="cuda")
+    ws = scfa.workspace(scfa.attn_workspace_size(scfa.MODE_QK, 1, B, H, Tq, Tk, D))
+    g = [t.cuda() for t in (q, k, v, do, q_idx, k_idx)]
+    scfa.scfa_qk_fwd(g[0], g[1], g[2], g[4], g[5], scale, o, lse, ws)
+    scfa.scfa_qk_bwd(g[0], g[1], g[2], o, lse, g[3], g[4], g[5], scale, dq, dk, dv, ws, scfa.FLAG_REUSE_TILES)
+    torch.cuda.synchronize()
+    assert scfa.scfa_get_device_status(ws) == 0
+    assert torch.all(o[0, 0, :260] == 0) and torch.all(torch.isneginf(lse[0, 0, :260]))
+    assert torch.all(dq[0, 0, :260] == 0)
+    ref = pipelines.run_qk(q, k, v, do, q_idx.numpy(), k_idx.numpy(), scale)
+    f = lambda t: t.cpu().double().numpy()
+    for (b, h), r in ref.items():
+        check_lse(f"LSE[{h}]", lse[b, h], r["lse"])
+        for key, got in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+            check_close(f"{key}[{h}]", got[b, h], r[key])
 
 
 def test_sentinel_padded_heads(scfa):
