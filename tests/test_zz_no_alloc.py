@@ -5,8 +5,9 @@ It exists for callers that may not call cudaMalloc where they run attention
 allocation inside its callbacks): it takes no
 workspace and uses a scratch array compiled into the library. These tests call
 it through the C ABI and compare it with scfa_qk_fwd (caller workspace) on two
-calls in a row, and check that a shape too large for the array is refused on
-the host. Collected last on purpose.
+calls in a row, check that the second takes no device memory (free bytes
+unchanged around it), and check that a shape too large for the array is
+refused on the host. Collected last on purpose.
 """
 import ctypes
 
@@ -52,8 +53,15 @@ def test_noalloc_matches_workspace_entry_point(lib):
         scfa.scfa_qk_fwd(q, k, v, qi, ki, p.wl.scale, o_ref, lse_ref, ws)
         o = torch.full_like(q, float("nan"))
         lse = torch.full((B, H, Tq), float("nan"), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         rc = fn(_p(q), _p(k), _p(v), _p(qi), _p(ki), B, H, Tq, Tk, 64, p.wl.scale, _p(o), _p(lse), stream)
         assert rc == 0, scfa.status_string(rc)
+        torch.cuda.synchronize()
+        if seed == 52:
+            # after a first call (which may load kernel code lazily), a call
+            # takes no device memory
+            assert torch.cuda.mem_get_info()[0] == free0
         # the device status word of the compiled-in scratch: the call's
         # pipeline and list checks passed
         st_fn = scfa._lib.scfa_qk_fwd_noalloc_status
