@@ -386,18 +386,142 @@ __global__ void __launch_bounds__(kHashRows) lsh_hash_kernel(const uint16_t* __r
   }
 }
 
+// Certified bucket id of one row, computed by a whole warp (the id is
+// returned in every lane). xr: the row in global memory; sR: R as fp32
+// [D][m4] in shared memory with rnmax / r_emin / r_emax from lsh_prologue;
+// sx: D floats of shared memory for this warp. The lanes share the row,
+// screen the columns lane + 32 k in fp32 with the same bound as the
+// single-thread path (it holds for any summation order), and evaluate every
+// candidate within the threshold of the top exactly in 128-bit integers, one
+// candidate at a time split over the lanes; the largest value wins, the
+// smallest index on ties. A row whose exponent span needs more than 128 bits
+// goes to the single-thread path (576-bit accumulator) on lane 0.
+__device__ int fix_row_warp(const uint16_t* __restrict__ xr, const uint16_t* __restrict__ R, const float* sR,
+                            float* sx, int D, int m, float rnmax, int r_emin, int r_emax, int lane) {
+  const int m4 = (m + 3) & ~3;
+  const float rel = static_cast<float>(D + 1) * 0x1p-23f;
+  const float absb = static_cast<float>(D) * 0x1p-148f;
+  // stage the row; norm and exponent range of its nonzero entries
+  float l2sq = 0.f;
+  int xemin = INT_MAX, xemax = INT_MIN;
+  for (int d = lane; d < D; d += 32) {
+    const uint16_t bb = xr[d];
+    const float v = bf16_to_f32(bb);
+    sx[d] = v;
+    l2sq = fmaf(v, v, l2sq);
+    bool ng;
+    uint32_t M;
+    int E;
+    bf16_parts(bb, &ng, &M, &E);
+    if (M != 0) {
+      xemin = min(xemin, E);
+      xemax = max(xemax, E);
+    }
+  }
+  for (int o = 16; o; o >>= 1) {
+    l2sq += __shfl_xor_sync(0xffffffffu, l2sq, o);
+    xemin = min(xemin, __shfl_xor_sync(0xffffffffu, xemin, o));
+    xemax = max(xemax, __shfl_xor_sync(0xffffffffu, xemax, o));
+  }
+  __syncwarp();
+  const float l2 = sqrtf(l2sq * (1.f + static_cast<float>(D + 2) * 0x1p-22f) + static_cast<float>(D) * 0x1p-148f) *
+                   1.000001f;
+  const float emax = l2 * rnmax * rel * 1.000001f + absb;
+  const float thr = 2.f * emax * 1.0001f;
+  // fp32 values of this lane's columns c = lane + 32 k (m <= 256: k < 8),
+  // each summed over d in order; the warp's top value
+  float scv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) scv[k] = 0.f;
+#pragma unroll 4
+  for (int d = 0; d < D; ++d) {
+    const float xv = sx[d];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = lane + 32 * k;
+      if (c < m) scv[k] = fmaf(xv, sR[d * m4 + c], scv[k]);
+    }
+  }
+  float best_v = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (lane + 32 * k < m) best_v = fmaxf(best_v, fmaxf(scv[k], -scv[k]));
+  float t0 = best_v;
+  for (int o = 16; o; o >>= 1) t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
+  // exact values of the candidates (within thr of the top, or NaN)
+  const bool any_term = xemin != INT_MAX && r_emin != INT_MAX;
+  const int ebase = any_term ? xemin + r_emin : 0;
+  const bool fits128 = !any_term || (xemax + r_emax) - ebase <= 100;
+  int h;
+  if (fits128) {
+    // candidates (column, sign) one at a time, each summed exactly by the
+    // whole warp: lane l takes d = l, l + 32, ... (an integer sum, so the
+    // order does not matter), then a butterfly of the 128-bit partials
+    bool have = false;
+    __int128 bv = 0;
+    int bj = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = lane + 32 * k;
+      const float sc = c < m ? scv[k] : 0.f;
+      const bool cp = c < m && ((t0 - sc <= thr) || (sc != sc));
+      const bool cn = c < m && ((t0 + sc <= thr) || (sc != sc));
+      unsigned todo_c = __ballot_sync(0xffffffffu, cp || cn);
+      const unsigned pos_mask = __ballot_sync(0xffffffffu, cp), neg_mask = __ballot_sync(0xffffffffu, cn);
+      while (todo_c) {
+        const int bit = __ffs(todo_c) - 1;
+        todo_c &= todo_c - 1;
+        const int cc = bit + 32 * k;
+        __int128 acc = 0;
+        if (any_term) {
+          for (int d = lane; d < D; d += 32) {
+            bool nx, nr2;
+            uint32_t Mx, Mr;
+            int Ex, Er;
+            bf16_parts(static_cast<uint16_t>(__float_as_uint(sx[d]) >> 16), &nx, &Mx, &Ex);
+            bf16_parts(static_cast<uint16_t>(__float_as_uint(sR[d * m4 + cc]) >> 16), &nr2, &Mr, &Er);
+            if (Mx == 0 || Mr == 0) continue;
+            const __int128 term = static_cast<__int128>(Mx * Mr) << (Ex + Er - ebase);
+            acc = (nx != nr2) ? acc - term : acc + term;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const unsigned long long lo = static_cast<unsigned long long>(acc);
+          const long long hi = static_cast<long long>(acc >> 64);
+          const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, o);
+          const long long ohi = __shfl_xor_sync(0xffffffffu, hi, o);
+          acc += (static_cast<__int128>(ohi) << 64) | static_cast<__int128>(olo);
+        }
+        // (+) column cc, then (-) column cc + m: larger value, then smaller index
+        if (((pos_mask >> bit) & 1u) && (!have || acc > bv || (acc == bv && cc < bj))) {
+          bv = acc;
+          bj = cc;
+          have = true;
+        }
+        if (((neg_mask >> bit) & 1u) && (!have || -acc > bv || (-acc == bv && cc + m < bj))) {
+          bv = -acc;
+          bj = cc + m;
+          have = true;
+        }
+      }
+    }
+    h = bj;
+  } else {
+    // exponent span beyond 128 bits: the single-thread path on lane 0
+    int hh = 0;
+    if (lane == 0) hh = hash_row(reinterpret_cast<const uint32_t*>(xr), xr, sR, R, D, m, rnmax, r_emin, r_emax);
+    h = __shfl_sync(0xffffffffu, hh, 0);
+  }
+  return h;
+}
+
 // Second pass after the tensor-core pass: rows it left at -1 (near ties,
 // non-finite or subnormal values, huge magnitudes) get the certified
-// computation, one warp per row. A CTA takes kFixSeg consecutive rows at a
-// time: its threads scan the ids, collect the flagged rows (a fraction of a
-// percent) in a shared list, and the warps then share that list evenly. Per
-// row the lanes share the row (staged as fp32 in shared memory), screen the
-// columns lane + 32 k in fp32 with the same bound as the single-thread path
-// (it holds for any summation order), and evaluate every candidate within
-// the threshold of the top exactly in 128-bit integers, one candidate at a
-// time split over the lanes; the largest value wins, the smallest index on
-// ties. A row whose exponent span needs more than 128 bits goes to the
-// single-thread path (576-bit accumulator) on lane 0.
+// computation, one warp per row (fix_row_warp). A CTA takes kFixSeg
+// consecutive rows at a time: its threads scan the ids, collect the flagged
+// rows (a fraction of a percent) in a shared list, and the warps then share
+// that list evenly.
 constexpr int kFixWarps = 8;
 constexpr int kFixSeg = 2048;  // rows per CTA step; the shared list holds up to this many
 
@@ -414,8 +538,6 @@ __global__ void __launch_bounds__(kFixWarps * 32, 2) lsh_fix_kernel(const uint16
   lsh_prologue(R, D, m, sR, &rnmax, &r_emin, &r_emax);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* sx = sxall + warp * D;
-  const float rel = static_cast<float>(D + 1) * 0x1p-23f;
-  const float absb = static_cast<float>(D) * 0x1p-148f;
   __shared__ int s_n;
   __shared__ int s_list[kFixSeg];  // offsets of the flagged rows in the segment
   const long long n_units = seg_units(sg, kFixSeg);
@@ -442,119 +564,7 @@ __global__ void __launch_bounds__(kFixWarps * 32, 2) lsh_fix_kernel(const uint16
     const int n_flag = s_n;
     for (int li = warp; li < n_flag; li += kFixWarps) {
       const long long r = seg + s_list[li];
-      const uint16_t* xr = x + r * D;
-      // stage the row; norm and exponent range of its nonzero entries
-      float l2sq = 0.f;
-      int xemin = INT_MAX, xemax = INT_MIN;
-      for (int d = lane; d < D; d += 32) {
-        const uint16_t bb = xr[d];
-        const float v = bf16_to_f32(bb);
-        sx[d] = v;
-        l2sq = fmaf(v, v, l2sq);
-        bool ng;
-        uint32_t M;
-        int E;
-        bf16_parts(bb, &ng, &M, &E);
-        if (M != 0) {
-          xemin = min(xemin, E);
-          xemax = max(xemax, E);
-        }
-      }
-      for (int o = 16; o; o >>= 1) {
-        l2sq += __shfl_xor_sync(0xffffffffu, l2sq, o);
-        xemin = min(xemin, __shfl_xor_sync(0xffffffffu, xemin, o));
-        xemax = max(xemax, __shfl_xor_sync(0xffffffffu, xemax, o));
-      }
-      __syncwarp();
-      const float l2 = sqrtf(l2sq * (1.f + static_cast<float>(D + 2) * 0x1p-22f) + static_cast<float>(D) * 0x1p-148f) *
-                       1.000001f;
-      const float emax = l2 * rnmax * rel * 1.000001f + absb;
-      const float thr = 2.f * emax * 1.0001f;
-      // fp32 values of this lane's columns c = lane + 32 k (m <= 256: k < 8),
-      // each summed over d in order; the warp's top value
-      float scv[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) scv[k] = 0.f;
-#pragma unroll 4
-      for (int d = 0; d < D; ++d) {
-        const float xv = sx[d];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int c = lane + 32 * k;
-          if (c < m) scv[k] = fmaf(xv, sR[d * m4 + c], scv[k]);
-        }
-      }
-      float best_v = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (lane + 32 * k < m) best_v = fmaxf(best_v, fmaxf(scv[k], -scv[k]));
-      float t0 = best_v;
-      for (int o = 16; o; o >>= 1) t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
-      // exact values of the candidates (within thr of the top, or NaN)
-      const bool any_term = xemin != INT_MAX && r_emin != INT_MAX;
-      const int ebase = any_term ? xemin + r_emin : 0;
-      const bool fits128 = !any_term || (xemax + r_emax) - ebase <= 100;
-      int h;
-      if (fits128) {
-        // candidates (column, sign) one at a time, each summed exactly by the
-        // whole warp: lane l takes d = l, l + 32, ... (an integer sum, so the
-        // order does not matter), then a butterfly of the 128-bit partials
-        bool have = false;
-        __int128 bv = 0;
-        int bj = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int c = lane + 32 * k;
-          const float sc = c < m ? scv[k] : 0.f;
-          const bool cp = c < m && ((t0 - sc <= thr) || (sc != sc));
-          const bool cn = c < m && ((t0 + sc <= thr) || (sc != sc));
-          unsigned todo_c = __ballot_sync(0xffffffffu, cp || cn);
-          const unsigned pos_mask = __ballot_sync(0xffffffffu, cp), neg_mask = __ballot_sync(0xffffffffu, cn);
-          while (todo_c) {
-            const int bit = __ffs(todo_c) - 1;
-            todo_c &= todo_c - 1;
-            const int cc = bit + 32 * k;
-            __int128 acc = 0;
-            if (any_term) {
-              for (int d = lane; d < D; d += 32) {
-                bool nx, nr2;
-                uint32_t Mx, Mr;
-                int Ex, Er;
-                bf16_parts(static_cast<uint16_t>(__float_as_uint(sx[d]) >> 16), &nx, &Mx, &Ex);
-                bf16_parts(static_cast<uint16_t>(__float_as_uint(sR[d * m4 + cc]) >> 16), &nr2, &Mr, &Er);
-                if (Mx == 0 || Mr == 0) continue;
-                const __int128 term = static_cast<__int128>(Mx * Mr) << (Ex + Er - ebase);
-                acc = (nx != nr2) ? acc - term : acc + term;
-              }
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-              const unsigned long long lo = static_cast<unsigned long long>(acc);
-              const long long hi = static_cast<long long>(acc >> 64);
-              const unsigned long long olo = __shfl_xor_sync(0xffffffffu, lo, o);
-              const long long ohi = __shfl_xor_sync(0xffffffffu, hi, o);
-              acc += (static_cast<__int128>(ohi) << 64) | static_cast<__int128>(olo);
-            }
-            // (+) column cc, then (-) column cc + m: larger value, then smaller index
-            if (((pos_mask >> bit) & 1u) && (!have || acc > bv || (acc == bv && cc < bj))) {
-              bv = acc;
-              bj = cc;
-              have = true;
-            }
-            if (((neg_mask >> bit) & 1u) && (!have || -acc > bv || (-acc == bv && cc + m < bj))) {
-              bv = -acc;
-              bj = cc + m;
-              have = true;
-            }
-          }
-        }
-        h = bj;
-      } else {
-        // exponent span beyond 128 bits: the single-thread path on lane 0
-        int hh = 0;
-        if (lane == 0) hh = hash_row(reinterpret_cast<const uint32_t*>(xr), xr, sR, R, D, m, rnmax, r_emin, r_emax);
-        h = __shfl_sync(0xffffffffu, hh, 0);
-      }
+      const int h = fix_row_warp(x + r * D, R, sR, sx, D, m, rnmax, r_emin, r_emax, lane);
       if (lane == 0) hash[r] = h;
       __syncwarp();
     }
